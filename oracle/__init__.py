@@ -1,0 +1,302 @@
+"""CPU oracle for the VeriCache draft-and-verify hot path.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are the only callers.  The product library never
+imports, links or executes anything here, and nothing here imports the product
+package.  The compiled part (``vc_oracle.c``) is plain C in fp64; this module
+only builds it, marshals numpy arrays into it, and holds the plain numpy pieces
+(gather, bf16 images).
+
+Every function states which passage of the pages it follows; the pages are
+"VeriCache: Turning Lossy KV Cache into Lossless LLM Inference" (neuraltrendhub
+paper page, "What the paper found" and abstract; pith.science summary).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liborc.so")
+_SRC = os.path.join(_HERE, "vc_oracle.c")
+_lock = threading.Lock()
+_lib = None
+
+RN, RD, RU = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into oracle/_build/liborc.so (gcc, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-frounding-math",
+               "-fno-fast-math", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_SO)
+            P = ctypes.c_void_p
+            i, l, d = ctypes.c_int, ctypes.c_long, ctypes.c_double
+            L.orc_f16_value.restype = d
+            L.orc_f16_value.argtypes = [ctypes.c_uint16]
+            L.orc_bf16_value.restype = ctypes.c_float
+            L.orc_bf16_value.argtypes = [ctypes.c_uint16]
+            L.orc_f32_to_f16.restype = ctypes.c_uint16
+            L.orc_f32_to_f16.argtypes = [ctypes.c_float, i]
+            L.orc_quantize_group.restype = None
+            L.orc_quantize_group.argtypes = [P, i, l, i, P, l, P, P]
+            L.orc_kivi_quantize.restype = l
+            L.orc_kivi_quantize.argtypes = [P, P, i, i, i, i, i, i, i, P, P, P, P, P, P]
+            L.orc_record_bytes.restype = l
+            L.orc_record_bytes.argtypes = [i, i, i]
+            L.orc_unpack_records.restype = i
+            L.orc_unpack_records.argtypes = [P, l, i, i, i, P, P, P, P, P, P]
+            L.orc_kivi_decode_attn.restype = None
+            L.orc_kivi_decode_attn.argtypes = [P, i, i, i, i, i, l, l, d,
+                                               P, P, P, P, P, P, P, P, P]
+            L.orc_dense_decode_attn.restype = None
+            L.orc_dense_decode_attn.argtypes = [P, P, P, P, i, i, i, i, l, d, P]
+            L.orc_verify_attn.restype = None
+            L.orc_verify_attn.argtypes = [P, P, P, P, i, i, i, i, i, l, d, P, i, P]
+            L.orc_accept.restype = i
+            L.orc_accept.argtypes = [P, P, i, i, l, P, P, P]
+            L.orc_drop_select.restype = l
+            L.orc_drop_select.argtypes = [P, i, i, l, l, l, P]
+            L.orc_num_threads.restype = i
+            _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def num_threads() -> int:
+    return int(lib().orc_num_threads())
+
+
+# --------------------------------------------------------------------------
+# number formats
+# --------------------------------------------------------------------------
+
+def f16_value(bits) -> np.ndarray:
+    """Exact value of binary16 bit patterns (IEEE 754 definition), fp64."""
+    b = np.asarray(bits, dtype=np.uint16)
+    f = lib().orc_f16_value
+    return np.array([f(int(x)) for x in b.ravel()], dtype=np.float64).reshape(b.shape)
+
+
+def f16_value_fast(bits) -> np.ndarray:
+    """Same values through numpy's binary16 decoding (exact: every binary16 is
+    a binary64); used for bulk decoding of large meta arrays."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def f32_to_f16(x: float, mode: int) -> int:
+    """binary32 -> binary16 bits under IEEE rounding direction `mode`."""
+    return int(lib().orc_f32_to_f16(ctypes.c_float(float(x)), int(mode)))
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """bfloat16 bit patterns -> their exact binary32 values."""
+    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# KIVI-style quantization (KIVI: source 4 on the podparley page, ref [42] on
+# pith.science; named as a compressor on the paper page, "What the paper found")
+# --------------------------------------------------------------------------
+
+def quantize_group(x, bits: int):
+    """Quantize one group; returns (codes uint8[n], s_bits, z_bits)."""
+    x = _f32(x)
+    n = x.size
+    codes = np.zeros(n, dtype=np.uint8)
+    s = np.zeros(1, dtype=np.uint16)
+    z = np.zeros(1, dtype=np.uint16)
+    lib().orc_quantize_group(_p(x), n, 1, bits, _p(codes), 1, _p(s), _p(z))
+    return codes, int(s[0]), int(z[0])
+
+
+def kivi_quantize(k, v, bits: int, group: int = 32, residual: int = 0):
+    """Quantize a cache k, v [B][H][L][d] (fp32 images of the inputs).
+
+    Returns a dict of logical arrays: nq, kcode [B,H,nq,d], kscale/kzero
+    [B,H,nq/G,d] (fp16 bits), vcode [B,H,nq,d], vscale/vzero [B,H,nq,d/G],
+    kres/vres [B,H,L-nq,d] (fp32)."""
+    k = _f32(k)
+    v = _f32(v)
+    B, H, L, d = k.shape
+    nq = ((L - residual) // group) * group if L - residual > 0 else 0
+    ng = nq // group
+    kcode = np.zeros((B, H, nq, d), np.uint8)
+    vcode = np.zeros((B, H, nq, d), np.uint8)
+    ks = np.zeros((B, H, ng, d), np.uint16)
+    kz = np.zeros((B, H, ng, d), np.uint16)
+    vs = np.zeros((B, H, nq, d // group), np.uint16)
+    vz = np.zeros((B, H, nq, d // group), np.uint16)
+    got = lib().orc_kivi_quantize(_p(k), _p(v), B, H, L, d, bits, group, residual,
+                                  _p(kcode), _p(ks), _p(kz), _p(vcode), _p(vs), _p(vz))
+    assert got == nq
+    return dict(nq=nq, bits=bits, group=group, kcode=kcode, kscale=ks, kzero=kz,
+                vcode=vcode, vscale=vs, vzero=vz,
+                kres=np.ascontiguousarray(k[:, :, nq:, :]),
+                vres=np.ascontiguousarray(v[:, :, nq:, :]))
+
+
+def kivi_dequant(qc) -> tuple[np.ndarray, np.ndarray]:
+    """x^ = code * s + z in fp64 for the quantized prefix (definition)."""
+    G = qc["group"]
+    ks = np.repeat(f16_value_fast(qc["kscale"]), G, axis=2)
+    kz = np.repeat(f16_value_fast(qc["kzero"]), G, axis=2)
+    vs = np.repeat(f16_value_fast(qc["vscale"]), G, axis=3)
+    vz = np.repeat(f16_value_fast(qc["vzero"]), G, axis=3)
+    kh = qc["kcode"].astype(np.float64) * ks + kz
+    vh = qc["vcode"].astype(np.float64) * vs + vz
+    return kh, vh
+
+
+def record_bytes(bits: int, d: int, group: int = 32) -> int:
+    return int(lib().orc_record_bytes(bits, d, group))
+
+
+def unpack_records(rec: np.ndarray, bits: int, d: int, group: int = 32):
+    """Read the library's packed group records (see vc_oracle.c for the
+    format statement).  rec: uint8 [..., n_rec * record_bytes]; returns
+    logical arrays shaped like kivi_quantize's, flattened over records."""
+    rec = np.ascontiguousarray(rec, dtype=np.uint8).ravel()
+    rb = record_bytes(bits, d, group)
+    assert rec.size % rb == 0
+    n = rec.size // rb
+    kcode = np.zeros((n * group, d), np.uint8)
+    vcode = np.zeros((n * group, d), np.uint8)
+    ks = np.zeros((n, d), np.uint16)
+    kz = np.zeros((n, d), np.uint16)
+    vs = np.zeros((n * group, d // 32), np.uint16)
+    vz = np.zeros((n * group, d // 32), np.uint16)
+    rc = lib().orc_unpack_records(_p(rec), n, bits, d, group, _p(kcode), _p(ks), _p(kz),
+                                  _p(vcode), _p(vs), _p(vz))
+    assert rc == 0
+    return dict(kcode=kcode, kscale=ks, kzero=kz, vcode=vcode, vscale=vs, vzero=vz)
+
+
+# --------------------------------------------------------------------------
+# attention (paper page: drafting attends over the compressed cache, the
+# verify pass over the full cache; definition o = softmax(q k^T s) v)
+# --------------------------------------------------------------------------
+
+def kivi_decode_attn(q, qc, scale: float) -> np.ndarray:
+    """Decode attention of q [B,Hq,d] over a KIVI cache from kivi_quantize
+    (all sequences the same length nq + residual)."""
+    q = _f32(q)
+    B, Hq, d = q.shape
+    Hkv = qc["kcode"].shape[1]
+    nq = qc["nq"]
+    nres = qc["kres"].shape[2]
+    out = np.zeros((B, Hq, d), np.float64)
+    kres = _f32(qc["kres"])
+    vres = _f32(qc["vres"])
+    lib().orc_kivi_decode_attn(_p(q), B, Hq, Hkv, d, qc["group"], nq, nq + nres, scale,
+                               _p(qc["kcode"]), _p(qc["kscale"]), _p(qc["kzero"]),
+                               _p(qc["vcode"]), _p(qc["vscale"]), _p(qc["vzero"]),
+                               _p(kres), _p(vres), _p(out))
+    return out
+
+
+def dense_decode_attn(q, k, v, lens, scale: float) -> np.ndarray:
+    """Decode attention of q [B,Hq,d] over k, v [B,Hkv,Ls,d]; sequence b sees
+    its first lens[b] tokens."""
+    q = _f32(q)
+    k = _f32(k)
+    v = _f32(v)
+    B, Hq, d = q.shape
+    Hkv, Ls = k.shape[1], k.shape[2]
+    lens = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+    out = np.zeros((B, Hq, d), np.float64)
+    lib().orc_dense_decode_attn(_p(q), _p(k), _p(v), _p(lens), B, Hq, Hkv, d, Ls, scale, _p(out))
+    return out
+
+
+def verify_attn(q, k, v, ctx, scale: float, units=None) -> np.ndarray:
+    """Causal block attention: q [B,Dq,Hq,d]; query i of sequence b sits at
+    position ctx[b]+i and sees keys 0..ctx[b]+i of k, v [B,Hkv,Ls,d].
+    `units` optionally restricts the work to a list of b*Hkv+kh (others 0)."""
+    q = _f32(q)
+    k = _f32(k)
+    v = _f32(v)
+    B, Dq, Hq, d = q.shape
+    Hkv, Ls = k.shape[1], k.shape[2]
+    ctx = np.ascontiguousarray(np.asarray(ctx, dtype=np.int32))
+    assert np.all(ctx + Dq <= Ls)
+    out = np.zeros((B, Dq, Hq, d), np.float64)
+    if units is None:
+        up, nu = None, 0
+    else:
+        ua = np.ascontiguousarray(np.asarray(units, dtype=np.int32))
+        up, nu = _p(ua), ua.size
+    lib().orc_verify_attn(_p(q), _p(k), _p(v), _p(ctx), B, Dq, Hq, Hkv, d, Ls, scale,
+                          up, nu, _p(out))
+    return out
+
+
+# --------------------------------------------------------------------------
+# greedy acceptance (speculative decoding's greedy rule, source 2 on the
+# podparley page; "identical to full-KV inference" on the paper page)
+# --------------------------------------------------------------------------
+
+def accept(logits, drafts):
+    """logits [B,D+1,V] (fp32 images), drafts [B,D] -> (n_acc[B], next[B],
+    row_argmax[B,D+1]).  argmax takes the lowest index on ties."""
+    lg = _f32(logits)
+    B, D1, V = lg.shape
+    D = D1 - 1
+    dr = np.ascontiguousarray(np.asarray(drafts, dtype=np.int32).reshape(B, D) if D else
+                              np.zeros((B, 0), np.int32))
+    n_acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    am = np.zeros((B, D1), np.int32)
+    rc = lib().orc_accept(_p(lg), _p(dr), B, D, V, _p(n_acc), _p(nxt), _p(am))
+    if rc != 0:
+        raise ValueError("non-finite logit")
+    return n_acc, nxt, am
+
+
+# --------------------------------------------------------------------------
+# token dropping (H2O: source 3 on the podparley page; KVzip 4x on the paper
+# page, "What the paper found")
+# --------------------------------------------------------------------------
+
+def drop_select(scores, keep_top: int, keep_recent: int) -> np.ndarray:
+    """Kept positions [B,H,n_keep], ascending (see vc_oracle.c)."""
+    s = _f32(scores)
+    B, H, L = s.shape
+    R = min(keep_recent, L)
+    k = min(keep_top, L - R)
+    kept = np.zeros((B, H, k + R), np.int32)
+    n = lib().orc_drop_select(_p(s), B, H, L, keep_top, keep_recent, _p(kept))
+    assert n == k + R
+    return kept
+
+
+def drop_gather(x, kept) -> np.ndarray:
+    """Compacted cache: x [B,H,L,d] rows at the kept positions, in order."""
+    return np.take_along_axis(np.asarray(x), np.asarray(kept)[..., None].astype(np.int64), axis=2)
