@@ -1,0 +1,312 @@
+/*
+ * vc.h -- C ABI of the GB300 (sm_103a) draft-and-verify hot path.
+ *
+ * The method ("VeriCache: Turning Lossy KV Cache into Lossless LLM Inference",
+ * paper page, "What the paper found" and abstract): run the target model on a
+ * compressed KV cache to draft tokens, overlap that HBM-bound drafting with the
+ * interconnect-bound swap-in of the full KV cache, verify the drafted block
+ * against the full cache, and keep the longest prefix on which the verify
+ * argmax equals the drafts, so that greedy output equals full-KV decoding.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are caller-owned.  "device" pointers are CUDA device
+ *    memory of the current device; "pinned host" pointers are page-locked host
+ *    memory.  The library never allocates, frees or retains memory.
+ *  - Layouts are dense, row-major, in the element type named by a vc_dtype
+ *    argument (VC_BF16: bfloat16, VC_F32: binary32).
+ *  - Every call validates its host-side arguments first and returns
+ *    VC_ERR_INVALID (bad size, null pointer, misalignment) or
+ *    VC_ERR_UNSUPPORTED (valid but not implemented) without touching the
+ *    stream.  On success the work is enqueued on `stream` and VC_OK is
+ *    returned; the call does not synchronize.  Errors raised later on the
+ *    device surface at the caller's next synchronization, or through
+ *    vc_check().
+ *  - Calls keep no state between invocations and may be issued from several
+ *    host threads on different streams.  Calls that share a workspace or a
+ *    cache must be ordered by the caller.
+ *  - Workspaces: entry points that combine partial results take a device
+ *    workspace `ws` of at least the size returned by the matching
+ *    *_workspace_bytes() query, 256-byte aligned.  The first 256 bytes of every
+ *    workspace are a status block; kernels whose waits are bounded record a
+ *    timeout there (read and cleared by vc_poll_status()).  A new workspace
+ *    must be zero-filled once before first use (vc_workspace_init()).
+ */
+#ifndef VC_H
+#define VC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vc_status {
+    VC_OK = 0,
+    VC_ERR_INVALID = 1,      /* bad argument: null pointer, size, alignment */
+    VC_ERR_UNSUPPORTED = 2,  /* valid request outside what is implemented */
+    VC_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+    VC_ERR_TIMEOUT = 4       /* a bounded device-side wait gave up */
+} vc_status;
+
+typedef enum vc_dtype {
+    VC_BF16 = 0,
+    VC_F32 = 1
+} vc_dtype;
+
+/* Human-readable text for a status code (static storage). */
+const char *vc_status_str(vc_status s);
+
+/* Library version string and the device architecture it was built for. */
+const char *vc_version(void);
+
+/* Synchronize `stream` and report any asynchronous CUDA error as VC_ERR_CUDA. */
+vc_status vc_check(cudaStream_t stream);
+
+/* Zero-fill a new workspace (ws_bytes bytes) on `stream`. */
+vc_status vc_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronize `stream`, read the status block of `ws`, clear it.  Returns
+ * VC_ERR_TIMEOUT if a kernel that used this workspace gave up on a wait
+ * (its outputs are then undefined), VC_OK otherwise. */
+vc_status vc_poll_status(void *ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (1) KIVI-style quantized draft cache                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * KIVI (named among the compressors on the paper page, "What the paper
+ * found"; ref [42] on pith.science): K is quantized per channel over groups of
+ * `group` consecutive tokens, V per token over groups of `group` consecutive
+ * channels; every group stores an fp16 scale s and zero-point z and b-bit
+ * codes, x^ = code * s + z.  The most recent tokens stay full precision.
+ *
+ * Rounding rule (the pages give only the name; this is the library's reading):
+ *   z = fp16 round-down(min), s = fp16 round-up((max - z) / (2^b - 1)) with
+ *   the fp32 subtraction and division rounded upward, code =
+ *   clamp(round-half-even((x - z) / s), 0, 2^b - 1) in fp32 round-to-nearest
+ *   (code = 0 when s = 0).  Hence z <= min, z + (2^b-1) s >= max and
+ *   |x - x^| <= s/2 (up to the rounding of the fp32 quotient).
+ *
+ * Storage.  Quantized token groups live in fixed-size records, one per
+ * (sequence, kv head, group), at
+ *   records + ((b * Hkv + h) * max_groups + g) * vc_record_bytes(bits, d).
+ * A record is [K codes | V codes | K meta | V meta]:
+ *   K codes, V codes: group*d*bits/8 bytes each, in the m16n8k16 operand
+ *     fragment order of the draft kernel (lane l in [0,32) owns a contiguous
+ *     E*bits/8-byte slice, E = group*d/32 codes; code pair p of a lane sits in
+ *     32-bit little-endian word p / (16/bits), first code at bit bits*(p %
+ *     (16/bits)), second at bit 16 + the same.  Element e = 2p + hh of lane l
+ *     is, for K: token 16 mt + l/4 + 8 (r&1), channel 16 ks + 2 (l%4) + hh +
+ *     8 (r>>1) with e = ((mt*(d/16) + ks)*4 + r)*2 + hh; for V: channel
+ *     16 mt + l/4 + 8 (r&1), token 16 ks + 2 (l%4) + hh + 8 (r>>1) with
+ *     e = ((mt*2 + ks)*4 + r)*2 + hh).
+ *   K meta (4d bytes): for j in 0..3, a d-byte block holding fp16 pairs
+ *     (s[c0], s[c0+1]) at byte j*d + 4*(2 ks + rr), c0 = 16 ks + 2 j + 8 rr,
+ *     then the zero pairs at byte j*d + d/2 + 4*(2 ks + rr).
+ *   V meta (4d bytes): for j in 0..3, a d-byte block holding fp16 pairs
+ *     (s[t0][gc], s[t0+1][gc]) at byte j*d + 4*((2 ks + rr)*(d/32) + gc),
+ *     t0 = 16 ks + 2 j + 8 rr, then the zero pairs at byte j*d + d/2 + same.
+ * Full-precision tokens (positions n_groups[b]*group .. seq_len[b]-1) live in
+ * a ring: position p of (b, h) at k_res/v_res + ((b * Hkv + h) * res_cap +
+ * p % res_cap) * d elements.
+ * Supported: bits in {2, 4}, group == 32, d in {64, 128}.
+ */
+typedef struct vc_quant_cfg {
+    int32_t bits;        /* 2 or 4 */
+    int32_t group;       /* 32 */
+    int32_t residual;    /* R: tokens kept full precision (the newest R..R+group-1) */
+} vc_quant_cfg;
+
+typedef struct vc_qcache {
+    void *records;        /* device, [B][Hkv][max_groups] records, 256-B aligned */
+    void *k_res;          /* device, [B][Hkv][res_cap][d] in res_dtype */
+    void *v_res;          /* device, same */
+    int32_t *n_groups;    /* device [B]: quantized groups of sequence b */
+    int32_t *seq_len;     /* device [B]: cached tokens of sequence b */
+    int32_t *status;      /* device, 1 word: nonzero after a ring overflow */
+    int32_t B, Hkv, d;
+    vc_quant_cfg cfg;
+    int32_t max_groups;   /* record capacity per (b, h) */
+    int32_t res_cap;      /* ring capacity per (b, h), >= cfg.residual + group */
+    vc_dtype res_dtype;
+} vc_qcache;
+
+/* Bytes of one group record: 2*group*d*bits/8 + 8*d (group = 32). */
+size_t vc_record_bytes(int bits, int d);
+
+/*
+ * vc_quantize_kv -- compress a prefill K/V cache into `cache`.
+ * k, v: device [B][Hkv][L_stride][d] in dt (dt must equal cache->res_dtype);
+ * tokens 0..L-1 are used.  With n_q = floor(max(L - R, 0) / group) groups,
+ * writes records 0..n_q-1 of every (b, h), copies positions n_q*group..L-1
+ * into the ring, and sets n_groups[b] = n_q, seq_len[b] = L.
+ * Requires n_q <= max_groups and L - n_q*group <= res_cap.
+ */
+vc_status vc_quantize_kv(const void *k, const void *v, vc_dtype dt, int B, int Hkv,
+                         int L, int L_stride, int d, vc_qcache *cache,
+                         cudaStream_t stream);
+
+/*
+ * vc_qcache_append -- append new tokens to the cache (draft steps and the
+ * commit after verification).
+ * k_new, v_new: device [B][Hkv][max_new][d] in cache->res_dtype; sequence b
+ * appends its first n_new[b] rows (device int32 [B], 0 <= n_new[b] <= max_new)
+ * at positions seq_len[b].., then seq_len[b] += n_new[b].  With requantize != 0
+ * every complete group that has left the residual window ((g+1)*group <=
+ * seq_len[b] - R) is quantized into record g and n_groups[b] advances.  A
+ * ring overflow (tokens that would overwrite unquantized ones) sets
+ * *cache->status and drops the excess tokens.
+ * Rolling back drafted tokens is a plain rewrite of seq_len by the caller.
+ */
+vc_status vc_qcache_append(vc_qcache *cache, const void *k_new, const void *v_new,
+                           const int32_t *n_new, int max_new, int requantize,
+                           cudaStream_t stream);
+
+/*
+ * vc_qcache_commit -- the end of a draft-and-verify round for the draft cache
+ * (paper page: the drafted tokens are verified against the full cache; the
+ * compressed cache then carries on from the verified output).  For every
+ * sequence b: roll back to round_len[b] (the length before drafting), append
+ * the first n_acc[b] + 1 rows of the verify block k_blk, v_blk (device
+ * [B][Hkv][Dq][d] in cache->res_dtype: the verify pass's K/V of the pending
+ * token and the accepted drafts), and re-quantize every group that left the
+ * residual window.  round_len, n_acc: device int32 [B] (n_acc as written by
+ * vc_accept, 0 <= n_acc[b] < Dq).
+ */
+vc_status vc_qcache_commit(vc_qcache *cache, const void *k_blk, const void *v_blk,
+                           const int32_t *round_len, const int32_t *n_acc, int Dq,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (2) token-dropping compressor                                             */
+/* ------------------------------------------------------------------------ */
+/*
+ * Token dropping by accumulated attention score (H2O, source 3 on the
+ * podparley page; KVzip 4x on the paper page, "What the paper found"): per
+ * (b, h) keep the `keep_recent` newest tokens and the `keep_top` best of the
+ * older ones, ranked by score descending, ties by position ascending, and
+ * compact them in ascending position order.
+ */
+typedef struct vc_drop_cfg {
+    int64_t keep_top;
+    int64_t keep_recent;
+} vc_drop_cfg;
+
+/* Kept tokens per (b, h): min(keep_top, max(L - R, 0)) + min(R, L). */
+int64_t vc_drop_kept_count(int64_t L, vc_drop_cfg cfg);
+
+size_t vc_drop_tokens_workspace_bytes(int B, int H, int L);
+
+/*
+ * scores: device fp32 [B][H][L] (finite); k, v: device [B][H][L][d] in dt.
+ * kept_idx: device int32 [B][H][n_keep] (ascending positions);
+ * k_out, v_out: device [B][H][n_keep][d] in dt, the gathered rows.
+ * Selection and compaction are exact: kept_idx is unique for given scores.
+ */
+vc_status vc_drop_tokens(const float *scores, const void *k, const void *v, vc_dtype dt,
+                         int B, int H, int L, int d, vc_drop_cfg cfg,
+                         int32_t *kept_idx, void *k_out, void *v_out,
+                         void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (3) draft decode attention over the compressed cache                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * Drafting runs the target model on the compressed cache (paper page, "What
+ * the paper found"); this is its attention: one query per sequence and query
+ * head, o = softmax(q K^T * sm_scale) V over every cached token, with query
+ * head hq reading kv head hq / (Hq / Hkv).
+ */
+typedef enum vc_cache_kind {
+    VC_CACHE_KIVI = 0,    /* quantized records + full-precision ring */
+    VC_CACHE_DENSE = 1    /* plain K/V rows (a compacted dropped cache, or full) */
+} vc_cache_kind;
+
+typedef struct vc_cache_view {
+    vc_cache_kind kind;
+    const vc_qcache *kivi;       /* VC_CACHE_KIVI */
+    const void *k, *v;           /* VC_CACHE_DENSE: device [B][Hkv][L_stride][d] */
+    vc_dtype dt;                 /* VC_CACHE_DENSE element type */
+    const int32_t *seq_len;      /* VC_CACHE_DENSE: device [B], tokens of sequence b */
+    int32_t B, Hkv, d;           /* VC_CACHE_DENSE shape */
+    int32_t L_stride;            /* VC_CACHE_DENSE row stride per (b, h) */
+    int32_t max_len;             /* VC_CACHE_DENSE: upper bound of seq_len (grid sizing) */
+} vc_cache_view;
+
+size_t vc_draft_attn_workspace_bytes(const vc_cache_view *view, int Hq);
+
+/*
+ * q: device [B][Hq][d] in q_dt; out: device [B][Hq][d] in q_dt.
+ * Hq must be a multiple of Hkv with Hq / Hkv <= 8 (<= 4 for VC_CACHE_KIVI).
+ * Sequences with no cached token produce zeros.
+ */
+vc_status vc_draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq,
+                        float sm_scale, void *out, void *ws, size_t ws_bytes,
+                        cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (4) verify attention over the full cache                                  */
+/* ------------------------------------------------------------------------ */
+/*
+ * Verification re-runs the drafted block against the full KV cache (paper
+ * page, "What the paper found"): a causal block of Dq queries.  Query i of
+ * sequence b sits at position ctx_len[b] + i and attends keys
+ * 0 .. ctx_len[b] + i; the block's own K/V must already be written at
+ * positions ctx_len[b] .. ctx_len[b] + Dq - 1 of k, v.
+ * q: device [B][Dq][Hq][d]; k, v: device [B][Hkv][L_stride][d];
+ * out: device [B][Dq][Hq][d]; all in dt.  ctx_len: device int32 [B] with
+ * ctx_len[b] + Dq <= L_stride and ctx_len[b] <= max_ctx.
+ * bf16 with d = 128 and Hq / Hkv in {1, 2, 4, 8} runs on the tensor cores
+ * (TMA + tcgen05, fp32 accumulation); other supported shapes (fp32, d = 64)
+ * run an fp32 CUDA-core kernel.
+ */
+size_t vc_verify_attn_workspace_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d,
+                                      int max_ctx);
+
+vc_status vc_verify_attn(const void *q, const void *k, const void *v, vc_dtype dt,
+                         const int32_t *ctx_len, int B, int Dq, int Hq, int Hkv, int d,
+                         int L_stride, int max_ctx, float sm_scale, void *out,
+                         void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (5) greedy acceptance                                                     */
+/* ------------------------------------------------------------------------ */
+/*
+ * The greedy rule of speculative decoding (source 2 on the podparley page),
+ * which makes the output identical to full-KV greedy decoding (paper page,
+ * "What the paper found"): with a_i = argmax of verify logits row i (lowest
+ * index on ties, -0 == +0), n = first i in [0, D) with a_i != drafts[i], else
+ * D; next = a_n.  The round emits drafts[0..n-1] and next.
+ * logits: device [B][D+1][V] in dt (finite values); drafts: device int32
+ * [B][D]; n_acc, next_tok: device int32 [B].
+ */
+size_t vc_accept_workspace_bytes(int B, int D, int V);
+
+vc_status vc_accept(const void *logits, vc_dtype dt, const int32_t *drafts, int B, int D,
+                    int V, int32_t *n_acc, int32_t *next_tok, void *ws, size_t ws_bytes,
+                    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (6) full-KV swap-in                                                       */
+/* ------------------------------------------------------------------------ */
+/*
+ * The full KV cache stays out of GPU memory and is swapped in for
+ * verification, overlapped with drafting (abstract: "keeping the full KV cache
+ * out of GPU memory and minimizing the overhead of swapping it in"; paper page:
+ * cross-resource staggering).  Copies `bytes` from pinned host memory to the
+ * device with one asynchronous copy on `side_stream` and, if `done` is not
+ * NULL, records `done` on that stream after it; the caller makes the verify
+ * stream wait on `done`.  Returns VC_ERR_INVALID if src is not page-locked
+ * host memory (a pageable source would serialize the copy).
+ */
+vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes,
+                     cudaStream_t side_stream, cudaEvent_t done);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VC_H */

@@ -1,0 +1,215 @@
+// accept.cu -- greedy acceptance of a drafted block (the greedy rule of
+// speculative decoding, source 2 on the podparley page; output identical to
+// full-KV greedy decoding, VeriCache paper page "What the paper found").
+//
+// One pass over the verify logits [B][D+1][V]: every (row, split) CTA scans a
+// contiguous slice with 128-bit streaming loads and reduces (value, index)
+// pairs -- larger value wins, equal values keep the lower index, so -0 and +0
+// tie -- through warp shuffles and shared memory.  The last CTA to finish a
+// sequence (device-scope counter) folds the split partials of its D+1 rows,
+// finds the first row whose argmax differs from the draft, and writes
+// n_acc and next_tok.  HBM-bound: the algorithmic traffic is the logits once.
+#include "vc_common.cuh"
+#include "vc_internal.h"
+
+namespace vc {
+namespace {
+
+constexpr int kThreads = 256;
+
+struct ArgMax {
+    float v;
+    int i;
+};
+
+__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b)
+{
+    // larger value wins; on equal values the lower index wins
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+    return a;
+}
+
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax a)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ArgMax b;
+        b.v = __shfl_xor_sync(0xffffffffu, a.v, o);
+        b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
+        a = better(a, b);
+    }
+    return a;
+}
+
+struct WsLayout {
+    int32_t *status;
+    unsigned int *counters;   // [B]
+    ArgMax *part;             // [rows][S]
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline int splits_for(int V) { return V >= 65536 ? 4 : (V >= 16384 ? 2 : 1); }
+
+__host__ __device__ inline WsLayout ws_layout(void *ws, int B)
+{
+    uint8_t *p = (uint8_t *)ws;
+    WsLayout L;
+    L.status = (int32_t *)p;
+    L.counters = (unsigned int *)(p + kStatusBytes);
+    L.part = (ArgMax *)(p + kStatusBytes + align256((size_t)B * 4));
+    return L;
+}
+
+template <typename T>
+__device__ __forceinline__ void scan_vec(const T *row, int lo, int hi, ArgMax &best)
+{
+    constexpr int PER = 16 / sizeof(T);
+    // lo, hi are multiples of PER; row is 16-byte aligned
+    int i = lo + threadIdx.x * PER;
+    constexpr int UNROLL = 4;
+    for (; i + (UNROLL - 1) * kThreads * PER < hi; i += UNROLL * kThreads * PER) {
+        uint4 u[UNROLL];
+#pragma unroll
+        for (int r = 0; r < UNROLL; ++r) u[r] = ldg_stream(row + i + r * kThreads * PER);
+#pragma unroll
+        for (int r = 0; r < UNROLL; ++r) {
+            const uint32_t w[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
+            const int base = i + r * kThreads * PER;
+            if constexpr (sizeof(T) == 2) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+                    if (a > best.v) { best.v = a; best.i = base + 2 * e; }
+                    if (b > best.v) { best.v = b; best.i = base + 2 * e + 1; }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float a = __uint_as_float(w[e]);
+                    if (a > best.v) { best.v = a; best.i = base + e; }
+                }
+            }
+        }
+    }
+    for (; i < hi; i += kThreads * PER) {
+        uint4 u = ldg_stream(row + i);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        if constexpr (sizeof(T) == 2) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+                if (a > best.v) { best.v = a; best.i = i + 2 * e; }
+                if (b > best.v) { best.v = b; best.i = i + 2 * e + 1; }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float a = __uint_as_float(w[e]);
+                if (a > best.v) { best.v = a; best.i = i + e; }
+            }
+        }
+    }
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads)
+accept_kernel(const T *__restrict__ logits, const int32_t *__restrict__ drafts, int B, int D,
+              int V, int S, int chunk, int32_t *__restrict__ n_acc, int32_t *__restrict__ next_tok,
+              void *ws)
+{
+    const WsLayout W = ws_layout(ws, B);
+    const int s = blockIdx.x, row = blockIdx.y;
+    const int b = row / (D + 1);
+    const T *rp = logits + (size_t)row * V;
+    const int lo = s * chunk, hi = min(V, lo + chunk);
+    // Threads scan increasing indices, so a strict '>' keeps the first
+    // occurrence of a tie inside each thread's subsequence.
+    ArgMax best{-INFINITY, 0x7fffffff};
+    if (VEC) {
+        scan_vec<T>(rp, lo, hi, best);
+    } else {
+        for (int i = lo + threadIdx.x; i < hi; i += kThreads) {
+            float a = Elem<T>::to_f(rp[i]);
+            if (a > best.v) { best.v = a; best.i = i; }
+        }
+    }
+    __shared__ ArgMax red[kThreads / 32];
+    __shared__ bool is_last;
+    best = warp_argmax(best);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ArgMax a = red[0];
+        for (int w = 1; w < kThreads / 32; ++w) a = better(a, red[w]);
+        W.part[(size_t)row * S + s] = a;
+        __threadfence();
+        const unsigned int done = atomicAdd(&W.counters[b], 1u);
+        is_last = (done == (unsigned int)((D + 1) * S - 1));
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // Last CTA of sequence b: fold the partials of its D+1 rows.
+    __shared__ int amax[1024 + 1];
+    for (int i = threadIdx.x; i <= D; i += kThreads) {
+        const ArgMax *pp = W.part + (size_t)(b * (D + 1) + i) * S;
+        ArgMax a;
+        a.v = __ldcg(&pp[0].v);
+        a.i = __ldcg(&pp[0].i);
+        for (int t = 1; t < S; ++t) {
+            ArgMax c;
+            c.v = __ldcg(&pp[t].v);
+            c.i = __ldcg(&pp[t].i);
+            a = better(a, c);
+        }
+        amax[i] = a.i;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int n = D;
+        for (int i = 0; i < D; ++i)
+            if (amax[i] != drafts[(size_t)b * D + i]) { n = i; break; }
+        n_acc[b] = n;
+        next_tok[b] = amax[n];
+    }
+}
+
+template <typename T>
+cudaError_t launch(const void *logits, const int32_t *drafts, int B, int D, int V, int32_t *n_acc,
+                   int32_t *next_tok, void *ws, cudaStream_t st)
+{
+    constexpr int PER = 16 / sizeof(T);
+    const WsLayout W = ws_layout(ws, B);
+    cudaError_t e = cudaMemsetAsync(W.counters, 0, (size_t)B * 4, st);
+    if (e != cudaSuccess) return e;
+    const int S = splits_for(V);
+    const bool vec = ((uintptr_t)logits % 16 == 0) && (V % PER == 0);
+    int chunk = cdiv(V, S);
+    if (vec) chunk = cdiv(chunk, PER) * PER;
+    dim3 grid(S, B * (D + 1));
+    if (vec)
+        accept_kernel<T, true><<<grid, kThreads, 0, st>>>((const T *)logits, drafts, B, D, V, S,
+                                                          chunk, n_acc, next_tok, ws);
+    else
+        accept_kernel<T, false><<<grid, kThreads, 0, st>>>((const T *)logits, drafts, B, D, V, S,
+                                                           chunk, n_acc, next_tok, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t accept_ws_bytes(int B, int D, int V)
+{
+    return kStatusBytes + align256((size_t)B * 4) +
+           align256((size_t)B * (D + 1) * splits_for(V) * sizeof(ArgMax));
+}
+
+cudaError_t accept(const void *logits, vc_dtype dt, const int32_t *drafts, int B, int D, int V,
+                   int32_t *n_acc, int32_t *next_tok, void *ws, cudaStream_t st)
+{
+    return dt == VC_BF16 ? launch<__nv_bfloat16>(logits, drafts, B, D, V, n_acc, next_tok, ws, st)
+                         : launch<float>(logits, drafts, B, D, V, n_acc, next_tok, ws, st);
+}
+
+}  // namespace vc

@@ -1,0 +1,234 @@
+// vc_api.cu -- the C-ABI entry points declared in include/vc.h: host-side
+// argument validation, then dispatch to the kernel launchers.
+#include <cstring>
+
+#include "vc_common.cuh"
+#include "vc_internal.h"
+
+using namespace vc;
+
+namespace {
+
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+inline size_t esize(vc_dtype dt) { return dt == VC_BF16 ? 2 : 4; }
+inline bool dtype_ok(vc_dtype dt) { return dt == VC_BF16 || dt == VC_F32; }
+inline vc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VC_OK : VC_ERR_CUDA; }
+
+bool qcache_ok(const vc_qcache *c)
+{
+    if (!c || !c->records || !c->k_res || !c->v_res || !c->n_groups || !c->seq_len) return false;
+    if (c->B <= 0 || c->Hkv <= 0 || (c->d != 64 && c->d != 128)) return false;
+    if ((c->cfg.bits != 2 && c->cfg.bits != 4) || c->cfg.group != 32 || c->cfg.residual < 0) return false;
+    if (c->max_groups < 0 || c->res_cap < c->cfg.residual + c->cfg.group) return false;
+    if (!dtype_ok(c->res_dtype)) return false;
+    if (!aligned(c->records, 256) || !aligned(c->k_res, 16) || !aligned(c->v_res, 16)) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *vc_status_str(vc_status s)
+{
+    switch (s) {
+    case VC_OK: return "ok";
+    case VC_ERR_INVALID: return "invalid argument";
+    case VC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VC_ERR_CUDA: return "CUDA runtime error";
+    case VC_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *vc_version(void) { return "vericache-gb300 0.1 (sm_103a)"; }
+
+vc_status vc_check(cudaStream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_status(e);
+}
+
+vc_status vc_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!ws || ws_bytes < (size_t)kStatusBytes || !aligned(ws, 256)) return VC_ERR_INVALID;
+    return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, stream));
+}
+
+vc_status vc_poll_status(void *ws, cudaStream_t stream)
+{
+    if (!ws) return VC_ERR_INVALID;
+    int32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return VC_ERR_CUDA;
+    if (word != 0) {
+        e = cudaMemsetAsync(ws, 0, sizeof(word), stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return VC_ERR_CUDA;
+        return VC_ERR_TIMEOUT;
+    }
+    return VC_OK;
+}
+
+size_t vc_record_bytes(int bits, int d)
+{
+    if ((bits != 2 && bits != 4) || d <= 0 || d % 32) return 0;
+    return (size_t)2 * 32 * d * bits / 8 + (size_t)8 * d;
+}
+
+vc_status vc_quantize_kv(const void *k, const void *v, vc_dtype dt, int B, int Hkv, int L, int L_stride,
+                         int d, vc_qcache *cache, cudaStream_t stream)
+{
+    if (!k || !v || !qcache_ok(cache)) return VC_ERR_INVALID;
+    if (!dtype_ok(dt) || dt != cache->res_dtype) return VC_ERR_INVALID;
+    if (B != cache->B || Hkv != cache->Hkv || d != cache->d) return VC_ERR_INVALID;
+    if (L < 0 || L_stride < L || !aligned(k, 16) || !aligned(v, 16)) return VC_ERR_INVALID;
+    const int G = cache->cfg.group, R = cache->cfg.residual;
+    const int nq = (L - R > 0) ? ((L - R) / G) * G : 0;
+    if (nq / G > cache->max_groups || L - nq > cache->res_cap) return VC_ERR_INVALID;
+    return cuda_status(quantize_prefill(k, v, dt, B, Hkv, L, L_stride, d, cache, stream));
+}
+
+vc_status vc_qcache_append(vc_qcache *cache, const void *k_new, const void *v_new, const int32_t *n_new,
+                           int max_new, int requantize, cudaStream_t stream)
+{
+    if (!qcache_ok(cache) || !k_new || !v_new || !n_new || max_new < 0) return VC_ERR_INVALID;
+    if (max_new == 0) return VC_OK;
+    return cuda_status(qcache_append(cache, k_new, v_new, n_new, nullptr, nullptr, max_new, requantize,
+                                     stream));
+}
+
+vc_status vc_qcache_commit(vc_qcache *cache, const void *k_blk, const void *v_blk, const int32_t *round_len,
+                           const int32_t *n_acc, int Dq, cudaStream_t stream)
+{
+    if (!qcache_ok(cache) || !k_blk || !v_blk || !round_len || !n_acc || Dq <= 0) return VC_ERR_INVALID;
+    return cuda_status(qcache_append(cache, k_blk, v_blk, nullptr, round_len, n_acc, Dq, 1, stream));
+}
+
+int64_t vc_drop_kept_count(int64_t L, vc_drop_cfg cfg)
+{
+    if (L < 0 || cfg.keep_top < 0 || cfg.keep_recent < 0) return -1;
+    const int64_t R = cfg.keep_recent < L ? cfg.keep_recent : L;
+    const int64_t cand = L - R;
+    return (cfg.keep_top < cand ? cfg.keep_top : cand) + R;
+}
+
+size_t vc_drop_tokens_workspace_bytes(int B, int H, int L)
+{
+    if (B <= 0 || H <= 0 || L < 0) return 0;
+    return drop_ws_bytes(B, H, L);
+}
+
+vc_status vc_drop_tokens(const float *scores, const void *k, const void *v, vc_dtype dt, int B, int H, int L,
+                         int d, vc_drop_cfg cfg, int32_t *kept_idx, void *k_out, void *v_out, void *ws,
+                         size_t ws_bytes, cudaStream_t stream)
+{
+    if (!scores || !k || !v || !kept_idx || !k_out || !v_out || !ws) return VC_ERR_INVALID;
+    if (!dtype_ok(dt) || B <= 0 || H <= 0 || L < 0 || d <= 0) return VC_ERR_INVALID;
+    if (cfg.keep_top < 0 || cfg.keep_recent < 0) return VC_ERR_INVALID;
+    if ((d * esize(dt)) % 16 || !aligned(k, 16) || !aligned(v, 16) || !aligned(k_out, 16) ||
+        !aligned(v_out, 16) || !aligned(ws, 256))
+        return VC_ERR_INVALID;
+    if (ws_bytes < drop_ws_bytes(B, H, L)) return VC_ERR_INVALID;
+    return cuda_status(drop_tokens(scores, k, v, dt, B, H, L, d, cfg.keep_top, cfg.keep_recent, kept_idx,
+                                   k_out, v_out, ws, stream));
+}
+
+size_t vc_draft_attn_workspace_bytes(const vc_cache_view *view, int Hq)
+{
+    if (!view) return 0;
+    if (view->kind == VC_CACHE_KIVI && !qcache_ok(view->kivi)) return 0;
+    if (view->kind == VC_CACHE_DENSE && (view->B <= 0 || view->Hkv <= 0 || view->max_len < 0)) return 0;
+    return draft_ws_bytes(view, Hq);
+}
+
+vc_status vc_draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq, float sm_scale,
+                        void *out, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!q || !view || !out || !ws || !dtype_ok(q_dt) || !aligned(ws, 256)) return VC_ERR_INVALID;
+    int Hkv, d;
+    if (view->kind == VC_CACHE_KIVI) {
+        if (!qcache_ok(view->kivi)) return VC_ERR_INVALID;
+        Hkv = view->kivi->Hkv;
+        d = view->kivi->d;
+        if (Hq <= 0 || Hq % Hkv || Hq / Hkv > 4) return VC_ERR_UNSUPPORTED;
+    } else if (view->kind == VC_CACHE_DENSE) {
+        if (!view->k || !view->v || !view->seq_len || !dtype_ok(view->dt)) return VC_ERR_INVALID;
+        if (view->B <= 0 || view->Hkv <= 0 || view->L_stride < view->max_len || view->max_len < 0)
+            return VC_ERR_INVALID;
+        if (view->d != 64 && view->d != 128) return VC_ERR_UNSUPPORTED;
+        if (view->dt != q_dt) return VC_ERR_INVALID;
+        if (!aligned(view->k, 16) || !aligned(view->v, 16)) return VC_ERR_INVALID;
+        Hkv = view->Hkv;
+        d = view->d;
+        if (Hq <= 0 || Hq % Hkv || Hq / Hkv > 4) return VC_ERR_UNSUPPORTED;
+    } else {
+        return VC_ERR_INVALID;
+    }
+    (void)d;
+    if (ws_bytes < draft_ws_bytes(view, Hq)) return VC_ERR_INVALID;
+    return cuda_status(draft_attn(q, q_dt, view, Hq, sm_scale, out, ws, stream));
+}
+
+size_t vc_verify_attn_workspace_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int max_ctx)
+{
+    if (!dtype_ok(dt) || B <= 0 || Dq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_ctx < 0) return 0;
+    return verify_ws_bytes(dt, B, Dq, Hq, Hkv, d, max_ctx);
+}
+
+vc_status vc_verify_attn(const void *q, const void *k, const void *v, vc_dtype dt, const int32_t *ctx_len,
+                         int B, int Dq, int Hq, int Hkv, int d, int L_stride, int max_ctx, float sm_scale,
+                         void *out, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!q || !k || !v || !ctx_len || !out || !ws || !dtype_ok(dt)) return VC_ERR_INVALID;
+    if (B <= 0 || Dq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_ctx < 0) return VC_ERR_INVALID;
+    if (d != 64 && d != 128) return VC_ERR_UNSUPPORTED;
+    if (L_stride < max_ctx + Dq) return VC_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(ws, 256)) return VC_ERR_INVALID;
+    if (ws_bytes < verify_ws_bytes(dt, B, Dq, Hq, Hkv, d, max_ctx)) return VC_ERR_INVALID;
+    if (!verify_uses_tensor_cores(dt, Dq, Hq, Hkv, d) && Hq / Hkv > 64) return VC_ERR_UNSUPPORTED;
+    return cuda_status(verify_attn(q, k, v, dt, ctx_len, B, Dq, Hq, Hkv, d, L_stride, max_ctx, sm_scale, out,
+                                   ws, stream));
+}
+
+size_t vc_accept_workspace_bytes(int B, int D, int V)
+{
+    if (B <= 0 || D < 0 || V <= 0) return 0;
+    return accept_ws_bytes(B, D, V);
+}
+
+vc_status vc_accept(const void *logits, vc_dtype dt, const int32_t *drafts, int B, int D, int V,
+                    int32_t *n_acc, int32_t *next_tok, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!logits || !n_acc || !next_tok || !ws || !dtype_ok(dt)) return VC_ERR_INVALID;
+    if (B <= 0 || D < 0 || D > 1024 || V <= 0 || (D > 0 && !drafts)) return VC_ERR_INVALID;
+    if (!aligned(ws, 256) || ws_bytes < accept_ws_bytes(B, D, V)) return VC_ERR_INVALID;
+    return cuda_status(accept(logits, dt, drafts, B, D, V, n_acc, next_tok, ws, stream));
+}
+
+vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes, cudaStream_t side_stream,
+                     cudaEvent_t done)
+{
+    if (!dst_dev || !src_pinned_host) return VC_ERR_INVALID;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, src_pinned_host) != cudaSuccess) {
+        cudaGetLastError();
+        return VC_ERR_INVALID;
+    }
+    if (a.type != cudaMemoryTypeHost) return VC_ERR_INVALID;   // pageable or device memory
+    cudaPointerAttributes ad;
+    if (cudaPointerGetAttributes(&ad, dst_dev) != cudaSuccess || ad.type != cudaMemoryTypeDevice) {
+        cudaGetLastError();
+        return VC_ERR_INVALID;
+    }
+    if (bytes) {
+        cudaError_t e = cudaMemcpyAsync(dst_dev, src_pinned_host, bytes, cudaMemcpyHostToDevice, side_stream);
+        if (e != cudaSuccess) return VC_ERR_CUDA;
+    }
+    if (done && cudaEventRecord(done, side_stream) != cudaSuccess) return VC_ERR_CUDA;
+    return VC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,567 @@
+// verify_attn.cu -- causal block attention of the drafted block against the
+// full KV cache (VeriCache verifies drafts against the full cache; the verify
+// step is compute-bound, paper page "What the paper found").
+//
+// Tensor-core path (bf16, d = 128): one CTA per (kv unit, 128-row query tile,
+// key split).  The 128 rows are the (query, head) pairs of the Hq/Hkv query
+// heads sharing one kv head, so the GQA heads and the drafted positions
+// together form a real dense M = 128 contraction.
+//   warp 0      TMA producer: Q once, then 64-key K and V tiles (128-byte
+//               swizzle) into a 2-stage ring;
+//   warp 1      single-thread tcgen05.mma issuer: S = Q K^T into a double-
+//               buffered TMEM tile (128 x 64 fp32), then O += P V into a TMEM
+//               accumulator (128 x 128 fp32), S(j+1) overlapping softmax(j);
+//   warps 2..5  softmax, one thread per row: tcgen05.ld of its S row, causal
+//               mask, exp2 online softmax with lazy rescaling of O (in TMEM),
+//               P written to shared memory as bf16 in the canonical K-major
+//               layout for the next MMA.
+// Every mbarrier wait is bounded; a timeout is recorded in the workspace
+// status block and the CTA drains out.  Split partials (m, l, o) go to the
+// workspace and a combine kernel writes the normalised output.
+//
+// CUDA-core path (fp32, or shapes outside the tensor-core kernel): one warp per
+// (row, key slice), fp32 throughout.
+#include <cudaTypedefs.h>
+
+#include "tcgen05.cuh"
+#include "vc_common.cuh"
+#include "vc_internal.h"
+
+namespace vc {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegBig = -1.0e30f;
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ======================================================= tensor-core kernel ==
+constexpr int TC_D = 128;
+constexpr int TC_M = 128;
+constexpr int TC_N = 64;                 // keys per tile
+constexpr int TC_STAGES = 2;
+constexpr int TC_THREADS = 192;          // 6 warps
+constexpr int TC_PART = 4 + TC_D;        // partial row: m, l, pad, pad, o[128]
+constexpr float TC_LAZY = 8.0f;
+
+// shared-memory carve-up (offsets from a 1024-byte aligned base)
+constexpr int SM_Q = 0;                                   // 2 x (128 x 128 B)
+constexpr int SM_K = SM_Q + TC_M * TC_D * 2;              // stages x (64 x 256 B)
+constexpr int SM_V = SM_K + TC_STAGES * TC_N * TC_D * 2;
+constexpr int SM_P = SM_V + TC_STAGES * TC_N * TC_D * 2;  // 128 x 64 bf16, no swizzle
+constexpr int SM_BAR = SM_P + TC_M * TC_N * 2;
+constexpr int SM_TOTAL = SM_BAR + 256;
+constexpr int TC_SMEM = SM_TOTAL;                         // 2 CTAs fit one SM
+
+constexpr uint32_t TMEM_COLS = 256;      // S0: 0..63, S1: 64..127, O: 128..255
+constexpr uint32_t TMEM_O = 128;
+
+struct TcParams {
+    const int32_t *ctx_len;
+    float *part;
+    int32_t *status;
+    int Hkv, Dq, grp, n_mtiles, n_split, tiles_per_split;
+    float scale_log2;
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t k_full[TC_STAGES], k_empty[TC_STAGES];
+    uint64_t v_full[TC_STAGES], v_empty[TC_STAGES];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_ready, pv_done;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Bars *B, int32_t *status,
+                                              int where)
+{
+    if (mbar_wait(bar, parity)) return true;
+    report_timeout(status, where);
+    atomicExch(&B->abort_flag, 1);
+    return false;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 2)
+verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, TcParams P)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw;
+    if (smem_u32(sm) & 1023u) {
+        // the swizzled operand tiles need 1024-byte alignment; never expected
+        if (threadIdx.x == 0) report_timeout(P.status, 99);
+        return;
+    }
+    Bars *B = reinterpret_cast<Bars *>(sm + SM_BAR);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int split = blockIdx.x;
+    const int mt = blockIdx.y % P.n_mtiles;
+    const int unit = blockIdx.y / P.n_mtiles;
+    const int b = unit / P.Hkv, kvh = unit % P.Hkv;
+    const int rows_q = TC_M / P.grp;                  // queries per tile
+    const int q0 = mt * rows_q;                       // first query of the tile
+    const int q_last = min(P.Dq, q0 + rows_q) - 1;
+    const int ctx = P.ctx_len[b];
+    const int n_tiles_all = (ctx + q_last + 1 + TC_N - 1) / TC_N;
+    const int t_lo = split * P.tiles_per_split;
+    const int t_hi = min(n_tiles_all, t_lo + P.tiles_per_split);
+    const int n = t_hi > t_lo ? t_hi - t_lo : 0;
+    float *part = P.part + ((size_t)blockIdx.y * P.n_split + split) * TC_M * TC_PART;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&B->q_full, 1);
+        for (int s = 0; s < TC_STAGES; ++s) {
+            mbar_init(&B->k_full[s], 1);
+            mbar_init(&B->k_empty[s], 1);
+            mbar_init(&B->v_full[s], 1);
+            mbar_init(&B->v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&B->s_full[s], 1);
+            mbar_init(&B->s_free[s], 128);
+        }
+        mbar_init(&B->p_ready, 128);
+        mbar_init(&B->pv_done, 1);
+        B->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && n > 0) {
+        tc::tmem_alloc(&B->tmem_base, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+
+    if (n == 0) {
+        // no key of this split is visible to the tile's rows: empty partial
+        for (int i = threadIdx.x; i < TC_M * TC_PART; i += TC_THREADS) {
+            const int c = i % TC_PART;
+            part[i] = c == 0 ? kNegBig : 0.f;
+        }
+        return;
+    }
+    const uint32_t tmem = B->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmQ);
+            tc::prefetch_tmap(&tmK);
+            tc::prefetch_tmap(&tmV);
+            mbar_arrive_expect_tx(&B->q_full, TC_M * TC_D * 2);
+            const int qrow = b * P.Dq + q0;
+            tc::tma_load_3d(sm + SM_Q, &tmQ, 0, kvh * P.grp, qrow, &B->q_full);
+            tc::tma_load_3d(sm + SM_Q + TC_M * 128, &tmQ, 64, kvh * P.grp, qrow, &B->q_full);
+            for (int j = 0; j < n; ++j) {
+                const int s = j % TC_STAGES;
+                const uint32_t par = ((j / TC_STAGES) - 1) & 1;
+                const int key0 = (t_lo + j) * TC_N;
+                if (j >= TC_STAGES && !wait_or_abort(&B->k_empty[s], par, B, P.status, 11)) break;
+                uint8_t *sk = sm + SM_K + s * TC_N * TC_D * 2;
+                mbar_arrive_expect_tx(&B->k_full[s], TC_N * TC_D * 2);
+                tc::tma_load_3d(sk, &tmK, 0, key0, unit, &B->k_full[s]);
+                tc::tma_load_3d(sk + TC_N * 128, &tmK, 64, key0, unit, &B->k_full[s]);
+                if (j >= TC_STAGES && !wait_or_abort(&B->v_empty[s], par, B, P.status, 12)) break;
+                uint8_t *sv = sm + SM_V + s * TC_N * TC_D * 2;
+                mbar_arrive_expect_tx(&B->v_full[s], TC_N * TC_D * 2);
+                tc::tma_load_3d(sv, &tmV, 0, key0, unit, &B->v_full[s]);
+                tc::tma_load_3d(sv + TC_N * 128, &tmV, 64, key0, unit, &B->v_full[s]);
+                if (*reinterpret_cast<volatile int32_t *>(&B->abort_flag)) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            const uint32_t idS = tc::idesc_bf16(TC_M, TC_N, false, false);
+            const uint32_t idO = tc::idesc_bf16(TC_M, TC_D, false, true);
+            const uint32_t sQ = smem_u32(sm + SM_Q);
+            bool ok = wait_or_abort(&B->q_full, 0, B, P.status, 21);
+            auto issue_S = [&](int j) -> bool {
+                const int s = j % TC_STAGES, sb = j & 1;
+                if (!wait_or_abort(&B->k_full[s], (j / TC_STAGES) & 1, B, P.status, 22)) return false;
+                if (j >= 2 && !wait_or_abort(&B->s_free[sb], ((j >> 1) - 1) & 1, B, P.status, 23))
+                    return false;
+                tc::fence_after();
+                const uint32_t sK = smem_u32(sm + SM_K + s * TC_N * TC_D * 2);
+#pragma unroll
+                for (int kk = 0; kk < TC_D / 16; ++kk) {
+                    const uint64_t ad = tc::smem_desc(sQ + (kk >> 2) * (TC_M * 128) + (kk & 3) * 32, 16,
+                                                      1024, tc::kSwizzle128B);
+                    const uint64_t bd = tc::smem_desc(sK + (kk >> 2) * (TC_N * 128) + (kk & 3) * 32, 16,
+                                                      1024, tc::kSwizzle128B);
+                    tc::mma_ss(tmem + sb * TC_N, ad, bd, idS, kk > 0);
+                }
+                tc::commit(&B->s_full[sb]);
+                tc::commit(&B->k_empty[s]);
+                return true;
+            };
+            if (ok) ok = issue_S(0);
+            for (int j = 0; ok && j < n; ++j) {
+                if (j + 1 < n && !issue_S(j + 1)) { ok = false; break; }
+                const int s = j % TC_STAGES;
+                if (!wait_or_abort(&B->p_ready, j & 1, B, P.status, 24)) { ok = false; break; }
+                if (!wait_or_abort(&B->v_full[s], (j / TC_STAGES) & 1, B, P.status, 25)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t sP = smem_u32(sm + SM_P);
+                const uint32_t sV = smem_u32(sm + SM_V + s * TC_N * TC_D * 2);
+#pragma unroll
+                for (int kk = 0; kk < TC_N / 16; ++kk) {
+                    // P: K-major, no swizzle; core matrices 8 rows x 16 B,
+                    // 128 B apart along K, 1024 B apart along M
+                    const uint64_t ad = tc::smem_desc(sP + kk * 256, 128, 1024, tc::kNoSwizzle);
+                    // V: MN-major (d contiguous), 128-B swizzle; atoms of 64 d x 8 keys,
+                    // next 64 d at +TC_N*128 bytes, next 8 keys at +1024 bytes
+                    const uint64_t bd = tc::smem_desc(sV + kk * 2048, TC_N * 128, 1024, tc::kSwizzle128B);
+                    tc::mma_ss(tmem + TMEM_O, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(&B->pv_done);
+                tc::commit(&B->v_empty[s]);
+            }
+        }
+    } else {
+        // --------------------------------------------------- softmax warps --
+        const int wq = warp & 3;                      // TMEM lane quarter
+        const int r = wq * 32 + lane;                 // tile row
+        const int qi = q0 + r / P.grp;                // query index in the block
+        const bool row_valid = qi < P.Dq;
+        const int kmax = ctx + qi;                    // last visible key
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        float m = kNegBig, l = 0.f;
+        uint8_t *sP = sm + SM_P;
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            const int sb = j & 1;
+            if (!wait_or_abort(&B->s_full[sb], (j >> 1) & 1, B, P.status, 31)) { ok = false; break; }
+            tc::fence_after();
+            float s[TC_N];
+            {
+                uint32_t u[32];
+#pragma unroll
+                for (int h = 0; h < TC_N / 32; ++h) {
+                    tc::ld32(tmem + lane_addr + sb * TC_N + h * 32, u);
+                    tc::ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) s[h * 32 + c] = __uint_as_float(u[c]);
+                }
+            }
+            tc::fence_before();
+            mbar_arrive(&B->s_free[sb]);
+            const int key0 = (t_lo + j) * TC_N;
+            float mx = kNegBig;
+#pragma unroll
+            for (int c = 0; c < TC_N; ++c) {
+                const bool vis = row_valid && (key0 + c <= kmax);
+                s[c] = vis ? s[c] * P.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[c]);
+            }
+            float alpha = 1.f;
+            if (mx > m + TC_LAZY) {
+                alpha = exp2f(m - mx);
+                m = mx;
+            }
+            float lsum = 0.f;
+            uint32_t pk[TC_N / 2];
+#pragma unroll
+            for (int c = 0; c < TC_N; c += 2) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s[c] - m), exp2f(s[c + 1] - m));
+                const float2 f2 = __bfloat1622float2(h2);
+                lsum += f2.x + f2.y;
+                pk[c / 2] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+            l = l * alpha + lsum;
+            // the single P buffer and O are free once PV(j-1) has completed
+            if (j > 0 && !wait_or_abort(&B->pv_done, (j - 1) & 1, B, P.status, 32)) { ok = false; break; }
+            tc::fence_after();
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int h = 0; h < TC_D / 32; ++h) {
+                    uint32_t u[32];
+                    tc::ld32(tmem + lane_addr + TMEM_O + h * 32, u);
+                    tc::ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) u[c] = __float_as_uint(__uint_as_float(u[c]) * alpha);
+                    tc::st32(tmem + lane_addr + TMEM_O + h * 32, u);
+                }
+                tc::st_wait();
+            }
+            // P row r: 8 chunks of 8 keys, core matrix (r/8, kb) at ((r/8)*8 + kb)*128 + (r%8)*16
+#pragma unroll
+            for (int kb = 0; kb < TC_N / 8; ++kb) {
+                uint4 v;
+                v.x = pk[kb * 4 + 0];
+                v.y = pk[kb * 4 + 1];
+                v.z = pk[kb * 4 + 2];
+                v.w = pk[kb * 4 + 3];
+                *reinterpret_cast<uint4 *>(sP + ((r >> 3) * 8 + kb) * 128 + (r & 7) * 16) = v;
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before();
+            mbar_arrive(&B->p_ready);
+        }
+        // epilogue: wait for the last PV, read O, store the partial row
+        float *pr = part + (size_t)r * TC_PART;
+        if (ok && wait_or_abort(&B->pv_done, (n - 1) & 1, B, P.status, 33)) {
+            tc::fence_after();
+            pr[0] = m;
+            pr[1] = l;
+            pr[2] = 0.f;
+            pr[3] = 0.f;
+#pragma unroll
+            for (int h = 0; h < TC_D / 32; ++h) {
+                uint32_t u[32];
+                tc::ld32(tmem + lane_addr + TMEM_O + h * 32, u);
+                tc::ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4 *>(pr + 4 + h * 32 + c) =
+                        make_float4(__uint_as_float(u[c]), __uint_as_float(u[c + 1]),
+                                    __uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
+            }
+        } else {
+            pr[0] = kNegBig;
+            pr[1] = 0.f;
+            for (int c = 2; c < TC_PART; ++c) pr[c] = 0.f;
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) {
+        __syncwarp();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// Merge the key splits of the tensor-core kernel.  One thread per (row, 4 channels).
+template <typename T>
+__global__ void verify_tc_combine(const float *__restrict__ part, int n_split, int n_mtiles, int Hkv,
+                                  int Hq, int Dq, int grp, T *__restrict__ out)
+{
+    const int item = blockIdx.x;                       // unit * n_mtiles + mt
+    const int mt = item % n_mtiles, unit = item / n_mtiles;
+    const int b = unit / Hkv, kvh = unit % Hkv;
+    const int r = blockIdx.y * 4 + (threadIdx.x >> 5);
+    const int c0 = (threadIdx.x & 31) * 4;
+    const int qi = mt * (TC_M / grp) + r / grp;
+    if (qi >= Dq) return;
+    const float *pp = part + (size_t)item * n_split * TC_M * TC_PART + (size_t)r * TC_PART;
+    const size_t sstride = (size_t)TC_M * TC_PART;
+    float M = kNegBig;
+    for (int s = 0; s < n_split; ++s) M = fmaxf(M, pp[s * sstride]);
+    float L = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < n_split; ++s) {
+        const float *q = pp + s * sstride;
+        const float w = exp2f(q[0] - M);
+        L += q[1] * w;
+        const float4 v = *reinterpret_cast<const float4 *>(q + 4 + c0);
+        o[0] += v.x * w;
+        o[1] += v.y * w;
+        o[2] += v.z * w;
+        o[3] += v.w * w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    T *dst = out + (((size_t)b * Dq + qi) * Hq + kvh * grp + r % grp) * TC_D + c0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = Elem<T>::from_f(o[i] * inv);
+}
+
+// ======================================================== CUDA-core kernel ===
+constexpr int SIMT_WARPS = 4;
+
+// grid (B*Dq*Hq); warp w of the CTA takes keys k = w, w+4, ...; merged in smem.
+template <typename T, int D>
+__global__ void __launch_bounds__(SIMT_WARPS * 32)
+verify_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                   const int32_t *__restrict__ ctx_len, int Dq, int Hq, int Hkv, int L_stride,
+                   float scale_log2, T *__restrict__ out)
+{
+    constexpr int CPL = D / 32;
+    const int row = blockIdx.x;                    // (b * Dq + i) * Hq + hq
+    const int hq = row % Hq, bi = row / Hq;
+    const int b = bi / Dq, i = bi % Dq;
+    const int grp = Hq / Hkv;
+    const int kvh = hq / grp;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nkeys = ctx_len[b] + i + 1;
+    const T *kb = k + ((size_t)b * Hkv + kvh) * L_stride * D;
+    const T *vb = v + ((size_t)b * Hkv + kvh) * L_stride * D;
+    float qv[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) qv[c] = Elem<T>::to_f(q[(size_t)row * D + lane * CPL + c]) * scale_log2;
+    float m = kNegBig, l = 0.f, o[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+    for (int t = warp; t < nkeys; t += SIMT_WARPS) {
+        float s = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) s = fmaf(qv[c], Elem<T>::to_f(kb[(size_t)t * D + lane * CPL + c]), s);
+        s = warp_sum(s);
+        const float mn = fmaxf(m, s);
+        const float a = exp2f(m - mn), p = exp2f(s - mn);
+        m = mn;
+        l = l * a + p;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) o[c] = o[c] * a + p * Elem<T>::to_f(vb[(size_t)t * D + lane * CPL + c]);
+    }
+    __shared__ float wm[SIMT_WARPS], wl[SIMT_WARPS], wo[SIMT_WARPS][D];
+    if (lane == 0) {
+        wm[warp] = m;
+        wl[warp] = l;
+    }
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) wo[warp][lane * CPL + c] = o[c];
+    __syncthreads();
+    if (warp == 0) {
+        float M = kNegBig;
+        for (int w = 0; w < SIMT_WARPS; ++w) M = fmaxf(M, wm[w]);
+        float L = 0.f;
+        for (int w = 0; w < SIMT_WARPS; ++w) L += wl[w] * exp2f(wm[w] - M);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            float acc = 0.f;
+            for (int w = 0; w < SIMT_WARPS; ++w) acc += wo[w][lane * CPL + c] * exp2f(wm[w] - M);
+            out[(size_t)row * D + lane * CPL + c] = Elem<T>::from_f(L > 0.f ? acc / L : 0.f);
+        }
+    }
+}
+
+// ================================================================== host ===
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms()
+{
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+struct TcPlan {
+    int n_mtiles, n_split, tiles_per_split;
+};
+
+TcPlan tc_plan(int B, int Dq, int Hkv, int grp, int max_ctx)
+{
+    TcPlan p;
+    p.n_mtiles = (Dq * grp + TC_M - 1) / TC_M;
+    const int tiles = (max_ctx + Dq + TC_N - 1) / TC_N;
+    const int items = B * Hkv * p.n_mtiles;
+    const int target = num_sms() * 2 * 3;            // ~3 waves of 2 CTAs per SM
+    int s = (target + items - 1) / items;
+    if (s > tiles) s = tiles;
+    if (s < 1) s = 1;
+    p.tiles_per_split = (tiles + s - 1) / s;
+    if (p.tiles_per_split < 2 && tiles >= 2) p.tiles_per_split = 2;
+    p.n_split = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    return p;
+}
+
+}  // namespace
+
+bool verify_uses_tensor_cores(vc_dtype dt, int Dq, int Hq, int Hkv, int d)
+{
+    const int grp = Hq / Hkv;
+    return dt == VC_BF16 && d == TC_D && (grp == 1 || grp == 2 || grp == 4 || grp == 8) && Dq >= 1;
+}
+
+size_t verify_ws_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int max_ctx)
+{
+    if (!verify_uses_tensor_cores(dt, Dq, Hq, Hkv, d)) return kStatusBytes;
+    const TcPlan p = tc_plan(B, Dq, Hkv, Hq / Hkv, max_ctx);
+    return kStatusBytes + align256((size_t)B * Hkv * p.n_mtiles * p.n_split * TC_M * TC_PART * 4);
+}
+
+cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt, const int32_t *ctx_len,
+                        int B, int Dq, int Hq, int Hkv, int d, int L_stride, int max_ctx, float sm_scale,
+                        void *out, void *ws, cudaStream_t st)
+{
+    const float sl2 = sm_scale * kLog2e;
+    if (verify_uses_tensor_cores(dt, Dq, Hq, Hkv, d)) {
+        const int grp = Hq / Hkv;
+        const TcPlan pl = tc_plan(B, Dq, Hkv, grp, max_ctx);
+        CUtensorMap mq, mk, mv;
+        if (!make_map_3d(&mq, q, TC_D, Hq, (uint64_t)B * Dq, (uint64_t)TC_D * 2, (uint64_t)Hq * TC_D * 2, 64,
+                         grp, TC_M / grp) ||
+            !make_map_3d(&mk, k, TC_D, L_stride, (uint64_t)B * Hkv, (uint64_t)TC_D * 2,
+                         (uint64_t)L_stride * TC_D * 2, 64, TC_N, 1) ||
+            !make_map_3d(&mv, v, TC_D, L_stride, (uint64_t)B * Hkv, (uint64_t)TC_D * 2,
+                         (uint64_t)L_stride * TC_D * 2, 64, TC_N, 1))
+            return cudaErrorInvalidValue;
+        TcParams P;
+        P.ctx_len = ctx_len;
+        P.status = (int32_t *)ws;
+        P.part = (float *)((uint8_t *)ws + kStatusBytes);
+        P.Hkv = Hkv;
+        P.Dq = Dq;
+        P.grp = grp;
+        P.n_mtiles = pl.n_mtiles;
+        P.n_split = pl.n_split;
+        P.tiles_per_split = pl.tiles_per_split;
+        P.scale_log2 = sl2;
+        cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        dim3 grid(pl.n_split, B * Hkv * pl.n_mtiles);
+        verify_tc_kernel<<<grid, TC_THREADS, TC_SMEM, st>>>(mq, mk, mv, P);
+        dim3 cgrid(B * Hkv * pl.n_mtiles, TC_M / 4);
+        verify_tc_combine<__nv_bfloat16><<<cgrid, 128, 0, st>>>(P.part, pl.n_split, pl.n_mtiles, Hkv, Hq, Dq,
+                                                                grp, (__nv_bfloat16 *)out);
+        return cudaGetLastError();
+    }
+    const int rows = B * Dq * Hq;
+    if (rows == 0) return cudaSuccess;
+    if (dt == VC_BF16) {
+        if (d == 128)
+            verify_simt_kernel<__nv_bfloat16, 128><<<rows, SIMT_WARPS * 32, 0, st>>>(
+                (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, ctx_len, Dq, Hq,
+                Hkv, L_stride, sl2, (__nv_bfloat16 *)out);
+        else
+            verify_simt_kernel<__nv_bfloat16, 64><<<rows, SIMT_WARPS * 32, 0, st>>>(
+                (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, ctx_len, Dq, Hq,
+                Hkv, L_stride, sl2, (__nv_bfloat16 *)out);
+    } else {
+        if (d == 128)
+            verify_simt_kernel<float, 128><<<rows, SIMT_WARPS * 32, 0, st>>>(
+                (const float *)q, (const float *)k, (const float *)v, ctx_len, Dq, Hq, Hkv, L_stride, sl2,
+                (float *)out);
+        else
+            verify_simt_kernel<float, 64><<<rows, SIMT_WARPS * 32, 0, st>>>(
+                (const float *)q, (const float *)k, (const float *)v, ctx_len, Dq, Hq, Hkv, L_stride, sl2,
+                (float *)out);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace vc

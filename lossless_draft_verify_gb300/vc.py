@@ -1,0 +1,313 @@
+"""Thin Python binding of the C ABI in include/vc.h (ctypes).
+
+Argument marshalling only: every function here turns torch tensors into
+pointers and sizes, calls the entry point of the same name in libvc.so and
+raises on a non-OK status.  No computation happens in Python, and there is no
+fallback: if the library is missing or cannot be loaded, importing the
+functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libvc.so")
+
+VC_OK, VC_ERR_INVALID, VC_ERR_UNSUPPORTED, VC_ERR_CUDA, VC_ERR_TIMEOUT = 0, 1, 2, 3, 4
+VC_BF16, VC_F32 = 0, 1
+VC_CACHE_KIVI, VC_CACHE_DENSE = 0, 1
+
+c_void_p, c_int, c_float, c_size_t, c_int64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                                                ctypes.c_size_t, ctypes.c_int64)
+c_int32 = ctypes.c_int32
+
+
+class VcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+
+
+class QuantCfg(ctypes.Structure):
+    _fields_ = [("bits", c_int32), ("group", c_int32), ("residual", c_int32)]
+
+
+class QCacheC(ctypes.Structure):
+    _fields_ = [("records", c_void_p), ("k_res", c_void_p), ("v_res", c_void_p),
+                ("n_groups", c_void_p), ("seq_len", c_void_p), ("status", c_void_p),
+                ("B", c_int32), ("Hkv", c_int32), ("d", c_int32), ("cfg", QuantCfg),
+                ("max_groups", c_int32), ("res_cap", c_int32), ("res_dtype", c_int)]
+
+
+class DropCfg(ctypes.Structure):
+    _fields_ = [("keep_top", c_int64), ("keep_recent", c_int64)]
+
+
+class CacheView(ctypes.Structure):
+    _fields_ = [("kind", c_int), ("kivi", ctypes.POINTER(QCacheC)), ("k", c_void_p), ("v", c_void_p),
+                ("dt", c_int), ("seq_len", c_void_p), ("B", c_int32), ("Hkv", c_int32), ("d", c_int32),
+                ("L_stride", c_int32), ("max_len", c_int32)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libvc.so (built by lossless_draft_verify_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libvc.so not built ({LIB_PATH}); run lossless_draft_verify_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P = c_void_p
+    L.vc_status_str.restype = ctypes.c_char_p
+    L.vc_status_str.argtypes = [c_int]
+    L.vc_version.restype = ctypes.c_char_p
+    L.vc_check.restype = c_int
+    L.vc_check.argtypes = [P]
+    L.vc_workspace_init.restype = c_int
+    L.vc_workspace_init.argtypes = [P, c_size_t, P]
+    L.vc_poll_status.restype = c_int
+    L.vc_poll_status.argtypes = [P, P]
+    L.vc_record_bytes.restype = c_size_t
+    L.vc_record_bytes.argtypes = [c_int, c_int]
+    L.vc_quantize_kv.restype = c_int
+    L.vc_quantize_kv.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(QCacheC), P]
+    L.vc_qcache_append.restype = c_int
+    L.vc_qcache_append.argtypes = [ctypes.POINTER(QCacheC), P, P, P, c_int, c_int, P]
+    L.vc_qcache_commit.restype = c_int
+    L.vc_qcache_commit.argtypes = [ctypes.POINTER(QCacheC), P, P, P, P, c_int, P]
+    L.vc_drop_kept_count.restype = c_int64
+    L.vc_drop_kept_count.argtypes = [c_int64, DropCfg]
+    L.vc_drop_tokens_workspace_bytes.restype = c_size_t
+    L.vc_drop_tokens_workspace_bytes.argtypes = [c_int, c_int, c_int]
+    L.vc_drop_tokens.restype = c_int
+    L.vc_drop_tokens.argtypes = [P, P, P, c_int, c_int, c_int, c_int, c_int, DropCfg, P, P, P, P, c_size_t, P]
+    L.vc_draft_attn_workspace_bytes.restype = c_size_t
+    L.vc_draft_attn_workspace_bytes.argtypes = [ctypes.POINTER(CacheView), c_int]
+    L.vc_draft_attn.restype = c_int
+    L.vc_draft_attn.argtypes = [P, c_int, ctypes.POINTER(CacheView), c_int, c_float, P, P, c_size_t, P]
+    L.vc_verify_attn_workspace_bytes.restype = c_size_t
+    L.vc_verify_attn_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int, c_int]
+    L.vc_verify_attn.restype = c_int
+    L.vc_verify_attn.argtypes = [P, P, P, c_int, P, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+                                 P, P, c_size_t, P]
+    L.vc_accept_workspace_bytes.restype = c_size_t
+    L.vc_accept_workspace_bytes.argtypes = [c_int, c_int, c_int]
+    L.vc_accept.restype = c_int
+    L.vc_accept.argtypes = [P, c_int, P, c_int, c_int, c_int, P, P, P, c_size_t, P]
+    L.vc_swap_in.restype = c_int
+    L.vc_swap_in.argtypes = [P, P, c_size_t, P, P]
+    _lib = L
+    return L
+
+
+EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_poll_status",
+            "vc_record_bytes", "vc_quantize_kv", "vc_qcache_append", "vc_qcache_commit", "vc_drop_kept_count",
+            "vc_drop_tokens_workspace_bytes", "vc_drop_tokens", "vc_draft_attn_workspace_bytes",
+            "vc_draft_attn", "vc_verify_attn_workspace_bytes", "vc_verify_attn",
+            "vc_accept_workspace_bytes", "vc_accept", "vc_swap_in"]
+
+
+def status_str(s: int) -> str:
+    return load().vc_status_str(int(s)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != VC_OK:
+        raise VcError(rc, where)
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return VC_BF16
+    if t.dtype == torch.float32:
+        return VC_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+# ---------------------------------------------------------------- memory --
+
+class Workspace:
+    """A zero-initialised device workspace (the caller-owned scratch buffer)."""
+
+    def __init__(self, nbytes: int, device="cuda"):
+        self.nbytes = max(int(nbytes), 256)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
+
+    def ensure(self, nbytes: int):
+        if nbytes > self.nbytes:
+            self.__init__(nbytes, self.buf.device)
+        return self
+
+    @property
+    def ptr(self):
+        return self.buf.data_ptr()
+
+
+class QCache:
+    """Caller-owned storage of one layer's KIVI cache (include/vc.h, vc_qcache)."""
+
+    def __init__(self, B, Hkv, d, bits, max_groups, res_cap, residual=0, group=32,
+                 res_dtype=torch.bfloat16, device="cuda"):
+        rb = vc_record_bytes(bits, d)
+        self.rec_bytes = rb
+        self.records = torch.zeros(B * Hkv * max(max_groups, 1) * rb, dtype=torch.uint8, device=device)
+        self.k_res = torch.zeros(B, Hkv, res_cap, d, dtype=res_dtype, device=device)
+        self.v_res = torch.zeros_like(self.k_res)
+        self.n_groups = torch.zeros(B, dtype=torch.int32, device=device)
+        self.seq_len = torch.zeros(B, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.c = QCacheC(self.records.data_ptr(), self.k_res.data_ptr(), self.v_res.data_ptr(),
+                         self.n_groups.data_ptr(), self.seq_len.data_ptr(), self.status.data_ptr(),
+                         B, Hkv, d, QuantCfg(bits, group, residual), max_groups, res_cap, _dt(self.k_res))
+        self.B, self.Hkv, self.d, self.bits, self.group, self.residual = B, Hkv, d, bits, group, residual
+        self.max_groups, self.res_cap = max_groups, res_cap
+
+    def view(self) -> CacheView:
+        v = CacheView()
+        v.kind = VC_CACHE_KIVI
+        v.kivi = ctypes.pointer(self.c)
+        return v
+
+    def record_view(self) -> torch.Tensor:
+        return self.records.view(self.B, self.Hkv, max(self.max_groups, 1), self.rec_bytes)
+
+
+def dense_view(k: torch.Tensor, v: torch.Tensor, seq_len: torch.Tensor, max_len: int) -> CacheView:
+    B, Hkv, Ls, d = k.shape
+    cv = CacheView()
+    cv.kind = VC_CACHE_DENSE
+    cv.k, cv.v, cv.dt = k.data_ptr(), v.data_ptr(), _dt(k)
+    cv.seq_len = seq_len.data_ptr()
+    cv.B, cv.Hkv, cv.d, cv.L_stride, cv.max_len = B, Hkv, d, Ls, int(max_len)
+    return cv
+
+
+# ----------------------------------------------------------- entry points --
+
+def vc_version() -> str:
+    return load().vc_version().decode()
+
+
+def vc_record_bytes(bits: int, d: int) -> int:
+    return int(load().vc_record_bytes(bits, d))
+
+
+def vc_check(stream=None):
+    _check(load().vc_check(_stream(stream)), "vc_check")
+
+
+def vc_workspace_init(ws: Workspace, stream=None):
+    _check(load().vc_workspace_init(ws.ptr, ws.nbytes, _stream(stream)), "vc_workspace_init")
+
+
+def vc_poll_status(ws: Workspace, stream=None) -> int:
+    return int(load().vc_poll_status(ws.ptr, _stream(stream)))
+
+
+def vc_quantize_kv(k: torch.Tensor, v: torch.Tensor, cache: QCache, L: int | None = None, stream=None):
+    B, Hkv, Ls, d = k.shape
+    L = Ls if L is None else int(L)
+    assert k.is_contiguous() and v.is_contiguous() and v.shape == k.shape
+    _check(load().vc_quantize_kv(k.data_ptr(), v.data_ptr(), _dt(k), B, Hkv, L, Ls, d,
+                                 ctypes.byref(cache.c), _stream(stream)), "vc_quantize_kv")
+
+
+def vc_qcache_append(cache: QCache, k_new: torch.Tensor, v_new: torch.Tensor, n_new: torch.Tensor,
+                     requantize: bool = True, stream=None):
+    assert k_new.is_contiguous() and v_new.is_contiguous() and n_new.dtype == torch.int32
+    max_new = k_new.shape[2]
+    _check(load().vc_qcache_append(ctypes.byref(cache.c), k_new.data_ptr(), v_new.data_ptr(),
+                                   n_new.data_ptr(), max_new, int(bool(requantize)), _stream(stream)),
+           "vc_qcache_append")
+
+
+def vc_qcache_commit(cache: QCache, k_blk: torch.Tensor, v_blk: torch.Tensor, round_len: torch.Tensor,
+                     n_acc: torch.Tensor, stream=None):
+    assert k_blk.is_contiguous() and v_blk.is_contiguous()
+    assert round_len.dtype == torch.int32 and n_acc.dtype == torch.int32
+    _check(load().vc_qcache_commit(ctypes.byref(cache.c), k_blk.data_ptr(), v_blk.data_ptr(),
+                                   round_len.data_ptr(), n_acc.data_ptr(), k_blk.shape[2], _stream(stream)),
+           "vc_qcache_commit")
+
+
+def vc_drop_kept_count(L: int, keep_top: int, keep_recent: int) -> int:
+    return int(load().vc_drop_kept_count(L, DropCfg(keep_top, keep_recent)))
+
+
+def vc_drop_tokens_workspace_bytes(B, H, L) -> int:
+    return int(load().vc_drop_tokens_workspace_bytes(B, H, L))
+
+
+def vc_drop_tokens(scores, k, v, keep_top: int, keep_recent: int, kept_idx, k_out, v_out, ws: Workspace,
+                   stream=None):
+    B, H, L, d = k.shape
+    assert scores.dtype == torch.float32 and scores.is_contiguous()
+    _check(load().vc_drop_tokens(scores.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(k), B, H, L, d,
+                                 DropCfg(keep_top, keep_recent), kept_idx.data_ptr(), k_out.data_ptr(),
+                                 v_out.data_ptr(), ws.ptr, ws.nbytes, _stream(stream)), "vc_drop_tokens")
+
+
+def vc_draft_attn_workspace_bytes(view: CacheView, Hq: int) -> int:
+    return int(load().vc_draft_attn_workspace_bytes(ctypes.byref(view), Hq))
+
+
+def vc_draft_attn(q: torch.Tensor, view: CacheView, sm_scale: float, out: torch.Tensor, ws: Workspace,
+                  stream=None):
+    B, Hq, d = q.shape
+    assert q.is_contiguous() and out.is_contiguous()
+    _check(load().vc_draft_attn(q.data_ptr(), _dt(q), ctypes.byref(view), Hq, sm_scale, out.data_ptr(), ws.ptr,
+                                ws.nbytes, _stream(stream)), "vc_draft_attn")
+
+
+def vc_verify_attn_workspace_bytes(dtype, B, Dq, Hq, Hkv, d, max_ctx) -> int:
+    dt = VC_BF16 if dtype == torch.bfloat16 else VC_F32
+    return int(load().vc_verify_attn_workspace_bytes(dt, B, Dq, Hq, Hkv, d, max_ctx))
+
+
+def vc_verify_attn(q, k, v, ctx_len, max_ctx: int, sm_scale: float, out, ws: Workspace, stream=None):
+    B, Dq, Hq, d = q.shape
+    _, Hkv, Ls, _ = k.shape
+    assert q.is_contiguous() and k.is_contiguous() and v.is_contiguous() and ctx_len.dtype == torch.int32
+    _check(load().vc_verify_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), ctx_len.data_ptr(), B, Dq, Hq,
+                                 Hkv, d, Ls, int(max_ctx), sm_scale, out.data_ptr(), ws.ptr, ws.nbytes,
+                                 _stream(stream)), "vc_verify_attn")
+
+
+def vc_accept_workspace_bytes(B, D, V) -> int:
+    return int(load().vc_accept_workspace_bytes(B, D, V))
+
+
+def vc_accept(logits, drafts, n_acc, next_tok, ws: Workspace, stream=None):
+    B, D1, V = logits.shape
+    assert logits.is_contiguous()
+    dp = drafts.data_ptr() if drafts is not None and drafts.numel() else None
+    _check(load().vc_accept(logits.data_ptr(), _dt(logits), dp, B, D1 - 1, V, n_acc.data_ptr(),
+                            next_tok.data_ptr(), ws.ptr, ws.nbytes, _stream(stream)), "vc_accept")
+
+
+def vc_swap_in(dst: torch.Tensor, src_pinned: torch.Tensor, nbytes: int | None = None, stream=None,
+               done_event: torch.cuda.Event | None = None):
+    n = dst.numel() * dst.element_size() if nbytes is None else int(nbytes)
+    ev = None
+    if done_event is not None:
+        if not done_event.cuda_event:          # torch creates the event lazily
+            done_event.record(torch.cuda.current_stream() if stream is None else stream)
+        ev = done_event.cuda_event
+    _check(load().vc_swap_in(dst.data_ptr(), src_pinned.data_ptr(), n, _stream(stream), ev), "vc_swap_in")

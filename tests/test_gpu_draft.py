@@ -1,0 +1,101 @@
+"""GPU parity of the draft decode attention (vc_draft_attn) against the fp64
+oracle on the oracle's own quantized cache (bit-identical to the GPU's, see
+test_gpu_quantize), and over dense (compacted or full) caches.
+Tolerance: max |gpu - oracle| <= 2e-2 * max |oracle| per output tensor."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_draft_verify_gb300 import inputs
+from helpers import assert_attn_close, f32, lib
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_kivi(vc, B, Hq, Hkv, L, d, bits, R, dtype=torch.bfloat16, seed=0, extra_groups=0):
+    k, v = inputs.kv_with_outliers(B, Hkv, L, d, seed=seed, device="cuda", dtype=dtype)
+    q = inputs.normal_bf16((B, Hq, d), seed + 100, device="cuda").to(dtype)
+    G = 32
+    maxg = max(1, (L - R) // G + extra_groups)
+    cache = vc.QCache(B, Hkv, d, bits, maxg, R + G + 8, R, res_dtype=dtype)
+    vc.vc_quantize_kv(k, v, cache)
+    view = cache.view()
+    ws = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, Hq))
+    out = torch.empty_like(q)
+    scale = inputs.default_scale(d)
+    vc.vc_draft_attn(q, view, scale, out, ws)
+    torch.cuda.synchronize()
+    assert vc.vc_poll_status(ws) == 0
+    return k, v, q, out, scale
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,d,bits,R,dtype", [
+    (2, 8, 2, 1000, 128, 2, 128, torch.bfloat16),    # many groups, ragged residual
+    (3, 8, 2, 777, 128, 4, 128, torch.bfloat16),
+    (2, 4, 2, 517, 64, 4, 0, torch.float32),         # tiny-decoder shape (fp32, grp 2)
+    (1, 4, 4, 300, 128, 2, 16, torch.bfloat16),      # grp 1
+    (2, 8, 2, 100, 128, 2, 128, torch.bfloat16),     # residual only (no group)
+    (1, 8, 2, 32, 64, 2, 0, torch.bfloat16),         # exactly one group, empty residual
+])
+def test_draft_kivi_matches_oracle(B, Hq, Hkv, L, d, bits, R, dtype):
+    vc = lib()
+    k, v, q, out, scale = _run_kivi(vc, B, Hq, Hkv, L, d, bits, R, dtype, seed=L + bits)
+    qc = oracle.kivi_quantize(f32(k), f32(v), bits, 32, R)
+    want = oracle.kivi_decode_attn(f32(q), qc, scale)
+    assert_attn_close(out, want, what=f"kivi {B}x{Hq}/{Hkv}x{L}x{d} b{bits}")
+
+
+def test_draft_kivi_spare_capacity_and_ragged_lengths():
+    """Record capacity beyond the used groups, and per-sequence lengths that
+    differ (appended tokens), still attend exactly the cached tokens."""
+    vc = lib()
+    B, Hq, Hkv, d, bits, R, G = 3, 8, 2, 128, 2, 64, 32
+    L0 = 400
+    k, v = inputs.kv_with_outliers(B, Hkv, L0 + 80, d, seed=3, device="cuda")
+    q = inputs.normal_bf16((B, Hq, d), 77, device="cuda")
+    cache = vc.QCache(B, Hkv, d, bits, 40, R + G + 96, R)
+    vc.vc_quantize_kv(k[:, :, :L0].contiguous(), v[:, :, :L0].contiguous(), cache)
+    add = [0, 37, 80]
+    kn = k[:, :, L0:].contiguous()
+    vn = v[:, :, L0:].contiguous()
+    vc.vc_qcache_append(cache, kn, vn, torch.tensor(add, dtype=torch.int32, device="cuda"), requantize=True)
+    view = cache.view()
+    ws = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, Hq))
+    out = torch.empty_like(q)
+    vc.vc_draft_attn(q, view, 0.09, out, ws)
+    torch.cuda.synchronize()
+    for b in range(B):
+        L = L0 + add[b]
+        qc = oracle.kivi_quantize(f32(k[b:b + 1, :, :L]), f32(v[b:b + 1, :, :L]), bits, G, R)
+        want = oracle.kivi_decode_attn(f32(q[b:b + 1]), qc, 0.09)
+        assert_attn_close(out[b:b + 1], want, what=f"seq {b}")
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_draft_dense_matches_oracle(dtype, d):
+    vc = lib()
+    B, Hq, Hkv, Ls = 3, 8, 2, 700
+    k, v = inputs.kv_with_outliers(B, Hkv, Ls, d, seed=9, device="cuda", dtype=dtype, n_out=0)
+    q = inputs.normal_bf16((B, Hq, d), 19, device="cuda").to(dtype)
+    lens = torch.tensor([700, 333, 1], dtype=torch.int32, device="cuda")
+    view = vc.dense_view(k, v, lens, 700)
+    ws = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, Hq))
+    out = torch.empty_like(q)
+    vc.vc_draft_attn(q, view, 0.1, out, ws)
+    torch.cuda.synchronize()
+    want = oracle.dense_decode_attn(f32(q), f32(k), f32(v), lens.cpu().numpy(), 0.1)
+    assert_attn_close(out, want, what="dense")
+
+
+def test_draft_full_size_sampled():
+    """The 16-sequence, 32/8-head, 32768-token 2-bit workload in the launch
+    configuration the benchmark times; outputs of sampled sequences against
+    the oracle."""
+    vc = lib()
+    B, Hq, Hkv, L, d, R = 16, 32, 8, 32768, 128, 128
+    k, v, q, out, scale = _run_kivi(vc, B, Hq, Hkv, L, d, 2, R, seed=1)
+    for b in (0, 7, 15):
+        qc = oracle.kivi_quantize(f32(k[b:b + 1]), f32(v[b:b + 1]), 2, 32, R)
+        want = oracle.kivi_decode_attn(f32(q[b:b + 1]), qc, scale)
+        assert_attn_close(out[b:b + 1], want, what=f"full-size seq {b}")
