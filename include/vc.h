@@ -289,6 +289,30 @@ vc_status vc_accept(const void *logits, vc_dtype dt, const int32_t *drafts, int 
                     int V, int32_t *n_acc, int32_t *next_tok, void *ws, size_t ws_bytes,
                     cudaStream_t stream);
 
+/*
+ * vc_accept_noalloc -- vc_accept for callers that cannot allocate device
+ * memory (no counterpart in the paper: this is a library convenience).
+ * Some callers have no way to provide the workspace vc_accept needs: code
+ * running inside another framework that owns all device memory through its
+ * own pool, plugin hosts that expose no allocator, and latency-critical loops
+ * where cudaMalloc/cudaFree would synchronize the device.  This entry point
+ * takes the same inputs and outputs as vc_accept and computes the same
+ * results, but keeps its scratch in a static device buffer inside the library
+ * (about 516 KiB, held by every GPU that loads the library until the process
+ * exits); it calls no allocator.
+ * Limits: B <= 1024 and B * (D + 1) <= 16384; larger requests return
+ * VC_ERR_INVALID and enqueue nothing.
+ * The first call on a device (made with that device current) looks up the
+ * buffer's device address; make that first call before any stream capture.
+ * All calls on one device share the buffer, so calls that may run
+ * concurrently on the GPU (different streams without ordering) race and
+ * must be serialized by the caller.  Each call clears the part of the buffer
+ * that must start at zero; the rest keeps the previous call's contents.
+ */
+vc_status vc_accept_noalloc(const void *logits, vc_dtype dt, const int32_t *drafts, int B,
+                            int D, int V, int32_t *n_acc, int32_t *next_tok,
+                            cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* (6) full-KV swap-in                                                       */
 /* ------------------------------------------------------------------------ */

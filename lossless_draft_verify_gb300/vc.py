@@ -100,6 +100,8 @@ def load() -> ctypes.CDLL:
     L.vc_accept_workspace_bytes.argtypes = [c_int, c_int, c_int]
     L.vc_accept.restype = c_int
     L.vc_accept.argtypes = [P, c_int, P, c_int, c_int, c_int, P, P, P, c_size_t, P]
+    L.vc_accept_noalloc.restype = c_int
+    L.vc_accept_noalloc.argtypes = [P, c_int, P, c_int, c_int, c_int, P, P, P]
     L.vc_swap_in.restype = c_int
     L.vc_swap_in.argtypes = [P, P, c_size_t, P, P]
     _lib = L
@@ -110,7 +112,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_record_bytes", "vc_quantize_kv", "vc_qcache_append", "vc_qcache_commit", "vc_drop_kept_count",
             "vc_drop_tokens_workspace_bytes", "vc_drop_tokens", "vc_draft_attn_workspace_bytes",
             "vc_draft_attn", "vc_verify_attn_workspace_bytes", "vc_verify_attn",
-            "vc_accept_workspace_bytes", "vc_accept", "vc_swap_in"]
+            "vc_accept_workspace_bytes", "vc_accept", "vc_accept_noalloc", "vc_swap_in"]
 
 
 def status_str(s: int) -> str:
@@ -300,6 +302,16 @@ def vc_accept(logits, drafts, n_acc, next_tok, ws: Workspace, stream=None):
     dp = drafts.data_ptr() if drafts is not None and drafts.numel() else None
     _check(load().vc_accept(logits.data_ptr(), _dt(logits), dp, B, D1 - 1, V, n_acc.data_ptr(),
                             next_tok.data_ptr(), ws.ptr, ws.nbytes, _stream(stream)), "vc_accept")
+
+
+def vc_accept_noalloc(logits, drafts, n_acc, next_tok, stream=None):
+    """vc_accept without a workspace: the library's static device buffer is
+    used instead (for callers that cannot allocate; see include/vc.h)."""
+    B, D1, V = logits.shape
+    assert logits.is_contiguous()
+    dp = drafts.data_ptr() if drafts is not None and drafts.numel() else None
+    _check(load().vc_accept_noalloc(logits.data_ptr(), _dt(logits), dp, B, D1 - 1, V, n_acc.data_ptr(),
+                                    next_tok.data_ptr(), _stream(stream)), "vc_accept_noalloc")
 
 
 def vc_swap_in(dst: torch.Tensor, src_pinned: torch.Tensor, nbytes: int | None = None, stream=None,
