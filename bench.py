@@ -335,6 +335,104 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------
+# single-kernel mode: one hot-path kernel at its own workload, for rooflines
+# and profiler captures (python bench.py --kernel draft|verify|accept|quantize|drop|dense_draft)
+# --------------------------------------------------------------------------
+
+def run_kernel(args, dev):
+    from lossless_draft_verify_gb300 import inputs, vc
+    hbm, tf_burst, _, peak_src = measured_peaks()
+    name = args.kernel
+    rec = {}
+    flops = None
+    if name in ("draft", "quantize"):
+        k, v = inputs.kv_with_outliers(B, HKV, CTX, D_HEAD, seed=1, device=dev)
+        cache = vc.QCache(B, HKV, D_HEAD, BITS, (CTX - RESIDUAL) // GROUP, RESIDUAL + GROUP + 8, RESIDUAL)
+        vc.vc_quantize_kv(k, v, cache)
+        rb = vc.vc_record_bytes(BITS, D_HEAD)
+        ng = (CTX - RESIDUAL) // GROUP
+        if name == "quantize":
+            fn = lambda: vc.vc_quantize_kv(k, v, cache)
+            nbytes = 2 * k.numel() * 2 + B * HKV * ng * rb
+            rec = {"workload": "KIVI 2-bit g32 prefill of bf16 K/V [16,8,32768,128], R=128"}
+        else:
+            del k, v
+            q = inputs.normal_bf16((B, HQ, D_HEAD), 5, device=dev)
+            out = torch.empty_like(q)
+            view = cache.view()
+            ws = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, HQ), device=dev)
+            scale = inputs.default_scale(D_HEAD)
+            fn = lambda: vc.vc_draft_attn(q, view, scale, out, ws)
+            nbytes = B * HKV * (ng * rb + 2 * RESIDUAL * D_HEAD * 2) + 2 * q.numel() * 2
+            rec = {"workload": "draft attention, KIVI 2-bit cache [16,8,32768,128] R=128, q [16,32,128] bf16"}
+    elif name == "verify":
+        dq = args.dq
+        q = inputs.normal_bf16((B, dq, HQ, D_HEAD), 8, device=dev)
+        k = inputs.normal_bf16((B, HKV, CTX + dq, D_HEAD), 9, device=dev)
+        v = inputs.normal_bf16((B, HKV, CTX + dq, D_HEAD), 10, device=dev)
+        ctx = torch.full((B,), CTX, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        ws = vc.Workspace(vc.vc_verify_attn_workspace_bytes(torch.bfloat16, B, dq, HQ, HKV, D_HEAD, CTX), device=dev)
+        scale = inputs.default_scale(D_HEAD)
+        fn = lambda: vc.vc_verify_attn(q, k, v, ctx, CTX, scale, out, ws)
+        nbytes = 2 * k.numel() * 2 + 2 * q.numel() * 2
+        flops = 4 * D_HEAD * B * HQ * sum(CTX + i + 1 for i in range(dq))
+        rec = {"workload": f"verify attention, Dq={dq}, bf16 K/V [16,8,{CTX + dq},128], 32/8 heads"}
+    elif name == "accept":
+        case = inputs.accept_case(B, HORIZON, VOCAB, seed=0, device=dev)
+        n = torch.empty(B, dtype=torch.int32, device=dev)
+        nx = torch.empty(B, dtype=torch.int32, device=dev)
+        ws = vc.Workspace(vc.vc_accept_workspace_bytes(B, HORIZON, VOCAB), device=dev)
+        fn = lambda: vc.vc_accept(case.logits, case.drafts, n, nx, ws)
+        nbytes = case.logits.numel() * 2
+        rec = {"workload": "greedy acceptance, logits [16,33,151936] bf16"}
+    elif name in ("drop", "dense_draft"):
+        Bd, Hd, Ld = 4, 8, 131072
+        scores = inputs.zipf_scores(Bd, Hd, Ld, seed=0, device=dev)
+        k, v = inputs.kv_with_outliers(Bd, Hd, Ld, D_HEAD, seed=8, device=dev, n_out=0)
+        n_keep = vc.vc_drop_kept_count(Ld, Ld // 4, 256)
+        kept = torch.empty(Bd, Hd, n_keep, dtype=torch.int32, device=dev)
+        ko = torch.empty(Bd, Hd, n_keep, D_HEAD, dtype=torch.bfloat16, device=dev)
+        vo = torch.empty_like(ko)
+        ws = vc.Workspace(vc.vc_drop_tokens_workspace_bytes(Bd, Hd, Ld), device=dev)
+        drop = lambda: vc.vc_drop_tokens(scores, k, v, Ld // 4, 256, kept, ko, vo, ws)
+        if name == "drop":
+            fn = drop
+            nbytes = scores.numel() * 4 + 2 * 2 * ko.numel() * 2 + kept.numel() * 4
+            rec = {"workload": "token dropping 4x: scores [4,8,131072] Zipf(1.1), keep 32768 + 256, gather K/V"}
+        else:
+            drop()
+            q = inputs.normal_bf16((Bd, 4 * Hd, D_HEAD), 5, device=dev)
+            out = torch.empty_like(q)
+            lens = torch.full((Bd,), n_keep, dtype=torch.int32, device=dev)
+            view = vc.dense_view(ko, vo, lens, n_keep)
+            ws2 = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, 4 * Hd), device=dev)
+            scale = inputs.default_scale(D_HEAD)
+            fn = lambda: vc.vc_draft_attn(q, view, scale, out, ws2)
+            nbytes = 2 * ko.numel() * 2 + 2 * q.numel() * 2
+            rec = {"workload": "decode attention over the compacted cache [4,8,33024,128] bf16, 32/8 heads"}
+    else:
+        raise SystemExit(f"unknown kernel {name}")
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    rec.update({"kernel": name, "ms": ms, "bytes": nbytes, "GB/s": gbs, "hbm_frac": gbs / hbm,
+                "peak_source": peak_src})
+    if flops:
+        rec.update({"flops": flops, "TFLOP/s": flops / (ms / 1e3) / 1e12,
+                    "tc_frac_burst": flops / (ms / 1e3) / 1e12 / tf_burst})
+    print(json.dumps(rec), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -342,10 +440,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernel", default=None,
+                    help="time one kernel alone: draft, verify, accept, quantize, drop, dense_draft")
+    ap.add_argument("--dq", type=int, default=32, help="verify block size for --kernel verify")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.kernel:
+        torch.cuda.set_device(local)
+        from lossless_draft_verify_gb300 import build
+        build.build()
+        run_kernel(args, torch.device("cuda", local))
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     torch.cuda.set_device(local)
@@ -405,20 +513,22 @@ def main():
     overlap = min(1.0, draft_total / statistics.mean(s_ms)) if s_ms else None
 
     # end-to-end: same round with host inputs copied in and results read back
-    for _ in range(2):
-        rnd.step(e2e=True)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        rnd.step(e2e=True)
-    e1.record()
-    barrier()
-    ms_e2e = torch.tensor([e0.elapsed_time(e1)], device=dev)
-    if pg is not None:
-        pg.all_reduce(ms_e2e, op=pg.ReduceOp.MAX)
-    e2e_val = world * tokens * args.steps / (float(ms_e2e.item()) / 1e3)
+    e2e_val = None
+    if not args.no_e2e:
+        for _ in range(2):
+            rnd.step(e2e=True)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            rnd.step(e2e=True)
+        e1.record()
+        barrier()
+        ms_e2e = torch.tensor([e0.elapsed_time(e1)], device=dev)
+        if pg is not None:
+            pg.all_reduce(ms_e2e, op=pg.ReduceOp.MAX)
+        e2e_val = world * tokens * args.steps / (float(ms_e2e.item()) / 1e3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
