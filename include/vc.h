@@ -94,21 +94,29 @@ vc_status vc_poll_status(void *ws, cudaStream_t stream);
  * (sequence, kv head, group), at
  *   records + ((b * Hkv + h) * max_groups + g) * vc_record_bytes(bits, d).
  * A record is [K codes | V codes | K meta | V meta]:
- *   K codes, V codes: group*d*bits/8 bytes each, in the m16n8k16 operand
- *     fragment order of the draft kernel (lane l in [0,32) owns a contiguous
- *     E*bits/8-byte slice, E = group*d/32 codes; code pair p of a lane sits in
- *     32-bit little-endian word p / (16/bits), first code at bit bits*(p %
- *     (16/bits)), second at bit 16 + the same.  Element e = 2p + hh of lane l
- *     is, for K: token 16 mt + l/4 + 8 (r&1), channel 16 ks + 2 (l%4) + hh +
- *     8 (r>>1) with e = ((mt*(d/16) + ks)*4 + r)*2 + hh; for V: channel
- *     16 mt + l/4 + 8 (r&1), token 16 ks + 2 (l%4) + hh + 8 (r>>1) with
- *     e = ((mt*2 + ks)*4 + r)*2 + hh).
- *   K meta (4d bytes): for j in 0..3, a d-byte block holding fp16 pairs
- *     (s[c0], s[c0+1]) at byte j*d + 4*(2 ks + rr), c0 = 16 ks + 2 j + 8 rr,
- *     then the zero pairs at byte j*d + d/2 + 4*(2 ks + rr).
- *   V meta (4d bytes): for j in 0..3, a d-byte block holding fp16 pairs
- *     (s[t0][gc], s[t0+1][gc]) at byte j*d + 4*((2 ks + rr)*(d/32) + gc),
- *     t0 = 16 ks + 2 j + 8 rr, then the zero pairs at byte j*d + d/2 + same.
+ *   Code sections (group*d*bits/8 bytes each).  Lane l in [0,32) of the draft
+ *     kernel owns W = d*bits/32 little-endian 32-bit words; word w of lane l
+ *     sits at byte 16*(32*(w/4) + l) + 4*(w%4) of the section.  A lane's d/2
+ *     code pairs follow the m16n8k16 operand fragments: pair (mt, ks, r)
+ *     holds elements hh = 0, 1 of fragment register r (row = l/4 + 8*(r&1),
+ *     col = 2*(l%4) + hh + 8*(r>>1)):
+ *       K: token 16 mt + row, channel 16 ks + col (mt < 2, ks < d/16),
+ *          class kappa = 2 ks + (r>>1), member mu = 2 mt + (r&1);
+ *       V: channel 16 mt + row, token 16 ks + col (mt < d/16, ks < 2),
+ *          class kappa = 2 mt + (r&1), member mu = 2 ks + (r>>1).
+ *     Pair (kappa, mu) sits in word `word` at slot `slot` (first element at
+ *     bit bits*slot, second at bit 16 + bits*slot):
+ *       2-bit, h = W/2, q = W/4: if kappa < 3h: word = 2 (kappa % h) + mu/2,
+ *         slot = kappa/h + 5 (mu % 2); else k2 = kappa - 3h: word =
+ *         4 (k2 % q) + mu, slot = 3 + k2/q.
+ *       4-bit, h = W/2: word = 2 (kappa % h) + mu/2, slot = kappa/h + 2 (mu % 2).
+ *     (Every class keeps one power-of-two factor through the draft kernel's
+ *     shift-free unpacking; the kernel cancels it per channel.)
+ *   Meta sections (4d bytes each), for lane quad j in [0,4): fp16 pair n of
+ *     quad j at byte 16*(4*(n/4) + j) + 4*(n%4), zero-point pair at the same
+ *     offset + 2d.  K: n = 2 ks + rr holds (s[c0], s[c0+1]), c0 = 16 ks + 2 j +
+ *     8 rr.  V: n = (2 ks + rr)*(d/32) + gc holds (s[t0][gc], s[t0+1][gc]),
+ *     t0 = 16 ks + 2 j + 8 rr.
  * Full-precision tokens (positions n_groups[b]*group .. seq_len[b]-1) live in
  * a ring: position p of (b, h) at k_res/v_res + ((b * Hkv + h) * res_cap +
  * p % res_cap) * d elements.

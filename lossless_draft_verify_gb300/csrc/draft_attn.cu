@@ -85,25 +85,56 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 constexpr uint32_t kMagic = 0x64006400u;   // half2(1024, 1024)
 constexpr uint32_t kOnes = 0x3C003C00u;    // half2(1, 1)
 
-template <int BITS>
-__device__ __forceinline__ uint32_t unpack_pair(const uint32_t *words, int p)
+// ------------------------------------------------------------ KIVI kernel --
+// Position of code pair (kappa, mu) of a lane (record format, include/vc.h)
+// and the power-of-two factor its slot gives the unpacked value:
+// lop3(word >> sh, mask << b*slot, 0x6400) = fp16(1024 + code * 2^(b*e)).
+template <int BITS, int D>
+struct Pairs {
+    static constexpr int W = D * BITS / 32;        // words per lane per section
+    struct Pos {
+        int word, slot, e;
+    };
+    static constexpr Pos pos(int kappa, int mu)
+    {
+        if (BITS == 2) {
+            const int h = W / 2, q = W / 4;
+            if (kappa < 3 * h) return {2 * (kappa % h) + mu / 2, kappa / h + 5 * (mu % 2), kappa / h};
+            const int k2 = kappa - 3 * h;
+            return {4 * (k2 % q) + mu, 3 + k2 / q, 3 + k2 / q};
+        } else {
+            const int h = W / 2;
+            return {2 * (kappa % h) + mu / 2, kappa / h + 2 * (mu % 2), kappa / h};
+        }
+    }
+    // exponent of class kappa: the unpacked code carries a factor 2^(BITS*e)
+    static constexpr int exp_of(int kappa) { return pos(kappa, 0).e; }
+};
+
+// Unpack pair (kappa, mu) from the lane's words w0 (as stored) and w1 (the
+// words shifted right so that the high slots land at the bottom).
+template <int BITS, int D>
+__device__ __forceinline__ uint32_t unpack(const uint32_t *w0, const uint32_t *w1, int kappa, int mu)
 {
-    constexpr int P = 16 / BITS;
-    constexpr uint32_t mask = BITS == 2 ? 0x00030003u : 0x000F000Fu;
-    return lop3_and_or(words[p / P] >> (BITS * (p % P)), mask, kMagic);
+    constexpr uint32_t base = BITS == 2 ? 0x00030003u : 0x000F000Fu;
+    constexpr int split = BITS == 2 ? 5 : 2;       // slots >= split come from the shifted words
+    const auto p = Pairs<BITS, D>::pos(kappa, mu);
+    const uint32_t src = p.slot < split ? w0[p.word] : w1[p.word];
+    const int sl = p.slot < split ? p.slot : p.slot - split;
+    return lop3_and_or(src, base << (BITS * sl), kMagic);
 }
 
-// ------------------------------------------------------------ KIVI kernel --
 template <int BITS, int D>
 struct KiviGeom {
     static constexpr int KS = D / 16;                  // QK k-steps, PV m-tiles
     static constexpr int NG = D / 32;                  // V channel groups
     static constexpr int CODE_BYTES = G * D * BITS / 8;
-    static constexpr int WPL = G * D / 32 * BITS / 32; // code words per lane per section
+    static constexpr int W = D * BITS / 32;            // code words per lane per section
     static constexpr int KM = 2 * CODE_BYTES;          // K meta offset
     static constexpr int VM = KM + 4 * D;              // V meta offset
     static constexpr int REC = VM + 4 * D;             // record bytes
-    static constexpr int NSTAGE = REC <= 3072 ? 4 : 3;
+    static constexpr int SHIFT = BITS == 2 ? 10 : 8;   // high-slot shift
+    static constexpr int NST = 2;                      // ring stages per warp (2 records each)
 };
 
 struct KiviParams {
@@ -147,16 +178,129 @@ __device__ void cta_merge_store(float *wbuf, float *dst, int grp)
     }
 }
 
+// Scores of one group: sc[mt][4] (rows = tokens 16 mt + gid (+8), columns =
+// heads 2 tig + {0,1}) with the zero-point and 1024-offset terms folded in.
+// ksrc: this lane's K-scale pairs (record, or ones for the head copies 4..7);
+// zsrc: this lane's bias-tile row (ones: row 0, K zeros: row 1, zeros: others).
+template <int BITS, int D>
+__device__ __forceinline__ void group_scores(const uint8_t *rec, const uint8_t *ksrc, const uint8_t *zsrc,
+                                             const uint32_t (&qf)[D / 16][2], int lane, int tig,
+                                             float (&sc)[2][4])
+{
+    using Gm = KiviGeom<BITS, D>;
+    constexpr int KS = Gm::KS;
+    uint32_t w0[Gm::W], w1[Gm::W];
+#pragma unroll
+    for (int c = 0; c < Gm::W / 4; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(rec + 16 * (32 * c + lane));
+        w0[4 * c] = u.x; w0[4 * c + 1] = u.y; w0[4 * c + 2] = u.z; w0[4 * c + 3] = u.w;
+    }
+#pragma unroll
+    for (int i = 0; i < Gm::W; ++i) w1[i] = w0[i] >> Gm::SHIFT;
+    float cb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+#pragma unroll
+    for (int c = 0; c < KS / 2; ++c) {
+        // quad tig's pairs n = 4c .. 4c+3, i.e. (ks, rr) = (2c, 0), (2c, 1), (2c+1, 0), (2c+1, 1)
+        const uint4 su = *reinterpret_cast<const uint4 *>(ksrc + 16 * (4 * c + tig));
+        const uint4 zu = *reinterpret_cast<const uint4 *>(zsrc + 16 * (4 * c + tig));
+        const uint32_t sp[4] = {su.x, su.y, su.z, su.w};
+        const uint32_t zp[4] = {zu.x, zu.y, zu.z, zu.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int ks = 2 * c + h;
+            const uint32_t b0 = hmul2(qf[ks][0], sp[2 * h]);
+            const uint32_t b1 = hmul2(qf[ks][1], sp[2 * h + 1]);
+            const uint32_t ab[4] = {zp[2 * h], 0u, zp[2 * h + 1], 0u};
+            mma16816(cb, ab, b0, b1);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                uint32_t a[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a[r] = unpack<BITS, D>(w0, w1, 2 * ks + (r >> 1), 2 * mt + (r & 1));
+                mma16816(sc[mt], a, b0, b1);
+            }
+        }
+    }
+    // row 0 of the bias tile = sum of q' (the 1024 offset), row 1 columns
+    // 4..7 = sum of z * q for heads 0..3
+    const int t1 = tig & 1;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const float sq = __shfl_sync(0xffffffffu, cb[e], t1);
+        const float zq = __shfl_sync(0xffffffffu, cb[e], 6 + t1);
+        const float bias = zq - 1024.f * sq;
+        sc[0][e] += bias;
+        sc[0][e + 2] += bias;
+        sc[1][e] += bias;
+        sc[1][e + 2] += bias;
+    }
+}
+
+// O += V^T p' for one group, plus the zero-point accumulator.
+template <int BITS, int D>
+__device__ __forceinline__ void group_values(const uint8_t *rec, const uint8_t *zvsrc, const uint32_t (&pb)[2][2],
+                                             int lane, int tig, float (&o_acc)[D / 16][4], float (&vb_acc)[4])
+{
+    using Gm = KiviGeom<BITS, D>;
+    constexpr int NG = Gm::NG;
+    uint32_t w0[Gm::W], w1[Gm::W];
+    const uint8_t *vsec = rec + Gm::CODE_BYTES;
+#pragma unroll
+    for (int c = 0; c < Gm::W / 4; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(vsec + 16 * (32 * c + lane));
+        w0[4 * c] = u.x; w0[4 * c + 1] = u.y; w0[4 * c + 2] = u.z; w0[4 * c + 3] = u.w;
+    }
+#pragma unroll
+    for (int i = 0; i < Gm::W; ++i) w1[i] = w0[i] >> Gm::SHIFT;
+    // scale pairs of quad tig: n = (2 ks + rr) * NG + gc
+    uint32_t sv[4 * NG];
+    const uint8_t *vmeta = rec + Gm::VM;
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(vmeta + 16 * (4 * c + tig));
+        sv[4 * c] = u.x; sv[4 * c + 1] = u.y; sv[4 * c + 2] = u.z; sv[4 * c + 3] = u.w;
+    }
+    // zero-point rows gc = lane/4 (< NG): pairs n = (2 ks + rr) * NG + gc
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const int gid = lane >> 2;
+        const int n0 = (2 * ks) * NG + (gid & (NG - 1)), n1 = (2 * ks + 1) * NG + (gid & (NG - 1));
+        const uint32_t z0 = *reinterpret_cast<const uint32_t *>(zvsrc + 16 * (4 * (n0 >> 2) + tig) + 4 * (n0 & 3));
+        const uint32_t z1 = *reinterpret_cast<const uint32_t *>(zvsrc + 16 * (4 * (n1 >> 2) + tig) + 4 * (n1 & 3));
+        const uint32_t az[4] = {z0, 0u, z1, 0u};
+        mma16816(vb_acc, az, pb[ks][0], pb[ks][1]);
+#pragma unroll
+        for (int gc = 0; gc < NG; ++gc) {
+            const uint32_t b0 = hmul2(pb[ks][0], sv[(2 * ks) * NG + gc]);
+            const uint32_t b1 = hmul2(pb[ks][1], sv[(2 * ks + 1) * NG + gc]);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int mt = 2 * gc + half;
+                uint32_t a[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    a[r] = hsub2(unpack<BITS, D>(w0, w1, 2 * mt + (r & 1), 2 * ks + (r >> 1)), kMagic);
+                mma16816(o_acc[mt], a, b0, b1);
+            }
+        }
+    }
+}
+
 template <int BITS, int D, typename TQ, typename TR>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
 draft_kivi_kernel(KiviParams P)
 {
     using Gm = KiviGeom<BITS, D>;
-    constexpr int KS = Gm::KS, NG = Gm::NG, REC = Gm::REC, NST = Gm::NSTAGE;
+    constexpr int KS = Gm::KS, NG = Gm::NG, REC = Gm::REC, NST = Gm::NST;
+    constexpr int STAGE = 2 * REC;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);               // [NW][NST]
-    uint8_t *ring = smem + 128;                                         // [NW][NST][REC]
-    float *wbuf = reinterpret_cast<float *>(smem + 128);                // reused after the loop
+    uint8_t *ones = smem + 128;                                         // 2D bytes of fp16 1.0
+    uint8_t *zeros = ones + 2 * D;                                      // 2D bytes of 0
+    uint8_t *ring = zeros + 2 * D;                                      // [NW][NST][2 records]
+    float *wbuf = reinterpret_cast<float *>(ring);                      // reused after the loop
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
@@ -164,15 +308,12 @@ draft_kivi_kernel(KiviParams P)
     const int b = unit / P.Hkv, kvh = unit % P.Hkv;
     const int grp = P.grp;
     float *dst = P.part + ((size_t)unit * (P.n_split_q + 1) + split) * part_floats(D);
-
-    // per-lane online-softmax state for columns 2*tig, 2*tig+1
-    float m_run[2] = {kNegBig, kNegBig}, l_run[2] = {0.f, 0.f};
-    float o_acc[KS][4];
-#pragma unroll
-    for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
-    float vb_acc[4] = {0.f, 0.f, 0.f, 0.f};
-
     const TQ *qg = reinterpret_cast<const TQ *>(P.q) + ((size_t)b * P.Hq + kvh * grp) * D;
+
+    for (int i = threadIdx.x; i < D / 2; i += kThreads) {
+        reinterpret_cast<uint32_t *>(ones)[i] = kOnes;
+        reinterpret_cast<uint32_t *>(zeros)[i] = 0u;
+    }
 
     if (split < P.n_split_q) {
         // ---------------------------------------------- quantized groups --
@@ -181,8 +322,9 @@ draft_kivi_kernel(KiviParams P)
         const int g_hi = min(ng, g_lo + P.groups_per_split);
         const uint8_t *rec_base = P.records + (size_t)unit * P.max_groups * REC;
         uint64_t *mybar = bars + warp * NST;
-        uint8_t *myring = ring + (size_t)warp * NST * REC;
-        // B fragments of q (columns n = gid; 0..3 real heads, 4..7 copies)
+        uint8_t *myring = ring + (size_t)warp * NST * STAGE;
+        // B fragments of q (column n = gid): heads 0..3 scaled by 2^(-b e) for
+        // the channel's code exponent, copies 4..7 unscaled (zero-point sums)
         uint32_t qf[KS][2];
         {
             const int h = gid & 3;
@@ -192,22 +334,32 @@ draft_kivi_kernel(KiviParams P)
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int c = 16 * ks + 2 * tig + 8 * rr;
-                    float a = valid ? load_q<TQ, D>(qg, h * D + c) * P.qscale : 0.f;
-                    float bb = valid ? load_q<TQ, D>(qg, h * D + c + 1) * P.qscale : 0.f;
+                    const float f = gid < 4 ? exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * ks + rr))) : 1.f;
+                    const float a = valid ? load_q<TQ, D>(qg, h * D + c) * P.qscale * f : 0.f;
+                    const float bb = valid ? load_q<TQ, D>(qg, h * D + c + 1) * P.qscale * f : 0.f;
                     qf[ks][rr] = pack_half2(a, bb);
                 }
         }
         if (lane == 0)
             for (int s = 0; s < NST; ++s) mbar_init(&mybar[s], 1);
         fence_mbar_init();
-        __syncwarp();
-        const int n_mine = g_hi > g_lo + warp ? (g_hi - g_lo - warp + NW - 1) / NW : 0;
+        __syncthreads();
+        const int n_pairs = (g_hi - g_lo + 1) / 2;
+        const int n_mine = n_pairs > warp ? (n_pairs - warp + NW - 1) / NW : 0;
+        auto issue = [&](int s, int it) {
+            const int g = g_lo + 2 * (warp + it * NW);
+            const uint32_t bytes = (g + 1 < g_hi ? 2 : 1) * REC;
+            mbar_arrive_expect_tx(&mybar[s], bytes);
+            bulk_g2s(myring + s * STAGE, rec_base + (size_t)g * REC, bytes, &mybar[s]);
+        };
         if (lane == 0)
-            for (int s = 0; s < NST && s < n_mine; ++s) {
-                const int g = g_lo + warp + s * NW;
-                mbar_arrive_expect_tx(&mybar[s], REC);
-                bulk_g2s(myring + s * REC, rec_base + (size_t)g * REC, REC, &mybar[s]);
-            }
+            for (int s = 0; s < NST && s < n_mine; ++s) issue(s, s);
+
+        float m_run[2] = {kNegBig, kNegBig}, l_run[2] = {0.f, 0.f};
+        float o_acc[KS][4];
+#pragma unroll
+        for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+        float vb_acc[4] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
         for (int it = 0; it < n_mine; ++it) {
             const int st = it % NST;
@@ -216,81 +368,42 @@ draft_kivi_kernel(KiviParams P)
                 ok = false;
                 break;
             }
-            const uint8_t *rec = myring + st * REC;
-            const uint32_t *kmeta = reinterpret_cast<const uint32_t *>(rec + Gm::KM + tig * D);
-            const uint32_t *vmeta = reinterpret_cast<const uint32_t *>(rec + Gm::VM + tig * D);
-
-            // ---- scores: S = codes * q' (+ zero/offset bias) ----------------
-            float cb[4] = {0.f, 0.f, 0.f, 0.f};
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const int g = g_lo + 2 * (warp + it * NW);
+            const bool two = g + 1 < g_hi;
+            const uint8_t *recA = myring + st * STAGE;
+            const uint8_t *recB = recA + REC;
+            // ---- scores of both groups
+            float sc[2][2][4];
             {
-                uint32_t kw[Gm::WPL];
-                const uint4 *src = reinterpret_cast<const uint4 *>(rec) + lane * (Gm::WPL / 4);
-#pragma unroll
-                for (int i = 0; i < Gm::WPL / 4; ++i) {
-                    uint4 u = src[i];
-                    kw[4 * i] = u.x; kw[4 * i + 1] = u.y; kw[4 * i + 2] = u.z; kw[4 * i + 3] = u.w;
-                }
-                uint32_t ks_pair[2 * KS], kz_pair[2 * KS];
-#pragma unroll
-                for (int i = 0; i < 2 * KS; i += 4) {
-                    uint4 u = *reinterpret_cast<const uint4 *>(kmeta + i);
-                    ks_pair[i] = u.x; ks_pair[i + 1] = u.y; ks_pair[i + 2] = u.z; ks_pair[i + 3] = u.w;
-                    uint4 z = *reinterpret_cast<const uint4 *>(kmeta + D / 8 + i);
-                    kz_pair[i] = z.x; kz_pair[i + 1] = z.y; kz_pair[i + 2] = z.z; kz_pair[i + 3] = z.w;
-                }
-#pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    uint32_t bq[2];
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr)
-                        bq[rr] = gid < 4 ? hmul2(qf[ks][rr], ks_pair[2 * ks + rr]) : qf[ks][rr];
-                    // bias rows: row 0 = ones (sum of q'), row 1 = z (sum of z*q)
-                    uint32_t ab[4];
-                    ab[0] = gid == 0 ? kOnes : (gid == 1 ? kz_pair[2 * ks] : 0u);
-                    ab[1] = 0u;
-                    ab[2] = gid == 0 ? kOnes : (gid == 1 ? kz_pair[2 * ks + 1] : 0u);
-                    ab[3] = 0u;
-                    mma16816(cb, ab, bq[0], bq[1]);
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        uint32_t a[4];
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) a[r] = unpack_pair<BITS>(kw, (mt * KS + ks) * 4 + r);
-                        mma16816(sc[mt], a, bq[0], bq[1]);
-                    }
-                }
+                const uint8_t *ks_src = gid < 4 ? recA + Gm::KM : ones;
+                const uint8_t *z_src = gid == 0 ? ones : (gid == 1 ? recA + Gm::KM + 2 * D : zeros);
+                group_scores<BITS, D>(recA, ks_src, z_src, qf, lane, tig, sc[0]);
             }
-            // bias for columns 2*tig + e (valid for tig < 2)
-            float bias[2];
-            {
-                const int t1 = tig & 1;
+            if (two) {
+                const uint8_t *ks_src = gid < 4 ? recB + Gm::KM : ones;
+                const uint8_t *z_src = gid == 0 ? ones : (gid == 1 ? recB + Gm::KM + 2 * D : zeros);
+                group_scores<BITS, D>(recB, ks_src, z_src, qf, lane, tig, sc[1]);
+            } else {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float sq = __shfl_sync(0xffffffffu, cb[e], t1);
-                    const float zq = __shfl_sync(0xffffffffu, cb[e], 6 + t1);
-                    bias[e] = zq - 1024.f * sq;
-                }
+                for (int mt = 0; mt < 2; ++mt) sc[1][mt][0] = sc[1][mt][1] = sc[1][mt][2] = sc[1][mt][3] = kNegBig;
             }
-            // ---- online softmax (exp2 domain) ---------------------------------
+            // ---- online softmax over the 64 tokens (exp2 domain, lazy rescale)
             float gmax[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                // padding columns (head >= grp, or 4..7) are pinned to a finite
-                // floor so they never trigger a rescale and stay finite
-                if (2 * tig + e >= grp) {
-                    sc[0][e] = sc[0][e + 2] = sc[1][e] = sc[1][e + 2] = kNegBig;
-                    bias[e] = 0.f;
+                float mx = kNegBig;
+                if (2 * tig + e < grp) {
+#pragma unroll
+                    for (int G2 = 0; G2 < 2; ++G2)
+#pragma unroll
+                        for (int mt = 0; mt < 2; ++mt) mx = fmaxf(mx, fmaxf(sc[G2][mt][e], sc[G2][mt][e + 2]));
+                } else {
+                    // padding columns (head >= grp, or 4..7) stay at a finite floor
+#pragma unroll
+                    for (int G2 = 0; G2 < 2; ++G2)
+#pragma unroll
+                        for (int mt = 0; mt < 2; ++mt) sc[G2][mt][e] = sc[G2][mt][e + 2] = kNegBig;
                 }
-                float x = sc[0][e] + bias[e];
-                sc[0][e] = x;
-                float y = sc[0][e + 2] + bias[e];
-                sc[0][e + 2] = y;
-                float z = sc[1][e] + bias[e];
-                sc[1][e] = z;
-                float w = sc[1][e + 2] + bias[e];
-                sc[1][e + 2] = w;
-                float mx = fmaxf(fmaxf(x, y), fmaxf(z, w));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -313,78 +426,35 @@ draft_kivi_kernel(KiviParams P)
                 }
                 l_run[0] *= alpha[0];
                 l_run[1] *= alpha[1];
-                // zero-point accumulator columns 4+h live on lanes tig = 2 + h/2
-                const float a0 = __shfl_sync(0xffffffffu, alpha[0], lane ^ 2);
-                const float a1 = __shfl_sync(0xffffffffu, alpha[1], lane ^ 2);
-                vb_acc[0] *= a0;
-                vb_acc[1] *= a1;
-                vb_acc[2] *= a0;
-                vb_acc[3] *= a1;
+                vb_acc[0] *= alpha[0];
+                vb_acc[1] *= alpha[1];
+                vb_acc[2] *= alpha[0];
+                vb_acc[3] *= alpha[1];
             }
-            uint32_t pb[2][2];          // B fragments of P^T per token half (ks) and k half
+            uint32_t pb[2][2][2];      // [group][token half][k half]
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                float p[4];
+            for (int G2 = 0; G2 < 2; ++G2)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) p[i] = exp2f(sc[mt][i] - m_run[i & 1]);
-                l_run[0] += p[0] + p[2];
-                l_run[1] += p[1] + p[3];
-                pb[mt][0] = movmatrix_trans(pack_half2(p[0], p[1]));
-                pb[mt][1] = movmatrix_trans(pack_half2(p[2], p[3]));
-                // columns 4..7 carry the unscaled p of heads 0..3
-                pb[mt][0] = __shfl_sync(0xffffffffu, pb[mt][0], lane & 15);
-                pb[mt][1] = __shfl_sync(0xffffffffu, pb[mt][1], lane & 15);
-            }
-            // ---- values: O += codes^T * p' (+ zero-point bias) ---------------
+                for (int mt = 0; mt < 2; ++mt) {
+                    float p[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) p[i] = exp2f(sc[G2][mt][i] - m_run[i & 1]);
+                    l_run[0] += p[0] + p[2];
+                    l_run[1] += p[1] + p[3];
+                    pb[G2][mt][0] = movmatrix_trans(pack_half2(p[0], p[1]));
+                    pb[G2][mt][1] = movmatrix_trans(pack_half2(p[2], p[3]));
+                }
+            // ---- values of both groups
             {
-                uint32_t vw[Gm::WPL];
-                const uint4 *src = reinterpret_cast<const uint4 *>(rec + Gm::CODE_BYTES) + lane * (Gm::WPL / 4);
-#pragma unroll
-                for (int i = 0; i < Gm::WPL / 4; ++i) {
-                    uint4 u = src[i];
-                    vw[4 * i] = u.x; vw[4 * i + 1] = u.y; vw[4 * i + 2] = u.z; vw[4 * i + 3] = u.w;
-                }
-                uint32_t sv[2][2][NG];
-#pragma unroll
-                for (int i = 0; i < 4 * NG; i += 4) {
-                    uint4 u = *reinterpret_cast<const uint4 *>(vmeta + i);
-                    uint32_t *f = &sv[0][0][0];
-                    f[i] = u.x; f[i + 1] = u.y; f[i + 2] = u.z; f[i + 3] = u.w;
-                }
-                // zero-point rows gc = gid (< NG): pairs (ks, rr) of channel group gid
-                uint32_t zv[2][2];
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr)
-                        zv[ks][rr] = gid < NG ? vmeta[D / 8 + (2 * ks + rr) * NG + gid] : 0u;
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    uint32_t az[4] = {zv[ks][0], 0u, zv[ks][1], 0u};
-                    mma16816(vb_acc, az, pb[ks][0], pb[ks][1]);
-#pragma unroll
-                    for (int gc = 0; gc < NG; ++gc) {
-                        const uint32_t b0 = gid < 4 ? hmul2(pb[ks][0], sv[ks][0][gc]) : pb[ks][0];
-                        const uint32_t b1 = gid < 4 ? hmul2(pb[ks][1], sv[ks][1][gc]) : pb[ks][1];
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const int mt = 2 * gc + half;
-                            uint32_t a[4];
-#pragma unroll
-                            for (int r = 0; r < 4; ++r)
-                                a[r] = hsub2(unpack_pair<BITS>(vw, (mt * 2 + ks) * 4 + r), kMagic);
-                            mma16816(o_acc[mt], a, b0, b1);
-                        }
-                    }
-                }
+                const uint8_t *zv_src = gid < NG ? recA + Gm::VM + 2 * D : zeros;
+                group_values<BITS, D>(recA, zv_src, pb[0], lane, tig, o_acc, vb_acc);
+            }
+            if (two) {
+                const uint8_t *zv_src = gid < NG ? recB + Gm::VM + 2 * D : zeros;
+                group_values<BITS, D>(recB, zv_src, pb[1], lane, tig, o_acc, vb_acc);
             }
             __syncwarp();
-            // refill this stage with the group NST iterations ahead
-            if (lane == 0 && it + NST < n_mine) {
-                const int g = g_lo + warp + (it + NST) * NW;
-                mbar_arrive_expect_tx(&mybar[st], REC);
-                bulk_g2s(myring + st * REC, rec_base + (size_t)g * REC, REC, &mybar[st]);
-            }
+            if (lane == 0 && it + NST < n_mine) issue(st, it + NST);
         }
         if (!ok) {
             // a bounded wait gave up: drop this warp's contribution
@@ -394,20 +464,20 @@ draft_kivi_kernel(KiviParams P)
             for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
             vb_acc[0] = vb_acc[1] = vb_acc[2] = vb_acc[3] = 0.f;
         }
-        // finish per-warp state: reduce l over lanes sharing a column
+        // lanes sharing a column hold partial row sums: reduce
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 4);
             l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 8);
             l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 16);
         }
-        // zero-point contribution of channel group gc for heads 2*tig+e
+        // zero-point contribution of channel group gc for heads 2 tig + e
+        // (row gc of the zero-point accumulator lives on lanes 4 gc + tig)
         float vbias[NG][2];
 #pragma unroll
         for (int gc = 0; gc < NG; ++gc)
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-                vbias[gc][e] = __shfl_sync(0xffffffffu, vb_acc[e], gc * 4 + (tig & 1) + 2);
+            for (int e = 0; e < 2; ++e) vbias[gc][e] = __shfl_sync(0xffffffffu, vb_acc[e], gc * 4 + tig);
         __syncthreads();   // every warp done with its ring before wbuf reuse
         float *wm = wbuf, *wl = wbuf + NW * 4, *wo = wbuf + NW * 8;
         if (tig < 2) {
@@ -420,9 +490,12 @@ draft_kivi_kernel(KiviParams P)
                 }
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
+                    // rows 16 mt + gid (+8): undo the code factor 2^(b e) of their class
+                    const float f0 = exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt)));
+                    const float f1 = exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt + 1)));
                     const int c0 = 16 * mt + gid;
-                    wo[(warp * 4 + h) * D + c0] = o_acc[mt][e] + vbias[mt / 2][e];
-                    wo[(warp * 4 + h) * D + c0 + 8] = o_acc[mt][e + 2] + vbias[mt / 2][e];
+                    wo[(warp * 4 + h) * D + c0] = o_acc[mt][e] * f0 + vbias[mt / 2][e];
+                    wo[(warp * 4 + h) * D + c0 + 8] = o_acc[mt][e + 2] * f1 + vbias[mt / 2][e];
                 }
             }
         }
@@ -471,6 +544,7 @@ draft_kivi_kernel(KiviParams P)
                 for (int i = 0; i < CPL; ++i) o[h][i] = o[h][i] * a + p * vx[i];
             }
         }
+        __syncthreads();
         float *wm = wbuf, *wl = wbuf + NW * 4, *wo = wbuf + NW * 8;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -684,13 +758,15 @@ KiviPlan kivi_plan(const vc_qcache *c)
 {
     const int units = c->B * c->Hkv;
     const int ng = c->max_groups;
-    const int target_ctas = num_sms() * 3 * 2;
-    int s = (target_ctas + units - 1) / units;
+    // about four waves of 4 resident CTAs per SM, counting the residual split
+    const int target_ctas = num_sms() * 4 * 4;
+    int s = (target_ctas + units - 1) / units - 1;
     s = s < 1 ? 1 : s;
-    const int max_s = (ng + NW * 2 - 1) / (NW * 2);    // keep >= 2 groups per warp
+    const int max_s = (ng + NW * 4 - 1) / (NW * 4);    // keep >= 2 group pairs per warp
     if (s > max_s) s = max_s > 0 ? max_s : 1;
     KiviPlan p;
-    p.groups_per_split = ng > 0 ? (ng + s - 1) / s : 1;
+    p.groups_per_split = ng > 0 ? (ng + s - 1) / s : 2;
+    p.groups_per_split += p.groups_per_split & 1;       // whole pairs
     p.n_split_q = ng > 0 ? (ng + p.groups_per_split - 1) / p.groups_per_split : 0;
     return p;
 }
@@ -737,9 +813,9 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     P.n_split_q = pl.n_split_q;
     P.groups_per_split = pl.groups_per_split;
     P.qscale = scale * kLog2e;
-    size_t smem = 128 + (size_t)NW * Gm::NSTAGE * Gm::REC;
-    const size_t merge = (size_t)NW * part_floats(D) * 4;
-    if (smem < 128 + merge) smem = 128 + merge;
+    size_t smem = 128 + 4 * D + (size_t)NW * Gm::NST * 2 * Gm::REC;
+    const size_t merge = 128 + 4 * D + (size_t)NW * part_floats(D) * 4;
+    if (smem < merge) smem = merge;
     auto kern = draft_kivi_kernel<BITS, D, TQ, TR>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(pl.n_split_q + 1, c->B * c->Hkv);

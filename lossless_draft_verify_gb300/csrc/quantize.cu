@@ -2,21 +2,26 @@
 // (KIVI: a compressor named on the VeriCache paper page, "What the paper
 // found"; ref [42] on pith.science).  K per channel over groups of 32 tokens,
 // V per token over groups of 32 channels, fp16 scale and zero-point per group,
-// packed into the record layout the draft kernel consumes (see include/vc.h).
+// packed into the record layout the draft kernel consumes (include/vc.h).
 //
-// One 128-thread CTA quantizes one (sequence, kv head, token group): the two
-// 32 x d tiles are staged in shared memory as fp32, each K channel / V
-// (token, channel-group) is reduced by one thread, and the record is written
-// with coalesced 32-bit stores.  The operation is HBM-bound (it reads the
-// bf16 tiles once and writes ~3/16 of that), with no tensor-core work.
+// One CTA of 2*d threads quantizes one (sequence, kv head, token group):
+// threads [0, d) own one K channel each (32 tokens), threads [d, 2d) own one
+// V (token, channel group) each.  Every thread reads its 32 inputs straight
+// from global memory, reduces min/max, derives the directed-rounded fp16
+// meta, computes the codes and ORs them into the record image in shared
+// memory at their fragment-order position; the image is then written with
+// 128-bit stores.  The quotient (x - z)/s is evaluated with the group's
+// reciprocal and recomputed with an exact IEEE division whenever it lies
+// within rounding distance of a half-integer, so the codes are those of the
+// correctly rounded quotient.  HBM-bound: reads 2*32*d*2 bytes, writes one
+// record per group.
 #include "vc_common.cuh"
 #include "vc_internal.h"
 
 namespace vc {
 namespace {
 
-constexpr int G = 32;            // group size (tokens for K, channels for V)
-constexpr int kThreads = 128;
+constexpr int G = 32;
 
 // Directed-rounding quantization parameters of one group (see include/vc.h).
 __device__ __forceinline__ void group_params(float mn, float mx, int qmax, uint16_t &sb,
@@ -32,177 +37,176 @@ __device__ __forceinline__ void group_params(float mn, float mx, int qmax, uint1
     zb = __half_as_ushort(z);
 }
 
-__device__ __forceinline__ uint32_t group_code(float x, float sf, float zf, int qmax)
+// code = clamp(rint(RN(RN(x - z) / s)), 0, qmax); rs = RN(1/s).  d * rs is
+// within a few ulp of RN(d / s) (q <= 15), so away from a half-integer both
+// round to the same integer; near one the exact quotient decides.
+__device__ __forceinline__ uint32_t group_code(float x, float sf, float zf, float rs, int qmax)
 {
     if (sf == 0.0f) return 0u;
-    float r = rintf(__fdiv_rn(__fadd_rn(x, -zf), sf));
+    const float d = __fadd_rn(x, -zf);
+    float q = d * rs;
+    const float fr = q - floorf(q);
+    if (fabsf(fr - 0.5f) < 1e-5f) q = __fdiv_rn(d, sf);
+    float r = rintf(q);
     r = fminf(fmaxf(r, 0.0f), (float)qmax);
     return (uint32_t)r;
 }
 
-template <int D>
-struct QSmem {
-    float k[G][D + 1];
-    float v[G][D + 1];
-    uint8_t kc[G][D];
-    uint8_t vc[G][D];
-    uint16_t ks[D], kz[D];
-    uint16_t vs[G][D / G], vz[G][D / G];
+// Position of code pair (kappa, mu) inside a lane's words (see include/vc.h).
+template <int BITS, int D>
+__device__ __forceinline__ void pair_pos(int kappa, int mu, int &word, int &slot)
+{
+    constexpr int W = D * BITS / 32;
+    if (BITS == 2) {
+        constexpr int h = W / 2, q = W / 4;
+        if (kappa < 3 * h) {
+            word = 2 * (kappa % h) + mu / 2;
+            slot = kappa / h + 5 * (mu % 2);
+        } else {
+            const int k2 = kappa - 3 * h;
+            word = 4 * (k2 % q) + mu;
+            slot = 3 + k2 / q;
+        }
+    } else {
+        constexpr int h = W / 2;
+        word = 2 * (kappa % h) + mu / 2;
+        slot = kappa / h + 2 * (mu % 2);
+    }
+}
+
+// byte offset of word w of lane l in a code section
+__device__ __forceinline__ int word_byte(int lane, int w) { return 16 * (32 * (w >> 2) + lane) + 4 * (w & 3); }
+
+template <int BITS, int D>
+struct RecGeom {
+    static constexpr int CODE = G * D * BITS / 8;   // bytes per code section
+    static constexpr int KM = 2 * CODE;
+    static constexpr int VM = KM + 4 * D;
+    static constexpr int REC = VM + 4 * D;
 };
 
-// Quantize the staged tiles and write one record.  All threads participate.
-template <int BITS, int D>
-__device__ void quantize_staged_group(QSmem<D> &sm, uint8_t *__restrict__ rec)
+// Quantize one group whose token rows are row(t) (t in [0, 32)); threads
+// [0, D) must be given K rows and threads [D, 2D) V rows.  Writes `rec`.
+// blockDim.x == 2 * D; img is a shared record image.
+template <typename T, int BITS, int D, typename RowFn>
+__device__ void quantize_group(RowFn row, uint8_t *__restrict__ rec, uint32_t *img)
 {
+    using Gm = RecGeom<BITS, D>;
     constexpr int qmax = (1 << BITS) - 1;
     constexpr int NG = D / G;
     const int tid = threadIdx.x;
-    // K: one thread per channel, over the 32 tokens of the group.
-    if (tid < D) {
-        const int c = tid;
-        float mn = sm.k[0][c], mx = mn;
-#pragma unroll 8
-        for (int t = 1; t < G; ++t) {
-            float x = sm.k[t][c];
-            mn = fminf(mn, x);
-            mx = fmaxf(mx, x);
-        }
-        uint16_t sb, zb;
-        float sf, zf;
-        group_params(mn, mx, qmax, sb, zb, sf, zf);
-        sm.ks[c] = sb;
-        sm.kz[c] = zb;
-#pragma unroll 8
-        for (int t = 0; t < G; ++t) sm.kc[t][c] = (uint8_t)group_code(sm.k[t][c], sf, zf, qmax);
-    }
-    // V: one thread per (token, channel group); warp = channel group, lane = token.
-    if (tid < G * NG) {
-        const int t = tid % G, gc = tid / G;
-        float mn = sm.v[t][gc * G], mx = mn;
-#pragma unroll 8
-        for (int i = 1; i < G; ++i) {
-            float x = sm.v[t][gc * G + i];
-            mn = fminf(mn, x);
-            mx = fmaxf(mx, x);
-        }
-        uint16_t sb, zb;
-        float sf, zf;
-        group_params(mn, mx, qmax, sb, zb, sf, zf);
-        sm.vs[t][gc] = sb;
-        sm.vz[t][gc] = zb;
-#pragma unroll 8
-        for (int i = 0; i < G; ++i)
-            sm.vc[t][gc * G + i] = (uint8_t)group_code(sm.v[t][gc * G + i], sf, zf, qmax);
-    }
+    uint8_t *bimg = reinterpret_cast<uint8_t *>(img);
+    for (int i = tid; i < Gm::REC / 4; i += 2 * D) img[i] = 0u;
     __syncthreads();
-
-    // Pack codes in fragment order.
-    constexpr int E = G * D / 32;                 // codes per lane
-    constexpr int WPL = E * BITS / 32;            // 32-bit words per lane
-    constexpr int P = 16 / BITS;                  // code pairs per word
-    constexpr int KS = D / 16;
-    constexpr int WORDS = 32 * WPL;               // words per code section
-    uint32_t *kcw = reinterpret_cast<uint32_t *>(rec);
-    uint32_t *vcw = kcw + WORDS;
-    for (int wi = tid; wi < WORDS; wi += kThreads) {
-        const int lane = wi / WPL, w = wi % WPL;
-        const int gid = lane >> 2, tig = lane & 3;
-        uint32_t kword = 0, vword = 0;
+    if (tid < D) {
+        // ---- K: channel c over the group's 32 tokens
+        const int c = tid;
+        float x[G];
 #pragma unroll
-        for (int j = 0; j < P; ++j) {
-            const int p = w * P + j;
-            const int r = p & 3, blk = p >> 2;
+        for (int t = 0; t < G; ++t) x[t] = Elem<T>::to_f(row(t)[c]);
+        float mn = x[0], mx = x[0];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int shift = BITS * j + 16 * hh;
-                {   // K: blk = mt * KS + ks
-                    const int mt = blk / KS, ks = blk % KS;
-                    const int t = 16 * mt + gid + 8 * (r & 1);
-                    const int c = 16 * ks + 2 * tig + hh + 8 * (r >> 1);
-                    kword |= (uint32_t)sm.kc[t][c] << shift;
-                }
-                {   // V: blk = mt * 2 + ks
-                    const int mt = blk >> 1, ks = blk & 1;
-                    const int c = 16 * mt + gid + 8 * (r & 1);
-                    const int t = 16 * ks + 2 * tig + hh + 8 * (r >> 1);
-                    vword |= (uint32_t)sm.vc[t][c] << shift;
-                }
-            }
+        for (int t = 1; t < G; ++t) {
+            mn = fminf(mn, x[t]);
+            mx = fmaxf(mx, x[t]);
         }
-        kcw[wi] = kword;
-        vcw[wi] = vword;
-    }
-    // Meta sections: 4 blocks of D bytes each = D words per section.
-    uint32_t *kmw = vcw + WORDS;
-    uint32_t *vmw = kmw + D;
-    for (int wi = tid; wi < D; wi += kThreads) {
-        const int j = (4 * wi) / D, o = 4 * wi - j * D;
-        const bool zero = o >= D / 2;
-        const int q = (zero ? o - D / 2 : o) / 4;
-        {   // K meta: q = 2 ks + rr
-            const int ks = q >> 1, rr = q & 1;
-            const int c0 = 16 * ks + 2 * j + 8 * rr;
-            const uint16_t *src = zero ? sm.kz : sm.ks;
-            kmw[wi] = (uint32_t)src[c0] | ((uint32_t)src[c0 + 1] << 16);
+        uint16_t sb, zb;
+        float sf, zf;
+        group_params(mn, mx, qmax, sb, zb, sf, zf);
+        const float rs = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
+        const int ks = c >> 4, col = c & 15;
+        const int tig = (col & 7) >> 1, hh = col & 1, rh = col >> 3;
+        const int kappa = 2 * ks + rh;
+#pragma unroll
+        for (int t = 0; t < G; ++t) {
+            const uint32_t code = group_code(x[t], sf, zf, rs, qmax);
+            const int mt = t >> 4, rowt = t & 15;
+            const int gid = rowt & 7, rb = rowt >> 3;
+            int w, s;
+            pair_pos<BITS, D>(kappa, 2 * mt + rb, w, s);
+            if (code)
+                atomicOr(reinterpret_cast<uint32_t *>(bimg + word_byte(gid * 4 + tig, w)),
+                         code << (BITS * s + 16 * hh));
         }
-        {   // V meta: q = (2 ks + rr) * NG + gc
-            const int gc = q % NG, kr = q / NG;
-            const int ks = kr >> 1, rr = kr & 1;
-            const int t0 = 16 * ks + 2 * j + 8 * rr;
-            const uint16_t(*src)[NG] = zero ? sm.vz : sm.vs;
-            vmw[wi] = (uint32_t)src[t0][gc] | ((uint32_t)src[t0 + 1][gc] << 16);
-        }
-    }
-}
-
-// Stage rows row0..row0+31 of a [rows][D] tensor (element type T) as fp32.
-template <typename T, int D>
-__device__ __forceinline__ void stage_tile(float (*dst)[D + 1], const T *__restrict__ src)
-{
-    constexpr int PER16 = 16 / sizeof(T);
-    constexpr int CHUNKS = G * D / PER16;
-    for (int i = threadIdx.x; i < CHUNKS; i += kThreads) {
-        const int t = i / (D / PER16), c0 = (i % (D / PER16)) * PER16;
-        uint4 u = ldg_stream(src + (size_t)t * D + c0);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        // meta: pair n = 2 ks + rr of quad j, half (c & 1)
+        const int j = tig, n = 2 * ks + rh;
+        const int off = Gm::KM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (c & 1);
+        *reinterpret_cast<uint16_t *>(bimg + off) = sb;
+        *reinterpret_cast<uint16_t *>(bimg + off + 2 * D) = zb;
+    } else if (tid < 2 * D) {
+        // ---- V: token t over channel group gc
+        const int i = tid - D;
+        const int t = i % G, gc = i / G;
+        float x[G];
+        const T *src = row(t) + gc * G;
         if constexpr (sizeof(T) == 2) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                dst[t][c0 + 2 * e] = bf16_lo(w[e]);
-                dst[t][c0 + 2 * e + 1] = bf16_hi(w[e]);
+            for (int e = 0; e < G; e += 8) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(src + e);
+                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    x[e + 2 * k] = bf16_lo(wv[k]);
+                    x[e + 2 * k + 1] = bf16_hi(wv[k]);
+                }
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[t][c0 + e] = __uint_as_float(w[e]);
+            for (int e = 0; e < G; e += 4) {
+                const float4 u = *reinterpret_cast<const float4 *>(src + e);
+                x[e] = u.x; x[e + 1] = u.y; x[e + 2] = u.z; x[e + 3] = u.w;
+            }
         }
+        float mn = x[0], mx = x[0];
+#pragma unroll
+        for (int e = 1; e < G; ++e) {
+            mn = fminf(mn, x[e]);
+            mx = fmaxf(mx, x[e]);
+        }
+        uint16_t sb, zb;
+        float sf, zf;
+        group_params(mn, mx, qmax, sb, zb, sf, zf);
+        const float rs = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
+        const int ks = t >> 4, colt = t & 15;
+        const int tig = (colt & 7) >> 1, hh = colt & 1, rh = colt >> 3;
+        const int mu = 2 * ks + rh;
+        uint8_t *vsec = bimg + Gm::CODE;
+#pragma unroll
+        for (int e = 0; e < G; ++e) {
+            const uint32_t code = group_code(x[e], sf, zf, rs, qmax);
+            const int c = gc * G + e;
+            const int mt = c >> 4, rowc = c & 15;
+            const int gid = rowc & 7, rb = rowc >> 3;
+            int w, s;
+            pair_pos<BITS, D>(2 * mt + rb, mu, w, s);
+            if (code)
+                atomicOr(reinterpret_cast<uint32_t *>(vsec + word_byte(gid * 4 + tig, w)),
+                         code << (BITS * s + 16 * hh));
+        }
+        const int j = tig, n = (2 * ks + rh) * NG + gc;
+        const int off = Gm::VM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (t & 1);
+        *reinterpret_cast<uint16_t *>(bimg + off) = sb;
+        *reinterpret_cast<uint16_t *>(bimg + off + 2 * D) = zb;
     }
-}
-
-// Stage ring positions pos0..pos0+31 of (b, h) as fp32.
-template <typename T, int D>
-__device__ __forceinline__ void stage_ring_tile(float (*dst)[D + 1], const T *__restrict__ ring,
-                                                long pos0, int res_cap)
-{
-    for (int i = threadIdx.x; i < G * D; i += kThreads) {
-        const int t = i / D, c = i % D;
-        dst[t][c] = Elem<T>::to_f(ring[(size_t)((pos0 + t) % res_cap) * D + c]);
-    }
+    __syncthreads();
+    uint4 *dst = reinterpret_cast<uint4 *>(rec);
+    const uint4 *srcv = reinterpret_cast<const uint4 *>(img);
+    for (int i = tid; i < Gm::REC / 16; i += 2 * D) dst[i] = srcv[i];
 }
 
 template <typename T, int BITS, int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(2 * D)
 quantize_prefill_kernel(const T *__restrict__ k, const T *__restrict__ v, int Hkv, int L_stride,
-                        int max_groups, uint8_t *__restrict__ records, size_t rec_bytes)
+                        int max_groups, uint8_t *__restrict__ records)
 {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    QSmem<D> &sm = *reinterpret_cast<QSmem<D> *>(smem_raw);
+    using Gm = RecGeom<BITS, D>;
+    __shared__ __align__(16) uint32_t img[Gm::REC / 4];
     const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const size_t bh = (size_t)b * Hkv + h;
     const size_t row0 = bh * L_stride + (size_t)g * G;
-    stage_tile<T, D>(sm.k, k + row0 * D);
-    stage_tile<T, D>(sm.v, v + row0 * D);
-    __syncthreads();
-    quantize_staged_group<BITS, D>(sm, records + (bh * max_groups + g) * rec_bytes);
+    const T *base = threadIdx.x < D ? k : v;
+    auto row = [&](int t) { return base + (row0 + t) * D; };
+    quantize_group<T, BITS, D>(row, records + (bh * max_groups + g) * Gm::REC, img);
 }
 
 // Copy positions n_q*G .. L-1 into the ring and publish the lengths.
@@ -231,21 +235,20 @@ __global__ void residual_copy_kernel(const T *__restrict__ k, const T *__restric
 // Append new tokens into the ring, then quantize every complete group that
 // left the residual window.  One CTA per sequence handles all its kv heads, so
 // the lengths of sequence b are read and written by exactly one CTA.
+// Commit mode (len_base, n_acc non-null): roll back to len_base[b] and take
+// n_acc[b] + 1 rows.
 template <typename T, int BITS, int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(2 * D)
 append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
               const int32_t *__restrict__ n_new, const int32_t *__restrict__ len_base,
               const int32_t *__restrict__ n_acc, int max_new, int Hkv, T *kres, T *vres,
               int res_cap, int residual, int requantize, int max_groups,
-              uint8_t *__restrict__ records, size_t rec_bytes, int32_t *n_groups,
-              int32_t *seq_len, int32_t *status)
+              uint8_t *__restrict__ records, int32_t *n_groups, int32_t *seq_len, int32_t *status)
 {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    QSmem<D> &sm = *reinterpret_cast<QSmem<D> *>(smem_raw);
+    using Gm = RecGeom<BITS, D>;
+    __shared__ __align__(16) uint32_t img[Gm::REC / 4];
     const int b = blockIdx.x;
     const int ng0 = n_groups[b];
-    // commit mode: roll back to the round-start length, then take the n_acc + 1
-    // verified tokens; never below the quantized prefix
     int len0 = len_base ? len_base[b] : seq_len[b];
     if (len0 < ng0 * G) {
         if (threadIdx.x == 0 && status) atomicOr(status, 2);
@@ -253,7 +256,7 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
     }
     int nn = n_acc ? n_acc[b] + 1 : n_new[b];
     nn = nn < 0 ? 0 : (nn > max_new ? max_new : nn);
-    // Unquantized tokens after the append must fit the ring.
+    // unquantized tokens after the append must fit the ring
     const int room = res_cap - (len0 - ng0 * G);
     if (nn > room) {
         if (threadIdx.x == 0 && status) atomicOr(status, 1);
@@ -266,7 +269,7 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
     }
     for (int h = 0; h < Hkv; ++h) {
         const size_t bh = (size_t)b * Hkv + h;
-        for (int i = threadIdx.x; i < nn * D; i += kThreads) {
+        for (int i = threadIdx.x; i < nn * D; i += 2 * D) {
             const int t = i / D, c = i % D;
             const size_t src = ((bh * max_new) + t) * D + c;
             const size_t dst = (bh * res_cap + (size_t)((len0 + t) % res_cap)) * D + c;
@@ -275,10 +278,11 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
         }
         __syncthreads();
         for (int g = ng0; g < ng1; ++g) {
-            stage_ring_tile<T, D>(sm.k, kres + bh * res_cap * D, (long)g * G, res_cap);
-            stage_ring_tile<T, D>(sm.v, vres + bh * res_cap * D, (long)g * G, res_cap);
-            __syncthreads();
-            quantize_staged_group<BITS, D>(sm, records + (bh * max_groups + g) * rec_bytes);
+            const T *ring = threadIdx.x < D ? kres : vres;
+            auto row = [&](int t) {
+                return ring + (bh * res_cap + (size_t)(((long)g * G + t) % res_cap)) * D;
+            };
+            quantize_group<T, BITS, D>(row, records + (bh * max_groups + g) * Gm::REC, img);
             __syncthreads();
         }
     }
@@ -294,14 +298,10 @@ cudaError_t launch_prefill(const void *k, const void *v, int B, int Hkv, int L, 
 {
     const int R = c->cfg.residual;
     const int nq = (L - R > 0) ? ((L - R) / G) * G : 0;
-    const size_t rb = vc_record_bytes(BITS, D);
-    const size_t smem = sizeof(QSmem<D>);
-    auto kern = quantize_prefill_kernel<T, BITS, D>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (nq > 0) {
         dim3 grid(nq / G, Hkv, B);
-        kern<<<grid, kThreads, smem, st>>>((const T *)k, (const T *)v, Hkv, L_stride,
-                                           c->max_groups, (uint8_t *)c->records, rb);
+        quantize_prefill_kernel<T, BITS, D><<<grid, 2 * D, 0, st>>>(
+            (const T *)k, (const T *)v, Hkv, L_stride, c->max_groups, (uint8_t *)c->records);
     }
     residual_copy_kernel<T, D><<<B * Hkv, 256, 0, st>>>(
         (const T *)k, (const T *)v, B, Hkv, L, L_stride, nq, (T *)c->k_res, (T *)c->v_res,
@@ -314,14 +314,10 @@ cudaError_t launch_append(const vc_qcache *c, const void *kn, const void *vn, co
                           const int32_t *len_base, const int32_t *n_acc, int max_new, int requantize,
                           cudaStream_t st)
 {
-    const size_t smem = sizeof(QSmem<D>);
-    auto kern = append_kernel<T, BITS, D>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<c->B, kThreads, smem, st>>>((const T *)kn, (const T *)vn, n_new, len_base, n_acc, max_new, c->Hkv,
-                                       (T *)c->k_res, (T *)c->v_res, c->res_cap, c->cfg.residual,
-                                       requantize, c->max_groups, (uint8_t *)c->records,
-                                       vc_record_bytes(BITS, D), c->n_groups, c->seq_len,
-                                       c->status);
+    append_kernel<T, BITS, D><<<c->B, 2 * D, 0, st>>>(
+        (const T *)kn, (const T *)vn, n_new, len_base, n_acc, max_new, c->Hkv, (T *)c->k_res,
+        (T *)c->v_res, c->res_cap, c->cfg.residual, requantize, c->max_groups,
+        (uint8_t *)c->records, c->n_groups, c->seq_len, c->status);
     return cudaGetLastError();
 }
 

@@ -238,40 +238,76 @@ long orc_kivi_quantize(const float *k, const float *v, int B, int H, int L, int 
 
 /* One record per (sequence, kv head, token group of G=32):
  *   [K codes: G*d*bits/8][V codes: G*d*bits/8][K meta: 4d][V meta: 4d] bytes.
- * Code sections are lane-major: lane l in [0,32) owns E*bits/8 consecutive
- * bytes, E = G*d/32 codes.  Inside a lane, codes come in pairs (e = 2p, 2p+1);
- * pair p sits in little-endian 32-bit word p / P, slot j = p % P
- * (P = 16/bits): the first code of the pair at bit bits*j, the second at bit
- * 16 + bits*j.
- * The lane/element -> (token, channel) map is the m16n8k16 operand fragment
- * layout of the PTX ISA (row = lane/4 + 8*(reg&1), col = 2*(lane%4) + half +
- * 8*(reg>>1)):
- *   K codes, element e = ((mt*(d/16) + ks)*4 + r)*2 + hh:
- *       token   = 16 mt + lane/4 + 8 (r & 1),  channel = 16 ks + 2 (lane%4) + hh + 8 (r >> 1)
- *   V codes, element e = ((mt*2 + ks)*4 + r)*2 + hh:
- *       channel = 16 mt + lane/4 + 8 (r & 1),  token   = 16 ks + 2 (lane%4) + hh + 8 (r >> 1)
- *   K meta: 4 blocks j (of d bytes).  Block j holds fp16 pairs (s[c0], s[c0+1])
- *       for (ks, rr) at byte j*d + 4*(2 ks + rr), c0 = 16 ks + 2 j + 8 rr, then
- *       the matching zero pairs at byte j*d + d/2 + 4*(2 ks + rr).
- *   V meta: 4 blocks j (of d bytes).  Block j holds fp16 pairs
- *       (s[t0][gc], s[t0+1][gc]) at byte j*d + 4*((2 ks + rr)*(d/32) + gc),
- *       t0 = 16 ks + 2 j + 8 rr, then the zero pairs at byte j*d + d/2 + same.
+ * Code sections.  Lane l in [0,32) owns W = d*bits/32 little-endian 32-bit
+ * words; word w of lane l sits at byte 16*(32*(w/4) + l) + 4*(w%4) (16-byte
+ * chunks interleaved across lanes).  A lane holds d/2 code pairs; pair
+ * (mt, ks, r) covers the two elements hh = 0, 1 of the m16n8k16 operand
+ * fragment register r (PTX ISA fragment layout: row = lane/4 + 8*(r&1),
+ * col = 2*(lane%4) + hh + 8*(r>>1)):
+ *   K (A = codes, rows = tokens):  mt in {0,1}, ks in [0,d/16):
+ *       token = 16 mt + lane/4 + 8 (r&1), channel = 16 ks + 2 (lane%4) + hh + 8 (r>>1);
+ *       class kappa = 2 ks + (r>>1), member mu = 2 mt + (r&1)
+ *   V (A = codes^T, rows = channels): mt in [0,d/16), ks in {0,1}:
+ *       channel = 16 mt + lane/4 + 8 (r&1), token = 16 ks + 2 (lane%4) + hh + 8 (r>>1);
+ *       class kappa = 2 mt + (r&1), member mu = 2 ks + (r>>1)
+ * Pair (kappa, mu) sits in word `word`, slot `slot` (first element at bit
+ * bits*slot, second at bit 16 + bits*slot):
+ *   bits = 2 (h = W/2, q = W/4): kappa < 3h: e = kappa / h, i = kappa % h,
+ *       word = 2 i + mu/2, slot = e + 5 (mu%2); else k2 = kappa - 3h:
+ *       e = 3 + k2 / q, i = k2 % q, word = 4 i + mu, slot = e.
+ *   bits = 4 (h = W/2): e = kappa / h, i = kappa % h, word = 2 i + mu/2,
+ *       slot = e + 2 (mu%2).
+ * Meta sections.  For lane quad j in [0,4) the library stores a sequence of
+ * fp16 pairs; pair n of quad j sits at byte 16*(4*(n/4) + j) + 4*(n%4) of the
+ * scale region, and the matching zero-point pair at the same offset + 2d.
+ *   K meta: n = 2 ks + rr, pair = (s[c0], s[c0+1]), c0 = 16 ks + 2 j + 8 rr.
+ *   V meta: n = (2 ks + rr)*(d/32) + gc, pair = (s[t0][gc], s[t0+1][gc]),
+ *           t0 = 16 ks + 2 j + 8 rr.
  * This reader implements the map directly from that statement; it shares
  * nothing with the GPU writer. */
-static int rec_code(const uint8_t *sec, int lane, int e, int bits, int E)
+static void pair_pos(int bits, int d, int kappa, int mu, int *word, int *slot)
 {
-    const uint8_t *lb = sec + (long)lane * E * bits / 8;
-    int p = e >> 1, hh = e & 1, P = 16 / bits;
-    int w = p / P, j = p % P;
-    uint32_t word = (uint32_t)lb[4 * w] | ((uint32_t)lb[4 * w + 1] << 8) |
-                    ((uint32_t)lb[4 * w + 2] << 16) | ((uint32_t)lb[4 * w + 3] << 24);
-    int shift = bits * j + (hh ? 16 : 0);
-    return (int)((word >> shift) & ((1u << bits) - 1));
+    int W = d * bits / 32;
+    if (bits == 2) {
+        int h = W / 2, q = W / 4;
+        if (kappa < 3 * h) {
+            int e = kappa / h, i = kappa % h;
+            *word = 2 * i + mu / 2;
+            *slot = e + 5 * (mu % 2);
+        } else {
+            int k2 = kappa - 3 * h;
+            int e = 3 + k2 / q, i = k2 % q;
+            *word = 4 * i + mu;
+            *slot = e;
+        }
+    } else {
+        int h = W / 2;
+        int e = kappa / h, i = kappa % h;
+        *word = 2 * i + mu / 2;
+        *slot = e + 2 * (mu % 2);
+    }
+}
+
+static uint32_t rd_u32(const uint8_t *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+static int rec_code(const uint8_t *sec, int lane, int word, int slot, int hh, int bits)
+{
+    uint32_t w = rd_u32(sec + 16 * (32 * (word / 4) + lane) + 4 * (word % 4));
+    int shift = bits * slot + (hh ? 16 : 0);
+    return (int)((w >> shift) & ((1u << bits) - 1));
 }
 
 static uint16_t rd_u16(const uint8_t *p)
 {
     return (uint16_t)(p[0] | (p[1] << 8));
+}
+
+static const uint8_t *meta_pair(const uint8_t *region, int j, int n)
+{
+    return region + 16 * (4 * (n / 4) + j) + 4 * (n % 4);
 }
 
 long orc_record_bytes(int bits, int d, int G)
@@ -286,10 +322,10 @@ int orc_unpack_records(const uint8_t *rec, long n_rec, int bits, int d, int G,
                        uint8_t *kcode, uint16_t *kscale, uint16_t *kzero,
                        uint8_t *vcode, uint16_t *vscale, uint16_t *vzero)
 {
-    if (G != 32 || (d % 32) != 0 || (bits != 2 && bits != 4))
+    if (G != 32 || (d != 64 && d != 128) || (bits != 2 && bits != 4))
         return -1;
     long rb = orc_record_bytes(bits, d, G);
-    int E = G * d / 32, KS = d / 16, ncg = d / 32;
+    int KS = d / 16, ncg = d / 32;
     for (long g = 0; g < n_rec; g++) {
         const uint8_t *r0 = rec + g * rb;
         const uint8_t *kc = r0;
@@ -298,30 +334,33 @@ int orc_unpack_records(const uint8_t *rec, long n_rec, int bits, int d, int G,
         const uint8_t *vm = km + 4L * d;
         for (int lane = 0; lane < 32; lane++) {
             int gid = lane / 4, tig = lane % 4;
-            for (int e = 0; e < E; e++) {
-                int hh = e & 1, r = (e >> 1) & 3, blk = e >> 3;
-                /* K codes: blk = mt*KS + ks */
-                {
-                    int mt = blk / KS, ks = blk % KS;
-                    int t = 16 * mt + gid + 8 * (r & 1);
-                    int c = 16 * ks + 2 * tig + hh + 8 * (r >> 1);
-                    kcode[(g * G + t) * d + c] = (uint8_t)rec_code(kc, lane, e, bits, E);
+            for (int r = 0; r < 4; r++)
+                for (int hh = 0; hh < 2; hh++) {
+                    int word, slot;
+                    /* K */
+                    for (int mt = 0; mt < 2; mt++)
+                        for (int ks = 0; ks < KS; ks++) {
+                            pair_pos(bits, d, 2 * ks + (r >> 1), 2 * mt + (r & 1), &word, &slot);
+                            int t = 16 * mt + gid + 8 * (r & 1);
+                            int c = 16 * ks + 2 * tig + hh + 8 * (r >> 1);
+                            kcode[(g * G + t) * d + c] = (uint8_t)rec_code(kc, lane, word, slot, hh, bits);
+                        }
+                    /* V */
+                    for (int mt = 0; mt < KS; mt++)
+                        for (int ks = 0; ks < 2; ks++) {
+                            pair_pos(bits, d, 2 * mt + (r & 1), 2 * ks + (r >> 1), &word, &slot);
+                            int c = 16 * mt + gid + 8 * (r & 1);
+                            int t = 16 * ks + 2 * tig + hh + 8 * (r >> 1);
+                            vcode[(g * G + t) * d + c] = (uint8_t)rec_code(vc, lane, word, slot, hh, bits);
+                        }
                 }
-                /* V codes: blk = mt*2 + ks */
-                {
-                    int mt = blk / 2, ks = blk % 2;
-                    int c = 16 * mt + gid + 8 * (r & 1);
-                    int t = 16 * ks + 2 * tig + hh + 8 * (r >> 1);
-                    vcode[(g * G + t) * d + c] = (uint8_t)rec_code(vc, lane, e, bits, E);
-                }
-            }
         }
         for (int j = 0; j < 4; j++) {
             for (int ks = 0; ks < KS; ks++)
                 for (int rr = 0; rr < 2; rr++) {
                     int c0 = 16 * ks + 2 * j + 8 * rr;
-                    const uint8_t *sp = km + (long)j * d + 4 * (2 * ks + rr);
-                    const uint8_t *zp = sp + d / 2;
+                    const uint8_t *sp = meta_pair(km, j, 2 * ks + rr);
+                    const uint8_t *zp = sp + 2 * d;
                     kscale[g * d + c0] = rd_u16(sp);
                     kscale[g * d + c0 + 1] = rd_u16(sp + 2);
                     kzero[g * d + c0] = rd_u16(zp);
@@ -331,8 +370,8 @@ int orc_unpack_records(const uint8_t *rec, long n_rec, int bits, int d, int G,
                 for (int rr = 0; rr < 2; rr++)
                     for (int gc = 0; gc < ncg; gc++) {
                         int t0 = 16 * ks + 2 * j + 8 * rr;
-                        const uint8_t *sp = vm + (long)j * d + 4 * ((2 * ks + rr) * ncg + gc);
-                        const uint8_t *zp = sp + d / 2;
+                        const uint8_t *sp = meta_pair(vm, j, (2 * ks + rr) * ncg + gc);
+                        const uint8_t *zp = sp + 2 * d;
                         vscale[(g * G + t0) * ncg + gc] = rd_u16(sp);
                         vscale[(g * G + t0 + 1) * ncg + gc] = rd_u16(sp + 2);
                         vzero[(g * G + t0) * ncg + gc] = rd_u16(zp);
