@@ -412,6 +412,28 @@ def run_kernel(args, dev):
             fn = lambda: vc.vc_draft_attn(q, view, scale, out, ws2)
             nbytes = 2 * ko.numel() * 2 + 2 * q.numel() * 2
             rec = {"workload": "decode attention over the compacted cache [4,8,33024,128] bf16, 32/8 heads"}
+    elif name == "swap":
+        # full-cache swap-in (host link): one copy, or the cache split in
+        # chunks issued on as many side streams
+        k = torch.empty(B, HKV, CTX + DQ, D_HEAD, dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        kh = torch.empty(k.shape, dtype=torch.bfloat16).pin_memory()
+        vh = torch.empty(k.shape, dtype=torch.bfloat16).pin_memory()
+        nch = max(1, args.chunks)
+        streams = [torch.cuda.Stream(device=dev) for _ in range(nch)]
+        main = torch.cuda.current_stream()
+        kc, vc_ = k.view(-1).chunk(nch), v.view(-1).chunk(nch)
+        khc, vhc = kh.view(-1).chunk(nch), vh.view(-1).chunk(nch)
+
+        def fn():
+            for i, st in enumerate(streams):
+                st.wait_stream(main)
+                vc.vc_swap_in(kc[i], khc[i], stream=st)
+                vc.vc_swap_in(vc_[i], vhc[i], stream=st)
+            for st in streams:
+                main.wait_stream(st)
+        nbytes = 2 * k.numel() * 2
+        rec = {"workload": f"full-KV swap-in, 2 x [16,8,{CTX + DQ},128] bf16 from pinned host, {nch} chunk(s)"}
     else:
         raise SystemExit(f"unknown kernel {name}")
     for _ in range(args.warmup):
@@ -444,6 +466,7 @@ def main():
     ap.add_argument("--kernel", default=None,
                     help="time one kernel alone: draft, verify, accept, quantize, drop, dense_draft")
     ap.add_argument("--dq", type=int, default=32, help="verify block size for --kernel verify")
+    ap.add_argument("--chunks", type=int, default=1, help="side streams for --kernel swap")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":

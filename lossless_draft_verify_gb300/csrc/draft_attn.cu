@@ -4,19 +4,19 @@
 //
 // KIVI cache kernel.  Grid = (split, kv unit); each CTA streams a contiguous
 // range of 32-token group records through per-warp shared-memory rings filled
-// by cp.async.bulk (one bulk copy per record, mbarrier completion).  A warp
-// owns whole groups and computes, for the Hq/Hkv <= 4 query heads of its kv
-// head, the scores and the weighted values with m16n8k16 tensor-core MMAs on
-// the integer codes themselves: the per-channel K scale is folded into the
-// query (q' = q * s), the per-token V scale into the probabilities
-// (p' = p * s), and the zero-points enter through two small MMAs whose
-// operands are the padding columns 4..7 of the head dimension (n = 8).  Codes
-// are turned into exact fp16 integers with one shift + one LOP3 per pair
-// (1024 + code), the 1024 offset being cancelled exactly for K through the
-// same MMA (sum of q') and subtracted with HSUB2 for V.  Online softmax in the
-// exp2 domain with lazy rescaling.  The residual (full-precision ring) is one
-// extra split handled with fp32 CUDA-core math.  A combine kernel merges the
-// split partials.
+// by cp.async.bulk (one bulk copy per pair of records, mbarrier completion).
+// A warp owns pairs of groups and computes, for the Hq/Hkv <= 4 query heads of
+// its kv head, the scores and the weighted values with m16n8k16 tensor-core
+// MMAs on the integer codes themselves: the per-channel K scale is folded into
+// the query (q' = q * s), the per-token V scale into the probabilities
+// (p' = p * s), and the K zero-point enters through one small MMA whose
+// operand is the padding head columns 4..7 (n = 8), the V zero-point through
+// another.  Codes become exact fp16 operands with a single AND per pair: the
+// masked bits are an fp16 subnormal code * 2^(b e) * 2^-24, the slot factor
+// 2^(b e) being fixed per channel by the record layout and cancelled in q (K)
+// or per output row (V).  Online softmax in the exp2 domain with lazy
+// rescaling.  The residual (full-precision ring) is one extra split handled
+// with fp32 CUDA-core math.  A combine kernel merges the split partials.
 //
 // Dense cache kernel (compacted dropped cache, or an uncompressed cache):
 // fp32 CUDA-core math over 32-token tiles staged by cp.async.bulk.
@@ -55,24 +55,10 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
     return y;
 }
 
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
 {
     uint32_t d;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
 
@@ -82,7 +68,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-constexpr uint32_t kMagic = 0x64006400u;   // half2(1024, 1024)
 constexpr uint32_t kOnes = 0x3C003C00u;    // half2(1, 1)
 
 // ------------------------------------------------------------ KIVI kernel --
@@ -112,7 +97,10 @@ struct Pairs {
 };
 
 // Unpack pair (kappa, mu) from the lane's words w0 (as stored) and w1 (the
-// words shifted right so that the high slots land at the bottom).
+// words shifted right so that the high slots land at the bottom).  Masking
+// the two codes in place yields two fp16 subnormals of exact value
+// code * 2^(b e) * 2^-24: the MMA multiplies them exactly and the caller
+// removes the 2^24 and 2^(b e) factors once.
 template <int BITS, int D>
 __device__ __forceinline__ uint32_t unpack(const uint32_t *w0, const uint32_t *w1, int kappa, int mu)
 {
@@ -121,7 +109,16 @@ __device__ __forceinline__ uint32_t unpack(const uint32_t *w0, const uint32_t *w
     const auto p = Pairs<BITS, D>::pos(kappa, mu);
     const uint32_t src = p.slot < split ? w0[p.word] : w1[p.word];
     const int sl = p.slot < split ? p.slot : p.slot - split;
-    return lop3_and_or(src, base << (BITS * sl), kMagic);
+    return src & (base << (BITS * sl));
+}
+
+constexpr float kTwo24 = 16777216.0f;          // undoes the subnormal 2^-24
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 template <int BITS, int D>
@@ -179,9 +176,9 @@ __device__ void cta_merge_store(float *wbuf, float *dst, int grp)
 }
 
 // Scores of one group: sc[mt][4] (rows = tokens 16 mt + gid (+8), columns =
-// heads 2 tig + {0,1}) with the zero-point and 1024-offset terms folded in.
+// heads 2 tig + {0,1}) with the zero-point term folded in.
 // ksrc: this lane's K-scale pairs (record, or ones for the head copies 4..7);
-// zsrc: this lane's bias-tile row (ones: row 0, K zeros: row 1, zeros: others).
+// zsrc: this lane's bias-tile row (K zeros for row 1, zeros otherwise).
 template <int BITS, int D>
 __device__ __forceinline__ void group_scores(const uint8_t *rec, const uint8_t *ksrc, const uint8_t *zsrc,
                                              const uint32_t (&qf)[D / 16][2], int lane, int tig,
@@ -223,18 +220,15 @@ __device__ __forceinline__ void group_scores(const uint8_t *rec, const uint8_t *
             }
         }
     }
-    // row 0 of the bias tile = sum of q' (the 1024 offset), row 1 columns
-    // 4..7 = sum of z * q for heads 0..3
+    // row 1 of the bias tile, columns 4..7 = sum of z * q for heads 0..3
     const int t1 = tig & 1;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-        const float sq = __shfl_sync(0xffffffffu, cb[e], t1);
-        const float zq = __shfl_sync(0xffffffffu, cb[e], 6 + t1);
-        const float bias = zq - 1024.f * sq;
-        sc[0][e] += bias;
-        sc[0][e + 2] += bias;
-        sc[1][e] += bias;
-        sc[1][e + 2] += bias;
+        const float bias = __shfl_sync(0xffffffffu, cb[e], 6 + t1);
+        sc[0][e] = fmaf(sc[0][e], kTwo24, bias);
+        sc[0][e + 2] = fmaf(sc[0][e + 2], kTwo24, bias);
+        sc[1][e] = fmaf(sc[1][e], kTwo24, bias);
+        sc[1][e + 2] = fmaf(sc[1][e + 2], kTwo24, bias);
     }
 }
 
@@ -280,8 +274,7 @@ __device__ __forceinline__ void group_values(const uint8_t *rec, const uint8_t *
                 const int mt = 2 * gc + half;
                 uint32_t a[4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    a[r] = hsub2(unpack<BITS, D>(w0, w1, 2 * mt + (r & 1), 2 * ks + (r >> 1)), kMagic);
+                for (int r = 0; r < 4; ++r) a[r] = unpack<BITS, D>(w0, w1, 2 * mt + (r & 1), 2 * ks + (r >> 1));
                 mma16816(o_acc[mt], a, b0, b1);
             }
         }
@@ -376,12 +369,12 @@ draft_kivi_kernel(KiviParams P)
             float sc[2][2][4];
             {
                 const uint8_t *ks_src = gid < 4 ? recA + Gm::KM : ones;
-                const uint8_t *z_src = gid == 0 ? ones : (gid == 1 ? recA + Gm::KM + 2 * D : zeros);
+                const uint8_t *z_src = gid == 1 ? recA + Gm::KM + 2 * D : zeros;
                 group_scores<BITS, D>(recA, ks_src, z_src, qf, lane, tig, sc[0]);
             }
             if (two) {
                 const uint8_t *ks_src = gid < 4 ? recB + Gm::KM : ones;
-                const uint8_t *z_src = gid == 0 ? ones : (gid == 1 ? recB + Gm::KM + 2 * D : zeros);
+                const uint8_t *z_src = gid == 1 ? recB + Gm::KM + 2 * D : zeros;
                 group_scores<BITS, D>(recB, ks_src, z_src, qf, lane, tig, sc[1]);
             } else {
 #pragma unroll
@@ -413,7 +406,7 @@ draft_kivi_kernel(KiviParams P)
 #pragma unroll
             for (int e = 0; e < 2; ++e)
                 if (gmax[e] > m_run[e] + kLazy) {
-                    alpha[e] = exp2f(m_run[e] - gmax[e]);
+                    alpha[e] = ex2(m_run[e] - gmax[e]);
                     m_run[e] = gmax[e];
                 }
             if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
@@ -438,7 +431,7 @@ draft_kivi_kernel(KiviParams P)
                 for (int mt = 0; mt < 2; ++mt) {
                     float p[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) p[i] = exp2f(sc[G2][mt][i] - m_run[i & 1]);
+                    for (int i = 0; i < 4; ++i) p[i] = ex2(sc[G2][mt][i] - m_run[i & 1]);
                     l_run[0] += p[0] + p[2];
                     l_run[1] += p[1] + p[3];
                     pb[G2][mt][0] = movmatrix_trans(pack_half2(p[0], p[1]));
@@ -490,9 +483,9 @@ draft_kivi_kernel(KiviParams P)
                 }
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
-                    // rows 16 mt + gid (+8): undo the code factor 2^(b e) of their class
-                    const float f0 = exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt)));
-                    const float f1 = exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt + 1)));
+                    // rows 16 mt + gid (+8): undo 2^-24 and the code factor 2^(b e) of their class
+                    const float f0 = kTwo24 * exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt)));
+                    const float f1 = kTwo24 * exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt + 1)));
                     const int c0 = 16 * mt + gid;
                     wo[(warp * 4 + h) * D + c0] = o_acc[mt][e] * f0 + vbias[mt / 2][e];
                     wo[(warp * 4 + h) * D + c0 + 8] = o_acc[mt][e + 2] * f1 + vbias[mt / 2][e];
