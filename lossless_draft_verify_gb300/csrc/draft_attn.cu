@@ -16,7 +16,8 @@
 // 2^(b e) being fixed per channel by the record layout and cancelled in q (K)
 // or per output row (V).  Online softmax in the exp2 domain with lazy
 // rescaling.  The residual (full-precision ring) is one extra split handled
-// with fp32 CUDA-core math.  A combine kernel merges the split partials.
+// with fp32 CUDA-core math.  The last CTA of each kv unit (device-scope counter
+// in the workspace, returned to zero after use) merges the split partials.
 //
 // Dense cache kernel (compacted dropped cache, or an uncompressed cache):
 // fp32 CUDA-core math over 32-token tiles staged by cp.async.bulk.
@@ -140,6 +141,8 @@ struct KiviParams {
     const void *kres, *vres;
     const int32_t *n_groups, *seq_len;
     float *part;
+    unsigned int *counters;                            // [units], zero between calls
+    void *out;
     int32_t *status;
     int Hkv, Hq, grp, max_groups, res_cap, n_split_q, groups_per_split;
     float qscale;                                      // sm_scale * log2(e)
@@ -173,6 +176,51 @@ __device__ void cta_merge_store(float *wbuf, float *dst, int grp)
         dst[h] = M;
         dst[4 + h] = h < grp ? L : 0.f;
     }
+}
+
+// The last CTA of a kv unit to finish merges the unit's split partials and
+// writes the normalised output rows out[h][D] (h < grp); the counter is left
+// at zero for the next call.  The per-split weights 2^(m_s - M) / L are
+// computed once in shared memory, so each output element is a sum of
+// independent loads.
+constexpr int kMaxSplit = 64;
+
+template <typename TO, int D>
+__device__ void last_cta_combine(const float *unit_part, int n_split, unsigned int *counter, int grp,
+                                 TO *out)
+{
+    __shared__ bool is_last;
+    __shared__ float wgt[4][kMaxSplit];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == (unsigned int)(n_split - 1);
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    if (threadIdx.x < 4) {
+        const int h = threadIdx.x;
+        float M = kNegBig;
+        for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldcg(unit_part + (size_t)s * part_floats(D) + h));
+        float L = 0.f;
+        for (int s = 0; s < n_split; ++s) {
+            const float *q = unit_part + (size_t)s * part_floats(D);
+            const float w = exp2f(__ldcg(q + h) - M);
+            wgt[h][s] = w;
+            L += __ldcg(q + 4 + h) * w;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int s = 0; s < n_split; ++s) wgt[h][s] *= inv;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < grp * D; i += kThreads) {
+        const int h = i / D, c = i % D;
+        const float *q = unit_part + 8 + h * D + c;
+        float O = 0.f;
+#pragma unroll 8
+        for (int s = 0; s < n_split; ++s) O = fmaf(__ldcg(q + (size_t)s * part_floats(D)), wgt[h][s], O);
+        out[h * D + c] = Elem<TO>::from_f(O);
+    }
+    if (threadIdx.x == 0) *counter = 0u;
 }
 
 // Scores of one group: sc[mt][4] (rows = tokens 16 mt + gid (+8), columns =
@@ -493,6 +541,9 @@ draft_kivi_kernel(KiviParams P)
             }
         }
         cta_merge_store<D>(wbuf, dst, grp);
+        last_cta_combine<TQ, D>(P.part + (size_t)unit * (P.n_split_q + 1) * part_floats(D), P.n_split_q + 1,
+                                P.counters + unit, grp,
+                                reinterpret_cast<TQ *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
     } else {
         // ------------------------------------- residual ring (fp32 SIMT) --
         const int len = P.seq_len[b];
@@ -549,6 +600,9 @@ draft_kivi_kernel(KiviParams P)
             for (int i = 0; i < CPL; ++i) wo[(warp * 4 + h) * D + lane * CPL + i] = o[h][i];
         }
         cta_merge_store<D>(wbuf, dst, grp);
+        last_cta_combine<TQ, D>(P.part + (size_t)unit * (P.n_split_q + 1) * part_floats(D), P.n_split_q + 1,
+                                P.counters + unit, grp,
+                                reinterpret_cast<TQ *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
     }
 }
 
@@ -561,6 +615,8 @@ struct DenseParams {
     const void *q, *k, *v;
     const int32_t *seq_len;
     float *part;
+    unsigned int *counters;                            // [units], zero between calls
+    void *out;
     int32_t *status;
     int Hkv, Hq, grp, L_stride, n_split, tiles_per_split;
     float qscale;
@@ -705,29 +761,8 @@ draft_dense_kernel(DenseParams P)
         for (int i = 0; i < CPL; ++i) wo[(warp * 4 + h) * D + lane * CPL + i] = o[h][i];
     }
     cta_merge_store<D>(wbuf, dst, grp);
-}
-
-// --------------------------------------------------------------- combine --
-template <typename TQ, int D>
-__global__ void combine_kernel(const float *__restrict__ part, int n_split, int Hkv, int Hq,
-                               int grp, TQ *__restrict__ out)
-{
-    const int unit = blockIdx.x;
-    const int b = unit / Hkv, kvh = unit % Hkv;
-    const float *pp = part + (size_t)unit * n_split * part_floats(D);
-    for (int i = threadIdx.x; i < grp * D; i += blockDim.x) {
-        const int h = i / D, c = i % D;
-        float M = kNegBig;
-        for (int s = 0; s < n_split; ++s) M = fmaxf(M, pp[(size_t)s * part_floats(D) + h]);
-        float L = 0.f, O = 0.f;
-        for (int s = 0; s < n_split; ++s) {
-            const float *q = pp + (size_t)s * part_floats(D);
-            const float w = exp2f(q[h] - M);
-            L += q[4 + h] * w;
-            O += q[8 + h * D + c] * w;
-        }
-        out[((size_t)b * Hq + kvh * grp + h) * D + c] = Elem<TQ>::from_f(L > 0.f ? O / L : 0.f);
-    }
+    last_cta_combine<T, D>(P.part + (size_t)unit * P.n_split * part_floats(D), P.n_split, P.counters + unit, grp,
+                           reinterpret_cast<T *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
 }
 
 // ----------------------------------------------------------------- host ----
@@ -757,6 +792,7 @@ KiviPlan kivi_plan(const vc_qcache *c)
     s = s < 1 ? 1 : s;
     const int max_s = (ng + NW * 4 - 1) / (NW * 4);    // keep >= 2 group pairs per warp
     if (s > max_s) s = max_s > 0 ? max_s : 1;
+    if (s > kMaxSplit - 1) s = kMaxSplit - 1;
     KiviPlan p;
     p.groups_per_split = ng > 0 ? (ng + s - 1) / s : 2;
     p.groups_per_split += p.groups_per_split & 1;       // whole pairs
@@ -776,6 +812,7 @@ DensePlan dense_plan(const vc_cache_view *v)
     int s = (target_ctas + units - 1) / units;
     const int max_s = (nt + NW - 1) / NW;
     if (s > max_s) s = max_s;
+    if (s > kMaxSplit) s = kMaxSplit;
     if (s < 1) s = 1;
     DensePlan p;
     p.tiles_per_split = nt > 0 ? (nt + s - 1) / s : 1;
@@ -797,7 +834,9 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     P.n_groups = c->n_groups;
     P.seq_len = c->seq_len;
     P.status = (int32_t *)ws;
-    P.part = (float *)((uint8_t *)ws + kStatusBytes);
+    P.counters = (unsigned int *)((uint8_t *)ws + kStatusBytes);
+    P.part = (float *)((uint8_t *)ws + kStatusBytes + align256((size_t)c->B * c->Hkv * 4));
+    P.out = out;
     P.Hkv = c->Hkv;
     P.Hq = Hq;
     P.grp = Hq / c->Hkv;
@@ -813,8 +852,6 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(pl.n_split_q + 1, c->B * c->Hkv);
     kern<<<grid, kThreads, smem, st>>>(P);
-    combine_kernel<TQ, D><<<c->B * c->Hkv, 256, 0, st>>>(P.part, pl.n_split_q + 1, c->Hkv, Hq,
-                                                         P.grp, (TQ *)out);
     return cudaGetLastError();
 }
 
@@ -829,7 +866,9 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
     P.v = v->v;
     P.seq_len = v->seq_len;
     P.status = (int32_t *)ws;
-    P.part = (float *)((uint8_t *)ws + kStatusBytes);
+    P.counters = (unsigned int *)((uint8_t *)ws + kStatusBytes);
+    P.part = (float *)((uint8_t *)ws + kStatusBytes + align256((size_t)v->B * v->Hkv * 4));
+    P.out = out;
     P.Hkv = v->Hkv;
     P.Hq = Hq;
     P.grp = Hq / v->Hkv;
@@ -846,8 +885,6 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(pl.n_split, v->B * v->Hkv);
     kern<<<grid, kThreads, smem, st>>>(P);
-    combine_kernel<T, D><<<v->B * v->Hkv, 256, 0, st>>>(P.part, pl.n_split, v->Hkv, Hq, P.grp,
-                                                       (T *)out);
     return cudaGetLastError();
 }
 
@@ -875,11 +912,12 @@ size_t draft_ws_bytes(const vc_cache_view *view, int Hq)
     if (view->kind == VC_CACHE_KIVI) {
         const vc_qcache *c = view->kivi;
         const KiviPlan p = kivi_plan(c);
-        return kStatusBytes +
+        return kStatusBytes + align256((size_t)c->B * c->Hkv * 4) +
                align256((size_t)c->B * c->Hkv * (p.n_split_q + 1) * part_floats(c->d) * 4);
     }
     const DensePlan p = dense_plan(view);
-    return kStatusBytes + align256((size_t)view->B * view->Hkv * p.n_split * part_floats(view->d) * 4);
+    return kStatusBytes + align256((size_t)view->B * view->Hkv * 4) +
+           align256((size_t)view->B * view->Hkv * p.n_split * part_floats(view->d) * 4);
 }
 
 cudaError_t draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq,

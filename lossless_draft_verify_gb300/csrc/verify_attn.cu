@@ -2,8 +2,8 @@
 // full KV cache (VeriCache verifies drafts against the full cache; the verify
 // step is compute-bound, paper page "What the paper found").
 //
-// Tensor-core path (bf16, d = 128): one CTA per (kv unit, 128-row query tile,
-// key split).  The 128 rows are the (query, head) pairs of the Hq/Hkv query
+// Tensor-core path (bf16, d = 128): one CTA per (kv unit, one or two 128-row
+// query tiles, key split).  The 128 rows are the (query, head) pairs of the Hq/Hkv query
 // heads sharing one kv head, so the GQA heads and the drafted positions
 // together form a real dense M = 128 contraction.
 //   warp 0      TMA producer: Q once, then 64-key K and V tiles (128-byte
@@ -11,7 +11,8 @@
 //   warp 1      single-thread tcgen05.mma issuer: S = Q K^T into a double-
 //               buffered TMEM tile (128 x 64 fp32), then O += P V into a TMEM
 //               accumulator (128 x 128 fp32), S(j+1) overlapping softmax(j);
-//   warps 2..5  softmax, one thread per row: tcgen05.ld of its S row, causal
+//   warps 2..5  softmax, one thread per row (warps 6..9 for a second 128-row
+//               tile sharing the K/V tiles): tcgen05.ld of its S row, causal
 //               mask, exp2 online softmax with lazy rescaling of O (in TMEM),
 //               P written to shared memory as bf16 in the canonical K-major
 //               layout for the next MMA.
@@ -39,42 +40,53 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 constexpr int TC_D = 128;
 constexpr int TC_M = 128;
 constexpr int TC_N = 64;                 // keys per tile
-constexpr int TC_STAGES = 2;
-constexpr int TC_THREADS = 192;          // 6 warps
 constexpr int TC_PART = 4 + TC_D;        // partial row: m, l, pad, pad, o[128]
 constexpr float TC_LAZY = 8.0f;
 
-// shared-memory carve-up (offsets from a 1024-byte aligned base)
-constexpr int SM_Q = 0;                                   // 2 x (128 x 128 B)
-constexpr int SM_K = SM_Q + TC_M * TC_D * 2;              // stages x (64 x 256 B)
-constexpr int SM_V = SM_K + TC_STAGES * TC_N * TC_D * 2;
-constexpr int SM_P = SM_V + TC_STAGES * TC_N * TC_D * 2;  // 128 x 64 bf16, no swizzle
-constexpr int SM_BAR = SM_P + TC_M * TC_N * 2;
-constexpr int SM_TOTAL = SM_BAR + 256;
-constexpr int TC_SMEM = SM_TOTAL;                         // 2 CTAs fit one SM
-
-constexpr uint32_t TMEM_COLS = 256;      // S0: 0..63, S1: 64..127, O: 128..255
-constexpr uint32_t TMEM_O = 128;
+// Geometry of a CTA holding MT row tiles of 128 (query, head) rows that share
+// every K/V tile.  MT = 1: 2 CTAs per SM; MT = 2: one CTA per SM, the whole
+// TMEM (per tile: S double buffer 2 x 64 columns + O 128 columns).
+template <int MT>
+struct TcGeom {
+    static constexpr int STAGES = MT == 1 ? 2 : 3;
+    static constexpr int THREADS = 64 + 128 * MT;
+    static constexpr int SM_Q = 0;                                    // MT x 2 x (128 x 128 B)
+    static constexpr int SM_K = SM_Q + MT * TC_M * TC_D * 2;          // stages x (64 x 256 B)
+    static constexpr int SM_V = SM_K + STAGES * TC_N * TC_D * 2;
+    static constexpr int SM_P = SM_V + STAGES * TC_N * TC_D * 2;      // MT x (128 x 64 bf16), no swizzle
+    static constexpr int SM_BAR = SM_P + MT * TC_M * TC_N * 2;
+    static constexpr int SMEM = SM_BAR + 512;
+    static constexpr uint32_t TMEM_COLS = 256 * MT;
+};
 
 struct TcParams {
     const int32_t *ctx_len;
     float *part;
     int32_t *status;
-    int Hkv, Dq, grp, n_mtiles, n_split, tiles_per_split;
+    int Hkv, Dq, grp, n_mtiles, n_cta_m, n_split, tiles_per_split;
     float scale_log2;
 };
 
+template <int MT, int STAGES>
 struct Bars {
     uint64_t q_full;
-    uint64_t k_full[TC_STAGES], k_empty[TC_STAGES];
-    uint64_t v_full[TC_STAGES], v_empty[TC_STAGES];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_ready, pv_done;
+    uint64_t k_full[STAGES], k_empty[STAGES];
+    uint64_t v_full[STAGES], v_empty[STAGES];
+    uint64_t s_full[MT][2], s_free[MT][2];
+    uint64_t p_ready[MT], pv_done[MT];
     uint32_t tmem_base;
     int32_t abort_flag;
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Bars *B, int32_t *status,
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename BarsT>
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, BarsT *B, int32_t *status,
                                               int where)
 {
     if (mbar_wait(bar, parity)) return true;
@@ -83,10 +95,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Ba
     return false;
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 2)
+template <int MT>
+__global__ void __launch_bounds__(TcGeom<MT>::THREADS, MT == 1 ? 2 : 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, TcParams P)
 {
+    using Gm = TcGeom<MT>;
+    using BarsT = Bars<MT, Gm::STAGES>;
+    constexpr int STAGES = Gm::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
     if (smem_u32(sm) & 1023u) {
@@ -94,42 +110,47 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (threadIdx.x == 0) report_timeout(P.status, 99);
         return;
     }
-    Bars *B = reinterpret_cast<Bars *>(sm + SM_BAR);
+    BarsT *B = reinterpret_cast<BarsT *>(sm + Gm::SM_BAR);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int split = blockIdx.x;
-    const int mt = blockIdx.y % P.n_mtiles;
-    const int unit = blockIdx.y / P.n_mtiles;
+    const int mtc = blockIdx.y % P.n_cta_m;           // which group of MT row tiles
+    const int unit = blockIdx.y / P.n_cta_m;
     const int b = unit / P.Hkv, kvh = unit % P.Hkv;
-    const int rows_q = TC_M / P.grp;                  // queries per tile
-    const int q0 = mt * rows_q;                       // first query of the tile
-    const int q_last = min(P.Dq, q0 + rows_q) - 1;
+    const int rows_q = TC_M / P.grp;                  // queries per row tile
+    const int q_first = mtc * MT * rows_q;            // first query of the CTA
+    const int q_last = min(P.Dq, q_first + MT * rows_q) - 1;
     const int ctx = P.ctx_len[b];
     const int n_tiles_all = (ctx + q_last + 1 + TC_N - 1) / TC_N;
     const int t_lo = split * P.tiles_per_split;
     const int t_hi = min(n_tiles_all, t_lo + P.tiles_per_split);
     const int n = t_hi > t_lo ? t_hi - t_lo : 0;
-    float *part = P.part + ((size_t)blockIdx.y * P.n_split + split) * TC_M * TC_PART;
+    auto part_of = [&](int t) {
+        const int mt = mtc * MT + t;
+        return P.part + (((size_t)unit * P.n_mtiles + mt) * P.n_split + split) * TC_M * TC_PART;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(&B->q_full, 1);
-        for (int s = 0; s < TC_STAGES; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(&B->k_full[s], 1);
             mbar_init(&B->k_empty[s], 1);
             mbar_init(&B->v_full[s], 1);
             mbar_init(&B->v_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&B->s_full[s], 1);
-            mbar_init(&B->s_free[s], 128);
+        for (int t = 0; t < MT; ++t) {
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(&B->s_full[t][s], 1);
+                mbar_init(&B->s_free[t][s], 128);
+            }
+            mbar_init(&B->p_ready[t], 128);
+            mbar_init(&B->pv_done[t], 1);
         }
-        mbar_init(&B->p_ready, 128);
-        mbar_init(&B->pv_done, 1);
         B->abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && n > 0) {
-        tc::tmem_alloc(&B->tmem_base, TMEM_COLS);
+        tc::tmem_alloc(&B->tmem_base, Gm::TMEM_COLS);
         tc::tmem_relinquish();
     }
     tc::fence_before();
@@ -137,10 +158,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc::fence_after();
 
     if (n == 0) {
-        // no key of this split is visible to the tile's rows: empty partial
-        for (int i = threadIdx.x; i < TC_M * TC_PART; i += TC_THREADS) {
-            const int c = i % TC_PART;
-            part[i] = c == 0 ? kNegBig : 0.f;
+        // no key of this split is visible to the CTA's rows: empty partials
+        for (int t = 0; t < MT; ++t) {
+            float *part = part_of(t);
+            for (int i = threadIdx.x; i < TC_M * TC_PART; i += Gm::THREADS) part[i] = (i % TC_PART) == 0 ? kNegBig : 0.f;
         }
         return;
     }
@@ -152,21 +173,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             tc::prefetch_tmap(&tmQ);
             tc::prefetch_tmap(&tmK);
             tc::prefetch_tmap(&tmV);
-            mbar_arrive_expect_tx(&B->q_full, TC_M * TC_D * 2);
-            const int qrow = b * P.Dq + q0;
-            tc::tma_load_3d(sm + SM_Q, &tmQ, 0, kvh * P.grp, qrow, &B->q_full);
-            tc::tma_load_3d(sm + SM_Q + TC_M * 128, &tmQ, 64, kvh * P.grp, qrow, &B->q_full);
+            mbar_arrive_expect_tx(&B->q_full, MT * TC_M * TC_D * 2);
+            for (int t = 0; t < MT; ++t) {
+                const int qrow = b * P.Dq + q_first + t * rows_q;
+                uint8_t *sq = sm + Gm::SM_Q + t * TC_M * TC_D * 2;
+                tc::tma_load_3d(sq, &tmQ, 0, kvh * P.grp, qrow, &B->q_full);
+                tc::tma_load_3d(sq + TC_M * 128, &tmQ, 64, kvh * P.grp, qrow, &B->q_full);
+            }
             for (int j = 0; j < n; ++j) {
-                const int s = j % TC_STAGES;
-                const uint32_t par = ((j / TC_STAGES) - 1) & 1;
+                const int s = j % STAGES;
+                const uint32_t par = ((j / STAGES) - 1) & 1;
                 const int key0 = (t_lo + j) * TC_N;
-                if (j >= TC_STAGES && !wait_or_abort(&B->k_empty[s], par, B, P.status, 11)) break;
-                uint8_t *sk = sm + SM_K + s * TC_N * TC_D * 2;
+                if (j >= STAGES && !wait_or_abort(&B->k_empty[s], par, B, P.status, 11)) break;
+                uint8_t *sk = sm + Gm::SM_K + s * TC_N * TC_D * 2;
                 mbar_arrive_expect_tx(&B->k_full[s], TC_N * TC_D * 2);
                 tc::tma_load_3d(sk, &tmK, 0, key0, unit, &B->k_full[s]);
                 tc::tma_load_3d(sk + TC_N * 128, &tmK, 64, key0, unit, &B->k_full[s]);
-                if (j >= TC_STAGES && !wait_or_abort(&B->v_empty[s], par, B, P.status, 12)) break;
-                uint8_t *sv = sm + SM_V + s * TC_N * TC_D * 2;
+                if (j >= STAGES && !wait_or_abort(&B->v_empty[s], par, B, P.status, 12)) break;
+                uint8_t *sv = sm + Gm::SM_V + s * TC_N * TC_D * 2;
                 mbar_arrive_expect_tx(&B->v_full[s], TC_N * TC_D * 2);
                 tc::tma_load_3d(sv, &tmV, 0, key0, unit, &B->v_full[s]);
                 tc::tma_load_3d(sv + TC_N * 128, &tmV, 64, key0, unit, &B->v_full[s]);
@@ -178,78 +202,100 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (lane == 0) {
             const uint32_t idS = tc::idesc_bf16(TC_M, TC_N, false, false);
             const uint32_t idO = tc::idesc_bf16(TC_M, TC_D, false, true);
-            const uint32_t sQ = smem_u32(sm + SM_Q);
             bool ok = wait_or_abort(&B->q_full, 0, B, P.status, 21);
             auto issue_S = [&](int j) -> bool {
-                const int s = j % TC_STAGES, sb = j & 1;
-                if (!wait_or_abort(&B->k_full[s], (j / TC_STAGES) & 1, B, P.status, 22)) return false;
-                if (j >= 2 && !wait_or_abort(&B->s_free[sb], ((j >> 1) - 1) & 1, B, P.status, 23))
-                    return false;
-                tc::fence_after();
-                const uint32_t sK = smem_u32(sm + SM_K + s * TC_N * TC_D * 2);
+                const int s = j % STAGES, sb = j & 1;
+                if (!wait_or_abort(&B->k_full[s], (j / STAGES) & 1, B, P.status, 22)) return false;
+                const uint32_t sK = smem_u32(sm + Gm::SM_K + s * TC_N * TC_D * 2);
+                for (int t = 0; t < MT; ++t) {
+                    if (j >= 2 && !wait_or_abort(&B->s_free[t][sb], ((j >> 1) - 1) & 1, B, P.status, 23))
+                        return false;
+                    tc::fence_after();
+                    const uint32_t sQ = smem_u32(sm + Gm::SM_Q + t * TC_M * TC_D * 2);
 #pragma unroll
-                for (int kk = 0; kk < TC_D / 16; ++kk) {
-                    const uint64_t ad = tc::smem_desc(sQ + (kk >> 2) * (TC_M * 128) + (kk & 3) * 32, 16,
-                                                      1024, tc::kSwizzle128B);
-                    const uint64_t bd = tc::smem_desc(sK + (kk >> 2) * (TC_N * 128) + (kk & 3) * 32, 16,
-                                                      1024, tc::kSwizzle128B);
-                    tc::mma_ss(tmem + sb * TC_N, ad, bd, idS, kk > 0);
+                    for (int kk = 0; kk < TC_D / 16; ++kk) {
+                        const uint64_t ad = tc::smem_desc(sQ + (kk >> 2) * (TC_M * 128) + (kk & 3) * 32, 16,
+                                                          1024, tc::kSwizzle128B);
+                        const uint64_t bd = tc::smem_desc(sK + (kk >> 2) * (TC_N * 128) + (kk & 3) * 32, 16,
+                                                          1024, tc::kSwizzle128B);
+                        tc::mma_ss(tmem + t * 256 + sb * TC_N, ad, bd, idS, kk > 0);
+                    }
+                    tc::commit(&B->s_full[t][sb]);
                 }
-                tc::commit(&B->s_full[sb]);
                 tc::commit(&B->k_empty[s]);
                 return true;
             };
             if (ok) ok = issue_S(0);
             for (int j = 0; ok && j < n; ++j) {
                 if (j + 1 < n && !issue_S(j + 1)) { ok = false; break; }
-                const int s = j % TC_STAGES;
-                if (!wait_or_abort(&B->p_ready, j & 1, B, P.status, 24)) { ok = false; break; }
-                if (!wait_or_abort(&B->v_full[s], (j / TC_STAGES) & 1, B, P.status, 25)) { ok = false; break; }
-                tc::fence_after();
-                const uint32_t sP = smem_u32(sm + SM_P);
-                const uint32_t sV = smem_u32(sm + SM_V + s * TC_N * TC_D * 2);
+                const int s = j % STAGES;
+                if (!wait_or_abort(&B->v_full[s], (j / STAGES) & 1, B, P.status, 25)) { ok = false; break; }
+                const uint32_t sV = smem_u32(sm + Gm::SM_V + s * TC_N * TC_D * 2);
+                for (int t = 0; t < MT; ++t) {
+                    if (!wait_or_abort(&B->p_ready[t], j & 1, B, P.status, 24)) { ok = false; break; }
+                    tc::fence_after();
+                    const uint32_t sP = smem_u32(sm + Gm::SM_P + t * TC_M * TC_N * 2);
 #pragma unroll
-                for (int kk = 0; kk < TC_N / 16; ++kk) {
-                    // P: K-major, no swizzle; core matrices 8 rows x 16 B,
-                    // 128 B apart along K, 1024 B apart along M
-                    const uint64_t ad = tc::smem_desc(sP + kk * 256, 128, 1024, tc::kNoSwizzle);
-                    // V: MN-major (d contiguous), 128-B swizzle; atoms of 64 d x 8 keys,
-                    // next 64 d at +TC_N*128 bytes, next 8 keys at +1024 bytes
-                    const uint64_t bd = tc::smem_desc(sV + kk * 2048, TC_N * 128, 1024, tc::kSwizzle128B);
-                    tc::mma_ss(tmem + TMEM_O, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < TC_N / 16; ++kk) {
+                        // P: K-major, no swizzle; core matrices 8 rows x 16 B,
+                        // 128 B apart along K, 1024 B apart along M
+                        const uint64_t ad = tc::smem_desc(sP + kk * 256, 128, 1024, tc::kNoSwizzle);
+                        // V: MN-major (d contiguous), 128-B swizzle; atoms of 64 d x 8 keys,
+                        // next 64 d at +TC_N*128 bytes, next 8 keys at +1024 bytes
+                        const uint64_t bd = tc::smem_desc(sV + kk * 2048, TC_N * 128, 1024, tc::kSwizzle128B);
+                        tc::mma_ss(tmem + t * 256 + 128, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(&B->pv_done[t]);
                 }
-                tc::commit(&B->pv_done);
+                if (!ok) break;
                 tc::commit(&B->v_empty[s]);
             }
         }
     } else {
         // --------------------------------------------------- softmax warps --
-        const int wq = warp & 3;                      // TMEM lane quarter
-        const int r = wq * 32 + lane;                 // tile row
-        const int qi = q0 + r / P.grp;                // query index in the block
+        const int t = (warp - 2) >> 2;                 // row tile of this warp
+        const int wq = warp & 3;                       // TMEM lane quarter
+        const int r = wq * 32 + lane;                  // row within the tile
+        const int qi = q_first + t * rows_q + r / P.grp;
         const bool row_valid = qi < P.Dq;
-        const int kmax = ctx + qi;                    // last visible key
+        const int kmax = ctx + qi;                     // last visible key
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        const uint32_t tbase = tmem + lane_addr + t * 256;
         float m = kNegBig, l = 0.f;
-        uint8_t *sP = sm + SM_P;
+        uint8_t *sP = sm + Gm::SM_P + t * TC_M * TC_N * 2;
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
+        // a warp whose 32 rows all lie beyond the query block keeps the barrier
+        // protocol (same waits and arrivals) but does no softmax work; its P
+        // rows and O rows are never read back
+        const bool warp_live = __any_sync(0xffffffffu, row_valid);
+        for (int j = 0; j < n && !warp_live; ++j) {
             const int sb = j & 1;
-            if (!wait_or_abort(&B->s_full[sb], (j >> 1) & 1, B, P.status, 31)) { ok = false; break; }
+            if (!wait_or_abort(&B->s_full[t][sb], (j >> 1) & 1, B, P.status, 34)) { ok = false; break; }
+            tc::fence_after();
+            tc::fence_before();
+            mbar_arrive(&B->s_free[t][sb]);
+            if (j > 0 && !wait_or_abort(&B->pv_done[t], (j - 1) & 1, B, P.status, 35)) { ok = false; break; }
+            tc::fence_after();
+            tc::fence_before();
+            mbar_arrive(&B->p_ready[t]);
+        }
+        for (int j = 0; j < n && warp_live; ++j) {
+            const int sb = j & 1;
+            if (!wait_or_abort(&B->s_full[t][sb], (j >> 1) & 1, B, P.status, 31)) { ok = false; break; }
             tc::fence_after();
             float s[TC_N];
             {
                 uint32_t u[32];
 #pragma unroll
                 for (int h = 0; h < TC_N / 32; ++h) {
-                    tc::ld32(tmem + lane_addr + sb * TC_N + h * 32, u);
+                    tc::ld32(tbase + sb * TC_N + h * 32, u);
                     tc::ld_wait();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) s[h * 32 + c] = __uint_as_float(u[c]);
                 }
             }
             tc::fence_before();
-            mbar_arrive(&B->s_free[sb]);
+            mbar_arrive(&B->s_free[t][sb]);
             const int key0 = (t_lo + j) * TC_N;
             float mx = kNegBig;
 #pragma unroll
@@ -260,31 +306,31 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
             float alpha = 1.f;
             if (mx > m + TC_LAZY) {
-                alpha = exp2f(m - mx);
+                alpha = ex2(m - mx);
                 m = mx;
             }
             float lsum = 0.f;
             uint32_t pk[TC_N / 2];
 #pragma unroll
             for (int c = 0; c < TC_N; c += 2) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s[c] - m), exp2f(s[c + 1] - m));
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2(s[c] - m), ex2(s[c + 1] - m));
                 const float2 f2 = __bfloat1622float2(h2);
                 lsum += f2.x + f2.y;
                 pk[c / 2] = *reinterpret_cast<uint32_t *>(&h2);
             }
             l = l * alpha + lsum;
-            // the single P buffer and O are free once PV(j-1) has completed
-            if (j > 0 && !wait_or_abort(&B->pv_done, (j - 1) & 1, B, P.status, 32)) { ok = false; break; }
+            // the P buffer of this tile and its O are free once PV(j-1) has completed
+            if (j > 0 && !wait_or_abort(&B->pv_done[t], (j - 1) & 1, B, P.status, 32)) { ok = false; break; }
             tc::fence_after();
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                 for (int h = 0; h < TC_D / 32; ++h) {
                     uint32_t u[32];
-                    tc::ld32(tmem + lane_addr + TMEM_O + h * 32, u);
+                    tc::ld32(tbase + 128 + h * 32, u);
                     tc::ld_wait();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) u[c] = __float_as_uint(__uint_as_float(u[c]) * alpha);
-                    tc::st32(tmem + lane_addr + TMEM_O + h * 32, u);
+                    tc::st32(tbase + 128 + h * 32, u);
                 }
                 tc::st_wait();
             }
@@ -300,11 +346,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
             tc::fence_proxy_async_smem();
             tc::fence_before();
-            mbar_arrive(&B->p_ready);
+            mbar_arrive(&B->p_ready[t]);
         }
         // epilogue: wait for the last PV, read O, store the partial row
-        float *pr = part + (size_t)r * TC_PART;
-        if (ok && wait_or_abort(&B->pv_done, (n - 1) & 1, B, P.status, 33)) {
+        float *pr = part_of(t) + (size_t)r * TC_PART;
+        if (ok && warp_live && wait_or_abort(&B->pv_done[t], (n - 1) & 1, B, P.status, 33)) {
             tc::fence_after();
             pr[0] = m;
             pr[1] = l;
@@ -313,7 +359,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
             for (int h = 0; h < TC_D / 32; ++h) {
                 uint32_t u[32];
-                tc::ld32(tmem + lane_addr + TMEM_O + h * 32, u);
+                tc::ld32(tbase + 128 + h * 32, u);
                 tc::ld_wait();
 #pragma unroll
                 for (int c = 0; c < 32; c += 4)
@@ -332,7 +378,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc::fence_after();
     if (warp == 0) {
         __syncwarp();
-        tc::tmem_dealloc(tmem, TMEM_COLS);
+        tc::tmem_dealloc(tmem, Gm::TMEM_COLS);
     }
 }
 
@@ -471,16 +517,23 @@ int num_sms()
 }
 
 struct TcPlan {
-    int n_mtiles, n_split, tiles_per_split;
+    int n_mtiles, mt_per_cta, n_cta_m, n_split, tiles_per_split;
 };
 
 TcPlan tc_plan(int B, int Dq, int Hkv, int grp, int max_ctx)
 {
     TcPlan p;
     p.n_mtiles = (Dq * grp + TC_M - 1) / TC_M;
+    // One row tile per CTA: a CTA holding two tiles that share every K/V tile
+    // (TcGeom<2>) halves the K/V reads at Dq*grp in (128, 256] but runs one
+    // CTA per SM, and its softmax/MMA handoff chain then limits it to about
+    // 1.0 ms against 0.77 ms for two single-tile CTAs per SM at Dq = 33.
+    p.mt_per_cta = 1;
+    p.n_cta_m = p.n_mtiles / p.mt_per_cta;
     const int tiles = (max_ctx + Dq + TC_N - 1) / TC_N;
-    const int items = B * Hkv * p.n_mtiles;
-    const int target = num_sms() * 2 * 3;            // ~3 waves of 2 CTAs per SM
+    const int items = B * Hkv * p.n_cta_m;
+    const int per_sm = p.mt_per_cta == 1 ? 2 : 1;
+    const int target = num_sms() * per_sm * 3;       // ~3 waves of resident CTAs
     int s = (target + items - 1) / items;
     if (s > tiles) s = tiles;
     if (s < 1) s = 1;
@@ -529,12 +582,18 @@ cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt
         P.Dq = Dq;
         P.grp = grp;
         P.n_mtiles = pl.n_mtiles;
+        P.n_cta_m = pl.n_cta_m;
         P.n_split = pl.n_split;
         P.tiles_per_split = pl.tiles_per_split;
         P.scale_log2 = sl2;
-        cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-        dim3 grid(pl.n_split, B * Hkv * pl.n_mtiles);
-        verify_tc_kernel<<<grid, TC_THREADS, TC_SMEM, st>>>(mq, mk, mv, P);
+        dim3 grid(pl.n_split, B * Hkv * pl.n_cta_m);
+        if (pl.mt_per_cta == 2) {
+            cudaFuncSetAttribute(verify_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<2>::SMEM);
+            verify_tc_kernel<2><<<grid, TcGeom<2>::THREADS, TcGeom<2>::SMEM, st>>>(mq, mk, mv, P);
+        } else {
+            cudaFuncSetAttribute(verify_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<1>::SMEM);
+            verify_tc_kernel<1><<<grid, TcGeom<1>::THREADS, TcGeom<1>::SMEM, st>>>(mq, mk, mv, P);
+        }
         dim3 cgrid(B * Hkv * pl.n_mtiles, TC_M / 4);
         verify_tc_combine<__nv_bfloat16><<<cgrid, 128, 0, st>>>(P.part, pl.n_split, pl.n_mtiles, Hkv, Hq, Dq,
                                                                 grp, (__nv_bfloat16 *)out);
