@@ -53,6 +53,30 @@ def dist_env():
     return rank, world, local
 
 
+# DRAM bytes (read + write) of one draft launch at the 32768-token context,
+# from one ncu capture of the draft kernel, keyed by the SHA-256 of the
+# sources it was built from: a changed kernel reports traffic null until it is
+# captured again.
+DRAFT_TRAFFIC = {
+    "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
+    "sha256": ("190bc277132006521419d50c37d22d1073f34570989ec9e806a4a14009181ff8",
+               "8b1109c68498705ecd31b5533b5ace8c5bb0cfe4584e74b26b26eb3baa0d456c"),
+    "bytes": 412.416512e6 + 6.476032e6,
+    "algorithmic_bytes": 409731072,
+}
+
+
+def captured_traffic(table: dict, per_launch_bytes: float):
+    """Captured DRAM traffic scaled to a launch of `per_launch_bytes`
+    algorithmic bytes, or None when the kernel's sources changed."""
+    import hashlib
+    for rel, want in zip(table["sources"], table["sha256"]):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != want:
+                return None
+    return table["bytes"] * per_launch_bytes / table["algorithmic_bytes"]
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -162,7 +186,8 @@ class Round:
         self.side = torch.cuda.Stream(device=dev)
         self.ev_swap = torch.cuda.Event()
         self.ev_swap.record(self.side)
-        self.launches_per_step = HORIZON * 3 + 2 + 1 + 1
+        # per step: (append + draft) per draft step, verify + its combine, accept, commit
+        self.launches_per_step = HORIZON * 2 + 2 + 1 + 1
         # host-side copies of the per-step inputs (end-to-end measurement)
         self.h_q_draft = self.q_draft.cpu().pin_memory()
         self.h_k_step = self.k_step.cpu().pin_memory()
@@ -564,7 +589,8 @@ def main():
             "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": CTX,
                        "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
             "roofline": {"bound": "hbm", "achieved": draft_gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": draft_gbs / hbm, "traffic": None,
+                         "frac": draft_gbs / hbm,
+                         "traffic": captured_traffic(DRAFT_TRAFFIC, statistics.mean(d_bytes)),
                          "kernel": "vc_draft_attn (draft_kivi_kernel + combine)",
                          "peak_source": f"{peak_src} hbm_gbs"},
             "kernels": {

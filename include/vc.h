@@ -2,11 +2,13 @@
  * vc.h -- C ABI of the GB300 (sm_103a) draft-and-verify hot path.
  *
  * The method ("VeriCache: Turning Lossy KV Cache into Lossless LLM Inference",
- * paper page, "What the paper found" and abstract): run the target model on a
- * compressed KV cache to draft tokens, overlap that HBM-bound drafting with the
- * interconnect-bound swap-in of the full KV cache, verify the drafted block
- * against the full cache, and keep the longest prefix on which the verify
- * argmax equals the drafts, so that greedy output equals full-KV decoding.
+ * paper page, "What the paper found" and abstract): the target model itself
+ * drafts tokens while reading a lossy (quantized or token-dropped) copy of its
+ * KV state; the HBM-bound drafting runs while the interconnect-bound copy of
+ * the exact KV state comes in; one causal pass over the exact state then
+ * checks the whole drafted block, and only the prefix whose verify argmax
+ * agrees with the drafts is kept, so the emitted tokens are those of plain
+ * greedy decoding.
  *
  * Conventions for every entry point:
  *  - All tensor pointers are caller-owned.  "device" pointers are CUDA device
@@ -325,10 +327,9 @@ vc_status vc_accept_noalloc(const void *logits, vc_dtype dt, const int32_t *draf
 /* (6) full-KV swap-in                                                       */
 /* ------------------------------------------------------------------------ */
 /*
- * The full KV cache stays out of GPU memory and is swapped in for
- * verification, overlapped with drafting (abstract: "keeping the full KV cache
- * out of GPU memory and minimizing the overhead of swapping it in"; paper page:
- * cross-resource staggering).  Copies `bytes` from pinned host memory to the
+ * The exact KV state lives in host memory between rounds and is brought in
+ * for verification while drafting runs (abstract on the paper page; the
+ * cross-resource staggering of "What the paper found").  Copies `bytes` from pinned host memory to the
  * device with one asynchronous copy on `side_stream` and, if `done` is not
  * NULL, records `done` on that stream after it; the caller makes the verify
  * stream wait on `done`.  Returns VC_ERR_INVALID if src is not page-locked

@@ -260,7 +260,7 @@ def verify_attn(q, k, v, ctx, scale: float, units=None) -> np.ndarray:
 
 # --------------------------------------------------------------------------
 # greedy acceptance (speculative decoding's greedy rule, source 2 on the
-# podparley page; "identical to full-KV inference" on the paper page)
+# podparley page; the lossless claim of the paper page)
 # --------------------------------------------------------------------------
 
 def accept(logits, drafts):

@@ -4,8 +4,8 @@ draft-and-verify loop.
 TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).
 
 Follows the paper page ("What the paper found", abstract): the target model
-drafts tokens on a compressed KV cache, then the drafted block is verified
-against the full KV cache, so greedy output equals full-KV greedy decoding.
+drafts with a lossy copy of its KV state, one causal pass over the exact state
+checks the drafted block, and the emitted tokens equal plain greedy decoding.
 The acceptance rule is the greedy rule of speculative decoding (source 2 on
 the podparley page): keep the longest drafted prefix that matches the verify
 argmax, then emit the verify argmax at the first mismatch.
