@@ -338,6 +338,121 @@ vc_status vc_accept_noalloc(const void *logits, vc_dtype dt, const int32_t *draf
 vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes,
                      cudaStream_t side_stream, cudaEvent_t done);
 
+/* ------------------------------------------------------------------------ */
+/* (7) target decoder around the hot path                                    */
+/* ------------------------------------------------------------------------ */
+/*
+ * The pages run the method inside a trained LLM; the drafting and the
+ * verification are forward passes of that one model (paper page, "What the
+ * paper found": the target model drafts for itself).  This section is the
+ * model around the six calls above: a Llama-style decoder (pre-RMSNorm with
+ * unit weight, rotate-half RoPE applied to q and k before caching, grouped
+ * query attention with q head h reading kv head h / (Hq/Hkv), SwiGLU MLP,
+ * final RMSNorm, untied LM head, no biases).  Its attention is vc_draft_attn
+ * over a vc_qcache (drafting) or vc_verify_attn over the full cache (verify,
+ * prefill, plain decoding); its projections are the library's own GEMMs.
+ *
+ * Row independence: every kernel of a forward pass computes a token's row
+ * with an operation order fixed by the model's shapes, the key positions and
+ * the device, never by how many rows or sequences share the launch.  A verify
+ * pass over [x, d1..dD] therefore gives, row for row and bit for bit, the
+ * logits that D+1 one-token passes give, which makes draft-and-verify
+ * decoding equal plain greedy decoding exactly (not only up to rounding).
+ */
+typedef struct vc_decoder_cfg {
+    int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ff, vocab;
+    float norm_eps;       /* RMSNorm epsilon */
+    float rope_theta;     /* RoPE base */
+    vc_dtype dt;          /* weights, activations, caches, logits */
+} vc_decoder_cfg;
+
+/* Device pointers, row-major, each matrix stored [in][out] (y = x W).  The
+ * per-layer arrays are host arrays of n_layers device pointers; they are
+ * copied by vc_decoder_create.  bf16 weights with N % 128 == 0 and K % 64 == 0
+ * use the tensor-core GEMM; 16-byte aligned. */
+typedef struct vc_decoder_weights {
+    const void *embed;                /* [vocab][d_model] */
+    const void *lm_head;              /* [d_model][vocab] */
+    const void *const *w_qkv;         /* [d_model][(Hq + 2 Hkv) head_dim]: q | k | v columns */
+    const void *const *w_o;           /* [Hq head_dim][d_model] */
+    const void *const *w_gate_up;     /* [d_model][2 d_ff]: gate | up columns */
+    const void *const *w_down;        /* [d_ff][d_model] */
+} vc_decoder_weights;
+
+typedef struct vc_decoder vc_decoder;   /* host object: configuration + weight pointers */
+
+/* Validate and record the model; no device memory is allocated.
+ * Supported: head_dim in {64, 128}, n_heads % n_kv_heads == 0 with at most 4
+ * q heads per kv head (the draft kernel), bf16 or fp32. */
+vc_status vc_decoder_create(const vc_decoder_cfg *cfg, const vc_decoder_weights *w, vc_decoder **out);
+void vc_decoder_destroy(vc_decoder *dec);
+
+/* Workspace for calls with up to B sequences of up to max_rows rows each and
+ * contexts up to max_ctx tokens; draft_cache (may be NULL when only
+ * vc_decoder_forward is used) is a cache of the geometry later passed to
+ * vc_decoder_draft_step.  Zero-fill once (vc_workspace_init); the status
+ * block of every kernel the decoder launches is folded into its first word
+ * (vc_poll_status). */
+size_t vc_decoder_workspace_bytes(const vc_decoder *dec, int B, int max_rows, int max_ctx,
+                                  const vc_qcache *draft_cache);
+
+/*
+ * vc_decoder_forward -- causal forward of Dq tokens per sequence against the
+ * full KV cache: prefill (ctx_len = 0 or a chunk start), the verify pass
+ * (paper page: the drafted block checked against the full cache) and plain
+ * one-token decoding (Dq = 1).
+ * Tokens: row (b, i) takes first_tok[b] for i = 0 when first_tok is not
+ * NULL, else tokens[b * tok_stride + i - (first_tok ? 1 : 0)] (device int32).
+ * Row (b, i) sits at position ctx_len[b] + i (device int32 [B], every value
+ * <= max_ctx).  k_cache, v_cache: device [n_layers][B][Hkv][L_stride][head_dim]
+ * (L_stride >= max_ctx + Dq); the pass writes its own K/V at those positions
+ * and, when k_blk/v_blk are not NULL, also to [n_layers][B][Hkv][Dq][head_dim]
+ * (the rows vc_qcache_commit consumes).  logits: device [B][Dq][vocab], or
+ * [B][vocab] for row Dq-1 only when logits_last_only != 0.
+ * Token ids outside [0, vocab) read row 0 and set the status block.
+ */
+vc_status vc_decoder_forward(const vc_decoder *dec, const int32_t *first_tok, const int32_t *tokens,
+                             int tok_stride, int B, int Dq, const int32_t *ctx_len, int max_ctx,
+                             void *k_cache, void *v_cache, int L_stride, void *k_blk, void *v_blk,
+                             int logits_last_only, void *logits, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/*
+ * vc_decoder_draft_step -- one draft step on the compressed caches (one
+ * vc_qcache per layer, host array of n_layers, all of one geometry): token
+ * tok[b] sits at position caches[l].seq_len[b]; its K/V are appended to every
+ * layer's ring (no re-quantization: drafted tokens are rolled back by
+ * vc_qcache_commit), attention is vc_draft_attn over the cache, and the
+ * greedy draft token argmax(logits[b]) (lowest index on ties) is written to
+ * next_tok[b] and, when drafts_out is not NULL, to drafts_out[b * drafts_stride].
+ * logits: device [B][vocab] (written).
+ */
+vc_status vc_decoder_draft_step(const vc_decoder *dec, const int32_t *tok, int B, vc_qcache *caches,
+                                void *logits, int32_t *next_tok, int32_t *drafts_out, int drafts_stride,
+                                void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * vc_kv_writeback -- after acceptance, store the verify pass's K/V of the
+ * n_acc[b] + 1 committed rows of every layer into the host-resident full cache
+ * (pinned memory, written directly by the GPU): row i of sequence b goes to
+ * position ctx_len[b] + i.  k_blk, v_blk: device [n_layers][B][Hkv][Dq][d];
+ * k_host, v_host: pinned [n_layers][B][Hkv][L_stride][d]; dt of both.
+ * Returns VC_ERR_INVALID if the host buffers are not page-locked.
+ */
+vc_status vc_kv_writeback(const void *k_blk, const void *v_blk, vc_dtype dt, int n_layers, int B, int Hkv,
+                          int Dq, int d, const int32_t *n_acc, const int32_t *ctx_len, void *k_host,
+                          void *v_host, int L_stride, cudaStream_t stream);
+
+/*
+ * vc_gemm -- out = x W (+ resid) with the decoder's GEMM: x [M][K], W [K][N],
+ * resid and out [M][N] (resid may equal out), dt for all; fp32 accumulation.
+ * The summation order of every output element depends on (N, K) and the
+ * device only.  ws: vc_gemm_workspace_bytes(dt, M, N, K) bytes (may be 0).
+ */
+size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K);
+vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
+                  void *ws, size_t ws_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

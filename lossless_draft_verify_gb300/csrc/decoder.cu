@@ -1,0 +1,555 @@
+// decoder.cu -- the target model around the draft-and-verify hot path: token
+// embedding, RMSNorm, RoPE with the K/V scatter into the caches, SwiGLU, the
+// LM head, and the host-side sequencing of one forward pass (prefill, verify
+// block, plain decoding) or one draft step (paper page, "What the paper
+// found": the target model drafts on its compressed cache and verifies on the
+// full one).
+//
+// Every kernel here keeps a row's arithmetic independent of the other rows
+// of the launch (one CTA per row where a row reduces; fixed reduction trees),
+// and so do the GEMMs (gemm.cu) and the fixed-split verify attention.  A
+// verify pass therefore reproduces one-token decoding bit for bit.
+#include <cuda.h>
+
+#include <new>
+#include <vector>
+
+#include "vc_common.cuh"
+#include "vc_internal.h"
+
+struct vc_decoder {
+    vc_decoder_cfg c;
+    const void *embed, *head;
+    std::vector<const void *> wqkv, wo, wgu, wd;
+};
+
+namespace vc {
+namespace {
+
+// Verify attention inside the decoder uses key splits of a fixed 2048 keys.
+constexpr int kSplitTiles = 32;
+constexpr int kRowThreads = 256;
+constexpr int kBadToken = 1 << 1;       // status bit: a token id outside [0, vocab)
+constexpr int kBadPosition = 1 << 2;    // status bit: a position outside the cache
+
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t esize(vc_dtype dt) { return dt == VC_BF16 ? 2 : 4; }
+
+// ------------------------------------------------------------------ kernels --
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+embed_kernel(const int32_t *__restrict__ first_tok, const int32_t *__restrict__ toks, int tok_stride,
+             int rows_per_seq, const T *__restrict__ E, int vocab, int D, T *__restrict__ x, int32_t *status)
+{
+    const int m = blockIdx.x;
+    const int b = m / rows_per_seq, i = m % rows_per_seq;
+    int t;
+    if (first_tok)
+        t = i == 0 ? first_tok[b] : toks[(size_t)b * tok_stride + i - 1];
+    else
+        t = toks[(size_t)b * tok_stride + i];
+    if (t < 0 || t >= vocab) {
+        if (threadIdx.x == 0) atomicOr(status, kBadToken);
+        t = 0;
+    }
+    const T *src = E + (size_t)t * D;
+    T *dst = x + (size_t)m * D;
+    for (int j = threadIdx.x; j < D; j += kRowThreads) dst[j] = src[j];
+}
+
+// y[r] = x[r*in_step + in_off] / sqrt(mean(x^2) + eps): one CTA per row, the
+// sum of squares over a fixed thread/warp tree.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+rmsnorm_kernel(const T *__restrict__ x, int D, int in_step, int in_off, float eps, T *__restrict__ y)
+{
+    __shared__ float wsum[kRowThreads / 32];
+    const int r = blockIdx.x;
+    const T *xr = x + ((size_t)r * in_step + in_off) * D;
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < D; j += kRowThreads) {
+        const float v = Elem<T>::to_f(xr[j]);
+        ss = fmaf(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRowThreads / 32; ++w) tot += wsum[w];
+    const float inv = 1.0f / sqrtf(tot / (float)D + eps);
+    T *yr = y + (size_t)r * D;
+    for (int j = threadIdx.x; j < D; j += kRowThreads) yr[j] = Elem<T>::from_f(Elem<T>::to_f(xr[j]) * inv);
+}
+
+// RoPE (rotate-half: pair (j, j + hd/2) turned by pos * theta^(-2j/hd)) on the
+// q and k parts of one qkv row, q to q_out, k and v scattered to up to two
+// destinations [.][Hkv][stride][hd]: dst1 at row (pos1 ? pos : 0) + i (the
+// cache), dst2 at row i (the block copy).  Angles in fp64 (positions reach
+// 10^5 radians), cos/sin rounded once to fp32.
+struct RopeDst {
+    void *k1, *v1;
+    size_t bstride1;   // elements between sequences
+    int stride1, pos1; // rows per (sequence, head); row = pos when pos1 else i
+    void *k2, *v2;
+    size_t bstride2;
+    int stride2;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd, const int32_t *__restrict__ pos_base,
+            float theta, T *__restrict__ q_out, RopeDst dst, int32_t *status)
+{
+    __shared__ float cs[64], sn[64];
+    const int m = blockIdx.x;
+    const int b = m / rows_per_seq, i = m % rows_per_seq;
+    const int pos = pos_base[b] + i;
+    const int half = hd / 2;
+    const int row1 = dst.pos1 ? pos : i;
+    if (row1 < 0 || row1 >= dst.stride1) {
+        // a position outside the cache: record it, write nothing
+        if (threadIdx.x == 0) atomicOr(status, kBadPosition);
+        return;
+    }
+    for (int j = threadIdx.x; j < half; j += kRowThreads) {
+        const double ang = (double)pos * pow((double)theta, -2.0 * (double)j / (double)hd);
+        double s, c;
+        sincos(ang, &s, &c);
+        cs[j] = (float)c;
+        sn[j] = (float)s;
+    }
+    __syncthreads();
+    const T *row = qkv + (size_t)m * (Hq + 2 * Hkv) * hd;
+    const int nq = Hq * half, nk = Hkv * half, nv = Hkv * hd;
+    for (int t = threadIdx.x; t < nq + nk + nv; t += kRowThreads) {
+        if (t < nq + nk) {
+            const bool isq = t < nq;
+            const int u = isq ? t : t - nq;
+            const int h = u / half, j = u % half;
+            const T *src = row + (isq ? 0 : Hq * hd) + h * hd;
+            const float x1 = Elem<T>::to_f(src[j]), x2 = Elem<T>::to_f(src[j + half]);
+            const float c = cs[j], s = sn[j];
+            const T y1 = Elem<T>::from_f(x1 * c - x2 * s);
+            const T y2 = Elem<T>::from_f(x2 * c + x1 * s);
+            if (isq) {
+                T *qo = q_out + (size_t)m * Hq * hd + h * hd;
+                qo[j] = y1;
+                qo[j + half] = y2;
+            } else {
+                T *k1 = (T *)dst.k1 + b * dst.bstride1 + ((size_t)h * dst.stride1 + row1) * hd;
+                k1[j] = y1;
+                k1[j + half] = y2;
+                if (dst.k2) {
+                    T *k2 = (T *)dst.k2 + b * dst.bstride2 + ((size_t)h * dst.stride2 + i) * hd;
+                    k2[j] = y1;
+                    k2[j + half] = y2;
+                }
+            }
+        } else {
+            const int u = t - nq - nk;
+            const int h = u / hd, c = u % hd;
+            const T val = row[(Hq + Hkv) * hd + u];
+            ((T *)dst.v1)[b * dst.bstride1 + ((size_t)h * dst.stride1 + row1) * hd + c] = val;
+            if (dst.v2) ((T *)dst.v2)[b * dst.bstride2 + ((size_t)h * dst.stride2 + i) * hd + c] = val;
+        }
+    }
+}
+
+// act = silu(gate) * up, gate | up the two halves of a [M][2F] row.
+template <typename T>
+__global__ void silu_mul_kernel(const T *__restrict__ gu, int M, int F, T *__restrict__ act)
+{
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)M * F) return;
+    const size_t m = idx / F, j = idx % F;
+    const float g = Elem<T>::to_f(gu[m * 2 * F + j]);
+    const float u = Elem<T>::to_f(gu[m * 2 * F + F + j]);
+    act[idx] = Elem<T>::from_f((g / (1.0f + expf(-g))) * u);
+}
+
+__global__ void scatter_tokens_kernel(const int32_t *__restrict__ src, int B, int32_t *dst, int stride)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) dst[(size_t)b * stride] = src[b];
+}
+
+// OR the status words of the sub-workspaces into the decoder's, clear them.
+__global__ void fold_status_kernel(int32_t *main, int32_t *a, int32_t *b, int32_t *c)
+{
+    int32_t v = 0;
+    if (a) { v |= *a; *a = 0; }
+    if (b) { v |= *b; *b = 0; }
+    if (c) { v |= *c; *c = 0; }
+    if (v) atomicOr(main, v);
+}
+
+// One CTA per (row i, sequence-head bh, layer); rows i <= n_acc[b] copied.
+template <typename T>
+__global__ void writeback_kernel(const T *__restrict__ kb, const T *__restrict__ vb, int B, int Hkv, int Dq, int d,
+                                 const int32_t *__restrict__ n_acc, const int32_t *__restrict__ ctx, T *kh, T *vh,
+                                 int L_stride)
+{
+    const int i = blockIdx.x, bh = blockIdx.y, layer = blockIdx.z;
+    const int b = bh / Hkv;
+    if (i > n_acc[b] || ctx[b] + i >= L_stride) return;
+    const size_t src = (((size_t)layer * B * Hkv + bh) * Dq + i) * d;
+    const size_t dst = (((size_t)layer * B * Hkv + bh) * L_stride + ctx[b] + i) * d;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+        kh[dst + c] = kb[src + c];
+        vh[dst + c] = vb[src + c];
+    }
+}
+
+// ------------------------------------------------------------------ layout --
+struct Layout {
+    size_t x, h, qkv, q, att, gu, act, kvn, hl, part, dws, vws, aws, nacc, total;
+};
+
+Layout layout_of(const vc_decoder *d, int B, int max_rows, int max_ctx, size_t draft_ws)
+{
+    const vc_decoder_cfg &c = d->c;
+    const size_t es = esize(c.dt);
+    const size_t M = (size_t)B * max_rows;
+    const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
+    const int nqkv = qd + 2 * kvd;
+    Layout L;
+    size_t o = kStatusBytes;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += a256(bytes);
+        return at;
+    };
+    L.x = take(M * c.d_model * es);
+    L.h = take(M * c.d_model * es);
+    L.qkv = take(M * nqkv * es);
+    L.q = take(M * qd * es);
+    L.att = take(M * qd * es);
+    L.gu = take(M * 2 * (size_t)c.d_ff * es);
+    L.act = take(M * (size_t)c.d_ff * es);
+    L.kvn = take(2 * (size_t)B * kvd * es);
+    L.hl = take((size_t)B * c.d_model * es);
+    size_t part = 0;
+    auto gp = [&](int rows, int N, int K) { part = std::max(part, gemm_ws_bytes(c.dt, rows, N, K)); };
+    gp((int)M, nqkv, c.d_model);
+    gp((int)M, c.d_model, qd);
+    gp((int)M, 2 * c.d_ff, c.d_model);
+    gp((int)M, c.d_model, c.d_ff);
+    gp((int)M, c.vocab, c.d_model);
+    L.part = take(part);
+    L.dws = take(draft_ws);
+    L.vws = take(verify_ws_bytes(c.dt, B, max_rows, c.n_heads, c.n_kv_heads, c.head_dim, max_ctx, kSplitTiles));
+    L.aws = take(accept_ws_bytes(B, 0, c.vocab));
+    L.nacc = take((size_t)B * 4);
+    L.total = o;
+    return L;
+}
+
+size_t draft_ws_of(const vc_decoder *d, const vc_qcache *cache)
+{
+    if (!cache) return 0;
+    vc_cache_view v{};
+    v.kind = VC_CACHE_KIVI;
+    v.kivi = const_cast<vc_qcache *>(cache);
+    return draft_ws_bytes(&v, d->c.n_heads);
+}
+
+// ------------------------------------------------------------ sequencing --
+struct Ctx {
+    const vc_decoder *d;
+    uint8_t *ws;
+    Layout L;
+    cudaStream_t st;
+    int32_t *status() const { return (int32_t *)ws; }
+    template <typename P = void> P *at(size_t off) const { return reinterpret_cast<P *>(ws + off); }
+};
+
+#define VC_TRY(expr)                                \
+    do {                                            \
+        cudaError_t e_ = (expr);                    \
+        if (e_ != cudaSuccess) return e_;           \
+    } while (0)
+
+template <typename T>
+cudaError_t rmsnorm(const Ctx &C, const void *x, int rows, int in_step, int in_off, void *y)
+{
+    rmsnorm_kernel<T><<<rows, kRowThreads, 0, C.st>>>((const T *)x, C.d->c.d_model, in_step, in_off,
+                                                      C.d->c.norm_eps, (T *)y);
+    return cudaGetLastError();
+}
+
+// The MLP and attention-output half of a layer, shared by both passes:
+// x += att Wo; x += silu(x' Wg) (x' Wu) Wd with x' = rmsnorm(x).
+template <typename T>
+cudaError_t layer_tail(const Ctx &C, int l, int M)
+{
+    const vc_decoder_cfg &c = C.d->c;
+    const int qd = c.n_heads * c.head_dim;
+    void *x = C.at(C.L.x), *h = C.at(C.L.h), *part = C.at(C.L.part);
+    VC_TRY(gemm(C.at(C.L.att), C.d->wo[l], x, x, c.dt, M, c.d_model, qd, qd, part, C.status(), C.st));
+    VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
+    VC_TRY(gemm(h, C.d->wgu[l], nullptr, C.at(C.L.gu), c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, part,
+                C.status(), C.st));
+    const size_t n = (size_t)M * c.d_ff;
+    silu_mul_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, C.st>>>(C.at<const T>(C.L.gu), M, c.d_ff,
+                                                                     C.at<T>(C.L.act));
+    VC_TRY(cudaGetLastError());
+    return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.status(), C.st);
+}
+
+template <typename T>
+cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *toks, int tok_stride, int B,
+                         int Dq, const int32_t *ctx, int max_ctx, void *kc, void *vcache, int L_stride, void *kb,
+                         void *vb, int last_only, void *logits)
+{
+    const vc_decoder_cfg &c = C.d->c;
+    const int M = B * Dq;
+    const int hd = c.head_dim, qd = c.n_heads * hd, nqkv = qd + 2 * c.n_kv_heads * hd;
+    const size_t layer_cache = (size_t)B * c.n_kv_heads * L_stride * hd;
+    const size_t layer_blk = (size_t)B * c.n_kv_heads * Dq * hd;
+    void *x = C.at(C.L.x), *h = C.at(C.L.h), *part = C.at(C.L.part);
+    const float scale = 1.0f / sqrtf((float)hd);
+    // the attention's status block sits where other calls keep activations
+    VC_TRY(cudaMemsetAsync(C.at(C.L.vws), 0, kStatusBytes, C.st));
+    embed_kernel<T><<<M, kRowThreads, 0, C.st>>>(first_tok, toks, tok_stride, Dq, (const T *)C.d->embed, c.vocab,
+                                                 c.d_model, (T *)x, C.status());
+    VC_TRY(cudaGetLastError());
+    for (int l = 0; l < c.n_layers; ++l) {
+        VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
+        VC_TRY(gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part, C.status(),
+                    C.st));
+        RopeDst dst;
+        dst.k1 = (T *)kc + l * layer_cache;
+        dst.v1 = (T *)vcache + l * layer_cache;
+        dst.bstride1 = (size_t)c.n_kv_heads * L_stride * hd;
+        dst.stride1 = L_stride;
+        dst.pos1 = 1;
+        dst.k2 = kb ? (void *)((T *)kb + l * layer_blk) : nullptr;
+        dst.v2 = vb ? (void *)((T *)vb + l * layer_blk) : nullptr;
+        dst.bstride2 = (size_t)c.n_kv_heads * Dq * hd;
+        dst.stride2 = Dq;
+        rope_kernel<T><<<M, kRowThreads, 0, C.st>>>(C.at<const T>(C.L.qkv), Dq, c.n_heads, c.n_kv_heads, hd, ctx,
+                                                    c.rope_theta, C.at<T>(C.L.q), dst, C.status());
+        VC_TRY(cudaGetLastError());
+        VC_TRY(verify_attn(C.at(C.L.q), dst.k1, dst.v1, c.dt, ctx, B, Dq, c.n_heads, c.n_kv_heads, hd, L_stride,
+                           max_ctx, scale, C.at(C.L.att), C.at(C.L.vws), C.st, kSplitTiles));
+        VC_TRY(layer_tail<T>(C, l, M));
+    }
+    if (last_only) {
+        VC_TRY(rmsnorm<T>(C, x, B, Dq, Dq - 1, C.at(C.L.hl)));
+        VC_TRY(gemm(C.at(C.L.hl), C.d->head, nullptr, logits, c.dt, B, c.vocab, c.d_model, c.d_model, part,
+                    C.status(), C.st));
+    } else {
+        VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
+        VC_TRY(gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st));
+    }
+    fold_status_kernel<<<1, 1, 0, C.st>>>(C.status(), C.at<int32_t>(C.L.vws), nullptr, nullptr);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *caches, void *logits, int32_t *next_tok,
+                       int32_t *drafts_out, int drafts_stride)
+{
+    const vc_decoder_cfg &c = C.d->c;
+    const int M = B;
+    const int hd = c.head_dim, qd = c.n_heads * hd, kvd = c.n_kv_heads * hd, nqkv = qd + 2 * kvd;
+    void *x = C.at(C.L.x), *h = C.at(C.L.h), *part = C.at(C.L.part);
+    T *kn = C.at<T>(C.L.kvn), *vn = kn + (size_t)B * kvd;
+    const float scale = 1.0f / sqrtf((float)hd);
+    // the draft kernel's status block and arrival counters (zero between its
+    // calls) share the workspace with regions that forward passes overwrite:
+    // clear them first
+    VC_TRY(cudaMemsetAsync(C.at(C.L.dws), 0, kStatusBytes + a256((size_t)B * c.n_kv_heads * 4), C.st));
+    embed_kernel<T><<<M, kRowThreads, 0, C.st>>>(tok, nullptr, 0, 1, (const T *)C.d->embed, c.vocab, c.d_model,
+                                                 (T *)x, C.status());
+    VC_TRY(cudaGetLastError());
+    for (int l = 0; l < c.n_layers; ++l) {
+        VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
+        VC_TRY(gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part, C.status(),
+                    C.st));
+        RopeDst dst;
+        dst.k1 = kn;
+        dst.v1 = vn;
+        dst.bstride1 = (size_t)kvd;
+        dst.stride1 = 1;
+        dst.pos1 = 0;
+        dst.k2 = dst.v2 = nullptr;
+        dst.bstride2 = 0;
+        dst.stride2 = 1;
+        rope_kernel<T><<<M, kRowThreads, 0, C.st>>>(C.at<const T>(C.L.qkv), 1, c.n_heads, c.n_kv_heads, hd,
+                                                    caches[l].seq_len, c.rope_theta, C.at<T>(C.L.q), dst,
+                                                    C.status());
+        VC_TRY(cudaGetLastError());
+        VC_TRY(qcache_append(&caches[l], kn, vn, nullptr, nullptr, nullptr, 1, 0, C.st));
+        vc_cache_view view{};
+        view.kind = VC_CACHE_KIVI;
+        view.kivi = &caches[l];
+        VC_TRY(draft_attn(C.at(C.L.q), c.dt, &view, c.n_heads, scale, C.at(C.L.att), C.at(C.L.dws), C.st));
+        VC_TRY(layer_tail<T>(C, l, M));
+    }
+    VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
+    VC_TRY(gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st));
+    VC_TRY(accept(logits, c.dt, nullptr, B, 0, c.vocab, C.at<int32_t>(C.L.nacc), next_tok, C.at(C.L.aws), C.st));
+    if (drafts_out) {
+        scatter_tokens_kernel<<<(B + 127) / 128, 128, 0, C.st>>>(next_tok, B, drafts_out, drafts_stride);
+        VC_TRY(cudaGetLastError());
+    }
+    fold_status_kernel<<<1, 1, 0, C.st>>>(C.status(), C.at<int32_t>(C.L.dws), nullptr, nullptr);
+    return cudaGetLastError();
+}
+
+vc_status to_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return VC_OK;
+    cudaGetLastError();
+    return e == cudaErrorInvalidValue ? VC_ERR_INVALID : VC_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+}  // namespace vc
+
+using namespace vc;
+
+extern "C" {
+
+vc_status vc_decoder_create(const vc_decoder_cfg *cfg, const vc_decoder_weights *w, vc_decoder **out)
+{
+    if (!cfg || !w || !out) return VC_ERR_INVALID;
+    *out = nullptr;
+    const vc_decoder_cfg &c = *cfg;
+    if (c.n_layers <= 0 || c.d_model <= 0 || c.n_heads <= 0 || c.n_kv_heads <= 0 || c.d_ff <= 0 || c.vocab <= 0)
+        return VC_ERR_INVALID;
+    if (c.dt != VC_BF16 && c.dt != VC_F32) return VC_ERR_INVALID;
+    if (c.n_heads % c.n_kv_heads || c.n_heads / c.n_kv_heads > 4) return VC_ERR_UNSUPPORTED;
+    if (c.head_dim != 64 && c.head_dim != 128) return VC_ERR_UNSUPPORTED;
+    if (c.d_model % 8 || c.d_ff % 8 || c.vocab % 8) return VC_ERR_UNSUPPORTED;
+    if (!(c.norm_eps >= 0.f) || !(c.rope_theta > 0.f)) return VC_ERR_INVALID;
+    if (!w->embed || !w->lm_head || !w->w_qkv || !w->w_o || !w->w_gate_up || !w->w_down) return VC_ERR_INVALID;
+    if (!aligned16(w->embed) || !aligned16(w->lm_head)) return VC_ERR_INVALID;
+    vc_decoder *d = new (std::nothrow) vc_decoder;
+    if (!d) return VC_ERR_INVALID;
+    d->c = c;
+    d->embed = w->embed;
+    d->head = w->lm_head;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const void *p[4] = {w->w_qkv[l], w->w_o[l], w->w_gate_up[l], w->w_down[l]};
+        for (const void *q : p)
+            if (!q || !aligned16(q)) {
+                delete d;
+                return VC_ERR_INVALID;
+            }
+        d->wqkv.push_back(p[0]);
+        d->wo.push_back(p[1]);
+        d->wgu.push_back(p[2]);
+        d->wd.push_back(p[3]);
+    }
+    *out = d;
+    return VC_OK;
+}
+
+void vc_decoder_destroy(vc_decoder *dec) { delete dec; }
+
+size_t vc_decoder_workspace_bytes(const vc_decoder *dec, int B, int max_rows, int max_ctx,
+                                  const vc_qcache *draft_cache)
+{
+    if (!dec || B <= 0 || max_rows <= 0 || max_ctx < 0) return 0;
+    return layout_of(dec, B, max_rows, max_ctx, draft_ws_of(dec, draft_cache)).total;
+}
+
+vc_status vc_decoder_forward(const vc_decoder *dec, const int32_t *first_tok, const int32_t *tokens,
+                             int tok_stride, int B, int Dq, const int32_t *ctx_len, int max_ctx,
+                             void *k_cache, void *v_cache, int L_stride, void *k_blk, void *v_blk,
+                             int logits_last_only, void *logits, void *ws, size_t ws_bytes,
+                             cudaStream_t stream)
+{
+    if (!dec || !ctx_len || !k_cache || !v_cache || !logits || !ws) return VC_ERR_INVALID;
+    if (B <= 0 || Dq <= 0 || max_ctx < 0 || L_stride < max_ctx + Dq) return VC_ERR_INVALID;
+    if ((k_blk == nullptr) != (v_blk == nullptr)) return VC_ERR_INVALID;
+    if (!first_tok && !tokens) return VC_ERR_INVALID;
+    if (tokens && tok_stride < (first_tok ? Dq - 1 : Dq)) return VC_ERR_INVALID;
+    if (first_tok && !tokens && Dq > 1) return VC_ERR_INVALID;
+    if (((uintptr_t)ws & 255u) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(logits))
+        return VC_ERR_INVALID;
+    const Layout L = layout_of(dec, B, Dq, max_ctx, 0);
+    if (ws_bytes < L.total) return VC_ERR_INVALID;
+    Ctx C{dec, (uint8_t *)ws, L, stream};
+    const cudaError_t e =
+        dec->c.dt == VC_BF16
+            ? forward_impl<__nv_bfloat16>(C, first_tok, tokens, tok_stride, B, Dq, ctx_len, max_ctx, k_cache, v_cache,
+                                          L_stride, k_blk, v_blk, logits_last_only, logits)
+            : forward_impl<float>(C, first_tok, tokens, tok_stride, B, Dq, ctx_len, max_ctx, k_cache, v_cache,
+                                  L_stride, k_blk, v_blk, logits_last_only, logits);
+    return to_status(e);
+}
+
+vc_status vc_decoder_draft_step(const vc_decoder *dec, const int32_t *tok, int B, vc_qcache *caches,
+                                void *logits, int32_t *next_tok, int32_t *drafts_out, int drafts_stride,
+                                void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!dec || !tok || !caches || !logits || !next_tok || !ws || B <= 0) return VC_ERR_INVALID;
+    if (drafts_out && drafts_stride <= 0) return VC_ERR_INVALID;
+    if (((uintptr_t)ws & 255u) || !aligned16(logits)) return VC_ERR_INVALID;
+    const vc_decoder_cfg &c = dec->c;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const vc_qcache &q = caches[l];
+        if (!q.records || !q.k_res || !q.v_res || !q.n_groups || !q.seq_len) return VC_ERR_INVALID;
+        if (q.B != B || q.Hkv != c.n_kv_heads || q.d != c.head_dim || q.res_dtype != c.dt) return VC_ERR_INVALID;
+        if (q.max_groups != caches[0].max_groups || q.res_cap != caches[0].res_cap ||
+            q.cfg.bits != caches[0].cfg.bits || q.cfg.residual != caches[0].cfg.residual)
+            return VC_ERR_INVALID;
+    }
+    const Layout L = layout_of(dec, B, 1, 0, draft_ws_of(dec, &caches[0]));
+    if (ws_bytes < L.total) return VC_ERR_INVALID;
+    Ctx C{dec, (uint8_t *)ws, L, stream};
+    const cudaError_t e =
+        c.dt == VC_BF16
+            ? draft_impl<__nv_bfloat16>(C, tok, B, caches, logits, next_tok, drafts_out, drafts_stride)
+            : draft_impl<float>(C, tok, B, caches, logits, next_tok, drafts_out, drafts_stride);
+    return to_status(e);
+}
+
+vc_status vc_kv_writeback(const void *k_blk, const void *v_blk, vc_dtype dt, int n_layers, int B, int Hkv, int Dq,
+                          int d, const int32_t *n_acc, const int32_t *ctx_len, void *k_host, void *v_host,
+                          int L_stride, cudaStream_t stream)
+{
+    if (!k_blk || !v_blk || !n_acc || !ctx_len || !k_host || !v_host) return VC_ERR_INVALID;
+    if ((dt != VC_BF16 && dt != VC_F32) || n_layers <= 0 || B <= 0 || Hkv <= 0 || Dq <= 0 || d <= 0 ||
+        L_stride < Dq)
+        return VC_ERR_INVALID;
+    void *kd = nullptr, *vd = nullptr;
+    if (cudaHostGetDevicePointer(&kd, k_host, 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&vd, v_host, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return VC_ERR_INVALID;
+    }
+    dim3 grid(Dq, B * Hkv, n_layers);
+    if (dt == VC_BF16)
+        writeback_kernel<__nv_bfloat16><<<grid, 64, 0, stream>>>(
+            (const __nv_bfloat16 *)k_blk, (const __nv_bfloat16 *)v_blk, B, Hkv, Dq, d, n_acc, ctx_len,
+            (__nv_bfloat16 *)kd, (__nv_bfloat16 *)vd, L_stride);
+    else
+        writeback_kernel<float><<<grid, 64, 0, stream>>>((const float *)k_blk, (const float *)v_blk, B, Hkv, Dq, d,
+                                                         n_acc, ctx_len, (float *)kd, (float *)vd, L_stride);
+    return to_status(cudaGetLastError());
+}
+
+size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K)
+{
+    if ((dt != VC_BF16 && dt != VC_F32) || M <= 0 || N <= 0 || K <= 0) return 0;
+    return gemm_ws_bytes(dt, M, N, K);
+}
+
+vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
+                  void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!x || !w || !out || (dt != VC_BF16 && dt != VC_F32) || M <= 0 || N <= 0 || K <= 0) return VC_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (resid && !aligned16(resid))) return VC_ERR_INVALID;
+    const size_t need = gemm_ws_bytes(dt, M, N, K);
+    if (need && (!ws || ws_bytes < need || !aligned16(ws))) return VC_ERR_INVALID;
+    return to_status(gemm(x, w, resid, out, dt, M, N, K, K, ws, nullptr, stream));
+}
+
+}  // extern "C"

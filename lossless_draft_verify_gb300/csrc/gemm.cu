@@ -1,0 +1,321 @@
+// gemm.cu -- the decoder's dense projections, y = x W (+ r), with row results
+// that do not depend on how many rows share the launch.
+//
+// The draft-and-verify loop is lossless only if the verify pass over a block
+// of D+1 tokens computes, for every token, exactly what one-token decoding
+// computes (paper page, "What the paper found": outputs identical to full-KV
+// greedy decoding; the thelatestinai page shows how far batch-dependent
+// floating-point order drifts KV-cached decoding).  Both kernels here fix the
+// summation order of every output element from the shapes (K, N) and the
+// device alone: the split of K, the order of the splits and the order inside
+// a split never depend on M.
+//
+// bf16 (x [M][K] and W [K][N] row-major, N a multiple of 128, K of 64):
+// tcgen05 tensor cores.  One CTA per (128-row tile, 128-column tile, K split):
+// warp 0 issues TMA loads of 64-wide K slices (x K-major, W MN-major, 128-byte
+// swizzle) into a 4-stage ring, warp 1 issues tcgen05.mma (M128 N128 K16)
+// into a TMEM accumulator, warps 2-5 read TMEM and write either the output
+// (one split) or fp32 partials that a second kernel sums in split order.
+// fp32 (any shape): CUDA cores, one output element per thread, K in order.
+#include <cuda.h>
+
+#include "tcgen05.cuh"
+#include "vc_common.cuh"
+#include "vc_internal.h"
+
+namespace vc {
+namespace {
+
+constexpr int GM = 128, GN = 128, GK = 64, GSTAGES = 4;
+constexpr int G_THREADS = 192;
+constexpr int G_STAGE_BYTES = GM * GK * 2 + GK * GN * 2;     // 16 KB x + 16 KB W
+constexpr int G_SMEM = GSTAGES * G_STAGE_BYTES + 256;
+constexpr uint32_t G_TMEM_COLS = 128;
+
+struct GemmBars {
+    uint64_t full[GSTAGES], empty[GSTAGES], acc_full;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+};
+
+struct GemmArgs {
+    float *part;                 // [S][M][N] fp32, used when S > 1
+    __nv_bfloat16 *out;          // [M][N]
+    const __nv_bfloat16 *resid;  // [M][N] or null (may equal out)
+    int32_t *status;
+    int M, N, K, S, kb_per_split;
+};
+
+__device__ __forceinline__ bool g_wait(uint64_t *bar, uint32_t parity, GemmBars *B, int32_t *status, int where)
+{
+    if (mbar_wait(bar, parity)) return true;
+    report_timeout(status, where);
+    atomicExch(&B->abort_flag, 1);
+    return false;
+}
+
+__global__ void __launch_bounds__(G_THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, GemmArgs A)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = smem_raw;
+    if (smem_u32(sm) & 1023u) {
+        if (threadIdx.x == 0) report_timeout(A.status, 98);
+        return;
+    }
+    GemmBars *B = reinterpret_cast<GemmBars *>(sm + GSTAGES * G_STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * GM;
+    const int n0 = blockIdx.y * GN;
+    const int split = blockIdx.z;
+    const int nkb = A.K / GK;
+    const int kb0 = split * A.kb_per_split;
+    const int kb1 = min(nkb, kb0 + A.kb_per_split);
+    const int n = kb1 - kb0;                       // >= 1 by construction of S
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GSTAGES; ++s) {
+            mbar_init(&B->full[s], 1);
+            mbar_init(&B->empty[s], 1);
+        }
+        mbar_init(&B->acc_full, 1);
+        B->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&B->tmem_base, G_TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = B->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmX);
+            tc::prefetch_tmap(&tmW);
+            for (int i = 0; i < n; ++i) {
+                const int s = i % GSTAGES;
+                if (i >= GSTAGES && !g_wait(&B->empty[s], ((i / GSTAGES) - 1) & 1, B, A.status, 41)) break;
+                if (*reinterpret_cast<volatile int32_t *>(&B->abort_flag)) break;
+                uint8_t *sx = sm + s * G_STAGE_BYTES;
+                uint8_t *sw = sx + GM * GK * 2;
+                const int k = (kb0 + i) * GK;
+                mbar_arrive_expect_tx(&B->full[s], G_STAGE_BYTES);
+                tc::tma_load_3d(sx, &tmX, k, m0, 0, &B->full[s]);
+                tc::tma_load_3d(sw, &tmW, n0, k, 0, &B->full[s]);
+                tc::tma_load_3d(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_bf16(GM, GN, false, true);
+            bool ok = true;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % GSTAGES;
+                if (!g_wait(&B->full[s], (i / GSTAGES) & 1, B, A.status, 42)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t sx = smem_u32(sm + s * G_STAGE_BYTES);
+                const uint32_t sw = sx + GM * GK * 2;
+#pragma unroll
+                for (int kk = 0; kk < GK / 16; ++kk) {
+                    // x: K-major rows of 128 B, 8-row atoms 1024 B apart
+                    const uint64_t ad = tc::smem_desc(sx + kk * 32, 16, 1024, tc::kSwizzle128B);
+                    // W: MN-major; 64-column halves GK*128 B apart, 8 K-rows 1024 B apart
+                    const uint64_t bd = tc::smem_desc(sw + kk * 2048, GK * 128, 1024, tc::kSwizzle128B);
+                    tc::mma_ss(tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(&B->empty[s]);
+            }
+            if (ok) tc::commit(&B->acc_full);
+        }
+    } else {
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const int m = m0 + r;
+        const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
+        const bool ok = g_wait(&B->acc_full, 0, B, A.status, 43);
+        if (ok) {
+            tc::fence_after();
+#pragma unroll 1
+            for (int h = 0; h < GN / 32; ++h) {
+                uint32_t u[32];
+                tc::ld32(taddr + h * 32, u);
+                tc::ld_wait();
+                if (m < A.M) {
+                    const int c0 = n0 + h * 32;
+                    if (A.S > 1) {
+                        float *dst = A.part + ((size_t)split * A.M + m) * A.N + c0;
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4)
+                            *reinterpret_cast<float4 *>(dst + c) =
+                                make_float4(__uint_as_float(u[c]), __uint_as_float(u[c + 1]),
+                                            __uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
+                    } else {
+                        const size_t off = (size_t)m * A.N + c0;
+                        uint32_t packed[16];
+                        if (A.resid) {
+                            const uint4 *rp = reinterpret_cast<const uint4 *>(A.resid + off);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint4 rv = rp[q];
+                                const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int c = q * 8 + e * 2;
+                                    const float a = __uint_as_float(u[c]) + bf16_lo(w4[e]);
+                                    const float b = __uint_as_float(u[c + 1]) + bf16_hi(w4[e]);
+                                    __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+                                    packed[c / 2] = *reinterpret_cast<uint32_t *>(&h2);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 32; c += 2) {
+                                __nv_bfloat162 h2 =
+                                    __floats2bfloat162_rn(__uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+                                packed[c / 2] = *reinterpret_cast<uint32_t *>(&h2);
+                            }
+                        }
+                        uint4 *op = reinterpret_cast<uint4 *>(A.out + off);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            op[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    }
+                }
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) {
+        __syncwarp();
+        tc::tmem_dealloc(tmem, G_TMEM_COLS);
+    }
+}
+
+// out[m][n] = bf16(sum_s part[s][m][n] (s in order) + resid[m][n]); 4 columns a thread.
+__global__ void gemm_splitk_reduce(const float *__restrict__ part, int S, int M, int N,
+                                   const __nv_bfloat16 *resid, __nv_bfloat16 *out)
+{
+    const size_t i4 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t total = (size_t)M * N;
+    const size_t i = i4 * 4;
+    if (i >= total) return;
+    float4 acc = *reinterpret_cast<const float4 *>(part + i);
+    for (int s = 1; s < S; ++s) {
+        const float4 p = *reinterpret_cast<const float4 *>(part + (size_t)s * total + i);
+        acc.x += p.x;
+        acc.y += p.y;
+        acc.z += p.z;
+        acc.w += p.w;
+    }
+    if (resid) {
+        const uint2 r = *reinterpret_cast<const uint2 *>(resid + i);
+        acc.x += bf16_lo(r.x);
+        acc.y += bf16_hi(r.x);
+        acc.z += bf16_lo(r.y);
+        acc.w += bf16_hi(r.y);
+    }
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t *>(&a);
+    o.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(out + i) = o;
+}
+
+// CUDA-core GEMM: one output element per thread, K summed strictly in order
+// (16 x 16 tiles staged through shared memory).
+template <typename T>
+__global__ void __launch_bounds__(256)
+gemm_simt_kernel(const T *__restrict__ x, const T *__restrict__ w, const T *resid, T *out, int M, int N, int K)
+{
+    __shared__ float sx[16][17], sw[16][17];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int m = blockIdx.y * 16 + ty, n = blockIdx.x * 16 + tx;
+    float acc = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        const int kx = k0 + tx, kw = k0 + ty;
+        sx[ty][tx] = (m < M && kx < K) ? Elem<T>::to_f(x[(size_t)m * K + kx]) : 0.f;
+        sw[ty][tx] = (kw < K && n < N) ? Elem<T>::to_f(w[(size_t)kw * N + n]) : 0.f;
+        __syncthreads();
+        const int kn = min(16, K - k0);
+        for (int k = 0; k < kn; ++k) acc = fmaf(sx[ty][k], sw[k][tx], acc);
+        __syncthreads();
+    }
+    if (m < M && n < N) {
+        const size_t o = (size_t)m * N + n;
+        if (resid) acc += Elem<T>::to_f(resid[o]);
+        out[o] = Elem<T>::from_f(acc);
+    }
+}
+
+}  // namespace
+
+bool gemm_uses_tensor_cores(vc_dtype dt, int N, int K)
+{
+    return dt == VC_BF16 && N % GN == 0 && K % GK == 0 && K > 0;
+}
+
+// The K split depends on (N, K) and the device only: enough CTAs to cover the
+// SMs when M is at most one row tile, and at least 8 K-slices per split.
+int gemm_splits(int N, int K)
+{
+    const int ntiles = N / GN, nkb = K / GK;
+    int s = (device_sm_count() + ntiles - 1) / ntiles;
+    s = max(1, min(s, nkb / 8));
+    const int per = (nkb + s - 1) / s;
+    return (nkb + per - 1) / per;
+}
+
+size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K)
+{
+    if (!gemm_uses_tensor_cores(dt, N, K)) return 0;
+    const int S = gemm_splits(N, K);
+    return S > 1 ? (size_t)S * M * N * 4 : 0;
+}
+
+cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
+                 int ldx, void *ws, int32_t *status, cudaStream_t st)
+{
+    if (M <= 0) return cudaSuccess;
+    if (gemm_uses_tensor_cores(dt, N, K)) {
+        CUtensorMap mx, mw;
+        if (!tma_map_bf16_3d(&mx, x, K, M, 1, (uint64_t)ldx * 2, (uint64_t)ldx * 2 * M, GK, GM, 1) ||
+            !tma_map_bf16_3d(&mw, w, N, K, 1, (uint64_t)N * 2, (uint64_t)N * 2 * K, 64, GK, 1))
+            return cudaErrorInvalidValue;
+        GemmArgs A;
+        A.S = gemm_splits(N, K);
+        const int nkb = K / GK;
+        A.kb_per_split = (nkb + A.S - 1) / A.S;
+        A.part = (float *)ws;
+        A.out = (__nv_bfloat16 *)out;
+        A.resid = (const __nv_bfloat16 *)resid;
+        A.status = status;
+        A.M = M;
+        A.N = N;
+        A.K = K;
+        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
+        dim3 grid((M + GM - 1) / GM, N / GN, A.S);
+        gemm_tc_kernel<<<grid, G_THREADS, G_SMEM, st>>>(mx, mw, A);
+        if (A.S > 1) {
+            const size_t q = (size_t)M * N / 4;
+            gemm_splitk_reduce<<<(unsigned)((q + 255) / 256), 256, 0, st>>>(A.part, A.S, M, N, A.resid, A.out);
+        }
+        return cudaGetLastError();
+    }
+    if (ldx != K) return cudaErrorInvalidValue;
+    dim3 grid((N + 15) / 16, (M + 15) / 16);
+    if (dt == VC_BF16)
+        gemm_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w,
+                                                               (const __nv_bfloat16 *)resid, (__nv_bfloat16 *)out,
+                                                               M, N, K);
+    else
+        gemm_simt_kernel<float><<<grid, 256, 0, st>>>((const float *)x, (const float *)w, (const float *)resid,
+                                                       (float *)out, M, N, K);
+    return cudaGetLastError();
+}
+
+}  // namespace vc

@@ -236,7 +236,7 @@ __global__ void residual_copy_kernel(const T *__restrict__ k, const T *__restric
 // left the residual window.  One CTA per sequence handles all its kv heads, so
 // the lengths of sequence b are read and written by exactly one CTA.
 // Commit mode (len_base, n_acc non-null): roll back to len_base[b] and take
-// n_acc[b] + 1 rows.
+// n_acc[b] + 1 rows.  With n_new null every sequence takes max_new rows.
 template <typename T, int BITS, int D>
 __global__ void __launch_bounds__(2 * D)
 append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
@@ -254,7 +254,7 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
         if (threadIdx.x == 0 && status) atomicOr(status, 2);
         len0 = ng0 * G;
     }
-    int nn = n_acc ? n_acc[b] + 1 : n_new[b];
+    int nn = n_acc ? n_acc[b] + 1 : (n_new ? n_new[b] : max_new);
     nn = nn < 0 ? 0 : (nn > max_new ? max_new : nn);
     // unquantized tokens after the append must fit the ring
     const int room = res_cap - (len0 - ng0 * G);

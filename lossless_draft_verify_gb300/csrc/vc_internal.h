@@ -2,6 +2,7 @@
 // entry points (vc_api.cu).  Arguments are validated by the caller.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,17 +28,33 @@ cudaError_t draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view, 
                        float sm_scale, void *out, void *ws, cudaStream_t st);
 
 // verify_attn.cu
-size_t verify_ws_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int max_ctx);
+// split_tiles > 0: fixed key splits of split_tiles x 64 keys (row results then
+// do not depend on B or Dq); 0: splits chosen to fill the GPU.
+size_t verify_ws_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int max_ctx, int split_tiles = 0);
 bool verify_uses_tensor_cores(vc_dtype dt, int Dq, int Hq, int Hkv, int d);
 cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt,
                         const int32_t *ctx_len, int B, int Dq, int Hq, int Hkv, int d,
                         int L_stride, int max_ctx, float sm_scale, void *out, void *ws,
-                        cudaStream_t st);
+                        cudaStream_t st, int split_tiles = 0);
 
 // drop.cu
 size_t drop_ws_bytes(int B, int H, int L);
 cudaError_t drop_tokens(const float *scores, const void *k, const void *v, vc_dtype dt, int B,
                         int H, int L, int d, int64_t keep_top, int64_t keep_recent,
                         int32_t *kept_idx, void *k_out, void *v_out, void *ws, cudaStream_t st);
+
+// gemm.cu: y = x W (+ resid), x [M][ldx] (first K columns), W [K][N], rows
+// independent of M.  ws: gemm_ws_bytes bytes of fp32 partials (bf16 path).
+bool gemm_uses_tensor_cores(vc_dtype dt, int N, int K);
+int gemm_splits(int N, int K);
+size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K);
+cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
+                 int ldx, void *ws, int32_t *status, cudaStream_t st);
+
+// host_util.cu
+int device_sm_count();
+// 3-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+bool tma_map_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                     uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 
 }  // namespace vc

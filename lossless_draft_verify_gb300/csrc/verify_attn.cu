@@ -476,51 +476,13 @@ verify_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 }
 
 // ================================================================== host ===
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-bool make_map_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-                 uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-    const cuuint32_t box[3] = {b0, b1, b2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int num_sms()
-{
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
-    }
-    return n;
-}
-
 struct TcPlan {
     int n_mtiles, mt_per_cta, n_cta_m, n_split, tiles_per_split;
 };
 
-TcPlan tc_plan(int B, int Dq, int Hkv, int grp, int max_ctx)
+// split_tiles > 0 fixes the number of 64-key tiles per split, so that the
+// split boundaries of a row depend on nothing but key positions.
+TcPlan tc_plan(int B, int Dq, int Hkv, int grp, int max_ctx, int split_tiles)
 {
     TcPlan p;
     p.n_mtiles = (Dq * grp + TC_M - 1) / TC_M;
@@ -533,12 +495,13 @@ TcPlan tc_plan(int B, int Dq, int Hkv, int grp, int max_ctx)
     const int tiles = (max_ctx + Dq + TC_N - 1) / TC_N;
     const int items = B * Hkv * p.n_cta_m;
     const int per_sm = p.mt_per_cta == 1 ? 2 : 1;
-    const int target = num_sms() * per_sm * 3;       // ~3 waves of resident CTAs
+    const int target = device_sm_count() * per_sm * 3;       // ~3 waves of resident CTAs
     int s = (target + items - 1) / items;
     if (s > tiles) s = tiles;
     if (s < 1) s = 1;
     p.tiles_per_split = (tiles + s - 1) / s;
     if (p.tiles_per_split < 2 && tiles >= 2) p.tiles_per_split = 2;
+    if (split_tiles > 0) p.tiles_per_split = split_tiles;
     p.n_split = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
     return p;
 }
@@ -551,27 +514,27 @@ bool verify_uses_tensor_cores(vc_dtype dt, int Dq, int Hq, int Hkv, int d)
     return dt == VC_BF16 && d == TC_D && (grp == 1 || grp == 2 || grp == 4 || grp == 8) && Dq >= 1;
 }
 
-size_t verify_ws_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int max_ctx)
+size_t verify_ws_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int max_ctx, int split_tiles)
 {
     if (!verify_uses_tensor_cores(dt, Dq, Hq, Hkv, d)) return kStatusBytes;
-    const TcPlan p = tc_plan(B, Dq, Hkv, Hq / Hkv, max_ctx);
+    const TcPlan p = tc_plan(B, Dq, Hkv, Hq / Hkv, max_ctx, split_tiles);
     return kStatusBytes + align256((size_t)B * Hkv * p.n_mtiles * p.n_split * TC_M * TC_PART * 4);
 }
 
 cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt, const int32_t *ctx_len,
                         int B, int Dq, int Hq, int Hkv, int d, int L_stride, int max_ctx, float sm_scale,
-                        void *out, void *ws, cudaStream_t st)
+                        void *out, void *ws, cudaStream_t st, int split_tiles)
 {
     const float sl2 = sm_scale * kLog2e;
     if (verify_uses_tensor_cores(dt, Dq, Hq, Hkv, d)) {
         const int grp = Hq / Hkv;
-        const TcPlan pl = tc_plan(B, Dq, Hkv, grp, max_ctx);
+        const TcPlan pl = tc_plan(B, Dq, Hkv, grp, max_ctx, split_tiles);
         CUtensorMap mq, mk, mv;
-        if (!make_map_3d(&mq, q, TC_D, Hq, (uint64_t)B * Dq, (uint64_t)TC_D * 2, (uint64_t)Hq * TC_D * 2, 64,
+        if (!tma_map_bf16_3d(&mq, q, TC_D, Hq, (uint64_t)B * Dq, (uint64_t)TC_D * 2, (uint64_t)Hq * TC_D * 2, 64,
                          grp, TC_M / grp) ||
-            !make_map_3d(&mk, k, TC_D, L_stride, (uint64_t)B * Hkv, (uint64_t)TC_D * 2,
+            !tma_map_bf16_3d(&mk, k, TC_D, L_stride, (uint64_t)B * Hkv, (uint64_t)TC_D * 2,
                          (uint64_t)L_stride * TC_D * 2, 64, TC_N, 1) ||
-            !make_map_3d(&mv, v, TC_D, L_stride, (uint64_t)B * Hkv, (uint64_t)TC_D * 2,
+            !tma_map_bf16_3d(&mv, v, TC_D, L_stride, (uint64_t)B * Hkv, (uint64_t)TC_D * 2,
                          (uint64_t)L_stride * TC_D * 2, 64, TC_N, 1))
             return cudaErrorInvalidValue;
         TcParams P;

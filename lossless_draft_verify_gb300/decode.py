@@ -1,0 +1,202 @@
+"""Host-side sequencing of VeriCache decoding on one GPU: prefill, plain
+full-KV greedy decoding, and draft-and-verify rounds.
+
+Every computation is a call into libvc.so (vc.py); this module only orders
+the calls on CUDA streams and moves bookkeeping tensors with plain copies
+(paper page, "What the paper found": draft on the compressed cache, swap the
+full cache in from host memory at the same time, verify the drafted block on
+the full cache, keep the longest prefix that matches).
+
+A round for B sequences whose pending token x sits at position P (its K/V
+not yet cached):
+  1. the full cache is copied in from pinned host memory on a side stream
+     (when the cache lives on the host);
+  2. D draft steps on the compressed per-layer caches, each appending the
+     input's K/V to the ring and producing the greedy draft token;
+  3. one forward of [x, d1..dD] at positions P..P+D over the full cache (the
+     verify pass, waiting for the copy), writing the block's K/V;
+  4. acceptance: n = longest prefix with argmax(row i) == d(i+1), next =
+     argmax(row n);
+  5. the compressed caches roll back to P and take the verify pass's K/V of
+     the n + 1 committed rows (re-quantized); the host copy of the full cache
+     receives the same rows.
+The round emits d1..dn and next.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import vc
+
+
+@dataclasses.dataclass
+class RoundLog:
+    drafts: torch.Tensor        # [R][B][D] int32 (device)
+    n_acc: torch.Tensor         # [R][B]
+    nxt: torch.Tensor           # [R][B]
+
+    def tokens(self) -> list[list[int]]:
+        """Emitted tokens per sequence (host lists), in order."""
+        d, n, x = self.drafts.cpu(), self.n_acc.cpu(), self.nxt.cpu()
+        R, B, _ = d.shape
+        out = [[] for _ in range(B)]
+        for r in range(R):
+            for b in range(B):
+                k = int(n[r, b])
+                out[b].extend(int(t) for t in d[r, b, :k])
+                out[b].append(int(x[r, b]))
+        return out
+
+    def accepted(self) -> list[list[int]]:
+        return self.n_acc.cpu().t().tolist()
+
+
+class VeriCacheRunner:
+    """Caches, workspaces and buffers of one decoding job (B sequences)."""
+
+    def __init__(self, dec: vc.Decoder, B: int, max_len: int, horizon: int, bits: int = 2, group: int = 32,
+                 residual: int = 128, host_cache: bool = False, prefill_chunk: int = 512, device="cuda"):
+        cfg = dec.cfg
+        self.dec, self.B, self.D, self.device = dec, B, horizon, device
+        self.dtype = dec.dtype
+        self.L_stride = max_len + horizon + 1
+        nl, hkv, hd = cfg.n_layers, cfg.n_kv_heads, cfg.head_dim
+        shape = (nl, B, hkv, self.L_stride, hd)
+        self.k_full = torch.zeros(shape, dtype=self.dtype, device=device)
+        self.v_full = torch.zeros_like(self.k_full)
+        self.host_cache = host_cache
+        if host_cache:
+            self.k_host = torch.zeros(shape, dtype=self.dtype).pin_memory()
+            self.v_host = torch.zeros(shape, dtype=self.dtype).pin_memory()
+        maxg = self.L_stride // group + 1
+        res_cap = ((residual + group + horizon + 1 + 15) // 16) * 16
+        self.qc = [vc.QCache(B, hkv, hd, bits, maxg, res_cap, residual, group=group, res_dtype=self.dtype,
+                             device=device) for _ in range(nl)]
+        self.qc_arr = vc.qcache_array(self.qc)
+        self.k_blk = torch.zeros(nl, B, hkv, horizon + 1, hd, dtype=self.dtype, device=device)
+        self.v_blk = torch.zeros_like(self.k_blk)
+        self.prefill_chunk = prefill_chunk
+        rows = max(prefill_chunk, horizon + 1)
+        self.ws = vc.Workspace(dec.workspace_bytes(B, rows, self.L_stride - rows, self.qc[0]), device=device)
+        self.logits_d = torch.zeros(B, cfg.vocab, dtype=self.dtype, device=device)
+        self.logits_v = torch.zeros(B, horizon + 1, cfg.vocab, dtype=self.dtype, device=device)
+        self.ws_acc = vc.Workspace(vc.vc_accept_workspace_bytes(B, horizon, cfg.vocab), device=device)
+        self.x = torch.zeros(B, dtype=torch.int32, device=device)          # pending token
+        self.next_d = torch.zeros(B, dtype=torch.int32, device=device)
+        self.drafts = torch.zeros(B, horizon, dtype=torch.int32, device=device)
+        self.n_acc = torch.zeros(B, dtype=torch.int32, device=device)
+        self.round_len = torch.zeros(B, dtype=torch.int32, device=device)
+        self.ctx = torch.zeros(B, dtype=torch.int32, device=device)
+        self.ctx_bound = 0
+        self.side = torch.cuda.Stream(device=device)
+        self.ev_swap = torch.cuda.Event()
+
+    # ------------------------------------------------------------ prefill --
+    def prefill(self, prompt: torch.Tensor):
+        """prompt: [B][P] int32 on the device.  Fills the full cache (and its
+        host copy), quantizes it into the draft caches, sets the pending
+        token to the greedy continuation."""
+        B, P = prompt.shape
+        assert B == self.B and P + 1 <= self.L_stride
+        prompt = prompt.to(torch.int32).contiguous()
+        C = self.prefill_chunk
+        starts = list(range(0, P, C))
+        ctxs = torch.tensor([[s] * B for s in starts], dtype=torch.int32, device=self.device)
+        last = torch.zeros(B, self.dec.cfg.vocab, dtype=self.dtype, device=self.device)
+        for ci, s in enumerate(starts):
+            n = min(C, P - s)
+            vc.vc_decoder_forward(self.dec, None, prompt[:, s:], P, B, n, ctxs[ci], s, self.k_full, self.v_full,
+                                  last, self.ws, last_only=True)
+        vc.vc_accept(last.view(B, 1, -1), None, self.n_acc, self.x, self.ws_acc)
+        for l, q in enumerate(self.qc):
+            vc.vc_quantize_kv(self.k_full[l], self.v_full[l], q, L=P)
+        if self.host_cache:
+            self.k_host.copy_(self.k_full)
+            self.v_host.copy_(self.v_full)
+        self.ctx.fill_(P)
+        self.ctx_bound = P
+        return self.x
+
+    # ------------------------------------------------------- plain greedy --
+    def greedy(self, n_new: int) -> list[list[int]]:
+        """Plain full-KV greedy decoding from the pending token: n_new tokens
+        per sequence, the first being the pending token itself."""
+        B = self.B
+        out = torch.zeros(n_new, B, dtype=torch.int32, device=self.device)
+        out[0].copy_(self.x)
+        for t in range(1, n_new):
+            vc.vc_decoder_forward(self.dec, self.x, None, 0, B, 1, self.ctx, self.ctx_bound, self.k_full,
+                                  self.v_full, self.logits_d, self.ws, last_only=True)
+            vc.vc_accept(self.logits_d.view(B, 1, -1), None, self.n_acc, self.x, self.ws_acc)
+            out[t].copy_(self.x)
+            self.ctx += 1
+            self.ctx_bound += 1
+        return out.t().cpu().tolist()
+
+    # --------------------------------------------------- draft and verify --
+    def round(self, log: RoundLog | None = None, r: int = 0, ev: dict | None = None):
+        """One draft-and-verify round (enqueued; no host synchronization)."""
+        B, D = self.B, self.D
+        main = torch.cuda.current_stream()
+        self.round_len.copy_(self.qc[0].seq_len)
+        if self.host_cache:
+            self.side.wait_stream(main)
+            if ev is not None:
+                ev["swap0"].record(self.side)
+            vc.vc_swap_in(self.k_full, self.k_host, stream=self.side)
+            vc.vc_swap_in(self.v_full, self.v_host, stream=self.side, done_event=self.ev_swap)
+            if ev is not None:
+                ev["swap1"].record(self.side)
+        if ev is not None:
+            ev["d0"].record(main)
+        tok = self.x
+        for j in range(D):
+            vc.vc_decoder_draft_step(self.dec, tok, self.qc_arr, self.logits_d, self.next_d, self.ws,
+                                     drafts_out=self.drafts[:, j], drafts_stride=D)
+            tok = self.next_d
+        if ev is not None:
+            ev["d1"].record(main)
+        if self.host_cache:
+            main.wait_event(self.ev_swap)
+        max_ctx = min(self.ctx_bound, self.L_stride - (D + 1))
+        vc.vc_decoder_forward(self.dec, self.x, self.drafts, D, B, D + 1, self.round_len, max_ctx, self.k_full,
+                              self.v_full, self.logits_v, self.ws, k_blk=self.k_blk, v_blk=self.v_blk)
+        if ev is not None:
+            ev["v1"].record(main)
+        vc.vc_accept(self.logits_v, self.drafts, self.n_acc, self.x, self.ws_acc)
+        for l, q in enumerate(self.qc):
+            vc.vc_qcache_commit(q, self.k_blk[l], self.v_blk[l], self.round_len, self.n_acc)
+        if self.host_cache:
+            vc.vc_kv_writeback(self.k_blk, self.v_blk, self.n_acc, self.round_len, self.k_host, self.v_host)
+        if ev is not None:
+            ev["c1"].record(main)
+        if log is not None:
+            log.drafts[r].copy_(self.drafts)
+            log.n_acc[r].copy_(self.n_acc)
+            log.nxt[r].copy_(self.x)
+        self.ctx_bound += D + 1
+
+    def new_log(self, rounds: int) -> RoundLog:
+        B, D = self.B, self.D
+        z = lambda *s: torch.zeros(*s, dtype=torch.int32, device=self.device)
+        return RoundLog(z(rounds, B, D), z(rounds, B), z(rounds, B))
+
+    def generate(self, n_new: int, max_rounds: int | None = None) -> tuple[list[list[int]], list[list[int]]]:
+        """Draft-and-verify until every sequence has n_new tokens (the first
+        being the pending token after prefill).  Returns (tokens, accepted
+        lengths per round) per sequence."""
+        first = self.x.cpu().tolist()
+        max_rounds = max_rounds or n_new
+        log = self.new_log(max_rounds)
+        have = [1] * self.B
+        r = 0
+        while min(have) < n_new and r < max_rounds:
+            self.round(log, r)
+            na = log.n_acc[r].cpu().tolist()
+            have = [h + k + 1 for h, k in zip(have, na)]
+            r += 1
+        used = RoundLog(log.drafts[:r], log.n_acc[:r], log.nxt[:r])
+        toks = [[first[b]] + t for b, t in enumerate(used.tokens())]
+        return [t[:n_new] for t in toks], used.accepted()

@@ -52,6 +52,18 @@ class CacheView(ctypes.Structure):
                 ("L_stride", c_int32), ("max_len", c_int32)]
 
 
+class DecoderCfg(ctypes.Structure):
+    _fields_ = [("n_layers", c_int32), ("d_model", c_int32), ("n_heads", c_int32), ("n_kv_heads", c_int32),
+                ("head_dim", c_int32), ("d_ff", c_int32), ("vocab", c_int32), ("norm_eps", c_float),
+                ("rope_theta", c_float), ("dt", c_int)]
+
+
+class DecoderWeights(ctypes.Structure):
+    _fields_ = [("embed", c_void_p), ("lm_head", c_void_p), ("w_qkv", ctypes.POINTER(c_void_p)),
+                ("w_o", ctypes.POINTER(c_void_p)), ("w_gate_up", ctypes.POINTER(c_void_p)),
+                ("w_down", ctypes.POINTER(c_void_p))]
+
+
 _lib = None
 
 
@@ -104,6 +116,24 @@ def load() -> ctypes.CDLL:
     L.vc_accept_noalloc.argtypes = [P, c_int, P, c_int, c_int, c_int, P, P, P]
     L.vc_swap_in.restype = c_int
     L.vc_swap_in.argtypes = [P, P, c_size_t, P, P]
+    L.vc_decoder_create.restype = c_int
+    L.vc_decoder_create.argtypes = [ctypes.POINTER(DecoderCfg), ctypes.POINTER(DecoderWeights),
+                                    ctypes.POINTER(c_void_p)]
+    L.vc_decoder_destroy.restype = None
+    L.vc_decoder_destroy.argtypes = [P]
+    L.vc_decoder_workspace_bytes.restype = c_size_t
+    L.vc_decoder_workspace_bytes.argtypes = [P, c_int, c_int, c_int, ctypes.POINTER(QCacheC)]
+    L.vc_decoder_forward.restype = c_int
+    L.vc_decoder_forward.argtypes = [P, P, P, c_int, c_int, c_int, P, c_int, P, P, c_int, P, P, c_int, P, P,
+                                     c_size_t, P]
+    L.vc_decoder_draft_step.restype = c_int
+    L.vc_decoder_draft_step.argtypes = [P, P, c_int, ctypes.POINTER(QCacheC), P, P, P, c_int, P, c_size_t, P]
+    L.vc_kv_writeback.restype = c_int
+    L.vc_kv_writeback.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_int, P, P, P, P, c_int, P]
+    L.vc_gemm_workspace_bytes.restype = c_size_t
+    L.vc_gemm_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
+    L.vc_gemm.restype = c_int
+    L.vc_gemm.argtypes = [P, P, P, P, c_int, c_int, c_int, c_int, P, c_size_t, P]
     _lib = L
     return L
 
@@ -112,7 +142,9 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_record_bytes", "vc_quantize_kv", "vc_qcache_append", "vc_qcache_commit", "vc_drop_kept_count",
             "vc_drop_tokens_workspace_bytes", "vc_drop_tokens", "vc_draft_attn_workspace_bytes",
             "vc_draft_attn", "vc_verify_attn_workspace_bytes", "vc_verify_attn",
-            "vc_accept_workspace_bytes", "vc_accept", "vc_accept_noalloc", "vc_swap_in"]
+            "vc_accept_workspace_bytes", "vc_accept", "vc_accept_noalloc", "vc_swap_in",
+            "vc_decoder_create", "vc_decoder_destroy", "vc_decoder_workspace_bytes", "vc_decoder_forward",
+            "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm"]
 
 
 def status_str(s: int) -> str:
@@ -323,3 +355,104 @@ def vc_swap_in(dst: torch.Tensor, src_pinned: torch.Tensor, nbytes: int | None =
             done_event.record(torch.cuda.current_stream() if stream is None else stream)
         ev = done_event.cuda_event
     _check(load().vc_swap_in(dst.data_ptr(), src_pinned.data_ptr(), n, _stream(stream), ev), "vc_swap_in")
+
+
+# ---------------------------------------------------------------- decoder --
+
+def vc_gemm_workspace_bytes(dtype, M, N, K) -> int:
+    dt = VC_BF16 if dtype == torch.bfloat16 else VC_F32
+    return int(load().vc_gemm_workspace_bytes(dt, M, N, K))
+
+
+def vc_gemm(x, w, out, resid=None, ws: Workspace | None = None, stream=None):
+    M, K = x.shape
+    K2, N = w.shape
+    assert K == K2 and out.shape == (M, N) and x.is_contiguous() and w.is_contiguous() and out.is_contiguous()
+    _check(load().vc_gemm(x.data_ptr(), w.data_ptr(), _ptr(resid), out.data_ptr(), _dt(x), M, N, K,
+                          ws.ptr if ws is not None else None, ws.nbytes if ws is not None else 0,
+                          _stream(stream)), "vc_gemm")
+
+
+class Decoder:
+    """A vc_decoder handle plus the device weights it points to (kept alive
+    here).  `weights` is a dict of tensors stored [in][out]: embed, lm_head
+    and per layer wq, wk, wv, wo, wg, wu, wd; the q|k|v and gate|up column
+    blocks are laid side by side once here, as the C ABI expects."""
+
+    def __init__(self, cfg, weights: dict, dtype=torch.bfloat16, device="cuda"):
+        def dev(t):
+            return t.to(device=device, dtype=dtype).contiguous()
+        self.cfg, self.dtype = cfg, dtype
+        self.embed = dev(weights["embed"])
+        self.lm_head = dev(weights["lm_head"])
+        self.wqkv, self.wo, self.wgu, self.wd = [], [], [], []
+        for lw in weights["layers"]:
+            self.wqkv.append(torch.cat([dev(lw["wq"]), dev(lw["wk"]), dev(lw["wv"])], dim=1).contiguous())
+            self.wo.append(dev(lw["wo"]))
+            self.wgu.append(torch.cat([dev(lw["wg"]), dev(lw["wu"])], dim=1).contiguous())
+            self.wd.append(dev(lw["wd"]))
+        self._init_handle()
+
+    @classmethod
+    def from_packed(cls, cfg, embed, lm_head, wqkv, wo, wgu, wd, dtype=torch.bfloat16):
+        """Weights already laid out as the C ABI wants them (device tensors)."""
+        self = cls.__new__(cls)
+        self.cfg, self.dtype = cfg, dtype
+        self.embed, self.lm_head = embed, lm_head
+        self.wqkv, self.wo, self.wgu, self.wd = list(wqkv), list(wo), list(wgu), list(wd)
+        self._init_handle()
+        return self
+
+    def _init_handle(self):
+        cfg = self.cfg
+        n = cfg.n_layers
+        arr = ctypes.c_void_p * n
+        self._arrs = [arr(*[t.data_ptr() for t in ts]) for ts in (self.wqkv, self.wo, self.wgu, self.wd)]
+        w = DecoderWeights(self.embed.data_ptr(), self.lm_head.data_ptr(), *self._arrs)
+        c = DecoderCfg(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.d_ff, cfg.vocab,
+                       cfg.norm_eps, cfg.rope_theta, VC_BF16 if self.dtype == torch.bfloat16 else VC_F32)
+        h = c_void_p()
+        _check(load().vc_decoder_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h)), "vc_decoder_create")
+        self.handle = h
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.vc_decoder_destroy(h)
+            self.handle = None
+
+    def workspace_bytes(self, B: int, max_rows: int, max_ctx: int, draft_cache: "QCache | None" = None) -> int:
+        dc = ctypes.byref(draft_cache.c) if draft_cache is not None else None
+        return int(load().vc_decoder_workspace_bytes(self.handle, B, max_rows, max_ctx, dc))
+
+
+def vc_decoder_forward(dec: Decoder, first_tok, tokens, tok_stride: int, B: int, Dq: int, ctx_len, max_ctx: int,
+                       k_cache, v_cache, logits, ws: Workspace, k_blk=None, v_blk=None, last_only=False,
+                       stream=None):
+    L_stride = k_cache.shape[3]
+    _check(load().vc_decoder_forward(dec.handle, _ptr(first_tok), _ptr(tokens), int(tok_stride), B, Dq,
+                                     ctx_len.data_ptr(), int(max_ctx), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     L_stride, _ptr(k_blk), _ptr(v_blk), int(bool(last_only)), logits.data_ptr(),
+                                     ws.ptr, ws.nbytes, _stream(stream)), "vc_decoder_forward")
+
+
+def qcache_array(caches: list):
+    """The host array of vc_qcache structs that vc_decoder_draft_step takes
+    (one per layer; the structs are copied, the storage stays in `caches`)."""
+    return (QCacheC * len(caches))(*[c.c for c in caches])
+
+
+def vc_decoder_draft_step(dec: Decoder, tok, caches_arr, logits, next_tok, ws: Workspace, drafts_out=None,
+                          drafts_stride: int = 1, stream=None):
+    """caches_arr: qcache_array(caches) (built once per set of caches)."""
+    _check(load().vc_decoder_draft_step(dec.handle, tok.data_ptr(), tok.shape[0], caches_arr, logits.data_ptr(),
+                                        next_tok.data_ptr(), _ptr(drafts_out), int(drafts_stride), ws.ptr,
+                                        ws.nbytes, _stream(stream)), "vc_decoder_draft_step")
+
+
+def vc_kv_writeback(k_blk, v_blk, n_acc, ctx_len, k_host, v_host, stream=None):
+    nl, B, Hkv, Dq, d = k_blk.shape
+    L_stride = k_host.shape[3]
+    _check(load().vc_kv_writeback(k_blk.data_ptr(), v_blk.data_ptr(), _dt(k_blk), nl, B, Hkv, Dq, d,
+                                  n_acc.data_ptr(), ctx_len.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
+                                  L_stride, _stream(stream)), "vc_kv_writeback")

@@ -63,3 +63,40 @@ def test_invalid_arguments_are_rejected_on_the_host(libvc):
                             None) == vc.VC_ERR_INVALID
     assert L.vc_swap_in(None, None, 16, None, None) == vc.VC_ERR_INVALID
     assert L.vc_workspace_init(None, 0, None) == vc.VC_ERR_INVALID
+
+
+def test_decoder_validation_on_the_host(libvc):
+    """vc_decoder_create checks the configuration and the weight pointers and
+    allocates nothing; unsupported shapes are refused, not approximated."""
+    import ctypes
+    from lossless_draft_verify_gb300 import vc
+    L = vc.load()
+    n = 2
+    arr = ctypes.c_void_p * n
+    ptrs = [arr(*[4096 * (i + 1 + 16 * k) for i in range(n)]) for k in range(4)]
+    w = vc.DecoderWeights(1 << 20, 2 << 20, *ptrs)
+    h = ctypes.c_void_p()
+
+    def create(**kw):
+        base = dict(n_layers=n, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, d_ff=512, vocab=512,
+                    norm_eps=1e-6, rope_theta=1e4, dt=vc.VC_F32)
+        base.update(kw)
+        c = vc.DecoderCfg(**base)
+        return L.vc_decoder_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h))
+
+    assert create() == vc.VC_OK and h.value
+    assert L.vc_decoder_workspace_bytes(h, 1, 16, 1024, None) > 0
+    assert L.vc_decoder_workspace_bytes(h, 0, 16, 1024, None) == 0
+    L.vc_decoder_destroy(h)
+    assert create(head_dim=96) == vc.VC_ERR_UNSUPPORTED
+    assert create(n_heads=16, n_kv_heads=2) == vc.VC_ERR_UNSUPPORTED     # 8 q heads per kv head
+    assert create(n_heads=6, n_kv_heads=4) == vc.VC_ERR_UNSUPPORTED
+    assert create(n_layers=0) == vc.VC_ERR_INVALID
+    assert create(dt=7) == vc.VC_ERR_INVALID
+    bad = vc.DecoderWeights(None, 2 << 20, *ptrs)
+    c = vc.DecoderCfg(n, 256, 4, 2, 64, 512, 512, 1e-6, 1e4, vc.VC_F32)
+    assert L.vc_decoder_create(ctypes.byref(c), ctypes.byref(bad), ctypes.byref(h)) == vc.VC_ERR_INVALID
+    assert L.vc_decoder_forward(None, None, None, 0, 1, 1, None, 0, None, None, 1, None, None, 0, None, None, 0,
+                                None) == vc.VC_ERR_INVALID
+    assert L.vc_gemm(None, None, None, None, 0, 1, 1, 1, None, 0, None) == vc.VC_ERR_INVALID
+    assert L.vc_kv_writeback(None, None, 0, 1, 1, 1, 1, 64, None, None, None, None, 8, None) == vc.VC_ERR_INVALID
