@@ -480,6 +480,206 @@ def run_kernel(args, dev):
     print(json.dumps(rec), flush=True)
 
 
+# --------------------------------------------------------------------------
+# end-to-end model workload: the 8-layer GQA decoder (d_model 4096, 32/8
+# heads, SwiGLU 14336, vocab 32000, bf16), B = 8 prompts at 32k context, the
+# full cache held in pinned host memory and swapped in every round while the
+# model drafts 32 tokens on its 2-bit caches
+# --------------------------------------------------------------------------
+
+M_B, M_HORIZON, M_BITS, M_RESIDUAL = 8, 32, 2, 128
+MODEL_WORKLOAD = ("decoder_e2e_{ctx}: 8-layer GQA decoder d4096 32/8 heads hd128 SwiGLU 14336 vocab 32000 bf16 "
+                  "(random init N(0,0.02), LM head x20), B8 random prompts of {ctx} tokens, KIVI 2-bit g32 R128 "
+                  "draft caches, horizon 32, full KV in pinned host memory swapped in every round")
+
+
+def model_bytes(cfg) -> dict:
+    """Algorithmic bytes of the decoder's weights, per GEMM kind."""
+    D, F, V = cfg.d_model, cfg.d_ff, cfg.vocab
+    qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    return {"gemm_qkv": D * (qd + 2 * kvd) * 2, "gemm_o": qd * D * 2, "gemm_gate_up": D * 2 * F * 2,
+            "gemm_down": F * D * 2, "gemm_head": D * V * 2}
+
+
+def run_model(args, dev, rank, world, barrier, pg):
+    from lossless_draft_verify_gb300 import decode, inputs, vc
+    hbm, tf_burst, tf_sus, peak_src = measured_peaks()
+    cfg = inputs.DecoderConfig()
+    P = args.prompt
+    W = inputs.decoder_weights_packed(cfg, seed=0, device=dev)
+    dec = vc.Decoder.from_packed(cfg, W["embed"], W["lm_head"], W["wqkv"], W["wo"], W["wgu"], W["wd"])
+    n_e2e = 0 if args.no_e2e else 3
+    total = args.warmup + args.steps + n_e2e
+    max_len = P + total * (M_HORIZON + 1) + 64
+    run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=M_BITS, residual=M_RESIDUAL, host_cache=True,
+                                 prefill_chunk=512, device=dev)
+    prompt = inputs.random_prompts(M_B, P, cfg.vocab, seed=rank, device=dev)
+    t_pf = time.perf_counter()
+    run.prefill(prompt)
+    torch.cuda.synchronize()
+    t_pf = time.perf_counter() - t_pf
+    first = run.x.cpu().tolist()
+    log = run.new_log(total)
+    for r in range(args.warmup):
+        run.round(log, r)
+    barrier()
+    evs = [run.new_events() for _ in range(args.steps)]
+    # per-operation trace of the timed rounds: every GEMM and attention call
+    ops_per_round = M_HORIZON * (5 * cfg.n_layers + 1) + 5 * cfg.n_layers + 1 + 2 * cfg.n_layers
+    trace = vc.DecoderTrace(dec, ops_per_round * args.steps)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    trace.start()
+    t0.record()
+    for i in range(args.steps):
+        run.round(log, args.warmup + i, evs[i])
+    t1.record()
+    barrier()
+    clk = clocks.stop()
+    ops = trace.stop()
+    ms = t0.elapsed_time(t1)
+    ms_t = torch.tensor([ms], device=dev)
+    if pg is not None:
+        pg.all_reduce(ms_t, op=pg.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    n_acc = log.n_acc[args.warmup:args.warmup + args.steps].cpu()
+    tokens = int((n_acc.long() + 1).sum())
+    tok_t = torch.tensor([tokens], device=dev, dtype=torch.float64)
+    if pg is not None:
+        pg.all_reduce(tok_t)
+    value = float(tok_t.item()) / (ms_max / 1e3)
+    st = vc.vc_poll_status(run.ws)
+
+    # end to end: the same rounds, each reading its emitted tokens back to the host
+    e2e_val = None
+    h_out = torch.empty(M_B * (M_HORIZON + 2), dtype=torch.int32).pin_memory()
+    d2h = h_out.numel() * 4
+    if n_e2e:
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        base = args.warmup + args.steps
+        for i in range(n_e2e):
+            run.round(log, base + i)
+            h_out[:M_B * M_HORIZON].copy_(run.drafts.view(-1), non_blocking=True)
+            h_out[M_B * M_HORIZON:M_B * (M_HORIZON + 1)].copy_(run.n_acc, non_blocking=True)
+            h_out[M_B * (M_HORIZON + 1):].copy_(run.x, non_blocking=True)
+        e1.record()
+        barrier()
+        e_tok = int((log.n_acc[base:base + n_e2e].cpu().long() + 1).sum())
+        e_ms = torch.tensor([e0.elapsed_time(e1)], device=dev)
+        if pg is not None:
+            pg.all_reduce(e_ms, op=pg.ReduceOp.MAX)
+        e2e_val = world * e_tok / (float(e_ms.item()) / 1e3)
+
+    # lossless check: the same prompts decoded greedily with the full cache
+    # resident, token for token against the draft-and-verify output
+    check = None
+    if not args.no_check:
+        emitted = [[first[b]] + t for b, t in enumerate(log.tokens())]
+        n_cmp = min(len(t) for t in emitted)
+        n_cmp = min(n_cmp, args.check_tokens)
+        del run
+        torch.cuda.empty_cache()
+        ref = decode.VeriCacheRunner(dec, M_B, P + n_cmp + 64, M_HORIZON, bits=M_BITS, residual=M_RESIDUAL,
+                                     host_cache=False, prefill_chunk=512, device=dev)
+        ref.prefill(prompt)
+        greedy = ref.greedy(n_cmp)
+        mism = sum(int(a != g) for b in range(M_B) for a, g in zip(emitted[b][:n_cmp], greedy[b]))
+        check = {"tokens_compared": n_cmp * M_B, "mismatches": mism,
+                 "reference": "plain full-KV greedy decoding of the same model and prompts (one-token forwards)"}
+
+    # per-phase times and rates
+    d_ms = statistics.mean(e["d0"].elapsed_time(e["d1"]) for e in evs)
+    v_ms = statistics.mean(e["v0"].elapsed_time(e["v1"]) for e in evs)
+    c_ms = statistics.mean(e["v1"].elapsed_time(e["c1"]) for e in evs)
+    s_ms = statistics.mean(e["swap0"].elapsed_time(e["swap1"]) for e in evs)
+    hidden = statistics.mean(
+        max(0.0, min(e["swap0"].elapsed_time(e["swap1"]), e["swap0"].elapsed_time(e["d1"]))
+            - max(0.0, e["swap0"].elapsed_time(e["d0"]))) / e["swap0"].elapsed_time(e["swap1"]) for e in evs)
+    wb = model_bytes(cfg)
+    by_kind = {}
+    for k, t in ops:
+        a = by_kind.setdefault(k, [0, 0.0])
+        a[0] += 1
+        a[1] += t
+    ctx_mean = P + (args.warmup + args.steps / 2) * (float(n_acc.float().mean()) + 1)
+    rec_b = vc.vc_record_bytes(M_BITS, cfg.head_dim)
+    draft_attn_bytes = M_B * cfg.n_kv_heads * (int((ctx_mean - M_RESIDUAL) // 32) * rec_b +
+                                               2 * (M_RESIDUAL + 16) * cfg.head_dim * 2)
+    kernels = {}
+    for k, (n, t) in by_kind.items():
+        ent = {"launches": n, "ms_total": t, "ms_per_launch": t / n, "share_of_time": t / ms}
+        if k in wb:
+            ent["GB/s"] = wb[k] / (t / n / 1e3) / 1e9
+            ent["hbm_frac"] = ent["GB/s"] / hbm
+            ent["bytes_per_launch"] = wb[k]
+        elif k == "draft_attn":
+            ent["GB/s"] = draft_attn_bytes / (t / n / 1e3) / 1e9
+            ent["hbm_frac"] = ent["GB/s"] / hbm
+            ent["bytes_per_launch"] = draft_attn_bytes
+        kernels[k] = ent
+    gemm_kinds = [k for k in by_kind if k.startswith("gemm")]
+    g_bytes = sum(wb[k] * by_kind[k][0] for k in gemm_kinds)
+    g_ms = sum(by_kind[k][1] for k in gemm_kinds)
+    dom = max(by_kind, key=lambda k: by_kind[k][1])
+    roof = {"bound": "hbm", "achieved": g_bytes / (g_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+            "frac": g_bytes / (g_ms / 1e3) / 1e9 / hbm, "traffic": None,
+            "kernel": "gemm_tc_kernel (+ split-K reduce): the decoder's projections, weight-streaming at M = 8 "
+                      "(draft) and 264 (verify)", "peak_source": f"{peak_src} hbm_gbs",
+            "dominant_by_time": dom}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
+            "config": {"workload": MODEL_WORKLOAD.format(ctx=P), "global_batch": M_B * world, "seq_len": P,
+                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
+            "roofline": roof,
+            "phases_ms": {"draft_32_steps": d_ms, "verify_forward": v_ms, "accept_commit_writeback": c_ms,
+                          "swap_in": s_ms, "swap_hidden_frac": hidden},
+            "swap": {"bytes": run_bytes(cfg, max_len), "GB/s": run_bytes(cfg, max_len) / (s_ms / 1e3) / 1e9},
+            "kernels": kernels,
+            "accepted_per_round_mean": float(n_acc.float().mean()), "tokens_per_round": tokens / args.steps,
+            "prefill_s": round(t_pf, 2), "status": st, "lossless_check": check,
+            "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc) * args.steps,
+            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, max_len),
+                    "d2h_bytes_per_step": d2h},
+            "cpu_baseline": None,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def model_launches_per_round(cfg, vc) -> int:
+    """Kernels the library launches in one round of the model workload
+    (counted from the decoder's sequencing: a GEMM adds its split-K reduction
+    when it has more than one split)."""
+    qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    shapes = [(qd + 2 * kvd, cfg.d_model), (cfg.d_model, qd), (2 * cfg.d_ff, cfg.d_model), (cfg.d_model, cfg.d_ff)]
+
+    def g(M, N, K):
+        return 1 + int(vc.vc_gemm_workspace_bytes(torch.bfloat16, M, N, K) > 0)
+
+    def layer(M, attn_kernels):
+        # rmsnorm, qkv, rope, attention, o, rmsnorm, gate_up, silu, down
+        return 2 + 1 + sum(g(M, N, K) for N, K in shapes) + 1 + attn_kernels
+
+    draft = 1 + cfg.n_layers * (layer(M_B, 1) + 1) + 1 + g(M_B, cfg.vocab, cfg.d_model) + 1 + 1 + 1
+    M = M_B * (M_HORIZON + 1)
+    verify = 1 + cfg.n_layers * layer(M, 2) + 1 + g(M, cfg.vocab, cfg.d_model) + 1
+    return M_HORIZON * draft + verify + 1 + cfg.n_layers + 1
+
+
+def run_bytes(cfg, max_len) -> int:
+    """Bytes of one full-cache swap-in (K and V, every layer, the whole ring of
+    positions the runner allocates)."""
+    return 2 * cfg.n_layers * M_B * cfg.n_kv_heads * (max_len + M_HORIZON + 1) * cfg.head_dim * 2
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,6 +692,11 @@ def main():
                     help="time one kernel alone: draft, verify, accept, quantize, drop, dense_draft")
     ap.add_argument("--dq", type=int, default=32, help="verify block size for --kernel verify")
     ap.add_argument("--chunks", type=int, default=1, help="side streams for --kernel swap")
+    ap.add_argument("--workload", default="round", choices=["round", "model"],
+                    help="round: one layer's hot path at 32k (B16); model: the 8-layer decoder end to end")
+    ap.add_argument("--prompt", type=int, default=32768, help="prompt tokens per sequence (--workload model)")
+    ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
+    ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
@@ -513,13 +718,18 @@ def main():
         pg = dist
     from lossless_draft_verify_gb300 import build
     build.build()
-    rnd = Round(dev)
-
     def barrier():
         torch.cuda.synchronize()
         if pg is not None:
             pg.barrier()
         torch.cuda.synchronize()
+
+    if args.workload == "model":
+        run_model(args, dev, rank, world, barrier, pg)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    rnd = Round(dev)
 
     for _ in range(args.warmup):
         rnd.step()

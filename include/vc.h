@@ -387,6 +387,23 @@ typedef struct vc_decoder vc_decoder;   /* host object: configuration + weight p
 vc_status vc_decoder_create(const vc_decoder_cfg *cfg, const vc_decoder_weights *w, vc_decoder **out);
 void vc_decoder_destroy(vc_decoder *dec);
 
+/*
+ * Tracing (measurement aid): after vc_decoder_set_trace, the decoder records
+ * events[2k] and events[2k+1] on the call's stream around its k-th operation
+ * whose kind bit (1 << kind) is set in kind_mask, writes the kind to
+ * kinds[k], and stops recording once `capacity` operations are traced.  The
+ * arrays are caller-owned (events created by the caller); capacity 0 turns
+ * tracing off.  Tracing mutates the decoder object: traced calls must not run
+ * concurrently on one vc_decoder.  A GEMM operation includes its split-K
+ * reduction.
+ */
+typedef enum vc_trace_kind {
+    VC_TRACE_GEMM_QKV = 0, VC_TRACE_GEMM_O = 1, VC_TRACE_GEMM_GATE_UP = 2, VC_TRACE_GEMM_DOWN = 3,
+    VC_TRACE_GEMM_HEAD = 4, VC_TRACE_DRAFT_ATTN = 5, VC_TRACE_VERIFY_ATTN = 6
+} vc_trace_kind;
+vc_status vc_decoder_set_trace(vc_decoder *dec, cudaEvent_t *events, int32_t *kinds, int capacity, int kind_mask);
+int vc_decoder_trace_count(const vc_decoder *dec);
+
 /* Workspace for calls with up to B sequences of up to max_rows rows each and
  * contexts up to max_ctx tokens; draft_cache (may be NULL when only
  * vc_decoder_forward is used) is a cache of the geometry later passed to

@@ -21,6 +21,10 @@ struct vc_decoder {
     vc_decoder_cfg c;
     const void *embed, *head;
     std::vector<const void *> wqkv, wo, wgu, wd;
+    // optional trace: event pairs around selected operations (caller-owned)
+    mutable cudaEvent_t *tr_ev = nullptr;
+    mutable int32_t *tr_kind = nullptr;
+    mutable int tr_cap = 0, tr_n = 0, tr_mask = 0;
 };
 
 namespace vc {
@@ -264,6 +268,22 @@ struct Ctx {
     template <typename P = void> P *at(size_t off) const { return reinterpret_cast<P *>(ws + off); }
 };
 
+// Record the trace events around op() when its kind is selected.
+template <typename F>
+cudaError_t traced(const Ctx &C, int kind, F &&op)
+{
+    const vc_decoder *d = C.d;
+    const bool on = d->tr_ev && (d->tr_mask & (1 << kind)) && d->tr_n < d->tr_cap;
+    if (on) cudaEventRecord(d->tr_ev[2 * d->tr_n], C.st);
+    const cudaError_t e = op();
+    if (on) {
+        cudaEventRecord(d->tr_ev[2 * d->tr_n + 1], C.st);
+        d->tr_kind[d->tr_n] = kind;
+        ++d->tr_n;
+    }
+    return e;
+}
+
 #define VC_TRY(expr)                                \
     do {                                            \
         cudaError_t e_ = (expr);                    \
@@ -286,15 +306,21 @@ cudaError_t layer_tail(const Ctx &C, int l, int M)
     const vc_decoder_cfg &c = C.d->c;
     const int qd = c.n_heads * c.head_dim;
     void *x = C.at(C.L.x), *h = C.at(C.L.h), *part = C.at(C.L.part);
-    VC_TRY(gemm(C.at(C.L.att), C.d->wo[l], x, x, c.dt, M, c.d_model, qd, qd, part, C.status(), C.st));
+    VC_TRY(traced(C, VC_TRACE_GEMM_O, [&] {
+        return gemm(C.at(C.L.att), C.d->wo[l], x, x, c.dt, M, c.d_model, qd, qd, part, C.status(), C.st);
+    }));
     VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
-    VC_TRY(gemm(h, C.d->wgu[l], nullptr, C.at(C.L.gu), c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, part,
-                C.status(), C.st));
+    VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
+        return gemm(h, C.d->wgu[l], nullptr, C.at(C.L.gu), c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, part,
+                    C.status(), C.st);
+    }));
     const size_t n = (size_t)M * c.d_ff;
     silu_mul_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, C.st>>>(C.at<const T>(C.L.gu), M, c.d_ff,
                                                                      C.at<T>(C.L.act));
     VC_TRY(cudaGetLastError());
-    return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.status(), C.st);
+    return traced(C, VC_TRACE_GEMM_DOWN, [&] {
+        return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.status(), C.st);
+    });
 }
 
 template <typename T>
@@ -316,8 +342,10 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
     VC_TRY(cudaGetLastError());
     for (int l = 0; l < c.n_layers; ++l) {
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
-        VC_TRY(gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part, C.status(),
-                    C.st));
+        VC_TRY(traced(C, VC_TRACE_GEMM_QKV, [&] {
+            return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
+                        C.status(), C.st);
+        }));
         RopeDst dst;
         dst.k1 = (T *)kc + l * layer_cache;
         dst.v1 = (T *)vcache + l * layer_cache;
@@ -331,17 +359,23 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
         rope_kernel<T><<<M, kRowThreads, 0, C.st>>>(C.at<const T>(C.L.qkv), Dq, c.n_heads, c.n_kv_heads, hd, ctx,
                                                     c.rope_theta, C.at<T>(C.L.q), dst, C.status());
         VC_TRY(cudaGetLastError());
-        VC_TRY(verify_attn(C.at(C.L.q), dst.k1, dst.v1, c.dt, ctx, B, Dq, c.n_heads, c.n_kv_heads, hd, L_stride,
-                           max_ctx, scale, C.at(C.L.att), C.at(C.L.vws), C.st, kSplitTiles));
+        VC_TRY(traced(C, VC_TRACE_VERIFY_ATTN, [&] {
+            return verify_attn(C.at(C.L.q), dst.k1, dst.v1, c.dt, ctx, B, Dq, c.n_heads, c.n_kv_heads, hd, L_stride,
+                               max_ctx, scale, C.at(C.L.att), C.at(C.L.vws), C.st, kSplitTiles);
+        }));
         VC_TRY(layer_tail<T>(C, l, M));
     }
     if (last_only) {
         VC_TRY(rmsnorm<T>(C, x, B, Dq, Dq - 1, C.at(C.L.hl)));
-        VC_TRY(gemm(C.at(C.L.hl), C.d->head, nullptr, logits, c.dt, B, c.vocab, c.d_model, c.d_model, part,
-                    C.status(), C.st));
+        VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
+            return gemm(C.at(C.L.hl), C.d->head, nullptr, logits, c.dt, B, c.vocab, c.d_model, c.d_model, part,
+                        C.status(), C.st);
+        }));
     } else {
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
-        VC_TRY(gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st));
+        VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
+            return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st);
+        }));
     }
     fold_status_kernel<<<1, 1, 0, C.st>>>(C.status(), C.at<int32_t>(C.L.vws), nullptr, nullptr);
     return cudaGetLastError();
@@ -366,8 +400,10 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
     VC_TRY(cudaGetLastError());
     for (int l = 0; l < c.n_layers; ++l) {
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
-        VC_TRY(gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part, C.status(),
-                    C.st));
+        VC_TRY(traced(C, VC_TRACE_GEMM_QKV, [&] {
+            return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
+                        C.status(), C.st);
+        }));
         RopeDst dst;
         dst.k1 = kn;
         dst.v1 = vn;
@@ -385,11 +421,15 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         vc_cache_view view{};
         view.kind = VC_CACHE_KIVI;
         view.kivi = &caches[l];
-        VC_TRY(draft_attn(C.at(C.L.q), c.dt, &view, c.n_heads, scale, C.at(C.L.att), C.at(C.L.dws), C.st));
+        VC_TRY(traced(C, VC_TRACE_DRAFT_ATTN, [&] {
+            return draft_attn(C.at(C.L.q), c.dt, &view, c.n_heads, scale, C.at(C.L.att), C.at(C.L.dws), C.st);
+        }));
         VC_TRY(layer_tail<T>(C, l, M));
     }
     VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
-    VC_TRY(gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st));
+    VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
+        return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st);
+    }));
     VC_TRY(accept(logits, c.dt, nullptr, B, 0, c.vocab, C.at<int32_t>(C.L.nacc), next_tok, C.at(C.L.aws), C.st));
     if (drafts_out) {
         scatter_tokens_kernel<<<(B + 127) / 128, 128, 0, C.st>>>(next_tok, B, drafts_out, drafts_stride);
@@ -451,6 +491,19 @@ vc_status vc_decoder_create(const vc_decoder_cfg *cfg, const vc_decoder_weights 
 }
 
 void vc_decoder_destroy(vc_decoder *dec) { delete dec; }
+
+vc_status vc_decoder_set_trace(vc_decoder *dec, cudaEvent_t *events, int32_t *kinds, int capacity, int kind_mask)
+{
+    if (!dec || capacity < 0 || (capacity > 0 && (!events || !kinds))) return VC_ERR_INVALID;
+    dec->tr_ev = capacity > 0 ? events : nullptr;
+    dec->tr_kind = kinds;
+    dec->tr_cap = capacity;
+    dec->tr_n = 0;
+    dec->tr_mask = kind_mask;
+    return VC_OK;
+}
+
+int vc_decoder_trace_count(const vc_decoder *dec) { return dec ? dec->tr_n : 0; }
 
 size_t vc_decoder_workspace_bytes(const vc_decoder *dec, int B, int max_rows, int max_ctx,
                                   const vc_qcache *draft_cache)

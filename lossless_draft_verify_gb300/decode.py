@@ -160,6 +160,8 @@ class VeriCacheRunner:
             ev["d1"].record(main)
         if self.host_cache:
             main.wait_event(self.ev_swap)
+        if ev is not None:
+            ev["v0"].record(main)
         max_ctx = min(self.ctx_bound, self.L_stride - (D + 1))
         vc.vc_decoder_forward(self.dec, self.x, self.drafts, D, B, D + 1, self.round_len, max_ctx, self.k_full,
                               self.v_full, self.logits_v, self.ws, k_blk=self.k_blk, v_blk=self.v_blk)
@@ -177,6 +179,11 @@ class VeriCacheRunner:
             log.n_acc[r].copy_(self.n_acc)
             log.nxt[r].copy_(self.x)
         self.ctx_bound += D + 1
+
+    @staticmethod
+    def new_events() -> dict:
+        mk = lambda: torch.cuda.Event(enable_timing=True)
+        return {k: mk() for k in ("swap0", "swap1", "d0", "d1", "v0", "v1", "c1")}
 
     def new_log(self, rounds: int) -> RoundLog:
         B, D = self.B, self.D

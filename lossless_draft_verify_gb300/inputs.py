@@ -162,3 +162,51 @@ def tiny_prompt(cfg: TinyConfig, length: int = 512, seed: int = 0) -> torch.Tens
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+# --------------------------------------------------------------------------
+# 8-layer GQA decoder of the end-to-end workload (7B-class widths)
+# --------------------------------------------------------------------------
+
+@dataclass
+class DecoderConfig:
+    n_layers: int = 8
+    d_model: int = 4096
+    n_heads: int = 32
+    n_kv_heads: int = 8
+    head_dim: int = 128
+    d_ff: int = 14336
+    vocab: int = 32000
+    init_std: float = 0.02
+    head_scale: float = 20.0
+    rope_theta: float = 10000.0
+    norm_eps: float = 1e-6
+
+
+def decoder_weights_packed(cfg, seed: int = 0, device="cuda", dtype=torch.bfloat16) -> dict:
+    """Weights ~ N(0, 0.02^2) (LM head x20) drawn on `device` directly in the
+    layout the decoder takes: embed [vocab][d], lm_head [d][vocab] and per
+    layer wqkv [d][(Hq+2Hkv) hd] (q|k|v), wo [Hq hd][d], wgu [d][2 ff]
+    (gate|up), wd [ff][d]."""
+    g = _gen(seed, device)
+
+    def w(i, o, s=1.0):
+        x = torch.randn(i, o, generator=g, device=device, dtype=torch.float32)
+        return x.mul_(cfg.init_std * s).to(dtype)
+
+    D, F = cfg.d_model, cfg.d_ff
+    qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    out = {"embed": w(cfg.vocab, D), "wqkv": [], "wo": [], "wgu": [], "wd": []}
+    for _ in range(cfg.n_layers):
+        out["wqkv"].append(w(D, qd + 2 * kvd))
+        out["wo"].append(w(qd, D))
+        out["wgu"].append(w(D, 2 * F))
+        out["wd"].append(w(F, D))
+    out["lm_head"] = w(D, cfg.vocab, cfg.head_scale)
+    return out
+
+
+def random_prompts(B: int, length: int, vocab: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Uniform random token ids [B][length] (int32)."""
+    g = _gen(seed, "cpu")
+    return torch.randint(0, vocab, (B, length), generator=g, dtype=torch.int32).to(device)

@@ -130,6 +130,10 @@ def load() -> ctypes.CDLL:
     L.vc_decoder_draft_step.argtypes = [P, P, c_int, ctypes.POINTER(QCacheC), P, P, P, c_int, P, c_size_t, P]
     L.vc_kv_writeback.restype = c_int
     L.vc_kv_writeback.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_int, P, P, P, P, c_int, P]
+    L.vc_decoder_set_trace.restype = c_int
+    L.vc_decoder_set_trace.argtypes = [P, P, P, c_int, c_int]
+    L.vc_decoder_trace_count.restype = c_int
+    L.vc_decoder_trace_count.argtypes = [P]
     L.vc_gemm_workspace_bytes.restype = c_size_t
     L.vc_gemm_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
     L.vc_gemm.restype = c_int
@@ -144,7 +148,10 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_draft_attn", "vc_verify_attn_workspace_bytes", "vc_verify_attn",
             "vc_accept_workspace_bytes", "vc_accept", "vc_accept_noalloc", "vc_swap_in",
             "vc_decoder_create", "vc_decoder_destroy", "vc_decoder_workspace_bytes", "vc_decoder_forward",
-            "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm"]
+            "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm",
+            "vc_decoder_set_trace", "vc_decoder_trace_count"]
+
+TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
 
 def status_str(s: int) -> str:
@@ -456,3 +463,31 @@ def vc_kv_writeback(k_blk, v_blk, n_acc, ctx_len, k_host, v_host, stream=None):
     _check(load().vc_kv_writeback(k_blk.data_ptr(), v_blk.data_ptr(), _dt(k_blk), nl, B, Hkv, Dq, d,
                                   n_acc.data_ptr(), ctx_len.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
                                   L_stride, _stream(stream)), "vc_kv_writeback")
+
+
+class DecoderTrace:
+    """Event pairs the decoder records around its GEMMs and attention calls
+    (vc_decoder_set_trace); capacity = operations to record."""
+
+    def __init__(self, dec: Decoder, capacity: int, kinds=TRACE_KINDS):
+        self.dec, self.capacity = dec, capacity
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.events:                       # torch creates events lazily
+            e.record()
+        torch.cuda.synchronize()
+        self._ev_arr = (c_void_p * (2 * capacity))(*[e.cuda_event for e in self.events])
+        self._kinds = (c_int32 * capacity)()
+        self.mask = sum(1 << TRACE_KINDS.index(k) for k in kinds)
+
+    def start(self):
+        _check(load().vc_decoder_set_trace(self.dec.handle, self._ev_arr, self._kinds, self.capacity, self.mask),
+               "vc_decoder_set_trace")
+
+    def stop(self) -> list[tuple[str, float]]:
+        """Turn tracing off; returns (kind, milliseconds) per recorded operation
+        (synchronizes)."""
+        n = int(load().vc_decoder_trace_count(self.dec.handle))
+        _check(load().vc_decoder_set_trace(self.dec.handle, None, None, 0, 0), "vc_decoder_set_trace")
+        torch.cuda.synchronize()
+        return [(TRACE_KINDS[self._kinds[k]], self.events[2 * k].elapsed_time(self.events[2 * k + 1]))
+                for k in range(n)]
