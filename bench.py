@@ -59,9 +59,9 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("190bc277132006521419d50c37d22d1073f34570989ec9e806a4a14009181ff8",
+    "sha256": ("f07d50cedc0e3d0010968e55210875bd71ebcf6b65067b5d0702aeac5b41bb08",
                "8b1109c68498705ecd31b5533b5ace8c5bb0cfe4584e74b26b26eb3baa0d456c"),
-    "bytes": 412.416512e6 + 6.476032e6,
+    "bytes": 409.788160e6 + 4.499968e6,
     "algorithmic_bytes": 409731072,
 }
 
@@ -369,6 +369,7 @@ def run_kernel(args, dev):
     from lossless_draft_verify_gb300 import inputs, vc
     hbm, tf_burst, _, peak_src = measured_peaks()
     name = args.kernel
+    B = args.batch
     rec = {}
     flops = None
     if name in ("draft", "quantize"):
@@ -390,7 +391,7 @@ def run_kernel(args, dev):
             scale = inputs.default_scale(D_HEAD)
             fn = lambda: vc.vc_draft_attn(q, view, scale, out, ws)
             nbytes = B * HKV * (ng * rb + 2 * RESIDUAL * D_HEAD * 2) + 2 * q.numel() * 2
-            rec = {"workload": "draft attention, KIVI 2-bit cache [16,8,32768,128] R=128, q [16,32,128] bf16"}
+            rec = {"workload": f"draft attention, KIVI 2-bit cache [{B},8,32768,128] R=128, q [{B},32,128] bf16"}
     elif name == "verify":
         dq = args.dq
         q = inputs.normal_bf16((B, dq, HQ, D_HEAD), 8, device=dev)
@@ -403,7 +404,7 @@ def run_kernel(args, dev):
         fn = lambda: vc.vc_verify_attn(q, k, v, ctx, CTX, scale, out, ws)
         nbytes = 2 * k.numel() * 2 + 2 * q.numel() * 2
         flops = 4 * D_HEAD * B * HQ * sum(CTX + i + 1 for i in range(dq))
-        rec = {"workload": f"verify attention, Dq={dq}, bf16 K/V [16,8,{CTX + dq},128], 32/8 heads"}
+        rec = {"workload": f"verify attention, Dq={dq}, bf16 K/V [{B},8,{CTX + dq},128], 32/8 heads"}
     elif name == "accept":
         case = inputs.accept_case(B, HORIZON, VOCAB, seed=0, device=dev)
         n = torch.empty(B, dtype=torch.int32, device=dev)
@@ -661,16 +662,15 @@ def model_launches_per_round(cfg, vc) -> int:
     qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
     shapes = [(qd + 2 * kvd, cfg.d_model), (cfg.d_model, qd), (2 * cfg.d_ff, cfg.d_model), (cfg.d_model, cfg.d_ff)]
 
-    def g(M, N, K):
-        return 1 + int(vc.vc_gemm_workspace_bytes(torch.bfloat16, M, N, K) > 0)
+    def g(N, K, decode):
+        return 1 + int(vc.vc_gemm_splits(torch.bfloat16, N, K, decode) > 1)
 
-    def layer(M, attn_kernels):
+    def layer(decode, attn_kernels):
         # rmsnorm, qkv, rope, attention, o, rmsnorm, gate_up, silu, down
-        return 2 + 1 + sum(g(M, N, K) for N, K in shapes) + 1 + attn_kernels
+        return 2 + 1 + sum(g(N, K, decode) for N, K in shapes) + 1 + attn_kernels
 
-    draft = 1 + cfg.n_layers * (layer(M_B, 1) + 1) + 1 + g(M_B, cfg.vocab, cfg.d_model) + 1 + 1 + 1
-    M = M_B * (M_HORIZON + 1)
-    verify = 1 + cfg.n_layers * layer(M, 2) + 1 + g(M, cfg.vocab, cfg.d_model) + 1
+    draft = 1 + cfg.n_layers * (layer(True, 1) + 1) + 1 + g(cfg.vocab, cfg.d_model, True) + 1 + 1 + 1
+    verify = 1 + cfg.n_layers * layer(False, 2) + 1 + g(cfg.vocab, cfg.d_model, False) + 1
     return M_HORIZON * draft + verify + 1 + cfg.n_layers + 1
 
 
@@ -691,6 +691,7 @@ def main():
     ap.add_argument("--kernel", default=None,
                     help="time one kernel alone: draft, verify, accept, quantize, drop, dense_draft")
     ap.add_argument("--dq", type=int, default=32, help="verify block size for --kernel verify")
+    ap.add_argument("--batch", type=int, default=B, help="sequences for --kernel draft/verify")
     ap.add_argument("--chunks", type=int, default=1, help="side streams for --kernel swap")
     ap.add_argument("--workload", default="round", choices=["round", "model"],
                     help="round: one layer's hot path at 32k (B16); model: the 8-layer decoder end to end")

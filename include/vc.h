@@ -467,6 +467,10 @@ vc_status vc_kv_writeback(const void *k_blk, const void *v_blk, vc_dtype dt, int
  * device only.  ws: vc_gemm_workspace_bytes(dt, M, N, K) bytes (may be 0).
  */
 size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K);
+/* Number of K splits of the decoder's GEMM for (N, K): decode_plan != 0 gives
+ * the plan of vc_decoder_draft_step (M <= 128, chosen to fill whole waves),
+ * 0 the row-invariant plan of vc_gemm and vc_decoder_forward.  0 on bad input. */
+int vc_gemm_splits(vc_dtype dt, int N, int K, int decode_plan);
 vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
                   void *ws, size_t ws_bytes, cudaStream_t stream);
 

@@ -234,7 +234,10 @@ Layout layout_of(const vc_decoder *d, int B, int max_rows, int max_ctx, size_t d
     L.kvn = take(2 * (size_t)B * kvd * es);
     L.hl = take((size_t)B * c.d_model * es);
     size_t part = 0;
-    auto gp = [&](int rows, int N, int K) { part = std::max(part, gemm_ws_bytes(c.dt, rows, N, K)); };
+    auto gp = [&](int rows, int N, int K) {
+        part = std::max(part, gemm_ws_bytes(c.dt, rows, N, K, kGemmRowInvariant));
+        part = std::max(part, gemm_ws_bytes(c.dt, std::min(rows, B), N, K, kGemmDecode));
+    };
     gp((int)M, nqkv, c.d_model);
     gp((int)M, c.d_model, qd);
     gp((int)M, 2 * c.d_ff, c.d_model);
@@ -264,6 +267,7 @@ struct Ctx {
     uint8_t *ws;
     Layout L;
     cudaStream_t st;
+    int plan;          // GEMM split plan: row-invariant (forward) or decode (draft)
     int32_t *status() const { return (int32_t *)ws; }
     template <typename P = void> P *at(size_t off) const { return reinterpret_cast<P *>(ws + off); }
 };
@@ -307,19 +311,21 @@ cudaError_t layer_tail(const Ctx &C, int l, int M)
     const int qd = c.n_heads * c.head_dim;
     void *x = C.at(C.L.x), *h = C.at(C.L.h), *part = C.at(C.L.part);
     VC_TRY(traced(C, VC_TRACE_GEMM_O, [&] {
-        return gemm(C.at(C.L.att), C.d->wo[l], x, x, c.dt, M, c.d_model, qd, qd, part, C.status(), C.st);
+        return gemm(C.at(C.L.att), C.d->wo[l], x, x, c.dt, M, c.d_model, qd, qd, part, C.status(), C.st,
+                    C.plan);
     }));
     VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
     VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
         return gemm(h, C.d->wgu[l], nullptr, C.at(C.L.gu), c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, part,
-                    C.status(), C.st);
+                    C.status(), C.st, C.plan);
     }));
     const size_t n = (size_t)M * c.d_ff;
     silu_mul_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, C.st>>>(C.at<const T>(C.L.gu), M, c.d_ff,
                                                                      C.at<T>(C.L.act));
     VC_TRY(cudaGetLastError());
     return traced(C, VC_TRACE_GEMM_DOWN, [&] {
-        return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.status(), C.st);
+        return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.status(), C.st,
+                    C.plan);
     });
 }
 
@@ -344,7 +350,7 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         VC_TRY(traced(C, VC_TRACE_GEMM_QKV, [&] {
             return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
-                        C.status(), C.st);
+                        C.status(), C.st, C.plan);
         }));
         RopeDst dst;
         dst.k1 = (T *)kc + l * layer_cache;
@@ -369,12 +375,13 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
         VC_TRY(rmsnorm<T>(C, x, B, Dq, Dq - 1, C.at(C.L.hl)));
         VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
             return gemm(C.at(C.L.hl), C.d->head, nullptr, logits, c.dt, B, c.vocab, c.d_model, c.d_model, part,
-                        C.status(), C.st);
+                        C.status(), C.st, C.plan);
         }));
     } else {
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
-            return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st);
+            return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(),
+                        C.st, C.plan);
         }));
     }
     fold_status_kernel<<<1, 1, 0, C.st>>>(C.status(), C.at<int32_t>(C.L.vws), nullptr, nullptr);
@@ -402,7 +409,7 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         VC_TRY(traced(C, VC_TRACE_GEMM_QKV, [&] {
             return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
-                        C.status(), C.st);
+                        C.status(), C.st, C.plan);
         }));
         RopeDst dst;
         dst.k1 = kn;
@@ -428,7 +435,8 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
     }
     VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
     VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
-        return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st);
+        return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st,
+                    C.plan);
     }));
     VC_TRY(accept(logits, c.dt, nullptr, B, 0, c.vocab, C.at<int32_t>(C.L.nacc), next_tok, C.at(C.L.aws), C.st));
     if (drafts_out) {
@@ -528,7 +536,7 @@ vc_status vc_decoder_forward(const vc_decoder *dec, const int32_t *first_tok, co
         return VC_ERR_INVALID;
     const Layout L = layout_of(dec, B, Dq, max_ctx, 0);
     if (ws_bytes < L.total) return VC_ERR_INVALID;
-    Ctx C{dec, (uint8_t *)ws, L, stream};
+    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmRowInvariant};
     const cudaError_t e =
         dec->c.dt == VC_BF16
             ? forward_impl<__nv_bfloat16>(C, first_tok, tokens, tok_stride, B, Dq, ctx_len, max_ctx, k_cache, v_cache,
@@ -556,7 +564,7 @@ vc_status vc_decoder_draft_step(const vc_decoder *dec, const int32_t *tok, int B
     }
     const Layout L = layout_of(dec, B, 1, 0, draft_ws_of(dec, &caches[0]));
     if (ws_bytes < L.total) return VC_ERR_INVALID;
-    Ctx C{dec, (uint8_t *)ws, L, stream};
+    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmDecode};
     const cudaError_t e =
         c.dt == VC_BF16
             ? draft_impl<__nv_bfloat16>(C, tok, B, caches, logits, next_tok, drafts_out, drafts_stride)
@@ -587,6 +595,13 @@ vc_status vc_kv_writeback(const void *k_blk, const void *v_blk, vc_dtype dt, int
         writeback_kernel<float><<<grid, 64, 0, stream>>>((const float *)k_blk, (const float *)v_blk, B, Hkv, Dq, d,
                                                          n_acc, ctx_len, (float *)kd, (float *)vd, L_stride);
     return to_status(cudaGetLastError());
+}
+
+int vc_gemm_splits(vc_dtype dt, int N, int K, int decode_plan)
+{
+    if ((dt != VC_BF16 && dt != VC_F32) || N <= 0 || K <= 0) return 0;
+    if (!gemm_uses_tensor_cores(dt, N, K)) return 1;
+    return gemm_splits(N, K, decode_plan ? kGemmDecode : kGemmRowInvariant);
 }
 
 size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K)

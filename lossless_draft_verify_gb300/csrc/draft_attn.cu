@@ -786,15 +786,27 @@ KiviPlan kivi_plan(const vc_qcache *c)
 {
     const int units = c->B * c->Hkv;
     const int ng = c->max_groups;
-    // about four waves of 4 resident CTAs per SM, counting the residual split
-    const int target_ctas = num_sms() * 4 * 4;
-    int s = (target_ctas + units - 1) / units - 1;
-    s = s < 1 ? 1 : s;
-    const int max_s = (ng + NW * 4 - 1) / (NW * 4);    // keep >= 2 group pairs per warp
-    if (s > max_s) s = max_s > 0 ? max_s : 1;
-    if (s > kMaxSplit - 1) s = kMaxSplit - 1;
+    const int slots = num_sms() * 4;                   // 4 resident CTAs per SM
+    // Split count minimising waves x (group pairs per warp + ~3 pairs of
+    // fixed cost per CTA) for CTAs of equal length; the residual ring is one
+    // more CTA per kv unit.
+    int best = 1;
+    long best_t = -1;
+    const int max_s = ng > 0 ? (ng + 3) / 4 : 1;       // at least two group pairs per split
+    for (int s = 1; s <= max_s && s < kMaxSplit; ++s) {
+        int gps = (ng + s - 1) / s;
+        gps += gps & 1;
+        const int se = ng > 0 ? (ng + gps - 1) / gps : 0;
+        const int pairs_per_warp = (gps / 2 + NW - 1) / NW;
+        const long waves = ((long)units * (se + 1) + slots - 1) / slots;
+        const long t = waves * (pairs_per_warp + 3);
+        if (best_t < 0 || t < best_t) {
+            best_t = t;
+            best = s;
+        }
+    }
     KiviPlan p;
-    p.groups_per_split = ng > 0 ? (ng + s - 1) / s : 2;
+    p.groups_per_split = ng > 0 ? (ng + best - 1) / best : 2;
     p.groups_per_split += p.groups_per_split & 1;       // whole pairs
     p.n_split_q = ng > 0 ? (ng + p.groups_per_split - 1) / p.groups_per_split : 0;
     return p;

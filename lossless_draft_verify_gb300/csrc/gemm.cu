@@ -6,14 +6,14 @@
 // computes (paper page, "What the paper found": outputs identical to full-KV
 // greedy decoding; the thelatestinai page shows how far batch-dependent
 // floating-point order drifts KV-cached decoding).  Both kernels here fix the
-// summation order of every output element from the shapes (K, N) and the
-// device alone: the split of K, the order of the splits and the order inside
-// a split never depend on M.
+// summation order of every output element from the shapes (K, N), the split
+// plan and the device alone: the split of K, the order of the splits and the
+// order inside a split never depend on M.
 //
 // bf16 (x [M][K] and W [K][N] row-major, N a multiple of 128, K of 64):
 // tcgen05 tensor cores.  One CTA per (128-row tile, 128-column tile, K split):
 // warp 0 issues TMA loads of 64-wide K slices (x K-major, W MN-major, 128-byte
-// swizzle) into a 4-stage ring, warp 1 issues tcgen05.mma (M128 N128 K16)
+// swizzle) into a 3-stage ring (2 CTAs per SM), warp 1 issues tcgen05.mma (M128 N128 K16)
 // into a TMEM accumulator, warps 2-5 read TMEM and write either the output
 // (one split) or fp32 partials that a second kernel sums in split order.
 // fp32 (any shape): CUDA cores, one output element per thread, K in order.
@@ -26,7 +26,7 @@
 namespace vc {
 namespace {
 
-constexpr int GM = 128, GN = 128, GK = 64, GSTAGES = 4;
+constexpr int GM = 128, GN = 128, GK = 64, GSTAGES = 3;
 constexpr int G_THREADS = 192;
 constexpr int G_STAGE_BYTES = GM * GK * 2 + GK * GN * 2;     // 16 KB x + 16 KB W
 constexpr int G_SMEM = GSTAGES * G_STAGE_BYTES + 256;
@@ -54,7 +54,7 @@ __device__ __forceinline__ bool g_wait(uint64_t *bar, uint32_t parity, GemmBars 
     return false;
 }
 
-__global__ void __launch_bounds__(G_THREADS, 1)
+__global__ void __launch_bounds__(G_THREADS, 2)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, GemmArgs A)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -259,26 +259,45 @@ bool gemm_uses_tensor_cores(vc_dtype dt, int N, int K)
     return dt == VC_BF16 && N % GN == 0 && K % GK == 0 && K > 0;
 }
 
-// The K split depends on (N, K) and the device only: enough CTAs to cover the
-// SMs when M is at most one row tile, and at least 8 K-slices per split.
-int gemm_splits(int N, int K)
+// The K split depends on (N, K), the plan and the device only, never on M.
+// kGemmRowInvariant (forward passes): few splits, so that blocks of a few row
+// tiles do not pay for large fp32 partials.  kGemmDecode (draft steps, M <= one
+// row tile): the split that fills whole waves of 2 CTAs per SM best.
+int gemm_splits(int N, int K, int plan)
 {
     const int ntiles = N / GN, nkb = K / GK;
-    int s = (device_sm_count() + ntiles - 1) / ntiles;
-    s = max(1, min(s, nkb / 8));
-    const int per = (nkb + s - 1) / s;
-    return (nkb + per - 1) / per;
+    const int slots = 2 * device_sm_count();
+    if (plan == kGemmRowInvariant) {
+        int s = (slots / 2 + ntiles - 1) / ntiles;          // about half a wave per row tile
+        s = max(1, min(s, nkb / 8));
+        const int per = (nkb + s - 1) / s;
+        return (nkb + per - 1) / per;
+    }
+    int best_s = 1;
+    long best_cost = -1;
+    for (int s = 1; s <= 16 && s <= nkb; ++s) {
+        const int per = (nkb + s - 1) / s;
+        const int se = (nkb + per - 1) / per;
+        const long waves = ((long)ntiles * se + slots - 1) / slots;
+        // time ~ waves x (K slices + about two slices of fixed CTA cost); fewer splits on ties
+        const long cost = waves * (per + 2) * 64 + se;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_s = se;
+        }
+    }
+    return best_s;
 }
 
-size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K)
+size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K, int plan)
 {
     if (!gemm_uses_tensor_cores(dt, N, K)) return 0;
-    const int S = gemm_splits(N, K);
+    const int S = gemm_splits(N, K, plan);
     return S > 1 ? (size_t)S * M * N * 4 : 0;
 }
 
 cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
-                 int ldx, void *ws, int32_t *status, cudaStream_t st)
+                 int ldx, void *ws, int32_t *status, cudaStream_t st, int plan)
 {
     if (M <= 0) return cudaSuccess;
     if (gemm_uses_tensor_cores(dt, N, K)) {
@@ -287,7 +306,7 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
             !tma_map_bf16_3d(&mw, w, N, K, 1, (uint64_t)N * 2, (uint64_t)N * 2 * K, 64, GK, 1))
             return cudaErrorInvalidValue;
         GemmArgs A;
-        A.S = gemm_splits(N, K);
+        A.S = gemm_splits(N, K, plan);
         const int nkb = K / GK;
         A.kb_per_split = (nkb + A.S - 1) / A.S;
         A.part = (float *)ws;

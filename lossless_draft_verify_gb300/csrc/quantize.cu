@@ -15,8 +15,12 @@
 // within rounding distance of a half-integer, so the codes are those of the
 // correctly rounded quotient.  HBM-bound: reads 2*32*d*2 bytes, writes one
 // record per group.
+#include <cooperative_groups.h>
+
 #include "vc_common.cuh"
 #include "vc_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace vc {
 namespace {
@@ -233,8 +237,10 @@ __global__ void residual_copy_kernel(const T *__restrict__ k, const T *__restric
 }
 
 // Append new tokens into the ring, then quantize every complete group that
-// left the residual window.  One CTA per sequence handles all its kv heads, so
-// the lengths of sequence b are read and written by exactly one CTA.
+// left the residual window.  Grid (Hc, B) in clusters of Hc = min(Hkv, 8)
+// CTAs: CTA r of sequence b handles kv heads r, r + Hc, ...; every CTA reads
+// the old lengths, and after a cluster barrier (all reads done) rank 0
+// publishes the new ones.
 // Commit mode (len_base, n_acc non-null): roll back to len_base[b] and take
 // n_acc[b] + 1 rows.  With n_new null every sequence takes max_new rows.
 template <typename T, int BITS, int D>
@@ -247,11 +253,13 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
 {
     using Gm = RecGeom<BITS, D>;
     __shared__ __align__(16) uint32_t img[Gm::REC / 4];
-    const int b = blockIdx.x;
+    const int rank = blockIdx.x, Hc = gridDim.x;
+    const int b = blockIdx.y;
+    const bool leader = rank == 0 && threadIdx.x == 0;
     const int ng0 = n_groups[b];
     int len0 = len_base ? len_base[b] : seq_len[b];
     if (len0 < ng0 * G) {
-        if (threadIdx.x == 0 && status) atomicOr(status, 2);
+        if (leader && status) atomicOr(status, 2);
         len0 = ng0 * G;
     }
     int nn = n_acc ? n_acc[b] + 1 : (n_new ? n_new[b] : max_new);
@@ -259,7 +267,7 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
     // unquantized tokens after the append must fit the ring
     const int room = res_cap - (len0 - ng0 * G);
     if (nn > room) {
-        if (threadIdx.x == 0 && status) atomicOr(status, 1);
+        if (leader && status) atomicOr(status, 1);
         nn = room > 0 ? room : 0;
     }
     const int len1 = len0 + nn;
@@ -267,7 +275,7 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
     if (requantize) {
         while ((ng1 + 1) * G <= len1 - residual && ng1 < max_groups) ++ng1;
     }
-    for (int h = 0; h < Hkv; ++h) {
+    for (int h = rank; h < Hkv; h += Hc) {
         const size_t bh = (size_t)b * Hkv + h;
         for (int i = threadIdx.x; i < nn * D; i += 2 * D) {
             const int t = i / D, c = i % D;
@@ -286,7 +294,8 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
             __syncthreads();
         }
     }
-    if (threadIdx.x == 0) {
+    cg::this_cluster().sync();
+    if (leader) {
         seq_len[b] = len1;
         n_groups[b] = ng1;
     }
@@ -314,11 +323,22 @@ cudaError_t launch_append(const vc_qcache *c, const void *kn, const void *vn, co
                           const int32_t *len_base, const int32_t *n_acc, int max_new, int requantize,
                           cudaStream_t st)
 {
-    append_kernel<T, BITS, D><<<c->B, 2 * D, 0, st>>>(
-        (const T *)kn, (const T *)vn, n_new, len_base, n_acc, max_new, c->Hkv, (T *)c->k_res,
-        (T *)c->v_res, c->res_cap, c->cfg.residual, requantize, c->max_groups,
-        (uint8_t *)c->records, c->n_groups, c->seq_len, c->status);
-    return cudaGetLastError();
+    const int hc = c->Hkv < 8 ? c->Hkv : 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(hc, c->B, 1);
+    cfg.blockDim = dim3(2 * D, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = hc;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_kernel<T, BITS, D>, (const T *)kn, (const T *)vn, n_new, len_base,
+                              n_acc, max_new, c->Hkv, (T *)c->k_res, (T *)c->v_res, c->res_cap,
+                              c->cfg.residual, requantize, c->max_groups, (uint8_t *)c->records, c->n_groups,
+                              c->seq_len, c->status);
 }
 
 template <typename T>

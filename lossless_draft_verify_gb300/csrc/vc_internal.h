@@ -43,13 +43,16 @@ cudaError_t drop_tokens(const float *scores, const void *k, const void *v, vc_dt
                         int H, int L, int d, int64_t keep_top, int64_t keep_recent,
                         int32_t *kept_idx, void *k_out, void *v_out, void *ws, cudaStream_t st);
 
-// gemm.cu: y = x W (+ resid), x [M][ldx] (first K columns), W [K][N], rows
-// independent of M.  ws: gemm_ws_bytes bytes of fp32 partials (bf16 path).
+// gemm.cu: y = x W (+ resid), x [M][ldx] (first K columns), W [K][N].  The
+// summation order of an output element depends on (N, K, plan) and the
+// device, never on M.  ws: gemm_ws_bytes bytes of fp32 partials (bf16 path).
+constexpr int kGemmRowInvariant = 0;   // forward passes (verify, plain decoding, prefill)
+constexpr int kGemmDecode = 1;         // draft steps (M <= 128)
 bool gemm_uses_tensor_cores(vc_dtype dt, int N, int K);
-int gemm_splits(int N, int K);
-size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K);
+int gemm_splits(int N, int K, int plan);
+size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K, int plan = kGemmRowInvariant);
 cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
-                 int ldx, void *ws, int32_t *status, cudaStream_t st);
+                 int ldx, void *ws, int32_t *status, cudaStream_t st, int plan = kGemmRowInvariant);
 
 // host_util.cu
 int device_sm_count();

@@ -494,12 +494,22 @@ TcPlan tc_plan(int B, int Dq, int Hkv, int grp, int max_ctx, int split_tiles)
     p.n_cta_m = p.n_mtiles / p.mt_per_cta;
     const int tiles = (max_ctx + Dq + TC_N - 1) / TC_N;
     const int items = B * Hkv * p.n_cta_m;
-    const int per_sm = p.mt_per_cta == 1 ? 2 : 1;
-    const int target = device_sm_count() * per_sm * 3;       // ~3 waves of resident CTAs
-    int s = (target + items - 1) / items;
-    if (s > tiles) s = tiles;
-    if (s < 1) s = 1;
-    p.tiles_per_split = (tiles + s - 1) / s;
+    const int slots = device_sm_count() * (p.mt_per_cta == 1 ? 2 : 1);
+    // Split count that minimises waves x (key tiles per CTA + ~4 tiles of
+    // fixed cost: setup, partial store) for resident CTAs of equal length.
+    int best = 1;
+    long best_t = -1;
+    for (int s = 1; s <= 32 && s <= tiles; ++s) {
+        const int per = (tiles + s - 1) / s;
+        const int se = (tiles + per - 1) / per;
+        const long waves = ((long)items * se + slots - 1) / slots;
+        const long t = waves * (per + 4);
+        if (best_t < 0 || t < best_t) {
+            best_t = t;
+            best = se;
+        }
+    }
+    p.tiles_per_split = (tiles + best - 1) / best;
     if (p.tiles_per_split < 2 && tiles >= 2) p.tiles_per_split = 2;
     if (split_tiles > 0) p.tiles_per_split = split_tiles;
     p.n_split = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;

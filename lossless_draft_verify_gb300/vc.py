@@ -134,6 +134,8 @@ def load() -> ctypes.CDLL:
     L.vc_decoder_set_trace.argtypes = [P, P, P, c_int, c_int]
     L.vc_decoder_trace_count.restype = c_int
     L.vc_decoder_trace_count.argtypes = [P]
+    L.vc_gemm_splits.restype = c_int
+    L.vc_gemm_splits.argtypes = [c_int, c_int, c_int, c_int]
     L.vc_gemm_workspace_bytes.restype = c_size_t
     L.vc_gemm_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
     L.vc_gemm.restype = c_int
@@ -149,7 +151,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_accept_workspace_bytes", "vc_accept", "vc_accept_noalloc", "vc_swap_in",
             "vc_decoder_create", "vc_decoder_destroy", "vc_decoder_workspace_bytes", "vc_decoder_forward",
             "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm",
-            "vc_decoder_set_trace", "vc_decoder_trace_count"]
+            "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -369,6 +371,11 @@ def vc_swap_in(dst: torch.Tensor, src_pinned: torch.Tensor, nbytes: int | None =
 def vc_gemm_workspace_bytes(dtype, M, N, K) -> int:
     dt = VC_BF16 if dtype == torch.bfloat16 else VC_F32
     return int(load().vc_gemm_workspace_bytes(dt, M, N, K))
+
+
+def vc_gemm_splits(dtype, N, K, decode_plan: bool = False) -> int:
+    dt = VC_BF16 if dtype == torch.bfloat16 else VC_F32
+    return int(load().vc_gemm_splits(dt, N, K, int(bool(decode_plan))))
 
 
 def vc_gemm(x, w, out, resid=None, ws: Workspace | None = None, stream=None):
