@@ -19,8 +19,10 @@
 // with fp32 CUDA-core math.  The last CTA of each kv unit (device-scope counter
 // in the workspace, returned to zero after use) merges the split partials.
 //
-// Dense cache kernel (compacted dropped cache, or an uncompressed cache):
-// fp32 CUDA-core math over 32-token tiles staged by cp.async.bulk.
+// Dense cache kernels (compacted dropped cache, or an uncompressed cache):
+// bf16 caches use the same MMA structure with the K/V tiles as operands
+// (ldmatrix from padded rows); fp32 caches use CUDA-core math over 32-token
+// tiles staged by cp.async.bulk.
 #include "vc_common.cuh"
 #include "vc_internal.h"
 
@@ -765,6 +767,220 @@ draft_dense_kernel(DenseParams P)
                            reinterpret_cast<T *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
 }
 
+// ------------------------------------------------- dense kernel, bf16 MMA --
+// bf16 caches: the same per-warp ring and online softmax as the KIVI kernel,
+// with the K and V tiles themselves as MMA operands.  A warp takes 16-token
+// tiles; each row arrives by its own bulk copy into a padded shared-memory
+// row (pitch D*2 + 16 bytes), so the ldmatrix reads below are free of bank
+// conflicts.  S = K q (A = K rows via ldmatrix, B = q), P moves to the B
+// layout with movmatrix, O^T += V^T P (A = V^T via ldmatrix.trans).
+constexpr int DM_TOK = 16;                    // tokens per tile
+constexpr int DM_NST = 2;                     // ring stages per warp
+
+template <int D>
+struct DmGeom {
+    static constexpr int PITCH = D * 2 + 16;
+    static constexpr int TILE = DM_TOK * PITCH;              // one K or V tile
+    static constexpr int STAGE = 2 * TILE;
+    static constexpr int RING = NW * DM_NST * STAGE;
+    static constexpr int SMEM = 128 + RING;                  // barriers + rings (merge buffer reuses the rings)
+};
+
+__device__ __forceinline__ void mma16816_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+draft_dense_mma_kernel(DenseParams P)
+{
+    using Gm = DmGeom<D>;
+    constexpr int KS = D / 16;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *ring = smem + 128;
+    float *wbuf = reinterpret_cast<float *>(ring);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int unit = blockIdx.y, split = blockIdx.x;
+    const int b = unit / P.Hkv, kvh = unit % P.Hkv;
+    const int grp = P.grp;
+    float *dst = P.part + ((size_t)unit * P.n_split + split) * part_floats(D);
+    const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(P.q) + ((size_t)b * P.Hq + kvh * grp) * D;
+    // stale rows of a partial last tile must hold finite values (their p is 0)
+    for (int i = threadIdx.x; i < Gm::RING / 16; i += kThreads) reinterpret_cast<uint4 *>(ring)[i] = make_uint4(0, 0, 0, 0);
+    // B fragments of q: column n = gid is head gid (zero for gid >= grp)
+    uint32_t qf[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int c = 16 * ks + 2 * tig + 8 * rr;
+            if (gid < grp)
+                qf[ks][rr] = *reinterpret_cast<const uint32_t *>(qg + gid * D + c);
+            else
+                qf[ks][rr] = 0u;
+        }
+    const int len = P.seq_len[b];
+    const int ntile = (len + DM_TOK - 1) / DM_TOK;
+    const int t_lo = split * P.tiles_per_split, t_hi = min(ntile, t_lo + P.tiles_per_split);
+    const __nv_bfloat16 *kb = reinterpret_cast<const __nv_bfloat16 *>(P.k) + (size_t)unit * P.L_stride * D;
+    const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(P.v) + (size_t)unit * P.L_stride * D;
+    uint64_t *mybar = bars + warp * DM_NST;
+    uint8_t *myring = ring + (size_t)warp * DM_NST * Gm::STAGE;
+    if (lane == 0)
+        for (int s = 0; s < DM_NST; ++s) mbar_init(&mybar[s], 1);
+    fence_mbar_init();
+    __syncthreads();
+
+    const int n_mine = t_hi > t_lo + warp ? (t_hi - t_lo - warp + NW - 1) / NW : 0;
+    auto issue = [&](int s, int tile) {          // all lanes: lane t copies token row t (t < 16)
+        const int rows = min(DM_TOK, len - tile * DM_TOK);
+        if (lane == 0) mbar_arrive_expect_tx(&mybar[s], 2 * rows * D * 2);
+        __syncwarp();
+        if (lane < rows) {
+            uint8_t *d0 = myring + s * Gm::STAGE + lane * Gm::PITCH;
+            const size_t row = (size_t)tile * DM_TOK + lane;
+            bulk_g2s(d0, kb + row * D, D * 2, &mybar[s]);
+            bulk_g2s(d0 + Gm::TILE, vb + row * D, D * 2, &mybar[s]);
+        }
+    };
+    for (int s = 0; s < DM_NST && s < n_mine; ++s) issue(s, t_lo + warp + s * NW);
+
+    float m_run[2] = {kNegBig, kNegBig}, l_run[2] = {0.f, 0.f};
+    float o_acc[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+    bool ok = true;
+    // ldmatrix lane addressing
+    const int a_row = lane & 15, a_col = (lane >> 4) * 8;                       // K tile (non-transposed)
+    const int v_tok = (lane & 7) + ((lane >> 4) << 3), v_col = ((lane >> 3) & 1) * 8;   // V tile (transposed)
+    for (int it = 0; it < n_mine; ++it) {
+        const int st = it % DM_NST;
+        const int tile = t_lo + warp + it * NW;
+        if (!mbar_wait(&mybar[st], (it / DM_NST) & 1)) {
+            if (lane == 0) report_timeout(P.status, 4);
+            ok = false;
+            break;
+        }
+        const uint8_t *kt = myring + st * Gm::STAGE;
+        const uint8_t *vt = kt + Gm::TILE;
+        const int rows = min(DM_TOK, len - tile * DM_TOK);
+        // ---- scores: rows = tokens gid, gid + 8; columns = heads 2 tig, 2 tig + 1
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, kt + a_row * Gm::PITCH + (16 * ks + a_col) * 2);
+            mma16816_bf16(sc, a, qf[ks][0], qf[ks][1]);
+        }
+        float gmax[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool col_ok = 2 * tig + e < grp;
+            sc[e] = (col_ok && gid < rows) ? sc[e] * P.qscale : kNegBig;
+            sc[e + 2] = (col_ok && gid + 8 < rows) ? sc[e + 2] * P.qscale : kNegBig;
+            float mx = fmaxf(sc[e], sc[e + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            gmax[e] = mx;
+        }
+        float alpha[2] = {1.f, 1.f};
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            if (gmax[e] > m_run[e] + kLazy) {
+                alpha[e] = ex2(m_run[e] - gmax[e]);
+                m_run[e] = gmax[e];
+            }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o_acc[mt][0] *= alpha[0];
+                o_acc[mt][1] *= alpha[1];
+                o_acc[mt][2] *= alpha[0];
+                o_acc[mt][3] *= alpha[1];
+            }
+            l_run[0] *= alpha[0];
+            l_run[1] *= alpha[1];
+        }
+        float p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = ex2(sc[i] - m_run[i & 1]);
+        const uint32_t b0 = movmatrix_trans(pack_bf162(p[0], p[1]));
+        const uint32_t b1 = movmatrix_trans(pack_bf162(p[2], p[3]));
+        // the sum uses the bf16-rounded probabilities the MMA multiplies
+        l_run[0] += __bfloat162float(__float2bfloat16_rn(p[0])) + __bfloat162float(__float2bfloat16_rn(p[2]));
+        l_run[1] += __bfloat162float(__float2bfloat16_rn(p[1])) + __bfloat162float(__float2bfloat16_rn(p[3]));
+        // ---- values: O^T[channel][head] += V^T P
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(a, vt + v_tok * Gm::PITCH + (16 * mt + v_col) * 2);
+            mma16816_bf16(o_acc[mt], a, b0, b1);
+        }
+        __syncwarp();
+        if (it + DM_NST < n_mine) issue(st, t_lo + warp + (it + DM_NST) * NW);
+    }
+    if (!ok) {
+        m_run[0] = m_run[1] = kNegBig;
+        l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 4);
+        l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 8);
+        l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 16);
+    }
+    __syncthreads();   // every warp done with its ring before wbuf reuse
+    float *wm = wbuf, *wl = wbuf + NW * 4, *wo = wbuf + NW * 8;
+    if (tig < 2) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * tig + e;
+            if (gid == 0) {
+                wm[warp * 4 + h] = m_run[e];
+                wl[warp * 4 + h] = l_run[e];
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                wo[(warp * 4 + h) * D + 16 * mt + gid] = o_acc[mt][e];
+                wo[(warp * 4 + h) * D + 16 * mt + gid + 8] = o_acc[mt][e + 2];
+            }
+        }
+    }
+    cta_merge_store<D>(wbuf, dst, grp);
+    last_cta_combine<__nv_bfloat16, D>(P.part + (size_t)unit * P.n_split * part_floats(D), P.n_split,
+                                       P.counters + unit, grp,
+                                       reinterpret_cast<__nv_bfloat16 *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
+}
+
 // ----------------------------------------------------------------- host ----
 int num_sms()
 {
@@ -819,6 +1035,28 @@ struct DensePlan {
 DensePlan dense_plan(const vc_cache_view *v)
 {
     const int units = v->B * v->Hkv;
+    DensePlan p;
+    if (v->dt == VC_BF16) {
+        // bf16 MMA kernel: split count minimising waves x (tiles per warp + ~4
+        // tiles of fixed cost) for CTAs of equal length, 3 CTAs per SM
+        const int nt = (v->max_len + DM_TOK - 1) / DM_TOK;
+        const int slots = num_sms() * 3;
+        int best = 1;
+        long best_t = -1;
+        for (int s = 1; s <= kMaxSplit && s <= (nt + NW - 1) / NW; ++s) {
+            const int per = (nt + s - 1) / s;
+            const int se = (nt + per - 1) / per;
+            const long waves = ((long)units * se + slots - 1) / slots;
+            const long t = waves * ((per + NW - 1) / NW + 4);
+            if (best_t < 0 || t < best_t) {
+                best_t = t;
+                best = se;
+            }
+        }
+        p.tiles_per_split = nt > 0 ? (nt + best - 1) / best : 1;
+        p.n_split = nt > 0 ? (nt + p.tiles_per_split - 1) / p.tiles_per_split : 1;
+        return p;
+    }
     const int nt = (v->max_len + G - 1) / G;
     const int target_ctas = num_sms() * 4 * 2;
     int s = (target_ctas + units - 1) / units;
@@ -826,7 +1064,6 @@ DensePlan dense_plan(const vc_cache_view *v)
     if (s > max_s) s = max_s;
     if (s > kMaxSplit) s = kMaxSplit;
     if (s < 1) s = 1;
-    DensePlan p;
     p.tiles_per_split = nt > 0 ? (nt + s - 1) / s : 1;
     p.n_split = nt > 0 ? (nt + p.tiles_per_split - 1) / p.tiles_per_split : 1;
     return p;
@@ -888,6 +1125,17 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
     P.n_split = pl.n_split;
     P.tiles_per_split = pl.tiles_per_split;
     P.qscale = scale * kLog2e;
+    if constexpr (sizeof(T) == 2) {
+        using Gm = DmGeom<D>;
+        size_t smem = Gm::SMEM;
+        const size_t merge = 128 + (size_t)NW * part_floats(D) * 4;
+        if (smem < merge) smem = merge;
+        auto kern = draft_dense_mma_kernel<D>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        dim3 grid(pl.n_split, v->B * v->Hkv);
+        kern<<<grid, kThreads, smem, st>>>(P);
+        return cudaGetLastError();
+    }
     constexpr int PER = 16 / sizeof(T);
     const size_t qbytes = (size_t)(D / PER) * (4 * PER + 4) * 4;
     size_t smem = 128 + qbytes + (size_t)NW * DENSE_NST * 2 * G * D * sizeof(T);

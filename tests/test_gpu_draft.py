@@ -72,10 +72,11 @@ def test_draft_kivi_spare_capacity_and_ragged_lengths():
         assert_attn_close(out[b:b + 1], want, what=f"seq {b}")
 
 
-@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
-def test_draft_dense_matches_oracle(dtype, d):
+@pytest.mark.parametrize("dtype,d,Hq", [(torch.bfloat16, 128, 8), (torch.bfloat16, 64, 4), (torch.bfloat16, 128, 2),
+                                        (torch.float32, 64, 8)])
+def test_draft_dense_matches_oracle(dtype, d, Hq):
     vc = lib()
-    B, Hq, Hkv, Ls = 3, 8, 2, 700
+    B, Hkv, Ls = 3, 2, 700
     k, v = inputs.kv_with_outliers(B, Hkv, Ls, d, seed=9, device="cuda", dtype=dtype, n_out=0)
     q = inputs.normal_bf16((B, Hq, d), 19, device="cuda").to(dtype)
     lens = torch.tensor([700, 333, 1], dtype=torch.int32, device="cuda")
@@ -86,6 +87,28 @@ def test_draft_dense_matches_oracle(dtype, d):
     torch.cuda.synchronize()
     want = oracle.dense_decode_attn(f32(q), f32(k), f32(v), lens.cpu().numpy(), 0.1)
     assert_attn_close(out, want, what="dense")
+
+
+def test_draft_dense_compacted_workload_sampled():
+    """Decode attention over a compacted cache of the token-dropping workload's
+    shape ([4, 8, 33024, 128] bf16, 32/8 heads); sampled sequences against the
+    oracle."""
+    vc = lib()
+    B, Hq, Hkv, L, d = 4, 32, 8, 33024, 128
+    k, v = inputs.kv_with_outliers(B, Hkv, L, d, seed=12, device="cuda", n_out=0)
+    q = inputs.normal_bf16((B, Hq, d), 13, device="cuda")
+    lens = torch.tensor([L, L - 5, 17, L], dtype=torch.int32, device="cuda")
+    view = vc.dense_view(k, v, lens, L)
+    ws = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, Hq))
+    out = torch.empty_like(q)
+    scale = inputs.default_scale(d)
+    vc.vc_draft_attn(q, view, scale, out, ws)
+    torch.cuda.synchronize()
+    assert vc.vc_poll_status(ws) == 0
+    for b in (1, 2):
+        want = oracle.dense_decode_attn(f32(q[b:b + 1]), f32(k[b:b + 1]), f32(v[b:b + 1]),
+                                        lens[b:b + 1].cpu().numpy(), scale)
+        assert_attn_close(out[b:b + 1], want, what=f"seq {b}")
 
 
 def test_draft_full_size_sampled():
