@@ -347,7 +347,7 @@ draft_kivi_kernel(KiviParams P)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const int unit = blockIdx.y, split = blockIdx.x;
+    const int unit = blockIdx.x, split = blockIdx.y;   // long splits first, residual split last
     const int b = unit / P.Hkv, kvh = unit % P.Hkv;
     const int grp = P.grp;
     float *dst = P.part + ((size_t)unit * (P.n_split_q + 1) + split) * part_floats(D);
@@ -366,6 +366,21 @@ draft_kivi_kernel(KiviParams P)
         const uint8_t *rec_base = P.records + (size_t)unit * P.max_groups * REC;
         uint64_t *mybar = bars + warp * NST;
         uint8_t *myring = ring + (size_t)warp * NST * STAGE;
+        const int n_pairs = (g_hi - g_lo + 1) / 2;
+        const int n_mine = n_pairs > warp ? (n_pairs - warp + NW - 1) / NW : 0;
+        auto issue = [&](int s, int it) {
+            const int g = g_lo + 2 * (warp + it * NW);
+            const uint32_t bytes = (g + 1 < g_hi ? 2 : 1) * REC;
+            mbar_arrive_expect_tx(&mybar[s], bytes);
+            bulk_g2s(myring + s * STAGE, rec_base + (size_t)g * REC, bytes, &mybar[s]);
+        };
+        // each warp's first records are requested before anything else, so the
+        // memory latency overlaps the q setup below
+        if (lane == 0) {
+            for (int s = 0; s < NST; ++s) mbar_init(&mybar[s], 1);
+            fence_mbar_init();
+            for (int s = 0; s < NST && s < n_mine; ++s) issue(s, s);
+        }
         // B fragments of q (column n = gid): heads 0..3 scaled by 2^(-b e) for
         // the channel's code exponent, copies 4..7 unscaled (zero-point sums)
         uint32_t qf[KS][2];
@@ -383,20 +398,7 @@ draft_kivi_kernel(KiviParams P)
                     qf[ks][rr] = pack_half2(a, bb);
                 }
         }
-        if (lane == 0)
-            for (int s = 0; s < NST; ++s) mbar_init(&mybar[s], 1);
-        fence_mbar_init();
-        __syncthreads();
-        const int n_pairs = (g_hi - g_lo + 1) / 2;
-        const int n_mine = n_pairs > warp ? (n_pairs - warp + NW - 1) / NW : 0;
-        auto issue = [&](int s, int it) {
-            const int g = g_lo + 2 * (warp + it * NW);
-            const uint32_t bytes = (g + 1 < g_hi ? 2 : 1) * REC;
-            mbar_arrive_expect_tx(&mybar[s], bytes);
-            bulk_g2s(myring + s * STAGE, rec_base + (size_t)g * REC, bytes, &mybar[s]);
-        };
-        if (lane == 0)
-            for (int s = 0; s < NST && s < n_mine; ++s) issue(s, s);
+        __syncthreads();                                  // ones / zeros written
 
         float m_run[2] = {kNegBig, kNegBig}, l_run[2] = {0.f, 0.f};
         float o_acc[KS][4];
@@ -1099,7 +1101,7 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     if (smem < merge) smem = merge;
     auto kern = draft_kivi_kernel<BITS, D, TQ, TR>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    dim3 grid(pl.n_split_q + 1, c->B * c->Hkv);
+    dim3 grid(c->B * c->Hkv, pl.n_split_q + 1);
     kern<<<grid, kThreads, smem, st>>>(P);
     return cudaGetLastError();
 }
