@@ -2,7 +2,10 @@
 
 One step = one VeriCache round over a synthetic 32k-context batch (16
 sequences, 32 query / 8 kv heads, head dim 128):
-  side stream: swap the full bf16 KV cache (2.15 GB) in from pinned host memory;
+  side stream: swap the full bf16 KV cache (2.15 GB) in from pinned host memory,
+               one half batch after the other (--stagger 2, the default): the
+               verify of the first half overlaps the swap of the second, and a
+               half's next swap waits only for this step's verify of that half;
   main stream: 32 draft steps, each appending one token to the 2-bit KIVI cache
                and running draft attention over it (HBM-bound);
                wait for the swap; verify attention of the 33-token block over
@@ -140,7 +143,15 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 
 class Round:
-    def __init__(self, dev):
+    """One step of the hot path for all B sequences.  With stagger = 2 the
+    full-cache swap-in and the verify pass run per half batch (cross-resource
+    staggering, paper page "What the paper found"): half A's verify starts as
+    soon as half A has arrived, while half B is still on the link, and the
+    next step's swap of a half only waits for this step's verify of that half,
+    so the host link never idles between steps.  Drafting, acceptance and the
+    commit stay whole-batch launches."""
+
+    def __init__(self, dev, stagger: int = 2):
         from lossless_draft_verify_gb300 import inputs, vc
         self.vc, self.dev = vc, dev
         g = torch.Generator(device=dev)
@@ -180,14 +191,23 @@ class Round:
         self.next_tok = torch.zeros(B, dtype=torch.int32, device=dev)
         # workspaces
         self.ws_d = vc.Workspace(vc.vc_draft_attn_workspace_bytes(self.view, HQ), device=dev)
-        self.ws_v = vc.Workspace(vc.vc_verify_attn_workspace_bytes(torch.bfloat16, B, DQ, HQ, HKV, D_HEAD, CTX),
+        assert B % stagger == 0
+        self.stagger = stagger
+        bp = B // stagger
+        self.parts = [(i * bp, (i + 1) * bp) for i in range(stagger)]
+        self.ws_v = vc.Workspace(vc.vc_verify_attn_workspace_bytes(torch.bfloat16, bp, DQ, HQ, HKV, D_HEAD, CTX),
                                  device=dev)
         self.ws_a = vc.Workspace(vc.vc_accept_workspace_bytes(B, HORIZON, VOCAB), device=dev)
         self.side = torch.cuda.Stream(device=dev)
-        self.ev_swap = torch.cuda.Event()
-        self.ev_swap.record(self.side)
-        # per step: (append + draft) per draft step, verify + its combine, accept, commit
-        self.launches_per_step = HORIZON * 2 + 2 + 1 + 1
+        main = torch.cuda.current_stream()
+        self.ev_swap = [torch.cuda.Event() for _ in self.parts]
+        self.ev_ver = [torch.cuda.Event() for _ in self.parts]
+        self.ev_acc = torch.cuda.Event()
+        self.ev_in = torch.cuda.Event()
+        for e in self.ev_swap + self.ev_ver + [self.ev_acc, self.ev_in]:
+            e.record(main)
+        # per step: (append + draft) per draft step, verify + its combine per part, accept, commit
+        self.launches_per_step = HORIZON * 2 + 2 * stagger + 1 + 1
         # host-side copies of the per-step inputs (end-to-end measurement)
         self.h_q_draft = self.q_draft.cpu().pin_memory()
         self.h_k_step = self.k_step.cpu().pin_memory()
@@ -206,19 +226,26 @@ class Round:
     def step(self, ev=None, e2e=False):
         vc, main = self.vc, torch.cuda.current_stream()
         if e2e:
-            # this round's inputs arrive from pinned host memory
-            self.q_draft.copy_(self.h_q_draft, non_blocking=True)
-            self.k_step.copy_(self.h_k_step, non_blocking=True)
-            self.v_step.copy_(self.h_v_step, non_blocking=True)
-            self.q_ver.copy_(self.h_q_ver, non_blocking=True)
-            self.logits.copy_(self.h_logits, non_blocking=True)
-            self.drafts.copy_(self.h_drafts, non_blocking=True)
-        # swap-in of the full cache on the side stream, overlapped with drafting
-        self.side.wait_stream(main)
-        if ev is not None:
-            ev["swap0"].record(self.side)
-        vc.vc_swap_in(self.kfull, self.kfull_host, stream=self.side)
-        vc.vc_swap_in(self.vfull, self.vfull_host, stream=self.side, done_event=self.ev_swap)
+            # this round's inputs arrive from pinned host memory, on the link's
+            # stream ahead of the swap (once the previous step has read them)
+            self.side.wait_event(self.ev_acc)
+            with torch.cuda.stream(self.side):
+                self.q_draft.copy_(self.h_q_draft, non_blocking=True)
+                self.k_step.copy_(self.h_k_step, non_blocking=True)
+                self.v_step.copy_(self.h_v_step, non_blocking=True)
+                self.q_ver.copy_(self.h_q_ver, non_blocking=True)
+                self.logits.copy_(self.h_logits, non_blocking=True)
+                self.drafts.copy_(self.h_drafts, non_blocking=True)
+            self.ev_in.record(self.side)
+            main.wait_event(self.ev_in)
+        # swap-in of the full cache on the side stream, overlapped with drafting;
+        # part p may be overwritten once the previous step's verify of p is done
+        for p, (b0, b1) in enumerate(self.parts):
+            self.side.wait_event(self.ev_ver[p])
+            if ev is not None and p == 0:
+                ev["swap0"].record(self.side)
+            vc.vc_swap_in(self.kfull[b0:b1], self.kfull_host[b0:b1], stream=self.side)
+            vc.vc_swap_in(self.vfull[b0:b1], self.vfull_host[b0:b1], stream=self.side, done_event=self.ev_swap[p])
         if ev is not None:
             ev["swap1"].record(self.side)
         for j in range(HORIZON):
@@ -228,13 +255,17 @@ class Round:
             vc.vc_draft_attn(self.q_draft[j], self.view, self.scale, self.o_draft[j], self.ws_d)
             if ev is not None:
                 ev["d1"][j].record(main)
-        main.wait_event(self.ev_swap)
-        if ev is not None:
-            ev["v0"].record(main)
-        vc.vc_verify_attn(self.q_ver, self.kfull, self.vfull, self.ctx, CTX, self.scale, self.o_ver, self.ws_v)
-        if ev is not None:
-            ev["v1"].record(main)
+        for p, (b0, b1) in enumerate(self.parts):
+            main.wait_event(self.ev_swap[p])
+            if ev is not None:
+                ev["v0"][p].record(main)
+            vc.vc_verify_attn(self.q_ver[b0:b1], self.kfull[b0:b1], self.vfull[b0:b1], self.ctx[b0:b1], CTX,
+                              self.scale, self.o_ver[b0:b1], self.ws_v)
+            if ev is not None:
+                ev["v1"][p].record(main)
+            self.ev_ver[p].record(main)
         vc.vc_accept(self.logits, self.drafts, self.n_acc, self.next_tok, self.ws_a)
+        self.ev_acc.record(main)
         if ev is not None:
             ev["a1"].record(main)
         vc.vc_qcache_commit(self.cache, self.k_blk, self.v_blk, self.round_len, self.n_acc)
@@ -264,10 +295,10 @@ class Round:
         return 4 * D_HEAD * B * HQ * rows_keys
 
 
-def make_events(n_draft):
+def make_events(n_draft, n_parts=1):
     mk = lambda: torch.cuda.Event(enable_timing=True)
-    return {"swap0": mk(), "swap1": mk(), "v0": mk(), "v1": mk(), "a1": mk(),
-            "d0": [mk() for _ in range(n_draft)], "d1": [mk() for _ in range(n_draft)]}
+    return {"swap0": mk(), "swap1": mk(), "v0": [mk() for _ in range(n_parts)], "v1": [mk() for _ in range(n_parts)],
+            "a1": mk(), "d0": [mk() for _ in range(n_draft)], "d1": [mk() for _ in range(n_draft)]}
 
 
 # --------------------------------------------------------------------------
@@ -693,6 +724,8 @@ def main():
     ap.add_argument("--dq", type=int, default=32, help="verify block size for --kernel verify")
     ap.add_argument("--batch", type=int, default=B, help="sequences for --kernel draft/verify")
     ap.add_argument("--chunks", type=int, default=1, help="side streams for --kernel swap")
+    ap.add_argument("--stagger", type=int, default=2, choices=[1, 2],
+                    help="round workload: swap and verify per half batch (2) or whole batch (1)")
     ap.add_argument("--workload", default="round", choices=["round", "model"],
                     help="round: one layer's hot path at 32k (B16); model: the 8-layer decoder end to end")
     ap.add_argument("--prompt", type=int, default=32768, help="prompt tokens per sequence (--workload model)")
@@ -730,12 +763,12 @@ def main():
         if pg is not None:
             pg.destroy_process_group()
         return
-    rnd = Round(dev)
+    rnd = Round(dev, stagger=args.stagger)
 
     for _ in range(args.warmup):
         rnd.step()
     barrier()
-    evs = [make_events(HORIZON) for _ in range(args.steps)]
+    evs = [make_events(HORIZON, rnd.stagger) for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -759,8 +792,8 @@ def main():
     # per-kernel times from the events
     d_ms = [e["d0"][j].elapsed_time(e["d1"][j]) for e in evs for j in range(HORIZON)]
     d_bytes = [rnd.draft_bytes(j) for _ in evs for j in range(HORIZON)]
-    v_ms = [e["v0"].elapsed_time(e["v1"]) for e in evs]
-    a_ms = [e["v1"].elapsed_time(e["a1"]) for e in evs]
+    v_ms = [sum(a.elapsed_time(b) for a, b in zip(e["v0"], e["v1"])) for e in evs]
+    a_ms = [e["v1"][-1].elapsed_time(e["a1"]) for e in evs]
     s_ms = [e["swap0"].elapsed_time(e["swap1"]) for e in evs]
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
     draft_gbs = sum(d_bytes) / (sum(d_ms) / 1e3) / 1e9
@@ -798,7 +831,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": CTX,
-                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
+                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)",
+                       "stagger": rnd.stagger},
             "roofline": {"bound": "hbm", "achieved": draft_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": draft_gbs / hbm,
                          "traffic": captured_traffic(DRAFT_TRAFFIC, statistics.mean(d_bytes)),
