@@ -444,7 +444,7 @@ def run_kernel(args, dev):
         fn = lambda: vc.vc_accept(case.logits, case.drafts, n, nx, ws)
         nbytes = case.logits.numel() * 2
         rec = {"workload": "greedy acceptance, logits [16,33,151936] bf16"}
-    elif name in ("drop", "dense_draft"):
+    elif name in ("drop", "dense_draft", "dense_draft_h2o"):
         Bd, Hd, Ld = 4, 8, 131072
         scores = inputs.zipf_scores(Bd, Hd, Ld, seed=0, device=dev)
         k, v = inputs.kv_with_outliers(Bd, Hd, Ld, D_HEAD, seed=8, device=dev, n_out=0)
@@ -466,9 +466,19 @@ def run_kernel(args, dev):
             view = vc.dense_view(ko, vo, lens, n_keep)
             ws2 = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, 4 * Hd), device=dev)
             scale = inputs.default_scale(D_HEAD)
-            fn = lambda: vc.vc_draft_attn(q, view, scale, out, ws2)
-            nbytes = 2 * ko.numel() * 2 + 2 * q.numel() * 2
-            rec = {"workload": "decode attention over the compacted cache [4,8,33024,128] bf16, 32/8 heads"}
+            if name == "dense_draft":
+                fn = lambda: vc.vc_draft_attn(q, view, scale, out, ws2)
+                nbytes = 2 * ko.numel() * 2 + 2 * q.numel() * 2
+                rec = {"workload": "decode attention over the compacted cache [4,8,33024,128] bf16, 32/8 heads"}
+            else:
+                acc = torch.zeros(Bd, Hd, Ld, dtype=torch.float32, device=dev)
+                ws3 = vc.Workspace(vc.vc_draft_attn_h2o_workspace_bytes(view, 4 * Hd), device=dev)
+                fn = lambda: vc.vc_draft_attn_h2o(q, view, scale, out, acc, ws3, kept_idx=kept)
+                # attention bytes + per kept row: scores written and read (16 B each), the
+                # index read (4 B) and the accumulated score read and written (8 B)
+                nbytes = 2 * ko.numel() * 2 + 2 * q.numel() * 2 + kept.numel() * (16 + 16 + 4 + 8)
+                rec = {"workload": "decode attention over the compacted cache [4,8,33024,128] bf16, 32/8 heads, "
+                                   "with H2O score accumulation at the kept positions"}
     elif name == "swap":
         # full-cache swap-in (host link): one copy, or the cache split in
         # chunks issued on as many side streams

@@ -257,6 +257,26 @@ vc_status vc_draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view,
                         float sm_scale, void *out, void *ws, size_t ws_bytes,
                         cudaStream_t stream);
 
+/*
+ * vc_draft_attn_h2o -- vc_draft_attn over a dense bf16 view that also
+ * accumulates attention scores for token dropping (H2O, source 3 on the
+ * podparley page: tokens are ranked by the attention mass they have received
+ * so far).  For kv unit u = b*Hkv + h and cached row j < seq_len[b]:
+ *   scores[u * scores_stride + pos] += sum over the Hq/Hkv query heads of h
+ *       of softmax_j(q . k_j * sm_scale),   pos = kept_idx ? kept_idx[u * kept_stride + j] : j
+ * (kept_idx maps rows of a compacted cache back to original positions, as
+ * vc_drop_tokens writes it).  The probabilities are those of this call's
+ * attention: each head's scores are stored in fp32 and normalised by the
+ * head's final max and sum after the split merge.  scores: device fp32, rows
+ * of one unit distinct positions.  Workspace: vc_draft_attn_h2o_workspace_bytes
+ * (the attention's plus 16 bytes per cached row).  VC_ERR_UNSUPPORTED for
+ * KIVI or fp32 views.
+ */
+size_t vc_draft_attn_h2o_workspace_bytes(const vc_cache_view *view, int Hq);
+vc_status vc_draft_attn_h2o(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq, float sm_scale,
+                            void *out, float *scores, int scores_stride, const int32_t *kept_idx, int kept_stride,
+                            void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* (4) verify attention over the full cache                                  */
 /* ------------------------------------------------------------------------ */

@@ -23,6 +23,8 @@
 // bf16 caches use the same MMA structure with the K/V tiles as operands
 // (ldmatrix from padded rows); fp32 caches use CUDA-core math over 32-token
 // tiles staged by cp.async.bulk.
+#include <algorithm>
+
 #include "vc_common.cuh"
 #include "vc_internal.h"
 
@@ -189,7 +191,7 @@ constexpr int kMaxSplit = 64;
 
 template <typename TO, int D>
 __device__ void last_cta_combine(const float *unit_part, int n_split, unsigned int *counter, int grp,
-                                 TO *out)
+                                 TO *out, float *ml_out = nullptr)
 {
     __shared__ bool is_last;
     __shared__ float wgt[4][kMaxSplit];
@@ -212,6 +214,10 @@ __device__ void last_cta_combine(const float *unit_part, int n_split, unsigned i
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
         for (int s = 0; s < n_split; ++s) wgt[h][s] *= inv;
+        if (ml_out) {
+            ml_out[h] = M;
+            ml_out[4 + h] = L;
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < grp * D; i += kThreads) {
@@ -624,6 +630,9 @@ struct DenseParams {
     int32_t *status;
     int Hkv, Hq, grp, L_stride, n_split, tiles_per_split;
     float qscale;
+    float *raw;                                        // optional [units][max_len][4] log2-domain scores
+    float *ml;                                         // optional [units][8]: final max, sum per head
+    int max_len;
 };
 
 template <typename T, int D>
@@ -906,6 +915,12 @@ draft_dense_mma_kernel(DenseParams P)
             const bool col_ok = 2 * tig + e < grp;
             sc[e] = (col_ok && gid < rows) ? sc[e] * P.qscale : kNegBig;
             sc[e + 2] = (col_ok && gid + 8 < rows) ? sc[e + 2] * P.qscale : kNegBig;
+            if (P.raw && col_ok) {
+                // H2O: keep every visible score for the mass pass after the combine
+                float *rw = P.raw + ((size_t)unit * P.max_len + (size_t)tile * DM_TOK + gid) * 4 + 2 * tig + e;
+                if (gid < rows) rw[0] = sc[e];
+                if (gid + 8 < rows) rw[8 * 4] = sc[e + 2];
+            }
             float mx = fmaxf(sc[e], sc[e + 2]);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -980,7 +995,37 @@ draft_dense_mma_kernel(DenseParams P)
     cta_merge_store<D>(wbuf, dst, grp);
     last_cta_combine<__nv_bfloat16, D>(P.part + (size_t)unit * P.n_split * part_floats(D), P.n_split,
                                        P.counters + unit, grp,
-                                       reinterpret_cast<__nv_bfloat16 *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
+                                       reinterpret_cast<__nv_bfloat16 *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D,
+                                       P.ml ? P.ml + (size_t)unit * 8 : nullptr);
+}
+
+// H2O mass pass: scores[unit][pos] += sum over the unit's query heads of
+// softmax probability of cached token j (pos = kept_idx[unit][j], or j), from
+// the stored log2-domain scores and each head's final max and sum.
+__global__ void h2o_accumulate_kernel(const float *__restrict__ raw, const float *__restrict__ ml,
+                                      const int32_t *__restrict__ seq_len, int max_len, int Hkv, int grp,
+                                      const int32_t *__restrict__ kept_idx, int kept_stride, float *scores,
+                                      int scores_stride)
+{
+    const int unit = blockIdx.y, b = unit / Hkv;
+    const int len = min(seq_len[b], max_len);
+    float M[4], invL[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        M[h] = ml[unit * 8 + h];
+        const float L = ml[unit * 8 + 4 + h];
+        invL[h] = (h < grp && L > 0.f) ? 1.f / L : 0.f;
+    }
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < len; j += gridDim.x * blockDim.x) {
+        const float4 r = *reinterpret_cast<const float4 *>(raw + ((size_t)unit * max_len + j) * 4);
+        const float rv[4] = {r.x, r.y, r.z, r.w};
+        float mass = 0.f;
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            if (h < grp) mass += exp2f(rv[h] - M[h]) * invL[h];
+        const int pos = kept_idx ? kept_idx[(size_t)unit * kept_stride + j] : j;
+        scores[(size_t)unit * scores_stride + pos] += mass;
+    }
 }
 
 // ----------------------------------------------------------------- host ----
@@ -1108,10 +1153,13 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
 
 template <typename T, int D>
 cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float scale, void *out,
-                         void *ws, cudaStream_t st)
+                         void *ws, cudaStream_t st, float *raw = nullptr, float *ml = nullptr)
 {
     const DensePlan pl = dense_plan(v);
     DenseParams P;
+    P.raw = raw;
+    P.ml = ml;
+    P.max_len = v->max_len;
     P.q = q;
     P.k = v->k;
     P.v = v->v;
@@ -1168,6 +1216,13 @@ cudaError_t kivi_by_bits(const void *q, const vc_qcache *c, int Hq, float s, voi
 
 }  // namespace
 
+size_t draft_h2o_ws_bytes(const vc_cache_view *view, int Hq)
+{
+    if (view->kind != VC_CACHE_DENSE) return 0;
+    return draft_ws_bytes(view, Hq) + align256((size_t)view->B * view->Hkv * 8 * 4) +
+           align256((size_t)view->B * view->Hkv * view->max_len * 4 * 4);
+}
+
 size_t draft_ws_bytes(const vc_cache_view *view, int Hq)
 {
     (void)Hq;
@@ -1198,6 +1253,30 @@ cudaError_t draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view, 
                                    : launch_dense<float, 128>(q, view, Hq, sm_scale, out, ws, st);
     return view->dt == VC_BF16 ? launch_dense<__nv_bfloat16, 64>(q, view, Hq, sm_scale, out, ws, st)
                                : launch_dense<float, 64>(q, view, Hq, sm_scale, out, ws, st);
+}
+
+}  // namespace vc
+
+namespace vc {
+
+cudaError_t draft_attn_h2o(const void *q, const vc_cache_view *view, int Hq, float sm_scale, void *out,
+                           float *scores, int scores_stride, const int32_t *kept_idx, int kept_stride, void *ws,
+                           cudaStream_t st)
+{
+    uint8_t *base = (uint8_t *)ws;
+    const size_t main_ws = draft_ws_bytes(view, Hq);
+    float *ml = (float *)(base + main_ws);
+    float *raw = (float *)(base + main_ws + align256((size_t)view->B * view->Hkv * 8 * 4));
+    const cudaError_t e = view->d == 128
+                              ? launch_dense<__nv_bfloat16, 128>(q, view, Hq, sm_scale, out, ws, st, raw, ml)
+                              : launch_dense<__nv_bfloat16, 64>(q, view, Hq, sm_scale, out, ws, st, raw, ml);
+    if (e != cudaSuccess) return e;
+    const int units = view->B * view->Hkv;
+    const int blocks = std::max(1, std::min(64, (view->max_len + 255) / 256));
+    h2o_accumulate_kernel<<<dim3(blocks, units), 256, 0, st>>>(raw, ml, view->seq_len, view->max_len, view->Hkv,
+                                                               Hq / view->Hkv, kept_idx, kept_stride, scores,
+                                                               scores_stride);
+    return cudaGetLastError();
 }
 
 }  // namespace vc

@@ -172,6 +172,31 @@ vc_status vc_draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view,
     return cuda_status(draft_attn(q, q_dt, view, Hq, sm_scale, out, ws, stream));
 }
 
+size_t vc_draft_attn_h2o_workspace_bytes(const vc_cache_view *view, int Hq)
+{
+    if (!view || view->kind != VC_CACHE_DENSE || view->dt != VC_BF16 || view->B <= 0 || view->Hkv <= 0 ||
+        view->max_len < 0 || Hq <= 0)
+        return 0;
+    return draft_h2o_ws_bytes(view, Hq);
+}
+
+vc_status vc_draft_attn_h2o(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq, float sm_scale,
+                            void *out, float *scores, int scores_stride, const int32_t *kept_idx, int kept_stride,
+                            void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!q || !view || !out || !scores || !ws || !aligned(ws, 256)) return VC_ERR_INVALID;
+    if (view->kind != VC_CACHE_DENSE || view->dt != VC_BF16 || q_dt != VC_BF16) return VC_ERR_UNSUPPORTED;
+    if (!view->k || !view->v || !view->seq_len || view->B <= 0 || view->Hkv <= 0) return VC_ERR_INVALID;
+    if (view->L_stride < view->max_len || view->max_len < 0) return VC_ERR_INVALID;
+    if (view->d != 64 && view->d != 128) return VC_ERR_UNSUPPORTED;
+    if (Hq <= 0 || Hq % view->Hkv || Hq / view->Hkv > 4) return VC_ERR_UNSUPPORTED;
+    if (!aligned(view->k, 16) || !aligned(view->v, 16) || !aligned(q, 4)) return VC_ERR_INVALID;
+    if (kept_idx ? kept_stride < view->max_len : scores_stride < view->max_len) return VC_ERR_INVALID;
+    if (ws_bytes < draft_h2o_ws_bytes(view, Hq)) return VC_ERR_INVALID;
+    return cuda_status(draft_attn_h2o(q, view, Hq, sm_scale, out, scores, scores_stride, kept_idx, kept_stride, ws,
+                                      stream));
+}
+
 size_t vc_verify_attn_workspace_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int max_ctx)
 {
     if (!dtype_ok(dt) || B <= 0 || Dq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_ctx < 0) return 0;

@@ -103,6 +103,11 @@ def load() -> ctypes.CDLL:
     L.vc_draft_attn_workspace_bytes.argtypes = [ctypes.POINTER(CacheView), c_int]
     L.vc_draft_attn.restype = c_int
     L.vc_draft_attn.argtypes = [P, c_int, ctypes.POINTER(CacheView), c_int, c_float, P, P, c_size_t, P]
+    L.vc_draft_attn_h2o_workspace_bytes.restype = c_size_t
+    L.vc_draft_attn_h2o_workspace_bytes.argtypes = [ctypes.POINTER(CacheView), c_int]
+    L.vc_draft_attn_h2o.restype = c_int
+    L.vc_draft_attn_h2o.argtypes = [P, c_int, ctypes.POINTER(CacheView), c_int, c_float, P, P, c_int, P, c_int, P,
+                                    c_size_t, P]
     L.vc_verify_attn_workspace_bytes.restype = c_size_t
     L.vc_verify_attn_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int, c_int]
     L.vc_verify_attn.restype = c_int
@@ -151,7 +156,8 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_accept_workspace_bytes", "vc_accept", "vc_accept_noalloc", "vc_swap_in",
             "vc_decoder_create", "vc_decoder_destroy", "vc_decoder_workspace_bytes", "vc_decoder_forward",
             "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm",
-            "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits"]
+            "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits",
+            "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -317,6 +323,22 @@ def vc_draft_attn(q: torch.Tensor, view: CacheView, sm_scale: float, out: torch.
     assert q.is_contiguous() and out.is_contiguous()
     _check(load().vc_draft_attn(q.data_ptr(), _dt(q), ctypes.byref(view), Hq, sm_scale, out.data_ptr(), ws.ptr,
                                 ws.nbytes, _stream(stream)), "vc_draft_attn")
+
+
+def vc_draft_attn_h2o_workspace_bytes(view: CacheView, Hq: int) -> int:
+    return int(load().vc_draft_attn_h2o_workspace_bytes(ctypes.byref(view), Hq))
+
+
+def vc_draft_attn_h2o(q: torch.Tensor, view: CacheView, sm_scale: float, out: torch.Tensor, scores: torch.Tensor,
+                      ws: Workspace, kept_idx: torch.Tensor | None = None, stream=None):
+    """scores: fp32 [B][Hkv][S] (S = original positions); kept_idx: int32
+    [B][Hkv][n_keep] mapping the view's rows to positions, or None."""
+    B, Hq, d = q.shape
+    assert q.is_contiguous() and out.is_contiguous() and scores.dtype == torch.float32 and scores.is_contiguous()
+    ks = kept_idx.shape[-1] if kept_idx is not None else 0
+    _check(load().vc_draft_attn_h2o(q.data_ptr(), _dt(q), ctypes.byref(view), Hq, sm_scale, out.data_ptr(),
+                                    scores.data_ptr(), scores.shape[-1], _ptr(kept_idx), ks, ws.ptr, ws.nbytes,
+                                    _stream(stream)), "vc_draft_attn_h2o")
 
 
 def vc_verify_attn_workspace_bytes(dtype, B, Dq, Hq, Hkv, d, max_ctx) -> int:

@@ -300,3 +300,27 @@ def drop_select(scores, keep_top: int, keep_recent: int) -> np.ndarray:
 def drop_gather(x, kept) -> np.ndarray:
     """Compacted cache: x [B,H,L,d] rows at the kept positions, in order."""
     return np.take_along_axis(np.asarray(x), np.asarray(kept)[..., None].astype(np.int64), axis=2)
+
+
+def h2o_mass(q, k, lens, scale: float) -> np.ndarray:
+    """Attention mass each cached token receives in one decode step, summed
+    over the query heads that read its kv head: the increment of H2O's
+    accumulated score (source 3 on the podparley page).  q [B,Hq,d], k
+    [B,Hkv,Ls,d]; out[b, h, j] = sum over q heads g of kv head h of
+    softmax_j(q[b,g] . k[b,h,j] * scale) for j < lens[b], 0 beyond (fp64)."""
+    q = _f32(q).astype(np.float64)
+    k = _f32(k).astype(np.float64)
+    B, Hq, d = q.shape
+    Hkv, Ls = k.shape[1], k.shape[2]
+    grp = Hq // Hkv
+    out = np.zeros((B, Hkv, Ls), np.float64)
+    for b in range(B):
+        n = int(lens[b])
+        if n <= 0:
+            continue
+        for g in range(Hq):
+            h = g // grp
+            s = (k[b, h, :n] @ q[b, g]) * scale
+            p = np.exp(s - s.max())
+            out[b, h, :n] += p / p.sum()
+    return out

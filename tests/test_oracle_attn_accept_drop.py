@@ -195,3 +195,50 @@ def test_drop_degenerate_sizes():
     k = np.arange(10 * 2, dtype=np.float32).reshape(1, 1, 10, 2)
     g = oracle.drop_gather(k, oracle.drop_select(s, 2, 1))
     assert g[0, 0, :, 0].tolist() == [14.0, 16.0, 18.0]
+
+
+# --------------------------------------------------------------------------
+# H2O accumulated-score increment (podparley source 3)
+# --------------------------------------------------------------------------
+
+def test_h2o_mass_sums_to_heads_per_kv_head():
+    rng = np.random.default_rng(4)
+    B, Hq, Hkv, L, d = 2, 8, 2, 50, 16
+    q = rng.standard_normal((B, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, L, d)).astype(np.float32)
+    lens = [50, 7]
+    m = oracle.h2o_mass(q, k, lens, 0.3)
+    for b in range(B):
+        for h in range(Hkv):
+            assert abs(m[b, h].sum() - Hq // Hkv) < 1e-12
+            assert (m[b, h, lens[b]:] == 0).all()
+            assert (m[b, h, :lens[b]] > 0).all()
+
+
+def test_h2o_mass_closed_forms():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, 4, 8)).astype(np.float32)
+    k = rng.standard_normal((1, 1, 9, 8)).astype(np.float32)
+    # one key: every head puts all its mass there
+    assert np.allclose(oracle.h2o_mass(q, k, [1], 1.0)[0, 0, 0], 4.0)
+    # equal keys: uniform
+    k[:] = k[:, :, :1]
+    m = oracle.h2o_mass(q, k, [9], 1.0)
+    assert np.allclose(m[0, 0], 4.0 / 9)
+
+
+def test_h2o_mass_equals_attention_weights_of_the_c_oracle():
+    """With one q head per kv head and V = identity rows, decode attention
+    returns the softmax weights themselves: the C oracle's attention and the
+    numpy mass must agree."""
+    rng = np.random.default_rng(6)
+    B, H, n, d = 2, 3, 12, 16
+    q = rng.standard_normal((B, H, d)).astype(np.float32)
+    k = rng.standard_normal((B, H, n, d)).astype(np.float32)
+    v = np.zeros((B, H, n, d), np.float32)
+    for j in range(n):
+        v[:, :, j, j] = 1.0
+    lens = np.array([12, 5], np.int32)
+    o = oracle.dense_decode_attn(q, k, v, lens, 0.25)
+    m = oracle.h2o_mass(q, k, lens, 0.25)
+    assert np.allclose(o[:, :, :n], m, atol=1e-12)
