@@ -531,7 +531,7 @@ def run_kernel(args, dev):
 
 M_B, M_HORIZON, M_BITS, M_RESIDUAL = 8, 32, 2, 128
 MODEL_WORKLOAD = ("decoder_e2e_{ctx}: 8-layer GQA decoder d4096 32/8 heads hd128 SwiGLU 14336 vocab 32000 bf16 "
-                  "(random init N(0,0.02), LM head x20), B8 random prompts of {ctx} tokens, KIVI 2-bit g32 R128 "
+                  "(random init N(0,0.02), LM head x20), B8 random prompts of {ctx} tokens, KIVI {bits}-bit g32 R128 "
                   "draft caches, horizon 32, full KV in pinned host memory swapped in every round")
 
 
@@ -553,7 +553,7 @@ def run_model(args, dev, rank, world, barrier, pg):
     n_e2e = 0 if args.no_e2e else 3
     total = args.warmup + args.steps + n_e2e
     max_len = P + total * (M_HORIZON + 1) + 64
-    run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=M_BITS, residual=M_RESIDUAL, host_cache=True,
+    run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=args.bits, residual=M_RESIDUAL, host_cache=True,
                                  prefill_chunk=512, device=dev)
     prompt = inputs.random_prompts(M_B, P, cfg.vocab, seed=rank, device=dev)
     t_pf = time.perf_counter()
@@ -627,7 +627,7 @@ def run_model(args, dev, rank, world, barrier, pg):
         n_cmp = min(n_cmp, args.check_tokens)
         del run
         torch.cuda.empty_cache()
-        ref = decode.VeriCacheRunner(dec, M_B, P + n_cmp + 64, M_HORIZON, bits=M_BITS, residual=M_RESIDUAL,
+        ref = decode.VeriCacheRunner(dec, M_B, P + n_cmp + 64, M_HORIZON, bits=args.bits, residual=M_RESIDUAL,
                                      host_cache=False, prefill_chunk=512, device=dev)
         ref.prefill(prompt)
         greedy = ref.greedy(n_cmp)
@@ -650,7 +650,7 @@ def run_model(args, dev, rank, world, barrier, pg):
         a[0] += 1
         a[1] += t
     ctx_mean = P + (args.warmup + args.steps / 2) * (float(n_acc.float().mean()) + 1)
-    rec_b = vc.vc_record_bytes(M_BITS, cfg.head_dim)
+    rec_b = vc.vc_record_bytes(args.bits, cfg.head_dim)
     draft_attn_bytes = M_B * cfg.n_kv_heads * (int((ctx_mean - M_RESIDUAL) // 32) * rec_b +
                                                2 * (M_RESIDUAL + 16) * cfg.head_dim * 2)
     kernels = {}
@@ -679,7 +679,8 @@ def run_model(args, dev, rank, world, barrier, pg):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
-            "config": {"workload": MODEL_WORKLOAD.format(ctx=P), "global_batch": M_B * world, "seq_len": P,
+            "config": {"workload": MODEL_WORKLOAD.format(ctx=P, bits=args.bits), "global_batch": M_B * world,
+                       "seq_len": P,
                        "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
             "roofline": roof,
             "phases_ms": {"draft_32_steps": d_ms, "verify_forward": v_ms, "accept_commit_writeback": c_ms,
@@ -741,6 +742,7 @@ def main():
     ap.add_argument("--prompt", type=int, default=32768, help="prompt tokens per sequence (--workload model)")
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")
+    ap.add_argument("--bits", type=int, default=2, choices=[2, 4], help="draft cache bits (--workload model)")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":

@@ -483,8 +483,8 @@ vc_status vc_kv_writeback(const void *k_blk, const void *v_blk, vc_dtype dt, int
 /*
  * vc_gemm -- out = x W (+ resid) with the decoder's GEMM: x [M][K], W [K][N],
  * resid and out [M][N] (resid may equal out), dt for all; fp32 accumulation.
- * The summation order of every output element depends on (N, K) and the
- * device only.  ws: vc_gemm_workspace_bytes(dt, M, N, K) bytes (may be 0).
+ * The summation order of every output element depends on (N, K), the plan and
+ * the device only.  ws: vc_gemm_workspace_bytes(dt, M, N, K) bytes (may be 0).
  */
 size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K);
 /* Number of K splits of the decoder's GEMM for (N, K): decode_plan != 0 gives
@@ -493,6 +493,12 @@ size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K);
 int vc_gemm_splits(vc_dtype dt, int N, int K, int decode_plan);
 vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
                   void *ws, size_t ws_bytes, cudaStream_t stream);
+/* vc_gemm with the split plan chosen explicitly: decode_plan != 0 runs the plan
+ * of vc_decoder_draft_step (for M <= 16 it loads only 16 rows of x per K slice
+ * and keeps six slices of W in flight); 0 is vc_gemm.  The workspace size from
+ * vc_gemm_workspace_bytes covers both plans. */
+vc_status vc_gemm_ex(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
+                     int decode_plan, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -11,6 +11,7 @@
 // verify pass therefore reproduces one-token decoding bit for bit.
 #include <cuda.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -607,17 +608,24 @@ int vc_gemm_splits(vc_dtype dt, int N, int K, int decode_plan)
 size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K)
 {
     if ((dt != VC_BF16 && dt != VC_F32) || M <= 0 || N <= 0 || K <= 0) return 0;
-    return gemm_ws_bytes(dt, M, N, K);
+    return std::max(gemm_ws_bytes(dt, M, N, K, kGemmRowInvariant), gemm_ws_bytes(dt, M, N, K, kGemmDecode));
+}
+
+vc_status vc_gemm_ex(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
+                     int decode_plan, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!x || !w || !out || (dt != VC_BF16 && dt != VC_F32) || M <= 0 || N <= 0 || K <= 0) return VC_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (resid && !aligned16(resid))) return VC_ERR_INVALID;
+    const int plan = decode_plan ? kGemmDecode : kGemmRowInvariant;
+    const size_t need = gemm_ws_bytes(dt, M, N, K, plan);
+    if (need && (!ws || ws_bytes < need || !aligned16(ws))) return VC_ERR_INVALID;
+    return to_status(gemm(x, w, resid, out, dt, M, N, K, K, ws, nullptr, stream, plan));
 }
 
 vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
                   void *ws, size_t ws_bytes, cudaStream_t stream)
 {
-    if (!x || !w || !out || (dt != VC_BF16 && dt != VC_F32) || M <= 0 || N <= 0 || K <= 0) return VC_ERR_INVALID;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (resid && !aligned16(resid))) return VC_ERR_INVALID;
-    const size_t need = gemm_ws_bytes(dt, M, N, K);
-    if (need && (!ws || ws_bytes < need || !aligned16(ws))) return VC_ERR_INVALID;
-    return to_status(gemm(x, w, resid, out, dt, M, N, K, K, ws, nullptr, stream));
+    return vc_gemm_ex(x, w, resid, out, dt, M, N, K, 0, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

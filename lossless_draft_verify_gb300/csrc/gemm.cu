@@ -13,7 +13,8 @@
 // bf16 (x [M][K] and W [K][N] row-major, N a multiple of 128, K of 64):
 // tcgen05 tensor cores.  One CTA per (128-row tile, 128-column tile, K split):
 // warp 0 issues TMA loads of 64-wide K slices (x K-major, W MN-major, 128-byte
-// swizzle) into a 3-stage ring (2 CTAs per SM), warp 1 issues tcgen05.mma (M128 N128 K16)
+// swizzle) into a 3-stage ring (2 CTAs per SM; draft steps with M <= 16 load
+// only 16 x rows per stage and keep 6 stages), warp 1 issues tcgen05.mma (M128 N128 K16)
 // into a TMEM accumulator, warps 2-5 read TMEM and write either the output
 // (one split) or fp32 partials that a second kernel sums in split order.
 // fp32 (any shape): CUDA cores, one output element per thread, K in order.
@@ -26,14 +27,27 @@
 namespace vc {
 namespace {
 
-constexpr int GM = 128, GN = 128, GK = 64, GSTAGES = 3;
+constexpr int GM = 128, GN = 128, GK = 64;
 constexpr int G_THREADS = 192;
-constexpr int G_STAGE_BYTES = GM * GK * 2 + GK * GN * 2;     // 16 KB x + 16 KB W
-constexpr int G_SMEM = GSTAGES * G_STAGE_BYTES + 256;
 constexpr uint32_t G_TMEM_COLS = 128;
+constexpr int G_MAX_STAGES = 6;
+
+// Shared-memory plan of one CTA: the x slices of every stage first, then the
+// W slices.  XR = x rows actually loaded per stage (128, or 16 for draft
+// steps with M <= 16: the MMA still reads 128 rows, the rows past 16 fall on
+// later x stages or on W data, and their accumulator rows are never stored).
+template <int XR, int STAGES>
+struct GemmGeom {
+    static constexpr int XB = XR * GK * 2;             // x bytes per stage
+    static constexpr int WB = GK * GN * 2;             // W bytes per stage (16 KB)
+    static constexpr int OFF_W = STAGES * XB;
+    static constexpr int OFF_BAR = OFF_W + STAGES * WB;
+    static constexpr int SMEM = OFF_BAR + 256;
+    static_assert(XR == 128 || OFF_W - XB + GM * GK * 2 <= OFF_BAR, "MMA read window must stay in shared memory");
+};
 
 struct GemmBars {
-    uint64_t full[GSTAGES], empty[GSTAGES], acc_full;
+    uint64_t full[G_MAX_STAGES], empty[G_MAX_STAGES], acc_full;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -54,16 +68,18 @@ __device__ __forceinline__ bool g_wait(uint64_t *bar, uint32_t parity, GemmBars 
     return false;
 }
 
+template <int XR, int GSTAGES>
 __global__ void __launch_bounds__(G_THREADS, 2)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, GemmArgs A)
 {
+    using Gg = GemmGeom<XR, GSTAGES>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
     if (smem_u32(sm) & 1023u) {
         if (threadIdx.x == 0) report_timeout(A.status, 98);
         return;
     }
-    GemmBars *B = reinterpret_cast<GemmBars *>(sm + GSTAGES * G_STAGE_BYTES);
+    GemmBars *B = reinterpret_cast<GemmBars *>(sm + Gg::OFF_BAR);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * GM;
     const int n0 = blockIdx.y * GN;
@@ -99,10 +115,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 const int s = i % GSTAGES;
                 if (i >= GSTAGES && !g_wait(&B->empty[s], ((i / GSTAGES) - 1) & 1, B, A.status, 41)) break;
                 if (*reinterpret_cast<volatile int32_t *>(&B->abort_flag)) break;
-                uint8_t *sx = sm + s * G_STAGE_BYTES;
-                uint8_t *sw = sx + GM * GK * 2;
+                uint8_t *sx = sm + s * Gg::XB;
+                uint8_t *sw = sm + Gg::OFF_W + s * Gg::WB;
                 const int k = (kb0 + i) * GK;
-                mbar_arrive_expect_tx(&B->full[s], G_STAGE_BYTES);
+                mbar_arrive_expect_tx(&B->full[s], Gg::XB + Gg::WB);
                 tc::tma_load_3d(sx, &tmX, k, m0, 0, &B->full[s]);
                 tc::tma_load_3d(sw, &tmW, n0, k, 0, &B->full[s]);
                 tc::tma_load_3d(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[s]);
@@ -116,8 +132,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 const int s = i % GSTAGES;
                 if (!g_wait(&B->full[s], (i / GSTAGES) & 1, B, A.status, 42)) { ok = false; break; }
                 tc::fence_after();
-                const uint32_t sx = smem_u32(sm + s * G_STAGE_BYTES);
-                const uint32_t sw = sx + GM * GK * 2;
+                const uint32_t sx = smem_u32(sm + s * Gg::XB);
+                const uint32_t sw = smem_u32(sm + Gg::OFF_W + s * Gg::WB);
 #pragma unroll
                 for (int kk = 0; kk < GK / 16; ++kk) {
                     // x: K-major rows of 128 B, 8-row atoms 1024 B apart
@@ -301,8 +317,9 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
 {
     if (M <= 0) return cudaSuccess;
     if (gemm_uses_tensor_cores(dt, N, K)) {
+        const bool small = plan == kGemmDecode && M <= 16;
         CUtensorMap mx, mw;
-        if (!tma_map_bf16_3d(&mx, x, K, M, 1, (uint64_t)ldx * 2, (uint64_t)ldx * 2 * M, GK, GM, 1) ||
+        if (!tma_map_bf16_3d(&mx, x, K, M, 1, (uint64_t)ldx * 2, (uint64_t)ldx * 2 * M, GK, small ? 16 : GM, 1) ||
             !tma_map_bf16_3d(&mw, w, N, K, 1, (uint64_t)N * 2, (uint64_t)N * 2 * K, 64, GK, 1))
             return cudaErrorInvalidValue;
         GemmArgs A;
@@ -316,9 +333,16 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         A.M = M;
         A.N = N;
         A.K = K;
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
         dim3 grid((M + GM - 1) / GM, N / GN, A.S);
-        gemm_tc_kernel<<<grid, G_THREADS, G_SMEM, st>>>(mx, mw, A);
+        if (small) {
+            using Gg = GemmGeom<16, 6>;
+            cudaFuncSetAttribute(gemm_tc_kernel<16, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gg::SMEM);
+            gemm_tc_kernel<16, 6><<<grid, G_THREADS, Gg::SMEM, st>>>(mx, mw, A);
+        } else {
+            using Gg = GemmGeom<128, 3>;
+            cudaFuncSetAttribute(gemm_tc_kernel<128, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gg::SMEM);
+            gemm_tc_kernel<128, 3><<<grid, G_THREADS, Gg::SMEM, st>>>(mx, mw, A);
+        }
         if (A.S > 1) {
             const size_t q = (size_t)M * N / 4;
             gemm_splitk_reduce<<<(unsigned)((q + 255) / 256), 256, 0, st>>>(A.part, A.S, M, N, A.resid, A.out);

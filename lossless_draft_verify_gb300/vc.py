@@ -145,6 +145,8 @@ def load() -> ctypes.CDLL:
     L.vc_gemm_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
     L.vc_gemm.restype = c_int
     L.vc_gemm.argtypes = [P, P, P, P, c_int, c_int, c_int, c_int, P, c_size_t, P]
+    L.vc_gemm_ex.restype = c_int
+    L.vc_gemm_ex.argtypes = [P, P, P, P, c_int, c_int, c_int, c_int, c_int, P, c_size_t, P]
     _lib = L
     return L
 
@@ -157,7 +159,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_decoder_create", "vc_decoder_destroy", "vc_decoder_workspace_bytes", "vc_decoder_forward",
             "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm",
             "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits",
-            "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o"]
+            "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -400,13 +402,13 @@ def vc_gemm_splits(dtype, N, K, decode_plan: bool = False) -> int:
     return int(load().vc_gemm_splits(dt, N, K, int(bool(decode_plan))))
 
 
-def vc_gemm(x, w, out, resid=None, ws: Workspace | None = None, stream=None):
+def vc_gemm(x, w, out, resid=None, ws: Workspace | None = None, stream=None, decode_plan: bool = False):
     M, K = x.shape
     K2, N = w.shape
     assert K == K2 and out.shape == (M, N) and x.is_contiguous() and w.is_contiguous() and out.is_contiguous()
-    _check(load().vc_gemm(x.data_ptr(), w.data_ptr(), _ptr(resid), out.data_ptr(), _dt(x), M, N, K,
-                          ws.ptr if ws is not None else None, ws.nbytes if ws is not None else 0,
-                          _stream(stream)), "vc_gemm")
+    _check(load().vc_gemm_ex(x.data_ptr(), w.data_ptr(), _ptr(resid), out.data_ptr(), _dt(x), M, N, K,
+                             int(bool(decode_plan)), ws.ptr if ws is not None else None,
+                             ws.nbytes if ws is not None else 0, _stream(stream)), "vc_gemm")
 
 
 class Decoder:

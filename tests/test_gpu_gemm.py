@@ -12,24 +12,26 @@ from helpers import f32, lib
 pytestmark = pytest.mark.gpu
 
 
-def _run(vc, x, w, resid=None):
+def _run(vc, x, w, resid=None, decode_plan=False):
     M, K = x.shape
     N = w.shape[1]
     out = torch.full((M, N), float("nan"), dtype=x.dtype, device="cuda")
     ws = vc.Workspace(vc.vc_gemm_workspace_bytes(x.dtype, M, N, K))
-    vc.vc_gemm(x, w, out, resid=resid, ws=ws)
+    vc.vc_gemm(x, w, out, resid=resid, ws=ws, decode_plan=decode_plan)
     torch.cuda.synchronize()
     return out
 
 
-@pytest.mark.parametrize("M,N,K", [(8, 384, 512), (300, 256, 1024), (1, 128, 64), (129, 640, 4096)])
-def test_gemm_bf16_matches_definition(M, N, K):
+@pytest.mark.parametrize("M,N,K,plan", [(8, 384, 512, False), (300, 256, 1024, False), (1, 128, 64, False),
+                                        (129, 640, 4096, False), (8, 6144, 4096, True), (16, 4096, 14336, True),
+                                        (3, 1024, 512, True), (40, 512, 1024, True)])
+def test_gemm_bf16_matches_definition(M, N, K, plan):
     vc = lib()
     x = inputs.normal_bf16((M, K), 1 + M, device="cuda")
     w = inputs.normal_bf16((K, N), 2 + N, device="cuda", std=0.02)
     r = inputs.normal_bf16((M, N), 3, device="cuda")
     for resid in (None, r):
-        got = f32(_run(vc, x, w, resid)).astype(np.float64)
+        got = f32(_run(vc, x, w, resid, decode_plan=plan)).astype(np.float64)
         want = f32(x).astype(np.float64) @ f32(w).astype(np.float64)
         if resid is not None:
             want = want + f32(resid)
