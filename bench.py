@@ -544,7 +544,7 @@ def model_bytes(cfg) -> dict:
 
 
 def run_model(args, dev, rank, world, barrier, pg):
-    from lossless_draft_verify_gb300 import decode, inputs, vc
+    from lossless_draft_verify_gb300 import decode, inputs, replicas, vc
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
     cfg = inputs.DecoderConfig()
     P = args.prompt
@@ -583,16 +583,9 @@ def run_model(args, dev, rank, world, barrier, pg):
     clk = clocks.stop()
     ops = trace.stop()
     ms = t0.elapsed_time(t1)
-    ms_t = torch.tensor([ms], device=dev)
-    if pg is not None:
-        pg.all_reduce(ms_t, op=pg.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
     n_acc = log.n_acc[args.warmup:args.warmup + args.steps].cpu()
     tokens = int((n_acc.long() + 1).sum())
-    tok_t = torch.tensor([tokens], device=dev, dtype=torch.float64)
-    if pg is not None:
-        pg.all_reduce(tok_t)
-    value = float(tok_t.item()) / (ms_max / 1e3)
+    value, ms_max = replicas.whole_job_rate(tokens, ms, pg, device=dev)
     st = vc.vc_poll_status(run.ws)
 
     # end to end: the same rounds, each reading its emitted tokens back to the host
@@ -613,10 +606,7 @@ def run_model(args, dev, rank, world, barrier, pg):
         e1.record()
         barrier()
         e_tok = int((log.n_acc[base:base + n_e2e].cpu().long() + 1).sum())
-        e_ms = torch.tensor([e0.elapsed_time(e1)], device=dev)
-        if pg is not None:
-            pg.all_reduce(e_ms, op=pg.ReduceOp.MAX)
-        e2e_val = world * e_tok / (float(e_ms.item()) / 1e3)
+        e2e_val, _ = replicas.whole_job_rate(e_tok, e0.elapsed_time(e1), pg, device=dev)
 
     # lossless check: the same prompts decoded greedily with the full cache
     # resident, token for token against the draft-and-verify output
@@ -762,8 +752,9 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
-    from lossless_draft_verify_gb300 import build
+    from lossless_draft_verify_gb300 import build, replicas
     build.build()
+
     def barrier():
         torch.cuda.synchronize()
         if pg is not None:
@@ -794,12 +785,8 @@ def main():
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     st = rnd.vc.vc_poll_status(rnd.ws_d) | rnd.vc.vc_poll_status(rnd.ws_v)
-    ms_t = torch.tensor([ms], device=dev)
-    if pg is not None:
-        pg.all_reduce(ms_t, op=pg.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
     tokens = rnd.tokens_per_round()
-    value = world * tokens * args.steps / (ms_max / 1e3)
+    value, ms_max = replicas.whole_job_rate(tokens * args.steps, ms, pg, device=dev)
 
     # per-kernel times from the events
     d_ms = [e["d0"][j].elapsed_time(e["d1"][j]) for e in evs for j in range(HORIZON)]
@@ -829,10 +816,7 @@ def main():
             rnd.step(e2e=True)
         e1.record()
         barrier()
-        ms_e2e = torch.tensor([e0.elapsed_time(e1)], device=dev)
-        if pg is not None:
-            pg.all_reduce(ms_e2e, op=pg.ReduceOp.MAX)
-        e2e_val = world * tokens * args.steps / (float(ms_e2e.item()) / 1e3)
+        e2e_val, _ = replicas.whole_job_rate(tokens * args.steps, e0.elapsed_time(e1), pg, device=dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

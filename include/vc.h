@@ -75,6 +75,17 @@ vc_status vc_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
  * (its outputs are then undefined), VC_OK otherwise. */
 vc_status vc_poll_status(void *ws, cudaStream_t stream);
 
+/*
+ * vc_wait_probe -- exercises the failure path of the bounded waits (no
+ * counterpart in the paper; it makes that path testable without faulting a
+ * GPU): one CTA waits on an mbarrier that nothing completes, the wait gives
+ * up after its iteration limit (about a second), records a timeout in the
+ * status block of `ws` (>= 256 bytes, 256-byte aligned) and the kernel
+ * returns.  vc_poll_status(ws) then reports VC_ERR_TIMEOUT and the context
+ * stays usable.
+ */
+vc_status vc_wait_probe(void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* (1) KIVI-style quantized draft cache                                      */
 /* ------------------------------------------------------------------------ */

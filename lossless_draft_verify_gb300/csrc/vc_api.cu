@@ -25,6 +25,19 @@ bool qcache_ok(const vc_qcache *c)
     return true;
 }
 
+// One CTA waits, with the library's bounded wait, on an mbarrier that nothing
+// completes: the wait gives up and records a timeout (where = 77).
+__global__ void wait_probe_kernel(int32_t *status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) report_timeout(status, 77);
+}
+
 }  // namespace
 
 extern "C" {
@@ -231,6 +244,13 @@ vc_status vc_accept(const void *logits, vc_dtype dt, const int32_t *drafts, int 
     if (B <= 0 || D < 0 || D > 1024 || V <= 0 || (D > 0 && !drafts)) return VC_ERR_INVALID;
     if (!aligned(ws, 256) || ws_bytes < accept_ws_bytes(B, D, V)) return VC_ERR_INVALID;
     return cuda_status(accept(logits, dt, drafts, B, D, V, n_acc, next_tok, ws, stream));
+}
+
+vc_status vc_wait_probe(void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!ws || ws_bytes < (size_t)kStatusBytes || !aligned(ws, 256)) return VC_ERR_INVALID;
+    wait_probe_kernel<<<1, 32, 0, stream>>>((int32_t *)ws);
+    return cuda_status(cudaGetLastError());
 }
 
 vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes, cudaStream_t side_stream,

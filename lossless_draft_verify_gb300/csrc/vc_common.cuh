@@ -83,18 +83,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^kSpinLog2 polls (each poll suspends for a
-// hardware-chosen interval, so the bound is of the order of a second) and
-// returns false; the caller records a timeout and skips the dependent work.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// One poll that may suspend the thread for at most `hint_ns` while the phase
+// is incomplete (returns as soon as it completes).
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: gives up after kWaitLimitNs of wall time (polls suspend for
+// at most 20 us each, so the bound holds whatever the hardware's default
+// suspend time is) and returns false; the caller records a timeout and skips
+// the dependent work.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (i > 64) __nanosleep(64);
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_for(bar, parity, 20000u)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
-    return false;
 }
 
 // ----- bulk (non-tensor) asynchronous copy global -> shared ---------------------

@@ -119,6 +119,8 @@ def load() -> ctypes.CDLL:
     L.vc_accept.argtypes = [P, c_int, P, c_int, c_int, c_int, P, P, P, c_size_t, P]
     L.vc_accept_noalloc.restype = c_int
     L.vc_accept_noalloc.argtypes = [P, c_int, P, c_int, c_int, c_int, P, P, P]
+    L.vc_wait_probe.restype = c_int
+    L.vc_wait_probe.argtypes = [P, c_size_t, P]
     L.vc_swap_in.restype = c_int
     L.vc_swap_in.argtypes = [P, P, c_size_t, P, P]
     L.vc_decoder_create.restype = c_int
@@ -159,7 +161,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_decoder_create", "vc_decoder_destroy", "vc_decoder_workspace_bytes", "vc_decoder_forward",
             "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm",
             "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits",
-            "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex"]
+            "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -266,6 +268,10 @@ def vc_check(stream=None):
 
 def vc_workspace_init(ws: Workspace, stream=None):
     _check(load().vc_workspace_init(ws.ptr, ws.nbytes, _stream(stream)), "vc_workspace_init")
+
+
+def vc_wait_probe(ws: Workspace, stream=None):
+    _check(load().vc_wait_probe(ws.ptr, ws.nbytes, _stream(stream)), "vc_wait_probe")
 
 
 def vc_poll_status(ws: Workspace, stream=None) -> int:
