@@ -151,9 +151,11 @@ class Round:
     so the host link never idles between steps.  Drafting, acceptance and the
     commit stay whole-batch launches."""
 
-    def __init__(self, dev, stagger: int = 2):
+    def __init__(self, dev, stagger: int = 2, horizon: int = HORIZON):
         from lossless_draft_verify_gb300 import inputs, vc
         self.vc, self.dev = vc, dev
+        HORIZON = self.D = horizon
+        DQ = self.DQ = horizon + 1
         g = torch.Generator(device=dev)
         self.scale = inputs.default_scale(D_HEAD)
         Ls = CTX + DQ
@@ -248,7 +250,7 @@ class Round:
             vc.vc_swap_in(self.vfull[b0:b1], self.vfull_host[b0:b1], stream=self.side, done_event=self.ev_swap[p])
         if ev is not None:
             ev["swap1"].record(self.side)
-        for j in range(HORIZON):
+        for j in range(self.D):
             vc.vc_qcache_append(self.cache, self.k_step[j], self.v_step[j], self.ones, requantize=False)
             if ev is not None:
                 ev["d0"][j].record(main)
@@ -288,10 +290,10 @@ class Round:
         return B * HKV * per_unit + 2 * B * HQ * D_HEAD * 2
 
     def verify_bytes(self) -> int:
-        return 2 * B * HKV * (CTX + DQ) * D_HEAD * 2 + 2 * B * DQ * HQ * D_HEAD * 2
+        return 2 * B * HKV * (CTX + self.DQ) * D_HEAD * 2 + 2 * B * self.DQ * HQ * D_HEAD * 2
 
     def verify_flops(self) -> int:
-        rows_keys = sum(CTX + i + 1 for i in range(DQ))
+        rows_keys = sum(CTX + i + 1 for i in range(self.DQ))
         return 4 * D_HEAD * B * HQ * rows_keys
 
 
@@ -712,6 +714,35 @@ def run_bytes(cfg, max_len) -> int:
     return 2 * cfg.n_layers * M_B * cfg.n_kv_heads * (max_len + M_HORIZON + 1) * cfg.head_dim * 2
 
 
+def run_sweep(args, dev):
+    """Draft-horizon sweep of the round workload (pages: draft horizon against
+    throughput; the divergence point of each sequence is uniform in [0, D]).
+    One JSON line per horizon: tokens per round, round time, drafting and swap
+    times.  Not the benchmark's contract line."""
+    for D in [int(x) for x in args.sweep_horizons.split(",")]:
+        rnd = Round(dev, stagger=args.stagger, horizon=D)
+        for _ in range(args.warmup):
+            rnd.step()
+        torch.cuda.synchronize()
+        evs = [make_events(D, rnd.stagger) for _ in range(args.steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(args.steps):
+            rnd.step(evs[i])
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / args.steps
+        tokens = rnd.tokens_per_round()
+        d_ms = statistics.mean(sum(e["d0"][j].elapsed_time(e["d1"][j]) for j in range(D)) for e in evs)
+        s_ms = statistics.mean(e["swap0"].elapsed_time(e["swap1"]) for e in evs)
+        print(json.dumps({"sweep": "horizon", "horizon": D, "tokens_per_round": tokens, "ms_per_round": ms,
+                          "tokens_per_s": tokens / (ms / 1e3), "draft_attn_ms_per_round": d_ms,
+                          "swap_ms": s_ms, "stagger": rnd.stagger}), flush=True)
+        del rnd
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -733,6 +764,8 @@ def main():
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4], help="draft cache bits (--workload model)")
+    ap.add_argument("--sweep", default=None, choices=["horizon"], help="print a sweep instead of the contract line")
+    ap.add_argument("--sweep-horizons", default="8,16,32,64,96,128")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
@@ -761,6 +794,9 @@ def main():
             pg.barrier()
         torch.cuda.synchronize()
 
+    if args.sweep:
+        run_sweep(args, dev)
+        return
     if args.workload == "model":
         run_model(args, dev, rank, world, barrier, pg)
         if pg is not None:
