@@ -62,9 +62,9 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("f07d50cedc0e3d0010968e55210875bd71ebcf6b65067b5d0702aeac5b41bb08",
-               "8b1109c68498705ecd31b5533b5ace8c5bb0cfe4584e74b26b26eb3baa0d456c"),
-    "bytes": 409.788160e6 + 4.499968e6,
+    "sha256": ("b95cb27ece693aaf2aa9f55244210f9eb60b08e37e375315b19f855d7ce7c520",
+               "607af49c7988512f8f8974c461106d2011be78ddbca72ebbb92fc5182dcc3286"),
+    "bytes": 411.009792e6 + 4.827904e6,
     "algorithmic_bytes": 409731072,
 }
 
@@ -481,6 +481,17 @@ def run_kernel(args, dev):
                 nbytes = 2 * ko.numel() * 2 + 2 * q.numel() * 2 + kept.numel() * (16 + 16 + 4 + 8)
                 rec = {"workload": "decode attention over the compacted cache [4,8,33024,128] bf16, 32/8 heads, "
                                    "with H2O score accumulation at the kept positions"}
+    elif name == "gemm":
+        # the decoder's gate|up projection in a draft step: M = 8 rows, K 4096, N 2 x 14336
+        M, K, N = 8, 4096, 2 * 14336
+        x = inputs.normal_bf16((M, K), 30, device=dev)
+        w = inputs.normal_bf16((K, N), 31, device=dev, std=0.02)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = vc.Workspace(vc.vc_gemm_workspace_bytes(torch.bfloat16, M, N, K), device=dev)
+        fn = lambda: vc.vc_gemm(x, w, y, ws=ws, decode_plan=True)
+        nbytes = K * N * 2 + M * K * 2 + M * N * 2
+        flops = 2 * M * N * K
+        rec = {"workload": "draft-step GEMM x[8,4096] W[4096,28672] bf16 (decode plan)"}
     elif name == "swap":
         # full-cache swap-in (host link): one copy, or the cache split in
         # chunks issued on as many side streams
