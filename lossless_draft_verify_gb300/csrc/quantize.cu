@@ -44,14 +44,15 @@ __device__ __forceinline__ void group_params(float mn, float mx, int qmax, uint1
 // code = clamp(rint(RN(RN(x - z) / s)), 0, qmax); rs = RN(1/s).  d * rs is
 // within a few ulp of RN(d / s) (q <= 15), so away from a half-integer both
 // round to the same integer; near one the exact quotient decides.
+__device__ __noinline__ float exact_quotient(float d, float s) { return __fdiv_rn(d, s); }
+
 __device__ __forceinline__ uint32_t group_code(float x, float sf, float zf, float rs, int qmax)
 {
     if (sf == 0.0f) return 0u;
     const float d = __fadd_rn(x, -zf);
-    float q = d * rs;
-    const float fr = q - floorf(q);
-    if (fabsf(fr - 0.5f) < 1e-5f) q = __fdiv_rn(d, sf);
+    const float q = d * rs;
     float r = rintf(q);
+    if (fabsf(q - r) > 0.49999f) r = rintf(exact_quotient(d, sf));   // rare: near a half-integer
     r = fminf(fmaxf(r, 0.0f), (float)qmax);
     return (uint32_t)r;
 }
@@ -121,16 +122,37 @@ __device__ void quantize_group(RowFn row, uint8_t *__restrict__ rec, uint32_t *i
         const int ks = c >> 4, col = c & 15;
         const int tig = (col & 7) >> 1, hh = col & 1, rh = col >> 3;
         const int kappa = 2 * ks + rh;
+        // token t = 16 (mu/2) + 8 (mu%2) + gid goes to lane 4 gid + tig, word
+        // w(mu), shift sh(mu): the four (word, shift) of this channel, once
+        int base[4], sh[4];
 #pragma unroll
-        for (int t = 0; t < G; ++t) {
-            const uint32_t code = group_code(x[t], sf, zf, rs, qmax);
-            const int mt = t >> 4, rowt = t & 15;
-            const int gid = rowt & 7, rb = rowt >> 3;
-            int w, s;
-            pair_pos<BITS, D>(kappa, 2 * mt + rb, w, s);
-            if (code)
-                atomicOr(reinterpret_cast<uint32_t *>(bimg + word_byte(gid * 4 + tig, w)),
-                         code << (BITS * s + 16 * hh));
+        for (int mu = 0; mu < 4; ++mu) {
+            int w, sl;
+            pair_pos<BITS, D>(kappa, mu, w, sl);
+            base[mu] = word_byte(tig, w);
+            sh[mu] = BITS * sl + 16 * hh;
+        }
+        const bool pair01 = base[0] == base[1], pair23 = base[2] == base[3];
+#pragma unroll
+        for (int gid = 0; gid < 8; ++gid) {
+            uint32_t cd[4];
+#pragma unroll
+            for (int mu = 0; mu < 4; ++mu)
+                cd[mu] = group_code(x[16 * (mu >> 1) + 8 * (mu & 1) + gid], sf, zf, rs, qmax) << sh[mu];
+            uint32_t *w0 = reinterpret_cast<uint32_t *>(bimg + base[0] + 64 * gid);
+            uint32_t *w2 = reinterpret_cast<uint32_t *>(bimg + base[2] + 64 * gid);
+            if (pair01) {
+                if (cd[0] | cd[1]) atomicOr(w0, cd[0] | cd[1]);
+            } else {
+                if (cd[0]) atomicOr(w0, cd[0]);
+                if (cd[1]) atomicOr(reinterpret_cast<uint32_t *>(bimg + base[1] + 64 * gid), cd[1]);
+            }
+            if (pair23) {
+                if (cd[2] | cd[3]) atomicOr(w2, cd[2] | cd[3]);
+            } else {
+                if (cd[2]) atomicOr(w2, cd[2]);
+                if (cd[3]) atomicOr(reinterpret_cast<uint32_t *>(bimg + base[3] + 64 * gid), cd[3]);
+            }
         }
         // meta: pair n = 2 ks + rr of quad j, half (c & 1)
         const int j = tig, n = 2 * ks + rh;
@@ -175,17 +197,21 @@ __device__ void quantize_group(RowFn row, uint8_t *__restrict__ rec, uint32_t *i
         const int tig = (colt & 7) >> 1, hh = colt & 1, rh = colt >> 3;
         const int mu = 2 * ks + rh;
         uint8_t *vsec = bimg + Gm::CODE;
+        // channel c = 32 gc + 8 m + gid (m = e / 8) has class kappa = 4 gc + m
+        // and goes to lane 4 gid + tig: the four (word, shift), once
+        int base[4], sh[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            int w, sl;
+            pair_pos<BITS, D>(4 * gc + m, mu, w, sl);
+            base[m] = word_byte(tig, w);
+            sh[m] = BITS * sl + 16 * hh;
+        }
 #pragma unroll
         for (int e = 0; e < G; ++e) {
+            const int m = e >> 3, gid = e & 7;
             const uint32_t code = group_code(x[e], sf, zf, rs, qmax);
-            const int c = gc * G + e;
-            const int mt = c >> 4, rowc = c & 15;
-            const int gid = rowc & 7, rb = rowc >> 3;
-            int w, s;
-            pair_pos<BITS, D>(2 * mt + rb, mu, w, s);
-            if (code)
-                atomicOr(reinterpret_cast<uint32_t *>(vsec + word_byte(gid * 4 + tig, w)),
-                         code << (BITS * s + 16 * hh));
+            if (code) atomicOr(reinterpret_cast<uint32_t *>(vsec + base[m] + 64 * gid), code << sh[m]);
         }
         const int j = tig, n = (2 * ks + rh) * NG + gc;
         const int off = Gm::VM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (t & 1);
@@ -199,7 +225,7 @@ __device__ void quantize_group(RowFn row, uint8_t *__restrict__ rec, uint32_t *i
 }
 
 template <typename T, int BITS, int D>
-__global__ void __launch_bounds__(2 * D)
+__global__ void __launch_bounds__(2 * D, 5)
 quantize_prefill_kernel(const T *__restrict__ k, const T *__restrict__ v, int Hkv, int L_stride,
                         int max_groups, uint8_t *__restrict__ records)
 {
