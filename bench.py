@@ -151,7 +151,7 @@ class Round:
     so the host link never idles between steps.  Drafting, acceptance and the
     commit stay whole-batch launches."""
 
-    def __init__(self, dev, stagger: int = 2, horizon: int = HORIZON):
+    def __init__(self, dev, stagger: int = 2, horizon: int = HORIZON, link_gbps: float | None = None):
         from lossless_draft_verify_gb300 import inputs, vc
         self.vc, self.dev = vc, dev
         HORIZON = self.D = horizon
@@ -195,6 +195,8 @@ class Round:
         self.ws_d = vc.Workspace(vc.vc_draft_attn_workspace_bytes(self.view, HQ), device=dev)
         assert B % stagger == 0
         self.stagger = stagger
+        self.link_gbps = link_gbps
+        self.pace_ws = torch.zeros(4, dtype=torch.int32, device=dev)
         bp = B // stagger
         self.parts = [(i * bp, (i + 1) * bp) for i in range(stagger)]
         self.ws_v = vc.Workspace(vc.vc_verify_attn_workspace_bytes(torch.bfloat16, bp, DQ, HQ, HKV, D_HEAD, CTX),
@@ -246,8 +248,14 @@ class Round:
             self.side.wait_event(self.ev_ver[p])
             if ev is not None and p == 0:
                 ev["swap0"].record(self.side)
-            vc.vc_swap_in(self.kfull[b0:b1], self.kfull_host[b0:b1], stream=self.side)
-            vc.vc_swap_in(self.vfull[b0:b1], self.vfull_host[b0:b1], stream=self.side, done_event=self.ev_swap[p])
+            if self.link_gbps:
+                vc.vc_swap_in_paced(self.kfull[b0:b1], self.kfull_host[b0:b1], self.link_gbps, self.pace_ws,
+                                    stream=self.side)
+                vc.vc_swap_in_paced(self.vfull[b0:b1], self.vfull_host[b0:b1], self.link_gbps, self.pace_ws,
+                                    stream=self.side, done_event=self.ev_swap[p])
+            else:
+                vc.vc_swap_in(self.kfull[b0:b1], self.kfull_host[b0:b1], stream=self.side)
+                vc.vc_swap_in(self.vfull[b0:b1], self.vfull_host[b0:b1], stream=self.side, done_event=self.ev_swap[p])
         if ev is not None:
             ev["swap1"].record(self.side)
         for j in range(self.D):
@@ -725,11 +733,72 @@ def run_bytes(cfg, max_len) -> int:
     return 2 * cfg.n_layers * M_B * cfg.n_kv_heads * (max_len + M_HORIZON + 1) * cfg.head_dim * 2
 
 
+def full_kv_step_ms(rnd, steps: int, warmup: int) -> float:
+    """Plain decoding with the full cache held on the host: every decoded token
+    needs the whole cache swapped in, then a one-query verify pass and the
+    argmax (the full-KV baseline of the pages' comparison).  Returns ms per
+    token step for all B sequences."""
+    vc, main = rnd.vc, torch.cuda.current_stream()
+    q1 = rnd.q_ver[:, :1].contiguous()
+    o1 = torch.empty_like(q1)
+    lg1 = rnd.logits[:, :1].contiguous()
+    ws = vc.Workspace(vc.vc_verify_attn_workspace_bytes(torch.bfloat16, B, 1, HQ, HKV, D_HEAD, CTX), device=rnd.dev)
+    ev = torch.cuda.Event()
+
+    def one():
+        rnd.side.wait_stream(main)
+        for t, h in ((rnd.kfull, rnd.kfull_host), (rnd.vfull, rnd.vfull_host)):
+            if rnd.link_gbps:
+                vc.vc_swap_in_paced(t, h, rnd.link_gbps, rnd.pace_ws, stream=rnd.side, done_event=ev)
+            else:
+                vc.vc_swap_in(t, h, stream=rnd.side, done_event=ev)
+        main.wait_event(ev)
+        vc.vc_verify_attn(q1, rnd.kfull, rnd.vfull, rnd.ctx, CTX, rnd.scale, o1, ws)
+        vc.vc_accept(lg1, None, rnd.n_acc, rnd.next_tok, rnd.ws_a)
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 def run_sweep(args, dev):
     """Draft-horizon sweep of the round workload (pages: draft horizon against
     throughput; the divergence point of each sequence is uniform in [0, D]).
     One JSON line per horizon: tokens per round, round time, drafting and swap
     times.  Not the benchmark's contract line."""
+    if args.sweep == "link":
+        # the full cache behind slower stores (remote prefix caching): draft and
+        # verify against the full-KV baseline at each source rate
+        for r in args.sweep_links.split(","):
+            gbps = None if r == "native" else float(r)
+            rnd = Round(dev, stagger=args.stagger, link_gbps=gbps)
+            for _ in range(args.warmup):
+                rnd.step()
+            torch.cuda.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(args.steps):
+                rnd.step()
+            t1.record()
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1) / args.steps
+            tokens = rnd.tokens_per_round()
+            base_ms = full_kv_step_ms(rnd, max(2, args.steps // 2), 2)
+            vt, bt = tokens / (ms / 1e3), B / (base_ms / 1e3)
+            print(json.dumps({"sweep": "link", "source_gbps": r, "ms_per_round": ms, "tokens_per_round": tokens,
+                              "tokens_per_s": vt, "full_kv_ms_per_token_step": base_ms, "full_kv_tokens_per_s": bt,
+                              "speedup": vt / bt}), flush=True)
+            del rnd
+            torch.cuda.empty_cache()
+        return
     for D in [int(x) for x in args.sweep_horizons.split(",")]:
         rnd = Round(dev, stagger=args.stagger, horizon=D)
         for _ in range(args.warmup):
@@ -775,7 +844,9 @@ def main():
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4], help="draft cache bits (--workload model)")
-    ap.add_argument("--sweep", default=None, choices=["horizon"], help="print a sweep instead of the contract line")
+    ap.add_argument("--sweep", default=None, choices=["horizon", "link"],
+                    help="print a sweep instead of the contract line")
+    ap.add_argument("--sweep-links", default="native,100,50,25,12.5", help="source rates in GB/s for --sweep link")
     ap.add_argument("--sweep-horizons", default="8,16,32,64,96,128")
     args = ap.parse_args()
     rank, world, local = dist_env()

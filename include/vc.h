@@ -369,6 +369,19 @@ vc_status vc_accept_noalloc(const void *logits, vc_dtype dt, const int32_t *draf
 vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes,
                      cudaStream_t side_stream, cudaEvent_t done);
 
+/*
+ * vc_swap_in_paced -- vc_swap_in as if the source produced data at `gbps`
+ * (GB/s): the emulation of a full cache held by a slower store, e.g. a remote
+ * prefix cache behind a network (paper page, "Key results": remote prefix
+ * caching).  The copy is cut into chunks of chunk_bytes; chunk i starts no
+ * earlier than i * chunk_bytes / gbps after the first, by a one-thread kernel
+ * on side_stream that sleeps until that time (never more than 30 s).  The rate
+ * is an upper bound: a link slower than gbps gives its own rate.  pace_ws:
+ * 16 device bytes, 16-byte aligned, used by this call until `done`.
+ */
+vc_status vc_swap_in_paced(void *dst_dev, const void *src_pinned_host, size_t bytes, double gbps,
+                           size_t chunk_bytes, void *pace_ws, cudaStream_t side_stream, cudaEvent_t done);
+
 /* ------------------------------------------------------------------------ */
 /* (7) target decoder around the hot path                                    */
 /* ------------------------------------------------------------------------ */

@@ -38,6 +38,21 @@ __global__ void wait_probe_kernel(int32_t *status)
     if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) report_timeout(status, 77);
 }
 
+// Pacing of an emulated slower link: chunk i of a paced copy may start only
+// at t0 + i * ns_per_chunk, t0 being the time the first pace kernel ran.  One
+// thread sleeps until its deadline (at most max_ns past t0, so every wait
+// ends).
+__global__ void pace_kernel(uint64_t *t0, int first, uint64_t offset_ns, uint64_t max_ns)
+{
+    if (first) {
+        *t0 = globaltimer_ns();
+        return;
+    }
+    const uint64_t start = *t0;
+    const uint64_t deadline = start + (offset_ns < max_ns ? offset_ns : max_ns);
+    while (globaltimer_ns() < deadline) __nanosleep(2000);
+}
+
 }  // namespace
 
 extern "C" {
@@ -251,6 +266,32 @@ vc_status vc_wait_probe(void *ws, size_t ws_bytes, cudaStream_t stream)
     if (!ws || ws_bytes < (size_t)kStatusBytes || !aligned(ws, 256)) return VC_ERR_INVALID;
     wait_probe_kernel<<<1, 32, 0, stream>>>((int32_t *)ws);
     return cuda_status(cudaGetLastError());
+}
+
+vc_status vc_swap_in_paced(void *dst_dev, const void *src_pinned_host, size_t bytes, double gbps,
+                           size_t chunk_bytes, void *pace_ws, cudaStream_t side_stream, cudaEvent_t done)
+{
+    if (!dst_dev || !src_pinned_host || !pace_ws || !aligned(pace_ws, 16)) return VC_ERR_INVALID;
+    if (!(gbps > 0.0) || chunk_bytes == 0) return VC_ERR_INVALID;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, src_pinned_host) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+        cudaGetLastError();
+        return VC_ERR_INVALID;
+    }
+    const double ns_per_byte = 1.0 / gbps;            // GB/s = bytes per ns
+    const uint64_t max_ns = 30000000000ull;           // no chunk waits past 30 s
+    uint64_t *t0 = (uint64_t *)pace_ws;
+    pace_kernel<<<1, 1, 0, side_stream>>>(t0, 1, 0, max_ns);
+    for (size_t off = 0; off < bytes; off += chunk_bytes) {
+        const size_t n = bytes - off < chunk_bytes ? bytes - off : chunk_bytes;
+        if (off > 0) pace_kernel<<<1, 1, 0, side_stream>>>(t0, 0, (uint64_t)(off * ns_per_byte), max_ns);
+        if (cudaMemcpyAsync((uint8_t *)dst_dev + off, (const uint8_t *)src_pinned_host + off, n,
+                            cudaMemcpyHostToDevice, side_stream) != cudaSuccess)
+            return VC_ERR_CUDA;
+    }
+    if (cudaGetLastError() != cudaSuccess) return VC_ERR_CUDA;
+    if (done && cudaEventRecord(done, side_stream) != cudaSuccess) return VC_ERR_CUDA;
+    return VC_OK;
 }
 
 vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes, cudaStream_t side_stream,

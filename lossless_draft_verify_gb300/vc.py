@@ -121,6 +121,8 @@ def load() -> ctypes.CDLL:
     L.vc_accept_noalloc.argtypes = [P, c_int, P, c_int, c_int, c_int, P, P, P]
     L.vc_wait_probe.restype = c_int
     L.vc_wait_probe.argtypes = [P, c_size_t, P]
+    L.vc_swap_in_paced.restype = c_int
+    L.vc_swap_in_paced.argtypes = [P, P, c_size_t, ctypes.c_double, c_size_t, P, P, P]
     L.vc_swap_in.restype = c_int
     L.vc_swap_in.argtypes = [P, P, c_size_t, P, P]
     L.vc_decoder_create.restype = c_int
@@ -161,7 +163,8 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_decoder_create", "vc_decoder_destroy", "vc_decoder_workspace_bytes", "vc_decoder_forward",
             "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm",
             "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits",
-            "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe"]
+            "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe",
+            "vc_swap_in_paced"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -528,3 +531,17 @@ class DecoderTrace:
         torch.cuda.synchronize()
         return [(TRACE_KINDS[self._kinds[k]], self.events[2 * k].elapsed_time(self.events[2 * k + 1]))
                 for k in range(n)]
+
+
+def vc_swap_in_paced(dst: torch.Tensor, src_pinned: torch.Tensor, gbps: float, pace_ws: torch.Tensor,
+                     chunk_bytes: int = 64 << 20, stream=None, done_event: torch.cuda.Event | None = None):
+    """vc_swap_in at an emulated source rate of `gbps` GB/s (see include/vc.h);
+    pace_ws: a 16-byte device tensor owned by the caller."""
+    n = dst.numel() * dst.element_size()
+    ev = None
+    if done_event is not None:
+        if not done_event.cuda_event:
+            done_event.record(torch.cuda.current_stream() if stream is None else stream)
+        ev = done_event.cuda_event
+    _check(load().vc_swap_in_paced(dst.data_ptr(), src_pinned.data_ptr(), n, float(gbps), int(chunk_bytes),
+                                   pace_ws.data_ptr(), _stream(stream), ev), "vc_swap_in_paced")
