@@ -508,7 +508,9 @@ vc_status vc_kv_writeback(const void *k_blk, const void *v_blk, vc_dtype dt, int
  * vc_gemm -- out = x W (+ resid) with the decoder's GEMM: x [M][K], W [K][N],
  * resid and out [M][N] (resid may equal out), dt for all; fp32 accumulation.
  * The summation order of every output element depends on (N, K), the plan and
- * the device only.  ws: vc_gemm_workspace_bytes(dt, M, N, K) bytes (may be 0).
+ * the device only.  ws: vc_gemm_workspace_bytes(dt, M, N, K) bytes (may be 0),
+ * zero-filled once before first use (it holds per-tile counters that every
+ * call leaves at zero).
  */
 size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K);
 /* Number of K splits of the decoder's GEMM for (N, K): decode_plan != 0 gives

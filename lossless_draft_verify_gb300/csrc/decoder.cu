@@ -91,7 +91,7 @@ rmsnorm_kernel(const T *__restrict__ x, int D, int in_step, int in_off, float ep
 // q and k parts of one qkv row, q to q_out, k and v scattered to up to two
 // destinations [.][Hkv][stride][hd]: dst1 at row (pos1 ? pos : 0) + i (the
 // cache), dst2 at row i (the block copy).  Angles in fp64 (positions reach
-// 10^5 radians), cos/sin rounded once to fp32.
+// 10^5 radians), reduced modulo 2 pi in fp64, cos/sin in fp32.
 struct RopeDst {
     void *k1, *v1;
     size_t bstride1;   // elements between sequences
@@ -118,11 +118,16 @@ rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd
         return;
     }
     for (int j = threadIdx.x; j < half; j += kRowThreads) {
-        const double ang = (double)pos * pow((double)theta, -2.0 * (double)j / (double)hd);
-        double s, c;
-        sincos(ang, &s, &c);
-        cs[j] = (float)c;
-        sn[j] = (float)s;
+        // angle in fp64 (positions reach 10^5 radians), reduced to [-pi, pi]
+        // in fp64, then fp32 cos/sin of the small remainder
+        constexpr double kTwoPi = 6.283185307179586476925286766559;
+        const double inv_freq = exp2(-(2.0 * (double)j / (double)hd) * log2((double)theta));
+        const double ang = (double)pos * inv_freq;
+        const double red = fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);
+        float s, c;
+        sincosf((float)red, &s, &c);
+        cs[j] = c;
+        sn[j] = s;
     }
     __syncthreads();
     const T *row = qkv + (size_t)m * (Hq + 2 * Hkv) * hd;
@@ -219,7 +224,7 @@ Layout layout_of(const vc_decoder *d, int B, int max_rows, int max_ctx, size_t d
     const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
     const int nqkv = qd + 2 * kvd;
     Layout L;
-    size_t o = kStatusBytes;
+    size_t o = kStatusBytes + kGemmCounterBytes;   // GEMM tile counters: same place in every call
     auto take = [&](size_t bytes) {
         const size_t at = o;
         o += a256(bytes);
@@ -270,6 +275,7 @@ struct Ctx {
     cudaStream_t st;
     int plan;          // GEMM split plan: row-invariant (forward) or decode (draft)
     int32_t *status() const { return (int32_t *)ws; }
+    unsigned int *counters() const { return (unsigned int *)(ws + kStatusBytes); }
     template <typename P = void> P *at(size_t off) const { return reinterpret_cast<P *>(ws + off); }
 };
 
@@ -312,21 +318,21 @@ cudaError_t layer_tail(const Ctx &C, int l, int M)
     const int qd = c.n_heads * c.head_dim;
     void *x = C.at(C.L.x), *h = C.at(C.L.h), *part = C.at(C.L.part);
     VC_TRY(traced(C, VC_TRACE_GEMM_O, [&] {
-        return gemm(C.at(C.L.att), C.d->wo[l], x, x, c.dt, M, c.d_model, qd, qd, part, C.status(), C.st,
-                    C.plan);
+        return gemm(C.at(C.L.att), C.d->wo[l], x, x, c.dt, M, c.d_model, qd, qd, part, C.counters(), C.status(),
+                    C.st, C.plan);
     }));
     VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
     VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
         return gemm(h, C.d->wgu[l], nullptr, C.at(C.L.gu), c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, part,
-                    C.status(), C.st, C.plan);
+                    C.counters(), C.status(), C.st, C.plan);
     }));
     const size_t n = (size_t)M * c.d_ff;
     silu_mul_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, C.st>>>(C.at<const T>(C.L.gu), M, c.d_ff,
                                                                      C.at<T>(C.L.act));
     VC_TRY(cudaGetLastError());
     return traced(C, VC_TRACE_GEMM_DOWN, [&] {
-        return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.status(), C.st,
-                    C.plan);
+        return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.counters(),
+                    C.status(), C.st, C.plan);
     });
 }
 
@@ -351,7 +357,7 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         VC_TRY(traced(C, VC_TRACE_GEMM_QKV, [&] {
             return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
-                        C.status(), C.st, C.plan);
+                        C.counters(), C.status(), C.st, C.plan);
         }));
         RopeDst dst;
         dst.k1 = (T *)kc + l * layer_cache;
@@ -376,13 +382,13 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
         VC_TRY(rmsnorm<T>(C, x, B, Dq, Dq - 1, C.at(C.L.hl)));
         VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
             return gemm(C.at(C.L.hl), C.d->head, nullptr, logits, c.dt, B, c.vocab, c.d_model, c.d_model, part,
-                        C.status(), C.st, C.plan);
+                        C.counters(), C.status(), C.st, C.plan);
         }));
     } else {
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
-            return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(),
-                        C.st, C.plan);
+            return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.counters(),
+                        C.status(), C.st, C.plan);
         }));
     }
     fold_status_kernel<<<1, 1, 0, C.st>>>(C.status(), C.at<int32_t>(C.L.vws), nullptr, nullptr);
@@ -410,7 +416,7 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         VC_TRY(traced(C, VC_TRACE_GEMM_QKV, [&] {
             return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
-                        C.status(), C.st, C.plan);
+                        C.counters(), C.status(), C.st, C.plan);
         }));
         RopeDst dst;
         dst.k1 = kn;
@@ -436,8 +442,8 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
     }
     VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
     VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
-        return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.status(), C.st,
-                    C.plan);
+        return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.counters(),
+                    C.status(), C.st, C.plan);
     }));
     VC_TRY(accept(logits, c.dt, nullptr, B, 0, c.vocab, C.at<int32_t>(C.L.nacc), next_tok, C.at(C.L.aws), C.st));
     if (drafts_out) {
@@ -608,7 +614,8 @@ int vc_gemm_splits(vc_dtype dt, int N, int K, int decode_plan)
 size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K)
 {
     if ((dt != VC_BF16 && dt != VC_F32) || M <= 0 || N <= 0 || K <= 0) return 0;
-    return std::max(gemm_ws_bytes(dt, M, N, K, kGemmRowInvariant), gemm_ws_bytes(dt, M, N, K, kGemmDecode));
+    const size_t p = std::max(gemm_ws_bytes(dt, M, N, K, kGemmRowInvariant), gemm_ws_bytes(dt, M, N, K, kGemmDecode));
+    return p ? p + kGemmCounterBytes : 0;
 }
 
 vc_status vc_gemm_ex(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
@@ -618,8 +625,9 @@ vc_status vc_gemm_ex(const void *x, const void *w, const void *resid, void *out,
     if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (resid && !aligned16(resid))) return VC_ERR_INVALID;
     const int plan = decode_plan ? kGemmDecode : kGemmRowInvariant;
     const size_t need = gemm_ws_bytes(dt, M, N, K, plan);
-    if (need && (!ws || ws_bytes < need || !aligned16(ws))) return VC_ERR_INVALID;
-    return to_status(gemm(x, w, resid, out, dt, M, N, K, K, ws, nullptr, stream, plan));
+    if (need && (!ws || ws_bytes < need + kGemmCounterBytes || !aligned16(ws))) return VC_ERR_INVALID;
+    return to_status(gemm(x, w, resid, out, dt, M, N, K, K, need ? (uint8_t *)ws + kGemmCounterBytes : nullptr,
+                          need ? (unsigned int *)ws : nullptr, nullptr, stream, plan));
 }
 
 vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,

@@ -16,7 +16,8 @@
 // swizzle) into a 3-stage ring (2 CTAs per SM; draft steps with M <= 16 load
 // only 16 x rows per stage and keep 6 stages), warp 1 issues tcgen05.mma (M128 N128 K16)
 // into a TMEM accumulator, warps 2-5 read TMEM and write either the output
-// (one split) or fp32 partials that a second kernel sums in split order.
+// (one split) or fp32 partials; the last CTA of each output tile to finish
+// (a self-resetting counter per tile in the workspace) sums them in split order.
 // fp32 (any shape): CUDA cores, one output element per thread, K in order.
 #include <cuda.h>
 
@@ -50,10 +51,12 @@ struct GemmBars {
     uint64_t full[G_MAX_STAGES], empty[G_MAX_STAGES], acc_full;
     uint32_t tmem_base;
     int32_t abort_flag;
+    int32_t is_last;
 };
 
 struct GemmArgs {
     float *part;                 // [S][M][N] fp32, used when S > 1
+    unsigned int *counters;      // [m tiles][n tiles], zero between launches (S > 1)
     __nv_bfloat16 *out;          // [M][N]
     const __nv_bfloat16 *resid;  // [M][N] or null (may equal out)
     int32_t *status;
@@ -168,6 +171,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                             *reinterpret_cast<float4 *>(dst + c) =
                                 make_float4(__uint_as_float(u[c]), __uint_as_float(u[c + 1]),
                                             __uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
+                        __threadfence();
                     } else {
                         const size_t off = (size_t)m * A.N + c0;
                         uint32_t packed[16];
@@ -209,6 +213,46 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     if (warp == 0) {
         __syncwarp();
         tc::tmem_dealloc(tmem, G_TMEM_COLS);
+    }
+    if (A.S > 1 && A.counters) {
+        // the last split CTA of this output tile sums the partials in split
+        // order (the same order for every M) and writes the result
+        const unsigned int tile = blockIdx.x * gridDim.y + blockIdx.y;
+        if (threadIdx.x == 0) {
+            __threadfence();
+            B->is_last = atomicAdd(&A.counters[tile], 1u) == (unsigned int)(A.S - 1);
+        }
+        __syncthreads();
+        if (B->is_last) {
+            __threadfence();
+            const int rows = min(GM, A.M - m0);
+            const size_t plane = (size_t)A.M * A.N;
+            for (int idx = threadIdx.x; idx < rows * (GN / 4); idx += G_THREADS) {
+                const int m = m0 + idx / (GN / 4);
+                const size_t off = (size_t)m * A.N + n0 + 4 * (idx % (GN / 4));
+                float4 acc = __ldcg(reinterpret_cast<const float4 *>(A.part + off));
+                for (int sp = 1; sp < A.S; ++sp) {
+                    const float4 p = __ldcg(reinterpret_cast<const float4 *>(A.part + sp * plane + off));
+                    acc.x += p.x;
+                    acc.y += p.y;
+                    acc.z += p.z;
+                    acc.w += p.w;
+                }
+                if (A.resid) {
+                    const uint2 r = *reinterpret_cast<const uint2 *>(A.resid + off);
+                    acc.x += bf16_lo(r.x);
+                    acc.y += bf16_hi(r.x);
+                    acc.z += bf16_lo(r.y);
+                    acc.w += bf16_hi(r.y);
+                }
+                __nv_bfloat162 a2 = __floats2bfloat162_rn(acc.x, acc.y), b2 = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 o;
+                o.x = *reinterpret_cast<uint32_t *>(&a2);
+                o.y = *reinterpret_cast<uint32_t *>(&b2);
+                *reinterpret_cast<uint2 *>(A.out + off) = o;
+            }
+            if (threadIdx.x == 0) A.counters[tile] = 0u;
+        }
     }
 }
 
@@ -313,7 +357,7 @@ size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K, int plan)
 }
 
 cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
-                 int ldx, void *ws, int32_t *status, cudaStream_t st, int plan)
+                 int ldx, void *ws, unsigned int *counters, int32_t *status, cudaStream_t st, int plan)
 {
     if (M <= 0) return cudaSuccess;
     if (gemm_uses_tensor_cores(dt, N, K)) {
@@ -327,6 +371,8 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         const int nkb = K / GK;
         A.kb_per_split = (nkb + A.S - 1) / A.S;
         A.part = (float *)ws;
+        const int tiles = ((M + GM - 1) / GM) * (N / GN);
+        A.counters = (A.S > 1 && counters && tiles <= kGemmMaxTiles) ? counters : nullptr;
         A.out = (__nv_bfloat16 *)out;
         A.resid = (const __nv_bfloat16 *)resid;
         A.status = status;
@@ -343,7 +389,7 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
             cudaFuncSetAttribute(gemm_tc_kernel<128, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gg::SMEM);
             gemm_tc_kernel<128, 3><<<grid, G_THREADS, Gg::SMEM, st>>>(mx, mw, A);
         }
-        if (A.S > 1) {
+        if (A.S > 1 && !A.counters) {
             const size_t q = (size_t)M * N / 4;
             gemm_splitk_reduce<<<(unsigned)((q + 255) / 256), 256, 0, st>>>(A.part, A.S, M, N, A.resid, A.out);
         }

@@ -52,14 +52,19 @@ cudaError_t drop_tokens(const float *scores, const void *k, const void *v, vc_dt
 
 // gemm.cu: y = x W (+ resid), x [M][ldx] (first K columns), W [K][N].  The
 // summation order of an output element depends on (N, K, plan) and the
-// device, never on M.  ws: gemm_ws_bytes bytes of fp32 partials (bf16 path).
+// device, never on M.  ws: gemm_ws_bytes bytes of fp32 partials (bf16 path);
+// counters: kGemmMaxTiles words that are zero on entry and left zero (the last
+// CTA of each output tile sums the partials), or null (a separate reduction).
 constexpr int kGemmRowInvariant = 0;   // forward passes (verify, plain decoding, prefill)
 constexpr int kGemmDecode = 1;         // draft steps (M <= 128)
+constexpr int kGemmMaxTiles = 16384;
+constexpr size_t kGemmCounterBytes = (size_t)kGemmMaxTiles * 4;
 bool gemm_uses_tensor_cores(vc_dtype dt, int N, int K);
 int gemm_splits(int N, int K, int plan);
 size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K, int plan = kGemmRowInvariant);
 cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
-                 int ldx, void *ws, int32_t *status, cudaStream_t st, int plan = kGemmRowInvariant);
+                 int ldx, void *ws, unsigned int *counters, int32_t *status, cudaStream_t st,
+                 int plan = kGemmRowInvariant);
 
 // host_util.cu
 int device_sm_count();

@@ -127,3 +127,25 @@ def test_swap_in_pinned_and_rejects_pageable():
     with pytest.raises(vc.VcError) as e:
         vc.vc_swap_in(dst, pageable, nbytes=64, stream=side)
     assert e.value.status == vc.VC_ERR_INVALID
+
+
+def test_paced_swap_in_keeps_its_rate_and_data():
+    """vc_swap_in_paced: the bytes arrive intact and no faster than the
+    emulated source rate (256 MiB at 25 GB/s: at least ~10.7 ms)."""
+    vc = lib()
+    n = 64 << 20
+    src = torch.arange(n, dtype=torch.int32).pin_memory()
+    dst = torch.zeros(n, dtype=torch.int32, device="cuda")
+    pace = torch.zeros(4, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(side)
+    vc.vc_swap_in_paced(dst, src, 25.0, pace, chunk_bytes=16 << 20, stream=side)
+    t1.record(side)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    assert torch.equal(dst.cpu(), src)
+    expect_ms = (4 * n) / 25e9 * 1e3
+    assert ms >= 0.9 * expect_ms * 3 / 4, ms          # the last chunk is not paced
+    assert ms < 20 * expect_ms, ms
