@@ -72,6 +72,51 @@ def test_draft_kivi_spare_capacity_and_ragged_lengths():
         assert_attn_close(out[b:b + 1], want, what=f"seq {b}")
 
 
+def test_draft_kivi_one_sequence_many_slices():
+    """One 32768-token sequence with 8 kv heads: each unit is cut into about
+    76 slices of the single wave, so the final merge spans more than one
+    block of split weights."""
+    vc = lib()
+    k, v, q, out, scale = _run_kivi(vc, 1, 32, 8, 32768, 128, 2, 128, seed=11)
+    qc = oracle.kivi_quantize(f32(k), f32(v), 2, 32, 128)
+    want = oracle.kivi_decode_attn(f32(q), qc, scale)
+    assert_attn_close(out, want, what="B1 32k")
+
+
+def test_draft_kivi_mixed_lengths_slices_cross_units():
+    """Sequences of very different lengths (quantized groups 1, 91, 29, 2):
+    slices of the wave start and end inside short units and inside rings."""
+    vc = lib()
+    B, Hq, Hkv, d, bits, R, G = 4, 8, 2, 128, 2, 64, 32
+    L0, target = 100, [100, 3000, 1000, 131]
+    k, v = inputs.kv_with_outliers(B, Hkv, max(target), d, seed=21, device="cuda")
+    q = inputs.normal_bf16((B, Hq, d), 121, device="cuda")
+    cache = vc.QCache(B, Hkv, d, bits, 100, R + G + 64, R)
+    vc.vc_quantize_kv(k[:, :, :L0].contiguous(), v[:, :, :L0].contiguous(), cache)
+    have = [L0] * B
+    while any(h < t for h, t in zip(have, target)):
+        n = [min(64, t - h) for h, t in zip(have, target)]
+        kn = torch.zeros(B, Hkv, 64, d, dtype=k.dtype, device="cuda")
+        vn = torch.zeros_like(kn)
+        for b in range(B):
+            kn[b, :, :n[b]] = k[b, :, have[b]:have[b] + n[b]]
+            vn[b, :, :n[b]] = v[b, :, have[b]:have[b] + n[b]]
+        vc.vc_qcache_append(cache, kn, vn, torch.tensor(n, dtype=torch.int32, device="cuda"), requantize=True)
+        have = [h + m for h, m in zip(have, n)]
+    view = cache.view()
+    ws = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, Hq))
+    out = torch.empty_like(q)
+    vc.vc_draft_attn(q, view, 0.09, out, ws)
+    torch.cuda.synchronize()
+    assert vc.vc_poll_status(ws) == 0
+    assert cache.n_groups.cpu().tolist() == [(t - R) // G for t in target]
+    for b in range(B):
+        L = target[b]
+        qc = oracle.kivi_quantize(f32(k[b:b + 1, :, :L]), f32(v[b:b + 1, :, :L]), bits, G, R)
+        want = oracle.kivi_decode_attn(f32(q[b:b + 1]), qc, 0.09)
+        assert_attn_close(out[b:b + 1], want, what=f"seq {b} (L={L})")
+
+
 @pytest.mark.parametrize("dtype,d,Hq", [(torch.bfloat16, 128, 8), (torch.bfloat16, 64, 4), (torch.bfloat16, 128, 2),
                                         (torch.float32, 64, 8)])
 def test_draft_dense_matches_oracle(dtype, d, Hq):
