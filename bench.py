@@ -151,9 +151,11 @@ class Round:
     so the host link never idles between steps.  Drafting, acceptance and the
     commit stay whole-batch launches."""
 
-    def __init__(self, dev, stagger: int = 2, horizon: int = HORIZON, link_gbps: float | None = None):
+    def __init__(self, dev, stagger: int = 2, horizon: int = HORIZON, link_gbps: float | None = None,
+                 bits: int = BITS, residual: int = RESIDUAL):
         from lossless_draft_verify_gb300 import inputs, vc
         self.vc, self.dev = vc, dev
+        self.bits, self.residual = bits, residual
         HORIZON = self.D = horizon
         DQ = self.DQ = horizon + 1
         g = torch.Generator(device=dev)
@@ -168,7 +170,7 @@ class Round:
         self.vfull_host.copy_(self.vfull)
         # compressed draft cache of the context
         maxg = (CTX + DQ) // GROUP + 1
-        self.cache = vc.QCache(B, HKV, D_HEAD, BITS, maxg, RESIDUAL + GROUP + DQ + 32, RESIDUAL)
+        self.cache = vc.QCache(B, HKV, D_HEAD, bits, maxg, residual + GROUP + DQ + 32, residual)
         vc.vc_quantize_kv(self.kfull, self.vfull, self.cache, L=CTX)
         torch.cuda.synchronize()
         self.len0 = self.cache.seq_len.clone()
@@ -291,8 +293,8 @@ class Round:
 
     # algorithmic bytes / flops of one launch
     def draft_bytes(self, j: int) -> int:
-        rec = self.vc.vc_record_bytes(BITS, D_HEAD)
-        ng = (CTX - RESIDUAL) // GROUP
+        rec = self.vc.vc_record_bytes(self.bits, D_HEAD)
+        ng = (CTX - self.residual) // GROUP
         n_res = CTX + j + 1 - ng * GROUP
         per_unit = ng * rec + 2 * n_res * D_HEAD * 2
         return B * HKV * per_unit + 2 * B * HQ * D_HEAD * 2
@@ -773,6 +775,36 @@ def run_sweep(args, dev):
     throughput; the divergence point of each sequence is uniform in [0, D]).
     One JSON line per horizon: tokens per round, round time, drafting and swap
     times.  Not the benchmark's contract line."""
+    if args.sweep == "budget":
+        # compressed-cache budget: code width and full-precision window; bytes
+        # the draft step reads per token of context, against round time
+        for cfg in args.sweep_budgets.split(","):
+            bits, res = (int(x) for x in cfg.split("/"))
+            rnd = Round(dev, stagger=args.stagger, bits=bits, residual=res)
+            for _ in range(args.warmup):
+                rnd.step()
+            torch.cuda.synchronize()
+            evs = [make_events(rnd.D, rnd.stagger) for _ in range(args.steps)]
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for i in range(args.steps):
+                rnd.step(evs[i])
+            t1.record()
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1) / args.steps
+            tokens = rnd.tokens_per_round()
+            d_ms = statistics.mean(sum(e["d0"][j].elapsed_time(e["d1"][j]) for j in range(rnd.D)) for e in evs)
+            per_step = rnd.draft_bytes(0)
+            full = 2 * B * HKV * CTX * D_HEAD * 2
+            print(json.dumps({"sweep": "budget", "bits": bits, "residual": res,
+                              "draft_bytes_per_step": per_step, "fraction_of_full_kv": per_step / full,
+                              "draft_attn_ms_per_round": d_ms, "draft_GB/s": rnd.D * per_step / d_ms / 1e6,
+                              "ms_per_round": ms, "tokens_per_round": tokens,
+                              "tokens_per_s": tokens / (ms / 1e3)}), flush=True)
+            del rnd
+            torch.cuda.empty_cache()
+        return
     if args.sweep == "link":
         # the full cache behind slower stores (remote prefix caching): draft and
         # verify against the full-KV baseline at each source rate
@@ -844,10 +876,12 @@ def main():
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4], help="draft cache bits (--workload model)")
-    ap.add_argument("--sweep", default=None, choices=["horizon", "link"],
+    ap.add_argument("--sweep", default=None, choices=["horizon", "link", "budget"],
                     help="print a sweep instead of the contract line")
     ap.add_argument("--sweep-links", default="native,100,50,25,12.5", help="source rates in GB/s for --sweep link")
     ap.add_argument("--sweep-horizons", default="8,16,32,64,96,128")
+    ap.add_argument("--sweep-budgets", default="2/128,2/1024,2/4096,4/128,4/1024,4/4096",
+                    help="bits/residual pairs for --sweep budget")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":

@@ -149,6 +149,7 @@ struct KiviParams {
     void *out;
     int32_t *status;
     int Hkv, Hq, grp, max_groups, res_cap, n_split_q, groups_per_split;
+    int n_split_r, res_per_split;                      // ring splits and ring tokens per split
     float qscale;                                      // sm_scale * log2(e)
 };
 
@@ -356,7 +357,8 @@ draft_kivi_kernel(KiviParams P)
     const int unit = blockIdx.x, split = blockIdx.y;   // long splits first, residual split last
     const int b = unit / P.Hkv, kvh = unit % P.Hkv;
     const int grp = P.grp;
-    float *dst = P.part + ((size_t)unit * (P.n_split_q + 1) + split) * part_floats(D);
+    const int n_split = P.n_split_q + P.n_split_r;
+    float *dst = P.part + ((size_t)unit * n_split + split) * part_floats(D);
     const TQ *qg = reinterpret_cast<const TQ *>(P.q) + ((size_t)b * P.Hq + kvh * grp) * D;
 
     for (int i = threadIdx.x; i < D / 2; i += kThreads) {
@@ -551,16 +553,32 @@ draft_kivi_kernel(KiviParams P)
             }
         }
         cta_merge_store<D>(wbuf, dst, grp);
-        last_cta_combine<TQ, D>(P.part + (size_t)unit * (P.n_split_q + 1) * part_floats(D), P.n_split_q + 1,
+        last_cta_combine<TQ, D>(P.part + (size_t)unit * n_split * part_floats(D), n_split,
                                 P.counters + unit, grp,
                                 reinterpret_cast<TQ *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
     } else {
         // ------------------------------------- residual ring (fp32 SIMT) --
+        // Split r of the ring takes positions p0 + r * res_per_split onwards;
+        // its rows are staged in shared memory (the idle stream ring) by bulk
+        // copies, a chunk at a time, so the per-token math never waits on a
+        // global load.
         const int len = P.seq_len[b];
         const int ng = min(P.n_groups[b], P.max_groups);
-        const int p0 = ng * G;
-        const TR *kr = reinterpret_cast<const TR *>(P.kres) + (size_t)unit * P.res_cap * D;
-        const TR *vr = reinterpret_cast<const TR *>(P.vres) + (size_t)unit * P.res_cap * D;
+        const int r = split - P.n_split_q;
+        const int t_lo = ng * G + r * P.res_per_split;
+        const int t_hi = min(len, t_lo + P.res_per_split);
+        constexpr int ROW = D * (int)sizeof(TR);
+        constexpr int CHUNK = (NW * Gm::NST * 2 * Gm::REC) / (2 * ROW);
+        static_assert(CHUNK >= NW, "the stream ring stages at least one token per warp");
+        const uint8_t *kr = reinterpret_cast<const uint8_t *>(P.kres) + (size_t)unit * P.res_cap * ROW;
+        const uint8_t *vr = reinterpret_cast<const uint8_t *>(P.vres) + (size_t)unit * P.res_cap * ROW;
+        const TR *ksm = reinterpret_cast<const TR *>(ring);
+        const TR *vsm = reinterpret_cast<const TR *>(ring + CHUNK * ROW);
+        uint64_t *resbar = bars;
+        if (threadIdx.x == 0) {
+            mbar_init(resbar, 1);
+            fence_mbar_init();
+        }
         constexpr int CPL = D / 32;          // channels per lane
         float qv[4][CPL];
 #pragma unroll
@@ -576,26 +594,57 @@ draft_kivi_kernel(KiviParams P)
 #pragma unroll
             for (int i = 0; i < CPL; ++i) o[h][i] = 0.f;
         }
-        for (int pos = p0 + warp; pos < len; pos += NW) {
-            const size_t slot = (size_t)(pos % P.res_cap) * D + lane * CPL;
-            float kx[CPL], vx[CPL];
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                kx[i] = Elem<TR>::to_f(kr[slot + i]);
-                vx[i] = Elem<TR>::to_f(vr[slot + i]);
+        int phase = 0;
+        for (int t0 = t_lo; t0 < t_hi; t0 += CHUNK) {
+            const int nt = min(CHUNK, t_hi - t0);
+            __syncthreads();                     // the staging bytes are free (and the barrier is set up)
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(resbar, 2u * nt * ROW);
+                // positions t0 .. t0 + nt - 1 sit at ring slots pos % res_cap:
+                // at most two contiguous runs
+                int done = 0, pos = t0;
+                while (done < nt) {
+                    const int slot = pos % P.res_cap;
+                    const int run = min(nt - done, P.res_cap - slot);
+                    bulk_g2s(ring + done * ROW, kr + (size_t)slot * ROW, run * ROW, resbar);
+                    bulk_g2s(ring + (CHUNK + done) * ROW, vr + (size_t)slot * ROW, run * ROW, resbar);
+                    done += run;
+                    pos += run;
+                }
             }
+            const bool got = mbar_wait(resbar, phase);
+            phase ^= 1;
+            if (!got) report_timeout(P.status, 2);
+            if (!__syncthreads_and(got)) {      // uniform exit; the split contributes nothing
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                float s = 0.f;
+                for (int h = 0; h < 4; ++h) {
+                    m[h] = kNegBig;
+                    l[h] = 0.f;
 #pragma unroll
-                for (int i = 0; i < CPL; ++i) s = fmaf(qv[h][i], kx[i], s);
-                s = warp_sum(s);
-                const float mn = fmaxf(m[h], s);
-                const float a = exp2f(m[h] - mn), p = exp2f(s - mn);
-                m[h] = mn;
-                l[h] = l[h] * a + p;
+                    for (int i = 0; i < CPL; ++i) o[h][i] = 0.f;
+                }
+                break;
+            }
+            for (int t = warp; t < nt; t += NW) {
+                float kx[CPL], vx[CPL];
 #pragma unroll
-                for (int i = 0; i < CPL; ++i) o[h][i] = o[h][i] * a + p * vx[i];
+                for (int i = 0; i < CPL; ++i) {
+                    kx[i] = Elem<TR>::to_f(ksm[t * D + lane * CPL + i]);
+                    vx[i] = Elem<TR>::to_f(vsm[t * D + lane * CPL + i]);
+                }
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float sdot = 0.f;
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) sdot = fmaf(qv[h][i], kx[i], sdot);
+                    sdot = warp_sum(sdot);
+                    const float mn = fmaxf(m[h], sdot);
+                    const float a = exp2f(m[h] - mn), pp = exp2f(sdot - mn);
+                    m[h] = mn;
+                    l[h] = l[h] * a + pp;
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) o[h][i] = o[h][i] * a + pp * vx[i];
+                }
             }
         }
         __syncthreads();
@@ -610,7 +659,7 @@ draft_kivi_kernel(KiviParams P)
             for (int i = 0; i < CPL; ++i) wo[(warp * 4 + h) * D + lane * CPL + i] = o[h][i];
         }
         cta_merge_store<D>(wbuf, dst, grp);
-        last_cta_combine<TQ, D>(P.part + (size_t)unit * (P.n_split_q + 1) * part_floats(D), P.n_split_q + 1,
+        last_cta_combine<TQ, D>(P.part + (size_t)unit * n_split * part_floats(D), n_split,
                                 P.counters + unit, grp,
                                 reinterpret_cast<TQ *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
     }
@@ -1042,33 +1091,38 @@ int num_sms()
 }
 
 struct KiviPlan {
-    int n_split_q, groups_per_split;
+    int n_split_q, groups_per_split, n_split_r, res_per_split;
 };
+
+constexpr int kResTokensPerSplit = 256;
 
 KiviPlan kivi_plan(const vc_qcache *c)
 {
     const int units = c->B * c->Hkv;
     const int ng = c->max_groups;
     const int slots = num_sms() * 4;                   // 4 resident CTAs per SM
+    KiviPlan p;
+    // the ring: one split per 256 of its capacity's tokens
+    p.n_split_r = std::max(1, std::min(kMaxSplit / 2, (c->res_cap + kResTokensPerSplit - 1) / kResTokensPerSplit));
+    p.res_per_split = (c->res_cap + p.n_split_r - 1) / p.n_split_r;
     // Split count minimising waves x (group pairs per warp + ~3 pairs of
-    // fixed cost per CTA) for CTAs of equal length; the residual ring is one
-    // more CTA per kv unit.
+    // fixed cost per CTA) for CTAs of equal length; the ring splits are more
+    // CTAs per kv unit.
     int best = 1;
     long best_t = -1;
     const int max_s = ng > 0 ? (ng + 3) / 4 : 1;       // at least two group pairs per split
-    for (int s = 1; s <= max_s && s < kMaxSplit; ++s) {
+    for (int s = 1; s <= max_s && s + p.n_split_r <= kMaxSplit; ++s) {
         int gps = (ng + s - 1) / s;
         gps += gps & 1;
         const int se = ng > 0 ? (ng + gps - 1) / gps : 0;
         const int pairs_per_warp = (gps / 2 + NW - 1) / NW;
-        const long waves = ((long)units * (se + 1) + slots - 1) / slots;
+        const long waves = ((long)units * (se + p.n_split_r) + slots - 1) / slots;
         const long t = waves * (pairs_per_warp + 3);
         if (best_t < 0 || t < best_t) {
             best_t = t;
             best = s;
         }
     }
-    KiviPlan p;
     p.groups_per_split = ng > 0 ? (ng + best - 1) / best : 2;
     p.groups_per_split += p.groups_per_split & 1;       // whole pairs
     p.n_split_q = ng > 0 ? (ng + p.groups_per_split - 1) / p.groups_per_split : 0;
@@ -1140,13 +1194,15 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     P.res_cap = c->res_cap;
     P.n_split_q = pl.n_split_q;
     P.groups_per_split = pl.groups_per_split;
+    P.n_split_r = pl.n_split_r;
+    P.res_per_split = pl.res_per_split;
     P.qscale = scale * kLog2e;
     size_t smem = 128 + 4 * D + (size_t)NW * Gm::NST * 2 * Gm::REC;
     const size_t merge = 128 + 4 * D + (size_t)NW * part_floats(D) * 4;
     if (smem < merge) smem = merge;
     auto kern = draft_kivi_kernel<BITS, D, TQ, TR>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    dim3 grid(c->B * c->Hkv, pl.n_split_q + 1);
+    dim3 grid(c->B * c->Hkv, pl.n_split_q + pl.n_split_r);
     kern<<<grid, kThreads, smem, st>>>(P);
     return cudaGetLastError();
 }
@@ -1230,7 +1286,7 @@ size_t draft_ws_bytes(const vc_cache_view *view, int Hq)
         const vc_qcache *c = view->kivi;
         const KiviPlan p = kivi_plan(c);
         return kStatusBytes + align256((size_t)c->B * c->Hkv * 4) +
-               align256((size_t)c->B * c->Hkv * (p.n_split_q + 1) * part_floats(c->d) * 4);
+               align256((size_t)c->B * c->Hkv * (p.n_split_q + p.n_split_r) * part_floats(c->d) * 4);
     }
     const DensePlan p = dense_plan(view);
     return kStatusBytes + align256((size_t)view->B * view->Hkv * 4) +

@@ -37,6 +37,8 @@ def _run_kivi(vc, B, Hq, Hkv, L, d, bits, R, dtype=torch.bfloat16, seed=0, extra
     (1, 4, 4, 300, 128, 2, 16, torch.bfloat16),      # grp 1
     (2, 8, 2, 100, 128, 2, 128, torch.bfloat16),     # residual only (no group)
     (1, 8, 2, 32, 64, 2, 0, torch.bfloat16),         # exactly one group, empty residual
+    (2, 8, 2, 3000, 128, 2, 1024, torch.bfloat16),   # long full-precision window: several ring splits
+    (1, 4, 2, 2000, 64, 4, 600, torch.float32),      # fp32 ring over several splits
 ])
 def test_draft_kivi_matches_oracle(B, Hq, Hkv, L, d, bits, R, dtype):
     vc = lib()
@@ -72,10 +74,9 @@ def test_draft_kivi_spare_capacity_and_ragged_lengths():
         assert_attn_close(out[b:b + 1], want, what=f"seq {b}")
 
 
-def test_draft_kivi_one_sequence_many_slices():
-    """One 32768-token sequence with 8 kv heads: each unit is cut into about
-    76 slices of the single wave, so the final merge spans more than one
-    block of split weights."""
+def test_draft_kivi_one_sequence_many_splits():
+    """One 32768-token sequence with 8 kv heads: each unit is cut into the
+    largest number of splits the merge takes."""
     vc = lib()
     k, v, q, out, scale = _run_kivi(vc, 1, 32, 8, 32768, 128, 2, 128, seed=11)
     qc = oracle.kivi_quantize(f32(k), f32(v), 2, 32, 128)
@@ -83,11 +84,13 @@ def test_draft_kivi_one_sequence_many_slices():
     assert_attn_close(out, want, what="B1 32k")
 
 
-def test_draft_kivi_mixed_lengths_slices_cross_units():
-    """Sequences of very different lengths (quantized groups 1, 91, 29, 2):
-    slices of the wave start and end inside short units and inside rings."""
+@pytest.mark.parametrize("R", [64, 512])
+def test_draft_kivi_mixed_lengths(R):
+    """Sequences of very different lengths (with R = 64: quantized groups 1,
+    91, 29, 2; with R = 512 two sequences are ring only), grown by appends so
+    that the ring wraps around many times."""
     vc = lib()
-    B, Hq, Hkv, d, bits, R, G = 4, 8, 2, 128, 2, 64, 32
+    B, Hq, Hkv, d, bits, G = 4, 8, 2, 128, 2, 32
     L0, target = 100, [100, 3000, 1000, 131]
     k, v = inputs.kv_with_outliers(B, Hkv, max(target), d, seed=21, device="cuda")
     q = inputs.normal_bf16((B, Hq, d), 121, device="cuda")
@@ -109,7 +112,7 @@ def test_draft_kivi_mixed_lengths_slices_cross_units():
     vc.vc_draft_attn(q, view, 0.09, out, ws)
     torch.cuda.synchronize()
     assert vc.vc_poll_status(ws) == 0
-    assert cache.n_groups.cpu().tolist() == [(t - R) // G for t in target]
+    assert cache.n_groups.cpu().tolist() == [max(0, (t - R) // G) for t in target]
     for b in range(B):
         L = target[b]
         qc = oracle.kivi_quantize(f32(k[b:b + 1, :, :L]), f32(v[b:b + 1, :, :L]), bits, G, R)
