@@ -331,6 +331,18 @@ vc_status vc_accept(const void *logits, vc_dtype dt, const int32_t *drafts, int 
                     cudaStream_t stream);
 
 /*
+ * vc_accept_tiles -- vc_accept from the tile maxima of the LM head's argmax
+ * epilogue (vc_gemm_argmax) instead of the logits: row (b, i), i = 0..D, has
+ * n_tiles entries tile_max[(b (D+1) + i) n_tiles + t] (the largest bf16 value
+ * of columns 128 t .. 128 t + 127, as float) and tile_idx[...] (its lowest
+ * column); the row's argmax is the largest value, the lowest column on ties,
+ * exactly the argmax vc_accept takes over the bf16 logits.  Device buffers; no
+ * workspace.  Same outputs as vc_accept.
+ */
+vc_status vc_accept_tiles(const float *tile_max, const int32_t *tile_idx, int n_tiles, const int32_t *drafts,
+                          int B, int D, int32_t *n_acc, int32_t *next_tok, cudaStream_t stream);
+
+/*
  * vc_accept_noalloc -- vc_accept for callers that cannot allocate device
  * memory (no counterpart in the paper: this is a library convenience).
  * Some callers have no way to provide the workspace vc_accept needs: code
@@ -479,6 +491,20 @@ vc_status vc_decoder_forward(const vc_decoder *dec, const int32_t *first_tok, co
                              cudaStream_t stream);
 
 /*
+ * vc_decoder_verify -- the verify pass and greedy acceptance in one call,
+ * without logits: the forward of [first_tok[b], drafts[b][0..D-1]] at
+ * positions ctx_len[b] .. ctx_len[b] + D over the full cache (as
+ * vc_decoder_forward with tokens = drafts, tok_stride = D), the LM head with
+ * the argmax epilogue, then vc_accept_tiles: n_acc[b], next_tok[b] are those
+ * vc_accept gives on the logits vc_decoder_forward would write.  D in
+ * [0, 1024]; workspace from vc_decoder_workspace_bytes with max_rows >= D + 1.
+ */
+vc_status vc_decoder_verify(const vc_decoder *dec, const int32_t *first_tok, const int32_t *drafts, int D, int B,
+                            const int32_t *ctx_len, int max_ctx, void *k_cache, void *v_cache, int L_stride,
+                            void *k_blk, void *v_blk, int32_t *n_acc, int32_t *next_tok, void *ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/*
  * vc_decoder_draft_step -- one draft step on the compressed caches (one
  * vc_qcache per layer, host array of n_layers, all of one geometry): token
  * tok[b] sits at position caches[l].seq_len[b]; its K/V are appended to every
@@ -486,7 +512,8 @@ vc_status vc_decoder_forward(const vc_decoder *dec, const int32_t *first_tok, co
  * vc_qcache_commit), attention is vc_draft_attn over the cache, and the
  * greedy draft token argmax(logits[b]) (lowest index on ties) is written to
  * next_tok[b] and, when drafts_out is not NULL, to drafts_out[b * drafts_stride].
- * logits: device [B][vocab] (written).
+ * logits: device [B][vocab] (written), or NULL: the LM head then runs with the
+ * argmax epilogue and no logits are written (same next_tok).
  */
 vc_status vc_decoder_draft_step(const vc_decoder *dec, const int32_t *tok, int B, vc_qcache *caches,
                                 void *logits, int32_t *next_tok, int32_t *drafts_out, int drafts_stride,
@@ -519,6 +546,19 @@ size_t vc_gemm_workspace_bytes(vc_dtype dt, int M, int N, int K);
 int vc_gemm_splits(vc_dtype dt, int N, int K, int decode_plan);
 vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
                   void *ws, size_t ws_bytes, cudaStream_t stream);
+/*
+ * vc_gemm_argmax -- the LM head of greedy decoding with an argmax epilogue:
+ * the product x W (bf16, N a multiple of 128, K of 64) is rounded to bf16
+ * element by element exactly as vc_gemm_ex with the same plan would store it,
+ * and every (row m, tile t of 128 columns) yields tile_max[m (N/128) + t] and
+ * tile_idx[...], the value and lowest column of the tile's maximum; the
+ * product itself is never written (paper page, "What the paper found": only
+ * the greedy token of each verify row is needed).  ws as for vc_gemm.
+ * VC_ERR_UNSUPPORTED for other shapes or types.
+ */
+vc_status vc_gemm_argmax(const void *x, const void *w, vc_dtype dt, int M, int N, int K, int decode_plan,
+                         float *tile_max, int32_t *tile_idx, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* vc_gemm with the split plan chosen explicitly: decode_plan != 0 runs the plan
  * of vc_decoder_draft_step (for M <= 16 it loads only 16 rows of x per K slice
  * and keeps six slices of W in flight); 0 is vc_gemm.  The workspace size from

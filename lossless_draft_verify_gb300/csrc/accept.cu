@@ -197,7 +197,47 @@ cudaError_t launch(const void *logits, const int32_t *drafts, int B, int D, int 
     return cudaGetLastError();
 }
 
+// Acceptance from the LM head's tile maxima ([B][D+1][n_tiles] value and
+// column of each 128-column tile's first maximum): a warp per row folds the
+// tiles with the same order (larger value, then lower column), thread 0
+// applies the greedy rule.
+__global__ void __launch_bounds__(kThreads)
+accept_tiles_kernel(const float *__restrict__ tmax, const int32_t *__restrict__ tidx, int n_tiles,
+                    const int32_t *__restrict__ drafts, int D, int32_t *__restrict__ n_acc,
+                    int32_t *__restrict__ next_tok)
+{
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ int amax[1024 + 1];
+    for (int i = warp; i <= D; i += kThreads / 32) {
+        const size_t row = (size_t)b * (D + 1) + i;
+        ArgMax best{-INFINITY, 0x7fffffff};
+        for (int t = lane; t < n_tiles; t += 32)
+            best = better(best, ArgMax{tmax[row * n_tiles + t], tidx[row * n_tiles + t]});
+        best = warp_argmax(best);
+        if (lane == 0) amax[i] = best.i;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int n = D;
+        for (int i = 0; i < D; ++i)
+            if (amax[i] != drafts[(size_t)b * D + i]) {
+                n = i;
+                break;
+            }
+        n_acc[b] = n;
+        next_tok[b] = amax[n];
+    }
+}
+
 }  // namespace
+
+cudaError_t accept_tiles(const float *tile_max, const int32_t *tile_idx, int n_tiles, const int32_t *drafts,
+                         int B, int D, int32_t *n_acc, int32_t *next_tok, cudaStream_t st)
+{
+    accept_tiles_kernel<<<B, kThreads, 0, st>>>(tile_max, tile_idx, n_tiles, drafts, D, n_acc, next_tok);
+    return cudaGetLastError();
+}
 
 size_t accept_ws_bytes(int B, int D, int V)
 {

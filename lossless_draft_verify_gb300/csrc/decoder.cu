@@ -213,7 +213,8 @@ __global__ void writeback_kernel(const T *__restrict__ kb, const T *__restrict__
 
 // ------------------------------------------------------------------ layout --
 struct Layout {
-    size_t x, h, qkv, q, att, gu, act, kvn, hl, part, dws, vws, aws, nacc, total;
+    size_t x, h, qkv, q, att, gu, act, kvn, hl, part, dws, vws, aws, nacc, tmax, tidx, lsc, total;
+    bool fused_head;      // LM head with the argmax epilogue (else logits staged in lsc)
 };
 
 Layout layout_of(const vc_decoder *d, int B, int max_rows, int max_ctx, size_t draft_ws)
@@ -252,8 +253,16 @@ Layout layout_of(const vc_decoder *d, int B, int max_rows, int max_ctx, size_t d
     L.part = take(part);
     L.dws = take(draft_ws);
     L.vws = take(verify_ws_bytes(c.dt, B, max_rows, c.n_heads, c.n_kv_heads, c.head_dim, max_ctx, kSplitTiles));
-    L.aws = take(accept_ws_bytes(B, 0, c.vocab));
+    L.aws = take(accept_ws_bytes(B, max_rows - 1, c.vocab));
     L.nacc = take((size_t)B * 4);
+    // greedy heads without a logits output: tile maxima of the argmax
+    // epilogue, or (no tensor-core head for this shape) staged logits
+    L.fused_head = gemm_argmax_ok(c.dt, (int)M, c.vocab, c.d_model, kGemmRowInvariant, true) &&
+                   gemm_argmax_ok(c.dt, B, c.vocab, c.d_model, kGemmDecode, true);
+    const size_t nt = c.vocab / kGemmTileN;
+    L.tmax = take(L.fused_head ? M * nt * 4 : 0);
+    L.tidx = take(L.fused_head ? M * nt * 4 : 0);
+    L.lsc = take(L.fused_head ? 0 : M * (size_t)c.vocab * es);
     L.total = o;
     return L;
 }
@@ -336,10 +345,34 @@ cudaError_t layer_tail(const Ctx &C, int l, int M)
     });
 }
 
+// The LM head of greedy decoding without a logits output: argmax epilogue and
+// acceptance over the tile maxima, or (no tensor-core head) staged logits and
+// the logits scan.  Rows [B][D+1]; drafts [B][D] (null for D = 0).
+cudaError_t greedy_head(const Ctx &C, const void *h, int B, int D, const int32_t *drafts, int32_t *n_acc,
+                        int32_t *next_tok)
+{
+    const vc_decoder_cfg &c = C.d->c;
+    const int M = B * (D + 1);
+    if (C.L.fused_head) {
+        const int nt = c.vocab / kGemmTileN;
+        VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
+            return gemm(h, C.d->head, nullptr, nullptr, c.dt, M, c.vocab, c.d_model, c.d_model, C.at(C.L.part),
+                        C.counters(), C.status(), C.st, C.plan, C.at<float>(C.L.tmax), C.at<int32_t>(C.L.tidx));
+        }));
+        return accept_tiles(C.at<float>(C.L.tmax), C.at<int32_t>(C.L.tidx), nt, drafts, B, D, n_acc, next_tok, C.st);
+    }
+    VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
+        return gemm(h, C.d->head, nullptr, C.at(C.L.lsc), c.dt, M, c.vocab, c.d_model, c.d_model, C.at(C.L.part),
+                    C.counters(), C.status(), C.st, C.plan);
+    }));
+    return accept(C.at(C.L.lsc), c.dt, drafts, B, D, c.vocab, n_acc, next_tok, C.at(C.L.aws), C.st);
+}
+
 template <typename T>
 cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *toks, int tok_stride, int B,
                          int Dq, const int32_t *ctx, int max_ctx, void *kc, void *vcache, int L_stride, void *kb,
-                         void *vb, int last_only, void *logits)
+                         void *vb, int last_only, void *logits, int32_t *n_acc = nullptr,
+                         int32_t *next_tok = nullptr)
 {
     const vc_decoder_cfg &c = C.d->c;
     const int M = B * Dq;
@@ -378,7 +411,12 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
         }));
         VC_TRY(layer_tail<T>(C, l, M));
     }
-    if (last_only) {
+    if (!logits) {
+        // verify: the head's argmax feeds acceptance directly (tokens after
+        // the first are the drafts)
+        VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
+        VC_TRY(greedy_head(C, h, B, Dq - 1, toks, n_acc, next_tok));
+    } else if (last_only) {
         VC_TRY(rmsnorm<T>(C, x, B, Dq, Dq - 1, C.at(C.L.hl)));
         VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
             return gemm(C.at(C.L.hl), C.d->head, nullptr, logits, c.dt, B, c.vocab, c.d_model, c.d_model, part,
@@ -441,11 +479,16 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         VC_TRY(layer_tail<T>(C, l, M));
     }
     VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
-    VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
-        return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.counters(),
-                    C.status(), C.st, C.plan);
-    }));
-    VC_TRY(accept(logits, c.dt, nullptr, B, 0, c.vocab, C.at<int32_t>(C.L.nacc), next_tok, C.at(C.L.aws), C.st));
+    if (logits) {
+        VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
+            return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.counters(),
+                        C.status(), C.st, C.plan);
+        }));
+        VC_TRY(accept(logits, c.dt, nullptr, B, 0, c.vocab, C.at<int32_t>(C.L.nacc), next_tok, C.at(C.L.aws),
+                      C.st));
+    } else {
+        VC_TRY(greedy_head(C, h, B, 0, nullptr, C.at<int32_t>(C.L.nacc), next_tok));
+    }
     if (drafts_out) {
         scatter_tokens_kernel<<<(B + 127) / 128, 128, 0, C.st>>>(next_tok, B, drafts_out, drafts_stride);
         VC_TRY(cudaGetLastError());
@@ -557,9 +600,9 @@ vc_status vc_decoder_draft_step(const vc_decoder *dec, const int32_t *tok, int B
                                 void *logits, int32_t *next_tok, int32_t *drafts_out, int drafts_stride,
                                 void *ws, size_t ws_bytes, cudaStream_t stream)
 {
-    if (!dec || !tok || !caches || !logits || !next_tok || !ws || B <= 0) return VC_ERR_INVALID;
+    if (!dec || !tok || !caches || !next_tok || !ws || B <= 0) return VC_ERR_INVALID;
     if (drafts_out && drafts_stride <= 0) return VC_ERR_INVALID;
-    if (((uintptr_t)ws & 255u) || !aligned16(logits)) return VC_ERR_INVALID;
+    if (((uintptr_t)ws & 255u) || (logits && !aligned16(logits))) return VC_ERR_INVALID;
     const vc_decoder_cfg &c = dec->c;
     for (int l = 0; l < c.n_layers; ++l) {
         const vc_qcache &q = caches[l];
@@ -634,6 +677,43 @@ vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc
                   void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     return vc_gemm_ex(x, w, resid, out, dt, M, N, K, 0, ws, ws_bytes, stream);
+}
+
+vc_status vc_gemm_argmax(const void *x, const void *w, vc_dtype dt, int M, int N, int K, int decode_plan,
+                         float *tile_max, int32_t *tile_idx, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!x || !w || !tile_max || !tile_idx || M <= 0 || N <= 0 || K <= 0) return VC_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w)) return VC_ERR_INVALID;
+    const int plan = decode_plan ? kGemmDecode : kGemmRowInvariant;
+    if (!gemm_argmax_ok(dt, M, N, K, plan, true)) return VC_ERR_UNSUPPORTED;
+    const size_t need = gemm_ws_bytes(dt, M, N, K, plan);
+    if (need && (!ws || ws_bytes < need + kGemmCounterBytes || !aligned16(ws))) return VC_ERR_INVALID;
+    return to_status(gemm(x, w, nullptr, nullptr, dt, M, N, K, K, need ? (uint8_t *)ws + kGemmCounterBytes : nullptr,
+                          need ? (unsigned int *)ws : nullptr, nullptr, stream, plan, tile_max, tile_idx));
+}
+
+vc_status vc_decoder_verify(const vc_decoder *dec, const int32_t *first_tok, const int32_t *drafts, int D, int B,
+                            const int32_t *ctx_len, int max_ctx, void *k_cache, void *v_cache, int L_stride,
+                            void *k_blk, void *v_blk, int32_t *n_acc, int32_t *next_tok, void *ws, size_t ws_bytes,
+                            cudaStream_t stream)
+{
+    if (!dec || !first_tok || !ctx_len || !k_cache || !v_cache || !n_acc || !next_tok || !ws) return VC_ERR_INVALID;
+    if (B <= 0 || D < 0 || D > 1024 || (D > 0 && !drafts)) return VC_ERR_INVALID;
+    const int Dq = D + 1;
+    if (max_ctx < 0 || L_stride < max_ctx + Dq) return VC_ERR_INVALID;
+    if ((k_blk == nullptr) != (v_blk == nullptr)) return VC_ERR_INVALID;
+    if (((uintptr_t)ws & 255u) || !aligned16(k_cache) || !aligned16(v_cache)) return VC_ERR_INVALID;
+    const Layout L = layout_of(dec, B, Dq, max_ctx, 0);
+    if (ws_bytes < L.total) return VC_ERR_INVALID;
+    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmRowInvariant};
+    const int32_t *toks = D > 0 ? drafts : nullptr;
+    const cudaError_t e =
+        dec->c.dt == VC_BF16
+            ? forward_impl<__nv_bfloat16>(C, first_tok, toks, D, B, Dq, ctx_len, max_ctx, k_cache, v_cache,
+                                          L_stride, k_blk, v_blk, 0, nullptr, n_acc, next_tok)
+            : forward_impl<float>(C, first_tok, toks, D, B, Dq, ctx_len, max_ctx, k_cache, v_cache, L_stride, k_blk,
+                                  v_blk, 0, nullptr, n_acc, next_tok);
+    return to_status(e);
 }
 
 }  // extern "C"

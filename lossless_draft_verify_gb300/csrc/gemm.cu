@@ -18,6 +18,9 @@
 // into a TMEM accumulator, warps 2-5 read TMEM and write either the output
 // (one split) or fp32 partials; the last CTA of each output tile to finish
 // (a self-resetting counter per tile in the workspace) sums them in split order.
+// Argmax epilogue (the LM head of greedy decoding): instead of the bf16 output,
+// each (row, 128-column tile) yields the value and column of the first maximum
+// of the bf16-rounded row, so the logits are never written.
 // fp32 (any shape): CUDA cores, one output element per thread, K in order.
 #include <cuda.h>
 
@@ -59,9 +62,20 @@ struct GemmArgs {
     unsigned int *counters;      // [m tiles][n tiles], zero between launches (S > 1)
     __nv_bfloat16 *out;          // [M][N]
     const __nv_bfloat16 *resid;  // [M][N] or null (may equal out)
+    float *amax_val;             // argmax epilogue: [M][N / GN] tile maxima (out not written), or null
+    int32_t *amax_idx;           // [M][N / GN] column of the first maximum in the tile
     int32_t *status;
     int M, N, K, S, kb_per_split;
 };
+
+// bf16 rounding of an output element, as the logits store would make it
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// (v, i) beats (bv, bi): larger value, the lower column on equal values
+__device__ __forceinline__ bool amax_better(float v, int i, float bv, int bi)
+{
+    return v > bv || (v == bv && i < bi);
+}
 
 __device__ __forceinline__ bool g_wait(uint64_t *bar, uint32_t parity, GemmBars *B, int32_t *status, int where)
 {
@@ -157,6 +171,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const bool ok = g_wait(&B->acc_full, 0, B, A.status, 43);
         if (ok) {
             tc::fence_after();
+            float best = -INFINITY;
+            int bidx = n0;
 #pragma unroll 1
             for (int h = 0; h < GN / 32; ++h) {
                 uint32_t u[32];
@@ -164,7 +180,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 tc::ld_wait();
                 if (m < A.M) {
                     const int c0 = n0 + h * 32;
-                    if (A.S > 1) {
+                    if (A.S == 1 && A.amax_val) {
+                        // argmax epilogue: the first maximum of the bf16-rounded row
+                        const __nv_bfloat16 *rp = A.resid ? A.resid + (size_t)m * A.N + c0 : nullptr;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const float v = bf16_round(__uint_as_float(u[c]) + (rp ? __bfloat162float(rp[c]) : 0.f));
+                            if (v > best) {
+                                best = v;
+                                bidx = c0 + c;
+                            }
+                        }
+                    } else if (A.S > 1) {
                         float *dst = A.part + ((size_t)split * A.M + m) * A.N + c0;
 #pragma unroll
                         for (int c = 0; c < 32; c += 4)
@@ -205,6 +232,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     }
                 }
             }
+            if (A.S == 1 && A.amax_val && m < A.M) {
+                const size_t t = (size_t)m * (A.N / GN) + blockIdx.y;
+                A.amax_val[t] = best;
+                A.amax_idx[t] = bidx;
+            }
         }
     }
     tc::fence_before();
@@ -244,6 +276,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     acc.y += bf16_hi(r.x);
                     acc.z += bf16_lo(r.y);
                     acc.w += bf16_hi(r.y);
+                }
+                if (A.amax_val) {
+                    // argmax epilogue: the 32 lanes of a warp hold one row's 128
+                    // columns, 4 each in column order
+                    const int c = n0 + 4 * (idx % (GN / 4));
+                    const float v[4] = {bf16_round(acc.x), bf16_round(acc.y), bf16_round(acc.z), bf16_round(acc.w)};
+                    float bv = v[0];
+                    int bi = c;
+#pragma unroll
+                    for (int e = 1; e < 4; ++e)
+                        if (v[e] > bv) {
+                            bv = v[e];
+                            bi = c + e;
+                        }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                        if (amax_better(ov, oi, bv, bi)) {
+                            bv = ov;
+                            bi = oi;
+                        }
+                    }
+                    if ((threadIdx.x & 31) == 0) {
+                        const size_t t = (size_t)m * (A.N / GN) + blockIdx.y;
+                        A.amax_val[t] = bv;
+                        A.amax_idx[t] = bi;
+                    }
+                    continue;
                 }
                 __nv_bfloat162 a2 = __floats2bfloat162_rn(acc.x, acc.y), b2 = __floats2bfloat162_rn(acc.z, acc.w);
                 uint2 o;
@@ -356,10 +417,19 @@ size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K, int plan)
     return S > 1 ? (size_t)S * M * N * 4 : 0;
 }
 
+bool gemm_argmax_ok(vc_dtype dt, int M, int N, int K, int plan, bool have_counters)
+{
+    if (!gemm_uses_tensor_cores(dt, N, K)) return false;
+    const int tiles = ((M + GM - 1) / GM) * (N / GN);
+    return gemm_splits(N, K, plan) == 1 || (have_counters && tiles <= kGemmMaxTiles);
+}
+
 cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
-                 int ldx, void *ws, unsigned int *counters, int32_t *status, cudaStream_t st, int plan)
+                 int ldx, void *ws, unsigned int *counters, int32_t *status, cudaStream_t st, int plan,
+                 float *amax_val, int32_t *amax_idx)
 {
     if (M <= 0) return cudaSuccess;
+    if (amax_val && !gemm_argmax_ok(dt, M, N, K, plan, counters != nullptr)) return cudaErrorNotSupported;
     if (gemm_uses_tensor_cores(dt, N, K)) {
         const bool small = plan == kGemmDecode && M <= 16;
         CUtensorMap mx, mw;
@@ -375,6 +445,8 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         A.counters = (A.S > 1 && counters && tiles <= kGemmMaxTiles) ? counters : nullptr;
         A.out = (__nv_bfloat16 *)out;
         A.resid = (const __nv_bfloat16 *)resid;
+        A.amax_val = amax_val;
+        A.amax_idx = amax_idx;
         A.status = status;
         A.M = M;
         A.N = N;

@@ -261,6 +261,14 @@ vc_status vc_accept(const void *logits, vc_dtype dt, const int32_t *drafts, int 
     return cuda_status(accept(logits, dt, drafts, B, D, V, n_acc, next_tok, ws, stream));
 }
 
+vc_status vc_accept_tiles(const float *tile_max, const int32_t *tile_idx, int n_tiles, const int32_t *drafts, int B,
+                          int D, int32_t *n_acc, int32_t *next_tok, cudaStream_t stream)
+{
+    if (!tile_max || !tile_idx || !n_acc || !next_tok) return VC_ERR_INVALID;
+    if (B <= 0 || D < 0 || D > 1024 || n_tiles <= 0 || (D > 0 && !drafts)) return VC_ERR_INVALID;
+    return cuda_status(accept_tiles(tile_max, tile_idx, n_tiles, drafts, B, D, n_acc, next_tok, stream));
+}
+
 vc_status vc_wait_probe(void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (!ws || ws_bytes < (size_t)kStatusBytes || !aligned(ws, 256)) return VC_ERR_INVALID;

@@ -19,6 +19,8 @@ cudaError_t qcache_append(const vc_qcache *c, const void *k_new, const void *v_n
 
 // accept.cu
 size_t accept_ws_bytes(int B, int D, int V);
+cudaError_t accept_tiles(const float *tile_max, const int32_t *tile_idx, int n_tiles, const int32_t *drafts,
+                         int B, int D, int32_t *n_acc, int32_t *next_tok, cudaStream_t st);
 cudaError_t accept(const void *logits, vc_dtype dt, const int32_t *drafts, int B, int D, int V,
                    int32_t *n_acc, int32_t *next_tok, void *ws, cudaStream_t st);
 
@@ -64,7 +66,11 @@ int gemm_splits(int N, int K, int plan);
 size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K, int plan = kGemmRowInvariant);
 cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
                  int ldx, void *ws, unsigned int *counters, int32_t *status, cudaStream_t st,
-                 int plan = kGemmRowInvariant);
+                 int plan = kGemmRowInvariant, float *amax_val = nullptr, int32_t *amax_idx = nullptr);
+// whether the argmax epilogue is available for this shape and plan (tensor-core
+// path, and one K split or per-tile counters)
+bool gemm_argmax_ok(vc_dtype dt, int M, int N, int K, int plan, bool have_counters);
+constexpr int kGemmTileN = 128;     // columns per argmax tile
 
 // host_util.cu
 int device_sm_count();

@@ -16,7 +16,8 @@ not yet cached):
   3. one forward of [x, d1..dD] at positions P..P+D over the full cache (the
      verify pass, waiting for the copy), writing the block's K/V;
   4. acceptance: n = longest prefix with argmax(row i) == d(i+1), next =
-     argmax(row n);
+     argmax(row n) (by default from the LM head's argmax epilogue, so the
+     verify logits are never written; fused_head=False writes them and scans);
   5. the compressed caches roll back to P and take the verify pass's K/V of
      the n + 1 committed rows (re-quantized); the host copy of the full cache
      receives the same rows.
@@ -57,9 +58,13 @@ class VeriCacheRunner:
     """Caches, workspaces and buffers of one decoding job (B sequences)."""
 
     def __init__(self, dec: vc.Decoder, B: int, max_len: int, horizon: int, bits: int = 2, group: int = 32,
-                 residual: int = 128, host_cache: bool = False, prefill_chunk: int = 512, device="cuda"):
+                 residual: int = 128, host_cache: bool = False, prefill_chunk: int = 512, device="cuda",
+                 fused_head: bool = True):
         cfg = dec.cfg
         self.dec, self.B, self.D, self.device = dec, B, horizon, device
+        # fused_head: draft steps and the verify pass take the greedy tokens
+        # from the LM head's argmax epilogue (no logits written)
+        self.fused_head = fused_head
         self.dtype = dec.dtype
         self.L_stride = max_len + horizon + 1
         nl, hkv, hd = cfg.n_layers, cfg.n_kv_heads, cfg.head_dim
@@ -152,8 +157,9 @@ class VeriCacheRunner:
         if ev is not None:
             ev["d0"].record(main)
         tok = self.x
+        logits_d = None if self.fused_head else self.logits_d
         for j in range(D):
-            vc.vc_decoder_draft_step(self.dec, tok, self.qc_arr, self.logits_d, self.next_d, self.ws,
+            vc.vc_decoder_draft_step(self.dec, tok, self.qc_arr, logits_d, self.next_d, self.ws,
                                      drafts_out=self.drafts[:, j], drafts_stride=D)
             tok = self.next_d
         if ev is not None:
@@ -163,11 +169,18 @@ class VeriCacheRunner:
         if ev is not None:
             ev["v0"].record(main)
         max_ctx = min(self.ctx_bound, self.L_stride - (D + 1))
-        vc.vc_decoder_forward(self.dec, self.x, self.drafts, D, B, D + 1, self.round_len, max_ctx, self.k_full,
-                              self.v_full, self.logits_v, self.ws, k_blk=self.k_blk, v_blk=self.v_blk)
-        if ev is not None:
-            ev["v1"].record(main)
-        vc.vc_accept(self.logits_v, self.drafts, self.n_acc, self.x, self.ws_acc)
+        if self.fused_head:
+            # verify pass and acceptance in one call; next token overwrites x
+            vc.vc_decoder_verify(self.dec, self.x, self.drafts, D, B, self.round_len, max_ctx, self.k_full,
+                                 self.v_full, self.n_acc, self.x, self.ws, k_blk=self.k_blk, v_blk=self.v_blk)
+            if ev is not None:
+                ev["v1"].record(main)
+        else:
+            vc.vc_decoder_forward(self.dec, self.x, self.drafts, D, B, D + 1, self.round_len, max_ctx, self.k_full,
+                                  self.v_full, self.logits_v, self.ws, k_blk=self.k_blk, v_blk=self.v_blk)
+            if ev is not None:
+                ev["v1"].record(main)
+            vc.vc_accept(self.logits_v, self.drafts, self.n_acc, self.x, self.ws_acc)
         for l, q in enumerate(self.qc):
             vc.vc_qcache_commit(q, self.k_blk[l], self.v_blk[l], self.round_len, self.n_acc)
         if self.host_cache:

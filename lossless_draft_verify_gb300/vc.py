@@ -151,6 +151,12 @@ def load() -> ctypes.CDLL:
     L.vc_gemm.argtypes = [P, P, P, P, c_int, c_int, c_int, c_int, P, c_size_t, P]
     L.vc_gemm_ex.restype = c_int
     L.vc_gemm_ex.argtypes = [P, P, P, P, c_int, c_int, c_int, c_int, c_int, P, c_size_t, P]
+    L.vc_gemm_argmax.restype = c_int
+    L.vc_gemm_argmax.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, P, P, P, c_size_t, P]
+    L.vc_accept_tiles.restype = c_int
+    L.vc_accept_tiles.argtypes = [P, P, c_int, P, c_int, c_int, P, P, P]
+    L.vc_decoder_verify.restype = c_int
+    L.vc_decoder_verify.argtypes = [P, P, P, c_int, c_int, P, c_int, P, P, c_int, P, P, P, P, P, c_size_t, P]
     _lib = L
     return L
 
@@ -164,7 +170,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm",
             "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits",
             "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe",
-            "vc_swap_in_paced"]
+            "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -420,6 +426,27 @@ def vc_gemm(x, w, out, resid=None, ws: Workspace | None = None, stream=None, dec
                              ws.nbytes if ws is not None else 0, _stream(stream)), "vc_gemm")
 
 
+def vc_gemm_argmax(x, w, tile_max, tile_idx, ws: Workspace | None = None, stream=None, decode_plan: bool = False):
+    """Tile maxima of bf16(x W): tile_max float32 [M][N/128], tile_idx int32."""
+    M, K = x.shape
+    K2, N = w.shape
+    assert K == K2 and x.is_contiguous() and w.is_contiguous()
+    assert tile_max.shape == (M, N // 128) and tile_idx.shape == (M, N // 128)
+    assert tile_max.dtype == torch.float32 and tile_idx.dtype == torch.int32
+    _check(load().vc_gemm_argmax(x.data_ptr(), w.data_ptr(), _dt(x), M, N, K, int(bool(decode_plan)),
+                                 tile_max.data_ptr(), tile_idx.data_ptr(), ws.ptr if ws is not None else None,
+                                 ws.nbytes if ws is not None else 0, _stream(stream)), "vc_gemm_argmax")
+
+
+def vc_accept_tiles(tile_max, tile_idx, drafts, n_acc, next_tok, stream=None):
+    """tile_max/tile_idx: [B][D+1][n_tiles]; same outputs as vc_accept."""
+    B, D1, nt = tile_max.shape
+    assert tile_max.is_contiguous() and tile_idx.is_contiguous()
+    dp = drafts.data_ptr() if drafts is not None and drafts.numel() else None
+    _check(load().vc_accept_tiles(tile_max.data_ptr(), tile_idx.data_ptr(), nt, dp, B, D1 - 1, n_acc.data_ptr(),
+                                  next_tok.data_ptr(), _stream(stream)), "vc_accept_tiles")
+
+
 class Decoder:
     """A vc_decoder handle plus the device weights it points to (kept alive
     here).  `weights` is a dict of tensors stored [in][out]: embed, lm_head
@@ -483,6 +510,16 @@ def vc_decoder_forward(dec: Decoder, first_tok, tokens, tok_stride: int, B: int,
                                      ws.ptr, ws.nbytes, _stream(stream)), "vc_decoder_forward")
 
 
+def vc_decoder_verify(dec: Decoder, first_tok, drafts, D: int, B: int, ctx_len, max_ctx: int, k_cache, v_cache,
+                      n_acc, next_tok, ws: Workspace, k_blk=None, v_blk=None, stream=None):
+    """Verify pass plus greedy acceptance without logits (vc_decoder_verify)."""
+    L_stride = k_cache.shape[3]
+    _check(load().vc_decoder_verify(dec.handle, first_tok.data_ptr(), _ptr(drafts), int(D), B, ctx_len.data_ptr(),
+                                    int(max_ctx), k_cache.data_ptr(), v_cache.data_ptr(), L_stride, _ptr(k_blk),
+                                    _ptr(v_blk), n_acc.data_ptr(), next_tok.data_ptr(), ws.ptr, ws.nbytes,
+                                    _stream(stream)), "vc_decoder_verify")
+
+
 def qcache_array(caches: list):
     """The host array of vc_qcache structs that vc_decoder_draft_step takes
     (one per layer; the structs are copied, the storage stays in `caches`)."""
@@ -491,8 +528,9 @@ def qcache_array(caches: list):
 
 def vc_decoder_draft_step(dec: Decoder, tok, caches_arr, logits, next_tok, ws: Workspace, drafts_out=None,
                           drafts_stride: int = 1, stream=None):
-    """caches_arr: qcache_array(caches) (built once per set of caches)."""
-    _check(load().vc_decoder_draft_step(dec.handle, tok.data_ptr(), tok.shape[0], caches_arr, logits.data_ptr(),
+    """caches_arr: qcache_array(caches) (built once per set of caches); logits
+    None runs the LM head with the argmax epilogue (no logits written)."""
+    _check(load().vc_decoder_draft_step(dec.handle, tok.data_ptr(), tok.shape[0], caches_arr, _ptr(logits),
                                         next_tok.data_ptr(), _ptr(drafts_out), int(drafts_stride), ws.ptr,
                                         ws.nbytes, _stream(stream)), "vc_decoder_draft_step")
 

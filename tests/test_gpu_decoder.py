@@ -132,8 +132,8 @@ def test_bf16_block_forward_equals_row_by_row():
     assert torch.isfinite(blk.float()).all()
 
 
-@pytest.mark.parametrize("host_cache", [True, False])
-def test_bf16_draft_and_verify_equals_greedy(host_cache):
+@pytest.mark.parametrize("host_cache,fused_head", [(True, True), (False, True), (False, False)])
+def test_bf16_draft_and_verify_equals_greedy(host_cache, fused_head):
     vc = lib()
     from lossless_draft_verify_gb300 import decode
     cfg, dec = _small_decoder(vc, seed=1)
@@ -144,9 +144,63 @@ def test_bf16_draft_and_verify_equals_greedy(host_cache):
     ref_run.prefill(prompt)
     ref = ref_run.greedy(n_new)
     run = decode.VeriCacheRunner(dec, B, P + n_new + 2 * D, D, bits=2, residual=128, host_cache=host_cache,
-                                 prefill_chunk=256)
+                                 prefill_chunk=256, fused_head=fused_head)
     run.prefill(prompt)
     toks, acc = run.generate(n_new)
     assert toks == ref
     assert _status_ok(vc, run.ws) and _status_ok(vc, ref_run.ws)
     assert all(0 <= a <= D for seq in acc for a in seq)
+
+
+def test_bf16_fused_verify_equals_logits_and_scan():
+    """vc_decoder_verify (LM head with the argmax epilogue, acceptance over the
+    tile maxima) gives the n_acc / next that the oracle's acceptance finds on
+    the logits vc_decoder_forward writes, with drafts that follow the greedy
+    tokens for a random number of rows and then diverge."""
+    import oracle
+    vc = lib()
+    cfg, dec = _small_decoder(vc, seed=2)
+    B, P, D = 4, 200, 6
+    g = torch.Generator().manual_seed(5)
+    prompt = torch.randint(0, cfg.vocab, (B, P), generator=g, dtype=torch.int32).cuda()
+    Ls = P + D + 8
+    shape = (cfg.n_layers, B, cfg.n_kv_heads, Ls, cfg.head_dim)
+    kc = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+    vcache = torch.zeros_like(kc)
+    ws = vc.Workspace(dec.workspace_bytes(B, P, Ls - P))
+    ctx0 = torch.zeros(B, dtype=torch.int32, device="cuda")
+    last = torch.zeros(B, cfg.vocab, dtype=torch.bfloat16, device="cuda")
+    vc.vc_decoder_forward(dec, None, prompt, P, B, P, ctx0, 0, kc, vcache, last, ws, last_only=True)
+    torch.cuda.synchronize()
+    x = torch.tensor(oracle.accept(last.float().cpu().numpy()[:, None, :], np.zeros((B, 0), np.int32))[1],
+                     dtype=torch.int32, device="cuda")
+    ctxP = torch.full((B,), P, dtype=torch.int32, device="cuda")
+    # greedy drafts for every row: one forward per row on a copy of the cache
+    kg, vg = kc.clone(), vcache.clone()
+    tok, greedy = x.clone(), []
+    for i in range(D):
+        c = torch.full((B,), P + i, dtype=torch.int32, device="cuda")
+        one = torch.zeros(B, cfg.vocab, dtype=torch.bfloat16, device="cuda")
+        vc.vc_decoder_forward(dec, tok, None, 0, B, 1, c, P + i, kg, vg, one, ws, last_only=True)
+        torch.cuda.synchronize()
+        tok = torch.tensor(oracle.accept(one.float().cpu().numpy()[:, None, :], np.zeros((B, 0), np.int32))[1],
+                           dtype=torch.int32, device="cuda")
+        greedy.append(tok)
+    drafts = torch.stack(greedy, 1).contiguous()
+    keep = [0, 2, D, 4]                          # rows of each sequence that follow the greedy tokens
+    for b, k in enumerate(keep):
+        if k < D:
+            drafts[b, k] = (drafts[b, k] + 1) % cfg.vocab
+    logits = torch.zeros(B, D + 1, cfg.vocab, dtype=torch.bfloat16, device="cuda")
+    k1, v1 = kc.clone(), vcache.clone()
+    vc.vc_decoder_forward(dec, x, drafts, D, B, D + 1, ctxP, P, k1, v1, logits, ws)
+    n_acc = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    nxt = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    k2, v2 = kc.clone(), vcache.clone()
+    vc.vc_decoder_verify(dec, x, drafts, D, B, ctxP, P, k2, v2, n_acc, nxt, ws)
+    torch.cuda.synchronize()
+    assert _status_ok(vc, ws)
+    want_n, want_next, _ = oracle.accept(logits.float().cpu().numpy(), drafts.cpu().numpy())
+    assert n_acc.cpu().tolist() == list(want_n) and nxt.cpu().tolist() == list(want_next)
+    assert n_acc.cpu().tolist() == keep
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)

@@ -78,3 +78,75 @@ def test_gemm_fp32_matches_definition():
     got = f32(_run(vc, x, w)).astype(np.float64)
     want = f32(x).astype(np.float64) @ f32(w).astype(np.float64)
     assert np.abs(got - want).max() <= 1e-5 * np.abs(want).max()
+
+
+def _tile_argmax(out_f32: np.ndarray):
+    """Per (row, 128-column tile): the largest value and the lowest column holding it."""
+    M, N = out_f32.shape
+    t = out_f32.reshape(M, N // 128, 128)
+    return t.max(-1), (t.argmax(-1) + 128 * np.arange(N // 128)[None, :]).astype(np.int32)
+
+
+@pytest.mark.parametrize("M,N,K,plan", [(8, 32000, 4096, True), (264, 32000, 4096, False), (33, 2048, 512, False),
+                                        (5, 151936, 1024, True), (1, 128, 64, False), (130, 1024, 2048, False)])
+def test_gemm_argmax_epilogue_matches_stored_product(M, N, K, plan):
+    """The argmax epilogue's tile maxima are those of the bf16 product vc_gemm
+    stores with the same plan (one K split and split-K shapes), including ties
+    planted by duplicating the winning column inside its tile, in a later
+    tile and in an earlier tile (the lowest column must win)."""
+    vc = lib()
+    x = inputs.normal_bf16((M, K), 11 + M, device="cuda")
+    w = inputs.normal_bf16((K, N), 12 + N, device="cuda", std=0.02)
+    out = _run(vc, x, w, decode_plan=plan)
+    a = int(f32(out)[0].argmax())
+    for j in {a ^ 1, (a + 3 * 128) % N, (a - 2 * 128) % N}:
+        w[:, j] = w[:, a]
+    out = f32(_run(vc, x, w, decode_plan=plan))
+    nt = N // 128
+    tmax = torch.empty(M, nt, dtype=torch.float32, device="cuda")
+    tidx = torch.empty(M, nt, dtype=torch.int32, device="cuda")
+    ws = vc.Workspace(vc.vc_gemm_workspace_bytes(x.dtype, M, N, K))
+    vc.vc_gemm_argmax(x, w, tmax, tidx, ws=ws, decode_plan=plan)
+    torch.cuda.synchronize()
+    want_v, want_i = _tile_argmax(out)
+    np.testing.assert_array_equal(tmax.cpu().numpy(), want_v)
+    np.testing.assert_array_equal(tidx.cpu().numpy(), want_i)
+    # the planted tie: row 0's overall argmax is the lowest duplicate
+    row0 = out[0]
+    assert int(np.flatnonzero(row0 == row0.max())[0]) == min({a, a ^ 1, (a + 3 * 128) % N, (a - 2 * 128) % N})
+
+
+@pytest.mark.parametrize("V", [2048, 151936])
+def test_accept_from_tile_maxima_matches_oracle(V):
+    """Greedy acceptance from the argmax epilogue's tile maxima equals the
+    oracle's acceptance over the stored logits (and vc_accept's), for drafts
+    that follow the greedy tokens for 0..D rows."""
+    import oracle
+    vc = lib()
+    B, D, K = 5, 7, 512
+    M = B * (D + 1)
+    x = inputs.normal_bf16((M, K), 21, device="cuda")
+    w = inputs.normal_bf16((K, V), 22, device="cuda", std=0.05)
+    logits = _run(vc, x, w).view(B, D + 1, V)
+    am = oracle.accept(f32(logits), np.zeros((B, D), np.int32))[2]
+    keep = [0, 3, D, 1, 6]
+    drafts = am[:, :D].copy()
+    for b, k in enumerate(keep):
+        if k < D:
+            drafts[b, k] = (drafts[b, k] + 1) % V
+    dr = torch.tensor(drafts, dtype=torch.int32, device="cuda")
+    tmax = torch.empty(M, V // 128, dtype=torch.float32, device="cuda")
+    tidx = torch.empty(M, V // 128, dtype=torch.int32, device="cuda")
+    ws = vc.Workspace(vc.vc_gemm_workspace_bytes(x.dtype, M, V, K))
+    vc.vc_gemm_argmax(x, w, tmax, tidx, ws=ws)
+    n_acc = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    nxt = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    vc.vc_accept_tiles(tmax.view(B, D + 1, -1), tidx.view(B, D + 1, -1), dr, n_acc, nxt)
+    n2, x2 = torch.full_like(n_acc, -1), torch.full_like(nxt, -1)
+    wa = vc.Workspace(vc.vc_accept_workspace_bytes(B, D, V))
+    vc.vc_accept(logits.contiguous(), dr, n2, x2, wa)
+    torch.cuda.synchronize()
+    want_n, want_x, _ = oracle.accept(f32(logits), drafts)
+    assert n_acc.cpu().tolist() == list(want_n) == keep
+    assert nxt.cpu().tolist() == list(want_x)
+    assert n2.cpu().tolist() == list(want_n) and x2.cpu().tolist() == list(want_x)
