@@ -13,13 +13,19 @@
 
 #include <algorithm>
 #include <new>
+#include <cmath>
 #include <vector>
 
 #include "vc_common.cuh"
 #include "vc_internal.h"
 
+struct RopeFreq {
+    double inv_freq[64];          // theta^(-2j / head_dim), j < head_dim / 2
+};
+
 struct vc_decoder {
     vc_decoder_cfg c;
+    RopeFreq rope;
     const void *embed, *head;
     std::vector<const void *> wqkv, wo, wgu, wd;
     // optional trace: event pairs around selected operations (caller-owned)
@@ -38,6 +44,7 @@ constexpr int kBadToken = 1 << 1;       // status bit: a token id outside [0, vo
 constexpr int kBadPosition = 1 << 2;    // status bit: a position outside the cache
 
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+int rope_blocks(const vc_decoder_cfg &c) { return (c.n_heads + 2 * c.n_kv_heads + 3) / 4; }
 size_t esize(vc_dtype dt) { return dt == VC_BF16 ? 2 : 4; }
 
 // ------------------------------------------------------------------ kernels --
@@ -101,12 +108,18 @@ struct RopeDst {
     int stride2;
 };
 
+// One CTA per (row, block of kRopeHeads heads of q|k|v), one thread per
+// rotated pair (j, j + hd/2).  The inverse frequencies are fp64 (tabulated
+// once per decoder); the angle pos * inv_freq is formed and reduced modulo
+// 2 pi in fp64 (positions reach 10^5 radians), then cos/sin of the small
+// remainder in fp32.
+constexpr int kRopeHeads = 4;
+
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kRopeHeads * 64)
 rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd, const int32_t *__restrict__ pos_base,
-            float theta, T *__restrict__ q_out, RopeDst dst, int32_t *status)
+            RopeFreq fr, T *__restrict__ q_out, RopeDst dst, int32_t *status)
 {
-    __shared__ float cs[64], sn[64];
     const int m = blockIdx.x;
     const int b = m / rows_per_seq, i = m % rows_per_seq;
     const int pos = pos_base[b] + i;
@@ -114,54 +127,49 @@ rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd
     const int row1 = dst.pos1 ? pos : i;
     if (row1 < 0 || row1 >= dst.stride1) {
         // a position outside the cache: record it, write nothing
-        if (threadIdx.x == 0) atomicOr(status, kBadPosition);
+        if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(status, kBadPosition);
         return;
     }
-    for (int j = threadIdx.x; j < half; j += kRowThreads) {
-        // angle in fp64 (positions reach 10^5 radians), reduced to [-pi, pi]
-        // in fp64, then fp32 cos/sin of the small remainder
-        constexpr double kTwoPi = 6.283185307179586476925286766559;
-        const double inv_freq = exp2(-(2.0 * (double)j / (double)hd) * log2((double)theta));
-        const double ang = (double)pos * inv_freq;
-        const double red = fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);
-        float s, c;
-        sincosf((float)red, &s, &c);
-        cs[j] = c;
-        sn[j] = s;
-    }
-    __syncthreads();
+    const int hh = blockIdx.y * kRopeHeads + threadIdx.x / half;   // head among q | k | v
+    const int j = threadIdx.x % half;
+    if (threadIdx.x >= kRopeHeads * half || hh >= Hq + 2 * Hkv) return;
     const T *row = qkv + (size_t)m * (Hq + 2 * Hkv) * hd;
-    const int nq = Hq * half, nk = Hkv * half, nv = Hkv * hd;
-    for (int t = threadIdx.x; t < nq + nk + nv; t += kRowThreads) {
-        if (t < nq + nk) {
-            const bool isq = t < nq;
-            const int u = isq ? t : t - nq;
-            const int h = u / half, j = u % half;
-            const T *src = row + (isq ? 0 : Hq * hd) + h * hd;
-            const float x1 = Elem<T>::to_f(src[j]), x2 = Elem<T>::to_f(src[j + half]);
-            const float c = cs[j], s = sn[j];
-            const T y1 = Elem<T>::from_f(x1 * c - x2 * s);
-            const T y2 = Elem<T>::from_f(x2 * c + x1 * s);
-            if (isq) {
-                T *qo = q_out + (size_t)m * Hq * hd + h * hd;
-                qo[j] = y1;
-                qo[j + half] = y2;
-            } else {
-                T *k1 = (T *)dst.k1 + b * dst.bstride1 + ((size_t)h * dst.stride1 + row1) * hd;
-                k1[j] = y1;
-                k1[j + half] = y2;
-                if (dst.k2) {
-                    T *k2 = (T *)dst.k2 + b * dst.bstride2 + ((size_t)h * dst.stride2 + i) * hd;
-                    k2[j] = y1;
-                    k2[j + half] = y2;
-                }
-            }
-        } else {
-            const int u = t - nq - nk;
-            const int h = u / hd, c = u % hd;
-            const T val = row[(Hq + Hkv) * hd + u];
-            ((T *)dst.v1)[b * dst.bstride1 + ((size_t)h * dst.stride1 + row1) * hd + c] = val;
-            if (dst.v2) ((T *)dst.v2)[b * dst.bstride2 + ((size_t)h * dst.stride2 + i) * hd + c] = val;
+    const T *src = row + (size_t)hh * hd;
+    if (hh >= Hq + Hkv) {
+        // v: copied into the cache (and the block copy)
+        const int h = hh - Hq - Hkv;
+        const T v0 = src[j], v1 = src[j + half];
+        T *d1 = (T *)dst.v1 + b * dst.bstride1 + ((size_t)h * dst.stride1 + row1) * hd;
+        d1[j] = v0;
+        d1[j + half] = v1;
+        if (dst.v2) {
+            T *d2 = (T *)dst.v2 + b * dst.bstride2 + ((size_t)h * dst.stride2 + i) * hd;
+            d2[j] = v0;
+            d2[j + half] = v1;
+        }
+        return;
+    }
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
+    const double ang = (double)pos * fr.inv_freq[j];
+    const double red = fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);
+    float sn, cs;
+    sincosf((float)red, &sn, &cs);
+    const float x1 = Elem<T>::to_f(src[j]), x2 = Elem<T>::to_f(src[j + half]);
+    const T y1 = Elem<T>::from_f(x1 * cs - x2 * sn);
+    const T y2 = Elem<T>::from_f(x2 * cs + x1 * sn);
+    if (hh < Hq) {
+        T *qo = q_out + (size_t)m * Hq * hd + (size_t)hh * hd;
+        qo[j] = y1;
+        qo[j + half] = y2;
+    } else {
+        const int h = hh - Hq;
+        T *k1 = (T *)dst.k1 + b * dst.bstride1 + ((size_t)h * dst.stride1 + row1) * hd;
+        k1[j] = y1;
+        k1[j + half] = y2;
+        if (dst.k2) {
+            T *k2 = (T *)dst.k2 + b * dst.bstride2 + ((size_t)h * dst.stride2 + i) * hd;
+            k2[j] = y1;
+            k2[j + half] = y2;
         }
     }
 }
@@ -402,8 +410,8 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
         dst.v2 = vb ? (void *)((T *)vb + l * layer_blk) : nullptr;
         dst.bstride2 = (size_t)c.n_kv_heads * Dq * hd;
         dst.stride2 = Dq;
-        rope_kernel<T><<<M, kRowThreads, 0, C.st>>>(C.at<const T>(C.L.qkv), Dq, c.n_heads, c.n_kv_heads, hd, ctx,
-                                                    c.rope_theta, C.at<T>(C.L.q), dst, C.status());
+        rope_kernel<T><<<dim3(M, rope_blocks(c)), kRopeHeads * 64, 0, C.st>>>(
+            C.at<const T>(C.L.qkv), Dq, c.n_heads, c.n_kv_heads, hd, ctx, C.d->rope, C.at<T>(C.L.q), dst, C.status());
         VC_TRY(cudaGetLastError());
         VC_TRY(traced(C, VC_TRACE_VERIFY_ATTN, [&] {
             return verify_attn(C.at(C.L.q), dst.k1, dst.v1, c.dt, ctx, B, Dq, c.n_heads, c.n_kv_heads, hd, L_stride,
@@ -465,9 +473,9 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         dst.k2 = dst.v2 = nullptr;
         dst.bstride2 = 0;
         dst.stride2 = 1;
-        rope_kernel<T><<<M, kRowThreads, 0, C.st>>>(C.at<const T>(C.L.qkv), 1, c.n_heads, c.n_kv_heads, hd,
-                                                    caches[l].seq_len, c.rope_theta, C.at<T>(C.L.q), dst,
-                                                    C.status());
+        rope_kernel<T><<<dim3(M, rope_blocks(c)), kRopeHeads * 64, 0, C.st>>>(
+            C.at<const T>(C.L.qkv), 1, c.n_heads, c.n_kv_heads, hd, caches[l].seq_len, C.d->rope, C.at<T>(C.L.q), dst,
+            C.status());
         VC_TRY(cudaGetLastError());
         VC_TRY(qcache_append(&caches[l], kn, vn, nullptr, nullptr, nullptr, 1, 0, C.st));
         vc_cache_view view{};
@@ -530,6 +538,8 @@ vc_status vc_decoder_create(const vc_decoder_cfg *cfg, const vc_decoder_weights 
     vc_decoder *d = new (std::nothrow) vc_decoder;
     if (!d) return VC_ERR_INVALID;
     d->c = c;
+    for (int j = 0; j < c.head_dim / 2; ++j)
+        d->rope.inv_freq[j] = std::pow((double)c.rope_theta, -2.0 * j / (double)c.head_dim);
     d->embed = w->embed;
     d->head = w->lm_head;
     for (int l = 0; l < c.n_layers; ++l) {

@@ -32,6 +32,7 @@ namespace vc {
 namespace {
 
 constexpr int GM = 128, GN = 128, GK = 64;
+constexpr int kGemmFusedReduceTiles = 64;
 constexpr int G_THREADS = 192;
 constexpr uint32_t G_TMEM_COLS = 128;
 constexpr int G_MAX_STAGES = 6;
@@ -198,7 +199,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                             *reinterpret_cast<float4 *>(dst + c) =
                                 make_float4(__uint_as_float(u[c]), __uint_as_float(u[c + 1]),
                                             __uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
-                        __threadfence();
                     } else {
                         const size_t off = (size_t)m * A.N + c0;
                         uint32_t packed[16];
@@ -237,6 +237,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 A.amax_val[t] = best;
                 A.amax_idx[t] = bidx;
             }
+            if (A.S > 1 && A.counters) __threadfence();   // partials visible before this CTA's arrival
         }
     }
     tc::fence_before();
@@ -262,13 +263,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             for (int idx = threadIdx.x; idx < rows * (GN / 4); idx += G_THREADS) {
                 const int m = m0 + idx / (GN / 4);
                 const size_t off = (size_t)m * A.N + n0 + 4 * (idx % (GN / 4));
+                // loads of up to 8 splits in flight at once, summed in split order
                 float4 acc = __ldcg(reinterpret_cast<const float4 *>(A.part + off));
-                for (int sp = 1; sp < A.S; ++sp) {
-                    const float4 p = __ldcg(reinterpret_cast<const float4 *>(A.part + sp * plane + off));
-                    acc.x += p.x;
-                    acc.y += p.y;
-                    acc.z += p.z;
-                    acc.w += p.w;
+                for (int s0 = 1; s0 < A.S; s0 += 8) {
+                    float4 p[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (s0 + j < A.S)
+                            p[j] = __ldcg(reinterpret_cast<const float4 *>(A.part + (s0 + j) * plane + off));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (s0 + j < A.S) {
+                            acc.x += p[j].x;
+                            acc.y += p[j].y;
+                            acc.z += p[j].z;
+                            acc.w += p[j].w;
+                        }
                 }
                 if (A.resid) {
                     const uint2 r = *reinterpret_cast<const uint2 *>(A.resid + off);
@@ -441,8 +451,14 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         const int nkb = K / GK;
         A.kb_per_split = (nkb + A.S - 1) / A.S;
         A.part = (float *)ws;
+        // Split-K partials are summed by the last CTA of each output tile when
+        // the grid has few tiles (measured faster there: one launch less) or
+        // when the argmax epilogue needs it; wider products use the
+        // all-SM reduction kernel, which measured faster once many tiles
+        // finish at the end of the launch (same summation order either way).
         const int tiles = ((M + GM - 1) / GM) * (N / GN);
-        A.counters = (A.S > 1 && counters && tiles <= kGemmMaxTiles) ? counters : nullptr;
+        const bool fuse = amax_val || tiles <= kGemmFusedReduceTiles;
+        A.counters = (A.S > 1 && counters && tiles <= kGemmMaxTiles && fuse) ? counters : nullptr;
         A.out = (__nv_bfloat16 *)out;
         A.resid = (const __nv_bfloat16 *)resid;
         A.amax_val = amax_val;
