@@ -62,9 +62,9 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("b95cb27ece693aaf2aa9f55244210f9eb60b08e37e375315b19f855d7ce7c520",
+    "sha256": ("2de3e9740fc01621b9a2aeb2b60d103cdb79d683c1234b880a533bfaf941c54c",
                "607af49c7988512f8f8974c461106d2011be78ddbca72ebbb92fc5182dcc3286"),
-    "bytes": 411.009792e6 + 4.827904e6,
+    "bytes": 411.015680e6 + 4.840192e6,
     "algorithmic_bytes": 409731072,
 }
 
