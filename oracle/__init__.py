@@ -121,6 +121,66 @@ def bf16_bits_to_f32(bits) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
+def bf16_round(x) -> np.ndarray:
+    """binary32 -> nearest bfloat16 (ties to even), as binary32 values
+    (finite inputs)."""
+    u = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return r.astype(np.uint32).view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# Rotation before quantization (RotateKV, named among the compressors on the
+# paper page, "What the paper found" and its reference list).  Reading: a
+# fixed Walsh-Hadamard rotation of every key row (channels mixed, outliers
+# spread) ahead of the KIVI quantizer, the query rotated the same way so that
+# q k^T is unchanged; the outlier-aware adaptive parts of RotateKV are not
+# described on the pages and are left out.
+# --------------------------------------------------------------------------
+
+def fwht_f32(x) -> np.ndarray:
+    """Walsh-Hadamard transform of the last axis (a power of two) in binary32:
+    the butterfly network with stages h = 1, 2, ..., d/2, each mapping the
+    pair (i, i + h), i mod 2h < h, to (a + b, a - b), every operation rounded
+    to binary32.  Equals x H_d with H_d the Sylvester Hadamard matrix up to
+    that rounding (exactly when no sum is inexact)."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    d = y.shape[-1]
+    assert d > 0 and d & (d - 1) == 0
+    lead = y.shape[:-1]
+    h = 1
+    while h < d:
+        z = y.reshape(*lead, d // (2 * h), 2, h)
+        a = z[..., 0, :].copy()
+        b = z[..., 1, :].copy()
+        z[..., 0, :] = a + b
+        z[..., 1, :] = a - b
+        y = z.reshape(*lead, d)
+        h *= 2
+    return y
+
+
+def rotation_scales(d: int) -> tuple[float, float]:
+    """Powers of two (key, query) whose product is 1/d: (x H s_k) . (y H s_q)
+    = x . y since H H^T = d I."""
+    lg = int(d).bit_length() - 1
+    return 2.0 ** -((lg + 1) // 2), 2.0 ** -(lg // 2)
+
+
+def rotate_keys(k, bf16: bool = True) -> np.ndarray:
+    """Key rows as the rotated cache stores them: fwht_f32(k) * s_k, rounded
+    to the cache's element type (bfloat16, or binary32)."""
+    sk, _ = rotation_scales(np.shape(k)[-1])
+    r = fwht_f32(_f32(k)) * np.float32(sk)
+    return bf16_round(r) if bf16 else r
+
+
+def rotate_queries(q) -> np.ndarray:
+    """Queries for a rotated cache: fwht_f32(q) * s_q (binary32)."""
+    _, sq = rotation_scales(np.shape(q)[-1])
+    return fwht_f32(_f32(q)) * np.float32(sq)
+
+
 # --------------------------------------------------------------------------
 # KIVI-style quantization (KIVI: source 4 on the podparley page, ref [42] on
 # pith.science; named as a compressor on the paper page, "What the paper found")
@@ -137,14 +197,19 @@ def quantize_group(x, bits: int):
     return codes, int(s[0]), int(z[0])
 
 
-def kivi_quantize(k, v, bits: int, group: int = 32, residual: int = 0):
-    """Quantize a cache k, v [B][H][L][d] (fp32 images of the inputs).
+def kivi_quantize(k, v, bits: int, group: int = 32, residual: int = 0, rotate: bool = False,
+                  rotate_bf16: bool = True):
+    """Quantize a cache k, v [B][H][L][d] (fp32 images of the inputs).  With
+    rotate, the key rows are first replaced by rotate_keys(k, rotate_bf16)
+    (the rotated cache, residual included, holds rotated keys).
 
     Returns a dict of logical arrays: nq, kcode [B,H,nq,d], kscale/kzero
     [B,H,nq/G,d] (fp16 bits), vcode [B,H,nq,d], vscale/vzero [B,H,nq,d/G],
     kres/vres [B,H,L-nq,d] (fp32)."""
     k = _f32(k)
     v = _f32(v)
+    if rotate:
+        k = np.ascontiguousarray(rotate_keys(k, rotate_bf16))
     B, H, L, d = k.shape
     nq = ((L - residual) // group) * group if L - residual > 0 else 0
     ng = nq // group
@@ -157,7 +222,7 @@ def kivi_quantize(k, v, bits: int, group: int = 32, residual: int = 0):
     got = lib().orc_kivi_quantize(_p(k), _p(v), B, H, L, d, bits, group, residual,
                                   _p(kcode), _p(ks), _p(kz), _p(vcode), _p(vs), _p(vz))
     assert got == nq
-    return dict(nq=nq, bits=bits, group=group, kcode=kcode, kscale=ks, kzero=kz,
+    return dict(nq=nq, bits=bits, group=group, rotate=bool(rotate), kcode=kcode, kscale=ks, kzero=kz,
                 vcode=vcode, vscale=vs, vzero=vz,
                 kres=np.ascontiguousarray(k[:, :, nq:, :]),
                 vres=np.ascontiguousarray(v[:, :, nq:, :]))
@@ -206,8 +271,11 @@ def unpack_records(rec: np.ndarray, bits: int, d: int, group: int = 32):
 
 def kivi_decode_attn(q, qc, scale: float) -> np.ndarray:
     """Decode attention of q [B,Hq,d] over a KIVI cache from kivi_quantize
-    (all sequences the same length nq + residual)."""
+    (all sequences the same length nq + residual); a rotated cache is read
+    with rotate_queries(q)."""
     q = _f32(q)
+    if qc.get("rotate"):
+        q = np.ascontiguousarray(rotate_queries(q))
     B, Hq, d = q.shape
     Hkv = qc["kcode"].shape[1]
     nq = qc["nq"]
