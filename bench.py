@@ -577,7 +577,7 @@ def run_model(args, dev, rank, world, barrier, pg):
     total = args.warmup + args.steps + n_e2e
     max_len = P + total * (M_HORIZON + 1) + 64
     run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=args.bits, residual=M_RESIDUAL, host_cache=True,
-                                 prefill_chunk=512, device=dev)
+                                 prefill_chunk=512, device=dev, rotate=args.rotate)
     prompt = inputs.random_prompts(M_B, P, cfg.vocab, seed=rank, device=dev)
     t_pf = time.perf_counter()
     run.prefill(prompt)
@@ -692,7 +692,9 @@ def run_model(args, dev, rank, world, barrier, pg):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
-            "config": {"workload": MODEL_WORKLOAD.format(ctx=P, bits=args.bits), "global_batch": M_B * world,
+            "config": {"workload": MODEL_WORKLOAD.format(ctx=P, bits=args.bits) +
+                       (", keys rotated (Walsh-Hadamard) before quantization" if args.rotate else ""),
+                       "global_batch": M_B * world,
                        "seq_len": P,
                        "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
             "roofline": roof,
@@ -876,6 +878,8 @@ def main():
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4], help="draft cache bits (--workload model)")
+    ap.add_argument("--rotate", action="store_true",
+                    help="draft caches with rotated keys (--workload model; the RotateKV-style variant)")
     ap.add_argument("--sweep", default=None, choices=["horizon", "link", "budget"],
                     help="print a sweep instead of the contract line")
     ap.add_argument("--sweep-links", default="native,100,50,25,12.5", help="source rates in GB/s for --sweep link")

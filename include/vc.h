@@ -130,6 +130,16 @@ vc_status vc_wait_probe(void *ws, size_t ws_bytes, cudaStream_t stream);
  *     offset + 2d.  K: n = 2 ks + rr holds (s[c0], s[c0+1]), c0 = 16 ks + 2 j +
  *     8 rr.  V: n = (2 ks + rr)*(d/32) + gc holds (s[t0][gc], s[t0+1][gc]),
  *     t0 = 16 ks + 2 j + 8 rr.
+ * Rotated cache (rotate = 1; RotateKV, named among the compressors on the
+ * paper page, "What the paper found"; the library's reading is a fixed
+ * rotation, the pages describe no adaptive part): every key row x, quantized
+ * or in the ring, is stored as res_dtype(W(x) * 2^-ceil(log2(d)/2)), W the
+ * binary32 Walsh-Hadamard butterfly network (stages h = 1, 2, ..., d/2, the
+ * pair (i, i + h), i mod 2h < h, becoming (a + b, a - b), each rounded to
+ * binary32); vc_draft_attn applies W(q) * 2^-floor(log2(d)/2) to the queries,
+ * so rotated dot products equal the plain ones.  Values are not rotated.
+ * Appends and commits rotate the new key rows the same way.
+ *
  * Full-precision tokens (positions n_groups[b]*group .. seq_len[b]-1) live in
  * a ring: position p of (b, h) at k_res/v_res + ((b * Hkv + h) * res_cap +
  * p % res_cap) * d elements.
@@ -139,6 +149,7 @@ typedef struct vc_quant_cfg {
     int32_t bits;        /* 2 or 4 */
     int32_t group;       /* 32 */
     int32_t residual;    /* R: tokens kept full precision (the newest R..R+group-1) */
+    int32_t rotate;      /* 1: rotated cache (below), 0: plain */
 } vc_quant_cfg;
 
 typedef struct vc_qcache {

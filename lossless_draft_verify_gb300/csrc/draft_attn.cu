@@ -338,7 +338,31 @@ __device__ __forceinline__ void group_values(const uint8_t *rec, const uint8_t *
     }
 }
 
-template <int BITS, int D, typename TQ, typename TR>
+// Rotated-cache queries: rq[h][c] = W(q_h)[c] * 2^-floor(log2(D)/2) for the
+// CTA's kv head (W the binary32 Walsh-Hadamard butterfly of the cache's key
+// rotation, stages h = 1, ..., D/2, pair (i, i + h) -> (a + b, a - b)); rows
+// h >= grp are zero.  Block-uniform call.
+template <typename TQ, int D>
+__device__ void rotate_queries(const TQ *qg, int grp, float *rq)
+{
+    for (int i = threadIdx.x; i < 4 * D; i += kThreads) rq[i] = i / D < grp ? Elem<TQ>::to_f(qg[i]) : 0.f;
+    __syncthreads();
+    for (int h = 1; h < D; h <<= 1) {
+        for (int p = threadIdx.x; p < 4 * (D / 2); p += kThreads) {
+            const int r = p / (D / 2), kk = p % (D / 2);
+            const int i = r * D + (kk / h) * 2 * h + (kk % h);
+            const float a = rq[i], b = rq[i + h];
+            rq[i] = a + b;
+            rq[i + h] = a - b;
+        }
+        __syncthreads();
+    }
+    constexpr float kScale = 0.125f;     // 2^-floor(log2(D)/2) for D = 128 and D = 64
+    for (int i = threadIdx.x; i < 4 * D; i += kThreads) rq[i] *= kScale;
+    __syncthreads();
+}
+
+template <int BITS, int D, typename TQ, typename TR, bool ROT>
 __global__ void __launch_bounds__(kThreads, 4)
 draft_kivi_kernel(KiviParams P)
 {
@@ -349,7 +373,8 @@ draft_kivi_kernel(KiviParams P)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);               // [NW][NST]
     uint8_t *ones = smem + 128;                                         // 2D bytes of fp16 1.0
     uint8_t *zeros = ones + 2 * D;                                      // 2D bytes of 0
-    uint8_t *ring = zeros + 2 * D;                                      // [NW][NST][2 records]
+    float *rq = reinterpret_cast<float *>(zeros + 2 * D);               // [4][D] rotated queries (ROT)
+    uint8_t *ring = zeros + 2 * D + (ROT ? 16 * D : 0);                 // [NW][NST][2 records]
     float *wbuf = reinterpret_cast<float *>(ring);                      // reused after the loop
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -391,6 +416,8 @@ draft_kivi_kernel(KiviParams P)
         }
         // B fragments of q (column n = gid): heads 0..3 scaled by 2^(-b e) for
         // the channel's code exponent, copies 4..7 unscaled (zero-point sums)
+        if constexpr (ROT) rotate_queries<TQ, D>(qg, grp, rq);
+        auto qval = [&](int idx) { return ROT ? rq[idx] : load_q<TQ, D>(qg, idx); };
         uint32_t qf[KS][2];
         {
             const int h = gid & 3;
@@ -401,8 +428,8 @@ draft_kivi_kernel(KiviParams P)
                 for (int rr = 0; rr < 2; ++rr) {
                     const int c = 16 * ks + 2 * tig + 8 * rr;
                     const float f = gid < 4 ? exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * ks + rr))) : 1.f;
-                    const float a = valid ? load_q<TQ, D>(qg, h * D + c) * P.qscale * f : 0.f;
-                    const float bb = valid ? load_q<TQ, D>(qg, h * D + c + 1) * P.qscale * f : 0.f;
+                    const float a = valid ? qval(h * D + c) * P.qscale * f : 0.f;
+                    const float bb = valid ? qval(h * D + c + 1) * P.qscale * f : 0.f;
                     qf[ks][rr] = pack_half2(a, bb);
                 }
         }
@@ -580,12 +607,15 @@ draft_kivi_kernel(KiviParams P)
             fence_mbar_init();
         }
         constexpr int CPL = D / 32;          // channels per lane
+        if constexpr (ROT) rotate_queries<TQ, D>(qg, grp, rq);
         float qv[4][CPL];
 #pragma unroll
         for (int h = 0; h < 4; ++h)
 #pragma unroll
             for (int i = 0; i < CPL; ++i)
-                qv[h][i] = h < grp ? load_q<TQ, D>(qg, h * D + lane * CPL + i) * P.qscale : 0.f;
+                qv[h][i] = h < grp ? (ROT ? rq[h * D + lane * CPL + i] : load_q<TQ, D>(qg, h * D + lane * CPL + i)) *
+                                         P.qscale
+                                   : 0.f;
         float m[4], l[4], o[4][CPL];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -1170,7 +1200,7 @@ DensePlan dense_plan(const vc_cache_view *v)
     return p;
 }
 
-template <int BITS, int D, typename TQ, typename TR>
+template <int BITS, int D, typename TQ, typename TR, bool ROT>
 cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, void *out, void *ws,
                         cudaStream_t st)
 {
@@ -1197,10 +1227,11 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     P.n_split_r = pl.n_split_r;
     P.res_per_split = pl.res_per_split;
     P.qscale = scale * kLog2e;
-    size_t smem = 128 + 4 * D + (size_t)NW * Gm::NST * 2 * Gm::REC;
-    const size_t merge = 128 + 4 * D + (size_t)NW * part_floats(D) * 4;
+    const size_t rot_bytes = ROT ? 16 * D : 0;
+    size_t smem = 128 + 4 * D + rot_bytes + (size_t)NW * Gm::NST * 2 * Gm::REC;
+    const size_t merge = 128 + 4 * D + rot_bytes + (size_t)NW * part_floats(D) * 4;
     if (smem < merge) smem = merge;
-    auto kern = draft_kivi_kernel<BITS, D, TQ, TR>;
+    auto kern = draft_kivi_kernel<BITS, D, TQ, TR, ROT>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(c->B * c->Hkv, pl.n_split_q + pl.n_split_r);
     kern<<<grid, kThreads, smem, st>>>(P);
@@ -1258,8 +1289,11 @@ template <int BITS, int D, typename TQ>
 cudaError_t kivi_by_res(const void *q, const vc_qcache *c, int Hq, float s, void *o, void *ws,
                         cudaStream_t st)
 {
-    return c->res_dtype == VC_BF16 ? launch_kivi<BITS, D, TQ, __nv_bfloat16>(q, c, Hq, s, o, ws, st)
-                                   : launch_kivi<BITS, D, TQ, float>(q, c, Hq, s, o, ws, st);
+    if (c->cfg.rotate)
+        return c->res_dtype == VC_BF16 ? launch_kivi<BITS, D, TQ, __nv_bfloat16, true>(q, c, Hq, s, o, ws, st)
+                                       : launch_kivi<BITS, D, TQ, float, true>(q, c, Hq, s, o, ws, st);
+    return c->res_dtype == VC_BF16 ? launch_kivi<BITS, D, TQ, __nv_bfloat16, false>(q, c, Hq, s, o, ws, st)
+                                   : launch_kivi<BITS, D, TQ, float, false>(q, c, Hq, s, o, ws, st);
 }
 
 template <int D, typename TQ>

@@ -224,7 +224,43 @@ __device__ void quantize_group(RowFn row, uint8_t *__restrict__ rec, uint32_t *i
     for (int i = tid; i < Gm::REC / 16; i += 2 * D) dst[i] = srcv[i];
 }
 
-template <typename T, int BITS, int D>
+// Key rotation (rotated caches, vc_quant_cfg.rotate): each key row x becomes
+// T(W(x) * 2^-ceil(log2(D)/2)), W the binary32 Walsh-Hadamard butterfly
+// network with stages h = 1, 2, ..., D/2 mapping the pair (i, i + h),
+// i mod 2h < h, to (a + b, a - b).  The query side uses 2^-floor(log2(D)/2),
+// so that rotated dot products equal the plain ones (H H^T = D I).
+template <int D>
+struct RotScale {
+    static constexpr int LG = D == 128 ? 7 : 6;
+    static constexpr float K = LG == 7 ? 0.0625f : 0.125f;
+};
+
+// n rows from src(r) to dst(r) (D elements of T each), ROWS at a time through
+// buf, by all threads of the block (block-uniform call).
+template <typename T, int D, int ROWS, typename SrcFn, typename DstFn>
+__device__ void rotate_rows(int n, SrcFn src, DstFn dst, float (*buf)[D])
+{
+    for (int r0 = 0; r0 < n; r0 += ROWS) {
+        const int nr = min(ROWS, n - r0);
+        for (int i = threadIdx.x; i < nr * D; i += blockDim.x) buf[i / D][i % D] = Elem<T>::to_f(src(r0 + i / D)[i % D]);
+        __syncthreads();
+        for (int h = 1; h < D; h <<= 1) {
+            for (int p = threadIdx.x; p < nr * (D / 2); p += blockDim.x) {
+                const int r = p / (D / 2), kk = p % (D / 2);
+                const int i = (kk / h) * 2 * h + (kk % h);
+                const float a = buf[r][i], b = buf[r][i + h];
+                buf[r][i] = a + b;
+                buf[r][i + h] = a - b;
+            }
+            __syncthreads();
+        }
+        for (int i = threadIdx.x; i < nr * D; i += blockDim.x)
+            dst(r0 + i / D)[i % D] = Elem<T>::from_f(buf[i / D][i % D] * RotScale<D>::K);
+        __syncthreads();
+    }
+}
+
+template <typename T, int BITS, int D, bool ROT>
 __global__ void __launch_bounds__(2 * D, 5)
 quantize_prefill_kernel(const T *__restrict__ k, const T *__restrict__ v, int Hkv, int L_stride,
                         int max_groups, uint8_t *__restrict__ records)
@@ -234,13 +270,24 @@ quantize_prefill_kernel(const T *__restrict__ k, const T *__restrict__ v, int Hk
     const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const size_t bh = (size_t)b * Hkv + h;
     const size_t row0 = bh * L_stride + (size_t)g * G;
-    const T *base = threadIdx.x < D ? k : v;
-    auto row = [&](int t) { return base + (row0 + t) * D; };
-    quantize_group<T, BITS, D>(row, records + (bh * max_groups + g) * Gm::REC, img);
+    if constexpr (ROT) {
+        // the group's key rows, rotated, in shared memory
+        __shared__ __align__(16) float buf[G][D];
+        __shared__ __align__(16) T kr[G][D];
+        rotate_rows<T, D, G>(
+            G, [&](int t) { return k + (row0 + t) * D; }, [&](int t) { return &kr[t][0]; }, buf);
+        auto row = [&](int t) -> const T * { return threadIdx.x < D ? &kr[t][0] : v + (row0 + t) * D; };
+        quantize_group<T, BITS, D>(row, records + (bh * max_groups + g) * Gm::REC, img);
+    } else {
+        const T *base = threadIdx.x < D ? k : v;
+        auto row = [&](int t) { return base + (row0 + t) * D; };
+        quantize_group<T, BITS, D>(row, records + (bh * max_groups + g) * Gm::REC, img);
+    }
 }
 
-// Copy positions n_q*G .. L-1 into the ring and publish the lengths.
-template <typename T, int D>
+// Copy positions n_q*G .. L-1 into the ring (keys rotated for a rotated
+// cache) and publish the lengths.
+template <typename T, int D, bool ROT>
 __global__ void residual_copy_kernel(const T *__restrict__ k, const T *__restrict__ v, int B,
                                      int Hkv, int L, int L_stride, int nq_tokens, T *kres,
                                      T *vres, int res_cap, int32_t *n_groups, int32_t *seq_len)
@@ -252,8 +299,14 @@ __global__ void residual_copy_kernel(const T *__restrict__ k, const T *__restric
         const long pos = nq_tokens + t;
         const size_t src = (bh * L_stride + pos) * D + c;
         const size_t dst = (bh * res_cap + pos % res_cap) * D + c;
-        kres[dst] = k[src];
+        if (!ROT) kres[dst] = k[src];
         vres[dst] = v[src];
+    }
+    if constexpr (ROT) {
+        __shared__ __align__(16) float buf[8][D];
+        rotate_rows<T, D, 8>(
+            ntok, [&](int t) { return k + (bh * L_stride + nq_tokens + t) * D; },
+            [&](int t) { return kres + (bh * res_cap + (size_t)((nq_tokens + t) % res_cap)) * D; }, buf);
     }
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < B; i += blockDim.x) {
@@ -269,7 +322,7 @@ __global__ void residual_copy_kernel(const T *__restrict__ k, const T *__restric
 // publishes the new ones.
 // Commit mode (len_base, n_acc non-null): roll back to len_base[b] and take
 // n_acc[b] + 1 rows.  With n_new null every sequence takes max_new rows.
-template <typename T, int BITS, int D>
+template <typename T, int BITS, int D, bool ROT>
 __global__ void __launch_bounds__(2 * D)
 append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
               const int32_t *__restrict__ n_new, const int32_t *__restrict__ len_base,
@@ -307,8 +360,14 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
             const int t = i / D, c = i % D;
             const size_t src = ((bh * max_new) + t) * D + c;
             const size_t dst = (bh * res_cap + (size_t)((len0 + t) % res_cap)) * D + c;
-            kres[dst] = k_new[src];
+            if (!ROT) kres[dst] = k_new[src];
             vres[dst] = v_new[src];
+        }
+        if constexpr (ROT) {
+            __shared__ __align__(16) float buf[8][D];
+            rotate_rows<T, D, 8>(
+                nn, [&](int t) { return k_new + (bh * max_new + t) * D; },
+                [&](int t) { return kres + (bh * res_cap + (size_t)((len0 + t) % res_cap)) * D; }, buf);
         }
         __syncthreads();
         for (int g = ng0; g < ng1; ++g) {
@@ -333,14 +392,19 @@ cudaError_t launch_prefill(const void *k, const void *v, int B, int Hkv, int L, 
 {
     const int R = c->cfg.residual;
     const int nq = (L - R > 0) ? ((L - R) / G) * G : 0;
+    const bool rot = c->cfg.rotate != 0;
     if (nq > 0) {
         dim3 grid(nq / G, Hkv, B);
-        quantize_prefill_kernel<T, BITS, D><<<grid, 2 * D, 0, st>>>(
-            (const T *)k, (const T *)v, Hkv, L_stride, c->max_groups, (uint8_t *)c->records);
+        if (rot)
+            quantize_prefill_kernel<T, BITS, D, true><<<grid, 2 * D, 0, st>>>(
+                (const T *)k, (const T *)v, Hkv, L_stride, c->max_groups, (uint8_t *)c->records);
+        else
+            quantize_prefill_kernel<T, BITS, D, false><<<grid, 2 * D, 0, st>>>(
+                (const T *)k, (const T *)v, Hkv, L_stride, c->max_groups, (uint8_t *)c->records);
     }
-    residual_copy_kernel<T, D><<<B * Hkv, 256, 0, st>>>(
-        (const T *)k, (const T *)v, B, Hkv, L, L_stride, nq, (T *)c->k_res, (T *)c->v_res,
-        c->res_cap, c->n_groups, c->seq_len);
+    auto rc = rot ? residual_copy_kernel<T, D, true> : residual_copy_kernel<T, D, false>;
+    rc<<<B * Hkv, 256, 0, st>>>((const T *)k, (const T *)v, B, Hkv, L, L_stride, nq, (T *)c->k_res,
+                                (T *)c->v_res, c->res_cap, c->n_groups, c->seq_len);
     return cudaGetLastError();
 }
 
@@ -361,7 +425,8 @@ cudaError_t launch_append(const vc_qcache *c, const void *kn, const void *vn, co
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, append_kernel<T, BITS, D>, (const T *)kn, (const T *)vn, n_new, len_base,
+    auto kern = c->cfg.rotate ? append_kernel<T, BITS, D, true> : append_kernel<T, BITS, D, false>;
+    return cudaLaunchKernelEx(&cfg, kern, (const T *)kn, (const T *)vn, n_new, len_base,
                               n_acc, max_new, c->Hkv, (T *)c->k_res, (T *)c->v_res, c->res_cap,
                               c->cfg.residual, requantize, c->max_groups, (uint8_t *)c->records, c->n_groups,
                               c->seq_len, c->status);

@@ -19,6 +19,7 @@ bool qcache_ok(const vc_qcache *c)
     if (!c || !c->records || !c->k_res || !c->v_res || !c->n_groups || !c->seq_len) return false;
     if (c->B <= 0 || c->Hkv <= 0 || (c->d != 64 && c->d != 128)) return false;
     if ((c->cfg.bits != 2 && c->cfg.bits != 4) || c->cfg.group != 32 || c->cfg.residual < 0) return false;
+    if (c->cfg.rotate != 0 && c->cfg.rotate != 1) return false;
     if (c->max_groups < 0 || c->res_cap < c->cfg.residual + c->cfg.group) return false;
     if (!dtype_ok(c->res_dtype)) return false;
     if (!aligned(c->records, 256) || !aligned(c->k_res, 16) || !aligned(c->v_res, 16)) return false;

@@ -59,7 +59,7 @@ class VeriCacheRunner:
 
     def __init__(self, dec: vc.Decoder, B: int, max_len: int, horizon: int, bits: int = 2, group: int = 32,
                  residual: int = 128, host_cache: bool = False, prefill_chunk: int = 512, device="cuda",
-                 fused_head: bool = True):
+                 fused_head: bool = True, rotate: bool = False):
         cfg = dec.cfg
         self.dec, self.B, self.D, self.device = dec, B, horizon, device
         # fused_head: draft steps and the verify pass take the greedy tokens
@@ -77,8 +77,9 @@ class VeriCacheRunner:
             self.v_host = torch.zeros(shape, dtype=self.dtype).pin_memory()
         maxg = self.L_stride // group + 1
         res_cap = ((residual + group + horizon + 1 + 15) // 16) * 16
+        # rotate: draft caches with rotated keys (vc_quant_cfg.rotate)
         self.qc = [vc.QCache(B, hkv, hd, bits, maxg, res_cap, residual, group=group, res_dtype=self.dtype,
-                             device=device) for _ in range(nl)]
+                             device=device, rotate=rotate) for _ in range(nl)]
         self.qc_arr = vc.qcache_array(self.qc)
         self.k_blk = torch.zeros(nl, B, hkv, horizon + 1, hd, dtype=self.dtype, device=device)
         self.v_blk = torch.zeros_like(self.k_blk)

@@ -32,7 +32,7 @@ class VcError(RuntimeError):
 
 
 class QuantCfg(ctypes.Structure):
-    _fields_ = [("bits", c_int32), ("group", c_int32), ("residual", c_int32)]
+    _fields_ = [("bits", c_int32), ("group", c_int32), ("residual", c_int32), ("rotate", c_int32)]
 
 
 class QCacheC(ctypes.Structure):
@@ -226,7 +226,7 @@ class QCache:
     """Caller-owned storage of one layer's KIVI cache (include/vc.h, vc_qcache)."""
 
     def __init__(self, B, Hkv, d, bits, max_groups, res_cap, residual=0, group=32,
-                 res_dtype=torch.bfloat16, device="cuda"):
+                 res_dtype=torch.bfloat16, device="cuda", rotate: bool = False):
         rb = vc_record_bytes(bits, d)
         self.rec_bytes = rb
         self.records = torch.zeros(B * Hkv * max(max_groups, 1) * rb, dtype=torch.uint8, device=device)
@@ -237,8 +237,10 @@ class QCache:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.c = QCacheC(self.records.data_ptr(), self.k_res.data_ptr(), self.v_res.data_ptr(),
                          self.n_groups.data_ptr(), self.seq_len.data_ptr(), self.status.data_ptr(),
-                         B, Hkv, d, QuantCfg(bits, group, residual), max_groups, res_cap, _dt(self.k_res))
+                         B, Hkv, d, QuantCfg(bits, group, residual, int(bool(rotate))), max_groups, res_cap,
+                         _dt(self.k_res))
         self.B, self.Hkv, self.d, self.bits, self.group, self.residual = B, Hkv, d, bits, group, residual
+        self.rotate = bool(rotate)
         self.max_groups, self.res_cap = max_groups, res_cap
 
     def view(self) -> CacheView:

@@ -132,8 +132,9 @@ def test_bf16_block_forward_equals_row_by_row():
     assert torch.isfinite(blk.float()).all()
 
 
-@pytest.mark.parametrize("host_cache,fused_head", [(True, True), (False, True), (False, False)])
-def test_bf16_draft_and_verify_equals_greedy(host_cache, fused_head):
+@pytest.mark.parametrize("host_cache,fused_head,rotate", [(True, True, False), (False, True, False),
+                                                       (False, False, False), (False, True, True)])
+def test_bf16_draft_and_verify_equals_greedy(host_cache, fused_head, rotate):
     vc = lib()
     from lossless_draft_verify_gb300 import decode
     cfg, dec = _small_decoder(vc, seed=1)
@@ -144,7 +145,7 @@ def test_bf16_draft_and_verify_equals_greedy(host_cache, fused_head):
     ref_run.prefill(prompt)
     ref = ref_run.greedy(n_new)
     run = decode.VeriCacheRunner(dec, B, P + n_new + 2 * D, D, bits=2, residual=128, host_cache=host_cache,
-                                 prefill_chunk=256, fused_head=fused_head)
+                                 prefill_chunk=256, fused_head=fused_head, rotate=rotate)
     run.prefill(prompt)
     toks, acc = run.generate(n_new)
     assert toks == ref

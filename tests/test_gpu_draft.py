@@ -13,12 +13,12 @@ from helpers import assert_attn_close, f32, lib
 pytestmark = pytest.mark.gpu
 
 
-def _run_kivi(vc, B, Hq, Hkv, L, d, bits, R, dtype=torch.bfloat16, seed=0, extra_groups=0):
+def _run_kivi(vc, B, Hq, Hkv, L, d, bits, R, dtype=torch.bfloat16, seed=0, extra_groups=0, rotate=False):
     k, v = inputs.kv_with_outliers(B, Hkv, L, d, seed=seed, device="cuda", dtype=dtype)
     q = inputs.normal_bf16((B, Hq, d), seed + 100, device="cuda").to(dtype)
     G = 32
     maxg = max(1, (L - R) // G + extra_groups)
-    cache = vc.QCache(B, Hkv, d, bits, maxg, R + G + 8, R, res_dtype=dtype)
+    cache = vc.QCache(B, Hkv, d, bits, maxg, R + G + 8, R, res_dtype=dtype, rotate=rotate)
     vc.vc_quantize_kv(k, v, cache)
     view = cache.view()
     ws = vc.Workspace(vc.vc_draft_attn_workspace_bytes(view, Hq))
@@ -118,6 +118,21 @@ def test_draft_kivi_mixed_lengths(R):
         qc = oracle.kivi_quantize(f32(k[b:b + 1, :, :L]), f32(v[b:b + 1, :, :L]), bits, G, R)
         want = oracle.kivi_decode_attn(f32(q[b:b + 1]), qc, 0.09)
         assert_attn_close(out[b:b + 1], want, what=f"seq {b} (L={L})")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,d,bits,R,dtype", [
+    (2, 8, 2, 1000, 128, 2, 128, torch.bfloat16),
+    (2, 4, 2, 517, 64, 4, 16, torch.float32),
+    (2, 8, 2, 2000, 128, 2, 600, torch.bfloat16),     # ring over several splits
+])
+def test_draft_kivi_rotated_cache_matches_oracle(B, Hq, Hkv, L, d, bits, R, dtype):
+    """Rotated keys (and queries rotated inside the kernel) against the
+    oracle's rotated cache, read through its rotated queries."""
+    vc = lib()
+    k, v, q, out, scale = _run_kivi(vc, B, Hq, Hkv, L, d, bits, R, dtype, seed=L + 7, rotate=True)
+    qc = oracle.kivi_quantize(f32(k), f32(v), bits, 32, R, rotate=True, rotate_bf16=dtype == torch.bfloat16)
+    want = oracle.kivi_decode_attn(f32(q), qc, scale)
+    assert_attn_close(out, want, what=f"rotated {B}x{Hq}/{Hkv}x{L}x{d} b{bits}")
 
 
 @pytest.mark.parametrize("dtype,d,Hq", [(torch.bfloat16, 128, 8), (torch.bfloat16, 64, 4), (torch.bfloat16, 128, 2),

@@ -13,7 +13,7 @@ from helpers import f32, lib
 pytestmark = pytest.mark.gpu
 
 
-def _check_cache(vc, cache, k, v, L, bits, R, bs=None, hs=None):
+def _check_cache(vc, cache, k, v, L, bits, R, bs=None, hs=None, rotate=False):
     B, H, _, d = k.shape
     G = 32
     nq = ((L - R) // G) * G if L - R > 0 else 0
@@ -21,7 +21,7 @@ def _check_cache(vc, cache, k, v, L, bits, R, bs=None, hs=None):
     hs = list(range(H)) if hs is None else list(hs)
     kq = f32(k[bs][:, hs, :L])
     vq = f32(v[bs][:, hs, :L])
-    ref = oracle.kivi_quantize(kq, vq, bits, G, R)
+    ref = oracle.kivi_quantize(kq, vq, bits, G, R, rotate=rotate, rotate_bf16=k.dtype == torch.bfloat16)
     recs = cache.record_view().cpu().numpy()
     for i, b in enumerate(bs):
         for j, h in enumerate(hs):
@@ -38,41 +38,44 @@ def _check_cache(vc, cache, k, v, L, bits, R, bs=None, hs=None):
     for i, b in enumerate(bs):
         for j, h in enumerate(hs):
             for p in range(nq, L):
-                assert np.array_equal(kr[b, h, p % cache.res_cap], kq[i, j, p])
+                assert np.array_equal(kr[b, h, p % cache.res_cap], ref["kres"][i, j, p - nq])
     assert cache.n_groups.cpu().tolist() == [nq // G] * B
     assert cache.seq_len.cpu().tolist() == [L] * B
 
 
-@pytest.mark.parametrize("bits,d,R,L,dtype", [
-    (2, 128, 128, 300, torch.bfloat16),     # several groups + ragged residual
-    (4, 128, 0, 256, torch.bfloat16),
-    (4, 64, 0, 517, torch.float32),         # tiny-decoder shape, fp32
-    (2, 64, 16, 40, torch.float32),         # one group
-    (2, 128, 128, 100, torch.bfloat16),     # shorter than the window: no group
+@pytest.mark.parametrize("bits,d,R,L,dtype,rotate", [
+    (2, 128, 128, 300, torch.bfloat16, False),     # several groups + ragged residual
+    (4, 128, 0, 256, torch.bfloat16, False),
+    (4, 64, 0, 517, torch.float32, False),         # tiny-decoder shape, fp32
+    (2, 64, 16, 40, torch.float32, False),         # one group
+    (2, 128, 128, 100, torch.bfloat16, False),     # shorter than the window: no group
+    (2, 128, 128, 300, torch.bfloat16, True),      # rotated keys
+    (4, 64, 16, 517, torch.float32, True),
+    (2, 128, 64, 100, torch.bfloat16, True),
 ])
-def test_quantize_matches_oracle(bits, d, R, L, dtype):
+def test_quantize_matches_oracle(bits, d, R, L, dtype, rotate):
     vc = lib()
     B, H = 3, 2
     k, v = inputs.kv_with_outliers(B, H, L + 5, d, seed=11 + bits + d, device="cuda", dtype=dtype)
     G = 32
     maxg = max(1, (L - R) // G + 1)
-    cache = vc.QCache(B, H, d, bits, maxg, R + G + 8, R, res_dtype=dtype)
+    cache = vc.QCache(B, H, d, bits, maxg, R + G + 8, R, res_dtype=dtype, rotate=rotate)
     vc.vc_quantize_kv(k.contiguous(), v.contiguous(), cache, L=L)
     torch.cuda.synchronize()
-    _check_cache(vc, cache, k, v, L, bits, R)
+    _check_cache(vc, cache, k, v, L, bits, R, rotate=rotate)
 
 
-@pytest.mark.parametrize("bits,R", [(2, 128), (4, 0)])
-def test_append_equals_one_shot(bits, R):
+@pytest.mark.parametrize("bits,R,rotate", [(2, 128, False), (4, 0, False), (2, 64, True)])
+def test_append_equals_one_shot(bits, R, rotate):
     """Appending tokens (ragged per sequence) and re-quantizing leaving groups
-    gives the same records as quantizing the whole sequence at once."""
+    gives the same records (and ring) as quantizing the whole sequence at once."""
     vc = lib()
     B, H, d, G = 3, 2, 128, 32
     L0, adds = 200, [[17, 0, 40], [33, 50, 1], [0, 12, 30]]
     total = L0 + max(sum(a[b] for a in adds) for b in range(B))
     k, v = inputs.kv_with_outliers(B, H, total + 1, d, seed=21, device="cuda")
     maxg = total // G + 1
-    cache = vc.QCache(B, H, d, bits, maxg, R + G + 64, R)
+    cache = vc.QCache(B, H, d, bits, maxg, R + G + 64, R, rotate=rotate)
     vc.vc_quantize_kv(k[:, :, :L0].contiguous(), v[:, :, :L0].contiguous(), cache)
     lens = [L0] * B
     for a in adds:
@@ -91,13 +94,17 @@ def test_append_equals_one_shot(bits, R):
         L = lens[b]
         nq = ((L - R) // G) * G if L > R else 0
         assert int(cache.n_groups[b]) == nq // G
-        ref = oracle.kivi_quantize(f32(k[b:b + 1, :, :L]), f32(v[b:b + 1, :, :L]), bits, G, R)
+        ref = oracle.kivi_quantize(f32(k[b:b + 1, :, :L]), f32(v[b:b + 1, :, :L]), bits, G, R, rotate=rotate)
         recs = cache.record_view().cpu().numpy()
+        ring = f32(cache.k_res)
         for h in range(H):
             got = oracle.unpack_records(recs[b, h, :nq // G], bits, d)
             assert np.array_equal(got["kcode"], ref["kcode"][0, h])
+            assert np.array_equal(got["kscale"], ref["kscale"][0, h])
             assert np.array_equal(got["vscale"], ref["vscale"][0, h])
             assert np.array_equal(got["kzero"], ref["kzero"][0, h])
+            for p in range(nq, L):
+                assert np.array_equal(ring[b, h, p % cache.res_cap], ref["kres"][0, h, p - nq])
 
 
 def test_append_without_requantize_then_rollback():
