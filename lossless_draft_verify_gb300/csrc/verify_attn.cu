@@ -46,7 +46,7 @@ constexpr float TC_LAZY = 8.0f;
 // Geometry of a CTA holding MT row tiles of 128 (query, head) rows that share
 // every K/V tile.  MT = 1: 2 CTAs per SM; MT = 2: one CTA per SM, the whole
 // TMEM (per tile: S double buffer 2 x 64 columns + O 128 columns).
-template <int MT>
+template <int MT, bool TAIL = false>
 struct TcGeom {
     static constexpr int STAGES = MT == 1 ? 2 : 3;
     static constexpr int THREADS = 64 + 128 * MT;
@@ -61,11 +61,54 @@ struct TcGeom {
 
 struct TcParams {
     const int32_t *ctx_len;
+    const __nv_bfloat16 *q;      // [B][Dq][Hq][128] (tail rows)
     float *part;
     int32_t *status;
-    int Hkv, Dq, grp, n_mtiles, n_cta_m, n_split, tiles_per_split;
+    int Hkv, Hq, Dq, grp, n_mtiles, n_cta_m, n_split, tiles_per_split;
+    int tail_rows;               // rows of the second row tile done by the tail warp (0: none)
     float scale_log2;
 };
+
+constexpr int kTailMaxRows = 8;
+
+__device__ __forceinline__ void mma_bf16_16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans_b16(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// byte address of 16-byte chunk c (0..15, 8 channels each) of key row `key`
+// in a 64-key K or V tile loaded by TMA with 128-byte swizzle as two halves of
+// 64 channels (the second half TC_N * 128 bytes on)
+__device__ __forceinline__ uint32_t swz_chunk(uint32_t tile, int key, int c)
+{
+    return tile + (uint32_t)((c >> 3) * (TC_N * 128) + key * 128 + (((c & 7) ^ (key & 7)) << 4));
+}
 
 template <int MT, int STAGES>
 struct Bars {
@@ -95,12 +138,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Ba
     return false;
 }
 
-template <int MT>
-__global__ void __launch_bounds__(TcGeom<MT>::THREADS, MT == 1 ? 2 : 1)
+template <int MT, bool TAIL>
+__global__ void __launch_bounds__(TcGeom<MT, TAIL>::THREADS, MT == 1 ? 2 : 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, TcParams P)
 {
-    using Gm = TcGeom<MT>;
+    using Gm = TcGeom<MT, TAIL>;
     using BarsT = Bars<MT, Gm::STAGES>;
     constexpr int STAGES = Gm::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -119,7 +162,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int b = unit / P.Hkv, kvh = unit % P.Hkv;
     const int rows_q = TC_M / P.grp;                  // queries per row tile
     const int q_first = mtc * MT * rows_q;            // first query of the CTA
-    const int q_last = min(P.Dq, q_first + MT * rows_q) - 1;
+    const int q_last = TAIL ? P.Dq - 1 : min(P.Dq, q_first + MT * rows_q) - 1;
     const int ctx = P.ctx_len[b];
     const int n_tiles_all = (ctx + q_last + 1 + TC_N - 1) / TC_N;
     const int t_lo = split * P.tiles_per_split;
@@ -129,14 +172,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int mt = mtc * MT + t;
         return P.part + (((size_t)unit * P.n_mtiles + mt) * P.n_split + split) * TC_M * TC_PART;
     };
+    // tail mode: the rows of the second tile, all in the first kTailMaxRows, by warp 1
+    float *part_tail = P.part + (((size_t)unit * P.n_mtiles + 1) * P.n_split + split) * TC_M * TC_PART;
 
     if (threadIdx.x == 0) {
         mbar_init(&B->q_full, 1);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&B->k_full[s], 1);
-            mbar_init(&B->k_empty[s], 1);
+            mbar_init(&B->k_empty[s], TAIL ? 2 : 1);      // the MMAs' commit (+ the tail warp)
             mbar_init(&B->v_full[s], 1);
-            mbar_init(&B->v_empty[s], 1);
+            mbar_init(&B->v_empty[s], TAIL ? 2 : 1);
         }
         for (int t = 0; t < MT; ++t) {
             for (int s = 0; s < 2; ++s) {
@@ -163,13 +208,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             float *part = part_of(t);
             for (int i = threadIdx.x; i < TC_M * TC_PART; i += Gm::THREADS) part[i] = (i % TC_PART) == 0 ? kNegBig : 0.f;
         }
+        if (TAIL)
+            for (int i = threadIdx.x; i < P.tail_rows * TC_PART; i += Gm::THREADS)
+                part_tail[i] = (i % TC_PART) == 0 ? kNegBig : 0.f;
         return;
     }
     const uint32_t tmem = B->tmem_base;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer --
-        if (lane == 0) {
+    // Roles.  Warp 0 lane 0: TMA producer.  tcgen05 issuer: warp 1 lane 0, or
+    // in tail mode warp 0 lane 1 (a second, independent single-thread loop in
+    // the same warp) so that warp 1 is free for the tail rows.  Warps 2..5
+    // (and 6..9 for a second tile): softmax.
+    const bool producer = warp == 0 && lane == 0;
+    const bool issuer = TAIL ? (warp == 0 && lane == 1) : (warp == 1 && lane == 0);
+    if (warp == 0 || (!TAIL && warp == 1)) {
+        if (producer) {
+            // -------------------------------------------------- TMA producer --
             tc::prefetch_tmap(&tmQ);
             tc::prefetch_tmap(&tmK);
             tc::prefetch_tmap(&tmV);
@@ -197,9 +251,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 if (*reinterpret_cast<volatile int32_t *>(&B->abort_flag)) break;
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer --
-        if (lane == 0) {
+        if (issuer) {
+            // --------------------------------------------------- MMA issuer --
             const uint32_t idS = tc::idesc_bf16(TC_M, TC_N, false, false);
             const uint32_t idO = tc::idesc_bf16(TC_M, TC_D, false, true);
             bool ok = wait_or_abort(&B->q_full, 0, B, P.status, 21);
@@ -249,6 +302,155 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 }
                 if (!ok) break;
                 tc::commit(&B->v_empty[s]);
+            }
+        }
+    } else if (TAIL && warp == 1) {
+        // ------------------------------------------------ tail rows (mma.sync) --
+        // Row r < tail_rows of the second tile (position rows_q + r / grp,
+        // head r % grp) against the same K/V tiles.  Transposed products keep
+        // the tail rows on the narrow side of m16n8k16 bf16 MMAs: S^T = K Q^T
+        // (keys x rows) and O^T += V^T P^T (channels x rows), the K and V
+        // operands read from the swizzled tiles by ldmatrix, P^T formed from
+        // the S^T fragments by movmatrix.  Lane (gid, tig) holds tail rows
+        // 2 tig + e (e = 0, 1).
+        const int gid = lane >> 2, tig = lane & 3;
+        // Q^T fragments (column n = gid: tail row gid)
+        uint32_t qb[TC_D / 16][2];
+        {
+            const bool rv = gid < P.tail_rows;
+            const int qpos = rows_q + gid / P.grp;
+            const __nv_bfloat16 *qr =
+                P.q + (((size_t)b * P.Dq + (rv ? qpos : 0)) * P.Hq + kvh * P.grp + gid % P.grp) * TC_D;
+#pragma unroll
+            for (int ks = 0; ks < TC_D / 16; ++ks) {
+                qb[ks][0] = rv ? *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 2 * tig) : 0u;
+                qb[ks][1] = rv ? *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 8 + 2 * tig) : 0u;
+            }
+        }
+        bool rv[2];
+        int kmax[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int rr = 2 * tig + e;
+            rv[e] = rr < P.tail_rows;
+            kmax[e] = ctx + rows_q + rr / P.grp;
+        }
+        float o[TC_D / 16][4];          // O^T: channels 16 mt + gid (+8) x rows 2 tig + e
+#pragma unroll
+        for (int i = 0; i < TC_D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        float m[2] = {kNegBig, kNegBig}, l[2] = {0.f, 0.f};
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            const int s = j % STAGES;
+            if (!__all_sync(0xffffffffu, wait_or_abort(&B->k_full[s], (j / STAGES) & 1, B, P.status, 41))) {
+                ok = false;
+                break;
+            }
+            const uint32_t sK = smem_u32(sm + Gm::SM_K + s * TC_N * TC_D * 2);
+            float sc[TC_N / 16][4];     // S^T: keys 16 mt + gid (+8) x rows 2 tig + e
+#pragma unroll
+            for (int i = 0; i < TC_N / 16; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < TC_D / 16; ++ks)
+#pragma unroll
+                for (int mt = 0; mt < TC_N / 16; ++mt) {
+                    // A = K rows: matrices (keys 16 mt + 8 (mi & 1) .., channel chunk 2 ks + (mi >> 1))
+                    const int mi = lane >> 3;
+                    const int key = 16 * mt + 8 * (mi & 1) + (lane & 7);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(swz_chunk(sK, key, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                    mma_bf16_16816(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B->k_empty[s]);
+            // causal mask, scale, online softmax per tail row (exp2 domain, lazy rescale)
+            const int key0 = (t_lo + j) * TC_N;
+            float mx[2] = {kNegBig, kNegBig};
+#pragma unroll
+            for (int mt = 0; mt < TC_N / 16; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = i & 1;
+                    const int key = key0 + 16 * mt + gid + 8 * (i >> 1);
+                    const bool vis = rv[e] && key <= kmax[e];
+                    sc[mt][i] = vis ? sc[mt][i] * P.scale_log2 : -INFINITY;
+                    mx[e] = fmaxf(mx[e], sc[mt][i]);
+                }
+            float alpha[2] = {1.f, 1.f};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 4));
+                mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
+                mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+                if (mx[e] > m[e] + TC_LAZY) {
+                    alpha[e] = ex2(m[e] - mx[e]);
+                    m[e] = mx[e];
+                }
+            }
+            if (alpha[0] != 1.f || alpha[1] != 1.f) {
+                l[0] *= alpha[0];
+                l[1] *= alpha[1];
+#pragma unroll
+                for (int i = 0; i < TC_D / 16; ++i) {
+                    o[i][0] *= alpha[0];
+                    o[i][1] *= alpha[1];
+                    o[i][2] *= alpha[0];
+                    o[i][3] *= alpha[1];
+                }
+            }
+            // P^T B fragments: keys 16 kk + 2 tig (+8) of row gid, by transposing
+            // the S^T fragment pairs
+            uint32_t pb[TC_N / 16][2];
+#pragma unroll
+            for (int mt = 0; mt < TC_N / 16; ++mt) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(ex2(sc[mt][0] - m[0]), ex2(sc[mt][1] - m[1]));
+                __nv_bfloat162 hi = __floats2bfloat162_rn(ex2(sc[mt][2] - m[0]), ex2(sc[mt][3] - m[1]));
+                const float2 fl = __bfloat1622float2(lo), fh = __bfloat1622float2(hi);
+                l[0] += fl.x + fh.x;
+                l[1] += fl.y + fh.y;
+                pb[mt][0] = movmatrix_trans_b16(*reinterpret_cast<uint32_t *>(&lo));
+                pb[mt][1] = movmatrix_trans_b16(*reinterpret_cast<uint32_t *>(&hi));
+            }
+            if (!__all_sync(0xffffffffu, wait_or_abort(&B->v_full[s], (j / STAGES) & 1, B, P.status, 42))) {
+                ok = false;
+                break;
+            }
+            const uint32_t sV = smem_u32(sm + Gm::SM_V + s * TC_N * TC_D * 2);
+#pragma unroll
+            for (int kk = 0; kk < TC_N / 16; ++kk)
+#pragma unroll
+                for (int mt = 0; mt < TC_D / 16; ++mt) {
+                    // A = V^T: matrices (channels 16 mt + 8 (mi & 1), keys 16 kk + 8 (mi >> 1)),
+                    // from key rows, transposed
+                    const int mi = lane >> 3;
+                    const int key = 16 * kk + 8 * (mi >> 1) + (lane & 7);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(swz_chunk(sV, key, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                    mma_bf16_16816(o[mt], a0, a1, a2, a3, pb[kk][0], pb[kk][1]);
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B->v_empty[s]);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 4);
+            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 8);
+            l[e] += __shfl_xor_sync(0xffffffffu, l[e], 16);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            if (!rv[e]) continue;
+            float *pr = part_tail + (size_t)(2 * tig + e) * TC_PART;
+            if (gid == 0) {
+                pr[0] = ok ? m[e] : kNegBig;
+                pr[1] = ok ? l[e] : 0.f;
+                pr[2] = 0.f;
+                pr[3] = 0.f;
+            }
+#pragma unroll
+            for (int mt = 0; mt < TC_D / 16; ++mt) {
+                pr[4 + 16 * mt + gid] = ok ? o[mt][e] : 0.f;
+                pr[4 + 16 * mt + gid + 8] = ok ? o[mt][2 + e] : 0.f;
             }
         }
     } else {
@@ -477,7 +679,7 @@ verify_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 
 // ================================================================== host ===
 struct TcPlan {
-    int n_mtiles, mt_per_cta, n_cta_m, n_split, tiles_per_split;
+    int n_mtiles, mt_per_cta, n_cta_m, n_split, tiles_per_split, tail_rows;
 };
 
 // split_tiles > 0 fixes the number of 64-key tiles per split, so that the
@@ -492,6 +694,16 @@ TcPlan tc_plan(int B, int Dq, int Hkv, int grp, int max_ctx, int split_tiles)
     // 1.0 ms against 0.77 ms for two single-tile CTAs per SM at Dq = 33.
     p.mt_per_cta = 1;
     p.n_cta_m = p.n_mtiles / p.mt_per_cta;
+    // A second tile of at most kTailMaxRows rows (Dq = 33 with 4 query heads
+    // per kv head: 4 rows) is done inside the first tile's CTA by a tail warp
+    // on the same K/V tiles, instead of by CTAs that repeat the whole tile's
+    // work.  Not under a fixed split size: callers that need every row's
+    // arithmetic independent of Dq keep all rows on the tcgen05 path.
+    p.tail_rows = 0;
+    if (split_tiles <= 0 && p.n_mtiles == 2 && Dq * grp - TC_M <= kTailMaxRows) {
+        p.tail_rows = Dq * grp - TC_M;
+        p.n_cta_m = 1;
+    }
     const int tiles = (max_ctx + Dq + TC_N - 1) / TC_N;
     const int items = B * Hkv * p.n_cta_m;
     const int slots = device_sm_count() * (p.mt_per_cta == 1 ? 2 : 1);
@@ -549,6 +761,9 @@ cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt
             return cudaErrorInvalidValue;
         TcParams P;
         P.ctx_len = ctx_len;
+        P.q = (const __nv_bfloat16 *)q;
+        P.Hq = Hq;
+        P.tail_rows = pl.tail_rows;
         P.status = (int32_t *)ws;
         P.part = (float *)((uint8_t *)ws + kStatusBytes);
         P.Hkv = Hkv;
@@ -561,11 +776,17 @@ cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt
         P.scale_log2 = sl2;
         dim3 grid(pl.n_split, B * Hkv * pl.n_cta_m);
         if (pl.mt_per_cta == 2) {
-            cudaFuncSetAttribute(verify_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<2>::SMEM);
-            verify_tc_kernel<2><<<grid, TcGeom<2>::THREADS, TcGeom<2>::SMEM, st>>>(mq, mk, mv, P);
+            auto kern = verify_tc_kernel<2, false>;
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<2>::SMEM);
+            kern<<<grid, TcGeom<2>::THREADS, TcGeom<2>::SMEM, st>>>(mq, mk, mv, P);
+        } else if (pl.tail_rows > 0) {
+            auto kern = verify_tc_kernel<1, true>;
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<1, true>::SMEM);
+            kern<<<grid, TcGeom<1, true>::THREADS, TcGeom<1, true>::SMEM, st>>>(mq, mk, mv, P);
         } else {
-            cudaFuncSetAttribute(verify_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<1>::SMEM);
-            verify_tc_kernel<1><<<grid, TcGeom<1>::THREADS, TcGeom<1>::SMEM, st>>>(mq, mk, mv, P);
+            auto kern = verify_tc_kernel<1, false>;
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<1>::SMEM);
+            kern<<<grid, TcGeom<1>::THREADS, TcGeom<1>::SMEM, st>>>(mq, mk, mv, P);
         }
         dim3 cgrid(B * Hkv * pl.n_mtiles, TC_M / 4);
         verify_tc_combine<__nv_bfloat16><<<cgrid, 128, 0, st>>>(P.part, pl.n_split, pl.n_mtiles, Hkv, Hq, Dq,

@@ -30,7 +30,12 @@ def _case(vc, B, Dq, Hq, Hkv, d, ctx, dtype, seed, pad=7):
 @pytest.mark.parametrize("B,Dq,Hq,Hkv,ctx", [
     (2, 5, 8, 2, [300, 123]),        # grp 4, ragged contexts, several key tiles and splits
     (2, 32, 8, 2, [640, 1000]),      # one full 128-row tile
-    (1, 33, 8, 2, [700]),            # 132 rows: two row tiles
+    (1, 33, 8, 2, [700]),            # 132 rows: the 4 rows past the tile go to the tail warp
+    (2, 34, 8, 2, [640, 1000]),      # 136 rows: 8 tail rows (the most the tail warp takes)
+    (2, 33, 8, 2, [0, 513]),         # tail rows with an empty and a ragged context
+    (1, 17, 8, 1, [300]),            # grp 8, 136 rows
+    (1, 65, 4, 2, [200]),            # grp 2, 130 rows
+    (1, 35, 8, 2, [260]),            # 140 rows: too many for the tail warp, two full tiles
     (2, 16, 8, 1, [257, 64]),        # grp 8
     (1, 40, 4, 4, [90]),             # grp 1
     (1, 7, 4, 2, [0]),               # empty context: the block attends to itself
@@ -68,3 +73,23 @@ def test_verify_full_size_sampled():
         b, kh = divmod(u, Hkv)
         heads = slice(kh * 4, kh * 4 + 4)
         assert_attn_close(got[b, :, heads], want[b, :, heads], what=f"unit {u}")
+
+
+def test_verify_full_size_dq33_sampled():
+    """The acceptance semantics' verify block (D = 32 drafts + 1) at full
+    size: 132 rows per kv unit, the tail rows done inside the first tile's
+    CTA; sampled kv units against the oracle."""
+    vc = lib()
+    B, Dq, Hq, Hkv, d, L = 16, 33, 32, 8, 128, 32768
+    q, k, v, out, scale = _case(vc, B, Dq, Hq, Hkv, d, [L] * B, torch.bfloat16, seed=4, pad=0)
+    units = [5, 64, 126]
+    bs = sorted({u // Hkv for u in units})
+    qs, ks, vs = f32(q[bs]), f32(k[bs]), f32(v[bs])
+    sub_units = [bs.index(u // Hkv) * Hkv + u % Hkv for u in units]
+    want = oracle.verify_attn(qs, ks, vs, [L] * len(bs), scale, units=sub_units)
+    got = out[bs]
+    for u in sub_units:
+        b, kh = divmod(u, Hkv)
+        heads = slice(kh * 4, kh * 4 + 4)
+        assert_attn_close(got[b, :, heads], want[b, :, heads], what=f"unit {u}")
+        assert_attn_close(got[b, 32:, heads], want[b, 32:, heads], what=f"unit {u} tail row")
