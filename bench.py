@@ -62,9 +62,9 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("2de3e9740fc01621b9a2aeb2b60d103cdb79d683c1234b880a533bfaf941c54c",
+    "sha256": ("0157fc58651040f974f2e031917d23164e045ff7fb73f06a72004be922d56ce6",
                "607af49c7988512f8f8974c461106d2011be78ddbca72ebbb92fc5182dcc3286"),
-    "bytes": 411.015680e6 + 4.840192e6,
+    "bytes": 411.008512e6 + 4.545792e6,
     "algorithmic_bytes": 409731072,
 }
 
