@@ -574,7 +574,8 @@ def run_model(args, dev, rank, world, barrier, pg):
     W = inputs.decoder_weights_packed(cfg, seed=0, device=dev)
     dec = vc.Decoder.from_packed(cfg, W["embed"], W["lm_head"], W["wqkv"], W["wo"], W["wgu"], W["wd"])
     n_e2e = 0 if args.no_e2e else 3
-    total = args.warmup + args.steps + n_e2e
+    n_tr = 2                                  # eager rounds for the per-operation trace
+    total = args.warmup + n_tr + args.steps + n_e2e
     max_len = P + total * (M_HORIZON + 1) + 64
     run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=args.bits, residual=M_RESIDUAL, host_cache=True,
                                  prefill_chunk=512, device=dev, rotate=args.rotate)
@@ -587,26 +588,32 @@ def run_model(args, dev, rank, world, barrier, pg):
     log = run.new_log(total)
     for r in range(args.warmup):
         run.round(log, r)
+    # per-operation trace (every GEMM and attention call) of n_tr eager rounds
+    ops_per_round = M_HORIZON * (5 * cfg.n_layers + 1) + 5 * cfg.n_layers + 1 + 2 * cfg.n_layers
+    trace = vc.DecoderTrace(dec, ops_per_round * n_tr)
+    trace.start()
+    for r in range(n_tr):
+        run.round(log, args.warmup + r)
+    ops = trace.stop()
+    # the timed rounds replay the draft steps as one CUDA graph
+    if not args.no_graph:
+        run.capture_draft_graph()
+    base0 = args.warmup + n_tr
     barrier()
     evs = [run.new_events() for _ in range(args.steps)]
-    # per-operation trace of the timed rounds: every GEMM and attention call
-    ops_per_round = M_HORIZON * (5 * cfg.n_layers + 1) + 5 * cfg.n_layers + 1 + 2 * cfg.n_layers
-    trace = vc.DecoderTrace(dec, ops_per_round * args.steps)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
-    trace.start()
     t0.record()
     for i in range(args.steps):
-        run.round(log, args.warmup + i, evs[i])
+        run.round(log, base0 + i, evs[i])
     t1.record()
     barrier()
     clk = clocks.stop()
-    ops = trace.stop()
     ms = t0.elapsed_time(t1)
-    n_acc = log.n_acc[args.warmup:args.warmup + args.steps].cpu()
+    n_acc = log.n_acc[base0:base0 + args.steps].cpu()
     tokens = int((n_acc.long() + 1).sum())
     value, ms_max = replicas.whole_job_rate(tokens, ms, pg, device=dev)
     st = vc.vc_poll_status(run.ws)
@@ -620,7 +627,7 @@ def run_model(args, dev, rank, world, barrier, pg):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        base = args.warmup + args.steps
+        base = base0 + args.steps
         for i in range(n_e2e):
             run.round(log, base + i)
             h_out[:M_B * M_HORIZON].copy_(run.drafts.view(-1), non_blocking=True)
@@ -662,13 +669,15 @@ def run_model(args, dev, rank, world, barrier, pg):
         a = by_kind.setdefault(k, [0, 0.0])
         a[0] += 1
         a[1] += t
-    ctx_mean = P + (args.warmup + args.steps / 2) * (float(n_acc.float().mean()) + 1)
+    ctx_mean = P + (args.warmup + n_tr / 2) * (float(n_acc.float().mean()) + 1)
     rec_b = vc.vc_record_bytes(args.bits, cfg.head_dim)
     draft_attn_bytes = M_B * cfg.n_kv_heads * (int((ctx_mean - M_RESIDUAL) // 32) * rec_b +
                                                2 * (M_RESIDUAL + 16) * cfg.head_dim * 2)
     kernels = {}
     for k, (n, t) in by_kind.items():
-        ent = {"launches": n, "ms_total": t, "ms_per_launch": t / n, "share_of_time": t / ms}
+        # per round of the eager trace rounds, against a timed round
+        ent = {"launches": n, "ms_total": t, "ms_per_launch": t / n,
+               "share_of_time": (t / n_tr) / (ms / args.steps)}
         if k in wb:
             ent["GB/s"] = wb[k] / (t / n / 1e3) / 1e9
             ent["hbm_frac"] = ent["GB/s"] / hbm
@@ -713,22 +722,29 @@ def run_model(args, dev, rank, world, barrier, pg):
 
 
 def model_launches_per_round(cfg, vc) -> int:
-    """Kernels the library launches in one round of the model workload
-    (counted from the decoder's sequencing: a GEMM adds its split-K reduction
-    when it has more than one split)."""
+    """Kernels the library launches in one round of the model workload,
+    counted from the decoder's sequencing.  A GEMM with more than one K split
+    adds a reduction launch when its grid has more than 64 output tiles (fewer
+    tiles, or the LM head's argmax epilogue, sum the splits inside the GEMM)."""
     qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
     shapes = [(qd + 2 * kvd, cfg.d_model), (cfg.d_model, qd), (2 * cfg.d_ff, cfg.d_model), (cfg.d_model, cfg.d_ff)]
 
-    def g(N, K, decode):
-        return 1 + int(vc.vc_gemm_splits(torch.bfloat16, N, K, decode) > 1)
+    def g(M, N, K, decode, argmax=False):
+        tiles = -(-M // 128) * (N // 128)
+        split = vc.vc_gemm_splits(torch.bfloat16, N, K, decode) > 1
+        return 1 + int(split and tiles > 64 and not argmax)
 
-    def layer(decode, attn_kernels):
+    def layer(M, decode, attn_kernels):
         # rmsnorm, qkv, rope, attention, o, rmsnorm, gate_up, silu, down
-        return 2 + 1 + sum(g(N, K, decode) for N, K in shapes) + 1 + attn_kernels
+        return 2 + 1 + sum(g(M, N, K, decode) for N, K in shapes) + 1 + attn_kernels
 
-    draft = 1 + cfg.n_layers * (layer(True, 1) + 1) + 1 + g(cfg.vocab, cfg.d_model, True) + 1 + 1 + 1
-    verify = 1 + cfg.n_layers * layer(False, 2) + 1 + g(cfg.vocab, cfg.d_model, False) + 1
-    return M_HORIZON * draft + verify + 1 + cfg.n_layers + 1
+    rows_v = M_B * (M_HORIZON + 1)
+    # embed, layers (+ append), rmsnorm, LM head (argmax), acceptance, scatter, status fold
+    draft = 1 + cfg.n_layers * (layer(M_B, True, 1) + 1) + 1 + g(M_B, cfg.vocab, cfg.d_model, True, True) + 3
+    # embed, layers (verify attention + its combine), rmsnorm, LM head (argmax), acceptance, status fold
+    verify = 1 + cfg.n_layers * layer(rows_v, False, 2) + 1 + g(rows_v, cfg.vocab, cfg.d_model, False, True) + 2
+    # + the commit (one append per layer) and the host write-back
+    return M_HORIZON * draft + verify + cfg.n_layers + 1
 
 
 def run_bytes(cfg, max_len) -> int:
@@ -878,6 +894,8 @@ def main():
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4], help="draft cache bits (--workload model)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="--workload model: launch the draft steps one by one instead of replaying a CUDA graph")
     ap.add_argument("--rotate", action="store_true",
                     help="draft caches with rotated keys (--workload model; the RotateKV-style variant)")
     ap.add_argument("--sweep", default=None, choices=["horizon", "link", "budget"],

@@ -59,9 +59,16 @@ class VeriCacheRunner:
 
     def __init__(self, dec: vc.Decoder, B: int, max_len: int, horizon: int, bits: int = 2, group: int = 32,
                  residual: int = 128, host_cache: bool = False, prefill_chunk: int = 512, device="cuda",
-                 fused_head: bool = True, rotate: bool = False):
+                 fused_head: bool = True, rotate: bool = False, use_graph: bool = False):
         cfg = dec.cfg
         self.dec, self.B, self.D, self.device = dec, B, horizon, device
+        # use_graph: after one eager round, the round's D draft steps (about a
+        # hundred short launches each) are captured once as a CUDA graph and
+        # replayed every round; every buffer they touch is fixed, so the graph
+        # stays valid for the runner's lifetime
+        self.use_graph = use_graph
+        self._graph = None
+        self._rounds = 0
         # fused_head: draft steps and the verify pass take the greedy tokens
         # from the LM head's argmax epilogue (no logits written)
         self.fused_head = fused_head
@@ -155,14 +162,14 @@ class VeriCacheRunner:
             vc.vc_swap_in(self.v_full, self.v_host, stream=self.side, done_event=self.ev_swap)
             if ev is not None:
                 ev["swap1"].record(self.side)
+        if self.use_graph and self._graph is None and self._rounds >= 1:
+            self.capture_draft_graph()
         if ev is not None:
             ev["d0"].record(main)
-        tok = self.x
-        logits_d = None if self.fused_head else self.logits_d
-        for j in range(D):
-            vc.vc_decoder_draft_step(self.dec, tok, self.qc_arr, logits_d, self.next_d, self.ws,
-                                     drafts_out=self.drafts[:, j], drafts_stride=D)
-            tok = self.next_d
+        if self._graph is not None:
+            self._graph.replay()
+        else:
+            self._draft_steps()
         if ev is not None:
             ev["d1"].record(main)
         if self.host_cache:
@@ -193,6 +200,24 @@ class VeriCacheRunner:
             log.n_acc[r].copy_(self.n_acc)
             log.nxt[r].copy_(self.x)
         self.ctx_bound += D + 1
+        self._rounds += 1
+
+    def _draft_steps(self):
+        """The round's D greedy draft steps on the compressed caches."""
+        tok = self.x
+        logits_d = None if self.fused_head else self.logits_d
+        for j in range(self.D):
+            vc.vc_decoder_draft_step(self.dec, tok, self.qc_arr, logits_d, self.next_d, self.ws,
+                                     drafts_out=self.drafts[:, j], drafts_stride=self.D)
+            tok = self.next_d
+
+    def capture_draft_graph(self):
+        """Record the D draft steps as one CUDA graph (nothing runs while it
+        is recorded); round() replays it from then on."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            self._draft_steps()
+        self._graph = g
 
     @staticmethod
     def new_events() -> dict:
