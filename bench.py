@@ -693,8 +693,9 @@ def run_model(args, dev, rank, world, barrier, pg):
     dom = max(by_kind, key=lambda k: by_kind[k][1])
     roof = {"bound": "hbm", "achieved": g_bytes / (g_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
             "frac": g_bytes / (g_ms / 1e3) / 1e9 / hbm, "traffic": None,
-            "kernel": "gemm_tc_kernel (split-K partials summed in the GEMM up to 64 tiles, else by a reduce kernel): the decoder's projections, weight-streaming at M = 8 "
-                      "(draft) and 264 (verify)", "peak_source": f"{peak_src} hbm_gbs",
+            "kernel": "gemm_tc_kernel (split-K partials summed in the GEMM up to 64 tiles, else by a reduce "
+                      "kernel): the decoder's projections, weight-streaming at M = 8 (draft) and 264 (verify)",
+            "peak_source": f"{peak_src} hbm_gbs",
             "dominant_by_time": dom}
     if rank == 0:
         line = {
