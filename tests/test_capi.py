@@ -100,3 +100,31 @@ def test_decoder_validation_on_the_host(libvc):
                                 None) == vc.VC_ERR_INVALID
     assert L.vc_gemm(None, None, None, None, 0, 1, 1, 1, None, 0, None) == vc.VC_ERR_INVALID
     assert L.vc_kv_writeback(None, None, 0, 1, 1, 1, 1, 64, None, None, None, None, 8, None) == vc.VC_ERR_INVALID
+
+
+def test_greedy_head_and_rotation_validation_on_the_host(libvc):
+    """The argmax-epilogue GEMM, acceptance from tile maxima, the fused verify
+    call and the rotated-cache flag reject bad arguments before any CUDA call."""
+    import ctypes
+    from lossless_draft_verify_gb300 import vc
+    L = vc.load()
+    fake = 1 << 20                      # aligned, never dereferenced on these paths
+    # argmax epilogue: null pointers; shapes or types without a tensor-core head
+    assert L.vc_gemm_argmax(None, fake, vc.VC_BF16, 8, 256, 64, 0, fake, fake, None, 0, None) == vc.VC_ERR_INVALID
+    assert L.vc_gemm_argmax(fake, fake, vc.VC_F32, 8, 256, 64, 0, fake, fake, None, 0,
+                            None) == vc.VC_ERR_UNSUPPORTED
+    assert L.vc_gemm_argmax(fake, fake, vc.VC_BF16, 8, 200, 64, 0, fake, fake, None, 0,
+                            None) == vc.VC_ERR_UNSUPPORTED              # N not a multiple of 128
+    assert L.vc_gemm_argmax(fake, fake, vc.VC_BF16, 8, 256, 40, 0, fake, fake, None, 0,
+                            None) == vc.VC_ERR_UNSUPPORTED              # K not a multiple of 64
+    # acceptance from tile maxima
+    assert L.vc_accept_tiles(None, fake, 4, fake, 2, 3, fake, fake, None) == vc.VC_ERR_INVALID
+    assert L.vc_accept_tiles(fake, fake, 0, fake, 2, 3, fake, fake, None) == vc.VC_ERR_INVALID
+    assert L.vc_accept_tiles(fake, fake, 4, None, 2, 3, fake, fake, None) == vc.VC_ERR_INVALID   # D > 0 needs drafts
+    assert L.vc_accept_tiles(fake, fake, 4, fake, 2, 1025, fake, fake, None) == vc.VC_ERR_INVALID
+    # fused verify: no decoder
+    assert L.vc_decoder_verify(None, fake, fake, 4, 2, fake, 0, fake, fake, 8, None, None, fake, fake, fake, 1 << 20,
+                               None) == vc.VC_ERR_INVALID
+    # the rotated-cache flag takes 0 or 1
+    q = vc.QCacheC(fake, fake, fake, fake, fake, fake, 1, 1, 128, vc.QuantCfg(2, 32, 0, 2), 4, 64, vc.VC_BF16)
+    assert L.vc_quantize_kv(fake, fake, vc.VC_BF16, 1, 1, 32, 32, 128, ctypes.byref(q), None) == vc.VC_ERR_INVALID
