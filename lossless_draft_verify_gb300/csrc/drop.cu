@@ -286,19 +286,38 @@ write_kernel(const float *__restrict__ scores, const T *__restrict__ k, const T 
         }
     }
     __syncthreads();
-    // row copy: 16-byte vectors, a warp moves whole rows
+    // row copy: 16-byte vectors, a warp moves whole rows; each thread has
+    // kUnroll K and kUnroll V loads in flight before it stores them
+    constexpr int kUnroll = 4;
     const int vec_per_row = d * (int)sizeof(T) / 16;
+    const int vshift = __ffs(vec_per_row) - 1;
+    const bool pow2 = (vec_per_row & (vec_per_row - 1)) == 0;
     const int nvec = nkept * vec_per_row;
-    const uint4 *ks = reinterpret_cast<const uint4 *>(k + (size_t)u * L * d);
-    const uint4 *vs = reinterpret_cast<const uint4 *>(v + (size_t)u * L * d);
-    uint4 *kd = reinterpret_cast<uint4 *>(ko + (size_t)u * n_keep * d);
-    uint4 *vd = reinterpret_cast<uint4 *>(vo + (size_t)u * n_keep * d);
-    for (int i = threadIdx.x; i < nvec; i += kThreads) {
-        const int r = i / vec_per_row, e = i % vec_per_row;
-        const size_t src = (size_t)srcpos[r] * vec_per_row + e;
-        const size_t dst = (size_t)dstslot[r] * vec_per_row + e;
-        kd[dst] = ldg_stream(ks + src);
-        vd[dst] = ldg_stream(vs + src);
+    const uint4 *__restrict__ ks = reinterpret_cast<const uint4 *>(k + (size_t)u * L * d);
+    const uint4 *__restrict__ vs = reinterpret_cast<const uint4 *>(v + (size_t)u * L * d);
+    uint4 *__restrict__ kd = reinterpret_cast<uint4 *>(ko + (size_t)u * n_keep * d);
+    uint4 *__restrict__ vd = reinterpret_cast<uint4 *>(vo + (size_t)u * n_keep * d);
+    for (int i0 = threadIdx.x; i0 < nvec; i0 += kUnroll * kThreads) {
+        uint4 bk[kUnroll], bv[kUnroll];
+        size_t dst[kUnroll];
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j) {
+            const int i = i0 + j * kThreads;
+            if (i < nvec) {
+                const int r = pow2 ? i >> vshift : i / vec_per_row;
+                const int e = i - r * vec_per_row;
+                const size_t src = (size_t)srcpos[r] * vec_per_row + e;
+                dst[j] = (size_t)dstslot[r] * vec_per_row + e;
+                bk[j] = ldg_stream(ks + src);
+                bv[j] = ldg_stream(vs + src);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j)
+            if (i0 + j * kThreads < nvec) {
+                kd[dst[j]] = bk[j];
+                vd[dst[j]] = bv[j];
+            }
     }
 }
 
