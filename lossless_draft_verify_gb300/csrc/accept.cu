@@ -206,6 +206,8 @@ accept_tiles_kernel(const float *__restrict__ tmax, const int32_t *__restrict__ 
                     const int32_t *__restrict__ drafts, int D, int32_t *__restrict__ n_acc,
                     int32_t *__restrict__ next_tok)
 {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int amax[1024 + 1];
@@ -235,8 +237,8 @@ accept_tiles_kernel(const float *__restrict__ tmax, const int32_t *__restrict__ 
 cudaError_t accept_tiles(const float *tile_max, const int32_t *tile_idx, int n_tiles, const int32_t *drafts,
                          int B, int D, int32_t *n_acc, int32_t *next_tok, cudaStream_t st)
 {
-    accept_tiles_kernel<<<B, kThreads, 0, st>>>(tile_max, tile_idx, n_tiles, drafts, D, n_acc, next_tok);
-    return cudaGetLastError();
+    return launch_pdl(accept_tiles_kernel, dim3(B), dim3(kThreads), 0, st, tile_max, tile_idx, n_tiles, drafts, D,
+                      n_acc, next_tok);
 }
 
 size_t accept_ws_bytes(int B, int D, int V)

@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(kRowThreads)
 embed_kernel(const int32_t *__restrict__ first_tok, const int32_t *__restrict__ toks, int tok_stride,
              int rows_per_seq, const T *__restrict__ E, int vocab, int D, T *__restrict__ x, int32_t *status)
 {
+    pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x;
     const int b = m / rows_per_seq, i = m % rows_per_seq;
     int t;
@@ -75,6 +77,8 @@ template <typename T>
 __global__ void __launch_bounds__(kRowThreads)
 rmsnorm_kernel(const T *__restrict__ x, int D, int in_step, int in_off, float eps, T *__restrict__ y)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float wsum[kRowThreads / 32];
     const int r = blockIdx.x;
     const T *xr = x + ((size_t)r * in_step + in_off) * D;
@@ -120,6 +124,8 @@ __global__ void __launch_bounds__(kRopeHeads * 64)
 rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd, const int32_t *__restrict__ pos_base,
             RopeFreq fr, T *__restrict__ q_out, RopeDst dst, int32_t *status)
 {
+    pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.x;
     const int b = m / rows_per_seq, i = m % rows_per_seq;
     const int pos = pos_base[b] + i;
@@ -178,6 +184,8 @@ rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd
 template <typename T>
 __global__ void silu_mul_kernel(const T *__restrict__ gu, int M, int F, T *__restrict__ act)
 {
+    pdl_wait();
+    pdl_trigger();
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)M * F) return;
     const size_t m = idx / F, j = idx % F;
@@ -188,6 +196,8 @@ __global__ void silu_mul_kernel(const T *__restrict__ gu, int M, int F, T *__res
 
 __global__ void scatter_tokens_kernel(const int32_t *__restrict__ src, int B, int32_t *dst, int stride)
 {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B) dst[(size_t)b * stride] = src[b];
 }
@@ -195,6 +205,8 @@ __global__ void scatter_tokens_kernel(const int32_t *__restrict__ src, int B, in
 // OR the status words of the sub-workspaces into the decoder's, clear them.
 __global__ void fold_status_kernel(int32_t *main, int32_t *a, int32_t *b, int32_t *c)
 {
+    pdl_wait();
+    pdl_trigger();
     int32_t v = 0;
     if (a) { v |= *a; *a = 0; }
     if (b) { v |= *b; *b = 0; }
@@ -321,9 +333,8 @@ cudaError_t traced(const Ctx &C, int kind, F &&op)
 template <typename T>
 cudaError_t rmsnorm(const Ctx &C, const void *x, int rows, int in_step, int in_off, void *y)
 {
-    rmsnorm_kernel<T><<<rows, kRowThreads, 0, C.st>>>((const T *)x, C.d->c.d_model, in_step, in_off,
-                                                      C.d->c.norm_eps, (T *)y);
-    return cudaGetLastError();
+    return launch_pdl(rmsnorm_kernel<T>, dim3(rows), dim3(kRowThreads), 0, C.st, (const T *)x, C.d->c.d_model,
+                      in_step, in_off, C.d->c.norm_eps, (T *)y);
 }
 
 // The MLP and attention-output half of a layer, shared by both passes:
@@ -344,9 +355,8 @@ cudaError_t layer_tail(const Ctx &C, int l, int M)
                     C.counters(), C.status(), C.st, C.plan);
     }));
     const size_t n = (size_t)M * c.d_ff;
-    silu_mul_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, C.st>>>(C.at<const T>(C.L.gu), M, c.d_ff,
-                                                                     C.at<T>(C.L.act));
-    VC_TRY(cudaGetLastError());
+    VC_TRY(launch_pdl(silu_mul_kernel<T>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, C.st,
+                      C.at<const T>(C.L.gu), M, c.d_ff, C.at<T>(C.L.act)));
     return traced(C, VC_TRACE_GEMM_DOWN, [&] {
         return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.counters(),
                     C.status(), C.st, C.plan);
@@ -391,6 +401,8 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
     const float scale = 1.0f / sqrtf((float)hd);
     // the attention's status block sits where other calls keep activations
     VC_TRY(cudaMemsetAsync(C.at(C.L.vws), 0, kStatusBytes, C.st));
+    // a plain launch after the memset; the kernels after it start early
+    // (programmatic dependent launch) and wait for their inputs on the device
     embed_kernel<T><<<M, kRowThreads, 0, C.st>>>(first_tok, toks, tok_stride, Dq, (const T *)C.d->embed, c.vocab,
                                                  c.d_model, (T *)x, C.status());
     VC_TRY(cudaGetLastError());
@@ -410,9 +422,9 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
         dst.v2 = vb ? (void *)((T *)vb + l * layer_blk) : nullptr;
         dst.bstride2 = (size_t)c.n_kv_heads * Dq * hd;
         dst.stride2 = Dq;
-        rope_kernel<T><<<dim3(M, rope_blocks(c)), kRopeHeads * 64, 0, C.st>>>(
-            C.at<const T>(C.L.qkv), Dq, c.n_heads, c.n_kv_heads, hd, ctx, C.d->rope, C.at<T>(C.L.q), dst, C.status());
-        VC_TRY(cudaGetLastError());
+        VC_TRY(launch_pdl(rope_kernel<T>, dim3(M, rope_blocks(c)), dim3(kRopeHeads * 64), 0, C.st,
+                          C.at<const T>(C.L.qkv), Dq, c.n_heads, c.n_kv_heads, hd, ctx, C.d->rope, C.at<T>(C.L.q),
+                          dst, C.status()));
         VC_TRY(traced(C, VC_TRACE_VERIFY_ATTN, [&] {
             return verify_attn(C.at(C.L.q), dst.k1, dst.v1, c.dt, ctx, B, Dq, c.n_heads, c.n_kv_heads, hd, L_stride,
                                max_ctx, scale, C.at(C.L.att), C.at(C.L.vws), C.st, kSplitTiles);
@@ -437,8 +449,8 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
                         C.status(), C.st, C.plan);
         }));
     }
-    fold_status_kernel<<<1, 1, 0, C.st>>>(C.status(), C.at<int32_t>(C.L.vws), nullptr, nullptr);
-    return cudaGetLastError();
+    return launch_pdl(fold_status_kernel, dim3(1), dim3(1), 0, C.st, C.status(), C.at<int32_t>(C.L.vws),
+                      (int32_t *)nullptr, (int32_t *)nullptr);
 }
 
 template <typename T>
@@ -473,10 +485,9 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         dst.k2 = dst.v2 = nullptr;
         dst.bstride2 = 0;
         dst.stride2 = 1;
-        rope_kernel<T><<<dim3(M, rope_blocks(c)), kRopeHeads * 64, 0, C.st>>>(
-            C.at<const T>(C.L.qkv), 1, c.n_heads, c.n_kv_heads, hd, caches[l].seq_len, C.d->rope, C.at<T>(C.L.q), dst,
-            C.status());
-        VC_TRY(cudaGetLastError());
+        VC_TRY(launch_pdl(rope_kernel<T>, dim3(M, rope_blocks(c)), dim3(kRopeHeads * 64), 0, C.st,
+                          C.at<const T>(C.L.qkv), 1, c.n_heads, c.n_kv_heads, hd, (const int32_t *)caches[l].seq_len,
+                          C.d->rope, C.at<T>(C.L.q), dst, C.status()));
         VC_TRY(qcache_append(&caches[l], kn, vn, nullptr, nullptr, nullptr, 1, 0, C.st));
         vc_cache_view view{};
         view.kind = VC_CACHE_KIVI;
@@ -498,11 +509,11 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         VC_TRY(greedy_head(C, h, B, 0, nullptr, C.at<int32_t>(C.L.nacc), next_tok));
     }
     if (drafts_out) {
-        scatter_tokens_kernel<<<(B + 127) / 128, 128, 0, C.st>>>(next_tok, B, drafts_out, drafts_stride);
-        VC_TRY(cudaGetLastError());
+        VC_TRY(launch_pdl(scatter_tokens_kernel, dim3((B + 127) / 128), dim3(128), 0, C.st, (const int32_t *)next_tok,
+                          B, drafts_out, drafts_stride));
     }
-    fold_status_kernel<<<1, 1, 0, C.st>>>(C.status(), C.at<int32_t>(C.L.dws), nullptr, nullptr);
-    return cudaGetLastError();
+    return launch_pdl(fold_status_kernel, dim3(1), dim3(1), 0, C.st, C.status(), C.at<int32_t>(C.L.dws),
+                      (int32_t *)nullptr, (int32_t *)nullptr);
 }
 
 vc_status to_status(cudaError_t e)

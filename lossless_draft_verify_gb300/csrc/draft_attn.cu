@@ -366,6 +366,8 @@ template <int BITS, int D, typename TQ, typename TR, bool ROT>
 __global__ void __launch_bounds__(kThreads, 4)
 draft_kivi_kernel(KiviParams P)
 {
+    pdl_wait();
+    pdl_trigger();
     using Gm = KiviGeom<BITS, D>;
     constexpr int KS = Gm::KS, NG = Gm::NG, REC = Gm::REC, NST = Gm::NST;
     constexpr int STAGE = 2 * REC;
@@ -718,6 +720,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 draft_dense_kernel(DenseParams P)
 {
+    pdl_wait();
+    pdl_trigger();
     constexpr int TILE = G * D * sizeof(T);
     constexpr int CPL = D / 32;
     constexpr int PER = 16 / sizeof(T);
@@ -907,6 +911,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads)
 draft_dense_mma_kernel(DenseParams P)
 {
+    pdl_wait();
+    pdl_trigger();
     using Gm = DmGeom<D>;
     constexpr int KS = D / 16;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1234,8 +1240,7 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     auto kern = draft_kivi_kernel<BITS, D, TQ, TR, ROT>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(c->B * c->Hkv, pl.n_split_q + pl.n_split_r);
-    kern<<<grid, kThreads, smem, st>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), smem, st, P);
 }
 
 template <typename T, int D>
@@ -1270,8 +1275,7 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
         auto kern = draft_dense_mma_kernel<D>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         dim3 grid(pl.n_split, v->B * v->Hkv);
-        kern<<<grid, kThreads, smem, st>>>(P);
-        return cudaGetLastError();
+        return launch_pdl(kern, grid, dim3(kThreads), smem, st, P);
     }
     constexpr int PER = 16 / sizeof(T);
     const size_t qbytes = (size_t)(D / PER) * (4 * PER + 4) * 4;
@@ -1281,8 +1285,7 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
     auto kern = draft_dense_kernel<T, D>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(pl.n_split, v->B * v->Hkv);
-    kern<<<grid, kThreads, smem, st>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), smem, st, P);
 }
 
 template <int BITS, int D, typename TQ>

@@ -94,6 +94,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
     if (smem_u32(sm) & 1023u) {
+        pdl_wait();
         if (threadIdx.x == 0) report_timeout(A.status, 98);
         return;
     }
@@ -125,21 +126,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     tc::fence_after();
     const uint32_t tmem = B->tmem_base;
 
+    // The weights are never written while the decoder runs: the first stages
+    // of W are requested before the wait for the previous kernel, so their
+    // loads overlap its tail.  x, the residual and the outputs come after it.
+    const int pre = min(n, GSTAGES);
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tmX);
+        tc::prefetch_tmap(&tmW);
+        for (int i = 0; i < pre; ++i) {
+            uint8_t *sw = sm + Gg::OFF_W + i * Gg::WB;
+            const int k = (kb0 + i) * GK;
+            mbar_arrive_expect_tx(&B->full[i], Gg::XB + Gg::WB);
+            tc::tma_load_3d(sw, &tmW, n0, k, 0, &B->full[i]);
+            tc::tma_load_3d(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[i]);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+
     if (warp == 0) {
         if (lane == 0) {
-            tc::prefetch_tmap(&tmX);
-            tc::prefetch_tmap(&tmW);
             for (int i = 0; i < n; ++i) {
                 const int s = i % GSTAGES;
-                if (i >= GSTAGES && !g_wait(&B->empty[s], ((i / GSTAGES) - 1) & 1, B, A.status, 41)) break;
-                if (*reinterpret_cast<volatile int32_t *>(&B->abort_flag)) break;
-                uint8_t *sx = sm + s * Gg::XB;
-                uint8_t *sw = sm + Gg::OFF_W + s * Gg::WB;
                 const int k = (kb0 + i) * GK;
-                mbar_arrive_expect_tx(&B->full[s], Gg::XB + Gg::WB);
-                tc::tma_load_3d(sx, &tmX, k, m0, 0, &B->full[s]);
-                tc::tma_load_3d(sw, &tmW, n0, k, 0, &B->full[s]);
-                tc::tma_load_3d(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[s]);
+                if (i >= pre) {
+                    if (!g_wait(&B->empty[s], ((i / GSTAGES) - 1) & 1, B, A.status, 41)) break;
+                    if (*reinterpret_cast<volatile int32_t *>(&B->abort_flag)) break;
+                    uint8_t *sw = sm + Gg::OFF_W + s * Gg::WB;
+                    mbar_arrive_expect_tx(&B->full[s], Gg::XB + Gg::WB);
+                    tc::tma_load_3d(sw, &tmW, n0, k, 0, &B->full[s]);
+                    tc::tma_load_3d(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[s]);
+                }
+                tc::tma_load_3d(sm + s * Gg::XB, &tmX, k, m0, 0, &B->full[s]);
             }
         }
     } else if (warp == 1) {
@@ -331,6 +349,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 __global__ void gemm_splitk_reduce(const float *__restrict__ part, int S, int M, int N,
                                    const __nv_bfloat16 *resid, __nv_bfloat16 *out)
 {
+    pdl_wait();
+    pdl_trigger();
     const size_t i4 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const size_t total = (size_t)M * N;
     const size_t i = i4 * 4;
@@ -468,20 +488,23 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         A.N = N;
         A.K = K;
         dim3 grid((M + GM - 1) / GM, N / GN, A.S);
+        cudaError_t e;
         if (small) {
             using Gg = GemmGeom<16, 6>;
             cudaFuncSetAttribute(gemm_tc_kernel<16, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gg::SMEM);
-            gemm_tc_kernel<16, 6><<<grid, G_THREADS, Gg::SMEM, st>>>(mx, mw, A);
+            e = launch_pdl(gemm_tc_kernel<16, 6>, grid, dim3(G_THREADS), Gg::SMEM, st, mx, mw, A);
         } else {
             using Gg = GemmGeom<128, 3>;
             cudaFuncSetAttribute(gemm_tc_kernel<128, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gg::SMEM);
-            gemm_tc_kernel<128, 3><<<grid, G_THREADS, Gg::SMEM, st>>>(mx, mw, A);
+            e = launch_pdl(gemm_tc_kernel<128, 3>, grid, dim3(G_THREADS), Gg::SMEM, st, mx, mw, A);
         }
+        if (e != cudaSuccess) return e;
         if (A.S > 1 && !A.counters) {
             const size_t q = (size_t)M * N / 4;
-            gemm_splitk_reduce<<<(unsigned)((q + 255) / 256), 256, 0, st>>>(A.part, A.S, M, N, A.resid, A.out);
+            return launch_pdl(gemm_splitk_reduce, dim3((unsigned)((q + 255) / 256)), dim3(256), 0, st,
+                              (const float *)A.part, A.S, M, N, A.resid, A.out);
         }
-        return cudaGetLastError();
+        return cudaSuccess;
     }
     if (ldx != K) return cudaErrorInvalidValue;
     dim3 grid((N + 15) / 16, (M + 15) / 16);

@@ -1,10 +1,12 @@
 // host_util.cu -- host-side helpers shared by the launchers: the SM count of
-// the current device and TMA tensor-map encoding through the driver entry
-// point obtained from the runtime (no link-time dependency on libcuda).
+// the current device, the programmatic-launch switch, and TMA tensor-map
+// encoding through the driver entry point obtained from the runtime (no
+// link-time dependency on libcuda).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "vc_internal.h"
@@ -29,6 +31,15 @@ int device_sm_count()
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+bool pdl_enabled()
+{
+    static const bool on = [] {
+        const char *e = std::getenv("VC_PDL");
+        return !(e && e[0] == '0' && e[1] == 0);
+    }();
+    return on;
 }
 
 namespace {

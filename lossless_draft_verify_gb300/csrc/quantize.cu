@@ -330,6 +330,8 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
               int res_cap, int residual, int requantize, int max_groups,
               uint8_t *__restrict__ records, int32_t *n_groups, int32_t *seq_len, int32_t *status)
 {
+    pdl_wait();
+    pdl_trigger();
     using Gm = RecGeom<BITS, D>;
     __shared__ __align__(16) uint32_t img[Gm::REC / 4];
     const int rank = blockIdx.x, Hc = gridDim.x;
@@ -418,13 +420,15 @@ cudaError_t launch_append(const vc_qcache *c, const void *kn, const void *vn, co
     cfg.gridDim = dim3(hc, c->B, 1);
     cfg.blockDim = dim3(2 * D, 1, 1);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = hc;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // the kernel waits on the device
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     auto kern = c->cfg.rotate ? append_kernel<T, BITS, D, true> : append_kernel<T, BITS, D, false>;
     return cudaLaunchKernelEx(&cfg, kern, (const T *)kn, (const T *)vn, n_new, len_base,
                               n_acc, max_new, c->Hkv, (T *)c->k_res, (T *)c->v_res, c->res_cap,

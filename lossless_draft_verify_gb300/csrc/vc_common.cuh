@@ -145,4 +145,40 @@ __device__ __forceinline__ float warp_sum(float v)
 
 __host__ __device__ constexpr int cdiv(long a, long b) { return (int)((a + b - 1) / b); }
 
+// ----- programmatic dependent launch ------------------------------------------
+// A kernel launched with launch_pdl() may start while the previous kernel of
+// its stream is still running.  It must call pdl_wait() before it reads
+// anything an earlier kernel writes, or writes anything an earlier kernel
+// reads: the wait returns once every earlier grid of the stream has completed
+// and its memory operations are visible.  Work before the wait touches only
+// shared memory, tensor memory, kernel parameters and read-only inputs
+// (weights).  pdl_trigger() lets the next kernel of the stream be scheduled;
+// the kernels here call it right after their own wait (and after any tensor
+// memory allocation), so at most two grids overlap and a kernel never holds
+// tensor memory that an earlier, still-starting grid needs.  Both are no-ops
+// in a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Programmatic dependent launch on (default on; VC_PDL=0 in the environment
+// turns it off, launching every kernel with full stream serialization).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 }  // namespace vc

@@ -148,6 +148,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     constexpr int STAGES = Gm::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = smem_raw;
+    // the context lengths and the cache may come from the previous kernel
+    pdl_wait();
     if (smem_u32(sm) & 1023u) {
         // the swizzled operand tiles need 1024-byte alignment; never expected
         if (threadIdx.x == 0) report_timeout(P.status, 99);
@@ -201,6 +203,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    pdl_trigger();      // after the allocation: a started dependent never holds tensor memory first
 
     if (n == 0) {
         // no key of this split is visible to the CTA's rows: empty partials
@@ -589,6 +592,8 @@ template <typename T>
 __global__ void verify_tc_combine(const float *__restrict__ part, int n_split, int n_mtiles, int Hkv,
                                   int Hq, int Dq, int grp, T *__restrict__ out)
 {
+    pdl_wait();
+    pdl_trigger();
     const int item = blockIdx.x;                       // unit * n_mtiles + mt
     const int mt = item % n_mtiles, unit = item / n_mtiles;
     const int b = unit / Hkv, kvh = unit % Hkv;
@@ -775,23 +780,24 @@ cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt
         P.tiles_per_split = pl.tiles_per_split;
         P.scale_log2 = sl2;
         dim3 grid(pl.n_split, B * Hkv * pl.n_cta_m);
+        cudaError_t e;
         if (pl.mt_per_cta == 2) {
             auto kern = verify_tc_kernel<2, false>;
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<2>::SMEM);
-            kern<<<grid, TcGeom<2>::THREADS, TcGeom<2>::SMEM, st>>>(mq, mk, mv, P);
+            e = launch_pdl(kern, grid, dim3(TcGeom<2>::THREADS), TcGeom<2>::SMEM, st, mq, mk, mv, P);
         } else if (pl.tail_rows > 0) {
             auto kern = verify_tc_kernel<1, true>;
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<1, true>::SMEM);
-            kern<<<grid, TcGeom<1, true>::THREADS, TcGeom<1, true>::SMEM, st>>>(mq, mk, mv, P);
+            e = launch_pdl(kern, grid, dim3(TcGeom<1, true>::THREADS), TcGeom<1, true>::SMEM, st, mq, mk, mv, P);
         } else {
             auto kern = verify_tc_kernel<1, false>;
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeom<1>::SMEM);
-            kern<<<grid, TcGeom<1>::THREADS, TcGeom<1>::SMEM, st>>>(mq, mk, mv, P);
+            e = launch_pdl(kern, grid, dim3(TcGeom<1>::THREADS), TcGeom<1>::SMEM, st, mq, mk, mv, P);
         }
+        if (e != cudaSuccess) return e;
         dim3 cgrid(B * Hkv * pl.n_mtiles, TC_M / 4);
-        verify_tc_combine<__nv_bfloat16><<<cgrid, 128, 0, st>>>(P.part, pl.n_split, pl.n_mtiles, Hkv, Hq, Dq,
-                                                                grp, (__nv_bfloat16 *)out);
-        return cudaGetLastError();
+        return launch_pdl(verify_tc_combine<__nv_bfloat16>, cgrid, dim3(128), 0, st, (const float *)P.part,
+                          pl.n_split, pl.n_mtiles, Hkv, Hq, Dq, grp, (__nv_bfloat16 *)out);
     }
     const int rows = B * Dq * Hq;
     if (rows == 0) return cudaSuccess;
