@@ -88,7 +88,8 @@ def _tile_argmax(out_f32: np.ndarray):
 
 
 @pytest.mark.parametrize("M,N,K,plan", [(8, 32000, 4096, True), (264, 32000, 4096, False), (33, 2048, 512, False),
-                                        (5, 151936, 1024, True), (1, 128, 64, False), (130, 1024, 2048, False)])
+                                        (5, 151936, 1024, True), (1, 128, 64, False), (130, 1024, 2048, False),
+                                        (8, 4096, 4096, True)])
 def test_gemm_argmax_epilogue_matches_stored_product(M, N, K, plan):
     """The argmax epilogue's tile maxima are those of the bf16 product vc_gemm
     stores with the same plan (one K split and split-K shapes), including ties
