@@ -62,9 +62,9 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("0157fc58651040f974f2e031917d23164e045ff7fb73f06a72004be922d56ce6",
-               "607af49c7988512f8f8974c461106d2011be78ddbca72ebbb92fc5182dcc3286"),
-    "bytes": 411.008512e6 + 4.545792e6,
+    "sha256": ("00eae9dd7822e2ca0a3a520a1680169c665782b60bcff0791d87d56648604bb6",
+               "5b85f3f8926d2a9eefa983caccea75742e2bcb3ec2f800acaf19894af45839ab"),
+    "bytes": 411.005696e6 + 4.248576e6,
     "algorithmic_bytes": 409731072,
 }
 
