@@ -26,6 +26,13 @@
  *  - Calls keep no state between invocations and may be issued from several
  *    host threads on different streams.  Calls that share a workspace or a
  *    cache must be ordered by the caller.
+ *  - Stream order holds as for any CUDA work.  Most kernels are launched with
+ *    programmatic dependent launch: such a kernel may begin while the
+ *    previous kernel on `stream` is still running, but it reads nothing
+ *    before that kernel has completed and its writes are visible.  The one
+ *    exception is the decoder's weights (vc_decoder_create), which must not
+ *    change while a decoder call is pending: its projections may start
+ *    reading them early.  The environment variable VC_PDL=0 turns this off.
  *  - Workspaces: entry points that combine partial results take a device
  *    workspace `ws` of at least the size returned by the matching
  *    *_workspace_bytes() query, 256-byte aligned.  The first 256 bytes of every

@@ -302,7 +302,7 @@ struct Ctx {
     uint8_t *ws;
     Layout L;
     cudaStream_t st;
-    int plan;          // GEMM split plan: row-invariant (forward) or decode (draft)
+    int plan;          // GEMM split plan: row-invariant (forward) or decode (draft), + kGemmEarlyWeights
     int32_t *status() const { return (int32_t *)ws; }
     unsigned int *counters() const { return (unsigned int *)(ws + kStatusBytes); }
     template <typename P = void> P *at(size_t off) const { return reinterpret_cast<P *>(ws + off); }
@@ -607,7 +607,7 @@ vc_status vc_decoder_forward(const vc_decoder *dec, const int32_t *first_tok, co
         return VC_ERR_INVALID;
     const Layout L = layout_of(dec, B, Dq, max_ctx, 0);
     if (ws_bytes < L.total) return VC_ERR_INVALID;
-    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmRowInvariant};
+    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmRowInvariant | kGemmEarlyWeights};
     const cudaError_t e =
         dec->c.dt == VC_BF16
             ? forward_impl<__nv_bfloat16>(C, first_tok, tokens, tok_stride, B, Dq, ctx_len, max_ctx, k_cache, v_cache,
@@ -635,7 +635,7 @@ vc_status vc_decoder_draft_step(const vc_decoder *dec, const int32_t *tok, int B
     }
     const Layout L = layout_of(dec, B, 1, 0, draft_ws_of(dec, &caches[0]));
     if (ws_bytes < L.total) return VC_ERR_INVALID;
-    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmDecode};
+    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmDecode | kGemmEarlyWeights};
     const cudaError_t e =
         c.dt == VC_BF16
             ? draft_impl<__nv_bfloat16>(C, tok, B, caches, logits, next_tok, drafts_out, drafts_stride)
@@ -726,7 +726,7 @@ vc_status vc_decoder_verify(const vc_decoder *dec, const int32_t *first_tok, con
     if (((uintptr_t)ws & 255u) || !aligned16(k_cache) || !aligned16(v_cache)) return VC_ERR_INVALID;
     const Layout L = layout_of(dec, B, Dq, max_ctx, 0);
     if (ws_bytes < L.total) return VC_ERR_INVALID;
-    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmRowInvariant};
+    Ctx C{dec, (uint8_t *)ws, L, stream, kGemmRowInvariant | kGemmEarlyWeights};
     const int32_t *toks = D > 0 ? drafts : nullptr;
     const cudaError_t e =
         dec->c.dt == VC_BF16

@@ -67,6 +67,7 @@ struct GemmArgs {
     int32_t *amax_idx;           // [M][N / GN] column of the first maximum in the tile
     int32_t *status;
     int M, N, K, S, kb_per_split;
+    int early_w;                 // W may be read before the previous kernel completes
 };
 
 // bf16 rounding of an output element, as the logits store would make it
@@ -126,10 +127,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     tc::fence_after();
     const uint32_t tmem = B->tmem_base;
 
-    // The weights are never written while the decoder runs: the first stages
-    // of W are requested before the wait for the previous kernel, so their
+    // The decoder's weights are never written while it runs: its GEMMs request
+    // the first stages of W before the wait for the previous kernel, so their
     // loads overlap its tail.  x, the residual and the outputs come after it.
-    const int pre = min(n, GSTAGES);
+    const int pre = A.early_w ? min(n, GSTAGES) : 0;
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tmX);
         tc::prefetch_tmap(&tmW);
@@ -464,6 +465,8 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
                  int ldx, void *ws, unsigned int *counters, int32_t *status, cudaStream_t st, int plan,
                  float *amax_val, int32_t *amax_idx)
 {
+    const bool early_w = (plan & kGemmEarlyWeights) != 0;
+    plan &= ~kGemmEarlyWeights;
     if (M <= 0) return cudaSuccess;
     if (amax_val && !gemm_argmax_ok(dt, M, N, K, plan, counters != nullptr)) return cudaErrorNotSupported;
     if (gemm_uses_tensor_cores(dt, N, K)) {
@@ -493,6 +496,7 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         A.M = M;
         A.N = N;
         A.K = K;
+        A.early_w = early_w ? 1 : 0;
         dim3 grid((M + GM - 1) / GM, N / GN, A.S);
         cudaError_t e;
         if (small) {

@@ -59,6 +59,10 @@ cudaError_t drop_tokens(const float *scores, const void *k, const void *v, vc_dt
 // CTA of each output tile sums the partials), or null (a separate reduction).
 constexpr int kGemmRowInvariant = 0;   // forward passes (verify, plain decoding, prefill)
 constexpr int kGemmDecode = 1;         // draft steps (M <= 128)
+// Flag OR-ed into the plan of gemm(): the weights cannot be written by work
+// still pending on the stream (the decoder's own weights), so the kernel may
+// request its first weight slices before the previous kernel completes.
+constexpr int kGemmEarlyWeights = 1 << 4;
 constexpr int kGemmMaxTiles = 16384;
 constexpr size_t kGemmCounterBytes = (size_t)kGemmMaxTiles * 4;
 bool gemm_uses_tensor_cores(vc_dtype dt, int N, int K);

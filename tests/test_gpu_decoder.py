@@ -209,3 +209,45 @@ def test_bf16_fused_verify_equals_logits_and_scan():
     assert n_acc.cpu().tolist() == list(want_n) and nxt.cpu().tolist() == list(want_next)
     assert n_acc.cpu().tolist() == keep
     assert torch.equal(k1, k2) and torch.equal(v1, v2)
+
+
+def _launch_order_probe(graph: bool) -> dict:
+    """Four draft-and-verify rounds of the small bf16 decoder: every round's
+    drafts, accepted lengths and next tokens."""
+    vc = lib()
+    from lossless_draft_verify_gb300 import decode
+    cfg, dec = _small_decoder(vc, seed=1)
+    B, P, D, rounds = 3, 700, 8, 4
+    g = torch.Generator().manual_seed(6)
+    prompt = torch.randint(0, cfg.vocab, (B, P), generator=g, dtype=torch.int32).cuda()
+    run = decode.VeriCacheRunner(dec, B, P + rounds * (D + 1) + 2 * D, D, bits=2, residual=128,
+                                 prefill_chunk=256, use_graph=graph)
+    run.prefill(prompt)
+    log = run.new_log(rounds)
+    for r in range(rounds):
+        run.round(log, r)
+    assert _status_ok(vc, run.ws)
+    return {"drafts": log.drafts.cpu().tolist(), "n_acc": log.n_acc.cpu().tolist(), "nxt": log.nxt.cpu().tolist()}
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_programmatic_launch_changes_no_result(graph):
+    """Programmatic dependent launch (the default) lets each kernel start
+    while the previous one drains; it must not change any result.  The same
+    rounds run in a child process with VC_PDL=0 (every launch fully
+    serialized) give bit for bit the same drafts (the lossy draft steps),
+    accepted lengths and next tokens."""
+    import json
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = ("import json, sys; sys.path.insert(0, %r); sys.path.insert(0, %r); "
+            "from test_gpu_decoder import _launch_order_probe; "
+            "print(json.dumps(_launch_order_probe(%r)))") % (here, os.path.dirname(here), graph)
+    env = dict(os.environ, VC_PDL="0")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+    assert out.returncode == 0, out.stderr[-2000:]
+    serialized = json.loads(out.stdout.strip().splitlines()[-1])
+    assert os.environ.get("VC_PDL", "1") != "0"
+    assert _launch_order_probe(graph) == serialized
