@@ -392,3 +392,77 @@ def h2o_mass(q, k, lens, scale: float) -> np.ndarray:
             p = np.exp(s - s.max())
             out[b, h, :n] += p / p.sum()
     return out
+
+
+# --------------------------------------------------------------------------
+# Lossless packing of bf16 K/V rows for the host link.  The full-KV swap-in
+# (paper page, "What the paper found": the exact KV state is copied in over
+# the interconnect while drafting runs) is bound by the link, so the full
+# cache may travel packed and be expanded on the GPU, bit for bit.  The
+# format is this build's own (the pages give none):
+#
+#   a row of d bf16 values (d even) becomes 16 + 3d/2 bytes:
+#     byte 0        base = E - 14 if E >= 14 else 0, E = the row's largest
+#                   biased exponent field (bits 14..7)
+#     byte 1        n_esc, the number of escaped values (0..7); 255 marks a
+#                   row with more than 7, which the format cannot hold
+#     bytes 2..15   7 escape slots (index, exponent field), in ascending
+#                   index order; unused slots are zero
+#     16 .. 16+d/2  4-bit codes, value i in the low nibble of byte i/2 when i
+#                   is even, the high nibble when odd: exponent - base when
+#                   that is in 0..14, else 15 (escaped)
+#     the last d    sign bit << 7 | the 7 mantissa bits, value i in byte i
+#
+# An escaped value's exponent field is in its slot.  The other bytes of a
+# row marked 255 are not specified.
+# --------------------------------------------------------------------------
+
+KV_PACK_SLOTS = 7
+
+
+def kv_packed_row_bytes(d: int) -> int:
+    return 16 + 3 * d // 2
+
+
+def kv_pack_rows(bits) -> tuple[np.ndarray, np.ndarray]:
+    """uint16 bf16 bit patterns [rows, d] -> (packed uint8 [rows, 16 + 3d/2],
+    bool [rows] marking the rows that need more than 7 escapes)."""
+    b = np.asarray(bits, dtype=np.uint16)
+    rows, d = b.shape
+    e = ((b >> 7) & 0xFF).astype(np.int32)
+    E = e.max(axis=1) if d else np.zeros(rows, np.int32)
+    base = np.where(E >= 14, E - 14, 0)
+    code = e - base[:, None]
+    esc = code < 0                      # e <= E = base + 14, so only below
+    n_esc = esc.sum(axis=1)
+    over = n_esc > KV_PACK_SLOTS
+    out = np.zeros((rows, kv_packed_row_bytes(d)), np.uint8)
+    out[:, 0] = base
+    out[:, 1] = np.where(over, 255, n_esc)
+    for r in np.flatnonzero(n_esc):
+        idx = np.flatnonzero(esc[r])[:KV_PACK_SLOTS]
+        out[r, 2:2 + 2 * len(idx):2] = idx
+        out[r, 3:3 + 2 * len(idx):2] = e[r, idx]
+    c = np.where(esc, 15, code).astype(np.uint8)
+    out[:, 16:16 + d // 2] = c[:, 0::2] | (c[:, 1::2] << 4)
+    out[:, 16 + d // 2:] = (((b >> 8) & 0x80) | (b & 0x7F)).astype(np.uint8)
+    return out, over
+
+
+def kv_unpack_rows(packed, d: int) -> np.ndarray:
+    """Inverse of kv_pack_rows for rows that were not marked: uint8 [rows,
+    16 + 3d/2] -> uint16 bf16 bit patterns [rows, d]."""
+    p = np.asarray(packed, dtype=np.uint8)
+    rows = p.shape[0]
+    base = p[:, 0].astype(np.int32)
+    nib = p[:, 16:16 + d // 2]
+    code = np.empty((rows, d), np.int32)
+    code[:, 0::2] = nib & 15
+    code[:, 1::2] = nib >> 4
+    e = base[:, None] + code
+    for r in np.flatnonzero(p[:, 1]):
+        n = int(p[r, 1])
+        assert n <= KV_PACK_SLOTS, "row marked as not representable"
+        e[r, p[r, 2:2 + 2 * n:2]] = p[r, 3:3 + 2 * n:2]
+    sm = p[:, 16 + d // 2:].astype(np.int32)
+    return (((sm & 0x80) << 8) | (e << 7) | (sm & 0x7F)).astype(np.uint16)
