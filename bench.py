@@ -47,6 +47,9 @@ METRIC = "lossless tokens/s at 32k ctx; draft-attn HBM GB/s and verify-attn TC %
 WORKLOAD = ("verify_round_32k: B16 x 32/8 heads x d128, 32768-token context, KIVI 2-bit g32 R128 "
             "draft cache, horizon 32 (verify block 33), bf16 full KV swapped in from pinned host, "
             "accept over [16,33,151936] bf16 logits")
+WORKLOAD_PACKED = WORKLOAD.replace("bf16 full KV swapped in from pinned host",
+                                   "bf16 full KV swapped in from pinned host (held losslessly packed, "
+                                   "expanded on the GPU)")
 
 
 def dist_env():
@@ -152,7 +155,7 @@ class Round:
     commit stay whole-batch launches."""
 
     def __init__(self, dev, stagger: int = 2, horizon: int = HORIZON, link_gbps: float | None = None,
-                 bits: int = BITS, residual: int = RESIDUAL):
+                 bits: int = BITS, residual: int = RESIDUAL, packed: bool = False):
         from lossless_draft_verify_gb300 import inputs, vc
         self.vc, self.dev = vc, dev
         self.bits, self.residual = bits, residual
@@ -168,6 +171,25 @@ class Round:
         self.vfull_host = torch.empty(self.vfull.shape, dtype=torch.bfloat16).pin_memory()
         self.kfull_host.copy_(self.kfull)
         self.vfull_host.copy_(self.vfull)
+        # packed host copy (lossless, 16 + 3d/2 bytes a row): the link moves
+        # it into a device staging buffer and vc_kv_unpack restores the bf16
+        self.packed = packed
+        if packed:
+            assert not link_gbps, "paced swaps move the bf16 cache"
+            rb = vc.vc_kv_packed_row_bytes(D_HEAD)
+            self.kpack = torch.empty(B, HKV, Ls, rb, dtype=torch.uint8, device=dev)
+            self.vpack = torch.empty_like(self.kpack)
+            n_over = torch.zeros(1, dtype=torch.int32, device=dev)
+            vc.vc_kv_pack(self.kfull, self.kpack, n_over)
+            vc.vc_kv_pack(self.vfull, self.vpack, n_over)
+            assert int(n_over.item()) == 0, "rows the packed format cannot hold"
+            self.kpack_host = self.kpack.cpu().pin_memory()
+            self.vpack_host = self.vpack.cpu().pin_memory()
+            # expansion runs on a stream of its own, so the link's copies stay
+            # back to back; a part's staging rows are rewritten only after its
+            # verify, which follows its expansion
+            self.unpack_stream = torch.cuda.Stream(device=dev)
+            self.ev_copied = [torch.cuda.Event() for _ in range(stagger)]
         # compressed draft cache of the context
         maxg = (CTX + DQ) // GROUP + 1
         self.cache = vc.QCache(B, HKV, D_HEAD, bits, maxg, residual + GROUP + DQ + 32, residual)
@@ -213,7 +235,7 @@ class Round:
         for e in self.ev_swap + self.ev_ver + [self.ev_acc, self.ev_in]:
             e.record(main)
         # per step: (append + draft) per draft step, verify + its combine per part, accept, commit
-        self.launches_per_step = HORIZON * 2 + 2 * stagger + 1 + 1
+        self.launches_per_step = HORIZON * 2 + 2 * stagger + 1 + 1 + (2 * stagger if packed else 0)
         # host-side copies of the per-step inputs (end-to-end measurement)
         self.h_q_draft = self.q_draft.cpu().pin_memory()
         self.h_k_step = self.k_step.cpu().pin_memory()
@@ -227,7 +249,7 @@ class Round:
                              (self.h_q_draft, self.h_k_step, self.h_v_step, self.h_q_ver, self.h_logits,
                               self.h_drafts))
         self.d2h_bytes = 2 * B * 4
-        self.swap_bytes = 2 * self.kfull.numel() * 2
+        self.swap_bytes = 2 * (self.kpack.numel() if packed else self.kfull.numel() * 2)
 
     def step(self, ev=None, e2e=False):
         vc, main = self.vc, torch.cuda.current_stream()
@@ -255,11 +277,20 @@ class Round:
                                     stream=self.side)
                 vc.vc_swap_in_paced(self.vfull[b0:b1], self.vfull_host[b0:b1], self.link_gbps, self.pace_ws,
                                     stream=self.side, done_event=self.ev_swap[p])
+            elif self.packed:
+                vc.vc_swap_in(self.kpack[b0:b1], self.kpack_host[b0:b1], stream=self.side)
+                vc.vc_swap_in(self.vpack[b0:b1], self.vpack_host[b0:b1], stream=self.side,
+                              done_event=self.ev_copied[p])
+                self.unpack_stream.wait_event(self.ev_copied[p])
+                vc.vc_kv_unpack(self.kpack[b0:b1], self.kfull[b0:b1], stream=self.unpack_stream)
+                vc.vc_kv_unpack(self.vpack[b0:b1], self.vfull[b0:b1], stream=self.unpack_stream)
+                self.ev_swap[p].record(self.unpack_stream)
             else:
                 vc.vc_swap_in(self.kfull[b0:b1], self.kfull_host[b0:b1], stream=self.side)
                 vc.vc_swap_in(self.vfull[b0:b1], self.vfull_host[b0:b1], stream=self.side, done_event=self.ev_swap[p])
         if ev is not None:
-            ev["swap1"].record(self.side)
+            # the swap ends with the last expansion when the cache travels packed
+            ev["swap1"].record(self.unpack_stream if self.packed else self.side)
         for j in range(self.D):
             vc.vc_qcache_append(self.cache, self.k_step[j], self.v_step[j], self.ones, requantize=False)
             if ev is not None:
@@ -502,6 +533,18 @@ def run_kernel(args, dev):
         nbytes = K * N * 2 + M * K * 2 + M * N * 2
         flops = 2 * M * N * K
         rec = {"workload": "draft-step GEMM x[8,4096] W[4096,28672] bf16 (decode plan)"}
+    elif name == "unpack":
+        # expansion of the round's packed full K cache [16, 8, 32801, 128]
+        k, _ = inputs.kv_with_outliers(B, HKV, CTX + DQ, D_HEAD, seed=1, device=dev)
+        rbytes = vc.vc_kv_packed_row_bytes(D_HEAD)
+        pk = torch.empty(*k.shape[:-1], rbytes, dtype=torch.uint8, device=dev)
+        n_over = torch.zeros(1, dtype=torch.int32, device=dev)
+        vc.vc_kv_pack(k, pk, n_over)
+        assert int(n_over.item()) == 0
+        out = torch.empty_like(k)
+        fn = lambda: vc.vc_kv_unpack(pk, out)
+        nbytes = pk.numel() + out.numel() * 2
+        rec = {"workload": f"expansion of the packed full K cache [{B},8,{CTX + DQ},128] ({rbytes} of 256 bytes a row)"}
     elif name == "swap":
         # full-cache swap-in (host link): one copy, or the cache split in
         # chunks issued on as many side streams
@@ -883,12 +926,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", default=None,
-                    help="time one kernel alone: draft, verify, accept, quantize, drop, dense_draft")
+                    help="time one kernel alone: draft, verify, accept, quantize, drop, dense_draft, gemm, "
+                         "unpack, swap")
     ap.add_argument("--dq", type=int, default=32, help="verify block size for --kernel verify")
     ap.add_argument("--batch", type=int, default=B, help="sequences for --kernel draft/verify")
     ap.add_argument("--chunks", type=int, default=1, help="side streams for --kernel swap")
     ap.add_argument("--stagger", type=int, default=2, choices=[1, 2],
                     help="round workload: swap and verify per half batch (2) or whole batch (1)")
+    ap.add_argument("--swap", default="packed", choices=["packed", "raw"],
+                    help="round workload: the full cache on the host packed (lossless rows of 16 + 3d/2 bytes, "
+                         "expanded on the GPU after each swap) or as plain bf16")
     ap.add_argument("--workload", default="round", choices=["round", "model"],
                     help="round: one layer's hot path at 32k (B16); model: the 8-layer decoder end to end")
     ap.add_argument("--prompt", type=int, default=32768, help="prompt tokens per sequence (--workload model)")
@@ -941,7 +988,7 @@ def main():
         if pg is not None:
             pg.destroy_process_group()
         return
-    rnd = Round(dev, stagger=args.stagger)
+    rnd = Round(dev, stagger=args.stagger, packed=args.swap == "packed")
 
     for _ in range(args.warmup):
         rnd.step()
@@ -1001,9 +1048,12 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": CTX,
+            "config": {"workload": WORKLOAD_PACKED if rnd.packed else WORKLOAD, "global_batch": B * world,
+                       "seq_len": CTX,
                        "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)",
-                       "stagger": rnd.stagger},
+                       "stagger": rnd.stagger,
+                       "swap": ("full cache held packed on the host (lossless, 208 of 256 bytes a row), "
+                                "expanded on the GPU" if rnd.packed else "full bf16 cache")},
             "roofline": {"bound": "hbm", "achieved": draft_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": draft_gbs / hbm,
                          "traffic": captured_traffic(DRAFT_TRAFFIC, statistics.mean(d_bytes)),

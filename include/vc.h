@@ -412,6 +412,46 @@ vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes,
 vc_status vc_swap_in_paced(void *dst_dev, const void *src_pinned_host, size_t bytes, double gbps,
                            size_t chunk_bytes, void *pace_ws, cudaStream_t side_stream, cudaEvent_t done);
 
+/*
+ * Packed full cache for the host link.  The swap-in above is bound by the
+ * link (paper page, "What the paper found": the exact KV state comes in over
+ * the interconnect while drafting runs), so the host may hold the full cache
+ * losslessly packed; it then moves 16 + 3d/2 bytes per row of d bf16 values
+ * instead of 2d (208 instead of 256 at d = 128) and vc_kv_unpack restores
+ * every bit on the GPU.  Packed row (d even):
+ *   byte 0           base = E - 14, or 0 when E < 14, E = the row's largest
+ *                    bf16 exponent field (bits 14..7)
+ *   byte 1           n_esc in 0..7, or 255: the row needs more than 7
+ *                    escapes and cannot be held (its other bytes are then
+ *                    unspecified)
+ *   bytes 2..15      7 escape slots (value index, exponent field), ascending
+ *                    index order, unused slots zero
+ *   16 .. 16 + d/2   4-bit codes: value i in the low nibble of byte i/2 for
+ *                    even i, the high nibble for odd i; code = field - base
+ *                    when that lies in 0..14, else 15 (the field is in a slot)
+ *   last d bytes     sign << 7 | 7 mantissa bits of value i, in byte i
+ * Rows are independent and 16-byte multiples, so a [B][Hkv][L][d] cache packs
+ * to [B][Hkv][L][16 + 3d/2] and appended rows pack on their own.
+ */
+size_t vc_kv_packed_row_bytes(int d);   /* 16 + 3d/2 for d in {64, 128}, else 0 */
+
+/*
+ * Pack `rows` rows of d bf16 values.  src_bf16: device, [rows][d], 8-byte
+ * aligned; dst_packed: device (or mapped pinned host), [rows][16 + 3d/2],
+ * 16-byte aligned.  n_over: device int32 or NULL; the number of rows marked
+ * 255 is added to it (a row so marked cannot be unpacked: keep the raw copy
+ * for that cache).  VC_ERR_UNSUPPORTED for d outside {64, 128}.
+ */
+vc_status vc_kv_pack(const void *src_bf16, void *dst_packed, int64_t rows, int d, int32_t *n_over,
+                     cudaStream_t stream);
+
+/*
+ * Unpack `rows` packed rows (none marked 255) into bf16.  src_packed: device,
+ * 16-byte aligned; dst_bf16: device, [rows][d], 8-byte aligned.  Bit-exact
+ * inverse of vc_kv_pack.
+ */
+vc_status vc_kv_unpack(const void *src_packed, void *dst_bf16, int64_t rows, int d, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* (7) target decoder around the hot path                                    */
 /* ------------------------------------------------------------------------ */

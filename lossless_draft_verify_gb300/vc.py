@@ -157,6 +157,12 @@ def load() -> ctypes.CDLL:
     L.vc_accept_tiles.argtypes = [P, P, c_int, P, c_int, c_int, P, P, P]
     L.vc_decoder_verify.restype = c_int
     L.vc_decoder_verify.argtypes = [P, P, P, c_int, c_int, P, c_int, P, P, c_int, P, P, P, P, P, c_size_t, P]
+    L.vc_kv_packed_row_bytes.restype = c_size_t
+    L.vc_kv_packed_row_bytes.argtypes = [c_int]
+    L.vc_kv_pack.restype = c_int
+    L.vc_kv_pack.argtypes = [P, P, c_int64, c_int, P, P]
+    L.vc_kv_unpack.restype = c_int
+    L.vc_kv_unpack.argtypes = [P, P, c_int64, c_int, P]
     _lib = L
     return L
 
@@ -170,7 +176,8 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_decoder_draft_step", "vc_kv_writeback", "vc_gemm_workspace_bytes", "vc_gemm",
             "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits",
             "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe",
-            "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify"]
+            "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify",
+            "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -571,6 +578,30 @@ class DecoderTrace:
         torch.cuda.synchronize()
         return [(TRACE_KINDS[self._kinds[k]], self.events[2 * k].elapsed_time(self.events[2 * k + 1]))
                 for k in range(n)]
+
+
+def vc_kv_packed_row_bytes(d: int) -> int:
+    return int(load().vc_kv_packed_row_bytes(d))
+
+
+def vc_kv_pack(src: torch.Tensor, dst: torch.Tensor, n_over: torch.Tensor | None = None, stream=None):
+    """src bf16 [..., d] (rows = everything before d) -> dst uint8 [..., 16 + 3d/2]
+    (device, or pinned host mapped into the device); n_over: int32 device
+    counter of rows that cannot be packed (added to)."""
+    d = src.shape[-1]
+    rows = src.numel() // d if d else 0
+    assert src.dtype == torch.bfloat16 and src.is_contiguous() and dst.dtype == torch.uint8 and dst.is_contiguous()
+    assert dst.numel() == rows * vc_kv_packed_row_bytes(d)
+    _check(load().vc_kv_pack(src.data_ptr(), dst.data_ptr(), rows, d, _ptr(n_over), _stream(stream)), "vc_kv_pack")
+
+
+def vc_kv_unpack(src: torch.Tensor, dst: torch.Tensor, stream=None):
+    """src uint8 [..., 16 + 3d/2] (device) -> dst bf16 [..., d]."""
+    d = dst.shape[-1]
+    rows = dst.numel() // d if d else 0
+    assert dst.dtype == torch.bfloat16 and dst.is_contiguous() and src.dtype == torch.uint8 and src.is_contiguous()
+    assert src.numel() == rows * vc_kv_packed_row_bytes(d)
+    _check(load().vc_kv_unpack(src.data_ptr(), dst.data_ptr(), rows, d, _stream(stream)), "vc_kv_unpack")
 
 
 def vc_swap_in_paced(dst: torch.Tensor, src_pinned: torch.Tensor, gbps: float, pace_ws: torch.Tensor,

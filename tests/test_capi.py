@@ -128,3 +128,23 @@ def test_greedy_head_and_rotation_validation_on_the_host(libvc):
     # the rotated-cache flag takes 0 or 1
     q = vc.QCacheC(fake, fake, fake, fake, fake, fake, 1, 1, 128, vc.QuantCfg(2, 32, 0, 2), 4, 64, vc.VC_BF16)
     assert L.vc_quantize_kv(fake, fake, vc.VC_BF16, 1, 1, 32, 32, 128, ctypes.byref(q), None) == vc.VC_ERR_INVALID
+
+
+def test_kv_pack_validation_on_the_host(libvc):
+    """Packing and unpacking reject bad arguments before any CUDA call; zero
+    rows are a no-op."""
+    from lossless_draft_verify_gb300 import vc
+    L = vc.load()
+    fake = 1 << 20
+    assert L.vc_kv_packed_row_bytes(128) == 208 and L.vc_kv_packed_row_bytes(64) == 112
+    assert L.vc_kv_packed_row_bytes(96) == 0
+    assert L.vc_kv_pack(None, fake, 4, 128, None, None) == vc.VC_ERR_INVALID
+    assert L.vc_kv_pack(fake, fake, -1, 128, None, None) == vc.VC_ERR_INVALID
+    assert L.vc_kv_pack(fake, fake, 4, 96, None, None) == vc.VC_ERR_UNSUPPORTED
+    assert L.vc_kv_pack(fake + 4, fake, 4, 128, None, None) == vc.VC_ERR_INVALID     # source not 8-byte aligned
+    assert L.vc_kv_pack(fake, fake + 8, 4, 128, None, None) == vc.VC_ERR_INVALID     # rows not 16-byte aligned
+    assert L.vc_kv_pack(None, None, 0, 128, None, None) == vc.VC_OK
+    assert L.vc_kv_unpack(fake, None, 4, 64, None) == vc.VC_ERR_INVALID
+    assert L.vc_kv_unpack(fake + 8, fake, 4, 64, None) == vc.VC_ERR_INVALID
+    assert L.vc_kv_unpack(fake, fake, 4, 32, None) == vc.VC_ERR_UNSUPPORTED
+    assert L.vc_kv_unpack(None, None, 0, 64, None) == vc.VC_OK
