@@ -620,8 +620,9 @@ def run_model(args, dev, rank, world, barrier, pg):
     n_tr = 2                                  # eager rounds for the per-operation trace
     total = args.warmup + n_tr + args.steps + n_e2e
     max_len = P + total * (M_HORIZON + 1) + 64
+    packed = args.swap == "packed"              # default raw
     run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=args.bits, residual=M_RESIDUAL, host_cache=True,
-                                 prefill_chunk=512, device=dev, rotate=args.rotate)
+                                 prefill_chunk=512, device=dev, rotate=args.rotate, pack_host=packed)
     prompt = inputs.random_prompts(M_B, P, cfg.vocab, seed=rank, device=dev)
     t_pf = time.perf_counter()
     run.prefill(prompt)
@@ -680,6 +681,7 @@ def run_model(args, dev, rank, world, barrier, pg):
         barrier()
         e_tok = int((log.n_acc[base:base + n_e2e].cpu().long() + 1).sum())
         e2e_val, _ = replicas.whole_job_rate(e_tok, e0.elapsed_time(e1), pg, device=dev)
+    run.check_packed()                   # every committed row was held by the packed host copy
 
     # lossless check: the same prompts decoded greedily with the full cache
     # resident, token for token against the draft-and-verify output
@@ -746,19 +748,22 @@ def run_model(args, dev, rank, world, barrier, pg):
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
             "config": {"workload": MODEL_WORKLOAD.format(ctx=P, bits=args.bits) +
-                       (", keys rotated (Walsh-Hadamard) before quantization" if args.rotate else ""),
+                       (", keys rotated (Walsh-Hadamard) before quantization" if args.rotate else "") +
+                       (", full cache held losslessly packed on the host, expanded on the GPU" if packed else ""),
                        "global_batch": M_B * world,
                        "seq_len": P,
                        "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
             "roofline": roof,
             "phases_ms": {"draft_32_steps": d_ms, "verify_forward": v_ms, "accept_commit_writeback": c_ms,
                           "swap_in": s_ms, "swap_hidden_frac": hidden},
-            "swap": {"bytes": run_bytes(cfg, max_len), "GB/s": run_bytes(cfg, max_len) / (s_ms / 1e3) / 1e9},
+            "swap": {"bytes": run_bytes(cfg, max_len, packed),
+                     "GB/s": run_bytes(cfg, max_len, packed) / (s_ms / 1e3) / 1e9,
+                     "format": "packed rows (lossless, 208 of 256 bytes)" if packed else "bf16"},
             "kernels": kernels,
             "accepted_per_round_mean": float(n_acc.float().mean()), "tokens_per_round": tokens / args.steps,
             "prefill_s": round(t_pf, 2), "status": st, "lossless_check": check,
             "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc) * args.steps,
-            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, max_len),
+            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, max_len, packed),
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": None,
         }
@@ -791,10 +796,11 @@ def model_launches_per_round(cfg, vc) -> int:
     return M_HORIZON * draft + verify + cfg.n_layers + 1
 
 
-def run_bytes(cfg, max_len) -> int:
+def run_bytes(cfg, max_len, packed: bool = False) -> int:
     """Bytes of one full-cache swap-in (K and V, every layer, the whole ring of
-    positions the runner allocates)."""
-    return 2 * cfg.n_layers * M_B * cfg.n_kv_heads * (max_len + M_HORIZON + 1) * cfg.head_dim * 2
+    positions the runner allocates), bf16 or packed rows."""
+    row = 16 + 3 * cfg.head_dim // 2 if packed else cfg.head_dim * 2
+    return 2 * cfg.n_layers * M_B * cfg.n_kv_heads * (max_len + M_HORIZON + 1) * row
 
 
 def full_kv_step_ms(rnd, steps: int, warmup: int) -> float:
@@ -933,9 +939,11 @@ def main():
     ap.add_argument("--chunks", type=int, default=1, help="side streams for --kernel swap")
     ap.add_argument("--stagger", type=int, default=2, choices=[1, 2],
                     help="round workload: swap and verify per half batch (2) or whole batch (1)")
-    ap.add_argument("--swap", default="packed", choices=["packed", "raw"],
-                    help="round workload: the full cache on the host packed (lossless rows of 16 + 3d/2 bytes, "
-                         "expanded on the GPU after each swap) or as plain bf16")
+    ap.add_argument("--swap", default=None, choices=["packed", "raw"],
+                    help="the full cache on the host packed (lossless rows of 16 + 3d/2 bytes, expanded on the "
+                         "GPU after each swap) or as plain bf16; default packed for the round (its swap outlasts "
+                         "drafting), raw for the model (at 32k drafting takes as long as the bf16 swap, and the "
+                         "expansion would slow drafting)")
     ap.add_argument("--workload", default="round", choices=["round", "model"],
                     help="round: one layer's hot path at 32k (B16); model: the 8-layer decoder end to end")
     ap.add_argument("--prompt", type=int, default=32768, help="prompt tokens per sequence (--workload model)")
@@ -988,7 +996,7 @@ def main():
         if pg is not None:
             pg.destroy_process_group()
         return
-    rnd = Round(dev, stagger=args.stagger, packed=args.swap == "packed")
+    rnd = Round(dev, stagger=args.stagger, packed=args.swap != "raw")      # default packed
 
     for _ in range(args.warmup):
         rnd.step()

@@ -452,6 +452,19 @@ vc_status vc_kv_pack(const void *src_bf16, void *dst_packed, int64_t rows, int d
  */
 vc_status vc_kv_unpack(const void *src_packed, void *dst_bf16, int64_t rows, int d, cudaStream_t stream);
 
+/*
+ * vc_kv_writeback_packed -- vc_kv_writeback for a packed host cache: the
+ * committed rows (i <= n_acc[b]) of the verify block, every layer, K and V,
+ * packed into k_host_packed / v_host_packed [n_layers][B][Hkv][L_stride]
+ * [16 + 3d/2] at position ctx_len[b] + i.  k_blk, v_blk: device bf16
+ * [n_layers][B][Hkv][Dq][d], 8-byte aligned; the host buffers pinned and
+ * 16-byte aligned.  Rows that cannot be packed are counted in n_over (device
+ * int32, or NULL) and marked: the caller must then stop using the packed copy.
+ */
+vc_status vc_kv_writeback_packed(const void *k_blk, const void *v_blk, int n_layers, int B, int Hkv, int Dq, int d,
+                                 const int32_t *n_acc, const int32_t *ctx_len, void *k_host_packed,
+                                 void *v_host_packed, int L_stride, int32_t *n_over, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* (7) target decoder around the hot path                                    */
 /* ------------------------------------------------------------------------ */

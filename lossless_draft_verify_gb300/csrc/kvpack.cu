@@ -53,76 +53,106 @@ __device__ __forceinline__ void split_word(typename LaneWord<VPL>::T w, uint32_t
     }
 }
 
+// Pack one row by one warp.  h: this warp's 16-byte shared header image.
 template <int D>
-__global__ void __launch_bounds__(kPackThreads)
-kv_pack_kernel(const uint16_t *__restrict__ src, uint8_t *__restrict__ dst, long long rows, int32_t *n_over)
+__device__ __forceinline__ void pack_row(const uint16_t *__restrict__ src_row, uint8_t *row, uint8_t *h, int lane,
+                                         int32_t *n_over)
 {
     using Gm = PackGeom<D>;
     constexpr int VPL = Gm::VPL;
     using W = typename LaneWord<VPL>::T;
+    uint32_t v[VPL];
+    split_word<VPL>(reinterpret_cast<const W *>(src_row)[lane], v);
+    uint32_t emax = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) emax = max(emax, (v[i] >> 7) & 0xFFu);
+    emax = __reduce_max_sync(0xffffffffu, emax);
+    const int base = emax >= 14 ? (int)emax - 14 : 0;
+    uint32_t code[VPL];
+    int nesc = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int c = (int)((v[i] >> 7) & 0xFFu) - base;     // <= 14 by the choice of base
+        code[i] = c < 0 ? 15u : (uint32_t)c;
+        nesc += c < 0;
+    }
+    int incl = nesc;                                         // inclusive prefix count over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    // header: zeroed, escape slots filled by their owners, then the counts
+    __syncwarp();                                            // h may still be read for the previous row
+    if (lane < 4) reinterpret_cast<uint32_t *>(h)[lane] = 0u;
+    __syncwarp();
+    int slot = incl - nesc;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+        if (code[i] == 15u) {
+            if (slot < kSlots) {
+                h[2 + 2 * slot] = (uint8_t)(lane * VPL + i);
+                h[3 + 2 * slot] = (uint8_t)((v[i] >> 7) & 0xFFu);
+            }
+            ++slot;
+        }
+    __syncwarp();
+    if (lane == 0) {
+        h[0] = (uint8_t)base;
+        h[1] = total > kSlots ? 255 : (uint8_t)total;
+        if (total > kSlots && n_over) atomicAdd(n_over, 1);
+    }
+    __syncwarp();
+    if (lane < 4) reinterpret_cast<uint32_t *>(row)[lane] = reinterpret_cast<const uint32_t *>(h)[lane];
+    uint32_t nib = 0, sm = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        nib |= code[i] << (4 * i);
+        sm |= (((v[i] >> 8) & 0x80u) | (v[i] & 0x7Fu)) << (8 * i);
+    }
+    if constexpr (VPL == 2) {
+        row[Gm::NIB + lane] = (uint8_t)nib;
+        reinterpret_cast<uint16_t *>(row + Gm::SM)[lane] = (uint16_t)sm;
+    } else {
+        reinterpret_cast<uint16_t *>(row + Gm::NIB)[lane] = (uint16_t)nib;
+        reinterpret_cast<uint32_t *>(row + Gm::SM)[lane] = sm;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPackThreads)
+kv_pack_kernel(const uint16_t *__restrict__ src, uint8_t *__restrict__ dst, long long rows, int32_t *n_over)
+{
     __shared__ __align__(16) uint8_t hdr[kPackThreads / 32][16];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const long long nw = (long long)gridDim.x * (kPackThreads / 32);
-    uint8_t *h = hdr[wib];
+    for (long long r = (long long)blockIdx.x * (kPackThreads / 32) + wib; r < rows; r += nw)
+        pack_row<D>(src + r * D, dst + r * PackGeom<D>::ROW, hdr[wib], lane, n_over);
+}
+
+// After acceptance: the n_acc[b] + 1 committed rows of the verify block (K
+// and V, every layer) packed into the host copy at positions ctx[b] + i.
+// One warp per (layer, sequence-head, row).
+template <int D>
+__global__ void __launch_bounds__(kPackThreads)
+kv_writeback_packed_kernel(const uint16_t *__restrict__ kb, const uint16_t *__restrict__ vb, int n_layers, int B,
+                           int Hkv, int Dq, const int32_t *__restrict__ n_acc, const int32_t *__restrict__ ctx,
+                           uint8_t *kh, uint8_t *vh, int L_stride, int32_t *n_over)
+{
+    __shared__ __align__(16) uint8_t hdr[kPackThreads / 32][16];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long long rows = (long long)n_layers * B * Hkv * Dq;
+    const long long nw = (long long)gridDim.x * (kPackThreads / 32);
     for (long long r = (long long)blockIdx.x * (kPackThreads / 32) + wib; r < rows; r += nw) {
-        uint32_t v[VPL];
-        split_word<VPL>(reinterpret_cast<const W *>(src + r * D)[lane], v);
-        uint32_t emax = 0;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) emax = max(emax, (v[i] >> 7) & 0xFFu);
-        emax = __reduce_max_sync(0xffffffffu, emax);
-        const int base = emax >= 14 ? (int)emax - 14 : 0;
-        uint32_t code[VPL];
-        int nesc = 0;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int c = (int)((v[i] >> 7) & 0xFFu) - base;     // <= 14 by the choice of base
-            code[i] = c < 0 ? 15u : (uint32_t)c;
-            nesc += c < 0;
-        }
-        int incl = nesc;                                         // inclusive prefix count over the lanes
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        // header: zeroed, escape slots filled by their owners, then the counts
-        if (lane < 4) reinterpret_cast<uint32_t *>(h)[lane] = 0u;
-        __syncwarp();
-        int slot = incl - nesc;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i)
-            if (code[i] == 15u) {
-                if (slot < kSlots) {
-                    h[2 + 2 * slot] = (uint8_t)(lane * VPL + i);
-                    h[3 + 2 * slot] = (uint8_t)((v[i] >> 7) & 0xFFu);
-                }
-                ++slot;
-            }
-        __syncwarp();
-        if (lane == 0) {
-            h[0] = (uint8_t)base;
-            h[1] = total > kSlots ? 255 : (uint8_t)total;
-            if (total > kSlots && n_over) atomicAdd(n_over, 1);
-        }
-        __syncwarp();
-        uint8_t *row = dst + r * Gm::ROW;
-        if (lane < 4) reinterpret_cast<uint32_t *>(row)[lane] = reinterpret_cast<const uint32_t *>(h)[lane];
-        uint32_t nib = 0, sm = 0;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            nib |= code[i] << (4 * i);
-            sm |= (((v[i] >> 8) & 0x80u) | (v[i] & 0x7Fu)) << (8 * i);
-        }
-        if constexpr (VPL == 2) {
-            row[Gm::NIB + lane] = (uint8_t)nib;
-            reinterpret_cast<uint16_t *>(row + Gm::SM)[lane] = (uint16_t)sm;
-        } else {
-            reinterpret_cast<uint16_t *>(row + Gm::NIB)[lane] = (uint16_t)nib;
-            reinterpret_cast<uint32_t *>(row + Gm::SM)[lane] = sm;
-        }
-        __syncwarp();                                            // h is reused by the next row
+        const int i = (int)(r % Dq);
+        const long long lbh = r / Dq;                       // (layer * B + b) * Hkv + h
+        const int b = (int)((lbh / Hkv) % B);
+        const int pos = ctx[b] + i;
+        if (i > n_acc[b] || pos >= L_stride) continue;      // uniform over the warp
+        const long long dst = lbh * L_stride + pos;
+        pack_row<D>(kb + r * D, kh + dst * PackGeom<D>::ROW, hdr[wib], lane, n_over);
+        pack_row<D>(vb + r * D, vh + dst * PackGeom<D>::ROW, hdr[wib], lane, n_over);
     }
 }
 
@@ -220,6 +250,24 @@ cudaError_t kv_unpack(const void *src, void *dst, long long rows, int d, cudaStr
     return cudaGetLastError();
 }
 
+cudaError_t kv_writeback_packed(const void *kb, const void *vb, int n_layers, int B, int Hkv, int Dq, int d,
+                                const int32_t *n_acc, const int32_t *ctx, void *kh, void *vh, int L_stride,
+                                int32_t *n_over, cudaStream_t st)
+{
+    const long long rows = (long long)n_layers * B * Hkv * Dq;
+    if (rows <= 0) return cudaSuccess;
+    const unsigned g = pack_grid(rows, 1);
+    if (d == 128)
+        kv_writeback_packed_kernel<128><<<g, kPackThreads, 0, st>>>((const uint16_t *)kb, (const uint16_t *)vb,
+                                                                    n_layers, B, Hkv, Dq, n_acc, ctx, (uint8_t *)kh,
+                                                                    (uint8_t *)vh, L_stride, n_over);
+    else
+        kv_writeback_packed_kernel<64><<<g, kPackThreads, 0, st>>>((const uint16_t *)kb, (const uint16_t *)vb,
+                                                                   n_layers, B, Hkv, Dq, n_acc, ctx, (uint8_t *)kh,
+                                                                   (uint8_t *)vh, L_stride, n_over);
+    return cudaGetLastError();
+}
+
 }  // namespace vc
 
 using namespace vc;
@@ -240,6 +288,28 @@ vc_status vc_kv_pack(const void *src_bf16, void *dst_packed, int64_t rows, int d
         ((uintptr_t)n_over & 3u))
         return VC_ERR_INVALID;
     return kv_pack(src_bf16, dst_packed, rows, d, n_over, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+}
+
+vc_status vc_kv_writeback_packed(const void *k_blk, const void *v_blk, int n_layers, int B, int Hkv, int Dq, int d,
+                                 const int32_t *n_acc, const int32_t *ctx_len, void *k_host_packed,
+                                 void *v_host_packed, int L_stride, int32_t *n_over, cudaStream_t stream)
+{
+    if (!k_blk || !v_blk || !n_acc || !ctx_len || !k_host_packed || !v_host_packed) return VC_ERR_INVALID;
+    if (n_layers <= 0 || B <= 0 || Hkv <= 0 || Dq <= 0 || L_stride < Dq) return VC_ERR_INVALID;
+    if (d != 64 && d != 128) return VC_ERR_UNSUPPORTED;
+    if (((uintptr_t)k_blk & 7u) || ((uintptr_t)v_blk & 7u) || ((uintptr_t)k_host_packed & 15u) ||
+        ((uintptr_t)v_host_packed & 15u) || ((uintptr_t)n_over & 3u))
+        return VC_ERR_INVALID;
+    void *kd = nullptr, *vd = nullptr;
+    if (cudaHostGetDevicePointer(&kd, k_host_packed, 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&vd, v_host_packed, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return VC_ERR_INVALID;
+    }
+    return kv_writeback_packed(k_blk, v_blk, n_layers, B, Hkv, Dq, d, n_acc, ctx_len, kd, vd, L_stride, n_over,
+                               stream) == cudaSuccess
+               ? VC_OK
+               : VC_ERR_CUDA;
 }
 
 vc_status vc_kv_unpack(const void *src_packed, void *dst_bf16, int64_t rows, int d, cudaStream_t stream)

@@ -59,7 +59,7 @@ class VeriCacheRunner:
 
     def __init__(self, dec: vc.Decoder, B: int, max_len: int, horizon: int, bits: int = 2, group: int = 32,
                  residual: int = 128, host_cache: bool = False, prefill_chunk: int = 512, device="cuda",
-                 fused_head: bool = True, rotate: bool = False, use_graph: bool = False):
+                 fused_head: bool = True, rotate: bool = False, use_graph: bool = False, pack_host: bool = False):
         cfg = dec.cfg
         self.dec, self.B, self.D, self.device = dec, B, horizon, device
         # use_graph: after one eager round, the round's D draft steps (about a
@@ -79,7 +79,23 @@ class VeriCacheRunner:
         self.k_full = torch.zeros(shape, dtype=self.dtype, device=device)
         self.v_full = torch.zeros_like(self.k_full)
         self.host_cache = host_cache
-        if host_cache:
+        # pack_host: the host copy is held packed (vc_kv_pack rows); each round
+        # moves the packed bytes into a device staging buffer and expands them
+        # into the full cache, and the write-back packs the committed rows
+        self.pack_host = host_cache and pack_host
+        if self.pack_host:
+            assert self.dtype == torch.bfloat16
+            pshape = shape[:-1] + (vc.vc_kv_packed_row_bytes(hd),)
+            self.k_host = torch.zeros(pshape, dtype=torch.uint8).pin_memory()
+            self.v_host = torch.zeros(pshape, dtype=torch.uint8).pin_memory()
+            self.k_pack = torch.zeros(pshape, dtype=torch.uint8, device=device)
+            self.v_pack = torch.zeros_like(self.k_pack)
+            self.n_over = torch.zeros(1, dtype=torch.int32, device=device)
+            # layer l is expanded on its own stream while layer l + 1 is on
+            # the link
+            self.unpack_stream = torch.cuda.Stream(device=device)
+            self.ev_layer = [torch.cuda.Event() for _ in range(nl)]
+        elif host_cache:
             self.k_host = torch.zeros(shape, dtype=self.dtype).pin_memory()
             self.v_host = torch.zeros(shape, dtype=self.dtype).pin_memory()
         maxg = self.L_stride // group + 1
@@ -125,12 +141,25 @@ class VeriCacheRunner:
         vc.vc_accept(last.view(B, 1, -1), None, self.n_acc, self.x, self.ws_acc)
         for l, q in enumerate(self.qc):
             vc.vc_quantize_kv(self.k_full[l], self.v_full[l], q, L=P)
-        if self.host_cache:
+        if self.pack_host:
+            vc.vc_kv_pack(self.k_full, self.k_pack, self.n_over)
+            vc.vc_kv_pack(self.v_full, self.v_pack, self.n_over)
+            self.k_host.copy_(self.k_pack)
+            self.v_host.copy_(self.v_pack)
+            self.check_packed()
+        elif self.host_cache:
             self.k_host.copy_(self.k_full)
             self.v_host.copy_(self.v_full)
         self.ctx.fill_(P)
         self.ctx_bound = P
         return self.x
+
+    def check_packed(self):
+        """Raise if a row of the packed host copy could not be packed (a row
+        with more than 7 values far below its largest one): the copy is then
+        unusable and the runner must keep the host cache as bf16."""
+        if self.pack_host and int(self.n_over.item()):
+            raise RuntimeError(f"{int(self.n_over.item())} K/V rows cannot be held packed; use pack_host=False")
 
     # ------------------------------------------------------- plain greedy --
     def greedy(self, n_new: int) -> list[list[int]]:
@@ -158,10 +187,20 @@ class VeriCacheRunner:
             self.side.wait_stream(main)
             if ev is not None:
                 ev["swap0"].record(self.side)
-            vc.vc_swap_in(self.k_full, self.k_host, stream=self.side)
-            vc.vc_swap_in(self.v_full, self.v_host, stream=self.side, done_event=self.ev_swap)
+            if self.pack_host:
+                self.unpack_stream.wait_stream(main)
+                for l in range(len(self.qc)):
+                    vc.vc_swap_in(self.k_pack[l], self.k_host[l], stream=self.side)
+                    vc.vc_swap_in(self.v_pack[l], self.v_host[l], stream=self.side, done_event=self.ev_layer[l])
+                    self.unpack_stream.wait_event(self.ev_layer[l])
+                    vc.vc_kv_unpack(self.k_pack[l], self.k_full[l], stream=self.unpack_stream)
+                    vc.vc_kv_unpack(self.v_pack[l], self.v_full[l], stream=self.unpack_stream)
+                self.ev_swap.record(self.unpack_stream)
+            else:
+                vc.vc_swap_in(self.k_full, self.k_host, stream=self.side)
+                vc.vc_swap_in(self.v_full, self.v_host, stream=self.side, done_event=self.ev_swap)
             if ev is not None:
-                ev["swap1"].record(self.side)
+                ev["swap1"].record(self.unpack_stream if self.pack_host else self.side)
         if self.use_graph and self._graph is None and self._rounds >= 1:
             self.capture_draft_graph()
         if ev is not None:
@@ -191,7 +230,10 @@ class VeriCacheRunner:
             vc.vc_accept(self.logits_v, self.drafts, self.n_acc, self.x, self.ws_acc)
         for l, q in enumerate(self.qc):
             vc.vc_qcache_commit(q, self.k_blk[l], self.v_blk[l], self.round_len, self.n_acc)
-        if self.host_cache:
+        if self.pack_host:
+            vc.vc_kv_writeback_packed(self.k_blk, self.v_blk, self.n_acc, self.round_len, self.k_host, self.v_host,
+                                      self.n_over)
+        elif self.host_cache:
             vc.vc_kv_writeback(self.k_blk, self.v_blk, self.n_acc, self.round_len, self.k_host, self.v_host)
         if ev is not None:
             ev["c1"].record(main)
@@ -241,6 +283,7 @@ class VeriCacheRunner:
         while min(have) < n_new and r < max_rounds:
             self.round(log, r)
             na = log.n_acc[r].cpu().tolist()
+            self.check_packed()              # before the next round's swap reads the host copy
             have = [h + k + 1 for h, k in zip(have, na)]
             r += 1
         used = RoundLog(log.drafts[:r], log.n_acc[:r], log.nxt[:r])

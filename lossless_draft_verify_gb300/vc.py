@@ -163,6 +163,8 @@ def load() -> ctypes.CDLL:
     L.vc_kv_pack.argtypes = [P, P, c_int64, c_int, P, P]
     L.vc_kv_unpack.restype = c_int
     L.vc_kv_unpack.argtypes = [P, P, c_int64, c_int, P]
+    L.vc_kv_writeback_packed.restype = c_int
+    L.vc_kv_writeback_packed.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, P, P, P, P, c_int, P, P]
     _lib = L
     return L
 
@@ -177,7 +179,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits",
             "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe",
             "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify",
-            "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack"]
+            "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack", "vc_kv_writeback_packed"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -602,6 +604,17 @@ def vc_kv_unpack(src: torch.Tensor, dst: torch.Tensor, stream=None):
     assert dst.dtype == torch.bfloat16 and dst.is_contiguous() and src.dtype == torch.uint8 and src.is_contiguous()
     assert src.numel() == rows * vc_kv_packed_row_bytes(d)
     _check(load().vc_kv_unpack(src.data_ptr(), dst.data_ptr(), rows, d, _stream(stream)), "vc_kv_unpack")
+
+
+def vc_kv_writeback_packed(k_blk, v_blk, n_acc, ctx_len, k_host_packed, v_host_packed, n_over=None, stream=None):
+    """k_blk/v_blk bf16 [n_layers][B][Hkv][Dq][d] (device); the host copies
+    pinned uint8 [n_layers][B][Hkv][L_stride][16 + 3d/2]."""
+    nl, B, hkv, dq, d = k_blk.shape
+    L_stride = k_host_packed.shape[3]
+    assert k_host_packed.shape == (nl, B, hkv, L_stride, vc_kv_packed_row_bytes(d)) == v_host_packed.shape
+    _check(load().vc_kv_writeback_packed(k_blk.data_ptr(), v_blk.data_ptr(), nl, B, hkv, dq, d, n_acc.data_ptr(),
+                                         ctx_len.data_ptr(), k_host_packed.data_ptr(), v_host_packed.data_ptr(),
+                                         L_stride, _ptr(n_over), _stream(stream)), "vc_kv_writeback_packed")
 
 
 def vc_swap_in_paced(dst: torch.Tensor, src_pinned: torch.Tensor, gbps: float, pace_ws: torch.Tensor,

@@ -132,12 +132,13 @@ def test_bf16_block_forward_equals_row_by_row():
     assert torch.isfinite(blk.float()).all()
 
 
-@pytest.mark.parametrize("host_cache,fused_head,rotate,graph", [(True, True, False, False),
-                                                             (False, True, False, False),
-                                                             (False, False, False, False),
-                                                             (False, True, True, False),
-                                                             (True, True, False, True)])
-def test_bf16_draft_and_verify_equals_greedy(host_cache, fused_head, rotate, graph):
+@pytest.mark.parametrize("host_cache,fused_head,rotate,graph,pack", [(True, True, False, False, False),
+                                                                  (False, True, False, False, False),
+                                                                  (False, False, False, False, False),
+                                                                  (False, True, True, False, False),
+                                                                  (True, True, False, True, False),
+                                                                  (True, True, False, True, True)])
+def test_bf16_draft_and_verify_equals_greedy(host_cache, fused_head, rotate, graph, pack):
     vc = lib()
     from lossless_draft_verify_gb300 import decode
     cfg, dec = _small_decoder(vc, seed=1)
@@ -148,9 +149,11 @@ def test_bf16_draft_and_verify_equals_greedy(host_cache, fused_head, rotate, gra
     ref_run.prefill(prompt)
     ref = ref_run.greedy(n_new)
     run = decode.VeriCacheRunner(dec, B, P + n_new + 2 * D, D, bits=2, residual=128, host_cache=host_cache,
-                                 prefill_chunk=256, fused_head=fused_head, rotate=rotate, use_graph=graph)
+                                 prefill_chunk=256, fused_head=fused_head, rotate=rotate, use_graph=graph,
+                                 pack_host=pack)
     run.prefill(prompt)
     toks, acc = run.generate(n_new)
+    assert run.pack_host == pack
     assert (run._graph is not None) == graph
     assert toks == ref
     assert _status_ok(vc, run.ws) and _status_ok(vc, ref_run.ws)

@@ -85,3 +85,35 @@ def test_full_round_cache_round_trip():
     want, over = oracle.kv_pack_rows(_bits(rows))
     np.testing.assert_array_equal(p.view(-1, 208)[idx].cpu().numpy(), want)
     assert not over.any()
+
+
+def test_writeback_packed_matches_oracle():
+    """The packed write-back stores exactly the oracle's packing of the
+    committed rows (i <= n_acc[b]) at ctx[b] + i, every layer, K and V, and
+    leaves every other row of the host copy untouched."""
+    vc = lib()
+    nl, B, hkv, dq, d, Ls = 2, 3, 2, 9, 128, 40
+    g = torch.Generator().manual_seed(11)
+    kb = torch.randn(nl, B, hkv, dq, d, generator=g).to(torch.bfloat16).cuda()
+    vb = torch.randn(nl, B, hkv, dq, d, generator=g).to(torch.bfloat16).cuda()
+    n_acc = torch.tensor([0, 8, 3], dtype=torch.int32, device="cuda")
+    ctx = torch.tensor([5, 31, 20], dtype=torch.int32, device="cuda")      # sequence 1 runs past L_stride
+    rb = vc.vc_kv_packed_row_bytes(d)
+    kh = torch.full((nl, B, hkv, Ls, rb), 0xA5, dtype=torch.uint8).pin_memory()
+    vh = torch.full((nl, B, hkv, Ls, rb), 0x5A, dtype=torch.uint8).pin_memory()
+    n_over = torch.zeros(1, dtype=torch.int32, device="cuda")
+    vc.vc_kv_writeback_packed(kb, vb, n_acc, ctx, kh, vh, n_over)
+    torch.cuda.synchronize()
+    assert int(n_over.item()) == 0
+    want_k = np.full(kh.shape, 0xA5, np.uint8)
+    want_v = np.full(vh.shape, 0x5A, np.uint8)
+    kbits, vbits = _bits(kb), _bits(vb)
+    for b in range(B):
+        for i in range(int(n_acc[b]) + 1):
+            pos = int(ctx[b]) + i
+            if pos >= Ls:
+                continue
+            want_k[:, b, :, pos] = oracle.kv_pack_rows(kbits[:, b, :, i].reshape(-1, d))[0].reshape(nl, hkv, rb)
+            want_v[:, b, :, pos] = oracle.kv_pack_rows(vbits[:, b, :, i].reshape(-1, d))[0].reshape(nl, hkv, rb)
+    np.testing.assert_array_equal(kh.numpy(), want_k)
+    np.testing.assert_array_equal(vh.numpy(), want_v)
