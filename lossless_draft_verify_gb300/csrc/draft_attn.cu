@@ -535,6 +535,7 @@ draft_kivi_kernel(KiviParams P)
                 const uint8_t *zv_src = gid < NG ? recB + Gm::VM + 2 * D : zeros;
                 group_values<BITS, D>(recB, zv_src, pb[1], lane, tig, o_acc, vb_acc);
             }
+            fence_async_smem();                  // this stage's reads before its bulk refill
             __syncwarp();
             if (lane == 0 && it + NST < n_mine) issue(st, it + NST);
         }
@@ -629,6 +630,7 @@ draft_kivi_kernel(KiviParams P)
         int phase = 0;
         for (int t0 = t_lo; t0 < t_hi; t0 += CHUNK) {
             const int nt = min(CHUNK, t_hi - t0);
+            fence_async_smem();                  // the previous chunk's reads before the refill
             __syncthreads();                     // the staging bytes are free (and the barrier is set up)
             if (threadIdx.x == 0) {
                 mbar_arrive_expect_tx(resbar, 2u * nt * ROW);
@@ -833,6 +835,7 @@ draft_dense_kernel(DenseParams P)
                 for (int i = 0; i < CPL; ++i) o[h][i] = fmaf(ph, vx[i], o[h][i]);
             }
         }
+        fence_async_smem();                      // this stage's reads before its bulk refill
         __syncwarp();
         if (lane == 0 && it + DENSE_NST < n_mine) issue(st, t_lo + warp + (it + DENSE_NST) * NW);
     }
@@ -1045,6 +1048,7 @@ draft_dense_mma_kernel(DenseParams P)
             ldsm_x4_trans(a, vt + v_tok * Gm::PITCH + (16 * mt + v_col) * 2);
             mma16816_bf16(o_acc[mt], a, b0, b1);
         }
+        fence_async_smem();                      // this stage's reads before its bulk refill
         __syncwarp();
         if (it + DM_NST < n_mine) issue(st, t_lo + warp + (it + DM_NST) * NW);
     }

@@ -119,6 +119,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     }
 }
 
+// Order this thread's generic-proxy accesses of shared memory before later
+// async-proxy accesses (bulk copies, TMA): every thread that read a buffer
+// with ordinary loads fences before the buffer is released to a refill.
+__device__ __forceinline__ void fence_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ----- bulk (non-tensor) asynchronous copy global -> shared ---------------------
 // dst/src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)

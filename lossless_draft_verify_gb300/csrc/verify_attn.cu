@@ -364,6 +364,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     ldsm_x4(swz_chunk(sK, key, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
                     mma_bf16_16816(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                 }
+            // the stage is refilled by TMA (async proxy) once released: order
+            // this warp's generic-proxy reads of it before that
+            fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B->k_empty[s]);
             // causal mask, scale, online softmax per tail row (exp2 domain, lazy rescale)
@@ -431,6 +434,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     ldsm_x4_t(swz_chunk(sV, key, 2 * mt + (mi & 1)), a0, a1, a2, a3);
                     mma_bf16_16816(o[mt], a0, a1, a2, a3, pb[kk][0], pb[kk][1]);
                 }
+            fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B->v_empty[s]);
         }
