@@ -65,9 +65,9 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("00eae9dd7822e2ca0a3a520a1680169c665782b60bcff0791d87d56648604bb6",
-               "5b85f3f8926d2a9eefa983caccea75742e2bcb3ec2f800acaf19894af45839ab"),
-    "bytes": 411.005696e6 + 4.248576e6,
+    "sha256": ("1133aaa237b78a74938a04b4aa734bc8f154c0223b75967a1432cbc0c42315f3",
+               "498f141e6a649946e153bbc76388c9bd507c1e9bc1db9e8beba8c9cf141a87cc"),
+    "bytes": 411.009280e6 + 4.302336e6,
     "algorithmic_bytes": 409731072,
 }
 
