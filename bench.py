@@ -762,7 +762,7 @@ def run_model(args, dev, rank, world, barrier, pg):
             "kernels": kernels,
             "accepted_per_round_mean": float(n_acc.float().mean()), "tokens_per_round": tokens / args.steps,
             "prefill_s": round(t_pf, 2), "status": st, "lossless_check": check,
-            "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc) * args.steps,
+            "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc, packed) * args.steps,
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, max_len, packed),
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": None,
@@ -770,11 +770,12 @@ def run_model(args, dev, rank, world, barrier, pg):
         print(json.dumps(line), flush=True)
 
 
-def model_launches_per_round(cfg, vc) -> int:
+def model_launches_per_round(cfg, vc, packed: bool = False) -> int:
     """Kernels the library launches in one round of the model workload,
     counted from the decoder's sequencing.  A GEMM with more than one K split
     adds a reduction launch when its grid has more than 64 output tiles (fewer
-    tiles, or the LM head's argmax epilogue, sum the splits inside the GEMM)."""
+    tiles, or the LM head's argmax epilogue, sum the splits inside the GEMM).
+    A packed host cache adds the expansion of K and V per layer."""
     qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
     shapes = [(qd + 2 * kvd, cfg.d_model), (cfg.d_model, qd), (2 * cfg.d_ff, cfg.d_model), (cfg.d_model, cfg.d_ff)]
 
@@ -793,7 +794,7 @@ def model_launches_per_round(cfg, vc) -> int:
     # embed, layers (verify attention + its combine), rmsnorm, LM head (argmax), acceptance, status fold
     verify = 1 + cfg.n_layers * layer(rows_v, False, 2) + 1 + g(rows_v, cfg.vocab, cfg.d_model, False, True) + 2
     # + the commit (one append per layer) and the host write-back
-    return M_HORIZON * draft + verify + cfg.n_layers + 1
+    return M_HORIZON * draft + verify + cfg.n_layers + 1 + (2 * cfg.n_layers if packed else 0)
 
 
 def run_bytes(cfg, max_len, packed: bool = False) -> int:
