@@ -426,7 +426,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "parallelism": "cpu oracle (OpenMP over kv units)",
+            "config": {"workload": WORKLOAD_PACKED, "parallelism": "cpu oracle (OpenMP over kv units)",
                        "global_batch": B, "seq_len": CTX},
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": f"{n_seq} of {B} sequences per step, time scaled by {B * HKV}/{units}"},
