@@ -124,11 +124,6 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
 }
 
-// Generic-proxy shared-memory writes -> visible to the async proxy (MMA operands).
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 }  // namespace tc
 }  // namespace vc

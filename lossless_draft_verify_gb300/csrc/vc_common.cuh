@@ -120,8 +120,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Order this thread's generic-proxy accesses of shared memory before later
-// async-proxy accesses (bulk copies, TMA): every thread that read a buffer
-// with ordinary loads fences before the buffer is released to a refill.
+// async-proxy accesses (bulk copies, TMA, tcgen05 operand reads): every thread
+// that read a buffer with ordinary loads fences before the buffer is released
+// to a refill, and every thread that wrote an MMA operand before it is handed
+// to the tensor cores.
 __device__ __forceinline__ void fence_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

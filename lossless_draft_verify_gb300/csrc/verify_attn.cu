@@ -553,7 +553,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 v.w = pk[kb * 4 + 3];
                 *reinterpret_cast<uint4 *>(sP + ((r >> 3) * 8 + kb) * 128 + (r & 7) * 16) = v;
             }
-            tc::fence_proxy_async_smem();
+            fence_async_smem();                  // P (generic writes) before the MMA reads it
             tc::fence_before();
             mbar_arrive(&B->p_ready[t]);
         }
