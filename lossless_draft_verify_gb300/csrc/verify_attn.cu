@@ -16,8 +16,14 @@
 //               mask, exp2 online softmax with lazy rescaling of O (in TMEM),
 //               P written to shared memory as bf16 in the canonical K-major
 //               layout for the next MMA.
+// Tail mode (a second tile of at most 8 rows, e.g. Dq = 33 with 4 heads per
+// kv head): warp 0 lane 1 issues the MMAs and warp 1 computes the tail rows
+// with mma.sync on the same K/V stages, read by ldmatrix; it fences those
+// generic-proxy reads (fence.proxy.async) before releasing a stage to the
+// TMA refill.
 // Every mbarrier wait is bounded; a timeout is recorded in the workspace
-// status block and the CTA drains out.  Split partials (m, l, o) go to the
+// status block and the CTA drains out.  Kernels wait on griddepcontrol.wait
+// before their first global access (programmatic dependent launch).  Split partials (m, l, o) go to the
 // workspace and a combine kernel writes the normalised output.
 //
 // CUDA-core path (fp32, or shapes outside the tensor-core kernel): one warp per
