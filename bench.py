@@ -65,8 +65,8 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("1133aaa237b78a74938a04b4aa734bc8f154c0223b75967a1432cbc0c42315f3",
-               "498f141e6a649946e153bbc76388c9bd507c1e9bc1db9e8beba8c9cf141a87cc"),
+    "sha256": ("99eb3fc6059e49b37c09a309d3ad46c49093c9550d43b79d9efe180e1ce893ff",
+               "10b95006df417026b33954ac060b27c984605c2a56c9c3179717bb6732c17edb"),
     "bytes": 411.009280e6 + 4.302336e6,
     "algorithmic_bytes": 409731072,
 }

@@ -23,6 +23,11 @@
 // bf16 caches use the same MMA structure with the K/V tiles as operands
 // (ldmatrix from padded rows); fp32 caches use CUDA-core math over 32-token
 // tiles staged by cp.async.bulk.
+//
+// Every ring stage is read with ordinary loads and refilled by a bulk copy
+// (async proxy): each reading lane fences (fence.proxy.async) before the
+// stage is released.  The kernels wait on griddepcontrol.wait before their
+// first global access (programmatic dependent launch).
 #include <algorithm>
 
 #include "vc_common.cuh"
