@@ -182,7 +182,11 @@ class Round:
             n_over = torch.zeros(1, dtype=torch.int32, device=dev)
             vc.vc_kv_pack(self.kfull, self.kpack, n_over)
             vc.vc_kv_pack(self.vfull, self.vpack, n_over)
-            assert int(n_over.item()) == 0, "rows the packed format cannot hold"
+            if int(n_over.item()):
+                # some row needs more than 7 escapes: this cache travels as bf16
+                packed = self.packed = False
+                del self.kpack, self.vpack
+        if packed:
             self.kpack_host = self.kpack.cpu().pin_memory()
             self.vpack_host = self.vpack.cpu().pin_memory()
             # expansion runs on a stream of its own, so the link's copies stay
