@@ -624,7 +624,7 @@ def run_model(args, dev, rank, world, barrier, pg):
     n_tr = 2                                  # eager rounds for the per-operation trace
     total = args.warmup + n_tr + args.steps + n_e2e
     max_len = P + total * (M_HORIZON + 1) + 64
-    packed = args.swap == "packed"              # default raw
+    packed = args.swap != "raw"                 # default packed
     run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=args.bits, residual=M_RESIDUAL, host_cache=True,
                                  prefill_chunk=512, device=dev, rotate=args.rotate, pack_host=packed)
     prompt = inputs.random_prompts(M_B, P, cfg.vocab, seed=rank, device=dev)
@@ -946,9 +946,7 @@ def main():
                     help="round workload: swap and verify per half batch (2) or whole batch (1)")
     ap.add_argument("--swap", default=None, choices=["packed", "raw"],
                     help="the full cache on the host packed (lossless rows of 16 + 3d/2 bytes, expanded on the "
-                         "GPU after each swap) or as plain bf16; default packed for the round (its swap outlasts "
-                         "drafting), raw for the model (at 32k drafting takes as long as the bf16 swap, and the "
-                         "expansion would slow drafting)")
+                         "GPU after each swap; the default) or as plain bf16")
     ap.add_argument("--workload", default="round", choices=["round", "model"],
                     help="round: one layer's hot path at 32k (B16); model: the 8-layer decoder end to end")
     ap.add_argument("--prompt", type=int, default=32768, help="prompt tokens per sequence (--workload model)")
