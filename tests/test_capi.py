@@ -148,3 +148,13 @@ def test_kv_pack_validation_on_the_host(libvc):
     assert L.vc_kv_unpack(fake + 8, fake, 4, 64, None) == vc.VC_ERR_INVALID
     assert L.vc_kv_unpack(fake, fake, 4, 32, None) == vc.VC_ERR_UNSUPPORTED
     assert L.vc_kv_unpack(None, None, 0, 64, None) == vc.VC_OK
+
+
+def test_kv_packed_row_size_agrees_with_the_oracle(libvc):
+    """The library's packed row size and the oracle's format give the same
+    bytes per row (both stated independently)."""
+    import oracle
+    from lossless_draft_verify_gb300 import vc
+    L = vc.load()
+    for d in (64, 128):
+        assert L.vc_kv_packed_row_bytes(d) == oracle.kv_packed_row_bytes(d)
