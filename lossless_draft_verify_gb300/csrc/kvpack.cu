@@ -163,7 +163,7 @@ kv_unpack_kernel(const uint8_t *__restrict__ src, uint16_t *__restrict__ dst, lo
 {
     using Gm = PackGeom<D>;
     constexpr int VPL = Gm::VPL;
-    constexpr int RPI = 4;
+    constexpr int RPI = 8;
     const int lane = threadIdx.x & 31;
     const long long w0 = (long long)blockIdx.x * (kPackThreads / 32) + (threadIdx.x >> 5);
     const long long nw = (long long)gridDim.x * (kPackThreads / 32);
@@ -242,7 +242,7 @@ cudaError_t kv_pack(const void *src, void *dst, long long rows, int d, int32_t *
 cudaError_t kv_unpack(const void *src, void *dst, long long rows, int d, cudaStream_t st)
 {
     if (rows <= 0) return cudaSuccess;
-    const unsigned g = pack_grid(rows, 4);
+    const unsigned g = pack_grid(rows, 8);
     if (d == 128)
         kv_unpack_kernel<128><<<g, kPackThreads, 0, st>>>((const uint8_t *)src, (uint16_t *)dst, rows);
     else
