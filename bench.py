@@ -632,6 +632,7 @@ def run_model(args, dev, rank, world, barrier, pg):
     run.prefill(prompt)
     torch.cuda.synchronize()
     t_pf = time.perf_counter() - t_pf
+    packed = run.pack_host                  # False if a prompt row could not be packed
     first = run.x.cpu().tolist()
     log = run.new_log(total)
     for r in range(args.warmup):

@@ -144,10 +144,16 @@ class VeriCacheRunner:
         if self.pack_host:
             vc.vc_kv_pack(self.k_full, self.k_pack, self.n_over)
             vc.vc_kv_pack(self.v_full, self.v_pack, self.n_over)
-            self.k_host.copy_(self.k_pack)
-            self.v_host.copy_(self.v_pack)
-            self.check_packed()
-        elif self.host_cache:
+            if int(self.n_over.item()):
+                # a prompt row the packed format cannot hold: keep a bf16 host copy
+                self.pack_host = False
+                del self.k_pack, self.v_pack, self.unpack_stream, self.ev_layer
+                self.k_host = torch.empty(self.k_full.shape, dtype=self.dtype).pin_memory()
+                self.v_host = torch.empty(self.v_full.shape, dtype=self.dtype).pin_memory()
+            else:
+                self.k_host.copy_(self.k_pack)
+                self.v_host.copy_(self.v_pack)
+        if self.host_cache and not self.pack_host:
             self.k_host.copy_(self.k_full)
             self.v_host.copy_(self.v_full)
         self.ctx.fill_(P)
@@ -155,9 +161,10 @@ class VeriCacheRunner:
         return self.x
 
     def check_packed(self):
-        """Raise if a row of the packed host copy could not be packed (a row
-        with more than 7 values far below its largest one): the copy is then
-        unusable and the runner must keep the host cache as bf16."""
+        """Raise if a committed row could not be packed into the host copy (a
+        row with more than 7 values far below its largest one): the copy is
+        then unusable.  (A prompt row that cannot be packed makes prefill keep a
+        bf16 host copy instead.)"""
         if self.pack_host and int(self.n_over.item()):
             raise RuntimeError(f"{int(self.n_over.item())} K/V rows cannot be held packed; use pack_host=False")
 
