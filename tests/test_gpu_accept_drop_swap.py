@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from lossless_draft_verify_gb300 import inputs
-from helpers import f32, lib
+from helpers import f32, lib, plain_accept_case
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +59,37 @@ def test_accept_full_size():
     assert nx.tolist() == wnx.tolist()
 
 
+def test_accept_full_size_plain_normal_with_cross_split_ties():
+    """[16, 33, 151936] bf16 ~ N(0,1), drafts from the oracle's argmax: the
+    natural ties of bf16 rows and the planted ties across splits (equal maxima,
+    -0 against +0) must all resolve to the lowest index, bit for bit."""
+    vc = lib()
+    lg, drafts, k = plain_accept_case(16, 32, 151936, seed=3)
+    host = f32(lg)
+    top = host.max(axis=2, keepdims=True)
+    assert ((host == top).sum(axis=2) > 1).sum() >= 8          # natural ties present
+    n, nx = _accept(vc, lg, drafts)
+    wn, wnx, _ = oracle.accept(host, drafts.cpu().numpy())
+    assert n.tolist() == wn.tolist() == k.tolist()
+    assert nx.tolist() == wnx.tolist()
+
+
+def test_accept_two_splits_with_ties():
+    """V = 40000 (two splits): integer-valued logits, so the row maximum is
+    tied across both splits in most rows."""
+    vc = lib()
+    g = torch.Generator().manual_seed(9)
+    B, D, V = 6, 12, 40000
+    lg = torch.randint(-40, 8, (B, D + 1, V), generator=g).to(torch.bfloat16)
+    _, _, am = oracle.accept(f32(lg), np.zeros((B, D), np.int32))
+    drafts = torch.randint(0, V, (B, D), generator=g, dtype=torch.int32)
+    for b in range(B):
+        drafts[b, :2 * b + 1] = torch.from_numpy(am[b, :2 * b + 1])
+    n, nx = _accept(vc, lg.cuda(), drafts.cuda())
+    wn, wnx, _ = oracle.accept(f32(lg), drafts.numpy())
+    assert n.tolist() == wn.tolist() and nx.tolist() == wnx.tolist()
+
+
 # --------------------------------------------------------------- drop ----
 
 def _drop(vc, scores, k, v, keep_top, keep_recent):
@@ -76,6 +107,7 @@ def _drop(vc, scores, k, v, keep_top, keep_recent):
 @pytest.mark.parametrize("B,H,L,top,recent,ties", [
     (2, 3, 10000, 2500, 256, False),
     (1, 2, 9000, 1000, 100, True),      # heavy ties: resolved by position
+    (2, 2, 12000, 4000, 64, "zeros"),   # -0 and +0 at the threshold: equal scores
     (1, 1, 300, 1000, 50, False),       # keep every candidate
     (1, 1, 300, 0, 50, False),          # recent window only
     (1, 1, 40, 10, 100, False),         # window covers the sequence
@@ -83,7 +115,12 @@ def _drop(vc, scores, k, v, keep_top, keep_recent):
 def test_drop_matches_oracle(B, H, L, top, recent, ties):
     vc = lib()
     d = 128
-    if ties:
+    if ties == "zeros":
+        g = torch.Generator().manual_seed(6)
+        scores = torch.randint(-1, 2, (B, H, L), generator=g).to(torch.float32)
+        neg = torch.rand(B, H, L, generator=g) < 0.5
+        scores = torch.where((scores == 0) & neg, torch.tensor(-0.0), scores).cuda()
+    elif ties:
         g = torch.Generator().manual_seed(2)
         scores = torch.randint(0, 20, (B, H, L), generator=g).to(torch.float32).cuda()
     else:
