@@ -27,7 +27,9 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 // larger score -> smaller key (so the kept set is the smallest keys)
 __device__ __forceinline__ uint32_t desc_key(float s)
 {
-    uint32_t u = __float_as_uint(s);
+    // -0 and +0 are the same score: both map to the key of +0, so a tie
+    // between them is broken by position like any other tie
+    uint32_t u = (s == 0.f) ? 0u : __float_as_uint(s);
     uint32_t asc = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     return ~asc;
 }
