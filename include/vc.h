@@ -86,7 +86,7 @@ vc_status vc_poll_status(void *ws, cudaStream_t stream);
  * vc_wait_probe -- exercises the failure path of the bounded waits (no
  * counterpart in the paper; it makes that path testable without faulting a
  * GPU): one CTA waits on an mbarrier that nothing completes, the wait gives
- * up after its iteration limit (about a second), records a timeout in the
+ * up after 2 s of wall time, records a timeout in the
  * status block of `ws` (>= 256 bytes, 256-byte aligned) and the kernel
  * returns.  vc_poll_status(ws) then reports VC_ERR_TIMEOUT and the context
  * stays usable.
@@ -340,7 +340,9 @@ vc_status vc_verify_attn(const void *q, const void *k, const void *v, vc_dtype d
  * index on ties, -0 == +0), n = first i in [0, D) with a_i != drafts[i], else
  * D; next = a_n.  The round emits drafts[0..n-1] and next.
  * logits: device [B][D+1][V] in dt (finite values); drafts: device int32
- * [B][D]; n_acc, next_tok: device int32 [B].
+ * [B][D]; n_acc, next_tok: device int32 [B].  Limits: D <= 1024 and
+ * B * (D + 1) <= 65535 rows; larger requests return VC_ERR_INVALID and
+ * enqueue nothing.
  */
 size_t vc_accept_workspace_bytes(int B, int D, int V);
 
@@ -375,6 +377,10 @@ vc_status vc_accept_tiles(const float *tile_max, const int32_t *tile_idx, int n_
  * VC_ERR_INVALID and enqueue nothing.
  * The first call on a device (made with that device current) looks up the
  * buffer's device address; make that first call before any stream capture.
+ * The address belongs to the CUDA context the call ran in: after a
+ * cudaDeviceReset, or when the caller switches to another context on the
+ * same device, the next call looks it up again and must also be made outside
+ * a stream capture.
  * All calls on one device share the buffer, so calls that may run
  * concurrently on the GPU (different streams without ordering) race and
  * must be serialized by the caller.  Each call clears the part of the buffer
@@ -394,7 +400,9 @@ vc_status vc_accept_noalloc(const void *logits, vc_dtype dt, const int32_t *draf
  * device with one asynchronous copy on `side_stream` and, if `done` is not
  * NULL, records `done` on that stream after it; the caller makes the verify
  * stream wait on `done`.  Returns VC_ERR_INVALID if src is not page-locked
- * host memory (a pageable source would serialize the copy).
+ * host memory (a pageable source would serialize the copy), or if the range
+ * [src, src + bytes) or [dst, dst + bytes) does not end inside memory of its
+ * kind (checked at its first and last byte).
  */
 vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes,
                      cudaStream_t side_stream, cudaEvent_t done);

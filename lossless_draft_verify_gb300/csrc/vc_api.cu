@@ -13,6 +13,17 @@ inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline size_t esize(vc_dtype dt) { return dt == VC_BF16 ? 2 : 4; }
 inline bool dtype_ok(vc_dtype dt) { return dt == VC_BF16 || dt == VC_F32; }
 inline vc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VC_OK : VC_ERR_CUDA; }
+// Largest B * (D + 1) acceptance serves: one CTA row of the grid per logit row.
+constexpr long kAcceptMaxRows = 65535;
+inline bool is_memory_type(const void *p, cudaMemoryType t)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == t;
+}
 
 bool qcache_ok(const vc_qcache *c)
 {
@@ -258,6 +269,7 @@ vc_status vc_accept(const void *logits, vc_dtype dt, const int32_t *drafts, int 
 {
     if (!logits || !n_acc || !next_tok || !ws || !dtype_ok(dt)) return VC_ERR_INVALID;
     if (B <= 0 || D < 0 || D > 1024 || V <= 0 || (D > 0 && !drafts)) return VC_ERR_INVALID;
+    if ((long)B * (D + 1) > kAcceptMaxRows) return VC_ERR_INVALID;
     if (!aligned(ws, 256) || ws_bytes < accept_ws_bytes(B, D, V)) return VC_ERR_INVALID;
     return cuda_status(accept(logits, dt, drafts, B, D, V, n_acc, next_tok, ws, stream));
 }
@@ -287,6 +299,10 @@ vc_status vc_swap_in_paced(void *dst_dev, const void *src_pinned_host, size_t by
         cudaGetLastError();
         return VC_ERR_INVALID;
     }
+    if (bytes && (!is_memory_type((const uint8_t *)src_pinned_host + bytes - 1, cudaMemoryTypeHost) ||
+                  !is_memory_type(dst_dev, cudaMemoryTypeDevice) ||
+                  !is_memory_type((const uint8_t *)dst_dev + bytes - 1, cudaMemoryTypeDevice)))
+        return VC_ERR_INVALID;
     const double ns_per_byte = 1.0 / gbps;            // GB/s = bytes per ns
     const uint64_t max_ns = 30000000000ull;           // no chunk waits past 30 s
     uint64_t *t0 = (uint64_t *)pace_ws;
@@ -318,6 +334,9 @@ vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes, c
         cudaGetLastError();
         return VC_ERR_INVALID;
     }
+    if (bytes && (!is_memory_type((const uint8_t *)src_pinned_host + bytes - 1, cudaMemoryTypeHost) ||
+                  !is_memory_type((const uint8_t *)dst_dev + bytes - 1, cudaMemoryTypeDevice)))
+        return VC_ERR_INVALID;                                 // the range leaves the allocation
     if (bytes) {
         cudaError_t e = cudaMemcpyAsync(dst_dev, src_pinned_host, bytes, cudaMemcpyHostToDevice, side_stream);
         if (e != cudaSuccess) return VC_ERR_CUDA;

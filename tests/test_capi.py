@@ -62,6 +62,11 @@ def test_invalid_arguments_are_rejected_on_the_host(libvc):
     assert L.vc_verify_attn(None, None, None, 0, None, 1, 1, 4, 2, 128, 64, 0, 1.0, None, None, 0,
                             None) == vc.VC_ERR_INVALID
     assert L.vc_swap_in(None, None, 16, None, None) == vc.VC_ERR_INVALID
+    fake = 1 << 20
+    # one grid row per logit row: B * (D + 1) beyond 65535 is refused up front
+    assert L.vc_accept(fake, 0, fake, 64, 1024, 8, fake, fake, fake, 1 << 30, None) == vc.VC_ERR_INVALID
+    assert L.vc_accept_noalloc(fake, 0, fake, 1025, 0, 8, fake, fake, None) == vc.VC_ERR_INVALID
+    assert L.vc_accept_noalloc(fake, 0, fake, 17, 1023, 8, fake, fake, None) == vc.VC_ERR_INVALID
     assert L.vc_workspace_init(None, 0, None) == vc.VC_ERR_INVALID
 
 
