@@ -12,11 +12,18 @@
 // GPU that loads the library holds it until the process exits.  Host code
 // cannot use the array's name as a device address, so the first call on a
 // device (with that device current) looks up its address with
-// cudaGetSymbolAddress and caches it.  All calls on a device share the one
+// cudaGetSymbolAddress and caches it.  The address belongs to the CUDA
+// context the module was loaded in, so the cache is keyed on the unique id
+// of the calling thread's current context: after a cudaDeviceReset, or from
+// another context on the same device, the next call looks the address up
+// again (and that call, like the first, must not be inside a stream
+// capture).  All calls on a device share the one
 // buffer: two calls that overlap on the GPU (different streams, no ordering)
 // race on it.  The per-sequence counters that must start at zero are cleared
 // on the stream by every call; the rest of the buffer keeps whatever the last
 // call left there and is fully rewritten before it is read.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "vc_common.cuh"
@@ -35,9 +42,52 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_accept_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+struct Cached {
+    unsigned long long ctx_id;
+    void *ptr;
+};
+Cached g_cache[kMaxDevices] = {};
 
-// Device address of the scratch buffer on the current device (looked up once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// Driver entry points for the current context and its process-unique id,
+// obtained through the runtime (no link-time dependency on libcuda).
+bool driver_fns(CtxGetCurrentFn *cur, CtxGetIdFn *id)
+{
+    static std::once_flag once;
+    static CtxGetCurrentFn f_cur = nullptr;
+    static CtxGetIdFn f_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r1) == cudaSuccess &&
+            r1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) == cudaSuccess &&
+            r2 == cudaDriverEntryPointSuccess) {
+            f_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+            f_id = reinterpret_cast<CtxGetIdFn>(q);
+        } else {
+            cudaGetLastError();
+        }
+    });
+    *cur = f_cur;
+    *id = f_id;
+    return f_cur && f_id;
+}
+
+// Unique id of the calling thread's current context, 0 if there is none yet.
+unsigned long long current_ctx_id(CtxGetCurrentFn cur, CtxGetIdFn id)
+{
+    CUcontext c = nullptr;
+    unsigned long long v = 0;
+    if (cur(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    if (id(c, &v) != CUDA_SUCCESS) return 0;
+    return v;
+}
+
+// Device address of the scratch buffer in the current device's current
+// context (looked up once per context).
 vc_status scratch_for_current_device(void **out)
 {
     int dev = 0;
@@ -46,16 +96,24 @@ vc_status scratch_for_current_device(void **out)
         return VC_ERR_CUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return VC_ERR_UNSUPPORTED;
+    CtxGetCurrentFn cur;
+    CtxGetIdFn idf;
+    if (!driver_fns(&cur, &idf)) return VC_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return VC_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
+    const unsigned long long id = current_ctx_id(cur, idf);
+    if (id != 0 && g_cache[dev].ptr && g_cache[dev].ctx_id == id) {
+        *out = g_cache[dev].ptr;
+        return VC_OK;
     }
-    *out = g_scratch_ptr[dev];
+    // First call in this context (or the runtime has not made one current
+    // yet): the lookup loads the module and binds the device's context.
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return VC_ERR_CUDA;
+    }
+    g_cache[dev] = Cached{current_ctx_id(cur, idf), p};
+    *out = p;
     return VC_OK;
 }
 

@@ -48,6 +48,39 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         assert got_n.cpu().tolist() == case.diverge.tolist()
 
 
+def test_noalloc_plain_normal_logits_with_cross_split_ties():
+    """Config-3 logits as stated (bf16 ~ N(0,1), natural ties at the row
+    maximum) with equal maxima and -0/+0 planted in different slices of a
+    row: the allocation-free call agrees with vc_accept and the oracle."""
+    import oracle
+    from helpers import f32, plain_accept_case
+    vc = lib()
+    lg, drafts, k = plain_accept_case(16, 32, 151936, seed=21)
+    case = inputs.AcceptCase(lg, drafts, torch.as_tensor(k, dtype=torch.int32), None)
+    for _ in range(2):
+        got_n, got_next = _without_workspace(vc, case)
+        want_n, want_next = _with_workspace(vc, case)
+        torch.cuda.synchronize()
+        assert torch.equal(got_n, want_n) and torch.equal(got_next, want_next)
+    wn, wnx, _ = oracle.accept(f32(lg), drafts.cpu().numpy())
+    assert got_n.cpu().tolist() == wn.tolist() == k.tolist()
+    assert got_next.cpu().tolist() == wnx.tolist()
+
+
+def test_noalloc_at_its_exact_limit():
+    """B = 1024 sequences and B * (D + 1) = 16384 rows at a vocabulary that
+    takes the most scratch (4 slices per row): the largest request the static
+    buffer serves, checked against vc_accept."""
+    vc = lib()
+    case = inputs.accept_case(1024, 15, 65536, seed=13, device="cuda")
+    for _ in range(2):
+        got_n, got_next = _without_workspace(vc, case)
+        want_n, want_next = _with_workspace(vc, case)
+        torch.cuda.synchronize()
+        assert torch.equal(got_n, want_n) and torch.equal(got_next, want_next)
+    assert got_n.cpu().tolist() == case.diverge.tolist()
+
+
 def test_noalloc_rejects_requests_beyond_its_buffer():
     vc = lib()
     big = torch.zeros(1025, 1, 8, dtype=torch.bfloat16, device="cuda")
