@@ -1,20 +1,25 @@
 """Benchmark of the draft-and-verify hot path on GB300.
 
-One step = one VeriCache round over a synthetic 32k-context batch (16
-sequences, 32 query / 8 kv heads, head dim 128):
-  side stream: swap the full bf16 KV cache (2.15 GB) in from pinned host memory,
-               one half batch after the other (--stagger 2, the default): the
-               verify of the first half overlaps the swap of the second, and a
-               half's next swap waits only for this step's verify of that half;
-  main stream: 32 draft steps, each appending one token to the 2-bit KIVI cache
-               and running draft attention over it (HBM-bound);
-               wait for the swap; verify attention of the 33-token block over
-               the full cache (tensor cores); greedy acceptance over
-               [16, 33, 151936] bf16 logits; commit the accepted tokens to the
-               compressed cache (roll back, append, re-quantize).
-Metric: lossless tokens/s = accepted + bonus tokens per round / round time.
-The per-kernel numbers (draft-attention HBM GB/s, verify tensor-core use) are
-reported next to it with their roofline fractions.
+Default (--workload model): one step = one VeriCache round of an 8-layer GQA
+decoder (d_model 4096, 32/8 heads, head dim 128, SwiGLU 14336, vocab 32000,
+bf16 random-init weights) for 8 sequences with 32768-token prompts:
+  side stream: swap the full KV cache of every layer in from pinned host memory
+               (held as lossless packed rows, expanded on the GPU);
+  main stream: 32 draft steps of the model on its 2-bit KIVI caches (one CUDA
+               graph), then the verify forward of the 33-token block over the
+               full cache, greedy acceptance, the commit of the accepted rows to
+               the draft caches and their write-back to the host copy.
+Metric: lossless tokens/s = emitted tokens (accepted drafts + one per
+sequence) per round / round time.  The same line carries the full-KV baseline
+(plain greedy decoding with the cache swapped in before every token), the
+losslessness check against it with its near-tie count, the swap's measured
+overlap with drafting, the draft-attention roofline inside the decoder, and the
+per-kernel numbers of the one-layer kernel workloads at B16 (draft attention
+over the 2-bit cache, verify attention, acceptance over [16, 33, 151936]).
+
+--workload round: one layer's hot path at 32k for 16 sequences (swap, 32 draft
+attention steps, verify attention, acceptance over planted logits, commit).
+--kernel NAME: one kernel alone at its own workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Multi-GPU (torchrun): independent replicas, one per GPU, weak scaling.
@@ -415,6 +420,9 @@ def cpu_baseline_record(rnd, tokens_per_round):
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    if args.workload == "model":
+        run_reference_model(args, world)
+        return
     from lossless_draft_verify_gb300 import inputs
     n_seq = sample_seqs()
     case = inputs.accept_case(B, HORIZON, VOCAB, seed=0)
@@ -434,6 +442,37 @@ def run_reference(args, rank, world):
                        "global_batch": B, "seq_len": CTX},
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": f"{n_seq} of {B} sequences per step, time scaled by {B * HKV}/{units}"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_model(args, world):
+    """The oracle on the decoder workload: every step times the bounded sample
+    of model_oracle_sample (one draft row and one verify row through one
+    layer, one head row) and scales it to a round.  Tokens per round: B, one
+    per sequence, the accepted-draft count this random-init model shows at 2
+    bits on the GPU (0 per round); the timing does not depend on it."""
+    from lossless_draft_verify_gb300 import inputs
+    cfg = inputs.DecoderConfig()
+    P = args.prompt
+    sample = ModelOracleSample(cfg, P, args.bits)
+    times = []
+    for i in range(args.warmup + args.steps):
+        s = sample.time_once()
+        if i >= args.warmup:
+            times.append(model_round_seconds(cfg, s))
+    t = statistics.mean(times)
+    val = M_B / t
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (random-init weights)",
+            "config": {"workload": MODEL_WORKLOAD.format(ctx=P, bits=args.bits), "global_batch": M_B,
+                       "seq_len": P, "parallelism": "cpu oracle, one core"},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step: one draft row and one verify row through one decoder layer at "
+                                       f"{P} tokens of context and one LM-head row (oracle/model.py, fp64), scaled "
+                                       f"to a round of {M_B}x{M_HORIZON} draft and {M_B}x{M_HORIZON + 1} verify rows "
+                                       f"through {cfg.n_layers} layers; {M_B} tokens per round"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -613,6 +652,90 @@ def model_bytes(cfg) -> dict:
             "gemm_down": F * D * 2, "gemm_head": D * V * 2}
 
 
+def decoder_draft_attn_bytes(vc, cfg, ctx: float, bits: int) -> int:
+    """Algorithmic bytes of one draft-attention launch of the decoder (all B
+    sequences of one layer) at `ctx` cached tokens: the packed records of the
+    quantized prefix, the full-precision ring, q and the output."""
+    rec_b = vc.vc_record_bytes(bits, cfg.head_dim)
+    ng = int((ctx - M_RESIDUAL) // 32)
+    n_res = ctx - ng * 32
+    per_unit = ng * rec_b + 2 * n_res * cfg.head_dim * 2
+    return int(M_B * cfg.n_kv_heads * per_unit + 2 * M_B * cfg.n_heads * cfg.head_dim * 2)
+
+
+class ModelOracleSample:
+    """The oracle (oracle/model.py, fp64, as it stands) on a bounded sample of
+    one round of the decoder workload: one draft step of one sequence through
+    one decoder layer on a 2-bit KIVI draft cache of `ctx` tokens, one verify
+    row of one sequence through one layer over a full cache of `ctx` tokens,
+    and one LM-head row.  The weights are one layer of the model's shapes
+    drawn by the shared generator, the cached K/V synthetic N(0,1) of the
+    workload's shapes (the oracle's cost does not depend on the values)."""
+
+    def __init__(self, cfg, ctx: int, bits: int):
+        import dataclasses
+        from lossless_draft_verify_gb300 import inputs
+        from oracle import model as om
+        self.om, self.ctx = om, ctx
+        c1 = dataclasses.replace(cfg, n_layers=1)
+        W = inputs.decoder_weights_packed(c1, seed=0, device="cpu", dtype=torch.float32)
+        qd, kvd, F = c1.n_heads * c1.head_dim, c1.n_kv_heads * c1.head_dim, c1.d_ff
+        f = lambda t: t.double().numpy()
+        wqkv, wgu = W["wqkv"][0], W["wgu"][0]
+        weights = {"embed": f(W["embed"]), "lm_head": f(W["lm_head"]),
+                   "layers": [{"wq": f(wqkv[:, :qd]), "wk": f(wqkv[:, qd:qd + kvd]), "wv": f(wqkv[:, qd + kvd:]),
+                               "wo": f(W["wo"][0]), "wg": f(wgu[:, :F]), "wu": f(wgu[:, F:]), "wd": f(W["wd"][0])}]}
+        del W
+        self.m = om.TinyDecoder(weights, c1)
+        self.g = np.random.default_rng(0)
+        hd, nq = c1.head_dim, (ctx - M_RESIDUAL) // 32 * 32
+        self.dc = om.KiviDraftCache(self.m, bits, 32, M_RESIDUAL)
+        self.full = om.FullKV(self.m)
+        g = self.g
+        for h in range(c1.n_kv_heads):
+            self.dc.qK[0][h], self.dc.qV[0][h] = g.standard_normal((nq, hd)), g.standard_normal((nq, hd))
+            self.dc.rK[0][h] = g.standard_normal((ctx - nq, hd)).astype(np.float32)
+            self.dc.rV[0][h] = g.standard_normal((ctx - nq, hd)).astype(np.float32)
+            self.full.K[0][h], self.full.V[0][h] = g.standard_normal((ctx, hd)), g.standard_normal((ctx, hd))
+
+    def time_once(self) -> dict:
+        """Seconds per draft row-layer, verify row-layer and head row."""
+        om, m, ctx = self.om, self.m, self.ctx
+        t0 = time.perf_counter()
+        om.draft_step(m, self.dc, 1, ctx)                 # one layer + the LM head
+        t1 = time.perf_counter()
+        om.forward_block(m, self.full, [1], ctx)          # one layer + the LM head
+        t2 = time.perf_counter()
+        m.logits(self.g.standard_normal(m.cfg.d_model))
+        t3 = time.perf_counter()
+        self.dc.truncate(ctx)
+        self.full.truncate(ctx)
+        head = t3 - t2
+        return {"draft_row_layer_s": max(t1 - t0 - head, 0.0), "verify_row_layer_s": max(t2 - t1 - head, 0.0),
+                "head_row_s": head, "sample_s": t3 - t0}
+
+
+def model_round_seconds(cfg, s: dict) -> float:
+    """Oracle seconds for one round (B sequences, D draft steps through every
+    layer and the head, a (D + 1)-row verify pass through every layer and the
+    head), from the per-row sample times."""
+    nl, D = cfg.n_layers, M_HORIZON
+    return (M_B * D * (nl * s["draft_row_layer_s"] + s["head_row_s"]) +
+            M_B * (D + 1) * (nl * s["verify_row_layer_s"] + s["head_row_s"]))
+
+
+def model_cpu_record(cfg, ctx: int, bits: int, tokens_per_round: float, tokens_note: str) -> dict:
+    s = ModelOracleSample(cfg, ctx, bits).time_once()
+    t_round = model_round_seconds(cfg, s)
+    return {"value": tokens_per_round / t_round, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": (f"oracle/model.py in fp64 on one core: one draft row and one verify row through one decoder "
+                       f"layer at {ctx} tokens of context and one LM-head row "
+                       f"({s['draft_row_layer_s']:.2f} / {s['verify_row_layer_s']:.2f} / {s['head_row_s']:.2f} s), "
+                       f"scaled to a round of {M_B}x{M_HORIZON} draft rows and {M_B}x{M_HORIZON + 1} verify rows "
+                       f"through {cfg.n_layers} layers plus their head rows ({t_round:.0f} s); {tokens_note}"),
+            "sample_seconds": round(s["sample_s"], 2), "round_seconds_estimate": t_round}
+
+
 def run_model(args, dev, rank, world, barrier, pg):
     from lossless_draft_verify_gb300 import decode, inputs, replicas, vc
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
@@ -620,8 +743,8 @@ def run_model(args, dev, rank, world, barrier, pg):
     P = args.prompt
     W = inputs.decoder_weights_packed(cfg, seed=0, device=dev)
     dec = vc.Decoder.from_packed(cfg, W["embed"], W["lm_head"], W["wqkv"], W["wo"], W["wgu"], W["wd"])
-    n_e2e = 0 if args.no_e2e else 3
-    n_tr = 2                                  # eager rounds for the per-operation trace
+    n_e2e = 0 if args.no_e2e else args.steps
+    n_tr = 1                                  # traced round
     total = args.warmup + n_tr + args.steps + n_e2e
     max_len = P + total * (M_HORIZON + 1) + 64
     packed = args.swap != "raw"                 # default packed
@@ -637,13 +760,20 @@ def run_model(args, dev, rank, world, barrier, pg):
     log = run.new_log(total)
     for r in range(args.warmup):
         run.round(log, r)
-    # per-operation trace (every GEMM and attention call) of n_tr eager rounds
+    # per-operation trace (every GEMM and attention call) of one round: the
+    # draft steps are captured with tracing on, so their event pairs become
+    # nodes of a graph and time the kernels as a graph replay runs them; the
+    # verify forward is traced as issued (it is queued behind the draft graph
+    # and the swap, so the host is well ahead of the device there)
     ops_per_round = M_HORIZON * (5 * cfg.n_layers + 1) + 5 * cfg.n_layers + 1 + 2 * cfg.n_layers
     trace = vc.DecoderTrace(dec, ops_per_round * n_tr)
+    torch.cuda.synchronize()
+    ctx_tr = float(run.qc[0].seq_len.float().mean())
     trace.start()
-    for r in range(n_tr):
-        run.round(log, args.warmup + r)
+    g_tr = run.capture_draft_graph(keep=False)
+    run.round(log, args.warmup, graph=g_tr)
     ops = trace.stop()
+    del g_tr
     # the timed rounds replay the draft steps as one CUDA graph
     if not args.no_graph:
         run.capture_draft_graph()
@@ -667,45 +797,31 @@ def run_model(args, dev, rank, world, barrier, pg):
     value, ms_max = replicas.whole_job_rate(tokens, ms, pg, device=dev)
     st = vc.vc_poll_status(run.ws)
 
-    # end to end: the same rounds, each reading its emitted tokens back to the host
+    # end to end: the same rounds through the public runner, each followed by
+    # the host reading that round's emitted tokens (drafts, accepted length,
+    # next token) from the device and waiting for them, as a serving loop must;
+    # every round's input, the full cache, comes in from pinned host memory
     e2e_val = None
     h_out = torch.empty(M_B * (M_HORIZON + 2), dtype=torch.int32).pin_memory()
     d2h = h_out.numel() * 4
     if n_e2e:
         barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
+        e0 = time.perf_counter()
         base = base0 + args.steps
         for i in range(n_e2e):
             run.round(log, base + i)
             h_out[:M_B * M_HORIZON].copy_(run.drafts.view(-1), non_blocking=True)
             h_out[M_B * M_HORIZON:M_B * (M_HORIZON + 1)].copy_(run.n_acc, non_blocking=True)
             h_out[M_B * (M_HORIZON + 1):].copy_(run.x, non_blocking=True)
-        e1.record()
+            torch.cuda.current_stream().synchronize()
+        e_ms = (time.perf_counter() - e0) * 1e3
         barrier()
         e_tok = int((log.n_acc[base:base + n_e2e].cpu().long() + 1).sum())
-        e2e_val, _ = replicas.whole_job_rate(e_tok, e0.elapsed_time(e1), pg, device=dev)
+        e2e_val, _ = replicas.whole_job_rate(e_tok, e_ms, pg, device=dev)
     run.check_packed()                   # every committed row was held by the packed host copy
 
-    # lossless check: the same prompts decoded greedily with the full cache
-    # resident, token for token against the draft-and-verify output
-    check = None
-    if not args.no_check:
-        emitted = [[first[b]] + t for b, t in enumerate(log.tokens())]
-        n_cmp = min(len(t) for t in emitted)
-        n_cmp = min(n_cmp, args.check_tokens)
-        del run
-        torch.cuda.empty_cache()
-        ref = decode.VeriCacheRunner(dec, M_B, P + n_cmp + 64, M_HORIZON, bits=args.bits, residual=M_RESIDUAL,
-                                     host_cache=False, prefill_chunk=512, device=dev)
-        ref.prefill(prompt)
-        greedy = ref.greedy(n_cmp)
-        mism = sum(int(a != g) for b in range(M_B) for a, g in zip(emitted[b][:n_cmp], greedy[b]))
-        check = {"tokens_compared": n_cmp * M_B, "mismatches": mism,
-                 "reference": "plain full-KV greedy decoding of the same model and prompts (one-token forwards)"}
-
-    # per-phase times and rates
+    # per-phase times and the swap's overlap with drafting, measured as the
+    # intersection of the two intervals on the device
     d_ms = statistics.mean(e["d0"].elapsed_time(e["d1"]) for e in evs)
     v_ms = statistics.mean(e["v0"].elapsed_time(e["v1"]) for e in evs)
     c_ms = statistics.mean(e["v1"].elapsed_time(e["c1"]) for e in evs)
@@ -719,34 +835,82 @@ def run_model(args, dev, rank, world, barrier, pg):
         a = by_kind.setdefault(k, [0, 0.0])
         a[0] += 1
         a[1] += t
-    ctx_mean = P + (args.warmup + n_tr / 2) * (float(n_acc.float().mean()) + 1)
-    rec_b = vc.vc_record_bytes(args.bits, cfg.head_dim)
-    draft_attn_bytes = M_B * cfg.n_kv_heads * (int((ctx_mean - M_RESIDUAL) // 32) * rec_b +
-                                               2 * (M_RESIDUAL + 16) * cfg.head_dim * 2)
+    da_bytes = decoder_draft_attn_bytes(vc, cfg, ctx_tr + M_HORIZON / 2, args.bits)
     kernels = {}
     for k, (n, t) in by_kind.items():
-        # per round of the eager trace rounds, against a timed round
-        ent = {"launches": n, "ms_total": t, "ms_per_launch": t / n,
-               "share_of_time": (t / n_tr) / (ms / args.steps)}
-        if k in wb:
-            ent["GB/s"] = wb[k] / (t / n / 1e3) / 1e9
+        ent = {"launches_per_round": n / n_tr, "ms_per_launch": t / n, "ms_per_round": t / n_tr}
+        nb = wb.get(k, da_bytes if k == "draft_attn" else None)
+        if nb is not None:
+            ent["bytes_per_launch"] = nb
+            ent["GB/s"] = nb / (t / n / 1e3) / 1e9
             ent["hbm_frac"] = ent["GB/s"] / hbm
-            ent["bytes_per_launch"] = wb[k]
-        elif k == "draft_attn":
-            ent["GB/s"] = draft_attn_bytes / (t / n / 1e3) / 1e9
-            ent["hbm_frac"] = ent["GB/s"] / hbm
-            ent["bytes_per_launch"] = draft_attn_bytes
         kernels[k] = ent
     gemm_kinds = [k for k in by_kind if k.startswith("gemm")]
     g_bytes = sum(wb[k] * by_kind[k][0] for k in gemm_kinds)
     g_ms = sum(by_kind[k][1] for k in gemm_kinds)
-    dom = max(by_kind, key=lambda k: by_kind[k][1])
-    roof = {"bound": "hbm", "achieved": g_bytes / (g_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-            "frac": g_bytes / (g_ms / 1e3) / 1e9 / hbm, "traffic": None,
-            "kernel": "gemm_tc_kernel (split-K partials summed in the GEMM up to 64 tiles, else by a reduce "
-                      "kernel): the decoder's projections, weight-streaming at M = 8 (draft) and 264 (verify)",
-            "peak_source": f"{peak_src} hbm_gbs",
-            "dominant_by_time": dom}
+    da_n, da_t = by_kind.get("draft_attn", (1, float("nan")))
+    da_gbs = da_bytes / (da_t / da_n / 1e3) / 1e9
+    round_dev_ms = sum(t for _, t in ops) / n_tr
+    roof = {"bound": "hbm", "achieved": da_gbs, "peak": hbm, "unit": "GB/s", "frac": da_gbs / hbm,
+            "traffic": captured_traffic(DRAFT_TRAFFIC, da_bytes),
+            "kernel": "vc_draft_attn inside the decoder's draft steps (draft_kivi_kernel + combine; B8, one layer "
+                      "per launch), the hot path's dominant kernel; per-launch times from event pairs captured "
+                      "into a replay of the round's draft-step graph",
+            "bytes_per_launch": da_bytes, "ms_per_launch": da_t / da_n,
+            "peak_source": f"{peak_src} hbm_gbs (copy, burst)"}
+    roof_gemm = {"bound": "hbm", "achieved": g_bytes / (g_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                 "frac": g_bytes / (g_ms / 1e3) / 1e9 / hbm,
+                 "kernel": "gemm_tc_kernel: the decoder's projections and LM head (weights streamed at M = 8 "
+                           "in draft steps, M = 264 in the verify forward); the largest share of device time",
+                 "share_of_traced_time": g_ms / n_tr / round_dev_ms}
+    del run
+    torch.cuda.empty_cache()
+
+    # full-KV baseline and losslessness: the same prompts decoded by plain
+    # greedy decoding with the full cache held on the host in the same format
+    # and swapped in before every token (one-token forwards); its tokens are
+    # the reference the draft-and-verify output must equal, its margins flag
+    # near ties, and its token steps time the baseline
+    emitted = [[first[b]] + t for b, t in enumerate(log.tokens())]
+    n_cmp = max(4, min(min(len(t) for t in emitted), args.check_tokens))
+    ref = decode.VeriCacheRunner(dec, M_B, P + n_cmp + 64, M_HORIZON, bits=args.bits, residual=M_RESIDUAL,
+                                 host_cache=True, prefill_chunk=512, device=dev, pack_host=packed)
+    ref.prefill(prompt)
+    margins = torch.zeros(n_cmp, M_B, dtype=torch.float32, device=dev)
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_cmp - 1)]
+    greedy = ref.greedy(n_cmp, margins=margins, events=sev)
+    torch.cuda.synchronize()
+    w0 = min(3, n_cmp - 2)
+    base_ms = sev[w0][0].elapsed_time(sev[-1][1]) / (n_cmp - 1 - w0)
+    base_tps = M_B / (base_ms / 1e3)
+    mg = margins.t().cpu().numpy()
+    near = mism = mism_near = 0
+    for b in range(M_B):
+        for t, (a, g) in enumerate(zip(emitted[b][:n_cmp], greedy[b])):
+            tie = bool(mg[b, t] < 1e-3)
+            near += tie
+            if a != g:
+                mism += 1
+                mism_near += tie
+    check = {"tokens_compared": n_cmp * M_B, "mismatches": mism, "near_ties": near,
+             "mismatches_at_near_ties": mism_near, "mismatches_elsewhere": mism - mism_near,
+             "near_tie_rule": "top-2 logit margin of the reference step below 1e-3",
+             "reference": "plain full-KV greedy decoding of the same model and prompts (one-token forwards)"}
+    base = {"tokens_per_s": base_tps, "ms_per_token_step": base_ms, "steps_timed": n_cmp - 1 - w0,
+            "what": "plain greedy decoding with the full cache in pinned host memory (same format) swapped in "
+                    "before every token, one-token forward, argmax, write-back of the new row",
+            "speedup_of_draft_and_verify": value / base_tps}
+    del ref
+    torch.cuda.empty_cache()
+
+    # the one-layer hot path at the configuration of the kernel workloads
+    # (B16, 32k): draft attention (2-bit KIVI), verify attention (Dq 33) and
+    # acceptance over [16, 33, 151936], timed inside a staggered round
+    round_k = None if args.no_round_kernels else round_kernels(dev, hbm, tf_burst)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = model_cpu_record(cfg, P, args.bits, tokens / args.steps,
+                               f"tokens per round as measured on the GPU ({tokens / args.steps:.1f})")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -759,20 +923,82 @@ def run_model(args, dev, rank, world, barrier, pg):
                        "seq_len": P,
                        "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
             "roofline": roof,
+            "roofline_gemm": roof_gemm,
+            "full_kv_baseline": base,
+            "lossless_check": check,
             "phases_ms": {"draft_32_steps": d_ms, "verify_forward": v_ms, "accept_commit_writeback": c_ms,
-                          "swap_in": s_ms, "swap_hidden_frac": hidden},
+                          "swap_in": s_ms},
             "swap": {"bytes": run_bytes(cfg, max_len, packed),
                      "GB/s": run_bytes(cfg, max_len, packed) / (s_ms / 1e3) / 1e9,
-                     "format": "packed rows (lossless, 208 of 256 bytes)" if packed else "bf16"},
+                     "format": "packed rows (lossless, 208 of 256 bytes)" if packed else "bf16",
+                     "hidden_frac": hidden,
+                     "hidden_frac_how": "per round, the part of the swap interval inside the drafting interval "
+                                        "(device events), over the swap interval"},
             "kernels": kernels,
+            "kernels_round_b16_32k": round_k,
             "accepted_per_round_mean": float(n_acc.float().mean()), "tokens_per_round": tokens / args.steps,
-            "prefill_s": round(t_pf, 2), "status": st, "lossless_check": check,
+            "prefill_s": round(t_pf, 2), "status": st,
             "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc, packed) * args.steps,
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, max_len, packed),
-                    "d2h_bytes_per_step": d2h},
-            "cpu_baseline": None,
+                    "d2h_bytes_per_step": d2h + model_writeback_bytes(cfg, n_acc, packed),
+                    "how": "host wall clock over the rounds, each ending with the host reading its tokens"},
+            "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+def model_writeback_bytes(cfg, n_acc, packed: bool) -> int:
+    """Bytes per round the write-back stores into the host copy (committed
+    rows, K and V, every layer)."""
+    row = 16 + 3 * cfg.head_dim // 2 if packed else cfg.head_dim * 2
+    rows = float((n_acc.float() + 1).sum(dim=1).mean()) if n_acc.dim() == 2 else float((n_acc.float() + 1).sum())
+    return int(2 * cfg.n_layers * cfg.n_kv_heads * rows * row)
+
+
+def round_kernels(dev, hbm, tf_burst, steps: int = 5, warmup: int = 3) -> dict:
+    """Per-kernel numbers of the one-layer round at B16 and 32k context
+    (draft attention over the 2-bit cache, verify attention at Dq 33,
+    acceptance over [16, 33, 151936] bf16 logits, the packed swap), timed
+    with events inside the staggered round."""
+    rnd = Round(dev, stagger=2, packed=True)
+    for _ in range(warmup):
+        rnd.step()
+    torch.cuda.synchronize()
+    evs = [make_events(HORIZON, rnd.stagger) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        rnd.step(evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    d_ms = [e["d0"][j].elapsed_time(e["d1"][j]) for e in evs for j in range(HORIZON)]
+    d_bytes = [rnd.draft_bytes(j) for _ in evs for j in range(HORIZON)]
+    v_ms = [sum(a.elapsed_time(b) for a, b in zip(e["v0"], e["v1"])) for e in evs]
+    a_ms = [e["v1"][-1].elapsed_time(e["a1"]) for e in evs]
+    s_ms = [e["swap0"].elapsed_time(e["swap1"]) for e in evs]
+    draft_gbs = sum(d_bytes) / (sum(d_ms) / 1e3) / 1e9
+    ver_tflops = rnd.verify_flops() / (statistics.mean(v_ms) / 1e3) / 1e12
+    ver_gbs = rnd.verify_bytes() / (statistics.mean(v_ms) / 1e3) / 1e9
+    acc_gbs = (rnd.logits.numel() * 2) / (statistics.mean(a_ms) / 1e3) / 1e9
+    out = {
+        "what": "one decoder layer's hot path at B16, 32/8 heads, d128, 32768-token context (the draft-attention, "
+                "verify-attention and acceptance workloads), timed with events inside the staggered round; these "
+                "rounds plant their acceptance in synthetic logits and are not lossless tokens",
+        "ms_per_round": t0.elapsed_time(t1) / steps,
+        "draft_attn": {"ms": statistics.mean(d_ms), "GB/s": draft_gbs, "hbm_frac": draft_gbs / hbm,
+                       "bytes": int(statistics.mean(d_bytes)),
+                       "traffic": captured_traffic(DRAFT_TRAFFIC, statistics.mean(d_bytes))},
+        "verify_attn_dq33": {"ms": statistics.mean(v_ms), "TFLOP/s": ver_tflops, "tc_frac_burst": ver_tflops / tf_burst,
+                             "GB/s": ver_gbs, "hbm_frac": ver_gbs / hbm, "flops": rnd.verify_flops(),
+                             "bytes": rnd.verify_bytes()},
+        "accept": {"ms": statistics.mean(a_ms), "GB/s": acc_gbs, "hbm_frac": acc_gbs / hbm},
+        "swap_in_packed": {"ms": statistics.mean(s_ms), "GB/s": rnd.swap_bytes / (statistics.mean(s_ms) / 1e3) / 1e9,
+                           "bytes": rnd.swap_bytes},
+    }
+    del rnd
+    torch.cuda.empty_cache()
+    return out
 
 
 def model_launches_per_round(cfg, vc, packed: bool = False) -> int:
@@ -948,8 +1174,11 @@ def main():
     ap.add_argument("--swap", default=None, choices=["packed", "raw"],
                     help="the full cache on the host packed (lossless rows of 16 + 3d/2 bytes, expanded on the "
                          "GPU after each swap; the default) or as plain bf16")
-    ap.add_argument("--workload", default="round", choices=["round", "model"],
-                    help="round: one layer's hot path at 32k (B16); model: the 8-layer decoder end to end")
+    ap.add_argument("--workload", default="model", choices=["round", "model"],
+                    help="model (default): the 8-layer decoder end to end, lossless tokens/s; round: one layer's "
+                         "hot path at 32k (B16) with planted acceptance")
+    ap.add_argument("--no-round-kernels", action="store_true",
+                    help="--workload model: skip the one-layer B16 round that reports the kernel workloads")
     ap.add_argument("--prompt", type=int, default=32768, help="prompt tokens per sequence (--workload model)")
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")

@@ -530,7 +530,9 @@ void vc_decoder_destroy(vc_decoder *dec);
  * arrays are caller-owned (events created by the caller); capacity 0 turns
  * tracing off.  Tracing mutates the decoder object: traced calls must not run
  * concurrently on one vc_decoder.  A GEMM operation includes its split-K
- * reduction.
+ * reduction.  Calls enqueued while their stream is being captured into a
+ * CUDA graph put the events into the graph as external event-record nodes:
+ * they are recorded each time the graph is replayed.
  */
 typedef enum vc_trace_kind {
     VC_TRACE_GEMM_QKV = 0, VC_TRACE_GEMM_O = 1, VC_TRACE_GEMM_GATE_UP = 2, VC_TRACE_GEMM_DOWN = 3,

@@ -308,16 +308,28 @@ struct Ctx {
     template <typename P = void> P *at(size_t off) const { return reinterpret_cast<P *>(ws + off); }
 };
 
+// A trace event on the call's stream.  While the stream is being captured
+// into a CUDA graph the event becomes an event-record node of the graph
+// (external), so it is recorded each time the graph is replayed.
+inline void trace_record(cudaEvent_t ev, cudaStream_t st)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, st);
+}
+
 // Record the trace events around op() when its kind is selected.
 template <typename F>
 cudaError_t traced(const Ctx &C, int kind, F &&op)
 {
     const vc_decoder *d = C.d;
     const bool on = d->tr_ev && (d->tr_mask & (1 << kind)) && d->tr_n < d->tr_cap;
-    if (on) cudaEventRecord(d->tr_ev[2 * d->tr_n], C.st);
+    if (on) trace_record(d->tr_ev[2 * d->tr_n], C.st);
     const cudaError_t e = op();
     if (on) {
-        cudaEventRecord(d->tr_ev[2 * d->tr_n + 1], C.st);
+        trace_record(d->tr_ev[2 * d->tr_n + 1], C.st);
         d->tr_kind[d->tr_n] = kind;
         ++d->tr_n;
     }

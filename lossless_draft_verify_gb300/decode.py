@@ -139,6 +139,7 @@ class VeriCacheRunner:
             vc.vc_decoder_forward(self.dec, None, prompt[:, s:], P, B, n, ctxs[ci], s, self.k_full, self.v_full,
                                   last, self.ws, last_only=True)
         vc.vc_accept(last.view(B, 1, -1), None, self.n_acc, self.x, self.ws_acc)
+        self.last_logits = last
         for l, q in enumerate(self.qc):
             vc.vc_quantize_kv(self.k_full[l], self.v_full[l], q, L=P)
         if self.pack_host:
@@ -169,50 +170,108 @@ class VeriCacheRunner:
             raise RuntimeError(f"{int(self.n_over.item())} K/V rows cannot be held packed; use pack_host=False")
 
     # ------------------------------------------------------- plain greedy --
-    def greedy(self, n_new: int) -> list[list[int]]:
+    def greedy(self, n_new: int, margins: torch.Tensor | None = None, events: list | None = None
+               ) -> list[list[int]]:
         """Plain full-KV greedy decoding from the pending token: n_new tokens
-        per sequence, the first being the pending token itself."""
+        per sequence, the first being the pending token itself.
+
+        With a host cache this is full-KV inference over an offloaded cache
+        (the baseline the paper page compares against, "What the paper
+        found"): the whole cache is swapped in before every token, and each
+        token's K/V row is written back to the host copy.
+        margins: optional device fp32 [n_new][B]; row t receives the gap
+        between the largest and second-largest logit of the step that chose
+        token t (row 0: the prefill's last row).  events: optional list of
+        n_new - 1 (start, end) CUDA event pairs around the token steps."""
         B = self.B
+        main = torch.cuda.current_stream()
         out = torch.zeros(n_new, B, dtype=torch.int32, device=self.device)
         out[0].copy_(self.x)
+        if margins is not None:
+            margins[0].copy_(self._top2_margin(self.last_logits))
+        if self.host_cache:
+            nl, hkv, hd = self.dec.cfg.n_layers, self.dec.cfg.n_kv_heads, self.dec.cfg.head_dim
+            k1 = torch.zeros(nl, B, hkv, 1, hd, dtype=self.dtype, device=self.device)
+            v1 = torch.zeros_like(k1)
+            zero = torch.zeros(B, dtype=torch.int32, device=self.device)
         for t in range(1, n_new):
-            vc.vc_decoder_forward(self.dec, self.x, None, 0, B, 1, self.ctx, self.ctx_bound, self.k_full,
-                                  self.v_full, self.logits_d, self.ws, last_only=True)
+            if events is not None:
+                events[t - 1][0].record(main)
+            if self.host_cache:
+                self._swap_in(main)
+                main.wait_event(self.ev_swap)
+                vc.vc_decoder_forward(self.dec, self.x, None, 0, B, 1, self.ctx, self.ctx_bound, self.k_full,
+                                      self.v_full, self.logits_d, self.ws, k_blk=k1, v_blk=v1, last_only=True)
+            else:
+                vc.vc_decoder_forward(self.dec, self.x, None, 0, B, 1, self.ctx, self.ctx_bound, self.k_full,
+                                      self.v_full, self.logits_d, self.ws, last_only=True)
             vc.vc_accept(self.logits_d.view(B, 1, -1), None, self.n_acc, self.x, self.ws_acc)
+            if self.host_cache:
+                self._write_back(k1, v1, zero, self.ctx)
+            if events is not None:
+                events[t - 1][1].record(main)
+            if margins is not None:
+                margins[t].copy_(self._top2_margin(self.logits_d))
             out[t].copy_(self.x)
             self.ctx += 1
             self.ctx_bound += 1
         return out.t().cpu().tolist()
 
+    @staticmethod
+    def _top2_margin(logits: torch.Tensor) -> torch.Tensor:
+        """Per row, largest minus second-largest logit (bookkeeping of the
+        losslessness check, not part of decoding)."""
+        top = torch.topk(logits.float(), 2, dim=-1).values
+        return top[..., 0] - top[..., 1]
+
+    def _swap_in(self, main: torch.cuda.Stream, ev: dict | None = None):
+        """Copy the host copy of the full cache into the device cache on the
+        side stream (packed rows are expanded layer by layer on a second
+        stream); self.ev_swap marks the end."""
+        self.side.wait_stream(main)
+        if ev is not None:
+            ev["swap0"].record(self.side)
+        if self.pack_host:
+            self.unpack_stream.wait_stream(main)
+            for l in range(len(self.qc)):
+                vc.vc_swap_in(self.k_pack[l], self.k_host[l], stream=self.side)
+                vc.vc_swap_in(self.v_pack[l], self.v_host[l], stream=self.side, done_event=self.ev_layer[l])
+                self.unpack_stream.wait_event(self.ev_layer[l])
+                vc.vc_kv_unpack(self.k_pack[l], self.k_full[l], stream=self.unpack_stream)
+                vc.vc_kv_unpack(self.v_pack[l], self.v_full[l], stream=self.unpack_stream)
+            self.ev_swap.record(self.unpack_stream)
+        else:
+            vc.vc_swap_in(self.k_full, self.k_host, stream=self.side)
+            vc.vc_swap_in(self.v_full, self.v_host, stream=self.side, done_event=self.ev_swap)
+        if ev is not None:
+            ev["swap1"].record(self.unpack_stream if self.pack_host else self.side)
+
+    def _write_back(self, k_blk, v_blk, n_acc, ctx_len):
+        """Committed rows (i <= n_acc[b]) of a block into the host copy at
+        ctx_len[b] + i."""
+        if self.pack_host:
+            vc.vc_kv_writeback_packed(k_blk, v_blk, n_acc, ctx_len, self.k_host, self.v_host, self.n_over)
+        else:
+            vc.vc_kv_writeback(k_blk, v_blk, n_acc, ctx_len, self.k_host, self.v_host)
+
     # --------------------------------------------------- draft and verify --
-    def round(self, log: RoundLog | None = None, r: int = 0, ev: dict | None = None):
-        """One draft-and-verify round (enqueued; no host synchronization)."""
+    def round(self, log: RoundLog | None = None, r: int = 0, ev: dict | None = None,
+              graph: torch.cuda.CUDAGraph | None = None):
+        """One draft-and-verify round (enqueued; no host synchronization).
+        graph: a recording of the draft steps to replay instead of the
+        runner's own (e.g. one captured with tracing on)."""
         B, D = self.B, self.D
         main = torch.cuda.current_stream()
         self.round_len.copy_(self.qc[0].seq_len)
         if self.host_cache:
-            self.side.wait_stream(main)
-            if ev is not None:
-                ev["swap0"].record(self.side)
-            if self.pack_host:
-                self.unpack_stream.wait_stream(main)
-                for l in range(len(self.qc)):
-                    vc.vc_swap_in(self.k_pack[l], self.k_host[l], stream=self.side)
-                    vc.vc_swap_in(self.v_pack[l], self.v_host[l], stream=self.side, done_event=self.ev_layer[l])
-                    self.unpack_stream.wait_event(self.ev_layer[l])
-                    vc.vc_kv_unpack(self.k_pack[l], self.k_full[l], stream=self.unpack_stream)
-                    vc.vc_kv_unpack(self.v_pack[l], self.v_full[l], stream=self.unpack_stream)
-                self.ev_swap.record(self.unpack_stream)
-            else:
-                vc.vc_swap_in(self.k_full, self.k_host, stream=self.side)
-                vc.vc_swap_in(self.v_full, self.v_host, stream=self.side, done_event=self.ev_swap)
-            if ev is not None:
-                ev["swap1"].record(self.unpack_stream if self.pack_host else self.side)
+            self._swap_in(main, ev)
         if self.use_graph and self._graph is None and self._rounds >= 1:
             self.capture_draft_graph()
         if ev is not None:
             ev["d0"].record(main)
-        if self._graph is not None:
+        if graph is not None:
+            graph.replay()
+        elif self._graph is not None:
             self._graph.replay()
         else:
             self._draft_steps()
@@ -237,11 +296,8 @@ class VeriCacheRunner:
             vc.vc_accept(self.logits_v, self.drafts, self.n_acc, self.x, self.ws_acc)
         for l, q in enumerate(self.qc):
             vc.vc_qcache_commit(q, self.k_blk[l], self.v_blk[l], self.round_len, self.n_acc)
-        if self.pack_host:
-            vc.vc_kv_writeback_packed(self.k_blk, self.v_blk, self.n_acc, self.round_len, self.k_host, self.v_host,
-                                      self.n_over)
-        elif self.host_cache:
-            vc.vc_kv_writeback(self.k_blk, self.v_blk, self.n_acc, self.round_len, self.k_host, self.v_host)
+        if self.host_cache:
+            self._write_back(self.k_blk, self.v_blk, self.n_acc, self.round_len)
         if ev is not None:
             ev["c1"].record(main)
         if log is not None:
@@ -260,13 +316,15 @@ class VeriCacheRunner:
                                      drafts_out=self.drafts[:, j], drafts_stride=self.D)
             tok = self.next_d
 
-    def capture_draft_graph(self):
+    def capture_draft_graph(self, keep: bool = True) -> torch.cuda.CUDAGraph:
         """Record the D draft steps as one CUDA graph (nothing runs while it
-        is recorded); round() replays it from then on."""
+        is recorded); with keep, round() replays it from then on."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, capture_error_mode="thread_local"):
             self._draft_steps()
-        self._graph = g
+        if keep:
+            self._graph = g
+        return g
 
     @staticmethod
     def new_events() -> dict:

@@ -575,11 +575,17 @@ class DecoderTrace:
     def stop(self) -> list[tuple[str, float]]:
         """Turn tracing off; returns (kind, milliseconds) per recorded operation
         (synchronizes)."""
-        n = int(load().vc_decoder_trace_count(self.dec.handle))
+        self.n = int(load().vc_decoder_trace_count(self.dec.handle))
         _check(load().vc_decoder_set_trace(self.dec.handle, None, None, 0, 0), "vc_decoder_set_trace")
         torch.cuda.synchronize()
+        return self.times()
+
+    def times(self, first: int = 0, count: int | None = None) -> list[tuple[str, float]]:
+        """(kind, milliseconds) of traced operations first .. first + count - 1
+        as last recorded (for a trace captured into a graph: the last replay)."""
+        n = self.n if count is None else count
         return [(TRACE_KINDS[self._kinds[k]], self.events[2 * k].elapsed_time(self.events[2 * k + 1]))
-                for k in range(n)]
+                for k in range(first, first + n)]
 
 
 def vc_kv_packed_row_bytes(d: int) -> int:
