@@ -458,24 +458,33 @@ draft_kivi_kernel(KiviParams P)
             const int g = g_lo + 2 * (warp + it * NW);
             const bool two = g + 1 < g_hi;
             const uint8_t *recA = myring + st * STAGE;
-            const uint8_t *recB = recA + REC;
-            // ---- scores of both groups
+            // a lone last group pairs with itself; its second copy is masked
+            // out below (scores -inf, so it adds nothing to the values)
+            const uint8_t *recB = two ? recA + REC : recA;
+            // ---- scores of both groups (no branch between them, so their
+            // instructions can interleave)
             float sc[2][2][4];
             {
                 const uint8_t *ks_src = gid < 4 ? recA + Gm::KM : ones;
                 const uint8_t *z_src = gid == 1 ? recA + Gm::KM + 2 * D : zeros;
                 group_scores<BITS, D>(recA, ks_src, z_src, qf, lane, tig, sc[0]);
             }
-            if (two) {
+            {
                 const uint8_t *ks_src = gid < 4 ? recB + Gm::KM : ones;
                 const uint8_t *z_src = gid == 1 ? recB + Gm::KM + 2 * D : zeros;
                 group_scores<BITS, D>(recB, ks_src, z_src, qf, lane, tig, sc[1]);
-            } else {
+            }
+            if (!two) {
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) sc[1][mt][0] = sc[1][mt][1] = sc[1][mt][2] = sc[1][mt][3] = kNegBig;
             }
-            // ---- online softmax over the 64 tokens (exp2 domain, lazy rescale)
-            float gmax[2];
+            // ---- online softmax over the 64 tokens (exp2 domain, lazy rescale).
+            // Each lane first takes the maximum of its own scores; the running
+            // maximum of a column moves only when some score exceeds it by more
+            // than kLazy (a factor 2^kLazy), and only then is the column maximum
+            // reduced across the lanes (after the first groups of a split that
+            // is rare).
+            float lmax[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 float mx = kNegBig;
@@ -491,19 +500,21 @@ draft_kivi_kernel(KiviParams P)
 #pragma unroll
                         for (int mt = 0; mt < 2; ++mt) sc[G2][mt][e] = sc[G2][mt][e + 2] = kNegBig;
                 }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                gmax[e] = mx;
+                lmax[e] = mx;
             }
-            float alpha[2] = {1.f, 1.f};
+            if (__any_sync(0xffffffffu, lmax[0] > m_run[0] + kLazy || lmax[1] > m_run[1] + kLazy)) {
+                float alpha[2] = {1.f, 1.f};
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-                if (gmax[e] > m_run[e] + kLazy) {
-                    alpha[e] = ex2(m_run[e] - gmax[e]);
-                    m_run[e] = gmax[e];
+                for (int e = 0; e < 2; ++e) {
+                    float mx = lmax[e];
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    if (mx > m_run[e] + kLazy) {
+                        alpha[e] = ex2(m_run[e] - mx);
+                        m_run[e] = mx;
+                    }
                 }
-            if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     o_acc[mt][0] *= alpha[0];
@@ -531,12 +542,12 @@ draft_kivi_kernel(KiviParams P)
                     pb[G2][mt][0] = movmatrix_trans(pack_half2(p[0], p[1]));
                     pb[G2][mt][1] = movmatrix_trans(pack_half2(p[2], p[3]));
                 }
-            // ---- values of both groups
+            // ---- values of both groups (a masked copy has p = 0)
             {
                 const uint8_t *zv_src = gid < NG ? recA + Gm::VM + 2 * D : zeros;
                 group_values<BITS, D>(recA, zv_src, pb[0], lane, tig, o_acc, vb_acc);
             }
-            if (two) {
+            {
                 const uint8_t *zv_src = gid < NG ? recB + Gm::VM + 2 * D : zeros;
                 group_values<BITS, D>(recB, zv_src, pb[1], lane, tig, o_acc, vb_acc);
             }
