@@ -5,16 +5,17 @@
 // packed into the record layout the draft kernel consumes (include/vc.h).
 //
 // One CTA of 2*d threads quantizes one (sequence, kv head, token group):
-// threads [0, d) own one K channel each (32 tokens), threads [d, 2d) own one
-// V (token, channel group) each.  Every thread reads its 32 inputs straight
-// from global memory, reduces min/max, derives the directed-rounded fp16
-// meta, computes the codes and ORs them into the record image in shared
-// memory at their fragment-order position; the image is then written with
-// 128-bit stores.  The quotient (x - z)/s is evaluated with the group's
-// reciprocal and recomputed with an exact IEEE division whenever it lies
-// within rounding distance of a half-integer, so the codes are those of the
-// correctly rounded quotient.  HBM-bound: reads 2*32*d*2 bytes, writes one
-// record per group.
+// the group's 32 K rows and 32 V rows are staged in shared memory with
+// 16-byte loads; d/2 threads reduce the min/max of K channel pairs and d
+// threads those of the V (token, 32-channel group) rows, each deriving the
+// directed-rounded fp16 meta and the reciprocal of its scale once; then
+// every thread assembles whole 32-bit code words of the record (the words one
+// draft-kernel lane reads, in fragment order) in registers, with no atomics,
+// and the record leaves with 128-bit stores.  The quotient (x - z)/s is
+// evaluated with the reciprocal and recomputed with an exact IEEE division
+// whenever it lies within rounding distance of a half-integer, so the codes
+// are those of the correctly rounded quotient.  HBM-bound: reads 2*32*d*2
+// bytes, writes one record per group.
 #include <cooperative_groups.h>
 
 #include "vc_common.cuh"
@@ -27,6 +28,24 @@ namespace {
 
 constexpr int G = 32;
 
+// RU(a / m) for finite a >= 0 and a small integer m: the smallest float y
+// with y * m >= a (the definition of rounding upward).  The estimate a * (1/m)
+// is within two ulps; each FMA computes y * m - a with one rounding, so its
+// sign is that of the exact difference and the steps land on the answer.
+__device__ __forceinline__ float div_ru_small(float a, float m, float inv_m)
+{
+    float y = a * inv_m;
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+        if (fmaf(y, m, -a) < 0.0f) y = __uint_as_float(__float_as_uint(y) + 1u);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const float p = __uint_as_float(__float_as_uint(y) - 1u);
+        if (y > 0.0f && fmaf(p, m, -a) >= 0.0f) y = p;
+    }
+    return y;
+}
+
 // Directed-rounding quantization parameters of one group (see include/vc.h).
 __device__ __forceinline__ void group_params(float mn, float mx, int qmax, uint16_t &sb,
                                              uint16_t &zb, float &sf, float &zf)
@@ -34,27 +53,35 @@ __device__ __forceinline__ void group_params(float mn, float mx, int qmax, uint1
     __half z = __float2half_rd(mn);
     zf = __half2float(z);
     float range = __fadd_ru(mx, -zf);
-    float step = __fdiv_ru(range, (float)qmax);
+    float step = div_ru_small(range, (float)qmax, 1.0f / (float)qmax);
     __half s = __float2half_ru(step);
     sf = __half2float(s);
     sb = __half_as_ushort(s);
     zb = __half_as_ushort(z);
 }
 
-// code = clamp(rint(RN(RN(x - z) / s)), 0, qmax); rs = RN(1/s).  d * rs is
-// within a few ulp of RN(d / s) (q <= 15), so away from a half-integer both
-// round to the same integer; near one the exact quotient decides.
-__device__ __noinline__ float exact_quotient(float d, float s) { return __fdiv_rn(d, s); }
-
-__device__ __forceinline__ uint32_t group_code(float x, float sf, float zf, float rs, int qmax)
+// Approximate reciprocal of a scale (at most 1 ulp off); the code logic
+// below tolerates it.
+__device__ __forceinline__ float rcp_scale(float s)
 {
-    if (sf == 0.0f) return 0u;
-    const float d = __fadd_rn(x, -zf);
-    const float q = d * rs;
-    float r = rintf(q);
-    if (fabsf(q - r) > 0.49999f) r = rintf(exact_quotient(d, sf));   // rare: near a half-integer
-    r = fminf(fmaxf(r, 0.0f), (float)qmax);
-    return (uint32_t)r;
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+    return s != 0.0f ? r : 0.0f;
+}
+
+// code = clamp(rint(RN(RN(x - z) / s)), 0, qmax).  The codes are first taken
+// from q = RN(x - z) * rcp(s), rounded to an integer by adding 1.5 * 2^23
+// (round to nearest, ties to even).  q lies within 2^-17 of RN(d / s) for
+// q <= 15, so whenever q is farther than kNearHalf from a half-integer both
+// round to the same integer; the codes nearer than that are recomputed from
+// the exact quotient.  d >= 0 and d / s <= qmax by the choice of z and s, so
+// no clamp is needed on either path.
+constexpr float kRoundMagic = 12582912.0f;
+constexpr float kNearHalf = 0.5f - 0x1p-15f;
+
+__device__ __noinline__ uint32_t exact_code(float x, float zf, float sf)
+{
+    return (uint32_t)rintf(__fdiv_rn(__fadd_rn(x, -zf), sf));
 }
 
 // Position of code pair (kappa, mu) inside a lane's words (see include/vc.h).
@@ -90,133 +117,258 @@ struct RecGeom {
     static constexpr int REC = VM + 4 * D;
 };
 
-// Quantize one group whose token rows are row(t) (t in [0, 32)); threads
-// [0, D) must be given K rows and threads [D, 2D) V rows.  Writes `rec`.
-// blockDim.x == 2 * D; img is a shared record image.
-template <typename T, int BITS, int D, typename RowFn>
-__device__ void quantize_group(RowFn row, uint8_t *__restrict__ rec, uint32_t *img)
+// ------------------------------------------------------------------------
+// Staged quantizer.  The group's 32 K rows and 32 V rows are copied
+// into shared memory with 16-byte loads; the scale, zero-point and reciprocal
+// of every K channel and every V (token, channel group) are computed once;
+// then each thread assembles whole 32-bit code words of the record (the words
+// a draft-kernel lane reads) in registers, with no shared-memory atomics, and
+// the finished record leaves with 128-bit stores.
+// ------------------------------------------------------------------------
+
+template <typename T, int BITS, int D>
+struct QStage {
+    static constexpr int NG = D / G;
+    static constexpr int PITCH = D + 16 / (int)sizeof(T);      // staged row, 16-byte pad (no bank conflicts)
+    static constexpr int X_BYTES = G * PITCH * (int)sizeof(T);
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + X_BYTES;
+    static constexpr int OFF_KST = OFF_V + X_BYTES;                  // float z[D], rs[D], s[D]
+    static constexpr int OFF_VST = OFF_KST + 3 * D * 4;             // float z[NG][G], rs[NG][G], s[NG][G]
+    static constexpr int OFF_IMG = OFF_VST + 3 * NG * G * 4;        // record image
+    static constexpr int BYTES = OFF_IMG + RecGeom<BITS, D>::REC;
+};
+
+// Copy n rows of D elements (16-byte aligned) into staged rows of PITCH.
+template <typename T, int D, typename RowFn>
+__device__ __forceinline__ void stage_rows(RowFn row, T *dst, int n, int tid, int nthr)
+{
+    constexpr int CH = D * (int)sizeof(T) / 16;
+    constexpr int PITCH = D + 16 / (int)sizeof(T);
+    for (int i = tid; i < n * CH; i += nthr) {
+        const int t = i / CH, ch = i % CH;
+        const uint4 u = *reinterpret_cast<const uint4 *>(row(t) + ch * (16 / (int)sizeof(T)));
+        *reinterpret_cast<uint4 *>(dst + t * PITCH + ch * (16 / (int)sizeof(T))) = u;
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float2 load_pair(const T *p);
+template <>
+__device__ __forceinline__ float2 load_pair<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
+    return make_float2(bf16_lo(w), bf16_hi(w));
+}
+template <>
+__device__ __forceinline__ float2 load_pair<float>(const float *p)
+{
+    return *reinterpret_cast<const float2 *>(p);
+}
+
+// Pair (kappa, mu) in slot sl of code word w, for a word index known only at
+// run time (inverse of pair_pos).
+template <int BITS, int D>
+__device__ __forceinline__ void slot_pair(int w, int sl, int &kappa, int &mu)
+{
+    constexpr int W = D * BITS / 32;
+    if (BITS == 2) {
+        constexpr int h = W / 2, q = W / 4;
+        if (sl < 3) {
+            kappa = h * sl + (w >> 1);
+            mu = 2 * (w & 1);
+        } else if (sl >= 5) {
+            kappa = h * (sl - 5) + (w >> 1);
+            mu = 2 * (w & 1) + 1;
+        } else {
+            kappa = 3 * h + q * (sl - 3) + (w >> 2);
+            mu = w & 3;
+        }
+    } else {
+        constexpr int h = W / 2;
+        kappa = h * (sl & 1) + (w >> 1);
+        mu = 2 * (w & 1) + (sl >> 1);
+    }
+}
+
+// The two values of code pair (kappa, mu) of lane (gid, tig) and the index of
+// their statistics: K pairs are channels c, c + 1 of one token (statistics
+// per channel), V pairs tokens t, t + 1 of one channel (statistics per token
+// of the channel's group, stored [group][token]).
+template <typename T, int D, int SEC>
+__device__ __forceinline__ float2 pair_values(const T *x, int kappa, int mu, int gid, int tig, int &st)
+{
+    constexpr int PITCH = D + 16 / (int)sizeof(T);
+    if (SEC == 0) {
+        const int t = 16 * (mu >> 1) + 8 * (mu & 1) + gid;
+        const int c = 16 * (kappa >> 1) + 8 * (kappa & 1) + 2 * tig;
+        st = c;
+        return load_pair<T>(x + t * PITCH + c);
+    } else {
+        const int c = 16 * (kappa >> 1) + 8 * (kappa & 1) + gid;
+        const int t = 16 * (mu >> 1) + 8 * (mu & 1) + 2 * tig;
+        st = (c / G) * G + t;
+        return make_float2(Elem<T>::to_f(x[t * PITCH + c]), Elem<T>::to_f(x[(t + 1) * PITCH + c]));
+    }
+}
+
+// Code words of one section for this thread: words WPT*p .. WPT*p + WPT - 1
+// of lane (gid, tig), stored into the section image.
+template <typename T, int BITS, int D, int SEC>
+__device__ __forceinline__ void code_words(const T *x, const float *stz, const float *strs, const float *sts,
+                                           uint8_t *secimg, int lane, int p)
+{
+    constexpr int WPT = BITS;                      // W * 32 / D words per thread
+    constexpr int SLOTS = 16 / BITS;
+    constexpr uint32_t qmax = (1u << BITS) - 1u;
+    const int gid = lane >> 2, tig = lane & 3;
+    uint32_t words[WPT];
+    uint32_t near = 0;                             // bit (i, sl, hh): needs the exact quotient
+#pragma unroll
+    for (int i = 0; i < WPT; ++i) {
+        const int w = WPT * p + i;
+        uint32_t word = 0;
+#pragma unroll
+        for (int sl = 0; sl < SLOTS; ++sl) {
+            int kappa, mu, st;
+            slot_pair<BITS, D>(w, sl, kappa, mu);
+            const float2 xv = pair_values<T, D, SEC>(x, kappa, mu, gid, tig, st);
+            const float2 z = *reinterpret_cast<const float2 *>(stz + st);
+            const float2 rs = *reinterpret_cast<const float2 *>(strs + st);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float d = __fadd_rn(hh ? xv.y : xv.x, -(hh ? z.y : z.x));
+                const float q = __fmul_rn(d, hh ? rs.y : rs.x);
+                const float m = __fadd_rn(q, kRoundMagic);
+                const float e = __fsub_rn(q, __fsub_rn(m, kRoundMagic));
+                const int bit = (i * SLOTS + sl) * 2 + hh;
+                near |= (fabsf(e) > kNearHalf ? 1u : 0u) << bit;
+                word += (__float_as_uint(m) & qmax) << (BITS * sl + 16 * hh);
+            }
+        }
+        words[i] = word;
+    }
+    // codes within rounding distance of a half-integer: the exact quotient
+    while (near) {
+        const int bit = __ffs(near) - 1;
+        near &= near - 1;
+        const int i = bit / (2 * SLOTS), sl = (bit / 2) % SLOTS, hh = bit & 1;
+        int kappa, mu, st;
+        slot_pair<BITS, D>(WPT * p + i, sl, kappa, mu);
+        const float2 xv = pair_values<T, D, SEC>(x, kappa, mu, gid, tig, st);
+        const uint32_t c = exact_code(hh ? xv.y : xv.x, stz[st + hh], sts[st + hh]);
+        const int sh = BITS * sl + 16 * hh;
+        words[i] = (words[i] & ~(qmax << sh)) | (c << sh);
+    }
+    uint8_t *dst = secimg + word_byte(lane, WPT * p);
+    if constexpr (WPT == 2)
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(words[0], words[1]);
+    else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+// min / max of n bf16 (or fp32) pairs at stride `step` elements
+template <typename T>
+__device__ __forceinline__ void pair_minmax(const T *x, int n, int step, float2 &mn, float2 &mx);
+template <>
+__device__ __forceinline__ void pair_minmax<__nv_bfloat16>(const __nv_bfloat16 *x, int n, int step, float2 &mn,
+                                                           float2 &mx)
+{
+    __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(x), hi = lo;
+#pragma unroll 8
+    for (int t = 1; t < n; ++t) {
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(x + t * step);
+        lo = __hmin2(lo, v);
+        hi = __hmax2(hi, v);
+    }
+    mn = __bfloat1622float2(lo);
+    mx = __bfloat1622float2(hi);
+}
+template <>
+__device__ __forceinline__ void pair_minmax<float>(const float *x, int n, int step, float2 &mn, float2 &mx)
+{
+    mn = mx = *reinterpret_cast<const float2 *>(x);
+#pragma unroll 8
+    for (int t = 1; t < n; ++t) {
+        const float2 v = *reinterpret_cast<const float2 *>(x + t * step);
+        mn.x = fminf(mn.x, v.x);
+        mn.y = fminf(mn.y, v.y);
+        mx.x = fmaxf(mx.x, v.x);
+        mx.y = fmaxf(mx.y, v.y);
+    }
+}
+
+// Quantize the staged group in `sm` (rows already staged; block of 2 D
+// threads) into the record `rec`.
+template <typename T, int BITS, int D>
+__device__ void quantize_staged(uint8_t *sm, uint8_t *__restrict__ rec)
 {
     using Gm = RecGeom<BITS, D>;
+    using St = QStage<T, BITS, D>;
     constexpr int qmax = (1 << BITS) - 1;
     constexpr int NG = D / G;
+    constexpr int PITCH = St::PITCH;
     const int tid = threadIdx.x;
-    uint8_t *bimg = reinterpret_cast<uint8_t *>(img);
-    for (int i = tid; i < Gm::REC / 4; i += 2 * D) img[i] = 0u;
+    const T *kx = reinterpret_cast<const T *>(sm + St::OFF_K);
+    const T *vx = reinterpret_cast<const T *>(sm + St::OFF_V);
+    float *kst = reinterpret_cast<float *>(sm + St::OFF_KST);
+    float *vst = reinterpret_cast<float *>(sm + St::OFF_VST);
+    uint8_t *img = sm + St::OFF_IMG;
+    __syncthreads();                                       // staged rows visible
+    // ---- statistics: K channel pairs on threads [0, D/2), V (token, group) pairs on [D/2, D)
+    if (tid < D / 2) {
+        const int c = 2 * tid;
+        float2 mn, mx;
+        pair_minmax<T>(kx + c, G, PITCH, mn, mx);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int ch = c + e;
+            uint16_t sb, zb;
+            float sf, zf;
+            group_params(e ? mn.y : mn.x, e ? mx.y : mx.x, qmax, sb, zb, sf, zf);
+            kst[ch] = zf;
+            kst[D + ch] = rcp_scale(sf);
+            kst[2 * D + ch] = sf;
+            const int ks = ch >> 4, col = ch & 15;
+            const int j = (col & 7) >> 1, n = 2 * ks + (col >> 3);
+            const int off = Gm::KM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (ch & 1);
+            *reinterpret_cast<uint16_t *>(img + off) = sb;
+            *reinterpret_cast<uint16_t *>(img + off + 2 * D) = zb;
+        }
+    } else if (tid < D) {
+        // tokens t, t + 1 of channel group gc: 32 channels each
+        const int i = tid - D / 2;
+        const int t = 2 * (i % (G / 2)), gc = i / (G / 2);
+        float2 a0, a1, b0, b1;
+        pair_minmax<T>(vx + t * PITCH + gc * G, G / 2, 2, a0, a1);
+        pair_minmax<T>(vx + (t + 1) * PITCH + gc * G, G / 2, 2, b0, b1);
+        const float mn[2] = {fminf(a0.x, a0.y), fminf(b0.x, b0.y)};
+        const float mx[2] = {fmaxf(a1.x, a1.y), fmaxf(b1.x, b1.y)};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int tt = t + e;
+            uint16_t sb, zb;
+            float sf, zf;
+            group_params(mn[e], mx[e], qmax, sb, zb, sf, zf);
+            vst[gc * G + tt] = zf;
+            vst[NG * G + gc * G + tt] = rcp_scale(sf);
+            vst[2 * NG * G + gc * G + tt] = sf;
+            const int ks = tt >> 4, colt = tt & 15;
+            const int j = (colt & 7) >> 1, n = (2 * ks + (colt >> 3)) * NG + gc;
+            const int off = Gm::VM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (tt & 1);
+            *reinterpret_cast<uint16_t *>(img + off) = sb;
+            *reinterpret_cast<uint16_t *>(img + off + 2 * D) = zb;
+        }
+    }
     __syncthreads();
-    if (tid < D) {
-        // ---- K: channel c over the group's 32 tokens
-        const int c = tid;
-        float x[G];
-#pragma unroll
-        for (int t = 0; t < G; ++t) x[t] = Elem<T>::to_f(row(t)[c]);
-        float mn = x[0], mx = x[0];
-#pragma unroll
-        for (int t = 1; t < G; ++t) {
-            mn = fminf(mn, x[t]);
-            mx = fmaxf(mx, x[t]);
-        }
-        uint16_t sb, zb;
-        float sf, zf;
-        group_params(mn, mx, qmax, sb, zb, sf, zf);
-        const float rs = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
-        const int ks = c >> 4, col = c & 15;
-        const int tig = (col & 7) >> 1, hh = col & 1, rh = col >> 3;
-        const int kappa = 2 * ks + rh;
-        // token t = 16 (mu/2) + 8 (mu%2) + gid goes to lane 4 gid + tig, word
-        // w(mu), shift sh(mu): the four (word, shift) of this channel, once
-        int base[4], sh[4];
-#pragma unroll
-        for (int mu = 0; mu < 4; ++mu) {
-            int w, sl;
-            pair_pos<BITS, D>(kappa, mu, w, sl);
-            base[mu] = word_byte(tig, w);
-            sh[mu] = BITS * sl + 16 * hh;
-        }
-        const bool pair01 = base[0] == base[1], pair23 = base[2] == base[3];
-#pragma unroll
-        for (int gid = 0; gid < 8; ++gid) {
-            uint32_t cd[4];
-#pragma unroll
-            for (int mu = 0; mu < 4; ++mu)
-                cd[mu] = group_code(x[16 * (mu >> 1) + 8 * (mu & 1) + gid], sf, zf, rs, qmax) << sh[mu];
-            uint32_t *w0 = reinterpret_cast<uint32_t *>(bimg + base[0] + 64 * gid);
-            uint32_t *w2 = reinterpret_cast<uint32_t *>(bimg + base[2] + 64 * gid);
-            if (pair01) {
-                if (cd[0] | cd[1]) atomicOr(w0, cd[0] | cd[1]);
-            } else {
-                if (cd[0]) atomicOr(w0, cd[0]);
-                if (cd[1]) atomicOr(reinterpret_cast<uint32_t *>(bimg + base[1] + 64 * gid), cd[1]);
-            }
-            if (pair23) {
-                if (cd[2] | cd[3]) atomicOr(w2, cd[2] | cd[3]);
-            } else {
-                if (cd[2]) atomicOr(w2, cd[2]);
-                if (cd[3]) atomicOr(reinterpret_cast<uint32_t *>(bimg + base[3] + 64 * gid), cd[3]);
-            }
-        }
-        // meta: pair n = 2 ks + rr of quad j, half (c & 1)
-        const int j = tig, n = 2 * ks + rh;
-        const int off = Gm::KM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (c & 1);
-        *reinterpret_cast<uint16_t *>(bimg + off) = sb;
-        *reinterpret_cast<uint16_t *>(bimg + off + 2 * D) = zb;
-    } else if (tid < 2 * D) {
-        // ---- V: token t over channel group gc
-        const int i = tid - D;
-        const int t = i % G, gc = i / G;
-        float x[G];
-        const T *src = row(t) + gc * G;
-        if constexpr (sizeof(T) == 2) {
-#pragma unroll
-            for (int e = 0; e < G; e += 8) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(src + e);
-                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    x[e + 2 * k] = bf16_lo(wv[k]);
-                    x[e + 2 * k + 1] = bf16_hi(wv[k]);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < G; e += 4) {
-                const float4 u = *reinterpret_cast<const float4 *>(src + e);
-                x[e] = u.x; x[e + 1] = u.y; x[e + 2] = u.z; x[e + 3] = u.w;
-            }
-        }
-        float mn = x[0], mx = x[0];
-#pragma unroll
-        for (int e = 1; e < G; ++e) {
-            mn = fminf(mn, x[e]);
-            mx = fmaxf(mx, x[e]);
-        }
-        uint16_t sb, zb;
-        float sf, zf;
-        group_params(mn, mx, qmax, sb, zb, sf, zf);
-        const float rs = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
-        const int ks = t >> 4, colt = t & 15;
-        const int tig = (colt & 7) >> 1, hh = colt & 1, rh = colt >> 3;
-        const int mu = 2 * ks + rh;
-        uint8_t *vsec = bimg + Gm::CODE;
-        // channel c = 32 gc + 8 m + gid (m = e / 8) has class kappa = 4 gc + m
-        // and goes to lane 4 gid + tig: the four (word, shift), once
-        int base[4], sh[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            int w, sl;
-            pair_pos<BITS, D>(4 * gc + m, mu, w, sl);
-            base[m] = word_byte(tig, w);
-            sh[m] = BITS * sl + 16 * hh;
-        }
-#pragma unroll
-        for (int e = 0; e < G; ++e) {
-            const int m = e >> 3, gid = e & 7;
-            const uint32_t code = group_code(x[e], sf, zf, rs, qmax);
-            if (code) atomicOr(reinterpret_cast<uint32_t *>(vsec + base[m] + 64 * gid), code << sh[m]);
-        }
-        const int j = tig, n = (2 * ks + rh) * NG + gc;
-        const int off = Gm::VM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (t & 1);
-        *reinterpret_cast<uint16_t *>(bimg + off) = sb;
-        *reinterpret_cast<uint16_t *>(bimg + off + 2 * D) = zb;
+    // ---- code words: threads [0, D) the K section, [D, 2D) the V section
+    {
+        const int j = tid % D;
+        const int lane = j & 31, p = j >> 5;
+        if (tid < D)
+            code_words<T, BITS, D, 0>(kx, kst, kst + D, kst + 2 * D, img, lane, p);
+        else
+            code_words<T, BITS, D, 1>(vx, vst, vst + NG * G, vst + 2 * NG * G, img + Gm::CODE, lane, p);
     }
     __syncthreads();
     uint4 *dst = reinterpret_cast<uint4 *>(rec);
@@ -261,28 +413,28 @@ __device__ void rotate_rows(int n, SrcFn src, DstFn dst, float (*buf)[D])
 }
 
 template <typename T, int BITS, int D, bool ROT>
-__global__ void __launch_bounds__(2 * D, 5)
+__global__ void __launch_bounds__(2 * D, 4)
 quantize_prefill_kernel(const T *__restrict__ k, const T *__restrict__ v, int Hkv, int L_stride,
                         int max_groups, uint8_t *__restrict__ records)
 {
     using Gm = RecGeom<BITS, D>;
-    __shared__ __align__(16) uint32_t img[Gm::REC / 4];
+    using St = QStage<T, BITS, D>;
+    __shared__ __align__(16) uint8_t sm[St::BYTES];
     const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const size_t bh = (size_t)b * Hkv + h;
     const size_t row0 = bh * L_stride + (size_t)g * G;
+    T *kst = reinterpret_cast<T *>(sm + St::OFF_K);
+    T *vst = reinterpret_cast<T *>(sm + St::OFF_V);
+    stage_rows<T, D>([&](int t) { return v + (row0 + t) * D; }, vst, G, threadIdx.x, 2 * D);
     if constexpr (ROT) {
-        // the group's key rows, rotated, in shared memory
-        __shared__ __align__(16) float buf[G][D];
-        __shared__ __align__(16) T kr[G][D];
-        rotate_rows<T, D, G>(
-            G, [&](int t) { return k + (row0 + t) * D; }, [&](int t) { return &kr[t][0]; }, buf);
-        auto row = [&](int t) -> const T * { return threadIdx.x < D ? &kr[t][0] : v + (row0 + t) * D; };
-        quantize_group<T, BITS, D>(row, records + (bh * max_groups + g) * Gm::REC, img);
+        // the group's key rows, rotated, straight into their staged rows
+        __shared__ __align__(16) float buf[8][D];
+        rotate_rows<T, D, 8>(
+            G, [&](int t) { return k + (row0 + t) * D; }, [&](int t) { return kst + t * St::PITCH; }, buf);
     } else {
-        const T *base = threadIdx.x < D ? k : v;
-        auto row = [&](int t) { return base + (row0 + t) * D; };
-        quantize_group<T, BITS, D>(row, records + (bh * max_groups + g) * Gm::REC, img);
+        stage_rows<T, D>([&](int t) { return k + (row0 + t) * D; }, kst, G, threadIdx.x, 2 * D);
     }
+    quantize_staged<T, BITS, D>(sm, records + (bh * max_groups + g) * Gm::REC);
 }
 
 // Copy positions n_q*G .. L-1 into the ring (keys rotated for a rotated
@@ -333,7 +485,8 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
     pdl_wait();
     pdl_trigger();
     using Gm = RecGeom<BITS, D>;
-    __shared__ __align__(16) uint32_t img[Gm::REC / 4];
+    using St = QStage<T, BITS, D>;
+    __shared__ __align__(16) uint8_t sm[St::BYTES];
     const int rank = blockIdx.x, Hc = gridDim.x;
     const int b = blockIdx.y;
     const bool leader = rank == 0 && threadIdx.x == 0;
@@ -373,11 +526,14 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
         }
         __syncthreads();
         for (int g = ng0; g < ng1; ++g) {
-            const T *ring = threadIdx.x < D ? kres : vres;
-            auto row = [&](int t) {
+            auto ring_row = [&](const T *ring, int t) {
                 return ring + (bh * res_cap + (size_t)(((long)g * G + t) % res_cap)) * D;
             };
-            quantize_group<T, BITS, D>(row, records + (bh * max_groups + g) * Gm::REC, img);
+            stage_rows<T, D>([&](int t) { return ring_row(kres, t); }, reinterpret_cast<T *>(sm + St::OFF_K), G,
+                             threadIdx.x, 2 * D);
+            stage_rows<T, D>([&](int t) { return ring_row(vres, t); }, reinterpret_cast<T *>(sm + St::OFF_V), G,
+                             threadIdx.x, 2 * D);
+            quantize_staged<T, BITS, D>(sm, records + (bh * max_groups + g) * Gm::REC);
             __syncthreads();
         }
     }
