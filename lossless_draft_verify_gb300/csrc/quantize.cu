@@ -16,6 +16,8 @@
 // whenever it lies within rounding distance of a half-integer, so the codes
 // are those of the correctly rounded quotient.  HBM-bound: reads 2*32*d*2
 // bytes, writes one record per group.
+#include <algorithm>
+
 #include <cooperative_groups.h>
 
 #include "vc_common.cuh"
@@ -30,7 +32,8 @@ constexpr int G = 32;
 
 // RU(a / m) for finite a >= 0 and a small integer m: the smallest float y
 // with y * m >= a (the definition of rounding upward).  The estimate a * (1/m)
-// is within two ulps; each FMA computes y * m - a with one rounding, so its
+// is within two ulps (three steps allow for a binade edge); each FMA computes
+// y * m - a with one rounding, so its
 // sign is that of the exact difference and the steps land on the answer.
 __device__ __forceinline__ float div_ru_small(float a, float m, float inv_m)
 {
@@ -67,6 +70,40 @@ __device__ __forceinline__ float rcp_scale(float s)
     float r;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
     return s != 0.0f ? r : 0.0f;
+}
+
+// Two-lane fp32 arithmetic (add/mul.rn.f32x2): both lanes round exactly as the
+// scalar instructions do.
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+// all ones when |e| lies above the near-half threshold, else zero
+__device__ __forceinline__ uint32_t near_mask(float e, float thr)
+{
+    uint32_t m;
+    asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(fabsf(e)), "f"(thr));
+    return m;
 }
 
 // code = clamp(rint(RN(RN(x - z) / s)), 0, qmax).  The codes are first taken
@@ -130,13 +167,10 @@ template <typename T, int BITS, int D>
 struct QStage {
     static constexpr int NG = D / G;
     static constexpr int PITCH = D + 16 / (int)sizeof(T);      // staged row, 16-byte pad (no bank conflicts)
-    static constexpr int X_BYTES = G * PITCH * (int)sizeof(T);
-    static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = OFF_K + X_BYTES;
-    static constexpr int OFF_KST = OFF_V + X_BYTES;                  // float z[D], rs[D], s[D]
-    static constexpr int OFF_VST = OFF_KST + 3 * D * 4;             // float z[NG][G], rs[NG][G], s[NG][G]
-    static constexpr int OFF_IMG = OFF_VST + 3 * NG * G * 4;        // record image
-    static constexpr int BYTES = OFF_IMG + RecGeom<BITS, D>::REC;
+    static constexpr int ROW_BYTES = PITCH * (int)sizeof(T);
+    static constexpr int X_BYTES = G * ROW_BYTES;                // one staged K or V group
+    static constexpr int WORK_BYTES = 3 * D * 4 + 3 * NG * G * 4 + RecGeom<BITS, D>::REC;
+    static constexpr int BYTES = 2 * X_BYTES + WORK_BYTES;      // one stage + work
 };
 
 // Copy n rows of D elements (16-byte aligned) into staged rows of PITCH.
@@ -235,15 +269,18 @@ __device__ __forceinline__ void code_words(const T *x, const float *stz, const f
             const float2 xv = pair_values<T, D, SEC>(x, kappa, mu, gid, tig, st);
             const float2 z = *reinterpret_cast<const float2 *>(stz + st);
             const float2 rs = *reinterpret_cast<const float2 *>(strs + st);
+            // d = RN(x - z), q = RN(d * rcp(s)), m = RN(q + 1.5 * 2^23) (integer
+            // part = rint(q)), e = q - rint(q), both lanes at once
+            const float2 magic = make_float2(kRoundMagic, kRoundMagic);
+            const float2 q = mul2(sub2(xv, z), rs);
+            const float2 m = add2(q, magic);
+            const float2 e = sub2(q, sub2(m, magic));
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const float d = __fadd_rn(hh ? xv.y : xv.x, -(hh ? z.y : z.x));
-                const float q = __fmul_rn(d, hh ? rs.y : rs.x);
-                const float m = __fadd_rn(q, kRoundMagic);
-                const float e = __fsub_rn(q, __fsub_rn(m, kRoundMagic));
                 const int bit = (i * SLOTS + sl) * 2 + hh;
-                near |= (fabsf(e) > kNearHalf ? 1u : 0u) << bit;
-                word += (__float_as_uint(m) & qmax) << (BITS * sl + 16 * hh);
+                const int sh = BITS * sl + 16 * hh;
+                near |= near_mask(hh ? e.y : e.x, kNearHalf) & (1u << bit);
+                word |= (__float_as_uint(hh ? m.y : m.x) << sh) & (qmax << sh);
             }
         }
         words[i] = word;
@@ -298,10 +335,13 @@ __device__ __forceinline__ void pair_minmax<float>(const float *x, int n, int st
     }
 }
 
-// Quantize the staged group in `sm` (rows already staged; block of 2 D
-// threads) into the record `rec`.
+// Quantize one staged group (K rows kx, V rows vx at the staged pitch) into
+// the record `rec`, by a block of 2 D threads; `work` holds the statistics and
+// the record image (QStage::WORK_BYTES).  The staged rows must be visible to
+// every thread on entry; they are no longer read once the second barrier
+// inside has passed.
 template <typename T, int BITS, int D>
-__device__ void quantize_staged(uint8_t *sm, uint8_t *__restrict__ rec)
+__device__ void quantize_staged(const T *kx, const T *vx, uint8_t *work, uint8_t *__restrict__ rec)
 {
     using Gm = RecGeom<BITS, D>;
     using St = QStage<T, BITS, D>;
@@ -309,58 +349,50 @@ __device__ void quantize_staged(uint8_t *sm, uint8_t *__restrict__ rec)
     constexpr int NG = D / G;
     constexpr int PITCH = St::PITCH;
     const int tid = threadIdx.x;
-    const T *kx = reinterpret_cast<const T *>(sm + St::OFF_K);
-    const T *vx = reinterpret_cast<const T *>(sm + St::OFF_V);
-    float *kst = reinterpret_cast<float *>(sm + St::OFF_KST);
-    float *vst = reinterpret_cast<float *>(sm + St::OFF_VST);
-    uint8_t *img = sm + St::OFF_IMG;
-    __syncthreads();                                       // staged rows visible
-    // ---- statistics: K channel pairs on threads [0, D/2), V (token, group) pairs on [D/2, D)
-    if (tid < D / 2) {
-        const int c = 2 * tid;
+    float *kst = reinterpret_cast<float *>(work);
+    float *vst = kst + 3 * D;
+    uint8_t *img = work + 3 * D * 4 + 3 * NG * G * 4;
+    // ---- statistics, one group parameter per thread: threads [0, D) take K
+    // channel c (the two lanes of a pair each reduce 16 tokens of channels
+    // c & ~1, c | 1 and exchange), threads [D, 2D) a V (token, channel group)
+    if (tid < D) {
+        const int cp = tid >> 1, half = tid & 1;
         float2 mn, mx;
-        pair_minmax<T>(kx + c, G, PITCH, mn, mx);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int ch = c + e;
-            uint16_t sb, zb;
-            float sf, zf;
-            group_params(e ? mn.y : mn.x, e ? mx.y : mx.x, qmax, sb, zb, sf, zf);
-            kst[ch] = zf;
-            kst[D + ch] = rcp_scale(sf);
-            kst[2 * D + ch] = sf;
-            const int ks = ch >> 4, col = ch & 15;
-            const int j = (col & 7) >> 1, n = 2 * ks + (col >> 3);
-            const int off = Gm::KM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (ch & 1);
-            *reinterpret_cast<uint16_t *>(img + off) = sb;
-            *reinterpret_cast<uint16_t *>(img + off + 2 * D) = zb;
-        }
-    } else if (tid < D) {
-        // tokens t, t + 1 of channel group gc: 32 channels each
-        const int i = tid - D / 2;
-        const int t = 2 * (i % (G / 2)), gc = i / (G / 2);
-        float2 a0, a1, b0, b1;
-        pair_minmax<T>(vx + t * PITCH + gc * G, G / 2, 2, a0, a1);
-        pair_minmax<T>(vx + (t + 1) * PITCH + gc * G, G / 2, 2, b0, b1);
-        const float mn[2] = {fminf(a0.x, a0.y), fminf(b0.x, b0.y)};
-        const float mx[2] = {fmaxf(a1.x, a1.y), fmaxf(b1.x, b1.y)};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int tt = t + e;
-            uint16_t sb, zb;
-            float sf, zf;
-            group_params(mn[e], mx[e], qmax, sb, zb, sf, zf);
-            vst[gc * G + tt] = zf;
-            vst[NG * G + gc * G + tt] = rcp_scale(sf);
-            vst[2 * NG * G + gc * G + tt] = sf;
-            const int ks = tt >> 4, colt = tt & 15;
-            const int j = (colt & 7) >> 1, n = (2 * ks + (colt >> 3)) * NG + gc;
-            const int off = Gm::VM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (tt & 1);
-            *reinterpret_cast<uint16_t *>(img + off) = sb;
-            *reinterpret_cast<uint16_t *>(img + off + 2 * D) = zb;
-        }
+        pair_minmax<T>(kx + half * (G / 2) * PITCH + 2 * cp, G / 2, PITCH, mn, mx);
+        mn.x = fminf(mn.x, __shfl_xor_sync(0xffffffffu, mn.x, 1));
+        mn.y = fminf(mn.y, __shfl_xor_sync(0xffffffffu, mn.y, 1));
+        mx.x = fmaxf(mx.x, __shfl_xor_sync(0xffffffffu, mx.x, 1));
+        mx.y = fmaxf(mx.y, __shfl_xor_sync(0xffffffffu, mx.y, 1));
+        const int ch = 2 * cp + half;
+        uint16_t sb, zb;
+        float sf, zf;
+        group_params(half ? mn.y : mn.x, half ? mx.y : mx.x, qmax, sb, zb, sf, zf);
+        kst[ch] = zf;
+        kst[D + ch] = rcp_scale(sf);
+        kst[2 * D + ch] = sf;
+        const int ks = ch >> 4, col = ch & 15;
+        const int j = (col & 7) >> 1, n = 2 * ks + (col >> 3);
+        const int off = Gm::KM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (ch & 1);
+        *reinterpret_cast<uint16_t *>(img + off) = sb;
+        *reinterpret_cast<uint16_t *>(img + off + 2 * D) = zb;
+    } else {
+        const int i = tid - D;
+        const int t = i % G, gc = i / G;
+        float2 a, b;
+        pair_minmax<T>(vx + t * PITCH + gc * G, G / 2, 2, a, b);
+        uint16_t sb, zb;
+        float sf, zf;
+        group_params(fminf(a.x, a.y), fmaxf(b.x, b.y), qmax, sb, zb, sf, zf);
+        vst[gc * G + t] = zf;
+        vst[NG * G + gc * G + t] = rcp_scale(sf);
+        vst[2 * NG * G + gc * G + t] = sf;
+        const int ks = t >> 4, colt = t & 15;
+        const int j = (colt & 7) >> 1, n = (2 * ks + (colt >> 3)) * NG + gc;
+        const int off = Gm::VM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (t & 1);
+        *reinterpret_cast<uint16_t *>(img + off) = sb;
+        *reinterpret_cast<uint16_t *>(img + off + 2 * D) = zb;
     }
-    __syncthreads();
+    __syncthreads();                                       // statistics and meta written
     // ---- code words: threads [0, D) the K section, [D, 2D) the V section
     {
         const int j = tid % D;
@@ -370,7 +402,7 @@ __device__ void quantize_staged(uint8_t *sm, uint8_t *__restrict__ rec)
         else
             code_words<T, BITS, D, 1>(vx, vst, vst + NG * G, vst + 2 * NG * G, img + Gm::CODE, lane, p);
     }
-    __syncthreads();
+    __syncthreads();                                       // record image complete
     uint4 *dst = reinterpret_cast<uint4 *>(rec);
     const uint4 *srcv = reinterpret_cast<const uint4 *>(img);
     for (int i = tid; i < Gm::REC / 16; i += 2 * D) dst[i] = srcv[i];
@@ -412,8 +444,10 @@ __device__ void rotate_rows(int n, SrcFn src, DstFn dst, float (*buf)[D])
     }
 }
 
+// Prefill: one CTA per (group, kv head, sequence); its rows are staged with
+// 16-byte loads (rotated in place for a rotated cache), then quantized.
 template <typename T, int BITS, int D, bool ROT>
-__global__ void __launch_bounds__(2 * D, 4)
+__global__ void __launch_bounds__(2 * D, 5)
 quantize_prefill_kernel(const T *__restrict__ k, const T *__restrict__ v, int Hkv, int L_stride,
                         int max_groups, uint8_t *__restrict__ records)
 {
@@ -423,18 +457,18 @@ quantize_prefill_kernel(const T *__restrict__ k, const T *__restrict__ v, int Hk
     const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const size_t bh = (size_t)b * Hkv + h;
     const size_t row0 = bh * L_stride + (size_t)g * G;
-    T *kst = reinterpret_cast<T *>(sm + St::OFF_K);
-    T *vst = reinterpret_cast<T *>(sm + St::OFF_V);
-    stage_rows<T, D>([&](int t) { return v + (row0 + t) * D; }, vst, G, threadIdx.x, 2 * D);
+    T *kx = reinterpret_cast<T *>(sm);
+    T *vx = reinterpret_cast<T *>(sm + St::X_BYTES);
+    stage_rows<T, D>([&](int t) { return k + (row0 + t) * D; }, kx, G, threadIdx.x, 2 * D);
+    stage_rows<T, D>([&](int t) { return v + (row0 + t) * D; }, vx, G, threadIdx.x, 2 * D);
+    __syncthreads();
     if constexpr (ROT) {
-        // the group's key rows, rotated, straight into their staged rows
+        // the key rows, rotated in place
         __shared__ __align__(16) float buf[8][D];
         rotate_rows<T, D, 8>(
-            G, [&](int t) { return k + (row0 + t) * D; }, [&](int t) { return kst + t * St::PITCH; }, buf);
-    } else {
-        stage_rows<T, D>([&](int t) { return k + (row0 + t) * D; }, kst, G, threadIdx.x, 2 * D);
+            G, [&](int t) { return kx + t * St::PITCH; }, [&](int t) { return kx + t * St::PITCH; }, buf);
     }
-    quantize_staged<T, BITS, D>(sm, records + (bh * max_groups + g) * Gm::REC);
+    quantize_staged<T, BITS, D>(kx, vx, sm + 2 * St::X_BYTES, records + (bh * max_groups + g) * Gm::REC);
 }
 
 // Copy positions n_q*G .. L-1 into the ring (keys rotated for a rotated
@@ -529,11 +563,12 @@ append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new,
             auto ring_row = [&](const T *ring, int t) {
                 return ring + (bh * res_cap + (size_t)(((long)g * G + t) % res_cap)) * D;
             };
-            stage_rows<T, D>([&](int t) { return ring_row(kres, t); }, reinterpret_cast<T *>(sm + St::OFF_K), G,
-                             threadIdx.x, 2 * D);
-            stage_rows<T, D>([&](int t) { return ring_row(vres, t); }, reinterpret_cast<T *>(sm + St::OFF_V), G,
-                             threadIdx.x, 2 * D);
-            quantize_staged<T, BITS, D>(sm, records + (bh * max_groups + g) * Gm::REC);
+            T *kx = reinterpret_cast<T *>(sm);
+            T *vx = reinterpret_cast<T *>(sm + St::X_BYTES);
+            stage_rows<T, D>([&](int t) { return ring_row(kres, t); }, kx, G, threadIdx.x, 2 * D);
+            stage_rows<T, D>([&](int t) { return ring_row(vres, t); }, vx, G, threadIdx.x, 2 * D);
+            __syncthreads();
+            quantize_staged<T, BITS, D>(kx, vx, sm + 2 * St::X_BYTES, records + (bh * max_groups + g) * Gm::REC);
             __syncthreads();
         }
     }
@@ -553,12 +588,9 @@ cudaError_t launch_prefill(const void *k, const void *v, int B, int Hkv, int L, 
     const bool rot = c->cfg.rotate != 0;
     if (nq > 0) {
         dim3 grid(nq / G, Hkv, B);
-        if (rot)
-            quantize_prefill_kernel<T, BITS, D, true><<<grid, 2 * D, 0, st>>>(
-                (const T *)k, (const T *)v, Hkv, L_stride, c->max_groups, (uint8_t *)c->records);
-        else
-            quantize_prefill_kernel<T, BITS, D, false><<<grid, 2 * D, 0, st>>>(
-                (const T *)k, (const T *)v, Hkv, L_stride, c->max_groups, (uint8_t *)c->records);
+        auto kern = rot ? quantize_prefill_kernel<T, BITS, D, true> : quantize_prefill_kernel<T, BITS, D, false>;
+        kern<<<grid, 2 * D, 0, st>>>((const T *)k, (const T *)v, Hkv, L_stride, c->max_groups,
+                                     (uint8_t *)c->records);
     }
     auto rc = rot ? residual_copy_kernel<T, D, true> : residual_copy_kernel<T, D, false>;
     rc<<<B * Hkv, 256, 0, st>>>((const T *)k, (const T *)v, B, Hkv, L, L_stride, nq, (T *)c->k_res,
