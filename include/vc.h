@@ -298,8 +298,11 @@ vc_status vc_draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view,
  * attention: each head's scores are stored in fp32 and normalised by the
  * head's final max and sum after the split merge.  scores: device fp32, rows
  * of one unit distinct positions.  Workspace: vc_draft_attn_h2o_workspace_bytes
- * (the attention's plus 16 bytes per cached row).  VC_ERR_UNSUPPORTED for
- * KIVI or fp32 views.
+ * (the attention's plus 16 bytes per cached row).
+ * Views: dense bf16 (q bf16), or KIVI (q bf16 or fp32; the mass of the
+ * dequantized cache x^ and of the ring; kept_idx must be NULL, the rows being
+ * the positions, and scores_stride >= max_groups * group + res_cap).
+ * VC_ERR_UNSUPPORTED for dense fp32 views.
  */
 size_t vc_draft_attn_h2o_workspace_bytes(const vc_cache_view *view, int Hq);
 vc_status vc_draft_attn_h2o(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq, float sm_scale,

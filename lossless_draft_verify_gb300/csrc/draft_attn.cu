@@ -156,6 +156,9 @@ struct KiviParams {
     int Hkv, Hq, grp, max_groups, res_cap, n_split_q, groups_per_split;
     int n_split_r, res_per_split;                      // ring splits and ring tokens per split
     float qscale;                                      // sm_scale * log2(e)
+    float *raw;                                        // optional [units][raw_stride][4] log2-domain scores (H2O)
+    float *ml;                                         // optional [units][8]: each head's final max and sum
+    int raw_stride;
 };
 
 template <typename TQ, int D>
@@ -478,6 +481,20 @@ draft_kivi_kernel(KiviParams P)
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) sc[1][mt][0] = sc[1][mt][1] = sc[1][mt][2] = sc[1][mt][3] = kNegBig;
             }
+            if (P.raw && tig < 2) {
+                // H2O: every visible score is kept for the mass pass after the merge
+                float *rw = P.raw + ((size_t)unit * P.raw_stride + (size_t)g * G + gid) * 4;
+#pragma unroll
+                for (int G2 = 0; G2 < 2; ++G2)
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int h = 2 * tig + (i & 1);
+                            if ((G2 == 0 || two) && h < grp)
+                                rw[(G2 * G + 16 * mt + 8 * (i >> 1)) * 4 + h] = sc[G2][mt][i];
+                        }
+            }
             // ---- online softmax over the 64 tokens (exp2 domain, lazy rescale).
             // Each lane first takes the maximum of its own scores; the running
             // maximum of a column moves only when some score exceeds it by more
@@ -601,7 +618,8 @@ draft_kivi_kernel(KiviParams P)
         cta_merge_store<D>(wbuf, dst, grp);
         last_cta_combine<TQ, D>(P.part + (size_t)unit * n_split * part_floats(D), n_split,
                                 P.counters + unit, grp,
-                                reinterpret_cast<TQ *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
+                                reinterpret_cast<TQ *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D,
+                                P.ml ? P.ml + (size_t)unit * 8 : nullptr);
     } else {
         // ------------------------------------- residual ring (fp32 SIMT) --
         // Split r of the ring takes positions p0 + r * res_per_split onwards;
@@ -688,6 +706,8 @@ draft_kivi_kernel(KiviParams P)
 #pragma unroll
                     for (int i = 0; i < CPL; ++i) sdot = fmaf(qv[h][i], kx[i], sdot);
                     sdot = warp_sum(sdot);
+                    if (P.raw && lane == 0 && h < grp)
+                        P.raw[((size_t)unit * P.raw_stride + t0 + t) * 4 + h] = sdot;
                     const float mn = fmaxf(m[h], sdot);
                     const float a = exp2f(m[h] - mn), pp = exp2f(sdot - mn);
                     m[h] = mn;
@@ -711,7 +731,8 @@ draft_kivi_kernel(KiviParams P)
         cta_merge_store<D>(wbuf, dst, grp);
         last_cta_combine<TQ, D>(P.part + (size_t)unit * n_split * part_floats(D), n_split,
                                 P.counters + unit, grp,
-                                reinterpret_cast<TQ *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D);
+                                reinterpret_cast<TQ *>(P.out) + ((size_t)b * P.Hq + kvh * grp) * D,
+                                P.ml ? P.ml + (size_t)unit * 8 : nullptr);
     }
 }
 
@@ -1226,13 +1247,19 @@ DensePlan dense_plan(const vc_cache_view *v)
     return p;
 }
 
+// Tokens a KIVI cache can hold per kv unit (the H2O score rows).
+inline int kivi_token_cap(const vc_qcache *c) { return c->max_groups * G + c->res_cap; }
+
 template <int BITS, int D, typename TQ, typename TR, bool ROT>
 cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, void *out, void *ws,
-                        cudaStream_t st)
+                        cudaStream_t st, float *raw = nullptr, float *ml = nullptr)
 {
     using Gm = KiviGeom<BITS, D>;
     const KiviPlan pl = kivi_plan(c);
     KiviParams P;
+    P.raw = raw;
+    P.ml = ml;
+    P.raw_stride = kivi_token_cap(c);
     P.q = q;
     P.records = (const uint8_t *)c->records;
     P.kres = c->k_res;
@@ -1310,28 +1337,33 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
 
 template <int BITS, int D, typename TQ>
 cudaError_t kivi_by_res(const void *q, const vc_qcache *c, int Hq, float s, void *o, void *ws,
-                        cudaStream_t st)
+                        cudaStream_t st, float *raw = nullptr, float *ml = nullptr)
 {
     if (c->cfg.rotate)
-        return c->res_dtype == VC_BF16 ? launch_kivi<BITS, D, TQ, __nv_bfloat16, true>(q, c, Hq, s, o, ws, st)
-                                       : launch_kivi<BITS, D, TQ, float, true>(q, c, Hq, s, o, ws, st);
-    return c->res_dtype == VC_BF16 ? launch_kivi<BITS, D, TQ, __nv_bfloat16, false>(q, c, Hq, s, o, ws, st)
-                                   : launch_kivi<BITS, D, TQ, float, false>(q, c, Hq, s, o, ws, st);
+        return c->res_dtype == VC_BF16
+                   ? launch_kivi<BITS, D, TQ, __nv_bfloat16, true>(q, c, Hq, s, o, ws, st, raw, ml)
+                   : launch_kivi<BITS, D, TQ, float, true>(q, c, Hq, s, o, ws, st, raw, ml);
+    return c->res_dtype == VC_BF16 ? launch_kivi<BITS, D, TQ, __nv_bfloat16, false>(q, c, Hq, s, o, ws, st, raw, ml)
+                                   : launch_kivi<BITS, D, TQ, float, false>(q, c, Hq, s, o, ws, st, raw, ml);
 }
 
 template <int D, typename TQ>
 cudaError_t kivi_by_bits(const void *q, const vc_qcache *c, int Hq, float s, void *o, void *ws,
-                         cudaStream_t st)
+                         cudaStream_t st, float *raw = nullptr, float *ml = nullptr)
 {
-    return c->cfg.bits == 2 ? kivi_by_res<2, D, TQ>(q, c, Hq, s, o, ws, st)
-                            : kivi_by_res<4, D, TQ>(q, c, Hq, s, o, ws, st);
+    return c->cfg.bits == 2 ? kivi_by_res<2, D, TQ>(q, c, Hq, s, o, ws, st, raw, ml)
+                            : kivi_by_res<4, D, TQ>(q, c, Hq, s, o, ws, st, raw, ml);
 }
 
 }  // namespace
 
 size_t draft_h2o_ws_bytes(const vc_cache_view *view, int Hq)
 {
-    if (view->kind != VC_CACHE_DENSE) return 0;
+    if (view->kind == VC_CACHE_KIVI) {
+        const vc_qcache *c = view->kivi;
+        return draft_ws_bytes(view, Hq) + align256((size_t)c->B * c->Hkv * 8 * 4) +
+               align256((size_t)c->B * c->Hkv * kivi_token_cap(c) * 4 * 4);
+    }
     return draft_ws_bytes(view, Hq) + align256((size_t)view->B * view->Hkv * 8 * 4) +
            align256((size_t)view->B * view->Hkv * view->max_len * 4 * 4);
 }
@@ -1372,11 +1404,32 @@ cudaError_t draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view, 
 
 namespace vc {
 
-cudaError_t draft_attn_h2o(const void *q, const vc_cache_view *view, int Hq, float sm_scale, void *out,
-                           float *scores, int scores_stride, const int32_t *kept_idx, int kept_stride, void *ws,
-                           cudaStream_t st)
+cudaError_t draft_attn_h2o(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq, float sm_scale,
+                           void *out, float *scores, int scores_stride, const int32_t *kept_idx, int kept_stride,
+                           void *ws, cudaStream_t st)
 {
     uint8_t *base = (uint8_t *)ws;
+    if (view->kind == VC_CACHE_KIVI) {
+        // quantized records and ring: scores stored by the draft kernel itself
+        const vc_qcache *c = view->kivi;
+        const size_t main_ws = draft_ws_bytes(view, Hq);
+        float *ml = (float *)(base + main_ws);
+        float *raw = (float *)(base + main_ws + align256((size_t)c->B * c->Hkv * 8 * 4));
+        cudaError_t e;
+        if (c->d == 128)
+            e = q_dt == VC_BF16 ? kivi_by_bits<128, __nv_bfloat16>(q, c, Hq, sm_scale, out, ws, st, raw, ml)
+                                : kivi_by_bits<128, float>(q, c, Hq, sm_scale, out, ws, st, raw, ml);
+        else
+            e = q_dt == VC_BF16 ? kivi_by_bits<64, __nv_bfloat16>(q, c, Hq, sm_scale, out, ws, st, raw, ml)
+                                : kivi_by_bits<64, float>(q, c, Hq, sm_scale, out, ws, st, raw, ml);
+        if (e != cudaSuccess) return e;
+        const int units = c->B * c->Hkv;
+        const int cap = kivi_token_cap(c);
+        const int blocks = std::max(1, std::min(64, (cap + 255) / 256));
+        h2o_accumulate_kernel<<<dim3(blocks, units), 256, 0, st>>>(raw, ml, c->seq_len, cap, c->Hkv, Hq / c->Hkv,
+                                                                   kept_idx, kept_stride, scores, scores_stride);
+        return cudaGetLastError();
+    }
     const size_t main_ws = draft_ws_bytes(view, Hq);
     float *ml = (float *)(base + main_ws);
     float *raw = (float *)(base + main_ws + align256((size_t)view->B * view->Hkv * 8 * 4));

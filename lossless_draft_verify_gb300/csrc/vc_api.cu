@@ -214,8 +214,10 @@ vc_status vc_draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view,
 
 size_t vc_draft_attn_h2o_workspace_bytes(const vc_cache_view *view, int Hq)
 {
-    if (!view || view->kind != VC_CACHE_DENSE || view->dt != VC_BF16 || view->B <= 0 || view->Hkv <= 0 ||
-        view->max_len < 0 || Hq <= 0)
+    if (!view || Hq <= 0) return 0;
+    if (view->kind == VC_CACHE_KIVI) return qcache_ok(view->kivi) ? draft_h2o_ws_bytes(view, Hq) : 0;
+    if (view->kind != VC_CACHE_DENSE || view->dt != VC_BF16 || view->B <= 0 || view->Hkv <= 0 ||
+        view->max_len < 0)
         return 0;
     return draft_h2o_ws_bytes(view, Hq);
 }
@@ -225,6 +227,16 @@ vc_status vc_draft_attn_h2o(const void *q, vc_dtype q_dt, const vc_cache_view *v
                             void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (!q || !view || !out || !scores || !ws || !aligned(ws, 256)) return VC_ERR_INVALID;
+    if (view->kind == VC_CACHE_KIVI) {
+        // rows of a KIVI cache are positions 0 .. seq_len - 1 themselves
+        const vc_qcache *c = view->kivi;
+        if (!qcache_ok(c) || !dtype_ok(q_dt) || kept_idx) return VC_ERR_INVALID;
+        if (Hq <= 0 || Hq % c->Hkv || Hq / c->Hkv > 4) return VC_ERR_UNSUPPORTED;
+        if ((long)scores_stride < (long)c->max_groups * c->cfg.group + c->res_cap) return VC_ERR_INVALID;
+        if (ws_bytes < draft_h2o_ws_bytes(view, Hq)) return VC_ERR_INVALID;
+        return cuda_status(
+            draft_attn_h2o(q, q_dt, view, Hq, sm_scale, out, scores, scores_stride, nullptr, 0, ws, stream));
+    }
     if (view->kind != VC_CACHE_DENSE || view->dt != VC_BF16 || q_dt != VC_BF16) return VC_ERR_UNSUPPORTED;
     if (!view->k || !view->v || !view->seq_len || view->B <= 0 || view->Hkv <= 0) return VC_ERR_INVALID;
     if (view->L_stride < view->max_len || view->max_len < 0) return VC_ERR_INVALID;
@@ -233,8 +245,8 @@ vc_status vc_draft_attn_h2o(const void *q, vc_dtype q_dt, const vc_cache_view *v
     if (!aligned(view->k, 16) || !aligned(view->v, 16) || !aligned(q, 4)) return VC_ERR_INVALID;
     if (kept_idx ? kept_stride < view->max_len : scores_stride < view->max_len) return VC_ERR_INVALID;
     if (ws_bytes < draft_h2o_ws_bytes(view, Hq)) return VC_ERR_INVALID;
-    return cuda_status(draft_attn_h2o(q, view, Hq, sm_scale, out, scores, scores_stride, kept_idx, kept_stride, ws,
-                                      stream));
+    return cuda_status(draft_attn_h2o(q, q_dt, view, Hq, sm_scale, out, scores, scores_stride, kept_idx, kept_stride,
+                                      ws, stream));
 }
 
 size_t vc_verify_attn_workspace_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int max_ctx)

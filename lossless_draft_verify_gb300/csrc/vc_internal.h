@@ -29,12 +29,12 @@ size_t draft_ws_bytes(const vc_cache_view *view, int Hq);
 cudaError_t draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq,
                        float sm_scale, void *out, void *ws, cudaStream_t st);
 
-// draft_attn.cu, H2O variant (dense bf16 views): also adds each token's
-// attention mass, summed over the query heads of its kv head, to scores.
+// draft_attn.cu, H2O variant (dense bf16 and KIVI views): also adds each
+// token's attention mass, summed over the query heads of its kv head, to scores.
 size_t draft_h2o_ws_bytes(const vc_cache_view *view, int Hq);
-cudaError_t draft_attn_h2o(const void *q, const vc_cache_view *view, int Hq, float sm_scale, void *out,
-                           float *scores, int scores_stride, const int32_t *kept_idx, int kept_stride, void *ws,
-                           cudaStream_t st);
+cudaError_t draft_attn_h2o(const void *q, vc_dtype q_dt, const vc_cache_view *view, int Hq, float sm_scale,
+                           void *out, float *scores, int scores_stride, const int32_t *kept_idx, int kept_stride,
+                           void *ws, cudaStream_t st);
 
 // verify_attn.cu
 // split_tiles > 0: fixed key splits of split_tiles x 64 keys (row results then

@@ -1,5 +1,5 @@
-"""GPU parity of the H2O score accumulation (vc_draft_attn_h2o): the attention
-mass every cached token receives, summed over the query heads of its kv head,
+"""GPU parity of the H2O score accumulation (vc_draft_attn_h2o, dense and KIVI
+views): the attention mass every cached token receives, summed over the query heads of its kv head,
 added to fp32 scores at its original position (H2O, source 3 on the podparley
 page), against the oracle's softmax weights (fp64).  Tolerance: the weights
 are normalised by the attention's own sum of bf16-rounded probabilities, so
@@ -80,3 +80,43 @@ def test_h2o_scores_through_kept_positions():
     mask = np.ones_like(got, dtype=bool)
     np.put_along_axis(mask, kp.astype(np.int64), False, axis=2)
     assert (got[mask] == 0).all()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,d,bits,R,dtype", [
+    (2, 8, 2, 1000, 128, 2, 128, torch.bfloat16),    # several splits, ragged ring
+    (1, 8, 2, 3000, 128, 4, 1024, torch.bfloat16),   # long ring over several ring splits
+    (2, 4, 2, 517, 64, 4, 0, torch.float32),         # fp32 caches (tiny-decoder shape)
+    (2, 8, 2, 100, 128, 2, 128, torch.bfloat16),     # ring only
+])
+def test_h2o_scores_on_kivi_cache(B, Hq, Hkv, L, d, bits, R, dtype):
+    """vc_draft_attn_h2o over a KIVI cache: each token's mass over the
+    dequantized cache x^ (and the full-precision ring) against the oracle's
+    softmax weights; two calls accumulate."""
+    vc = lib()
+    G = 32
+    k, v = inputs.kv_with_outliers(B, Hkv, L, d, seed=L + 5, device="cuda", dtype=dtype)
+    q = inputs.normal_bf16((B, Hq, d), L + 6, device="cuda").to(dtype)
+    maxg = max(1, (L - R) // G)
+    cache = vc.QCache(B, Hkv, d, bits, maxg, R + G + 8, R, res_dtype=dtype)
+    vc.vc_quantize_kv(k, v, cache)
+    view = cache.view()
+    cap = cache.max_groups * G + cache.res_cap
+    ws = vc.Workspace(vc.vc_draft_attn_h2o_workspace_bytes(view, Hq))
+    out = torch.empty_like(q)
+    scores = torch.zeros(B, Hkv, cap, dtype=torch.float32, device="cuda")
+    scale = inputs.default_scale(d)
+    for _ in range(2):
+        vc.vc_draft_attn_h2o(q, view, scale, out, scores, ws)
+    torch.cuda.synchronize()
+    assert vc.vc_poll_status(ws) == 0
+    # the oracle's cache: x^ = code * s + z on the quantized prefix, the ring as stored
+    qc = oracle.kivi_quantize(f32(k), f32(v), bits, G, R)
+    kh, _ = oracle.kivi_dequant(qc)
+    nq = kh.shape[2]
+    keff = np.concatenate([kh, f32(k)[:, :, nq:]], axis=2)
+    assert_attn_close(out, oracle.kivi_decode_attn(f32(q), qc, scale), what="attention output")
+    mass = oracle.h2o_mass(f32(q), keff, np.full(B, L), scale)
+    got = scores.cpu().numpy().astype(np.float64)
+    _check_mass(got[:, :, :L], 2 * mass, f"kivi b{bits} L{L}")
+    assert (got[:, :, L:] == 0).all()
+    assert np.allclose(got.sum(axis=-1), 2 * Hq // Hkv, rtol=1e-2)
