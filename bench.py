@@ -522,6 +522,23 @@ def run_kernel(args, dev):
         nbytes = 2 * k.numel() * 2 + 2 * q.numel() * 2
         flops = 4 * D_HEAD * B * HQ * sum(CTX + i + 1 for i in range(dq))
         rec = {"workload": f"verify attention, Dq={dq}, bf16 K/V [{B},8,{CTX + dq},128], 32/8 heads"}
+    elif name == "verify_h2o":
+        # verify attention plus the H2O mass pass (a second pass over K)
+        dq = args.dq
+        q = inputs.normal_bf16((B, dq, HQ, D_HEAD), 8, device=dev)
+        k = inputs.normal_bf16((B, HKV, CTX + dq, D_HEAD), 9, device=dev)
+        v = inputs.normal_bf16((B, HKV, CTX + dq, D_HEAD), 10, device=dev)
+        ctx = torch.full((B,), CTX, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        scores = torch.zeros(B, HKV, CTX + dq, dtype=torch.float32, device=dev)
+        ws = vc.Workspace(vc.vc_verify_attn_h2o_workspace_bytes(B, dq, HQ, HKV, D_HEAD, CTX), device=dev)
+        scale = inputs.default_scale(D_HEAD)
+        fn = lambda: vc.vc_verify_attn_h2o(q, k, v, ctx, CTX, scale, out, scores, ws)
+        # verify's K and V, the mass pass's K again, the scores read and written
+        nbytes = 3 * k.numel() * 2 + 2 * q.numel() * 2 + 2 * scores.numel() * 4
+        flops = 2 * 4 * D_HEAD * B * HQ * sum(CTX + i + 1 for i in range(dq))
+        rec = {"workload": f"verify attention with H2O accumulation, Dq={dq}, bf16 K/V [{B},8,{CTX + dq},128], "
+                           "32/8 heads"}
     elif name == "accept":
         case = inputs.accept_case(B, HORIZON, VOCAB, seed=0, device=dev)
         n = torch.empty(B, dtype=torch.int32, device=dev)
@@ -1164,8 +1181,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", default=None,
-                    help="time one kernel alone: draft, verify, accept, quantize, drop, dense_draft, gemm, "
-                         "unpack, swap")
+                    help="time one kernel alone: draft, verify, verify_h2o, accept, quantize, drop, dense_draft, "
+                         "dense_draft_h2o, gemm, unpack, swap")
     ap.add_argument("--dq", type=int, default=32, help="verify block size for --kernel verify")
     ap.add_argument("--batch", type=int, default=B, help="sequences for --kernel draft/verify")
     ap.add_argument("--chunks", type=int, default=1, help="side streams for --kernel swap")

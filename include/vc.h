@@ -333,6 +333,27 @@ vc_status vc_verify_attn(const void *q, const void *k, const void *v, vc_dtype d
                          int L_stride, int max_ctx, float sm_scale, void *out,
                          void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * vc_verify_attn_h2o -- vc_verify_attn that also accumulates attention
+ * scores for token dropping (H2O, source 3 on the podparley page: tokens are
+ * ranked by the attention mass they have received).  For kv unit
+ * u = b*Hkv + h and key j < ctx_len[b] + Dq:
+ *   scores[u * scores_stride + j] += sum over the block's rows (query i,
+ *       query head of h) with j <= ctx_len[b] + i of softmax_j(q . k_j * sm_scale)
+ * The probabilities use each row's final max and sum from the verify pass;
+ * a second pass over K recomputes the scores on the tensor cores.
+ * Shapes: bf16, d = 128, Hq / Hkv in {1, 2, 4, 8}, Dq * Hq / Hkv <= 272;
+ * VC_ERR_UNSUPPORTED otherwise.  scores: device fp32 with
+ * scores_stride >= max_ctx + Dq.  Workspace: vc_verify_attn_h2o_workspace_bytes
+ * (the verify pass's plus 8 bytes per row).
+ */
+size_t vc_verify_attn_h2o_workspace_bytes(int B, int Dq, int Hq, int Hkv, int d, int max_ctx);
+
+vc_status vc_verify_attn_h2o(const void *q, const void *k, const void *v, const int32_t *ctx_len, int B,
+                             int Dq, int Hq, int Hkv, int d, int L_stride, int max_ctx, float sm_scale,
+                             void *out, float *scores, int scores_stride, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* (5) greedy acceptance                                                     */
 /* ------------------------------------------------------------------------ */

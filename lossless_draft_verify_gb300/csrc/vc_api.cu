@@ -270,6 +270,27 @@ vc_status vc_verify_attn(const void *q, const void *k, const void *v, vc_dtype d
                                    ws, stream));
 }
 
+size_t vc_verify_attn_h2o_workspace_bytes(int B, int Dq, int Hq, int Hkv, int d, int max_ctx)
+{
+    if (B <= 0 || Dq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_ctx < 0) return 0;
+    if (!verify_h2o_supported(VC_BF16, Dq, Hq, Hkv, d)) return 0;
+    return verify_h2o_ws_bytes(B, Dq, Hq, Hkv, max_ctx);
+}
+
+vc_status vc_verify_attn_h2o(const void *q, const void *k, const void *v, const int32_t *ctx_len, int B, int Dq,
+                             int Hq, int Hkv, int d, int L_stride, int max_ctx, float sm_scale, void *out,
+                             float *scores, int scores_stride, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!q || !k || !v || !ctx_len || !out || !scores || !ws) return VC_ERR_INVALID;
+    if (B <= 0 || Dq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_ctx < 0) return VC_ERR_INVALID;
+    if (!verify_h2o_supported(VC_BF16, Dq, Hq, Hkv, d)) return VC_ERR_UNSUPPORTED;
+    if (L_stride < max_ctx + Dq || scores_stride < max_ctx + Dq) return VC_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(ws, 256)) return VC_ERR_INVALID;
+    if (ws_bytes < verify_h2o_ws_bytes(B, Dq, Hq, Hkv, max_ctx)) return VC_ERR_INVALID;
+    return cuda_status(verify_attn_h2o(q, k, v, ctx_len, B, Dq, Hq, Hkv, L_stride, max_ctx, sm_scale, out, scores,
+                                       scores_stride, ws, stream));
+}
+
 size_t vc_accept_workspace_bytes(int B, int D, int V)
 {
     if (B <= 0 || D < 0 || V <= 0) return 0;

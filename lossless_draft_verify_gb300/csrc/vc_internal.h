@@ -44,7 +44,15 @@ bool verify_uses_tensor_cores(vc_dtype dt, int Dq, int Hq, int Hkv, int d);
 cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt,
                         const int32_t *ctx_len, int B, int Dq, int Hq, int Hkv, int d,
                         int L_stride, int max_ctx, float sm_scale, void *out, void *ws,
-                        cudaStream_t st, int split_tiles = 0);
+                        cudaStream_t st, int split_tiles = 0, float2 *ml = nullptr);
+// H2O variant (tensor-core shapes, Dq * Hq / Hkv <= 272 rows): the verify
+// pass, then each key's attention mass summed over the block's rows added to
+// scores (a second pass over K with the rows' final max and sum).
+size_t verify_h2o_ws_bytes(int B, int Dq, int Hq, int Hkv, int max_ctx);
+bool verify_h2o_supported(vc_dtype dt, int Dq, int Hq, int Hkv, int d);
+cudaError_t verify_attn_h2o(const void *q, const void *k, const void *v, const int32_t *ctx_len, int B, int Dq,
+                            int Hq, int Hkv, int L_stride, int max_ctx, float sm_scale, void *out, float *scores,
+                            int scores_stride, void *ws, cudaStream_t st);
 
 // drop.cu
 size_t drop_ws_bytes(int B, int H, int L);

@@ -30,6 +30,8 @@
 // (row, key slice), fp32 throughout.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "tcgen05.cuh"
 #include "vc_common.cuh"
 #include "vc_internal.h"
@@ -600,7 +602,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 // Merge the key splits of the tensor-core kernel.  One thread per (row, 4 channels).
 template <typename T>
 __global__ void verify_tc_combine(const float *__restrict__ part, int n_split, int n_mtiles, int Hkv,
-                                  int Hq, int Dq, int grp, T *__restrict__ out)
+                                  int Hq, int Dq, int grp, T *__restrict__ out, float2 *__restrict__ ml)
 {
     pdl_wait();
     pdl_trigger();
@@ -627,6 +629,7 @@ __global__ void verify_tc_combine(const float *__restrict__ part, int n_split, i
         o[3] += v.w * w;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
+    if (ml && c0 == 0) ml[((size_t)b * Dq + qi) * Hq + kvh * grp + r % grp] = make_float2(M, L);
     T *dst = out + (((size_t)b * Dq + qi) * Hq + kvh * grp + r % grp) * TC_D + c0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[i] = Elem<T>::from_f(o[i] * inv);
@@ -743,6 +746,163 @@ TcPlan tc_plan(int B, int Dq, int Hkv, int grp, int max_ctx, int split_tiles)
     return p;
 }
 
+// ===================================================== H2O mass of a verify ==
+// The attention mass each key receives from the verify block (H2O ranks
+// tokens by accumulated attention, source 3 on the podparley page): for kv
+// unit u and key j < ctx_len[b] + Dq, the sum over the block's rows (query i,
+// head of the unit's group) that see j (j <= ctx + i) of
+// exp2(q.k * scale_log2 - M_row) / L_row, with M_row and L_row the row's final
+// max and sum from the verify pass.  The scores are recomputed on the tensor
+// cores with the keys on the MMA's M side and the rows on its N side, so a
+// warp finishes the mass of its 16 keys on its own: the CTA stages the unit's
+// Q rows (and each row's max and 1/sum) once, then every warp streams its own
+// 16-key K tiles through a two-stage ring (one bulk copy per key row, padded
+// rows for conflict-free ldmatrix), sums the weights over all rows, and adds
+// each key's mass to scores[u * scores_stride + j] (each key by one warp).
+constexpr int H2O_KT = 16;                      // keys per warp tile
+constexpr int H2O_PITCH = TC_D * 2 + 16;        // bytes per staged row
+constexpr int H2O_MAXROWS = 272;                // Dq * grp
+constexpr int H2O_WARPS = 8;
+
+struct H2oParams {
+    const __nv_bfloat16 *q, *k;
+    const int32_t *ctx_len;
+    const float2 *ml;
+    float *scores;
+    int32_t *status;
+    int Dq, Hq, Hkv, grp, L_stride, keys_per_split, scores_stride, rows_pad;
+    float scale_log2;
+};
+
+__global__ void __launch_bounds__(H2O_WARPS * 32)
+verify_h2o_mass_kernel(H2oParams P)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(128) uint8_t hsm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(hsm);                               // [warps][2]
+    float4 *mlv = reinterpret_cast<float4 *>(hsm + 256);                              // [rows_pad / 2]: (M, 1/L) x 2
+    uint8_t *qs = hsm + 256 + P.rows_pad * 8;                                        // [rows_pad][PITCH]
+    uint8_t *ring = qs + P.rows_pad * H2O_PITCH + warp * 2 * H2O_KT * H2O_PITCH;     // this warp's [2][16][PITCH]
+    const int unit = blockIdx.y, b = unit / P.Hkv, kvh = unit % P.Hkv;
+    const int rows = P.Dq * P.grp;
+    const int ctx = P.ctx_len[b];
+    const int n_keys = ctx + P.Dq;
+    const int k_lo = blockIdx.x * P.keys_per_split;
+    const int k_hi = min(n_keys, k_lo + P.keys_per_split);
+    if (k_lo >= k_hi) return;
+    // the unit's rows: Q (bf16, zero beyond `rows`) and (M, 1/L)
+    for (int i = threadIdx.x; i < P.rows_pad * (TC_D / 8); i += blockDim.x) {
+        const int r = i / (TC_D / 8), ch = i % (TC_D / 8);
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows) {
+            const size_t row = ((size_t)b * P.Dq + r / P.grp) * P.Hq + kvh * P.grp + r % P.grp;
+            u = *reinterpret_cast<const uint4 *>(P.q + row * TC_D + ch * 8);
+        }
+        *reinterpret_cast<uint4 *>(qs + r * H2O_PITCH + ch * 16) = u;
+    }
+    for (int i = threadIdx.x; i < P.rows_pad / 2; i += blockDim.x) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * i + e;
+            if (r < rows) {
+                const float2 m = P.ml[((size_t)b * P.Dq + r / P.grp) * P.Hq + kvh * P.grp + r % P.grp];
+                v[2 * e] = m.x;
+                v[2 * e + 1] = m.y > 0.f ? 1.f / m.y : 0.f;
+            }
+        }
+        mlv[i] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    uint64_t *bar = bars + 2 * warp;
+    if (lane == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const __nv_bfloat16 *kb = P.k + (size_t)unit * P.L_stride * TC_D;
+    const int nwarps = blockDim.x >> 5;
+    // key tiles of this warp: k_lo + 16 (warp + i * nwarps)
+    auto issue = [&](int key0, int s) {
+        const int nk = min(H2O_KT, k_hi - key0);
+        if (lane == 0) mbar_arrive_expect_tx(&bar[s], (uint32_t)nk * TC_D * 2);
+        __syncwarp();
+        if (lane < nk) bulk_g2s(ring + (s * H2O_KT + lane) * H2O_PITCH, kb + (size_t)(key0 + lane) * TC_D, TC_D * 2,
+                                &bar[s]);
+    };
+    const int step = H2O_KT * nwarps;
+    int key0 = k_lo + H2O_KT * warp;
+    if (key0 < k_hi) issue(key0, 0);
+    if (key0 + step < k_hi) issue(key0 + step, 1);
+    const uint32_t qs_u = smem_u32(qs);
+    const int n_nt = P.rows_pad / 8;
+    for (int it = 0; key0 < k_hi; key0 += step, ++it) {
+        const int s = it & 1;
+        if (!mbar_wait(&bar[s], (it >> 1) & 1)) {
+            report_timeout(P.status, 51);
+            if (key0 + step < k_hi) mbar_wait(&bar[s ^ 1], ((it + 1) >> 1) & 1);
+            return;
+        }
+        const uint32_t st = smem_u32(ring + s * H2O_KT * H2O_PITCH);
+        // A = K rows of the tile: keys (lane & 7) + 8 ((lane >> 3) & 1), chunk 2 ks + (lane >> 4)
+        uint32_t ka[TC_D / 16][4];
+#pragma unroll
+        for (int ks = 0; ks < TC_D / 16; ++ks)
+            ldsm_x4(st + ((lane & 7) + 8 * ((lane >> 3) & 1)) * H2O_PITCH + (2 * ks + (lane >> 4)) * 16, ka[ks][0],
+                    ka[ks][1], ka[ks][2], ka[ks][3]);
+        // the stage has been read (generic proxy): release it to the refill
+        fence_async_smem();
+        __syncwarp();
+        if (key0 + 2 * step < k_hi) issue(key0 + 2 * step, s);
+        const int klo = key0 + gid, khi = key0 + gid + 8;    // this lane's two keys
+        const bool all_visible = key0 + H2O_KT - 1 < ctx;     // every row sees every key of the tile
+        float mlo = 0.f, mhi = 0.f;
+#pragma unroll 2
+        for (int nt = 0; nt < n_nt; ++nt) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kp = 0; kp < TC_D / 32; ++kp) {
+                // B = Q^T: rows 8 nt + (lane & 7), chunks 4 kp + (lane >> 3)
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(qs_u + (8 * nt + (lane & 7)) * H2O_PITCH + (4 * kp + (lane >> 3)) * 16, b0, b1, b2, b3);
+                mma_bf16_16816(c, ka[2 * kp][0], ka[2 * kp][1], ka[2 * kp][2], ka[2 * kp][3], b0, b1);
+                mma_bf16_16816(c, ka[2 * kp + 1][0], ka[2 * kp + 1][1], ka[2 * kp + 1][2], ka[2 * kp + 1][3], b2, b3);
+            }
+            // rows 8 nt + 2 tig + e: (M, 1/L)
+            const float4 ml = mlv[4 * nt + tig];
+            float p[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = i & 1;
+                p[i] = ex2(c[i] * P.scale_log2 - (e ? ml.z : ml.x)) * (e ? ml.w : ml.y);
+            }
+            if (!all_visible) {
+                // keys of the block itself: row r (query r / grp) sees keys <= ctx + r / grp
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 8 * nt + 2 * tig + (i & 1);
+                    const int key = (i >> 1) ? khi : klo;
+                    if (key > ctx + r / P.grp) p[i] = 0.f;
+                }
+            }
+            mlo += p[0] + p[1];
+            mhi += p[2] + p[3];
+        }
+        mlo += __shfl_xor_sync(0xffffffffu, mlo, 1);
+        mlo += __shfl_xor_sync(0xffffffffu, mlo, 2);
+        mhi += __shfl_xor_sync(0xffffffffu, mhi, 1);
+        mhi += __shfl_xor_sync(0xffffffffu, mhi, 2);
+        if (tig == 0) {
+            float *dst = P.scores + (size_t)unit * P.scores_stride;
+            if (klo < k_hi) atomicAdd(dst + klo, mlo);
+            if (khi < k_hi) atomicAdd(dst + khi, mhi);
+        }
+    }
+}
+
 }  // namespace
 
 bool verify_uses_tensor_cores(vc_dtype dt, int Dq, int Hq, int Hkv, int d)
@@ -760,7 +920,7 @@ size_t verify_ws_bytes(vc_dtype dt, int B, int Dq, int Hq, int Hkv, int d, int m
 
 cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt, const int32_t *ctx_len,
                         int B, int Dq, int Hq, int Hkv, int d, int L_stride, int max_ctx, float sm_scale,
-                        void *out, void *ws, cudaStream_t st, int split_tiles)
+                        void *out, void *ws, cudaStream_t st, int split_tiles, float2 *ml)
 {
     const float sl2 = sm_scale * kLog2e;
     if (verify_uses_tensor_cores(dt, Dq, Hq, Hkv, d)) {
@@ -807,7 +967,7 @@ cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt
         if (e != cudaSuccess) return e;
         dim3 cgrid(B * Hkv * pl.n_mtiles, TC_M / 4);
         return launch_pdl(verify_tc_combine<__nv_bfloat16>, cgrid, dim3(128), 0, st, (const float *)P.part,
-                          pl.n_split, pl.n_mtiles, Hkv, Hq, Dq, grp, (__nv_bfloat16 *)out);
+                          pl.n_split, pl.n_mtiles, Hkv, Hq, Dq, grp, (__nv_bfloat16 *)out, ml);
     }
     const int rows = B * Dq * Hq;
     if (rows == 0) return cudaSuccess;
@@ -831,6 +991,53 @@ cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt
                 (float *)out);
     }
     return cudaGetLastError();
+}
+
+size_t verify_h2o_ws_bytes(int B, int Dq, int Hq, int Hkv, int max_ctx)
+{
+    return verify_ws_bytes(VC_BF16, B, Dq, Hq, Hkv, TC_D, max_ctx) + align256((size_t)B * Dq * Hq * 8);
+}
+
+bool verify_h2o_supported(vc_dtype dt, int Dq, int Hq, int Hkv, int d)
+{
+    return verify_uses_tensor_cores(dt, Dq, Hq, Hkv, d) && Dq * (Hq / Hkv) <= H2O_MAXROWS;
+}
+
+cudaError_t verify_attn_h2o(const void *q, const void *k, const void *v, const int32_t *ctx_len, int B, int Dq,
+                            int Hq, int Hkv, int L_stride, int max_ctx, float sm_scale, void *out, float *scores,
+                            int scores_stride, void *ws, cudaStream_t st)
+{
+    const size_t main_ws = verify_ws_bytes(VC_BF16, B, Dq, Hq, Hkv, TC_D, max_ctx);
+    float2 *ml = (float2 *)((uint8_t *)ws + main_ws);
+    cudaError_t e = verify_attn(q, k, v, VC_BF16, ctx_len, B, Dq, Hq, Hkv, TC_D, L_stride, max_ctx, sm_scale, out,
+                                ws, st, 0, ml);
+    if (e != cudaSuccess) return e;
+    H2oParams P;
+    P.q = (const __nv_bfloat16 *)q;
+    P.k = (const __nv_bfloat16 *)k;
+    P.ctx_len = ctx_len;
+    P.ml = ml;
+    P.scores = scores;
+    P.status = (int32_t *)ws;
+    P.Dq = Dq;
+    P.Hq = Hq;
+    P.Hkv = Hkv;
+    P.grp = Hq / Hkv;
+    P.L_stride = L_stride;
+    P.scores_stride = scores_stride;
+    P.scale_log2 = sm_scale * kLog2e;
+    const int units = B * Hkv;
+    const int rows = Dq * P.grp;
+    P.rows_pad = (rows + 7) / 8 * 8;
+    const int n_keys = max_ctx + Dq;
+    // about two CTAs per SM over the units; splits of whole 16-key tiles per warp pass
+    const int want = std::max(1, (2 * device_sm_count() + units - 1) / units);
+    const int per = (n_keys + want - 1) / want;
+    P.keys_per_split = (per + H2O_KT * H2O_WARPS - 1) / (H2O_KT * H2O_WARPS) * (H2O_KT * H2O_WARPS);
+    const int smem = 256 + P.rows_pad * 8 + P.rows_pad * H2O_PITCH + H2O_WARPS * 2 * H2O_KT * H2O_PITCH;
+    cudaFuncSetAttribute(verify_h2o_mass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    dim3 grid((n_keys + P.keys_per_split - 1) / P.keys_per_split, units);
+    return launch_pdl(verify_h2o_mass_kernel, grid, dim3(32 * H2O_WARPS), smem, st, P);
 }
 
 }  // namespace vc

@@ -113,6 +113,11 @@ def load() -> ctypes.CDLL:
     L.vc_verify_attn.restype = c_int
     L.vc_verify_attn.argtypes = [P, P, P, c_int, P, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                                  P, P, c_size_t, P]
+    L.vc_verify_attn_h2o_workspace_bytes.restype = c_size_t
+    L.vc_verify_attn_h2o_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int]
+    L.vc_verify_attn_h2o.restype = c_int
+    L.vc_verify_attn_h2o.argtypes = [P, P, P, P, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, P, P,
+                                     c_int, P, c_size_t, P]
     L.vc_accept_workspace_bytes.restype = c_size_t
     L.vc_accept_workspace_bytes.argtypes = [c_int, c_int, c_int]
     L.vc_accept.restype = c_int
@@ -179,7 +184,8 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_decoder_set_trace", "vc_decoder_trace_count", "vc_gemm_splits",
             "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe",
             "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify",
-            "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack", "vc_kv_writeback_packed"]
+            "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack", "vc_kv_writeback_packed",
+            "vc_verify_attn_h2o_workspace_bytes", "vc_verify_attn_h2o"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -381,6 +387,22 @@ def vc_verify_attn(q, k, v, ctx_len, max_ctx: int, sm_scale: float, out, ws: Wor
     _check(load().vc_verify_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), ctx_len.data_ptr(), B, Dq, Hq,
                                  Hkv, d, Ls, int(max_ctx), sm_scale, out.data_ptr(), ws.ptr, ws.nbytes,
                                  _stream(stream)), "vc_verify_attn")
+
+
+def vc_verify_attn_h2o_workspace_bytes(B, Dq, Hq, Hkv, d, max_ctx) -> int:
+    return int(load().vc_verify_attn_h2o_workspace_bytes(B, Dq, Hq, Hkv, d, max_ctx))
+
+
+def vc_verify_attn_h2o(q, k, v, ctx_len, max_ctx: int, sm_scale: float, out, scores, ws: Workspace, stream=None):
+    """vc_verify_attn plus H2O accumulation into scores fp32 [B][Hkv][S]
+    (S >= max_ctx + Dq: one entry per key position)."""
+    B, Dq, Hq, d = q.shape
+    _, Hkv, Ls, _ = k.shape
+    assert q.is_contiguous() and k.is_contiguous() and v.is_contiguous() and ctx_len.dtype == torch.int32
+    assert scores.dtype == torch.float32 and scores.is_contiguous() and scores.shape[:2] == (B, Hkv)
+    _check(load().vc_verify_attn_h2o(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctx_len.data_ptr(), B, Dq, Hq, Hkv,
+                                     d, Ls, int(max_ctx), sm_scale, out.data_ptr(), scores.data_ptr(),
+                                     scores.shape[2], ws.ptr, ws.nbytes, _stream(stream)), "vc_verify_attn_h2o")
 
 
 def vc_accept_workspace_bytes(B, D, V) -> int:

@@ -120,3 +120,40 @@ def test_h2o_scores_on_kivi_cache(B, Hq, Hkv, L, d, bits, R, dtype):
     _check_mass(got[:, :, :L], 2 * mass, f"kivi b{bits} L{L}")
     assert (got[:, :, L:] == 0).all()
     assert np.allclose(got.sum(axis=-1), 2 * Hq // Hkv, rtol=1e-2)
+
+
+@pytest.mark.parametrize("B,Dq,Hq,Hkv,ctx", [
+    (2, 33, 8, 2, 1500),       # the acceptance block (Dq = D + 1), tail rows of the verify kernel
+    (3, 32, 8, 2, 700),        # one full 128-row tile
+    (1, 5, 8, 8, 300),         # grp 1
+    (2, 17, 16, 2, 2000),      # grp 8: 136 rows
+])
+def test_verify_h2o_scores_match_oracle(B, Dq, Hq, Hkv, ctx):
+    """vc_verify_attn_h2o: the verify output is unchanged and every key gets
+    the attention mass of the block's rows that see it (causal within the
+    block), against the oracle's softmax weights summed over the queries."""
+    vc = lib()
+    d = 128
+    q = inputs.normal_bf16((B, Dq, Hq, d), 31, device="cuda")
+    k = inputs.normal_bf16((B, Hkv, ctx + Dq, d), 32, device="cuda")
+    v = inputs.normal_bf16((B, Hkv, ctx + Dq, d), 33, device="cuda")
+    lens = [ctx, max(ctx - 111, 0), ctx // 2][:B]
+    ctx_len = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    scale = inputs.default_scale(d)
+    out = torch.empty_like(q)
+    ws = vc.Workspace(vc.vc_verify_attn_h2o_workspace_bytes(B, Dq, Hq, Hkv, d, ctx))
+    scores = torch.zeros(B, Hkv, ctx + Dq, dtype=torch.float32, device="cuda")
+    vc.vc_verify_attn_h2o(q, k, v, ctx_len, ctx, scale, out, scores, ws)
+    torch.cuda.synchronize()
+    assert vc.vc_poll_status(ws) == 0
+    want_o = oracle.verify_attn(f32(q), f32(k), f32(v), lens, scale)
+    assert_attn_close(out, want_o, what="verify output")
+    # mass: sum over the block's queries i of the decode mass over keys 0 .. ctx + i
+    mass = np.zeros((B, Hkv, ctx + Dq))
+    for i in range(Dq):
+        mass += oracle.h2o_mass(f32(q[:, i]), f32(k), np.array(lens) + i + 1, scale)
+    got = scores.cpu().numpy().astype(np.float64)
+    _check_mass(got, mass, f"verify Dq{Dq} grp{Hq // Hkv}")
+    for b, n in enumerate(lens):
+        assert (got[b, :, n + Dq:] == 0).all()
+        assert np.allclose(got[b].sum(axis=-1), Dq * Hq // Hkv, rtol=1e-2)
