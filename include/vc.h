@@ -366,7 +366,8 @@ vc_status vc_verify_attn_h2o(const void *q, const void *k, const void *v, const 
  * logits: device [B][D+1][V] in dt (finite values); drafts: device int32
  * [B][D]; n_acc, next_tok: device int32 [B].  Limits: D <= 1024 and
  * B * (D + 1) <= 65535 rows; larger requests return VC_ERR_INVALID and
- * enqueue nothing.
+ * enqueue nothing.  The workspace's per-sequence counters are left at zero
+ * by every call, so a workspace zero-filled once serves any number of calls.
  */
 size_t vc_accept_workspace_bytes(int B, int D, int V);
 

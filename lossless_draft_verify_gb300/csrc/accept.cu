@@ -6,9 +6,9 @@
 // contiguous slice with 128-bit streaming loads and reduces (value, index)
 // pairs -- larger value wins, equal values keep the lower index, so -0 and +0
 // tie -- through warp shuffles and shared memory.  The last CTA to finish a
-// sequence (device-scope counter) folds the split partials of its D+1 rows,
-// finds the first row whose argmax differs from the draft, and writes
-// n_acc and next_tok.  HBM-bound: the algorithmic traffic is the logits once.
+// sequence (device-scope counter, returned to zero by that CTA) folds the split
+// partials of its D+1 rows, finds the first row whose argmax differs from the
+// draft, and writes n_acc and next_tok.  HBM-bound: the algorithmic traffic is the logits once.
 #include "vc_common.cuh"
 #include "vc_internal.h"
 
@@ -67,7 +67,7 @@ __device__ __forceinline__ void scan_vec(const T *row, int lo, int hi, ArgMax &b
     constexpr int PER = 16 / sizeof(T);
     // lo, hi are multiples of PER; row is 16-byte aligned
     int i = lo + threadIdx.x * PER;
-    constexpr int UNROLL = 4;
+    constexpr int UNROLL = 8;
     for (; i + (UNROLL - 1) * kThreads * PER < hi; i += UNROLL * kThreads * PER) {
         uint4 u[UNROLL];
 #pragma unroll
@@ -118,6 +118,8 @@ accept_kernel(const T *__restrict__ logits, const int32_t *__restrict__ drafts, 
               int V, int S, int chunk, int32_t *__restrict__ n_acc, int32_t *__restrict__ next_tok,
               void *ws)
 {
+    pdl_wait();
+    pdl_trigger();
     const WsLayout W = ws_layout(ws, B);
     const int s = blockIdx.x, row = blockIdx.y;
     const int b = row / (D + 1);
@@ -172,29 +174,33 @@ accept_kernel(const T *__restrict__ logits, const int32_t *__restrict__ drafts, 
             if (amax[i] != drafts[(size_t)b * D + i]) { n = i; break; }
         n_acc[b] = n;
         next_tok[b] = amax[n];
+        W.counters[b] = 0u;                 // every CTA of b has arrived: ready for the next call
     }
 }
 
 template <typename T>
 cudaError_t launch(const void *logits, const int32_t *drafts, int B, int D, int V, int32_t *n_acc,
-                   int32_t *next_tok, void *ws, cudaStream_t st)
+                   int32_t *next_tok, void *ws, bool clear_counters, cudaStream_t st)
 {
     constexpr int PER = 16 / sizeof(T);
     const WsLayout W = ws_layout(ws, B);
-    cudaError_t e = cudaMemsetAsync(W.counters, 0, (size_t)B * 4, st);
-    if (e != cudaSuccess) return e;
+    if (clear_counters) {
+        const cudaError_t e = cudaMemsetAsync(W.counters, 0, (size_t)B * 4, st);
+        if (e != cudaSuccess) return e;
+    }
     const int S = splits_for(V);
     const bool vec = ((uintptr_t)logits % 16 == 0) && (V % PER == 0);
     int chunk = cdiv(V, S);
     if (vec) chunk = cdiv(chunk, PER) * PER;
     dim3 grid(S, B * (D + 1));
-    if (vec)
-        accept_kernel<T, true><<<grid, kThreads, 0, st>>>((const T *)logits, drafts, B, D, V, S,
-                                                          chunk, n_acc, next_tok, ws);
-    else
-        accept_kernel<T, false><<<grid, kThreads, 0, st>>>((const T *)logits, drafts, B, D, V, S,
-                                                           chunk, n_acc, next_tok, ws);
-    return cudaGetLastError();
+    auto kern = vec ? accept_kernel<T, true> : accept_kernel<T, false>;
+    if (clear_counters) {
+        // after the memset: a plain launch (the kernel's grid-dependency wait is then a no-op)
+        kern<<<grid, kThreads, 0, st>>>((const T *)logits, drafts, B, D, V, S, chunk, n_acc, next_tok, ws);
+        return cudaGetLastError();
+    }
+    return launch_pdl(kern, grid, dim3(kThreads), 0, st, (const T *)logits, drafts, B, D, V, S, chunk, n_acc,
+                      next_tok, ws);
 }
 
 // Acceptance from the LM head's tile maxima ([B][D+1][n_tiles] value and
@@ -248,10 +254,10 @@ size_t accept_ws_bytes(int B, int D, int V)
 }
 
 cudaError_t accept(const void *logits, vc_dtype dt, const int32_t *drafts, int B, int D, int V,
-                   int32_t *n_acc, int32_t *next_tok, void *ws, cudaStream_t st)
+                   int32_t *n_acc, int32_t *next_tok, void *ws, cudaStream_t st, bool clear_counters)
 {
-    return dt == VC_BF16 ? launch<__nv_bfloat16>(logits, drafts, B, D, V, n_acc, next_tok, ws, st)
-                         : launch<float>(logits, drafts, B, D, V, n_acc, next_tok, ws, st);
+    return dt == VC_BF16 ? launch<__nv_bfloat16>(logits, drafts, B, D, V, n_acc, next_tok, ws, clear_counters, st)
+                         : launch<float>(logits, drafts, B, D, V, n_acc, next_tok, ws, clear_counters, st);
 }
 
 }  // namespace vc

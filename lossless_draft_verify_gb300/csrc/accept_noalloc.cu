@@ -130,6 +130,6 @@ extern "C" vc_status vc_accept_noalloc(const void *logits, vc_dtype dt, const in
     void *ws = nullptr;
     const vc_status s = scratch_for_current_device(&ws);
     if (s != VC_OK) return s;
-    const cudaError_t e = vc::accept(logits, dt, drafts, B, D, V, n_acc, next_tok, ws, stream);
+    const cudaError_t e = vc::accept(logits, dt, drafts, B, D, V, n_acc, next_tok, ws, stream, true);
     return e == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }

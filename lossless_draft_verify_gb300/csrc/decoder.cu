@@ -395,7 +395,9 @@ cudaError_t greedy_head(const Ctx &C, const void *h, int B, int D, const int32_t
         return gemm(h, C.d->head, nullptr, C.at(C.L.lsc), c.dt, M, c.vocab, c.d_model, c.d_model, C.at(C.L.part),
                     C.counters(), C.status(), C.st, C.plan);
     }));
-    return accept(C.at(C.L.lsc), c.dt, drafts, B, D, c.vocab, n_acc, next_tok, C.at(C.L.aws), C.st);
+    // the workspace layout depends on the call's shape, so other buffers may
+    // have used these bytes since the last acceptance: clear its counters
+    return accept(C.at(C.L.lsc), c.dt, drafts, B, D, c.vocab, n_acc, next_tok, C.at(C.L.aws), C.st, true);
 }
 
 template <typename T>
@@ -516,7 +518,7 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
                         C.status(), C.st, C.plan);
         }));
         VC_TRY(accept(logits, c.dt, nullptr, B, 0, c.vocab, C.at<int32_t>(C.L.nacc), next_tok, C.at(C.L.aws),
-                      C.st));
+                      C.st, true));
     } else {
         VC_TRY(greedy_head(C, h, B, 0, nullptr, C.at<int32_t>(C.L.nacc), next_tok));
     }

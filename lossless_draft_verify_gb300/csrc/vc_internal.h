@@ -21,8 +21,10 @@ cudaError_t qcache_append(const vc_qcache *c, const void *k_new, const void *v_n
 size_t accept_ws_bytes(int B, int D, int V);
 cudaError_t accept_tiles(const float *tile_max, const int32_t *tile_idx, int n_tiles, const int32_t *drafts,
                          int B, int D, int32_t *n_acc, int32_t *next_tok, cudaStream_t st);
+// The per-sequence counters in ws are left at zero by every call; with
+// clear_counters they are also zeroed on the stream first.
 cudaError_t accept(const void *logits, vc_dtype dt, const int32_t *drafts, int B, int D, int V,
-                   int32_t *n_acc, int32_t *next_tok, void *ws, cudaStream_t st);
+                   int32_t *n_acc, int32_t *next_tok, void *ws, cudaStream_t st, bool clear_counters = false);
 
 // draft_attn.cu
 size_t draft_ws_bytes(const vc_cache_view *view, int Hq);
