@@ -132,10 +132,15 @@ vc_status vc_wait_probe(void *ws, size_t ws_bytes, cudaStream_t stream);
  *       4-bit, h = W/2: word = 2 (kappa % h) + mu/2, slot = kappa/h + 2 (mu % 2).
  *     (Every class keeps one power-of-two factor through the draft kernel's
  *     shift-free unpacking; the kernel cancels it per channel.)
- *   Meta sections (4d bytes each), for lane quad j in [0,4): fp16 pair n of
- *     quad j at byte 16*(4*(n/4) + j) + 4*(n%4), zero-point pair at the same
- *     offset + 2d.  K: n = 2 ks + rr holds (s[c0], s[c0+1]), c0 = 16 ks + 2 j +
- *     8 rr.  V: n = (2 ks + rr)*(d/32) + gc holds (s[t0][gc], s[t0+1][gc]),
+ *   K meta section (4d bytes): for lane quad j in [0,4) and k-step ks in
+ *     [0, d/16), the 16 bytes at 16*(4 ks + j) hold, for rr = 0 then rr = 1,
+ *     the fp16 zero-point pair (z[c0], z[c0+1]) and then the scale pair
+ *     (s[c0], s[c0+1]), c0 = 16 ks + 2 j + 8 rr (zero pair at + 8 rr, scale
+ *     pair at + 8 rr + 4): one 16-byte load is both the scales of a k-step and
+ *     the operand of the draft kernel's zero-point MMA.
+ *   V meta section (4d bytes): fp16 pair n of quad j at byte
+ *     16*(4*(n/4) + j) + 4*(n%4), zero-point pair at the same offset + 2d;
+ *     n = (2 ks + rr)*(d/32) + gc holds (s[t0][gc], s[t0+1][gc]),
  *     t0 = 16 ks + 2 j + 8 rr.
  * Rotated cache (rotate = 1; RotateKV, named among the compressors on the
  * paper page, "What the paper found"; the library's reading is a fixed

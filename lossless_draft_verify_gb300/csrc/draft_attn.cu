@@ -242,10 +242,14 @@ __device__ void last_cta_combine(const float *unit_part, int n_split, unsigned i
 
 // Scores of one group: sc[mt][4] (rows = tokens 16 mt + gid (+8), columns =
 // heads 2 tig + {0,1}) with the zero-point term folded in.
-// ksrc: this lane's K-scale pairs (record, or ones for the head copies 4..7);
-// zsrc: this lane's bias-tile row (K zeros for row 1, zeros otherwise).
+// kmeta: this lane quad's K meta chunks (the record's, or fp16 ones for the
+// head copies 4..7 on lanes gid >= 4).  The chunk of k-step ks is
+// {z pair rr=0, s pair rr=0, z pair rr=1, s pair rr=1}: as loaded it is the
+// A operand of the zero-point MMA (rows gid: the zero-points, rows gid + 8:
+// the scales, whose products land in output rows that are never read), and
+// its scale pairs scale q into the B operand.
 template <int BITS, int D>
-__device__ __forceinline__ void group_scores(const uint8_t *rec, const uint8_t *ksrc, const uint8_t *zsrc,
+__device__ __forceinline__ void group_scores(const uint8_t *rec, const uint8_t *kmeta,
                                              const uint32_t (&qf)[D / 16][2], int lane, int tig,
                                              float (&sc)[2][4])
 {
@@ -263,29 +267,21 @@ __device__ __forceinline__ void group_scores(const uint8_t *rec, const uint8_t *
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
 #pragma unroll
-    for (int c = 0; c < KS / 2; ++c) {
-        // quad tig's pairs n = 4c .. 4c+3, i.e. (ks, rr) = (2c, 0), (2c, 1), (2c+1, 0), (2c+1, 1)
-        const uint4 su = *reinterpret_cast<const uint4 *>(ksrc + 16 * (4 * c + tig));
-        const uint4 zu = *reinterpret_cast<const uint4 *>(zsrc + 16 * (4 * c + tig));
-        const uint32_t sp[4] = {su.x, su.y, su.z, su.w};
-        const uint32_t zp[4] = {zu.x, zu.y, zu.z, zu.w};
+    for (int ks = 0; ks < KS; ++ks) {
+        const uint4 m = *reinterpret_cast<const uint4 *>(kmeta + 16 * (4 * ks + tig));
+        const uint32_t b0 = hmul2(qf[ks][0], m.y);
+        const uint32_t b1 = hmul2(qf[ks][1], m.w);
+        const uint32_t ab[4] = {m.x, m.y, m.z, m.w};
+        mma16816(cb, ab, b0, b1);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int ks = 2 * c + h;
-            const uint32_t b0 = hmul2(qf[ks][0], sp[2 * h]);
-            const uint32_t b1 = hmul2(qf[ks][1], sp[2 * h + 1]);
-            const uint32_t ab[4] = {zp[2 * h], 0u, zp[2 * h + 1], 0u};
-            mma16816(cb, ab, b0, b1);
+        for (int mt = 0; mt < 2; ++mt) {
+            uint32_t a[4];
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                uint32_t a[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) a[r] = unpack<BITS, D>(w0, w1, 2 * ks + (r >> 1), 2 * mt + (r & 1));
-                mma16816(sc[mt], a, b0, b1);
-            }
+            for (int r = 0; r < 4; ++r) a[r] = unpack<BITS, D>(w0, w1, 2 * ks + (r >> 1), 2 * mt + (r & 1));
+            mma16816(sc[mt], a, b0, b1);
         }
     }
-    // row 1 of the bias tile, columns 4..7 = sum of z * q for heads 0..3
+    // rows 0..3 of the bias tile, columns 4..7 = sum of z * q for heads 0..3
     const int t1 = tig & 1;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -381,8 +377,8 @@ draft_kivi_kernel(KiviParams P)
     constexpr int STAGE = 2 * REC;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);               // [NW][NST]
-    uint8_t *ones = smem + 128;                                         // 2D bytes of fp16 1.0
-    uint8_t *zeros = ones + 2 * D;                                      // 2D bytes of 0
+    uint8_t *ones = smem + 128;                                         // 4D bytes of fp16 1.0 (a K meta section)
+    uint8_t *zeros = ones + 4 * D;                                      // 2D bytes of 0
     float *rq = reinterpret_cast<float *>(zeros + 2 * D);               // [4][D] rotated queries (ROT)
     uint8_t *ring = zeros + 2 * D + (ROT ? 16 * D : 0);                 // [NW][NST][2 records]
     float *wbuf = reinterpret_cast<float *>(ring);                      // reused after the loop
@@ -396,10 +392,8 @@ draft_kivi_kernel(KiviParams P)
     float *dst = P.part + ((size_t)unit * n_split + split) * part_floats(D);
     const TQ *qg = reinterpret_cast<const TQ *>(P.q) + ((size_t)b * P.Hq + kvh * grp) * D;
 
-    for (int i = threadIdx.x; i < D / 2; i += kThreads) {
-        reinterpret_cast<uint32_t *>(ones)[i] = kOnes;
-        reinterpret_cast<uint32_t *>(zeros)[i] = 0u;
-    }
+    for (int i = threadIdx.x; i < D; i += kThreads) reinterpret_cast<uint32_t *>(ones)[i] = kOnes;
+    for (int i = threadIdx.x; i < D / 2; i += kThreads) reinterpret_cast<uint32_t *>(zeros)[i] = 0u;
 
     if (split < P.n_split_q) {
         // ---------------------------------------------- quantized groups --
@@ -467,16 +461,8 @@ draft_kivi_kernel(KiviParams P)
             // ---- scores of both groups (no branch between them, so their
             // instructions can interleave)
             float sc[2][2][4];
-            {
-                const uint8_t *ks_src = gid < 4 ? recA + Gm::KM : ones;
-                const uint8_t *z_src = gid == 1 ? recA + Gm::KM + 2 * D : zeros;
-                group_scores<BITS, D>(recA, ks_src, z_src, qf, lane, tig, sc[0]);
-            }
-            {
-                const uint8_t *ks_src = gid < 4 ? recB + Gm::KM : ones;
-                const uint8_t *z_src = gid == 1 ? recB + Gm::KM + 2 * D : zeros;
-                group_scores<BITS, D>(recB, ks_src, z_src, qf, lane, tig, sc[1]);
-            }
+            group_scores<BITS, D>(recA, gid < 4 ? recA + Gm::KM : ones, qf, lane, tig, sc[0]);
+            group_scores<BITS, D>(recB, gid < 4 ? recB + Gm::KM : ones, qf, lane, tig, sc[1]);
             if (!two) {
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) sc[1][mt][0] = sc[1][mt][1] = sc[1][mt][2] = sc[1][mt][3] = kNegBig;
@@ -1281,8 +1267,8 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     P.res_per_split = pl.res_per_split;
     P.qscale = scale * kLog2e;
     const size_t rot_bytes = ROT ? 16 * D : 0;
-    size_t smem = 128 + 4 * D + rot_bytes + (size_t)NW * Gm::NST * 2 * Gm::REC;
-    const size_t merge = 128 + 4 * D + rot_bytes + (size_t)NW * part_floats(D) * 4;
+    size_t smem = 128 + 6 * D + rot_bytes + (size_t)NW * Gm::NST * 2 * Gm::REC;
+    const size_t merge = 128 + 6 * D + rot_bytes + (size_t)NW * part_floats(D) * 4;
     if (smem < merge) smem = merge;
     auto kern = draft_kivi_kernel<BITS, D, TQ, TR, ROT>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -370,11 +370,12 @@ __device__ void quantize_staged(const T *kx, const T *vx, uint8_t *work, uint8_t
         kst[ch] = zf;
         kst[D + ch] = rcp_scale(sf);
         kst[2 * D + ch] = sf;
+        // quad j, k-step ks: zero pair then scale pair for rr = 0, then rr = 1
         const int ks = ch >> 4, col = ch & 15;
-        const int j = (col & 7) >> 1, n = 2 * ks + (col >> 3);
-        const int off = Gm::KM + 16 * (4 * (n >> 2) + j) + 4 * (n & 3) + 2 * (ch & 1);
-        *reinterpret_cast<uint16_t *>(img + off) = sb;
-        *reinterpret_cast<uint16_t *>(img + off + 2 * D) = zb;
+        const int j = (col & 7) >> 1, rr = col >> 3;
+        const int off = Gm::KM + 16 * (4 * ks + j) + 8 * rr + 2 * (ch & 1);
+        *reinterpret_cast<uint16_t *>(img + off) = zb;
+        *reinterpret_cast<uint16_t *>(img + off + 4) = sb;
     } else {
         const int i = tid - D;
         const int t = i % G, gc = i / G;

@@ -257,12 +257,15 @@ long orc_kivi_quantize(const float *k, const float *v, int B, int H, int L, int 
  *       e = 3 + k2 / q, i = k2 % q, word = 4 i + mu, slot = e.
  *   bits = 4 (h = W/2): e = kappa / h, i = kappa % h, word = 2 i + mu/2,
  *       slot = e + 2 (mu%2).
- * Meta sections.  For lane quad j in [0,4) the library stores a sequence of
- * fp16 pairs; pair n of quad j sits at byte 16*(4*(n/4) + j) + 4*(n%4) of the
- * scale region, and the matching zero-point pair at the same offset + 2d.
- *   K meta: n = 2 ks + rr, pair = (s[c0], s[c0+1]), c0 = 16 ks + 2 j + 8 rr.
- *   V meta: n = (2 ks + rr)*(d/32) + gc, pair = (s[t0][gc], s[t0+1][gc]),
- *           t0 = 16 ks + 2 j + 8 rr.
+ * K meta section.  For lane quad j in [0,4) and k-step ks in [0,d/16) the
+ * 16 bytes at 16*(4 ks + j) hold, for rr = 0 then rr = 1, the fp16 zero-point
+ * pair (z[c0], z[c0+1]) followed by the scale pair (s[c0], s[c0+1]),
+ * c0 = 16 ks + 2 j + 8 rr (zero pair at +8 rr, scale pair at +8 rr + 4).
+ * V meta section.  For lane quad j the library stores a sequence of fp16
+ * pairs; pair n of quad j sits at byte 16*(4*(n/4) + j) + 4*(n%4) of the
+ * scale region, and the matching zero-point pair at the same offset + 2d:
+ *   n = (2 ks + rr)*(d/32) + gc, pair = (s[t0][gc], s[t0+1][gc]),
+ *   t0 = 16 ks + 2 j + 8 rr.
  * This reader implements the map directly from that statement; it shares
  * nothing with the GPU writer. */
 static void pair_pos(int bits, int d, int kappa, int mu, int *word, int *slot)
@@ -359,8 +362,8 @@ int orc_unpack_records(const uint8_t *rec, long n_rec, int bits, int d, int G,
             for (int ks = 0; ks < KS; ks++)
                 for (int rr = 0; rr < 2; rr++) {
                     int c0 = 16 * ks + 2 * j + 8 * rr;
-                    const uint8_t *sp = meta_pair(km, j, 2 * ks + rr);
-                    const uint8_t *zp = sp + 2 * d;
+                    const uint8_t *zp = km + 16 * (4 * ks + j) + 8 * rr;
+                    const uint8_t *sp = zp + 4;
                     kscale[g * d + c0] = rd_u16(sp);
                     kscale[g * d + c0 + 1] = rd_u16(sp + 2);
                     kzero[g * d + c0] = rd_u16(zp);
