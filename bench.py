@@ -70,9 +70,9 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("99eb3fc6059e49b37c09a309d3ad46c49093c9550d43b79d9efe180e1ce893ff",
+    "sha256": ("e44000c5a1e88ea70ac2f871177a31020c27a3bef5f6a96fb5f794e962315aca",
                "10b95006df417026b33954ac060b27c984605c2a56c9c3179717bb6732c17edb"),
-    "bytes": 411.009280e6 + 4.302336e6,
+    "bytes": 410.966016e6 + 4.440064e6,
     "algorithmic_bytes": 409731072,
 }
 
@@ -803,8 +803,10 @@ def run_model(args, dev, rank, world, barrier, pg):
     clocks.start()
     time.sleep(0.3)
     t0.record()
+    torch.cuda.nvtx.range_push("timed_rounds")
     for i in range(args.steps):
         run.round(log, base0 + i, evs[i])
+    torch.cuda.nvtx.range_pop()
     t1.record()
     barrier()
     clk = clocks.stop()
