@@ -932,6 +932,12 @@ def run_model(args, dev, rank, world, barrier, pg):
     del ref
     torch.cuda.empty_cache()
 
+    # cross-resource staggering of two request groups (half the batch each):
+    # one group's full-cache swap crosses the link while the other drafts and
+    # verifies; measured against the unstaggered rounds above
+    stag = None if args.no_stagger else run_staggered(args, dec, cfg, prompt, packed, dev, greedy, n_cmp,
+                                                      value / world)
+
     # the one-layer hot path at the configuration of the kernel workloads
     # (B16, 32k): draft attention (2-bit KIVI), verify attention (Dq 33) and
     # acceptance over [16, 33, 151936], timed inside a staggered round
@@ -955,6 +961,7 @@ def run_model(args, dev, rank, world, barrier, pg):
             "roofline_gemm": roof_gemm,
             "full_kv_baseline": base,
             "lossless_check": check,
+            "staggered": stag,
             "phases_ms": {"draft_32_steps": d_ms, "verify_forward": v_ms, "accept_commit_writeback": c_ms,
                           "swap_in": s_ms},
             "swap": {"bytes": run_bytes(cfg, max_len, packed),
@@ -975,6 +982,73 @@ def run_model(args, dev, rank, world, barrier, pg):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+def run_staggered(args, dec, cfg, prompt, packed, dev, greedy, n_cmp, unstaggered_tps, cycles: int = 8,
+                  warm: int = 3) -> dict:
+    """Two half-batch runners ping-ponging on the main stream (decode.StaggeredPair).
+    Returns tokens/s, ms per cycle, each swap's overlap with the other group's
+    drafting and verify (device events), and the lossless check of both groups
+    against the same greedy decoding."""
+    from lossless_draft_verify_gb300 import decode
+    half = M_B // 2
+    P = prompt.shape[1]
+    max_len = P + (warm + cycles + 1) * (M_HORIZON + 1) + 64
+    mk = lambda: decode.VeriCacheRunner(dec, half, max_len, M_HORIZON, bits=args.bits, residual=M_RESIDUAL,
+                                        host_cache=True, prefill_chunk=512, device=dev, pack_host=packed)
+    ra, rb = mk(), mk()
+    ra.prefill(prompt[:half].contiguous())
+    rb.prefill(prompt[half:].contiguous())
+    first = ra.x.cpu().tolist() + rb.x.cpu().tolist()
+    pair = decode.StaggeredPair(ra, rb)
+    la, lb = ra.new_log(warm + cycles), rb.new_log(warm + cycles)
+    for i in range(warm):
+        pair.cycle(la, lb, i)
+    torch.cuda.synchronize()
+    ra.capture_draft_graph()
+    rb.capture_draft_graph()
+    evs = [{k: decode.VeriCacheRunner.new_events() for k in ("A", "B", "A_swap", "B_swap")} for _ in range(cycles)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(cycles):
+        pair.cycle(la, lb, warm + i, evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    tokens = int((la.n_acc[warm:].long() + 1).sum() + (lb.n_acc[warm:].long() + 1).sum())
+
+    def inside(sw: dict, w0, w1) -> float:
+        """Part of the swap interval [swap0, swap1] within [w0, w1], over the swap."""
+        span = sw["swap0"].elapsed_time(sw["swap1"])
+        lo = max(0.0, sw["swap0"].elapsed_time(w0))
+        hi = min(span, sw["swap0"].elapsed_time(w1))
+        return max(0.0, hi - lo) / span if span > 0 else 0.0
+
+    ov = []
+    for i in range(cycles):
+        # A's swap of cycle i runs under B's turn of cycle i, B's under A's turn of cycle i + 1
+        ov.append(inside(evs[i]["A_swap"], evs[i]["B"]["d0"], evs[i]["B"]["c1"]))
+        if i + 1 < cycles:
+            ov.append(inside(evs[i]["B_swap"], evs[i + 1]["A"]["d0"], evs[i + 1]["A"]["c1"]))
+    swap_ms = statistics.mean(e[k]["swap0"].elapsed_time(e[k]["swap1"]) for e in evs for k in ("A_swap", "B_swap"))
+    turn_ms = statistics.mean(e[k]["d0"].elapsed_time(e[k]["c1"]) for e in evs for k in ("A", "B"))
+    draft_ms = statistics.mean(e[k]["d0"].elapsed_time(e[k]["d1"]) for e in evs for k in ("A", "B"))
+    emitted = [[first[b]] + t for b, t in enumerate(la.tokens() + lb.tokens())]
+    n = min(n_cmp, min(len(t) for t in emitted))
+    mism = sum(int(a != g) for b in range(M_B) for a, g in zip(emitted[b][:n], greedy[b][:n]))
+    tps = tokens / (ms / 1e3)
+    out = {"tokens_per_s": tps, "ms_per_cycle": ms / cycles, "groups": 2, "sequences_per_group": half,
+           "swap_ms_per_group": swap_ms, "group_turn_ms": turn_ms, "group_draft_ms": draft_ms,
+           "swap_hidden_under_other_group_frac": statistics.mean(ov),
+           "vs_unstaggered": tps / unstaggered_tps,
+           "lossless_check": {"tokens_compared": n * M_B, "mismatches": mism},
+           "what": "two groups of 4 sequences, each its own runner; a group's swap runs while the other group "
+                   "drafts and verifies (one link, one main stream); drafting streams the model's weights per "
+                   "group, so each group's 32 draft steps cost about what the whole batch's do"}
+    del pair, ra, rb
+    torch.cuda.empty_cache()
+    return out
 
 
 def model_writeback_bytes(cfg, n_acc, packed: bool) -> int:
@@ -1209,6 +1283,8 @@ def main():
                          "hot path at 32k (B16) with planted acceptance")
     ap.add_argument("--no-round-kernels", action="store_true",
                     help="--workload model: skip the one-layer B16 round that reports the kernel workloads")
+    ap.add_argument("--no-stagger", action="store_true",
+                    help="--workload model: skip the staggered two-group measurement")
     ap.add_argument("--prompt", type=int, default=32768, help="prompt tokens per sequence (--workload model)")
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")

@@ -153,7 +153,7 @@ struct KiviParams {
     unsigned int *counters;                            // [units], zero between calls
     void *out;
     int32_t *status;
-    int Hkv, Hq, grp, max_groups, res_cap, n_split_q, groups_per_split;
+    int Hkv, Hq, grp, max_groups, res_cap, n_split_q;
     int n_split_r, res_per_split;                      // ring splits and ring tokens per split
     float qscale;                                      // sm_scale * log2(e)
     float *raw;                                        // optional [units][raw_stride][4] log2-domain scores (H2O)
@@ -398,8 +398,11 @@ draft_kivi_kernel(KiviParams P)
     if (split < P.n_split_q) {
         // ---------------------------------------------- quantized groups --
         const int ng = min(P.n_groups[b], P.max_groups);
-        const int g_lo = split * P.groups_per_split;
-        const int g_hi = min(ng, g_lo + P.groups_per_split);
+        // the unit's filled groups (often fewer than the capacity the split
+        // count was planned for) are divided evenly over the splits, in pairs
+        const int npairs = (ng + 1) / 2;
+        const int g_lo = min(ng, 2 * (int)((long)npairs * split / P.n_split_q));
+        const int g_hi = min(ng, 2 * (int)((long)npairs * (split + 1) / P.n_split_q));
         const uint8_t *rec_base = P.records + (size_t)unit * P.max_groups * REC;
         uint64_t *mybar = bars + warp * NST;
         uint8_t *myring = ring + (size_t)warp * NST * STAGE;
@@ -1262,7 +1265,6 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     P.max_groups = c->max_groups;
     P.res_cap = c->res_cap;
     P.n_split_q = pl.n_split_q;
-    P.groups_per_split = pl.groups_per_split;
     P.n_split_r = pl.n_split_r;
     P.res_per_split = pl.res_per_split;
     P.qscale = scale * kLog2e;

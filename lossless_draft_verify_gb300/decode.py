@@ -159,6 +159,7 @@ class VeriCacheRunner:
             self.v_host.copy_(self.v_full)
         self.ctx.fill_(P)
         self.ctx_bound = P
+        self.round_len.copy_(self.qc[0].seq_len)
         return self.x
 
     def check_packed(self):
@@ -224,15 +225,17 @@ class VeriCacheRunner:
         top = torch.topk(logits.float(), 2, dim=-1).values
         return top[..., 0] - top[..., 1]
 
-    def _swap_in(self, main: torch.cuda.Stream, ev: dict | None = None):
+    def _swap_in(self, main: torch.cuda.Stream, ev: dict | None = None, wait_main: bool = True):
         """Copy the host copy of the full cache into the device cache on the
         side stream (packed rows are expanded layer by layer on a second
-        stream); self.ev_swap marks the end."""
-        self.side.wait_stream(main)
+        stream); self.ev_swap marks the end.  wait_main: the copy waits for
+        everything issued on `main` so far (else the caller has ordered it)."""
+        if wait_main:
+            self.side.wait_stream(main)
         if ev is not None:
             ev["swap0"].record(self.side)
         if self.pack_host:
-            self.unpack_stream.wait_stream(main)
+            self.unpack_stream.wait_stream(self.side)
             for l in range(len(self.qc)):
                 vc.vc_swap_in(self.k_pack[l], self.k_host[l], stream=self.side)
                 vc.vc_swap_in(self.v_pack[l], self.v_host[l], stream=self.side, done_event=self.ev_layer[l])
@@ -260,11 +263,24 @@ class VeriCacheRunner:
         """One draft-and-verify round (enqueued; no host synchronization).
         graph: a recording of the draft steps to replay instead of the
         runner's own (e.g. one captured with tracing on)."""
-        B, D = self.B, self.D
         main = torch.cuda.current_stream()
         self.round_len.copy_(self.qc[0].seq_len)
         if self.host_cache:
-            self._swap_in(main, ev)
+            self.side.wait_stream(main)
+            self.swap_phase(ev)
+        self.draft_phase(ev, graph)
+        self.verify_phase(log, r, ev)
+
+    def swap_phase(self, ev: dict | None = None, after: torch.cuda.Event | None = None):
+        """Copy the host copy of the full cache in on the side stream (after
+        `after` when given); self.ev_swap marks its end."""
+        if after is not None:
+            self.side.wait_event(after)
+        self._swap_in(torch.cuda.current_stream(), ev, wait_main=False)
+
+    def draft_phase(self, ev: dict | None = None, graph: torch.cuda.CUDAGraph | None = None):
+        """The round's D draft steps on the compressed caches (main stream)."""
+        main = torch.cuda.current_stream()
         if self.use_graph and self._graph is None and self._rounds >= 1:
             self.capture_draft_graph()
         if ev is not None:
@@ -277,6 +293,13 @@ class VeriCacheRunner:
             self._draft_steps()
         if ev is not None:
             ev["d1"].record(main)
+
+    def verify_phase(self, log: RoundLog | None = None, r: int = 0, ev: dict | None = None):
+        """Verify forward of [x, d1..dD] over the full cache (after the swap),
+        acceptance, commit to the compressed caches and write-back to the host
+        copy (main stream)."""
+        B, D = self.B, self.D
+        main = torch.cuda.current_stream()
         if self.host_cache:
             main.wait_event(self.ev_swap)
         if ev is not None:
@@ -306,6 +329,8 @@ class VeriCacheRunner:
             log.nxt[r].copy_(self.x)
         self.ctx_bound += D + 1
         self._rounds += 1
+        # the next round's lengths (a copy on the main stream, after the commit)
+        self.round_len.copy_(self.qc[0].seq_len)
 
     def _draft_steps(self):
         """The round's D greedy draft steps on the compressed caches."""
@@ -354,3 +379,42 @@ class VeriCacheRunner:
         used = RoundLog(log.drafts[:r], log.n_acc[:r], log.nxt[:r])
         toks = [[first[b]] + t for b, t in enumerate(used.tokens())]
         return [t[:n_new] for t in toks], used.accepted()
+
+
+class StaggeredPair:
+    """Cross-resource staggering of two request groups (paper page, "What the
+    paper found"): each group is a runner of half the batch with its own caches
+    and side streams, and the two ping-pong on the main stream, so that one
+    group's full-cache swap crosses the link while the other group drafts and
+    verifies.  A cycle: A drafts, A verifies (after its swap), A's next swap is
+    issued; then B drafts, B verifies (after its swap), B's next swap is issued.
+    Each group's tokens are those of its own runner (greedy decoding of its
+    sequences)."""
+
+    def __init__(self, a: VeriCacheRunner, b: VeriCacheRunner):
+        self.a, self.b = a, b
+        self.started = False
+
+    def _start(self):
+        main = torch.cuda.current_stream()
+        for g in (self.a, self.b):
+            g.side.wait_stream(main)
+            g.swap_phase()
+        self.started = True
+
+    def cycle(self, log_a: RoundLog | None = None, log_b: RoundLog | None = None, r: int = 0,
+              evs: dict | None = None):
+        """One cycle (enqueued).  evs: optional {"A", "B", "A_swap", "B_swap"}
+        event dicts (new_events()): each group's phases in this cycle, and the
+        swap each group issues at the end of its turn."""
+        if not self.started:
+            self._start()
+        main = torch.cuda.current_stream()
+        for name, g, log in (("A", self.a, log_a), ("B", self.b, log_b)):
+            ev = evs[name] if evs else None
+            g.draft_phase(ev)
+            g.verify_phase(log, r, ev)
+            done = torch.cuda.Event()
+            done.record(main)
+            g.swap_phase(evs[name + "_swap"] if evs else None, after=done)
+

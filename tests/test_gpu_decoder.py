@@ -160,6 +160,44 @@ def test_bf16_draft_and_verify_equals_greedy(host_cache, fused_head, rotate, gra
     assert all(0 <= a <= D for seq in acc for a in seq)
 
 
+@pytest.mark.parametrize("pack,graph", [(True, True), (False, False)])
+def test_staggered_groups_equal_greedy(pack, graph):
+    """Two request groups ping-ponging (decode.StaggeredPair: one group's swap
+    runs while the other drafts and verifies) emit exactly the greedy tokens of
+    their own sequences, and a host copy that the swaps read stays consistent
+    across the interleaving."""
+    vc = lib()
+    from lossless_draft_verify_gb300 import decode
+    cfg, dec = _small_decoder(vc, seed=1)
+    B, P, n_new, D = 4, 700, 40, 8
+    g = torch.Generator().manual_seed(5)
+    prompt = torch.randint(0, cfg.vocab, (B, P), generator=g, dtype=torch.int32).cuda()
+    ref_run = decode.VeriCacheRunner(dec, B, P + n_new + 2 * D, D, bits=2, residual=128, prefill_chunk=256)
+    ref_run.prefill(prompt)
+    ref = ref_run.greedy(n_new)
+    runs = [decode.VeriCacheRunner(dec, 2, P + n_new * (D + 1) + 2 * D, D, bits=2, residual=128, host_cache=True,
+                                   prefill_chunk=256, pack_host=pack) for _ in range(2)]
+    runs[0].prefill(prompt[:2].contiguous())
+    runs[1].prefill(prompt[2:].contiguous())
+    first = runs[0].x.cpu().tolist() + runs[1].x.cpu().tolist()
+    pair = decode.StaggeredPair(*runs)
+    cycles = n_new
+    logs = [r.new_log(cycles) for r in runs]
+    for i in range(cycles):
+        if graph and i == 2:
+            torch.cuda.synchronize()
+            for r in runs:
+                r.capture_draft_graph()
+        pair.cycle(logs[0], logs[1], i)
+    torch.cuda.synchronize()
+    toks = [[first[b]] + t for b, t in enumerate(logs[0].tokens() + logs[1].tokens())]
+    for b in range(B):
+        assert toks[b][:n_new] == ref[b], b
+    for r in runs:
+        r.check_packed()
+        assert _status_ok(vc, r.ws)
+
+
 def test_bf16_fused_verify_equals_logits_and_scan():
     """vc_decoder_verify (LM head with the argmax epilogue, acceptance over the
     tile maxima) gives the n_acc / next that the oracle's acceptance finds on
