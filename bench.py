@@ -70,9 +70,9 @@ def dist_env():
 # captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("e44000c5a1e88ea70ac2f871177a31020c27a3bef5f6a96fb5f794e962315aca",
-               "10b95006df417026b33954ac060b27c984605c2a56c9c3179717bb6732c17edb"),
-    "bytes": 410.966016e6 + 4.440064e6,
+    "sha256": ("e673bffc0e74b782ea09ef60de89e932136f4ebb217a53156555d484c307b50a",
+               "7f0d10f52269831e89674cc5efb2a594696ee3ebaae36acf379853a23e3f594a"),
+    "bytes": 411.130624e6 + 4.275968e6,
     "algorithmic_bytes": 409731072,
 }
 

@@ -29,6 +29,7 @@
 // stage is released.  The kernels wait on griddepcontrol.wait before their
 // first global access (programmatic dependent launch).
 #include <algorithm>
+#include <type_traits>
 
 #include "vc_common.cuh"
 #include "vc_internal.h"
@@ -56,6 +57,33 @@ __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma16816_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
 }
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
@@ -282,15 +310,18 @@ __device__ __forceinline__ void group_scores(const uint8_t *rec, const uint8_t *
         }
     }
     // rows 0..3 of the bias tile, columns 4..7 = sum of z * q for heads 0..3
+    // (columns 2 tig + {0, 1} of a lane are one register pair: packed FMAs)
     const int t1 = tig & 1;
+    const float2 bias = make_float2(__shfl_sync(0xffffffffu, cb[0], 6 + t1), __shfl_sync(0xffffffffu, cb[1], 6 + t1));
+    const float2 k24 = make_float2(kTwo24, kTwo24);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const float bias = __shfl_sync(0xffffffffu, cb[e], 6 + t1);
-        sc[0][e] = fmaf(sc[0][e], kTwo24, bias);
-        sc[0][e + 2] = fmaf(sc[0][e + 2], kTwo24, bias);
-        sc[1][e] = fmaf(sc[1][e], kTwo24, bias);
-        sc[1][e + 2] = fmaf(sc[1][e + 2], kTwo24, bias);
-    }
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; r += 2) {
+            const float2 v = fma2(make_float2(sc[mt][r], sc[mt][r + 1]), k24, bias);
+            sc[mt][r] = v.x;
+            sc[mt][r + 1] = v.y;
+        }
 }
 
 // O += V^T p' for one group, plus the zero-point accumulator.
@@ -317,14 +348,16 @@ __device__ __forceinline__ void group_values(const uint8_t *rec, const uint8_t *
         const uint4 u = *reinterpret_cast<const uint4 *>(vmeta + 16 * (4 * c + tig));
         sv[4 * c] = u.x; sv[4 * c + 1] = u.y; sv[4 * c + 2] = u.z; sv[4 * c + 3] = u.w;
     }
-    // zero-point rows gc = lane/4 (< NG): pairs n = (2 ks + rr) * NG + gc
+    // zero-point rows gc = lane/4 (< NG): pairs n = (2 ks + rr) * NG + gc;
+    // rows gid + 8 are ones, so accumulator rows 8..15 sum the probabilities
+    // (the softmax denominator, over the fp16 p the MMAs multiply)
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         const int gid = lane >> 2;
         const int n0 = (2 * ks) * NG + (gid & (NG - 1)), n1 = (2 * ks + 1) * NG + (gid & (NG - 1));
         const uint32_t z0 = *reinterpret_cast<const uint32_t *>(zvsrc + 16 * (4 * (n0 >> 2) + tig) + 4 * (n0 & 3));
         const uint32_t z1 = *reinterpret_cast<const uint32_t *>(zvsrc + 16 * (4 * (n1 >> 2) + tig) + 4 * (n1 & 3));
-        const uint32_t az[4] = {z0, 0u, z1, 0u};
+        const uint32_t az[4] = {z0, kOnes, z1, kOnes};
         mma16816(vb_acc, az, pb[ks][0], pb[ks][1]);
 #pragma unroll
         for (int gc = 0; gc < NG; ++gc) {
@@ -364,6 +397,128 @@ __device__ void rotate_queries(const TQ *qg, int grp, float *rq)
     constexpr float kScale = 0.125f;     // 2^-floor(log2(D)/2) for D = 128 and D = 64
     for (int i = threadIdx.x; i < 4 * D; i += kThreads) rq[i] *= kScale;
     __syncthreads();
+}
+
+// Full-precision window tokens of a bf16 ring with bf16 tensor-core MMAs,
+// continuing a warp's online-softmax state (m, per-lane partial l, o in plain
+// units; rows = channels 16 mt + gid (+8), columns = heads 2 tig + {0,1}).
+// The window's positions [ng G, len) are cut into 16-token tiles; tile j goes
+// to split j % n_split and, within it, to warp NW - 1 - (j / n_split) % NW
+// (the last warps hold the fewest group pairs of a split).  A tile's
+// rows are bulk-copied from their ring slots (pos % res_cap) into the warp's
+// idle stream stage with a padded pitch (conflict-free ldmatrix); rows past the
+// window's end are zeroed (their p is 0 and their V must be finite).
+// S = K q (A = K rows, B = q in bf16), O^T += V^T P (A = V^T via
+// ldmatrix.trans).  Returns false when a bounded wait gave up.
+template <int D, typename TQ, bool ROT>
+__device__ bool ring_tiles_mma(const KiviParams &P, int unit, int b, int split, int warp, int lane, const TQ *qg,
+                               const float *rq, uint8_t *stage, uint64_t *bar, uint32_t phase, float (&m_run)[2],
+                               float (&l_run)[2], float (&o)[D / 16][4])
+{
+    constexpr int KS = D / 16, PITCH = 2 * D + 16, TILE = 16 * PITCH, ROW = 2 * D;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int len = P.seq_len[b];
+    const int r0 = min(P.n_groups[b], P.max_groups) * G;
+    const int r1 = min(len, r0 + P.res_cap);             // the window holds at most res_cap tokens
+    const int ntile = r1 > r0 ? (r1 - r0 + 15) / 16 : 0;
+    const int step = P.n_split_q * NW;
+    int j = split + P.n_split_q * (NW - 1 - warp);
+    if (j >= ntile) return true;
+    uint32_t qb[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int c = 16 * ks + 2 * tig + 8 * rr;
+            float a = 0.f, bb = 0.f;
+            if (gid < P.grp) {
+                a = ROT ? rq[gid * D + c] : load_q<TQ, D>(qg, gid * D + c);
+                bb = ROT ? rq[gid * D + c + 1] : load_q<TQ, D>(qg, gid * D + c + 1);
+            }
+            qb[ks][rr] = pack_bf162(a, bb);
+        }
+    const uint8_t *kr = reinterpret_cast<const uint8_t *>(P.kres) + (size_t)unit * P.res_cap * ROW;
+    const uint8_t *vr = reinterpret_cast<const uint8_t *>(P.vres) + (size_t)unit * P.res_cap * ROW;
+    const int a_row = lane & 15, a_col = (lane >> 4) * 8;
+    const int v_tok = (lane & 7) + ((lane >> 4) << 3), v_col = ((lane >> 3) & 1) * 8;
+    for (; j < ntile; j += step) {
+        const int t0 = r0 + 16 * j;
+        const int rows = min(16, r1 - t0);
+        if (lane >= rows && lane < 16) {
+            uint4 *zk = reinterpret_cast<uint4 *>(stage + lane * PITCH);
+            uint4 *zv = reinterpret_cast<uint4 *>(stage + TILE + lane * PITCH);
+#pragma unroll
+            for (int i = 0; i < ROW / 16; ++i) zk[i] = zv[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar, 2u * rows * ROW);
+        __syncwarp();
+        if (lane < rows) {
+            const int slot = (t0 + lane) % P.res_cap;
+            bulk_g2s(stage + lane * PITCH, kr + (size_t)slot * ROW, ROW, bar);
+            bulk_g2s(stage + TILE + lane * PITCH, vr + (size_t)slot * ROW, ROW, bar);
+        }
+        if (!mbar_wait(bar, phase)) return false;
+        phase ^= 1;
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, stage + a_row * PITCH + (16 * ks + a_col) * 2);
+            mma16816_bf16(sc, a, qb[ks][0], qb[ks][1]);
+        }
+        float gmax[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool col_ok = 2 * tig + e < P.grp;
+            sc[e] = (col_ok && gid < rows) ? sc[e] * P.qscale : kNegBig;
+            sc[e + 2] = (col_ok && gid + 8 < rows) ? sc[e + 2] * P.qscale : kNegBig;
+            if (P.raw && col_ok) {
+                float *rw = P.raw + ((size_t)unit * P.raw_stride + t0 + gid) * 4 + 2 * tig + e;
+                if (gid < rows) rw[0] = sc[e];
+                if (gid + 8 < rows) rw[8 * 4] = sc[e + 2];
+            }
+            float mx = fmaxf(sc[e], sc[e + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            gmax[e] = mx;
+        }
+        float alpha[2] = {1.f, 1.f};
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            if (gmax[e] > m_run[e] + kLazy) {
+                alpha[e] = ex2(m_run[e] - gmax[e]);
+                m_run[e] = gmax[e];
+            }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][0] *= alpha[0];
+                o[mt][1] *= alpha[1];
+                o[mt][2] *= alpha[0];
+                o[mt][3] *= alpha[1];
+            }
+            l_run[0] *= alpha[0];
+            l_run[1] *= alpha[1];
+        }
+        float p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = ex2(sc[i] - m_run[i & 1]);
+        const uint32_t b0 = movmatrix_trans(pack_bf162(p[0], p[1]));
+        const uint32_t b1 = movmatrix_trans(pack_bf162(p[2], p[3]));
+        // the sum uses the bf16-rounded probabilities the MMA multiplies
+        l_run[0] += __bfloat162float(__float2bfloat16_rn(p[0])) + __bfloat162float(__float2bfloat16_rn(p[2]));
+        l_run[1] += __bfloat162float(__float2bfloat16_rn(p[1])) + __bfloat162float(__float2bfloat16_rn(p[3]));
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(a, stage + TILE + v_tok * PITCH + (16 * mt + v_col) * 2);
+            mma16816_bf16(o[mt], a, b0, b1);
+        }
+        fence_async_smem();                      // this tile's reads before the next tile's bulk copies
+        __syncwarp();
+    }
+    return true;
 }
 
 template <int BITS, int D, typename TQ, typename TR, bool ROT>
@@ -528,8 +683,6 @@ draft_kivi_kernel(KiviParams P)
                     o_acc[mt][2] *= alpha[0];
                     o_acc[mt][3] *= alpha[1];
                 }
-                l_run[0] *= alpha[0];
-                l_run[1] *= alpha[1];
                 vb_acc[0] *= alpha[0];
                 vb_acc[1] *= alpha[1];
                 vb_acc[2] *= alpha[0];
@@ -540,13 +693,11 @@ draft_kivi_kernel(KiviParams P)
             for (int G2 = 0; G2 < 2; ++G2)
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
-                    float p[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) p[i] = ex2(sc[G2][mt][i] - m_run[i & 1]);
-                    l_run[0] += p[0] + p[2];
-                    l_run[1] += p[1] + p[3];
-                    pb[G2][mt][0] = movmatrix_trans(pack_half2(p[0], p[1]));
-                    pb[G2][mt][1] = movmatrix_trans(pack_half2(p[2], p[3]));
+                    const float2 m2 = make_float2(m_run[0], m_run[1]);
+                    const float2 d01 = sub2(make_float2(sc[G2][mt][0], sc[G2][mt][1]), m2);
+                    const float2 d23 = sub2(make_float2(sc[G2][mt][2], sc[G2][mt][3]), m2);
+                    pb[G2][mt][0] = movmatrix_trans(pack_half2(ex2(d01.x), ex2(d01.y)));
+                    pb[G2][mt][1] = movmatrix_trans(pack_half2(ex2(d23.x), ex2(d23.y)));
                 }
             // ---- values of both groups (a masked copy has p = 0)
             {
@@ -569,13 +720,11 @@ draft_kivi_kernel(KiviParams P)
             for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
             vb_acc[0] = vb_acc[1] = vb_acc[2] = vb_acc[3] = 0.f;
         }
-        // lanes sharing a column hold partial row sums: reduce
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 4);
-            l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 8);
-            l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 16);
-        }
+        // the probability sums are rows 8..15 of the zero-point accumulator,
+        // equal on every lane of a column: one lane per column keeps them, so
+        // the lane reduction below counts them once
+        l_run[0] = gid == 0 ? vb_acc[2] : 0.f;
+        l_run[1] = gid == 0 ? vb_acc[3] : 0.f;
         // zero-point contribution of channel group gc for heads 2 tig + e
         // (row gc of the zero-point accumulator lives on lanes 4 gc + tig)
         float vbias[NG][2];
@@ -583,6 +732,36 @@ draft_kivi_kernel(KiviParams P)
         for (int gc = 0; gc < NG; ++gc)
 #pragma unroll
             for (int e = 0; e < 2; ++e) vbias[gc][e] = __shfl_sync(0xffffffffu, vb_acc[e], gc * 4 + tig);
+        // o in plain units: rows 16 mt + gid (+8) lose 2^-24 and the code
+        // factor 2^(b e) of their class and gain the zero-point sums
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const float f0 = kTwo24 * exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt)));
+            const float f1 = kTwo24 * exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt + 1)));
+            o_acc[mt][0] = fmaf(o_acc[mt][0], f0, vbias[mt / 2][0]);
+            o_acc[mt][1] = fmaf(o_acc[mt][1], f0, vbias[mt / 2][1]);
+            o_acc[mt][2] = fmaf(o_acc[mt][2], f1, vbias[mt / 2][0]);
+            o_acc[mt][3] = fmaf(o_acc[mt][3], f1, vbias[mt / 2][1]);
+        }
+        if constexpr (std::is_same<TR, __nv_bfloat16>::value) {
+            // the bf16 window's tiles of this split continue the same state
+            // (stage 0 of the warp's stream ring has had (n_mine + 1) / 2 phases)
+            if (ok && !ring_tiles_mma<D, TQ, ROT>(P, unit, b, split, warp, lane, qg, rq, myring, &mybar[0],
+                                                  (uint32_t)((n_mine + 1) / 2) & 1u, m_run, l_run, o_acc)) {
+                if (lane == 0) report_timeout(P.status, 2);
+                m_run[0] = m_run[1] = kNegBig;
+                l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+                for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+            }
+        }
+        // lanes sharing a column hold partial row sums: reduce
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 4);
+            l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 8);
+            l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 16);
+        }
         __syncthreads();   // every warp done with its ring before wbuf reuse
         float *wm = wbuf, *wl = wbuf + NW * 4, *wo = wbuf + NW * 8;
         if (tig < 2) {
@@ -595,12 +774,8 @@ draft_kivi_kernel(KiviParams P)
                 }
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
-                    // rows 16 mt + gid (+8): undo 2^-24 and the code factor 2^(b e) of their class
-                    const float f0 = kTwo24 * exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt)));
-                    const float f1 = kTwo24 * exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * mt + 1)));
-                    const int c0 = 16 * mt + gid;
-                    wo[(warp * 4 + h) * D + c0] = o_acc[mt][e] * f0 + vbias[mt / 2][e];
-                    wo[(warp * 4 + h) * D + c0 + 8] = o_acc[mt][e + 2] * f1 + vbias[mt / 2][e];
+                    wo[(warp * 4 + h) * D + 16 * mt + gid] = o_acc[mt][e];
+                    wo[(warp * 4 + h) * D + 16 * mt + gid + 8] = o_acc[mt][e + 2];
                 }
             }
         }
@@ -909,33 +1084,6 @@ struct DmGeom {
     static constexpr int SMEM = 128 + RING;                  // barriers + rings (merge buffer reuses the rings)
 };
 
-__device__ __forceinline__ void mma16816_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void *p)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
-}
-
-__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi)
-{
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads)
 draft_dense_mma_kernel(DenseParams P)
@@ -1166,9 +1314,42 @@ KiviPlan kivi_plan(const vc_qcache *c)
 {
     const int units = c->B * c->Hkv;
     const int ng = c->max_groups;
-    const int slots = num_sms() * 4;                   // 4 resident CTAs per SM
+    const int sms = num_sms();
     KiviPlan p;
-    // the ring: one split per 256 of its capacity's tokens
+    if (c->res_dtype == VC_BF16) {
+        // The bf16 window is handled inside the quantized splits (tensor-core
+        // tiles), so every CTA is a quantized split.  Split count minimising
+        // waves x (group pairs per warp + ~3 pairs of fixed cost per CTA) /
+        // the last wave's fill: full waves of equal CTAs keep every SM busy
+        // to the end (measured at 32k: 9 splits for 64 kv units, 576 CTAs in
+        // one wave of 608 slots; 9 for 128 units).
+        p.n_split_r = 0;
+        p.res_per_split = 0;
+        const int slots = sms * 4;                     // 4 resident CTAs per SM
+        int best = 1;
+        double best_t = -1.0;
+        const int max_s = ng > 0 ? std::min(kMaxSplit, (ng + 3) / 4) : 1;   // at least two group pairs per split
+        for (int s = 1; s <= max_s; ++s) {
+            int gps = (ng + s - 1) / s;
+            gps += gps & 1;
+            const int se = ng > 0 ? (ng + gps - 1) / gps : 1;
+            const int pairs_per_warp = (gps / 2 + NW - 1) / NW;
+            const long n_cta = (long)units * se;
+            const long waves = (n_cta + slots - 1) / slots;
+            const double fill = (double)n_cta / ((double)waves * slots);
+            const double t = (double)waves * (pairs_per_warp + 3) / fill;
+            if (best_t < 0.0 || t < best_t) {
+                best_t = t;
+                best = s;
+            }
+        }
+        p.groups_per_split = ng > 0 ? (ng + best - 1) / best : 2;
+        p.groups_per_split += p.groups_per_split & 1;
+        p.n_split_q = ng > 0 ? (ng + p.groups_per_split - 1) / p.groups_per_split : 1;
+        return p;
+    }
+    const int slots = sms * 4;                         // 4 resident CTAs per SM
+    // the fp32 ring: one split per 256 of its capacity's tokens
     p.n_split_r = std::max(1, std::min(kMaxSplit / 2, (c->res_cap + kResTokensPerSplit - 1) / kResTokensPerSplit));
     p.res_per_split = (c->res_cap + p.n_split_r - 1) / p.n_split_r;
     // Split count minimising waves x (group pairs per warp + ~3 pairs of

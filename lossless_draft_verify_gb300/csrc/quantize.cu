@@ -72,32 +72,6 @@ __device__ __forceinline__ float rcp_scale(float s)
     return s != 0.0f ? r : 0.0f;
 }
 
-// Two-lane fp32 arithmetic (add/mul.rn.f32x2): both lanes round exactly as the
-// scalar instructions do.
-__device__ __forceinline__ float2 add2(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "add.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
-        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "sub.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
-        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "mul.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
-        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
 // all ones when |e| lies above the near-half threshold, else zero
 __device__ __forceinline__ uint32_t near_mask(float e, float thr)
 {
