@@ -17,10 +17,11 @@
 //               P written to shared memory as bf16 in the canonical K-major
 //               layout for the next MMA.
 // Tail mode (a second tile of at most 8 rows, e.g. Dq = 33 with 4 heads per
-// kv head): warp 0 lane 1 issues the MMAs and warp 1 computes the tail rows
-// with mma.sync on the same K/V stages, read by ldmatrix; it fences those
-// generic-proxy reads (fence.proxy.async) before releasing a stage to the
-// TMA refill.
+// kv head): kTailWarps further warps compute the tail rows with mma.sync on
+// the same K/V stages, read by ldmatrix, each over its own share of every
+// tile's keys (its own online-softmax state; the combine merges the shares);
+// each fences those generic-proxy reads (fence.proxy.async) before releasing
+// a stage to the TMA refill.
 // Every mbarrier wait is bounded; a timeout is recorded in the workspace
 // status block and the CTA drains out.  Kernels wait on griddepcontrol.wait
 // before their first global access (programmatic dependent launch).  Split partials (m, l, o) go to the
@@ -54,10 +55,13 @@ constexpr float TC_LAZY = 8.0f;
 // Geometry of a CTA holding MT row tiles of 128 (query, head) rows that share
 // every K/V tile.  MT = 1: 2 CTAs per SM; MT = 2: one CTA per SM, the whole
 // TMEM (per tile: S double buffer 2 x 64 columns + O 128 columns).
+constexpr int kTailMaxRows = 8;
+constexpr int kTailWarps = 2;            // tail warps; each takes TC_N / kTailWarps keys of a tile
+
 template <int MT, bool TAIL = false>
 struct TcGeom {
     static constexpr int STAGES = MT == 1 ? 2 : 3;
-    static constexpr int THREADS = 64 + 128 * MT;
+    static constexpr int THREADS = 64 + 128 * MT + (TAIL ? 32 * kTailWarps : 0);
     static constexpr int SM_Q = 0;                                    // MT x 2 x (128 x 128 B)
     static constexpr int SM_K = SM_Q + MT * TC_M * TC_D * 2;          // stages x (64 x 256 B)
     static constexpr int SM_V = SM_K + STAGES * TC_N * TC_D * 2;
@@ -76,8 +80,6 @@ struct TcParams {
     int tail_rows;               // rows of the second row tile done by the tail warp (0: none)
     float scale_log2;
 };
-
-constexpr int kTailMaxRows = 8;
 
 __device__ __forceinline__ void mma_bf16_16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1)
@@ -182,16 +184,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int mt = mtc * MT + t;
         return P.part + (((size_t)unit * P.n_mtiles + mt) * P.n_split + split) * TC_M * TC_PART;
     };
-    // tail mode: the rows of the second tile, all in the first kTailMaxRows, by warp 1
+    // tail mode: the rows of the second tile, all in the first kTailMaxRows;
+    // tail warp w keeps its share of the keys in partial rows w * kTailMaxRows + r
     float *part_tail = P.part + (((size_t)unit * P.n_mtiles + 1) * P.n_split + split) * TC_M * TC_PART;
 
     if (threadIdx.x == 0) {
         mbar_init(&B->q_full, 1);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&B->k_full[s], 1);
-            mbar_init(&B->k_empty[s], TAIL ? 2 : 1);      // the MMAs' commit (+ the tail warp)
+            mbar_init(&B->k_empty[s], TAIL ? 1 + kTailWarps : 1);      // the MMAs' commit (+ the tail warps)
             mbar_init(&B->v_full[s], 1);
-            mbar_init(&B->v_empty[s], TAIL ? 2 : 1);
+            mbar_init(&B->v_empty[s], TAIL ? 1 + kTailWarps : 1);
         }
         for (int t = 0; t < MT; ++t) {
             for (int s = 0; s < 2; ++s) {
@@ -220,19 +223,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             for (int i = threadIdx.x; i < TC_M * TC_PART; i += Gm::THREADS) part[i] = (i % TC_PART) == 0 ? kNegBig : 0.f;
         }
         if (TAIL)
-            for (int i = threadIdx.x; i < P.tail_rows * TC_PART; i += Gm::THREADS)
-                part_tail[i] = (i % TC_PART) == 0 ? kNegBig : 0.f;
+            for (int w = 0; w < kTailWarps; ++w)
+                for (int i = threadIdx.x; i < P.tail_rows * TC_PART; i += Gm::THREADS)
+                    part_tail[w * kTailMaxRows * TC_PART + i] = (i % TC_PART) == 0 ? kNegBig : 0.f;
         return;
     }
     const uint32_t tmem = B->tmem_base;
 
-    // Roles.  Warp 0 lane 0: TMA producer.  tcgen05 issuer: warp 1 lane 0, or
-    // in tail mode warp 0 lane 1 (a second, independent single-thread loop in
-    // the same warp) so that warp 1 is free for the tail rows.  Warps 2..5
-    // (and 6..9 for a second tile): softmax.
+    // Roles.  Warp 0 lane 0: TMA producer.  Warp 1 lane 0: tcgen05 issuer.
+    // Warps 2..5 (and 6..9 for a second tile): softmax.  Tail mode: warps
+    // 6 .. 5 + kTailWarps take the tail rows.
     const bool producer = warp == 0 && lane == 0;
-    const bool issuer = TAIL ? (warp == 0 && lane == 1) : (warp == 1 && lane == 0);
-    if (warp == 0 || (!TAIL && warp == 1)) {
+    const bool issuer = warp == 1 && lane == 0;
+    constexpr int kFirstTailWarp = 2 + 4 * MT;
+    if (warp <= 1) {
         if (producer) {
             // -------------------------------------------------- TMA producer --
             tc::prefetch_tmap(&tmQ);
@@ -315,7 +319,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 tc::commit(&B->v_empty[s]);
             }
         }
-    } else if (TAIL && warp == 1) {
+    } else if (TAIL && warp >= kFirstTailWarp) {
         // ------------------------------------------------ tail rows (mma.sync) --
         // Row r < tail_rows of the second tile (position rows_q + r / grp,
         // head r % grp) against the same K/V tiles.  Transposed products keep
@@ -323,7 +327,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         // (keys x rows) and O^T += V^T P^T (channels x rows), the K and V
         // operands read from the swizzled tiles by ldmatrix, P^T formed from
         // the S^T fragments by movmatrix.  Lane (gid, tig) holds tail rows
-        // 2 tig + e (e = 0, 1).
+        // 2 tig + e (e = 0, 1).  Tail warp wt takes the 16-key chunks
+        // wt * MTS .. wt * MTS + MTS - 1 of every tile.
+        constexpr int MTS = TC_N / 16 / kTailWarps;
+        const int wt = warp - kFirstTailWarp;
+        float *part_w = part_tail + (size_t)wt * kTailMaxRows * TC_PART;
         const int gid = lane >> 2, tig = lane & 3;
         // Q^T fragments (column n = gid: tail row gid)
         uint32_t qb[TC_D / 16][2];
@@ -358,19 +366,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 break;
             }
             const uint32_t sK = smem_u32(sm + Gm::SM_K + s * TC_N * TC_D * 2);
-            float sc[TC_N / 16][4];     // S^T: keys 16 mt + gid (+8) x rows 2 tig + e
+            float sc[MTS][4];           // S^T: keys 16 (wt MTS + i) + gid (+8) x rows 2 tig + e
 #pragma unroll
-            for (int i = 0; i < TC_N / 16; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+            for (int i = 0; i < MTS; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < TC_D / 16; ++ks)
 #pragma unroll
-                for (int mt = 0; mt < TC_N / 16; ++mt) {
+                for (int i = 0; i < MTS; ++i) {
                     // A = K rows: matrices (keys 16 mt + 8 (mi & 1) .., channel chunk 2 ks + (mi >> 1))
+                    const int mt = wt * MTS + i;
                     const int mi = lane >> 3;
                     const int key = 16 * mt + 8 * (mi & 1) + (lane & 7);
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(swz_chunk(sK, key, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-                    mma_bf16_16816(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    mma_bf16_16816(sc[i], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                 }
             // the stage is refilled by TMA (async proxy) once released: order
             // this warp's generic-proxy reads of it before that
@@ -381,14 +390,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const int key0 = (t_lo + j) * TC_N;
             float mx[2] = {kNegBig, kNegBig};
 #pragma unroll
-            for (int mt = 0; mt < TC_N / 16; ++mt)
+            for (int mi2 = 0; mi2 < MTS; ++mi2)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int e = i & 1;
-                    const int key = key0 + 16 * mt + gid + 8 * (i >> 1);
+                    const int key = key0 + 16 * (wt * MTS + mi2) + gid + 8 * (i >> 1);
                     const bool vis = rv[e] && key <= kmax[e];
-                    sc[mt][i] = vis ? sc[mt][i] * P.scale_log2 : -INFINITY;
-                    mx[e] = fmaxf(mx[e], sc[mt][i]);
+                    sc[mi2][i] = vis ? sc[mi2][i] * P.scale_log2 : -INFINITY;
+                    mx[e] = fmaxf(mx[e], sc[mi2][i]);
                 }
             float alpha[2] = {1.f, 1.f};
 #pragma unroll
@@ -414,9 +423,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
             // P^T B fragments: keys 16 kk + 2 tig (+8) of row gid, by transposing
             // the S^T fragment pairs
-            uint32_t pb[TC_N / 16][2];
+            uint32_t pb[MTS][2];
 #pragma unroll
-            for (int mt = 0; mt < TC_N / 16; ++mt) {
+            for (int mt = 0; mt < MTS; ++mt) {
                 __nv_bfloat162 lo = __floats2bfloat162_rn(ex2(sc[mt][0] - m[0]), ex2(sc[mt][1] - m[1]));
                 __nv_bfloat162 hi = __floats2bfloat162_rn(ex2(sc[mt][2] - m[0]), ex2(sc[mt][3] - m[1]));
                 const float2 fl = __bfloat1622float2(lo), fh = __bfloat1622float2(hi);
@@ -431,16 +440,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
             const uint32_t sV = smem_u32(sm + Gm::SM_V + s * TC_N * TC_D * 2);
 #pragma unroll
-            for (int kk = 0; kk < TC_N / 16; ++kk)
+            for (int k2 = 0; k2 < MTS; ++k2)
 #pragma unroll
                 for (int mt = 0; mt < TC_D / 16; ++mt) {
                     // A = V^T: matrices (channels 16 mt + 8 (mi & 1), keys 16 kk + 8 (mi >> 1)),
                     // from key rows, transposed
+                    const int kk = wt * MTS + k2;
                     const int mi = lane >> 3;
                     const int key = 16 * kk + 8 * (mi >> 1) + (lane & 7);
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(swz_chunk(sV, key, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-                    mma_bf16_16816(o[mt], a0, a1, a2, a3, pb[kk][0], pb[kk][1]);
+                    mma_bf16_16816(o[mt], a0, a1, a2, a3, pb[k2][0], pb[k2][1]);
                 }
             fence_async_smem();
             __syncwarp();
@@ -455,7 +465,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             if (!rv[e]) continue;
-            float *pr = part_tail + (size_t)(2 * tig + e) * TC_PART;
+            float *pr = part_w + (size_t)(2 * tig + e) * TC_PART;
             if (gid == 0) {
                 pr[0] = ok ? m[e] : kNegBig;
                 pr[1] = ok ? l[e] : 0.f;
@@ -600,9 +610,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 }
 
 // Merge the key splits of the tensor-core kernel.  One thread per (row, 4 channels).
+// In tail mode (tail_sub > 1) the last row tile's rows r come in tail_sub
+// shares of the keys, at partial rows w * kTailMaxRows + r, merged as splits.
 template <typename T>
 __global__ void verify_tc_combine(const float *__restrict__ part, int n_split, int n_mtiles, int Hkv,
-                                  int Hq, int Dq, int grp, T *__restrict__ out, float2 *__restrict__ ml)
+                                  int Hq, int Dq, int grp, int tail_sub, T *__restrict__ out,
+                                  float2 *__restrict__ ml)
 {
     pdl_wait();
     pdl_trigger();
@@ -615,19 +628,23 @@ __global__ void verify_tc_combine(const float *__restrict__ part, int n_split, i
     if (qi >= Dq) return;
     const float *pp = part + (size_t)item * n_split * TC_M * TC_PART + (size_t)r * TC_PART;
     const size_t sstride = (size_t)TC_M * TC_PART;
+    const int n_sub = mt == n_mtiles - 1 ? tail_sub : 1;
+    const size_t wstride = (size_t)kTailMaxRows * TC_PART;
     float M = kNegBig;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, pp[s * sstride]);
+    for (int s = 0; s < n_split; ++s)
+        for (int w = 0; w < n_sub; ++w) M = fmaxf(M, pp[s * sstride + w * wstride]);
     float L = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < n_split; ++s) {
-        const float *q = pp + s * sstride;
-        const float w = exp2f(q[0] - M);
-        L += q[1] * w;
-        const float4 v = *reinterpret_cast<const float4 *>(q + 4 + c0);
-        o[0] += v.x * w;
-        o[1] += v.y * w;
-        o[2] += v.z * w;
-        o[3] += v.w * w;
-    }
+    for (int s = 0; s < n_split; ++s)
+        for (int w = 0; w < n_sub; ++w) {
+            const float *q = pp + s * sstride + w * wstride;
+            const float wt = exp2f(q[0] - M);
+            L += q[1] * wt;
+            const float4 v = *reinterpret_cast<const float4 *>(q + 4 + c0);
+            o[0] += v.x * wt;
+            o[1] += v.y * wt;
+            o[2] += v.z * wt;
+            o[3] += v.w * wt;
+        }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     if (ml && c0 == 0) ml[((size_t)b * Dq + qi) * Hq + kvh * grp + r % grp] = make_float2(M, L);
     T *dst = out + (((size_t)b * Dq + qi) * Hq + kvh * grp + r % grp) * TC_D + c0;
@@ -967,7 +984,8 @@ cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt
         if (e != cudaSuccess) return e;
         dim3 cgrid(B * Hkv * pl.n_mtiles, TC_M / 4);
         return launch_pdl(verify_tc_combine<__nv_bfloat16>, cgrid, dim3(128), 0, st, (const float *)P.part,
-                          pl.n_split, pl.n_mtiles, Hkv, Hq, Dq, grp, (__nv_bfloat16 *)out, ml);
+                          pl.n_split, pl.n_mtiles, Hkv, Hq, Dq, grp, pl.tail_rows > 0 ? kTailWarps : 1,
+                          (__nv_bfloat16 *)out, ml);
     }
     const int rows = B * Dq * Hq;
     if (rows == 0) return cudaSuccess;
