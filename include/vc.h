@@ -170,7 +170,8 @@ typedef struct vc_qcache {
     void *v_res;          /* device, same */
     int32_t *n_groups;    /* device [B]: quantized groups of sequence b */
     int32_t *seq_len;     /* device [B]: cached tokens of sequence b */
-    int32_t *status;      /* device, 1 word: nonzero after a ring overflow */
+    int32_t *status;      /* device, 1 word: bits 0-1 set by a ring overflow, bit 2 by a
+                             prefill staging wait that gave up (bounded, about 2 s) */
     int32_t B, Hkv, d;
     vc_quant_cfg cfg;
     int32_t max_groups;   /* record capacity per (b, h) */

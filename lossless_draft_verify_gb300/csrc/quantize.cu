@@ -220,44 +220,88 @@ __device__ __forceinline__ float2 pair_values(const T *x, int kappa, int mu, int
     }
 }
 
+// Where the code pair of slot sl in word i of a thread sits: (kappa, mu) =
+// (kc + kp, mc + mp), with (kc, mc) fixed by (i, sl) and (kp, mp) one of two
+// per-thread pairs (sel) that depend only on the thread's warp p of the
+// section (the inverse of pair_pos split into its constant and per-thread
+// parts; with the loops over i and sl unrolled, kc and mc are constants).
+struct SlotSplit {
+    int kc, mc, sel;
+};
+template <int BITS, int D>
+__device__ __forceinline__ SlotSplit slot_split(int i, int sl)
+{
+    constexpr int W = D * BITS / 32;
+    if (BITS == 2) {
+        constexpr int h = W / 2, q = W / 4;
+        if (sl < 3) return {h * sl, 2 * i, 0};
+        if (sl >= 5) return {h * (sl - 5), 2 * i + 1, 0};
+        return {3 * h + q * (sl - 3), i, 1};
+    } else {
+        constexpr int h = W / 2;
+        return {h * (sl & 1) + (i >> 1), 2 * (i & 1) + (sl >> 1), 0};
+    }
+}
+
 // Code words of one section for this thread: words WPT*p .. WPT*p + WPT - 1
-// of lane (gid, tig), stored into the section image.
+// of lane (gid, tig), stored into the section image.  A pair (kappa, mu) holds
+// channels 8 kappa + 2 tig, +1 of token 8 mu + gid (K) or tokens 8 mu + 2 tig,
+// +1 of channel 8 kappa + gid (V), so every staged value and statistic is at a
+// per-thread base plus a constant offset.
 template <typename T, int BITS, int D, int SEC>
 __device__ __forceinline__ void code_words(const T *x, const float *stz, const float *strs, const float *sts,
                                            uint8_t *secimg, int lane, int p)
 {
     constexpr int WPT = BITS;                      // W * 32 / D words per thread
     constexpr int SLOTS = 16 / BITS;
+    constexpr int PITCH = D + 16 / (int)sizeof(T);
     constexpr uint32_t qmax = (1u << BITS) - 1u;
     const int gid = lane >> 2, tig = lane & 3;
+    // per-thread parts: sel 0 (kp, mp) = (p or 2p, 0), sel 1 (p / 2, 2 (p % 2))
+    const int kp[2] = {BITS == 2 ? p : 2 * p, p >> 1};
+    const int mp[2] = {0, 2 * (p & 1)};
+    int cb[2], tb[2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        cb[s] = 8 * kp[s] + (SEC == 0 ? 2 * tig : gid);
+        tb[s] = 8 * mp[s] + (SEC == 0 ? gid : 2 * tig);
+    }
+    const T *xb[2] = {x + tb[0] * PITCH + cb[0], x + tb[1] * PITCH + cb[1]};
     uint32_t words[WPT];
     uint32_t near = 0;                             // bit (i, sl, hh): needs the exact quotient
 #pragma unroll
     for (int i = 0; i < WPT; ++i) {
-        const int w = WPT * p + i;
-        uint32_t word = 0;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int sl = 0; sl < SLOTS; ++sl) {
-            int kappa, mu, st;
-            slot_pair<BITS, D>(w, sl, kappa, mu);
-            const float2 xv = pair_values<T, D, SEC>(x, kappa, mu, gid, tig, st);
+            const SlotSplit ss = slot_split<BITS, D>(i, sl);
+            const T *px = xb[ss.sel] + 8 * ss.mc * PITCH + 8 * ss.kc;
+            float2 xv;
+            int st;
+            if constexpr (SEC == 0) {
+                xv = load_pair<T>(px);
+                st = cb[ss.sel] + 8 * ss.kc;
+            } else {
+                xv = make_float2(Elem<T>::to_f(px[0]), Elem<T>::to_f(px[PITCH]));
+                st = ((cb[ss.sel] + 8 * ss.kc) & ~(G - 1)) + tb[ss.sel] + 8 * ss.mc;
+            }
             const float2 z = *reinterpret_cast<const float2 *>(stz + st);
             const float2 rs = *reinterpret_cast<const float2 *>(strs + st);
             // d = RN(x - z), q = RN(d * rcp(s)), m = RN(q + 1.5 * 2^23) (integer
             // part = rint(q)), e = q - rint(q), both lanes at once
             const float2 magic = make_float2(kRoundMagic, kRoundMagic);
             const float2 q = mul2(sub2(xv, z), rs);
-            const float2 m = add2(q, magic);
-            const float2 e = sub2(q, sub2(m, magic));
+            const float2 r = sub2(add2(q, magic), magic);
+            const float2 e = sub2(q, r);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int bit = (i * SLOTS + sl) * 2 + hh;
-                const int sh = BITS * sl + 16 * hh;
                 near |= near_mask(hh ? e.y : e.x, kNearHalf) & (1u << bit);
-                word |= (__float_as_uint(hh ? m.y : m.x) << sh) & (qmax << sh);
             }
+            const float wsl = (float)(1u << (BITS * sl));
+            acc = fma2(r, make_float2(wsl, wsl), acc);
         }
-        words[i] = word;
+        words[i] = (uint32_t)acc.x | ((uint32_t)acc.y << 16);
     }
     // codes within rounding distance of a half-integer: the exact quotient
     while (near) {
@@ -419,24 +463,42 @@ __device__ void rotate_rows(int n, SrcFn src, DstFn dst, float (*buf)[D])
     }
 }
 
-// Prefill: one CTA per (group, kv head, sequence); its rows are staged with
-// 16-byte loads (rotated in place for a rotated cache), then quantized.
+// Prefill: one CTA per (group, kv head, sequence); its 32 K and 32 V rows
+// arrive by one bulk copy each (all 64 in flight at once, one mbarrier with a
+// bounded wait; a wait that gives up sets bit 2 of the cache's status word
+// and leaves the group's record unwritten), are rotated in place for a
+// rotated cache, then quantized.
 template <typename T, int BITS, int D, bool ROT>
 __global__ void __launch_bounds__(2 * D, 5)
 quantize_prefill_kernel(const T *__restrict__ k, const T *__restrict__ v, int Hkv, int L_stride,
-                        int max_groups, uint8_t *__restrict__ records)
+                        int max_groups, uint8_t *__restrict__ records, int32_t *status)
 {
     using Gm = RecGeom<BITS, D>;
     using St = QStage<T, BITS, D>;
+    constexpr int ROW = D * (int)sizeof(T);
     __shared__ __align__(16) uint8_t sm[St::BYTES];
+    __shared__ __align__(8) uint64_t bar;
     const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const size_t bh = (size_t)b * Hkv + h;
     const size_t row0 = bh * L_stride + (size_t)g * G;
     T *kx = reinterpret_cast<T *>(sm);
     T *vx = reinterpret_cast<T *>(sm + St::X_BYTES);
-    stage_rows<T, D>([&](int t) { return k + (row0 + t) * D; }, kx, G, threadIdx.x, 2 * D);
-    stage_rows<T, D>([&](int t) { return v + (row0 + t) * D; }, vx, G, threadIdx.x, 2 * D);
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
     __syncthreads();
+    if (threadIdx.x < 2 * G) {
+        const int t = threadIdx.x & (G - 1);
+        const bool is_v = threadIdx.x >= G;
+        bulk_g2s((is_v ? vx : kx) + t * St::PITCH, (is_v ? v : k) + (row0 + t) * D, ROW, &bar);
+    }
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&bar, 2 * G * ROW);
+    const bool got = mbar_wait(&bar, 0);
+    if (!__syncthreads_and(got)) {
+        if (threadIdx.x == 0 && status) atomicOr(status, 4);
+        return;
+    }
     if constexpr (ROT) {
         // the key rows, rotated in place
         __shared__ __align__(16) float buf[8][D];
@@ -565,7 +627,7 @@ cudaError_t launch_prefill(const void *k, const void *v, int B, int Hkv, int L, 
         dim3 grid(nq / G, Hkv, B);
         auto kern = rot ? quantize_prefill_kernel<T, BITS, D, true> : quantize_prefill_kernel<T, BITS, D, false>;
         kern<<<grid, 2 * D, 0, st>>>((const T *)k, (const T *)v, Hkv, L_stride, c->max_groups,
-                                     (uint8_t *)c->records);
+                                     (uint8_t *)c->records, c->status);
     }
     auto rc = rot ? residual_copy_kernel<T, D, true> : residual_copy_kernel<T, D, false>;
     rc<<<B * Hkv, 256, 0, st>>>((const T *)k, (const T *)v, B, Hkv, L, L_stride, nq, (T *)c->k_res,

@@ -65,6 +65,34 @@ def test_quantize_matches_oracle(bits, d, R, L, dtype, rotate):
     _check_cache(vc, cache, k, v, L, bits, R, rotate=rotate)
 
 
+@pytest.mark.parametrize("bits,d", [(2, 128), (4, 128), (2, 64)])
+def test_quantize_codes_at_half_integers(bits, d):
+    """Every group spans [0, qmax * 2^j] (K: tokens 0 and 1 of each channel;
+    V: channels 0 and 1 of each 32-channel group), so its scale is exactly 2^j
+    and the other values, drawn from the multiples of 2^(j-1), put x / s on
+    integers and on ties (rint: ties to even).  Every word holding a tie takes
+    the quantizer's exact-quotient path; the records must still equal the
+    oracle's bit for bit."""
+    vc = lib()
+    B, H, L, G = 2, 2, 96, 32
+    qmax = (1 << bits) - 1
+    rng = np.random.default_rng(7 + bits + d)
+    halves = rng.integers(0, 2 * qmax + 1, size=(2, B, H, L, d)).astype(np.float32) * 0.5
+    halves[0, :, :, 0::G, :] = 0.0
+    halves[0, :, :, 1::G, :] = qmax
+    halves[1, :, :, :, 0::G] = 0.0
+    halves[1, :, :, :, 1::G] = qmax
+    scale = np.array([0.125, 1.0, 4.0, 0.5], dtype=np.float32).reshape(B, H, 1, 1)
+    k = torch.from_numpy(halves[0] * scale).to(torch.bfloat16).cuda()
+    v = torch.from_numpy(halves[1] * scale).to(torch.bfloat16).cuda()
+    assert torch.equal(k.float().cpu(), torch.from_numpy(halves[0] * scale))   # exact in bf16
+    cache = vc.QCache(B, H, d, bits, L // G, G + 8, 0)
+    vc.vc_quantize_kv(k, v, cache, L=L)
+    torch.cuda.synchronize()
+    _check_cache(vc, cache, k, v, L, bits, 0)
+    assert int(cache.status.item()) == 0
+
+
 @pytest.mark.parametrize("bits,R,rotate", [(2, 128, False), (4, 0, False), (2, 64, True)])
 def test_append_equals_one_shot(bits, R, rotate):
     """Appending tokens (ragged per sequence) and re-quantizing leaving groups
