@@ -760,9 +760,12 @@ def run_model(args, dev, rank, world, barrier, pg):
     P = args.prompt
     W = inputs.decoder_weights_packed(cfg, seed=0, device=dev)
     dec = vc.Decoder.from_packed(cfg, W["embed"], W["lm_head"], W["wqkv"], W["wo"], W["wgu"], W["wd"])
-    n_e2e = 0 if args.no_e2e else args.steps
     n_tr = 1                                  # traced round
-    total = args.warmup + n_tr + args.steps + n_e2e
+    # K untimed rounds after the timed ones add tokens to the losslessness
+    # check (the cache capacity, and so the bytes every swap moves, follow the
+    # round count: it is kept at warm-up + traced + 2 K)
+    n_extra = args.steps
+    total = args.warmup + n_tr + args.steps + n_extra
     max_len = P + total * (M_HORIZON + 1) + 64
     packed = args.swap != "raw"                 # default packed
     run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=args.bits, residual=M_RESIDUAL, host_cache=True,
@@ -795,19 +798,51 @@ def run_model(args, dev, rank, world, barrier, pg):
     if not args.no_graph:
         run.capture_draft_graph()
     base0 = args.warmup + n_tr
-    barrier()
+    # The K timed rounds are timed by two clocks at once.  value: device events
+    # around the rounds (tokens / device time).  e2e: the host's wall clock
+    # around the same rounds, as a serving loop sees them: each round's emitted
+    # tokens (drafts, accepted length, next token) are copied to pinned host
+    # memory and read by the host; the next round needs nothing from the host,
+    # so round i + 1 is issued before the host waits for round i's tokens.
+    # Every round's input, the full cache, comes in from pinned host memory
+    # inside the round.  Timing both on the same rounds keeps the host link's
+    # drift between runs out of their comparison.
+    want_e2e = not args.no_e2e
+    n_out = M_B * (M_HORIZON + 2)
+    h_out = [torch.empty(n_out, dtype=torch.int32).pin_memory() for _ in range(2)]
+    d2h = n_out * 4
+    ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+    checksum = 0
     evs = [run.new_events() for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
+    torch.cuda.synchronize()
+    barrier()
+    wall0 = time.perf_counter()
     t0.record()
     torch.cuda.nvtx.range_push("timed_rounds")
     for i in range(args.steps):
         run.round(log, base0 + i, evs[i])
+        if want_e2e:
+            ho = h_out[i & 1]
+            ho[:M_B * M_HORIZON].copy_(run.drafts.view(-1), non_blocking=True)
+            ho[M_B * M_HORIZON:M_B * (M_HORIZON + 1)].copy_(run.n_acc, non_blocking=True)
+            ho[M_B * (M_HORIZON + 1):].copy_(run.x, non_blocking=True)
+            ev_out[i & 1].record()
+        if i == args.steps - 1:
+            t1.record()
+        if want_e2e and i > 0:
+            ev_out[(i - 1) & 1].synchronize()              # round i - 1's tokens are on the host
+            checksum += int(h_out[(i - 1) & 1].sum())
+    if want_e2e:
+        ev_out[(args.steps - 1) & 1].synchronize()
+        checksum += int(h_out[(args.steps - 1) & 1].sum())
+    wall1 = time.perf_counter()
     torch.cuda.nvtx.range_pop()
-    t1.record()
+    torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
@@ -815,38 +850,11 @@ def run_model(args, dev, rank, world, barrier, pg):
     tokens = int((n_acc.long() + 1).sum())
     value, ms_max = replicas.whole_job_rate(tokens, ms, pg, device=dev)
     st = vc.vc_poll_status(run.ws)
-
-    # end to end: the same rounds through the public runner, each round's
-    # emitted tokens (drafts, accepted length, next token) copied to pinned host
-    # memory and read by the host, as a serving loop does.  The next round needs
-    # nothing from the host, so round i + 1 is issued before the host waits for
-    # round i's tokens; every round's input, the full cache, comes in from
-    # pinned host memory inside the round
     e2e_val = None
-    n_out = M_B * (M_HORIZON + 2)
-    h_out = [torch.empty(n_out, dtype=torch.int32).pin_memory() for _ in range(2)]
-    d2h = n_out * 4
-    if n_e2e:
-        barrier()
-        e0 = time.perf_counter()
-        base = base0 + args.steps
-        ev_out = [torch.cuda.Event(), torch.cuda.Event()]
-        checksum = 0
-        for i in range(n_e2e + 1):
-            if i < n_e2e:
-                run.round(log, base + i)
-                ho = h_out[i & 1]
-                ho[:M_B * M_HORIZON].copy_(run.drafts.view(-1), non_blocking=True)
-                ho[M_B * M_HORIZON:M_B * (M_HORIZON + 1)].copy_(run.n_acc, non_blocking=True)
-                ho[M_B * (M_HORIZON + 1):].copy_(run.x, non_blocking=True)
-                ev_out[i & 1].record()
-            if i > 0:
-                ev_out[(i - 1) & 1].synchronize()          # round i - 1's tokens are on the host
-                checksum += int(h_out[(i - 1) & 1].sum())
-        e_ms = (time.perf_counter() - e0) * 1e3
-        barrier()
-        e_tok = int((log.n_acc[base:base + n_e2e].cpu().long() + 1).sum())
-        e2e_val, _ = replicas.whole_job_rate(e_tok, e_ms, pg, device=dev)
+    if want_e2e:
+        e2e_val, _ = replicas.whole_job_rate(tokens, (wall1 - wall0) * 1e3, pg, device=dev)
+    for i in range(n_extra):
+        run.round(log, base0 + args.steps + i)
     run.check_packed()                   # every committed row was held by the packed host copy
 
     # per-phase times and the swap's overlap with drafting, measured as the
@@ -977,8 +985,9 @@ def run_model(args, dev, rank, world, barrier, pg):
             "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc, packed) * args.steps,
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, max_len, packed),
                     "d2h_bytes_per_step": d2h + model_writeback_bytes(cfg, n_acc, packed),
-                    "how": "host wall clock over the rounds; each round's tokens are copied to pinned host memory "
-                           "and read by the host while the next round runs"},
+                    "how": "host wall clock over the same K rounds as value (which uses device events around "
+                           "them); each round's tokens are copied to pinned host memory and read by the host while "
+                           "the next round runs"},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

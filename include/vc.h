@@ -572,6 +572,23 @@ typedef enum vc_trace_kind {
 vc_status vc_decoder_set_trace(vc_decoder *dec, cudaEvent_t *events, int32_t *kinds, int capacity, int kind_mask);
 int vc_decoder_trace_count(const vc_decoder *dec);
 
+/*
+ * Per-layer arrival of a full cache that is being copied in (the swap-in
+ * overlapped with the rest of the round, paper page "What the paper found"):
+ * after vc_decoder_set_layer_events(dec, events, n_layers), vc_decoder_forward
+ * and vc_decoder_verify make their stream wait on events[l]
+ * (cudaStreamWaitEvent) before their first access to layer l of k_cache and
+ * v_cache, so layer l's work starts once that layer is resident instead of
+ * once the whole cache is.  The caller records events[l] on the copying
+ * stream after layer l's copy (and expansion) is enqueued, before it enqueues
+ * the forward; an event never recorded is no wait.  The handles are copied
+ * (the caller owns the events and keeps them alive while set); n = 0 clears
+ * them.  Not for calls enqueued while their stream is being captured.
+ * Errors: VC_ERR_INVALID for dec NULL, n < 0, or n > 0 with events NULL, a
+ * NULL handle or n != n_layers.
+ */
+vc_status vc_decoder_set_layer_events(vc_decoder *dec, const cudaEvent_t *events, int n);
+
 /* Workspace for calls with up to B sequences of up to max_rows rows each and
  * contexts up to max_ctx tokens; draft_cache (may be NULL when only
  * vc_decoder_forward is used) is a cache of the geometry later passed to

@@ -32,6 +32,9 @@ struct vc_decoder {
     mutable cudaEvent_t *tr_ev = nullptr;
     mutable int32_t *tr_kind = nullptr;
     mutable int tr_cap = 0, tr_n = 0, tr_mask = 0;
+    // optional: one event per layer, recorded when that layer's full cache is
+    // resident; a forward waits on event l before it touches layer l's cache
+    std::vector<cudaEvent_t> layer_ev;
 };
 
 namespace vc {
@@ -426,6 +429,7 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
             return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
                         C.counters(), C.status(), C.st, C.plan);
         }));
+        if (!C.d->layer_ev.empty()) VC_TRY(cudaStreamWaitEvent(C.st, C.d->layer_ev[l], 0));
         RopeDst dst;
         dst.k1 = (T *)kc + l * layer_cache;
         dst.v1 = (T *)vcache + l * layer_cache;
@@ -597,6 +601,20 @@ vc_status vc_decoder_set_trace(vc_decoder *dec, cudaEvent_t *events, int32_t *ki
 }
 
 int vc_decoder_trace_count(const vc_decoder *dec) { return dec ? dec->tr_n : 0; }
+
+vc_status vc_decoder_set_layer_events(vc_decoder *dec, const cudaEvent_t *events, int n)
+{
+    if (!dec || n < 0) return VC_ERR_INVALID;
+    if (n == 0) {
+        dec->layer_ev.clear();
+        return VC_OK;
+    }
+    if (!events || n != dec->c.n_layers) return VC_ERR_INVALID;
+    for (int l = 0; l < n; ++l)
+        if (!events[l]) return VC_ERR_INVALID;
+    dec->layer_ev.assign(events, events + n);
+    return VC_OK;
+}
 
 size_t vc_decoder_workspace_bytes(const vc_decoder *dec, int B, int max_rows, int max_ctx,
                                   const vc_qcache *draft_cache)

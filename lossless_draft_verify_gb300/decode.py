@@ -25,6 +25,7 @@ The round emits d1..dn and next.
 """
 from __future__ import annotations
 
+import contextlib
 import dataclasses
 
 import torch
@@ -121,6 +122,10 @@ class VeriCacheRunner:
         self.ctx_bound = 0
         self.side = torch.cuda.Stream(device=device)
         self.ev_swap = torch.cuda.Event()
+        # ev_ready[l]: layer l of the swapped-in cache is resident (copied, and
+        # expanded when packed); a forward over the full cache waits on it
+        # before touching layer l, so the verify pass overlaps the swap's tail
+        self.ev_ready = [torch.cuda.Event() for _ in range(nl)] if host_cache else None
 
     # ------------------------------------------------------------ prefill --
     def prefill(self, prompt: torch.Tensor):
@@ -200,14 +205,15 @@ class VeriCacheRunner:
                 events[t - 1][0].record(main)
             if self.host_cache:
                 self._swap_in(main)
-                main.wait_event(self.ev_swap)
-                vc.vc_decoder_forward(self.dec, self.x, None, 0, B, 1, self.ctx, self.ctx_bound, self.k_full,
-                                      self.v_full, self.logits_d, self.ws, k_blk=k1, v_blk=v1, last_only=True)
+                with self._layer_arrivals():
+                    vc.vc_decoder_forward(self.dec, self.x, None, 0, B, 1, self.ctx, self.ctx_bound, self.k_full,
+                                          self.v_full, self.logits_d, self.ws, k_blk=k1, v_blk=v1, last_only=True)
             else:
                 vc.vc_decoder_forward(self.dec, self.x, None, 0, B, 1, self.ctx, self.ctx_bound, self.k_full,
                                       self.v_full, self.logits_d, self.ws, last_only=True)
             vc.vc_accept(self.logits_d.view(B, 1, -1), None, self.n_acc, self.x, self.ws_acc)
             if self.host_cache:
+                main.wait_event(self.ev_swap)          # the copy has read the host copy
                 self._write_back(k1, v1, zero, self.ctx)
             if events is not None:
                 events[t - 1][1].record(main)
@@ -217,6 +223,20 @@ class VeriCacheRunner:
             self.ctx += 1
             self.ctx_bound += 1
         return out.t().cpu().tolist()
+
+    @contextlib.contextmanager
+    def _layer_arrivals(self):
+        """While enqueuing a forward over the swapped-in cache: the decoder
+        waits on this runner's per-layer arrival events (the decoder object
+        may be shared with other runners, so they are cleared afterwards)."""
+        if not self.host_cache:
+            yield
+            return
+        vc.vc_decoder_set_layer_events(self.dec, self.ev_ready)
+        try:
+            yield
+        finally:
+            vc.vc_decoder_set_layer_events(self.dec, None)
 
     @staticmethod
     def _top2_margin(logits: torch.Tensor) -> torch.Tensor:
@@ -242,10 +262,13 @@ class VeriCacheRunner:
                 self.unpack_stream.wait_event(self.ev_layer[l])
                 vc.vc_kv_unpack(self.k_pack[l], self.k_full[l], stream=self.unpack_stream)
                 vc.vc_kv_unpack(self.v_pack[l], self.v_full[l], stream=self.unpack_stream)
+                self.ev_ready[l].record(self.unpack_stream)
             self.ev_swap.record(self.unpack_stream)
         else:
-            vc.vc_swap_in(self.k_full, self.k_host, stream=self.side)
-            vc.vc_swap_in(self.v_full, self.v_host, stream=self.side, done_event=self.ev_swap)
+            for l in range(len(self.qc)):
+                vc.vc_swap_in(self.k_full[l], self.k_host[l], stream=self.side)
+                vc.vc_swap_in(self.v_full[l], self.v_host[l], stream=self.side, done_event=self.ev_ready[l])
+            self.ev_swap.record(self.side)
         if ev is not None:
             ev["swap1"].record(self.unpack_stream if self.pack_host else self.side)
 
@@ -300,26 +323,28 @@ class VeriCacheRunner:
         copy (main stream)."""
         B, D = self.B, self.D
         main = torch.cuda.current_stream()
-        if self.host_cache:
-            main.wait_event(self.ev_swap)
         if ev is not None:
             ev["v0"].record(main)
         max_ctx = min(self.ctx_bound, self.L_stride - (D + 1))
         if self.fused_head:
             # verify pass and acceptance in one call; next token overwrites x
-            vc.vc_decoder_verify(self.dec, self.x, self.drafts, D, B, self.round_len, max_ctx, self.k_full,
-                                 self.v_full, self.n_acc, self.x, self.ws, k_blk=self.k_blk, v_blk=self.v_blk)
+            with self._layer_arrivals():
+                vc.vc_decoder_verify(self.dec, self.x, self.drafts, D, B, self.round_len, max_ctx, self.k_full,
+                                     self.v_full, self.n_acc, self.x, self.ws, k_blk=self.k_blk, v_blk=self.v_blk)
             if ev is not None:
                 ev["v1"].record(main)
         else:
-            vc.vc_decoder_forward(self.dec, self.x, self.drafts, D, B, D + 1, self.round_len, max_ctx, self.k_full,
-                                  self.v_full, self.logits_v, self.ws, k_blk=self.k_blk, v_blk=self.v_blk)
+            with self._layer_arrivals():
+                vc.vc_decoder_forward(self.dec, self.x, self.drafts, D, B, D + 1, self.round_len, max_ctx,
+                                      self.k_full, self.v_full, self.logits_v, self.ws, k_blk=self.k_blk,
+                                      v_blk=self.v_blk)
             if ev is not None:
                 ev["v1"].record(main)
             vc.vc_accept(self.logits_v, self.drafts, self.n_acc, self.x, self.ws_acc)
         for l, q in enumerate(self.qc):
             vc.vc_qcache_commit(q, self.k_blk[l], self.v_blk[l], self.round_len, self.n_acc)
         if self.host_cache:
+            main.wait_event(self.ev_swap)              # the copy has read the host copy
             self._write_back(self.k_blk, self.v_blk, self.n_acc, self.round_len)
         if ev is not None:
             ev["c1"].record(main)

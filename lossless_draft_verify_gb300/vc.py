@@ -148,6 +148,8 @@ def load() -> ctypes.CDLL:
     L.vc_decoder_set_trace.argtypes = [P, P, P, c_int, c_int]
     L.vc_decoder_trace_count.restype = c_int
     L.vc_decoder_trace_count.argtypes = [P]
+    L.vc_decoder_set_layer_events.restype = c_int
+    L.vc_decoder_set_layer_events.argtypes = [P, P, c_int]
     L.vc_gemm_splits.restype = c_int
     L.vc_gemm_splits.argtypes = [c_int, c_int, c_int, c_int]
     L.vc_gemm_workspace_bytes.restype = c_size_t
@@ -185,7 +187,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe",
             "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify",
             "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack", "vc_kv_writeback_packed",
-            "vc_verify_attn_h2o_workspace_bytes", "vc_verify_attn_h2o"]
+            "vc_verify_attn_h2o_workspace_bytes", "vc_verify_attn_h2o", "vc_decoder_set_layer_events"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -574,6 +576,21 @@ def vc_kv_writeback(k_blk, v_blk, n_acc, ctx_len, k_host, v_host, stream=None):
     _check(load().vc_kv_writeback(k_blk.data_ptr(), v_blk.data_ptr(), _dt(k_blk), nl, B, Hkv, Dq, d,
                                   n_acc.data_ptr(), ctx_len.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
                                   L_stride, _stream(stream)), "vc_kv_writeback")
+
+
+def vc_decoder_set_layer_events(dec: Decoder, events: list | None):
+    """Per-layer arrival events of a full cache being copied in: the decoder's
+    forward and verify wait on events[l] before touching layer l (include/vc.h,
+    vc_decoder_set_layer_events).  events: one torch.cuda.Event per layer,
+    recorded by the caller on the copying stream; None clears them."""
+    if not events:
+        _check(load().vc_decoder_set_layer_events(dec.handle, None, 0), "vc_decoder_set_layer_events")
+        return
+    for e in events:                                 # torch creates events lazily
+        if not e.cuda_event:
+            e.record()
+    arr = (c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(load().vc_decoder_set_layer_events(dec.handle, arr, len(events)), "vc_decoder_set_layer_events")
 
 
 class DecoderTrace:

@@ -92,6 +92,15 @@ def test_decoder_validation_on_the_host(libvc):
     assert create() == vc.VC_OK and h.value
     assert L.vc_decoder_workspace_bytes(h, 1, 16, 1024, None) > 0
     assert L.vc_decoder_workspace_bytes(h, 0, 16, 1024, None) == 0
+    # per-layer arrival events: one non-null handle per layer, or none
+    evs = (ctypes.c_void_p * n)(0x1000, 0x2000)
+    assert L.vc_decoder_set_layer_events(h, evs, n) == vc.VC_OK
+    assert L.vc_decoder_set_layer_events(h, None, 0) == vc.VC_OK
+    assert L.vc_decoder_set_layer_events(h, evs, n - 1) == vc.VC_ERR_INVALID
+    assert L.vc_decoder_set_layer_events(h, None, n) == vc.VC_ERR_INVALID
+    assert L.vc_decoder_set_layer_events(h, (ctypes.c_void_p * n)(0x1000, None), n) == vc.VC_ERR_INVALID
+    assert L.vc_decoder_set_layer_events(h, evs, -1) == vc.VC_ERR_INVALID
+    assert L.vc_decoder_set_layer_events(None, evs, n) == vc.VC_ERR_INVALID
     L.vc_decoder_destroy(h)
     assert create(head_dim=96) == vc.VC_ERR_UNSUPPORTED
     assert create(n_heads=16, n_kv_heads=2) == vc.VC_ERR_UNSUPPORTED     # 8 q heads per kv head
