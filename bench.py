@@ -770,6 +770,7 @@ def run_model(args, dev, rank, world, barrier, pg):
     packed = args.swap != "raw"                 # default packed
     run = decode.VeriCacheRunner(dec, M_B, max_len, M_HORIZON, bits=args.bits, residual=M_RESIDUAL, host_cache=True,
                                  prefill_chunk=512, device=dev, rotate=args.rotate, pack_host=packed)
+    run.expand_after_draft = not args.expand_during_draft
     prompt = inputs.random_prompts(M_B, P, cfg.vocab, seed=rank, device=dev)
     t_pf = time.perf_counter()
     run.prefill(prompt)
@@ -1298,6 +1299,9 @@ def main():
     ap.add_argument("--no-check", action="store_true", help="skip the lossless check (--workload model)")
     ap.add_argument("--check-tokens", type=int, default=256, help="tokens per sequence compared by the check")
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4], help="draft cache bits (--workload model)")
+    ap.add_argument("--expand-during-draft", action="store_true",
+                    help="model workload: expand the packed swap as each layer lands, during the draft steps "
+                         "(default: after them)")
     ap.add_argument("--no-graph", action="store_true",
                     help="--workload model: launch the draft steps one by one instead of replaying a CUDA graph")
     ap.add_argument("--rotate", action="store_true",

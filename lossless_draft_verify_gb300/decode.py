@@ -126,6 +126,10 @@ class VeriCacheRunner:
         # expanded when packed); a forward over the full cache waits on it
         # before touching layer l, so the verify pass overlaps the swap's tail
         self.ev_ready = [torch.cuda.Event() for _ in range(nl)] if host_cache else None
+        # expand_after_draft: in round(), packed rows are expanded after the
+        # draft steps instead of while they run
+        self.expand_after_draft = True
+        self.ev_drafted = torch.cuda.Event()
 
     # ------------------------------------------------------------ prefill --
     def prefill(self, prompt: torch.Tensor):
@@ -245,32 +249,50 @@ class VeriCacheRunner:
         top = torch.topk(logits.float(), 2, dim=-1).values
         return top[..., 0] - top[..., 1]
 
+    def _swap_copies(self, ev: dict | None = None):
+        """The link part of the swap: the host copy of the full cache into the
+        device, layer by layer on the side stream (packed rows into the
+        staging buffer, each layer marked by ev_layer[l]; bf16 rows straight
+        into the cache, each layer marked by ev_ready[l]).  ev["swap0"] and
+        ev["swap1"] bracket the transfer."""
+        if ev is not None:
+            ev["swap0"].record(self.side)
+        for l in range(len(self.qc)):
+            if self.pack_host:
+                vc.vc_swap_in(self.k_pack[l], self.k_host[l], stream=self.side)
+                vc.vc_swap_in(self.v_pack[l], self.v_host[l], stream=self.side, done_event=self.ev_layer[l])
+            else:
+                vc.vc_swap_in(self.k_full[l], self.k_host[l], stream=self.side)
+                vc.vc_swap_in(self.v_full[l], self.v_host[l], stream=self.side, done_event=self.ev_ready[l])
+        if ev is not None:
+            ev["swap1"].record(self.side)
+        if not self.pack_host:
+            self.ev_swap.record(self.side)
+
+    def _swap_expand(self, after: torch.cuda.Event | None = None):
+        """Packed rows: each layer expanded into the bf16 cache on the unpack
+        stream once its copy has landed (and after `after` when given);
+        ev_ready[l] marks layer l, self.ev_swap the whole cache."""
+        if not self.pack_host:
+            return
+        if after is not None:
+            self.unpack_stream.wait_event(after)
+        for l in range(len(self.qc)):
+            self.unpack_stream.wait_event(self.ev_layer[l])
+            vc.vc_kv_unpack(self.k_pack[l], self.k_full[l], stream=self.unpack_stream)
+            vc.vc_kv_unpack(self.v_pack[l], self.v_full[l], stream=self.unpack_stream)
+            self.ev_ready[l].record(self.unpack_stream)
+        self.ev_swap.record(self.unpack_stream)
+
     def _swap_in(self, main: torch.cuda.Stream, ev: dict | None = None, wait_main: bool = True):
         """Copy the host copy of the full cache into the device cache on the
-        side stream (packed rows are expanded layer by layer on a second
-        stream); self.ev_swap marks the end.  wait_main: the copy waits for
+        side stream, packed rows expanded layer by layer on a second stream as
+        they land; self.ev_swap marks the end.  wait_main: the copy waits for
         everything issued on `main` so far (else the caller has ordered it)."""
         if wait_main:
             self.side.wait_stream(main)
-        if ev is not None:
-            ev["swap0"].record(self.side)
-        if self.pack_host:
-            self.unpack_stream.wait_stream(self.side)
-            for l in range(len(self.qc)):
-                vc.vc_swap_in(self.k_pack[l], self.k_host[l], stream=self.side)
-                vc.vc_swap_in(self.v_pack[l], self.v_host[l], stream=self.side, done_event=self.ev_layer[l])
-                self.unpack_stream.wait_event(self.ev_layer[l])
-                vc.vc_kv_unpack(self.k_pack[l], self.k_full[l], stream=self.unpack_stream)
-                vc.vc_kv_unpack(self.v_pack[l], self.v_full[l], stream=self.unpack_stream)
-                self.ev_ready[l].record(self.unpack_stream)
-            self.ev_swap.record(self.unpack_stream)
-        else:
-            for l in range(len(self.qc)):
-                vc.vc_swap_in(self.k_full[l], self.k_host[l], stream=self.side)
-                vc.vc_swap_in(self.v_full[l], self.v_host[l], stream=self.side, done_event=self.ev_ready[l])
-            self.ev_swap.record(self.side)
-        if ev is not None:
-            ev["swap1"].record(self.unpack_stream if self.pack_host else self.side)
+        self._swap_copies(ev)
+        self._swap_expand()
 
     def _write_back(self, k_blk, v_blk, n_acc, ctx_len):
         """Committed rows (i <= n_acc[b]) of a block into the host copy at
@@ -288,10 +310,20 @@ class VeriCacheRunner:
         runner's own (e.g. one captured with tracing on)."""
         main = torch.cuda.current_stream()
         self.round_len.copy_(self.qc[0].seq_len)
+        defer = self.host_cache and self.pack_host and self.expand_after_draft
         if self.host_cache:
             self.side.wait_stream(main)
-            self.swap_phase(ev)
+            if defer:
+                self._swap_copies(ev)
+            else:
+                self.swap_phase(ev)
         self.draft_phase(ev, graph)
+        if defer:
+            # the packed rows are expanded once the draft steps have run, so
+            # the expansion's HBM traffic does not slow them (the link copies
+            # still overlap them); layer l's verify waits for layer l only
+            self.ev_drafted.record(main)
+            self._swap_expand(after=self.ev_drafted)
         self.verify_phase(log, r, ev)
 
     def swap_phase(self, ev: dict | None = None, after: torch.cuda.Event | None = None):
