@@ -699,9 +699,11 @@ class ModelOracleSample:
         qd, kvd, F = c1.n_heads * c1.head_dim, c1.n_kv_heads * c1.head_dim, c1.d_ff
         f = lambda t: t.double().numpy()
         wqkv, wgu = W["wqkv"][0], W["wgu"][0]
+        gu = wgu.reshape(c1.d_model, F // 64, 2, 64)        # gate and up interleaved per 64 columns
         weights = {"embed": f(W["embed"]), "lm_head": f(W["lm_head"]),
                    "layers": [{"wq": f(wqkv[:, :qd]), "wk": f(wqkv[:, qd:qd + kvd]), "wv": f(wqkv[:, qd + kvd:]),
-                               "wo": f(W["wo"][0]), "wg": f(wgu[:, :F]), "wu": f(wgu[:, F:]), "wd": f(W["wd"][0])}]}
+                               "wo": f(W["wo"][0]), "wg": f(gu[:, :, 0].reshape(c1.d_model, F)),
+                               "wu": f(gu[:, :, 1].reshape(c1.d_model, F)), "wd": f(W["wd"][0])}]}
         del W
         self.m = om.TinyDecoder(weights, c1)
         self.g = np.random.default_rng(0)
@@ -1130,8 +1132,10 @@ def model_launches_per_round(cfg, vc, packed: bool = False) -> int:
         return 1 + int(split and tiles > 64 and not argmax)
 
     def layer(M, decode, attn_kernels):
-        # rmsnorm, qkv, rope, attention, o, rmsnorm, gate_up, silu, down
-        return 2 + 1 + sum(g(M, N, K, decode) for N, K in shapes) + 1 + attn_kernels
+        # rmsnorm, qkv, rope, attention, o, rmsnorm, gate_up, silu, down; the
+        # SwiGLU runs in the gate|up GEMM's epilogue when that product is unsplit
+        fused = vc.vc_gemm_splits(torch.bfloat16, 2 * cfg.d_ff, cfg.d_model, decode) == 1
+        return 2 + 1 + sum(g(M, N, K, decode) for N, K in shapes) + (0 if fused else 1) + attn_kernels
 
     rows_v = M_B * (M_HORIZON + 1)
     # embed, layers (+ append), rmsnorm, LM head (argmax), acceptance, scatter, status fold

@@ -541,7 +541,10 @@ typedef struct vc_decoder_weights {
     const void *lm_head;              /* [d_model][vocab] */
     const void *const *w_qkv;         /* [d_model][(Hq + 2 Hkv) head_dim]: q | k | v columns */
     const void *const *w_o;           /* [Hq head_dim][d_model] */
-    const void *const *w_gate_up;     /* [d_model][2 d_ff]: gate | up columns */
+    const void *const *w_gate_up;     /* [d_model][2 d_ff]: gate and up columns interleaved per 64
+                                         (column 128 t + j is gate column 64 t + j, column 128 t + 64 + j
+                                         up column 64 t + j), so that a 128-column GEMM tile holds the
+                                         gate and up halves of 64 activations (d_ff % 64 == 0) */
     const void *const *w_down;        /* [d_ff][d_model] */
 } vc_decoder_weights;
 
@@ -549,7 +552,7 @@ typedef struct vc_decoder vc_decoder;   /* host object: configuration + weight p
 
 /* Validate and record the model; no device memory is allocated.
  * Supported: head_dim in {64, 128}, n_heads % n_kv_heads == 0 with at most 4
- * q heads per kv head (the draft kernel), bf16 or fp32. */
+ * q heads per kv head (the draft kernel), d_ff % 64 == 0, bf16 or fp32. */
 vc_status vc_decoder_create(const vc_decoder_cfg *cfg, const vc_decoder_weights *w, vc_decoder **out);
 void vc_decoder_destroy(vc_decoder *dec);
 
@@ -687,6 +690,18 @@ vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc
  */
 vc_status vc_gemm_argmax(const void *x, const void *w, vc_dtype dt, int M, int N, int K, int decode_plan,
                          float *tile_max, int32_t *tile_idx, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * vc_gemm_swiglu -- the decoder's gate|up projection with its SwiGLU in the
+ * GEMM epilogue: with g, u the bf16-rounded products x W of a gate column and
+ * its up column (w_gate_up [K][2F] in the decoder's interleaved layout, see
+ * vc_decoder_weights), act [M][F] (row-major) receives bf16(g / (1 + exp(-g))
+ * * u), the value a separate pass over the stored bf16 product gives.  For
+ * bf16 products the plan (decode_plan as for vc_gemm_ex) leaves unsplit,
+ * F % 64 == 0, K % 64 == 0; VC_ERR_UNSUPPORTED otherwise.  No workspace.
+ */
+vc_status vc_gemm_swiglu(const void *x, const void *w_gate_up, void *act, vc_dtype dt, int M, int F, int K,
+                         int decode_plan, cudaStream_t stream);
 
 /* vc_gemm with the split plan chosen explicitly: decode_plan != 0 runs the plan
  * of vc_decoder_draft_step (for M <= 16 it loads only 16 rows of x per K slice

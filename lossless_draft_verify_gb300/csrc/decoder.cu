@@ -183,7 +183,9 @@ rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd
     }
 }
 
-// act = silu(gate) * up, gate | up the two halves of a [M][2F] row.
+// act = silu(gate) * up from a [M][2F] row whose columns hold gate and up
+// interleaved per 64 (columns 128 t + j: gate 64 t + j; 128 t + 64 + j: up
+// 64 t + j), the layout of the decoder's gate|up weight.
 template <typename T>
 __global__ void silu_mul_kernel(const T *__restrict__ gu, int M, int F, T *__restrict__ act)
 {
@@ -192,8 +194,9 @@ __global__ void silu_mul_kernel(const T *__restrict__ gu, int M, int F, T *__res
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)M * F) return;
     const size_t m = idx / F, j = idx % F;
-    const float g = Elem<T>::to_f(gu[m * 2 * F + j]);
-    const float u = Elem<T>::to_f(gu[m * 2 * F + F + j]);
+    const size_t gc = (j / 64) * 128 + j % 64;
+    const float g = Elem<T>::to_f(gu[m * 2 * F + gc]);
+    const float u = Elem<T>::to_f(gu[m * 2 * F + gc + 64]);
     act[idx] = Elem<T>::from_f((g / (1.0f + expf(-g))) * u);
 }
 
@@ -365,13 +368,21 @@ cudaError_t layer_tail(const Ctx &C, int l, int M)
                     C.st, C.plan);
     }));
     VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
-    VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
-        return gemm(h, C.d->wgu[l], nullptr, C.at(C.L.gu), c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, part,
-                    C.counters(), C.status(), C.st, C.plan);
-    }));
-    const size_t n = (size_t)M * c.d_ff;
-    VC_TRY(launch_pdl(silu_mul_kernel<T>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, C.st,
-                      C.at<const T>(C.L.gu), M, c.d_ff, C.at<T>(C.L.act)));
+    if (gemm_swiglu_ok(c.dt, c.d_ff, c.d_model, C.plan)) {
+        // gate|up product and SwiGLU in one launch (the tensor-core epilogue)
+        VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
+            return gemm_swiglu(h, C.d->wgu[l], C.at(C.L.act), c.dt, M, c.d_ff, c.d_model, c.d_model, C.status(),
+                               C.st, C.plan);
+        }));
+    } else {
+        VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
+            return gemm(h, C.d->wgu[l], nullptr, C.at(C.L.gu), c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, part,
+                        C.counters(), C.status(), C.st, C.plan);
+        }));
+        const size_t n = (size_t)M * c.d_ff;
+        VC_TRY(launch_pdl(silu_mul_kernel<T>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, C.st,
+                          C.at<const T>(C.L.gu), M, c.d_ff, C.at<T>(C.L.act)));
+    }
     return traced(C, VC_TRACE_GEMM_DOWN, [&] {
         return gemm(C.at(C.L.act), C.d->wd[l], x, x, c.dt, M, c.d_model, c.d_ff, c.d_ff, part, C.counters(),
                     C.status(), C.st, C.plan);
@@ -560,7 +571,7 @@ vc_status vc_decoder_create(const vc_decoder_cfg *cfg, const vc_decoder_weights 
     if (c.dt != VC_BF16 && c.dt != VC_F32) return VC_ERR_INVALID;
     if (c.n_heads % c.n_kv_heads || c.n_heads / c.n_kv_heads > 4) return VC_ERR_UNSUPPORTED;
     if (c.head_dim != 64 && c.head_dim != 128) return VC_ERR_UNSUPPORTED;
-    if (c.d_model % 8 || c.d_ff % 8 || c.vocab % 8) return VC_ERR_UNSUPPORTED;
+    if (c.d_model % 8 || c.d_ff % 64 || c.vocab % 8) return VC_ERR_UNSUPPORTED;   // gate|up interleaved per 64
     if (!(c.norm_eps >= 0.f) || !(c.rope_theta > 0.f)) return VC_ERR_INVALID;
     if (!w->embed || !w->lm_head || !w->w_qkv || !w->w_o || !w->w_gate_up || !w->w_down) return VC_ERR_INVALID;
     if (!aligned16(w->embed) || !aligned16(w->lm_head)) return VC_ERR_INVALID;
@@ -730,6 +741,16 @@ vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc
                   void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     return vc_gemm_ex(x, w, resid, out, dt, M, N, K, 0, ws, ws_bytes, stream);
+}
+
+vc_status vc_gemm_swiglu(const void *x, const void *w_gate_up, void *act, vc_dtype dt, int M, int F, int K,
+                         int decode_plan, cudaStream_t stream)
+{
+    if (!x || !w_gate_up || !act || M <= 0 || F <= 0 || K <= 0) return VC_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w_gate_up) || !aligned16(act)) return VC_ERR_INVALID;
+    const int plan = decode_plan ? kGemmDecode : kGemmRowInvariant;
+    if (!gemm_swiglu_ok(dt, F, K, plan)) return VC_ERR_UNSUPPORTED;
+    return to_status(gemm_swiglu(x, w_gate_up, act, dt, M, F, K, K, nullptr, stream, plan));
 }
 
 vc_status vc_gemm_argmax(const void *x, const void *w, vc_dtype dt, int M, int N, int K, int decode_plan,

@@ -68,6 +68,7 @@ struct GemmArgs {
     int32_t *status;
     int M, N, K, S, kb_per_split;
     int early_w;                 // W may be read before the previous kernel completes
+    int swiglu;                  // SwiGLU epilogue (S = 1): out is act [M][N / 2]
 };
 
 // bf16 rounding of an output element, as the logits store would make it
@@ -189,7 +190,37 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int m = m0 + r;
         const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
         const bool ok = g_wait(&B->acc_full, 0, B, A.status, 43);
-        if (ok) {
+        if (ok && A.swiglu) {
+            // SwiGLU epilogue: columns [0, 64) of the tile are gate columns and
+            // [64, 128) the matching up columns (the weight's columns are
+            // interleaved per 64); act = silu(g) u from the bf16-rounded g and
+            // u, the expression a separate pass over the stored product uses
+            tc::fence_after();
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t ug[32], uu[32];
+                tc::ld32(taddr + h * 32, ug);
+                tc::ld32(taddr + (h + 2) * 32, uu);
+                tc::ld_wait();
+                if (m < A.M) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float g0 = bf16_round(__uint_as_float(ug[c]));
+                        const float g1 = bf16_round(__uint_as_float(ug[c + 1]));
+                        const float u0 = bf16_round(__uint_as_float(uu[c]));
+                        const float u1 = bf16_round(__uint_as_float(uu[c + 1]));
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn((g0 / (1.0f + expf(-g0))) * u0,
+                                                                  (g1 / (1.0f + expf(-g1))) * u1);
+                        packed[c / 2] = *reinterpret_cast<uint32_t *>(&h2);
+                    }
+                    uint4 *op = reinterpret_cast<uint4 *>(A.out + (size_t)m * (A.N / 2) + n0 / 2 + h * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        op[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
+            }
+        } else if (ok) {
             tc::fence_after();
             float best = -INFINITY;
             int bidx = n0;
@@ -497,6 +528,7 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         A.N = N;
         A.K = K;
         A.early_w = early_w ? 1 : 0;
+        A.swiglu = 0;
         dim3 grid((M + GM - 1) / GM, N / GN, A.S);
         cudaError_t e;
         if (small) {
@@ -526,6 +558,51 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         gemm_simt_kernel<float><<<grid, 256, 0, st>>>((const float *)x, (const float *)w, (const float *)resid,
                                                        (float *)out, M, N, K);
     return cudaGetLastError();
+}
+
+bool gemm_swiglu_ok(vc_dtype dt, int F, int K, int plan)
+{
+    plan &= ~kGemmEarlyWeights;
+    return F > 0 && F % 64 == 0 && gemm_uses_tensor_cores(dt, 2 * F, K) && gemm_splits(2 * F, K, plan) == 1;
+}
+
+cudaError_t gemm_swiglu(const void *x, const void *w, void *act, vc_dtype dt, int M, int F, int K, int ldx,
+                        int32_t *status, cudaStream_t st, int plan)
+{
+    if (!gemm_swiglu_ok(dt, F, K, plan)) return cudaErrorNotSupported;
+    const bool early_w = (plan & kGemmEarlyWeights) != 0;
+    plan &= ~kGemmEarlyWeights;
+    if (M <= 0) return cudaSuccess;
+    const int N = 2 * F;
+    const bool small = plan == kGemmDecode && M <= 16;
+    CUtensorMap mx, mw;
+    if (!tma_map_bf16_3d(&mx, x, K, M, 1, (uint64_t)ldx * 2, (uint64_t)ldx * 2 * M, GK, small ? 16 : GM, 1) ||
+        !tma_map_bf16_3d(&mw, w, N, K, 1, (uint64_t)N * 2, (uint64_t)N * 2 * K, 64, GK, 1))
+        return cudaErrorInvalidValue;
+    GemmArgs A;
+    A.S = 1;
+    A.kb_per_split = K / GK;
+    A.part = nullptr;
+    A.counters = nullptr;
+    A.out = (__nv_bfloat16 *)act;
+    A.resid = nullptr;
+    A.amax_val = nullptr;
+    A.amax_idx = nullptr;
+    A.status = status;
+    A.M = M;
+    A.N = N;
+    A.K = K;
+    A.early_w = early_w ? 1 : 0;
+    A.swiglu = 1;
+    dim3 grid((M + GM - 1) / GM, N / GN, 1);
+    if (small) {
+        using Gg = GemmGeom<16, 6>;
+        cudaFuncSetAttribute(gemm_tc_kernel<16, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gg::SMEM);
+        return launch_pdl(gemm_tc_kernel<16, 6>, grid, dim3(G_THREADS), Gg::SMEM, st, mx, mw, A);
+    }
+    using Gg = GemmGeom<128, 3>;
+    cudaFuncSetAttribute(gemm_tc_kernel<128, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gg::SMEM);
+    return launch_pdl(gemm_tc_kernel<128, 3>, grid, dim3(G_THREADS), Gg::SMEM, st, mx, mw, A);
 }
 
 }  // namespace vc

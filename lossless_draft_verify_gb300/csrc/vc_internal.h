@@ -84,6 +84,13 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
 // whether the argmax epilogue is available for this shape and plan (tensor-core
 // path, and one K split or per-tile counters)
 bool gemm_argmax_ok(vc_dtype dt, int M, int N, int K, int plan, bool have_counters);
+// act [M][F] = silu(g) * u for the product x W with W [K][2F] whose columns hold
+// gate and up interleaved per 64 (columns 128 t + j: gate 64 t + j, 128 t + 64 + j:
+// up 64 t + j), g and u rounded to bf16 first: the SwiGLU epilogue of the
+// tensor-core GEMM, for bf16 products the plan leaves unsplit
+bool gemm_swiglu_ok(vc_dtype dt, int F, int K, int plan);
+cudaError_t gemm_swiglu(const void *x, const void *w, void *act, vc_dtype dt, int M, int F, int K, int ldx,
+                        int32_t *status, cudaStream_t st, int plan);
 constexpr int kGemmTileN = 128;     // columns per argmax tile
 
 // host_util.cu

@@ -187,7 +187,9 @@ def decoder_weights_packed(cfg, seed: int = 0, device="cuda", dtype=torch.bfloat
     """Weights ~ N(0, 0.02^2) (LM head x20) drawn on `device` directly in the
     layout the decoder takes: embed [vocab][d], lm_head [d][vocab] and per
     layer wqkv [d][(Hq+2Hkv) hd] (q|k|v), wo [Hq hd][d], wgu [d][2 ff]
-    (gate|up), wd [ff][d]."""
+    (gate and up columns interleaved per 64, the decoder's layout; every
+    column is an independent draw, so the layout only names which columns are
+    gate and which are up), wd [ff][d]."""
     g = _gen(seed, device)
 
     def w(i, o, s=1.0):

@@ -160,6 +160,8 @@ def load() -> ctypes.CDLL:
     L.vc_gemm_ex.argtypes = [P, P, P, P, c_int, c_int, c_int, c_int, c_int, P, c_size_t, P]
     L.vc_gemm_argmax.restype = c_int
     L.vc_gemm_argmax.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, P, P, P, c_size_t, P]
+    L.vc_gemm_swiglu.restype = c_int
+    L.vc_gemm_swiglu.argtypes = [P, P, P, c_int, c_int, c_int, c_int, c_int, P]
     L.vc_accept_tiles.restype = c_int
     L.vc_accept_tiles.argtypes = [P, P, c_int, P, c_int, c_int, P, P, P]
     L.vc_decoder_verify.restype = c_int
@@ -187,7 +189,8 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_draft_attn_h2o_workspace_bytes", "vc_draft_attn_h2o", "vc_gemm_ex", "vc_wait_probe",
             "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify",
             "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack", "vc_kv_writeback_packed",
-            "vc_verify_attn_h2o_workspace_bytes", "vc_verify_attn_h2o", "vc_decoder_set_layer_events"]
+            "vc_verify_attn_h2o_workspace_bytes", "vc_verify_attn_h2o", "vc_decoder_set_layer_events",
+            "vc_gemm_swiglu"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -473,6 +476,25 @@ def vc_gemm_argmax(x, w, tile_max, tile_idx, ws: Workspace | None = None, stream
                                  ws.nbytes if ws is not None else 0, _stream(stream)), "vc_gemm_argmax")
 
 
+def interleave_gate_up(wg: torch.Tensor, wu: torch.Tensor) -> torch.Tensor:
+    """The decoder's gate|up weight layout (include/vc.h, vc_decoder_weights):
+    [K][F] gate and up columns interleaved per 64 into [K][2F]."""
+    K, F = wg.shape
+    assert wu.shape == (K, F) and F % 64 == 0
+    return torch.stack([wg.reshape(K, F // 64, 64), wu.reshape(K, F // 64, 64)], dim=2).reshape(K, 2 * F)
+
+
+def vc_gemm_swiglu(x, w_gate_up, act, stream=None, decode_plan: bool = False):
+    """act [M][F] = silu(g) * u of the bf16-rounded gate and up products of
+    x [M][K] with w_gate_up [K][2F] (interleaved layout), in the GEMM epilogue."""
+    M, K = x.shape
+    K2, N = w_gate_up.shape
+    assert K == K2 and act.shape == (M, N // 2)
+    assert x.is_contiguous() and w_gate_up.is_contiguous() and act.is_contiguous()
+    _check(load().vc_gemm_swiglu(x.data_ptr(), w_gate_up.data_ptr(), act.data_ptr(), _dt(x), M, N // 2, K,
+                                 int(bool(decode_plan)), _stream(stream)), "vc_gemm_swiglu")
+
+
 def vc_accept_tiles(tile_max, tile_idx, drafts, n_acc, next_tok, stream=None):
     """tile_max/tile_idx: [B][D+1][n_tiles]; same outputs as vc_accept."""
     B, D1, nt = tile_max.shape
@@ -498,7 +520,7 @@ class Decoder:
         for lw in weights["layers"]:
             self.wqkv.append(torch.cat([dev(lw["wq"]), dev(lw["wk"]), dev(lw["wv"])], dim=1).contiguous())
             self.wo.append(dev(lw["wo"]))
-            self.wgu.append(torch.cat([dev(lw["wg"]), dev(lw["wu"])], dim=1).contiguous())
+            self.wgu.append(interleave_gate_up(dev(lw["wg"]), dev(lw["wu"])).contiguous())
             self.wd.append(dev(lw["wd"]))
         self._init_handle()
 

@@ -151,3 +151,44 @@ def test_accept_from_tile_maxima_matches_oracle(V):
     assert n_acc.cpu().tolist() == list(want_n) == keep
     assert nxt.cpu().tolist() == list(want_x)
     assert n2.cpu().tolist() == list(want_n) and x2.cpu().tolist() == list(want_x)
+
+
+@pytest.mark.parametrize("M,F,K,plan", [(8, 14336, 4096, True), (264, 14336, 4096, False), (8, 256, 256, False),
+                                        (33, 1024, 512, False), (1, 64, 64, False)])
+def test_gemm_swiglu_epilogue_matches_stored_product(M, F, K, plan):
+    """The SwiGLU epilogue (gate and up columns interleaved per 64) equals
+    silu(g) * u computed from the bf16 product vc_gemm stores with the same
+    plan: gate column j is stored column 128 (j // 64) + j % 64, its up column
+    64 further.  Within one bf16 ulp everywhere (exp is the host's here, the
+    device's there) and equal for almost every element."""
+    vc = lib()
+    x = inputs.normal_bf16((M, K), 21 + M, device="cuda")
+    w = inputs.normal_bf16((K, 2 * F), 22 + F, device="cuda", std=0.05)
+    assert vc.vc_gemm_splits(torch.bfloat16, 2 * F, K, plan) == 1
+    gu = f32(_run(vc, x, w, decode_plan=plan)).reshape(M, F // 64, 2, 64)
+    g = gu[:, :, 0, :].reshape(M, F).astype(np.float32)
+    u = gu[:, :, 1, :].reshape(M, F).astype(np.float32)
+    want = (g / (np.float32(1) + np.exp(-g))) * u
+    want_bf = f32(torch.from_numpy(want).to(torch.bfloat16))
+    act = torch.full((M, F), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc.vc_gemm_swiglu(x, w, act, decode_plan=plan)
+    torch.cuda.synchronize()
+    got = f32(act)
+    assert np.isfinite(got).all()
+    ulp = np.maximum(np.abs(want_bf), 2.0 ** -126) * 2.0 ** -7
+    assert (np.abs(got - want_bf) <= ulp).all(), np.abs(got - want_bf).max()
+    assert (got == want_bf).mean() > 0.99
+
+
+def test_gemm_swiglu_refuses_split_products():
+    """A gate|up product the plan splits over K is refused (the decoder then
+    stores the product and runs the separate SwiGLU pass)."""
+    vc = lib()
+    M, F, K = 40, 512, 1024
+    assert vc.vc_gemm_splits(torch.bfloat16, 2 * F, K, True) > 1
+    x = inputs.normal_bf16((M, K), 31, device="cuda")
+    w = inputs.normal_bf16((K, 2 * F), 32, device="cuda", std=0.05)
+    act = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_gemm_swiglu(x, w, act, decode_plan=True)
+    assert e.value.status == vc.VC_ERR_UNSUPPORTED
