@@ -65,26 +65,37 @@ def dist_env():
 
 
 # DRAM bytes (read + write) of one draft launch at the 32768-token context,
-# from one ncu capture of the draft kernel, keyed by the SHA-256 of the
-# sources it was built from: a changed kernel reports traffic null until it is
-# captured again.
+# from one ncu capture of the draft kernel, keyed by the code digest (SHA-256
+# without comments or blank lines) of the sources it was built from: a changed
+# kernel reports traffic null until it is captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("e673bffc0e74b782ea09ef60de89e932136f4ebb217a53156555d484c307b50a",
-               "7f0d10f52269831e89674cc5efb2a594696ee3ebaae36acf379853a23e3f594a"),
+    "sha256": ("9a7f1836708520b79c496dfc00c3f3f972c6da53058e457723f87f898aa21ac4",
+               "b510bbe2c0a3fd00dc0834096e12cd05dbcccf7f60c5931ba04e9be74c8ea859"),
     "bytes": 411.130624e6 + 4.275968e6,
     "algorithmic_bytes": 409731072,
 }
 
 
+def code_digest(path: str) -> str:
+    """SHA-256 of a C++/CUDA source with its comments and blank lines removed,
+    so that an edit to comments alone does not count as a changed kernel."""
+    import hashlib
+    import re
+    with open(path) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    lines = [ln.rstrip() for ln in src.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def captured_traffic(table: dict, per_launch_bytes: float):
     """Captured DRAM traffic scaled to a launch of `per_launch_bytes`
-    algorithmic bytes, or None when the kernel's sources changed."""
-    import hashlib
+    algorithmic bytes, or None when the kernel's code changed."""
     for rel, want in zip(table["sources"], table["sha256"]):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != want:
-                return None
+        if code_digest(os.path.join(ROOT, rel)) != want:
+            return None
     return table["bytes"] * per_launch_bytes / table["algorithmic_bytes"]
 
 

@@ -15,9 +15,12 @@
 // masked bits are an fp16 subnormal code * 2^(b e) * 2^-24, the slot factor
 // 2^(b e) being fixed per channel by the record layout and cancelled in q (K)
 // or per output row (V).  Online softmax in the exp2 domain with lazy
-// rescaling.  The residual (full-precision ring) is one extra split handled
-// with fp32 CUDA-core math.  The last CTA of each kv unit (device-scope counter
-// in the workspace, returned to zero after use) merges the split partials.
+// rescaling.  The residual window (the most recent tokens, full precision):
+// a bf16 window is cut into 16-token tiles that run on bf16 MMAs inside the
+// quantized splits, continuing the warps' softmax state; an fp32 window is
+// one or more extra splits of fp32 CUDA-core math.  The last CTA of each kv
+// unit (device-scope counter in the workspace, returned to zero after use)
+// merges the split partials.
 //
 // Dense cache kernels (compacted dropped cache, or an uncompressed cache):
 // bf16 caches use the same MMA structure with the K/V tiles as operands
