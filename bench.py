@@ -277,13 +277,10 @@ class Round:
             # this round's inputs arrive from pinned host memory, on the link's
             # stream ahead of the swap (once the previous step has read them)
             self.side.wait_event(self.ev_acc)
-            with torch.cuda.stream(self.side):
-                self.q_draft.copy_(self.h_q_draft, non_blocking=True)
-                self.k_step.copy_(self.h_k_step, non_blocking=True)
-                self.v_step.copy_(self.h_v_step, non_blocking=True)
-                self.q_ver.copy_(self.h_q_ver, non_blocking=True)
-                self.logits.copy_(self.h_logits, non_blocking=True)
-                self.drafts.copy_(self.h_drafts, non_blocking=True)
+            for dst, src in ((self.q_draft, self.h_q_draft), (self.k_step, self.h_k_step),
+                             (self.v_step, self.h_v_step), (self.q_ver, self.h_q_ver),
+                             (self.logits, self.h_logits), (self.drafts, self.h_drafts)):
+                vc.vc_swap_in(dst, src, stream=self.side)      # pinned host -> device through the C ABI
             self.ev_in.record(self.side)
             main.wait_event(self.ev_in)
         # swap-in of the full cache on the side stream, overlapped with drafting;
