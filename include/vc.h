@@ -586,7 +586,9 @@ int vc_decoder_trace_count(const vc_decoder *dec);
  * stream after layer l's copy (and expansion) is enqueued, before it enqueues
  * the forward; an event never recorded is no wait.  The handles are copied
  * (the caller owns the events and keeps them alive while set); n = 0 clears
- * them.  Not for calls enqueued while their stream is being captured.
+ * them.  Like tracing, this mutates the decoder object: a change of the
+ * events must not race with another host thread's call on the same
+ * vc_decoder.  Not for calls enqueued while their stream is being captured.
  * Errors: VC_ERR_INVALID for dec NULL, n < 0, or n > 0 with events NULL, a
  * NULL handle or n != n_layers.
  */
