@@ -210,6 +210,9 @@ class Round:
             # verify, which follows its expansion
             self.unpack_stream = torch.cuda.Stream(device=dev)
             self.ev_copied = [torch.cuda.Event() for _ in range(stagger)]
+            # the expansion runs after the draft steps (its HBM traffic would
+            # slow them); the copies still overlap them
+            self.ev_drafted = torch.cuda.Event()
         # compressed draft cache of the context
         maxg = (CTX + DQ) // GROUP + 1
         self.cache = vc.QCache(B, HKV, D_HEAD, bits, maxg, residual + GROUP + DQ + 32, residual)
@@ -298,16 +301,11 @@ class Round:
                 vc.vc_swap_in(self.kpack[b0:b1], self.kpack_host[b0:b1], stream=self.side)
                 vc.vc_swap_in(self.vpack[b0:b1], self.vpack_host[b0:b1], stream=self.side,
                               done_event=self.ev_copied[p])
-                self.unpack_stream.wait_event(self.ev_copied[p])
-                vc.vc_kv_unpack(self.kpack[b0:b1], self.kfull[b0:b1], stream=self.unpack_stream)
-                vc.vc_kv_unpack(self.vpack[b0:b1], self.vfull[b0:b1], stream=self.unpack_stream)
-                self.ev_swap[p].record(self.unpack_stream)
             else:
                 vc.vc_swap_in(self.kfull[b0:b1], self.kfull_host[b0:b1], stream=self.side)
                 vc.vc_swap_in(self.vfull[b0:b1], self.vfull_host[b0:b1], stream=self.side, done_event=self.ev_swap[p])
-        if ev is not None:
-            # the swap ends with the last expansion when the cache travels packed
-            ev["swap1"].record(self.unpack_stream if self.packed else self.side)
+        if ev is not None and (not self.packed or self.link_gbps):
+            ev["swap1"].record(self.side)
         for j in range(self.D):
             vc.vc_qcache_append(self.cache, self.k_step[j], self.v_step[j], self.ones, requantize=False)
             if ev is not None:
@@ -315,6 +313,17 @@ class Round:
             vc.vc_draft_attn(self.q_draft[j], self.view, self.scale, self.o_draft[j], self.ws_d)
             if ev is not None:
                 ev["d1"][j].record(main)
+        if self.packed and not self.link_gbps:
+            # expansion of each part once it has landed and the draft steps have run
+            self.ev_drafted.record(main)
+            self.unpack_stream.wait_event(self.ev_drafted)
+            for p, (b0, b1) in enumerate(self.parts):
+                self.unpack_stream.wait_event(self.ev_copied[p])
+                vc.vc_kv_unpack(self.kpack[b0:b1], self.kfull[b0:b1], stream=self.unpack_stream)
+                vc.vc_kv_unpack(self.vpack[b0:b1], self.vfull[b0:b1], stream=self.unpack_stream)
+                self.ev_swap[p].record(self.unpack_stream)
+            if ev is not None:
+                ev["swap1"].record(self.unpack_stream)
         for p, (b0, b1) in enumerate(self.parts):
             main.wait_event(self.ev_swap[p])
             if ev is not None:
