@@ -840,6 +840,7 @@ def run_model(args, dev, rank, world, barrier, pg):
     clocks.start()
     time.sleep(0.3)
     torch.cuda.synchronize()
+    swap_log0 = len(run.swap_rows)
     barrier()
     wall0 = time.perf_counter()
     t0.record()
@@ -866,6 +867,7 @@ def run_model(args, dev, rank, world, barrier, pg):
     barrier()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
+    swap_rows = statistics.mean(run.swap_rows[swap_log0:swap_log0 + args.steps])
     n_acc = log.n_acc[base0:base0 + args.steps].cpu()
     tokens = int((n_acc.long() + 1).sum())
     value, ms_max = replicas.whole_job_rate(tokens, ms, pg, device=dev)
@@ -992,8 +994,9 @@ def run_model(args, dev, rank, world, barrier, pg):
             "staggered": stag,
             "phases_ms": {"draft_32_steps": d_ms, "verify_forward": v_ms, "accept_commit_writeback": c_ms,
                           "swap_in": s_ms},
-            "swap": {"bytes": run_bytes(cfg, max_len, packed),
-                     "GB/s": run_bytes(cfg, max_len, packed) / (s_ms / 1e3) / 1e9,
+            "swap": {"bytes": run_bytes(cfg, swap_rows, packed),
+                     "rows_per_sequence_and_head": swap_rows,
+                     "GB/s": run_bytes(cfg, swap_rows, packed) / (s_ms / 1e3) / 1e9,
                      "format": "packed rows (lossless, 208 of 256 bytes)" if packed else "bf16",
                      "hidden_frac": hidden,
                      "hidden_frac_how": "per round, the part of the swap interval inside the drafting interval "
@@ -1003,7 +1006,7 @@ def run_model(args, dev, rank, world, barrier, pg):
             "accepted_per_round_mean": float(n_acc.float().mean()), "tokens_per_round": tokens / args.steps,
             "prefill_s": round(t_pf, 2), "status": st,
             "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc, packed) * args.steps,
-            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, max_len, packed),
+            "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, swap_rows, packed),
                     "d2h_bytes_per_step": d2h + model_writeback_bytes(cfg, n_acc, packed),
                     "how": "host wall clock over the same K rounds as value (which uses device events around "
                            "them); each round's tokens are copied to pinned host memory and read by the host while "
@@ -1163,11 +1166,11 @@ def model_launches_per_round(cfg, vc, packed: bool = False) -> int:
     return M_HORIZON * draft + verify + cfg.n_layers + 1 + (2 * cfg.n_layers if packed else 0)
 
 
-def run_bytes(cfg, max_len, packed: bool = False) -> int:
-    """Bytes of one full-cache swap-in (K and V, every layer, the whole ring of
-    positions the runner allocates), bf16 or packed rows."""
+def run_bytes(cfg, rows: float, packed: bool = False) -> float:
+    """Bytes of one full-cache swap-in of `rows` rows per (sequence, kv head)
+    (K and V, every layer), bf16 or packed rows."""
     row = 16 + 3 * cfg.head_dim // 2 if packed else cfg.head_dim * 2
-    return 2 * cfg.n_layers * M_B * cfg.n_kv_heads * (max_len + M_HORIZON + 1) * row
+    return 2 * cfg.n_layers * M_B * cfg.n_kv_heads * rows * row
 
 
 def full_kv_step_ms(rnd, steps: int, warmup: int) -> float:

@@ -439,6 +439,19 @@ vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes,
                      cudaStream_t side_stream, cudaEvent_t done);
 
 /*
+ * vc_swap_in_rows -- vc_swap_in of the used prefix of a blocked cache: src and
+ * dst hold `blocks` blocks of `pitch_rows` rows of `row_bytes` bytes each
+ * ([blocks][pitch_rows][row_bytes], e.g. one layer's [B][Hkv][L_stride] rows);
+ * the first `rows` rows of every block are copied by one 2-D asynchronous copy
+ * on `side_stream` (a cache whose sequences hold at most `rows` tokens needs
+ * nothing past them), then `done` is recorded as for vc_swap_in.  Returns
+ * VC_ERR_INVALID if rows > pitch_rows, or if src is not page-locked host
+ * memory or dst not device memory at the first and the last byte copied.
+ */
+vc_status vc_swap_in_rows(void *dst_dev, const void *src_pinned_host, size_t row_bytes, size_t rows,
+                          size_t pitch_rows, size_t blocks, cudaStream_t side_stream, cudaEvent_t done);
+
+/*
  * vc_swap_in_paced -- vc_swap_in as if the source produced data at `gbps`
  * (GB/s): the emulation of a full cache held by a slower store, e.g. a remote
  * prefix cache behind a network (paper page, "Key results": remote prefix

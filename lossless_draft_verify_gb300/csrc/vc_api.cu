@@ -378,4 +378,24 @@ vc_status vc_swap_in(void *dst_dev, const void *src_pinned_host, size_t bytes, c
     return VC_OK;
 }
 
+vc_status vc_swap_in_rows(void *dst_dev, const void *src_pinned_host, size_t row_bytes, size_t rows,
+                          size_t pitch_rows, size_t blocks, cudaStream_t side_stream, cudaEvent_t done)
+{
+    if (!dst_dev || !src_pinned_host || rows > pitch_rows) return VC_ERR_INVALID;
+    if (row_bytes && blocks && pitch_rows && rows) {
+        const size_t pitch = row_bytes * pitch_rows, width = row_bytes * rows;
+        const size_t last = (blocks - 1) * pitch + width - 1;       // the last byte copied
+        if (!is_memory_type(src_pinned_host, cudaMemoryTypeHost) ||
+            !is_memory_type((const uint8_t *)src_pinned_host + last, cudaMemoryTypeHost) ||
+            !is_memory_type(dst_dev, cudaMemoryTypeDevice) ||
+            !is_memory_type((const uint8_t *)dst_dev + last, cudaMemoryTypeDevice))
+            return VC_ERR_INVALID;                                 // pageable, or the range leaves the allocation
+        cudaError_t e = cudaMemcpy2DAsync(dst_dev, pitch, src_pinned_host, pitch, width, blocks,
+                                          cudaMemcpyHostToDevice, side_stream);
+        if (e != cudaSuccess) return VC_ERR_CUDA;
+    }
+    if (done && cudaEventRecord(done, side_stream) != cudaSuccess) return VC_ERR_CUDA;
+    return VC_OK;
+}
+
 }  // extern "C"

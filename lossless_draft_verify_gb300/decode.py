@@ -130,6 +130,7 @@ class VeriCacheRunner:
         # draft steps instead of while they run
         self.expand_after_draft = True
         self.ev_drafted = torch.cuda.Event()
+        self.swap_rows: list[int] = []    # rows per (sequence, head) each swap copied
 
     # ------------------------------------------------------------ prefill --
     def prefill(self, prompt: torch.Tensor):
@@ -250,20 +251,26 @@ class VeriCacheRunner:
         return top[..., 0] - top[..., 1]
 
     def _swap_copies(self, ev: dict | None = None):
-        """The link part of the swap: the host copy of the full cache into the
-        device, layer by layer on the side stream (packed rows into the
+        """The link part of the swap: the host copy of the full cache (the rows
+        that can hold tokens) into the device, layer by layer on the side stream (packed rows into the
         staging buffer, each layer marked by ev_layer[l]; bf16 rows straight
         into the cache, each layer marked by ev_ready[l]).  ev["swap0"] and
         ev["swap1"] bracket the transfer."""
         if ev is not None:
             ev["swap0"].record(self.side)
+        # every sequence holds at most ctx_bound tokens, and a forward writes its
+        # own rows before reading them: the rows past the bound stay behind
+        rows = min(self.ctx_bound, self.L_stride)
+        self.swap_rows.append(rows)
         for l in range(len(self.qc)):
             if self.pack_host:
-                vc.vc_swap_in(self.k_pack[l], self.k_host[l], stream=self.side)
-                vc.vc_swap_in(self.v_pack[l], self.v_host[l], stream=self.side, done_event=self.ev_layer[l])
+                vc.vc_swap_in_rows(self.k_pack[l], self.k_host[l], rows, stream=self.side)
+                vc.vc_swap_in_rows(self.v_pack[l], self.v_host[l], rows, stream=self.side,
+                                   done_event=self.ev_layer[l])
             else:
-                vc.vc_swap_in(self.k_full[l], self.k_host[l], stream=self.side)
-                vc.vc_swap_in(self.v_full[l], self.v_host[l], stream=self.side, done_event=self.ev_ready[l])
+                vc.vc_swap_in_rows(self.k_full[l], self.k_host[l], rows, stream=self.side)
+                vc.vc_swap_in_rows(self.v_full[l], self.v_host[l], rows, stream=self.side,
+                                   done_event=self.ev_ready[l])
         if ev is not None:
             ev["swap1"].record(self.side)
         if not self.pack_host:

@@ -161,6 +161,8 @@ def load() -> ctypes.CDLL:
     L.vc_gemm_argmax.restype = c_int
     L.vc_gemm_argmax.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, P, P, P, c_size_t, P]
     L.vc_gemm_swiglu.restype = c_int
+    L.vc_swap_in_rows.restype = c_int
+    L.vc_swap_in_rows.argtypes = [P, P, c_size_t, c_size_t, c_size_t, c_size_t, P, P]
     L.vc_gemm_swiglu.argtypes = [P, P, P, c_int, c_int, c_int, c_int, c_int, P]
     L.vc_accept_tiles.restype = c_int
     L.vc_accept_tiles.argtypes = [P, P, c_int, P, c_int, c_int, P, P, P]
@@ -190,7 +192,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify",
             "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack", "vc_kv_writeback_packed",
             "vc_verify_attn_h2o_workspace_bytes", "vc_verify_attn_h2o", "vc_decoder_set_layer_events",
-            "vc_gemm_swiglu"]
+            "vc_gemm_swiglu", "vc_swap_in_rows"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -441,6 +443,24 @@ def vc_swap_in(dst: torch.Tensor, src_pinned: torch.Tensor, nbytes: int | None =
             done_event.record(torch.cuda.current_stream() if stream is None else stream)
         ev = done_event.cuda_event
     _check(load().vc_swap_in(dst.data_ptr(), src_pinned.data_ptr(), n, _stream(stream), ev), "vc_swap_in")
+
+
+def vc_swap_in_rows(dst: torch.Tensor, src_pinned: torch.Tensor, rows: int, stream=None,
+                    done_event: torch.cuda.Event | None = None):
+    """The first `rows` rows of every block of a [..][pitch_rows][row] tensor
+    pair (the last two dimensions are rows and the row's elements): one 2-D
+    copy from pinned host memory (include/vc.h, vc_swap_in_rows)."""
+    assert dst.shape == src_pinned.shape and dst.is_contiguous() and src_pinned.is_contiguous()
+    pitch_rows = dst.shape[-2]
+    row_bytes = dst.shape[-1] * dst.element_size()
+    blocks = dst.numel() // (dst.shape[-1] * pitch_rows)
+    ev = None
+    if done_event is not None:
+        if not done_event.cuda_event:          # torch creates the event lazily
+            done_event.record(torch.cuda.current_stream() if stream is None else stream)
+        ev = done_event.cuda_event
+    _check(load().vc_swap_in_rows(dst.data_ptr(), src_pinned.data_ptr(), row_bytes, min(int(rows), pitch_rows),
+                                  pitch_rows, blocks, _stream(stream), ev), "vc_swap_in_rows")
 
 
 # ---------------------------------------------------------------- decoder --

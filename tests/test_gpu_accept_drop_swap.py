@@ -166,6 +166,27 @@ def test_swap_in_pinned_and_rejects_pageable():
     assert e.value.status == vc.VC_ERR_INVALID
 
 
+@pytest.mark.parametrize("rows", [0, 1, 37, 100])
+def test_swap_in_rows_copies_the_prefix_of_every_block(rows):
+    """vc_swap_in_rows: the first `rows` rows of every [pitch_rows][row] block
+    arrive exactly; the device rows past them keep their old contents."""
+    vc = lib()
+    blocks, pitch, width = 6, 100, 208
+    src = torch.randint(0, 256, (2, 3, pitch, width), dtype=torch.uint8).pin_memory()
+    dst = torch.full((2, 3, pitch, width), 7, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    vc.vc_swap_in_rows(dst, src, rows, stream=side, done_event=ev)
+    torch.cuda.current_stream().wait_event(ev)
+    got = dst.cpu().reshape(blocks, pitch, width)
+    want = src.reshape(blocks, pitch, width)
+    assert torch.equal(got[:, :rows], want[:, :rows])
+    assert bool((got[:, rows:] == 7).all())
+    with pytest.raises(vc.VcError) as e:       # a pageable source is refused
+        vc.vc_swap_in_rows(dst, torch.zeros_like(src).contiguous(), max(rows, 1), stream=side)
+    assert e.value.status == vc.VC_ERR_INVALID
+
+
 def test_paced_swap_in_keeps_its_rate_and_data():
     """vc_swap_in_paced: the bytes arrive intact and no faster than the
     emulated source rate (256 MiB at 25 GB/s: at least ~10.7 ms)."""
