@@ -292,3 +292,72 @@ def test_programmatic_launch_changes_no_result(graph):
     serialized = json.loads(out.stdout.strip().splitlines()[-1])
     assert os.environ.get("VC_PDL", "1") != "0"
     assert _launch_order_probe(graph) == serialized
+
+
+def test_config5_model_spot_check_against_oracle():
+    """The 8-layer bf16 decoder of the end-to-end workload (d_model 4096,
+    32/8 heads, SwiGLU 14336, vocab 32000) against the fp64 oracle on the same
+    weights: a 32-token prompt, then 8 greedy tokens (full-KV decoding, the
+    losslessness reference of the model workload).  The oracle runs row by
+    row, so each (row, layer) streams about 1.7 GB of fp64 weights; 39 rows
+    take about a minute and a half, where a 2048-token prompt would take over
+    an hour.  The GPU computes in bf16 (weights exact, activations rounded
+    between kernels), so the prompt's last-row logits must agree within 5% of
+    their largest magnitude (rms error within 1%), and the tokens must agree
+    while the oracle's top-2 margin exceeds six times the rms logit error (a
+    margin is the difference of two logits, each off by about the rms error);
+    at the first position where it does not, the two sequences may part and
+    the comparison stops there."""
+    from lossless_draft_verify_gb300 import decode
+    from oracle import model as om
+    vc = lib()
+    cfg = inputs.DecoderConfig()
+    P, n_new = 32, 8
+    W = inputs.decoder_weights_packed(cfg, seed=0, device="cuda")
+    dec = vc.Decoder.from_packed(cfg, W["embed"], W["lm_head"], W["wqkv"], W["wo"], W["wgu"], W["wd"])
+    prompt = inputs.random_prompts(1, P, cfg.vocab, seed=5, device="cuda")
+    run = decode.VeriCacheRunner(dec, 1, P + n_new + 64, 8, bits=2, residual=0, prefill_chunk=64)
+    run.prefill(prompt)
+    torch.cuda.synchronize()
+    gpu_logits = run.last_logits.float().cpu().numpy()[0]
+    gpu_tokens = run.greedy(n_new)[0]
+    torch.cuda.synchronize()
+    # the oracle's weights: the same bf16 values, widened exactly to fp64
+    qd, kvd, F, D = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.d_ff, cfg.d_model
+    layers = []
+    for l in range(cfg.n_layers):
+        wqkv = W["wqkv"][l].double().cpu()
+        gu = W["wgu"][l].double().cpu().reshape(D, F // 64, 2, 64)      # gate and up interleaved per 64
+        layers.append({"wq": wqkv[:, :qd].numpy(), "wk": wqkv[:, qd:qd + kvd].numpy(),
+                       "wv": wqkv[:, qd + kvd:].numpy(), "wo": W["wo"][l].double().cpu().numpy(),
+                       "wg": gu[:, :, 0].reshape(D, F).numpy(), "wu": gu[:, :, 1].reshape(D, F).numpy(),
+                       "wd": W["wd"][l].double().cpu().numpy()})
+    weights = {"embed": W["embed"].double().cpu().numpy(), "lm_head": W["lm_head"].double().cpu().numpy(),
+               "layers": layers}
+    del W, dec, run
+    torch.cuda.empty_cache()
+    model = om.TinyDecoder(weights, cfg)
+    cache = om.FullKV(model)
+    lg, _ = om.forward_block(model, cache, [int(t) for t in prompt[0].tolist()], 0)
+    want_logits = lg[-1]
+    err = np.abs(gpu_logits - want_logits).max()
+    rms = float(np.sqrt(np.mean((gpu_logits - want_logits) ** 2)))
+    top = np.abs(want_logits).max()
+    assert err <= 5e-2 * top and rms <= 1e-2 * top, (err, rms, top)
+    want_tokens = [om.argmax_lowest(want_logits)]
+    margins = [om._margin(want_logits)]
+    while len(want_tokens) < n_new:
+        lg, _ = om.forward_block(model, cache, [want_tokens[-1]], cache.length())
+        want_tokens.append(om.argmax_lowest(lg[-1]))
+        margins.append(om._margin(lg[-1]))
+    compared = 0
+    for t in range(n_new):
+        if margins[t] <= 6 * rms:
+            break                                   # a near tie at bf16 precision: the sequences may part
+        assert gpu_tokens[t] == want_tokens[t], (t, gpu_tokens[t], want_tokens[t], margins[t], rms)
+        compared += 1
+        if gpu_tokens[t] != want_tokens[t]:
+            break
+    print(f"config-5 spot check: logit error max {err:.3e} rms {rms:.3e} of max {top:.2f}; "
+          f"tokens compared {compared} of {n_new}; oracle margins {[round(m, 3) for m in margins]}")
+    assert compared >= 1
