@@ -40,8 +40,8 @@ struct vc_decoder {
 namespace vc {
 namespace {
 
-// Verify attention inside the decoder uses key splits of a fixed 2048 keys.
-constexpr int kSplitTiles = 32;
+// Verify attention inside the decoder uses key splits of a fixed 4096 keys.
+constexpr int kSplitTiles = 64;
 constexpr int kRowThreads = 256;
 constexpr int kBadToken = 1 << 1;       // status bit: a token id outside [0, vocab)
 constexpr int kBadPosition = 1 << 2;    // status bit: a position outside the cache
