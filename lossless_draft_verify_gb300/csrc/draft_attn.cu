@@ -51,6 +51,8 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 
 // partial record per (unit, split): m[4], l[4], o[4][D] (fp32, unnormalized)
 __host__ __device__ constexpr int part_floats(int D) { return 8 + 4 * D; }
+// the CTA merge's shared buffer: every warp's (m, l, o), then the warps' weights and the maxima
+__host__ __device__ constexpr int merge_floats(int D) { return NW * part_floats(D) + NW * 4 + 4; }
 
 // ---------------------------------------------------------------- PTX ----
 __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
@@ -195,6 +197,21 @@ struct KiviParams {
 template <typename TQ, int D>
 __device__ __forceinline__ float load_q(const TQ *q, int idx) { return Elem<TQ>::to_f(q[idx]); }
 
+// q[idx], q[idx + 1] for even idx, one load when the pair is aligned
+template <typename TQ, int D>
+__device__ __forceinline__ float2 load_q2(const TQ *q, int idx, bool pairs)
+{
+    if (pairs) {
+        if constexpr (std::is_same<TQ, float>::value) {
+            return *reinterpret_cast<const float2 *>(q + idx);
+        } else {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(q + idx);
+            return make_float2(bf16_lo(w), bf16_hi(w));
+        }
+    }
+    return make_float2(load_q<TQ, D>(q, idx), load_q<TQ, D>(q, idx + 1));
+}
+
 // Merge the NW warps' (m, l, o) of this CTA in shared memory and store the
 // CTA partial.  Every warp has written wm[w][h], wl[w][h], wo[w][h][c].
 template <int D>
@@ -204,20 +221,27 @@ __device__ void cta_merge_store(float *wbuf, float *dst, int grp)
     float *wm = wbuf;                       // [NW][4]
     float *wl = wbuf + NW * 4;              // [NW][4]
     float *wo = wbuf + NW * 8;              // [NW][4][D]
-    for (int i = threadIdx.x; i < 4 * D; i += kThreads) {
-        const int h = i / D;
+    float *ww = wo + NW * 4 * D;            // [NW][4] weights 2^(m_w - M), then [4] M
+    if (threadIdx.x < NW * 4) {
+        const int h = threadIdx.x & 3;
         float M = kNegBig;
         for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w * 4 + h]);
+        ww[threadIdx.x] = exp2f(wm[threadIdx.x] - M);
+        if (threadIdx.x < 4) ww[NW * 4 + h] = M;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * D; i += kThreads) {
+        const int h = i / D;
         float o = 0.f;
-        for (int w = 0; w < NW; ++w) o += wo[(w * 4 + h) * D + (i % D)] * exp2f(wm[w * 4 + h] - M);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) o += wo[(w * 4 + h) * D + (i % D)] * ww[w * 4 + h];
         dst[8 + i] = h < grp ? o : 0.f;
     }
     if (threadIdx.x < 4) {
         const int h = threadIdx.x;
-        float M = kNegBig, L = 0.f;
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w * 4 + h]);
-        for (int w = 0; w < NW; ++w) L += wl[w * 4 + h] * exp2f(wm[w * 4 + h] - M);
-        dst[h] = M;
+        float L = 0.f;
+        for (int w = 0; w < NW; ++w) L += wl[w * 4 + h] * ww[w * 4 + h];
+        dst[h] = ww[NW * 4 + h];
         dst[4 + h] = h < grp ? L : 0.f;
     }
 }
@@ -234,23 +258,31 @@ __device__ void last_cta_combine(const float *unit_part, int n_split, unsigned i
                                  TO *out, float *ml_out = nullptr)
 {
     __shared__ bool is_last;
-    __shared__ float wgt[4][kMaxSplit];
+    __shared__ float wgt[4][kMaxSplit];      // the splits' m, then their weights
+    __shared__ float lsp[4][kMaxSplit];      // the splits' l
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == (unsigned int)(n_split - 1);
     __syncthreads();
     if (!is_last) return;
     __threadfence();
+    // every split's (m, l) in one round of independent loads
+    for (int i = threadIdx.x; i < 4 * n_split; i += kThreads) {
+        const int s = i >> 2, h = i & 3;
+        const float *q = unit_part + (size_t)s * part_floats(D);
+        wgt[h][s] = __ldcg(q + h);
+        lsp[h][s] = __ldcg(q + 4 + h);
+    }
+    __syncthreads();
     if (threadIdx.x < 4) {
         const int h = threadIdx.x;
         float M = kNegBig;
-        for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldcg(unit_part + (size_t)s * part_floats(D) + h));
+        for (int s = 0; s < n_split; ++s) M = fmaxf(M, wgt[h][s]);
         float L = 0.f;
         for (int s = 0; s < n_split; ++s) {
-            const float *q = unit_part + (size_t)s * part_floats(D);
-            const float w = exp2f(__ldcg(q + h) - M);
+            const float w = exp2f(wgt[h][s] - M);
             wgt[h][s] = w;
-            L += __ldcg(q + 4 + h) * w;
+            L += lsp[h][s] * w;
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
         for (int s = 0; s < n_split; ++s) wgt[h][s] *= inv;
@@ -260,13 +292,25 @@ __device__ void last_cta_combine(const float *unit_part, int n_split, unsigned i
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < grp * D; i += kThreads) {
+    // four consecutive channels per thread (the split rows are 16-byte aligned)
+    static_assert(part_floats(D) % 4 == 0 && D % 4 == 0, "float4 partial rows");
+    for (int i = 4 * threadIdx.x; i < grp * D; i += 4 * kThreads) {
         const int h = i / D, c = i % D;
         const float *q = unit_part + 8 + h * D + c;
-        float O = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-        for (int s = 0; s < n_split; ++s) O = fmaf(__ldcg(q + (size_t)s * part_floats(D)), wgt[h][s], O);
-        out[h * D + c] = Elem<TO>::from_f(O);
+        for (int s = 0; s < n_split; ++s) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(q + (size_t)s * part_floats(D)));
+            const float w = wgt[h][s];
+            O.x = fmaf(x.x, w, O.x);
+            O.y = fmaf(x.y, w, O.y);
+            O.z = fmaf(x.z, w, O.z);
+            O.w = fmaf(x.w, w, O.w);
+        }
+        out[h * D + c] = Elem<TO>::from_f(O.x);
+        out[h * D + c + 1] = Elem<TO>::from_f(O.y);
+        out[h * D + c + 2] = Elem<TO>::from_f(O.z);
+        out[h * D + c + 3] = Elem<TO>::from_f(O.w);
     }
     if (threadIdx.x == 0) *counter = 0u;
 }
@@ -572,32 +616,49 @@ draft_kivi_kernel(KiviParams P)
             mbar_arrive_expect_tx(&mybar[s], bytes);
             bulk_g2s(myring + s * STAGE, rec_base + (size_t)g * REC, bytes, &mybar[s]);
         };
-        // each warp's first records are requested before anything else, so the
-        // memory latency overlaps the q setup below
+        // q first, as (c, c + 1) pairs (one 32-bit bf16 or 64-bit fp32 load
+        // each when the unit's q rows are aligned for it): every warp's first
+        // record copies, requested next, fill the memory system for a few
+        // microseconds, and loads issued after them wait behind that traffic
+        const int hq = gid & 3;
+        const bool qvalid = hq < grp;
+        const bool q_pairs = (reinterpret_cast<uintptr_t>(qg) & (2 * sizeof(TQ) - 1)) == 0;
+        float2 qq[KS][2];
+        if constexpr (!ROT) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr)
+                    qq[ks][rr] = qvalid ? load_q2<TQ, D>(qg, hq * D + 16 * ks + 2 * tig + 8 * rr, q_pairs)
+                                        : make_float2(0.f, 0.f);
+        }
         if (lane == 0) {
             for (int s = 0; s < NST; ++s) mbar_init(&mybar[s], 1);
             fence_mbar_init();
             for (int s = 0; s < NST && s < n_mine; ++s) issue(s, s);
         }
-        // B fragments of q (column n = gid): heads 0..3 scaled by 2^(-b e) for
-        // the channel's code exponent, copies 4..7 unscaled (zero-point sums)
-        if constexpr (ROT) rotate_queries<TQ, D>(qg, grp, rq);
-        auto qval = [&](int idx) { return ROT ? rq[idx] : load_q<TQ, D>(qg, idx); };
-        uint32_t qf[KS][2];
-        {
-            const int h = gid & 3;
-            const bool valid = h < grp;
+        if constexpr (ROT) {
+            rotate_queries<TQ, D>(qg, grp, rq);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
-                    const int c = 16 * ks + 2 * tig + 8 * rr;
-                    const float f = gid < 4 ? exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * ks + rr))) : 1.f;
-                    const float a = valid ? qval(h * D + c) * P.qscale * f : 0.f;
-                    const float bb = valid ? qval(h * D + c + 1) * P.qscale * f : 0.f;
-                    qf[ks][rr] = pack_half2(a, bb);
+                    const int c = hq * D + 16 * ks + 2 * tig + 8 * rr;
+                    qq[ks][rr] = qvalid ? make_float2(rq[c], rq[c + 1]) : make_float2(0.f, 0.f);
                 }
         }
+        // B fragments of q (column n = gid): heads 0..3 scaled by 2^(-b e) for
+        // the channel's code exponent, copies 4..7 unscaled (zero-point sums)
+        uint32_t qf[KS][2];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const float f = gid < 4 ? exp2f(-(float)(BITS * Pairs<BITS, D>::exp_of(2 * ks + rr))) : 1.f;
+                const float a = qvalid ? qq[ks][rr].x * P.qscale * f : 0.f;
+                const float bb = qvalid ? qq[ks][rr].y * P.qscale * f : 0.f;
+                qf[ks][rr] = pack_half2(a, bb);
+            }
         __syncthreads();                                  // ones / zeros written
 
         float m_run[2] = {kNegBig, kNegBig}, l_run[2] = {0.f, 0.f};
@@ -1454,7 +1515,7 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     P.qscale = scale * kLog2e;
     const size_t rot_bytes = ROT ? 16 * D : 0;
     size_t smem = 128 + 6 * D + rot_bytes + (size_t)NW * Gm::NST * 2 * Gm::REC;
-    const size_t merge = 128 + 6 * D + rot_bytes + (size_t)NW * part_floats(D) * 4;
+    const size_t merge = 128 + 6 * D + rot_bytes + (size_t)merge_floats(D) * 4;
     if (smem < merge) smem = merge;
     auto kern = draft_kivi_kernel<BITS, D, TQ, TR, ROT>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1489,7 +1550,7 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
     if constexpr (sizeof(T) == 2) {
         using Gm = DmGeom<D>;
         size_t smem = Gm::SMEM;
-        const size_t merge = 128 + (size_t)NW * part_floats(D) * 4;
+        const size_t merge = 128 + (size_t)merge_floats(D) * 4;
         if (smem < merge) smem = merge;
         auto kern = draft_dense_mma_kernel<D>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1499,7 +1560,7 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
     constexpr int PER = 16 / sizeof(T);
     const size_t qbytes = (size_t)(D / PER) * (4 * PER + 4) * 4;
     size_t smem = 128 + qbytes + (size_t)NW * DENSE_NST * 2 * G * D * sizeof(T);
-    const size_t merge = 128 + qbytes + (size_t)NW * part_floats(D) * 4;
+    const size_t merge = 128 + qbytes + (size_t)merge_floats(D) * 4;
     if (smem < merge) smem = merge;
     auto kern = draft_dense_kernel<T, D>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
