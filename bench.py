@@ -70,9 +70,9 @@ def dist_env():
 # kernel reports traffic null until it is captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("9a7f1836708520b79c496dfc00c3f3f972c6da53058e457723f87f898aa21ac4",
+    "sha256": ("27d917349fc87023672562faddf09a0fe0d9847f37c603dae611698bc466d9d5",
                "b510bbe2c0a3fd00dc0834096e12cd05dbcccf7f60c5931ba04e9be74c8ea859"),
-    "bytes": 411.130624e6 + 4.275968e6,
+    "bytes": 411.150848e6 + 4.481536e6,
     "algorithmic_bytes": 409731072,
 }
 
