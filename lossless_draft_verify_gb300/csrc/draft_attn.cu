@@ -610,11 +610,14 @@ draft_kivi_kernel(KiviParams P)
         uint8_t *myring = ring + (size_t)warp * NST * STAGE;
         const int n_pairs = (g_hi - g_lo + 1) / 2;
         const int n_mine = n_pairs > warp ? (n_pairs - warp + NW - 1) / NW : 0;
+        // the records are read once per launch: evict-first, so they do not push
+        // the partials, the window rows and this kernel's code out of L2
+        const uint64_t rec_policy = l2_evict_first();
         auto issue = [&](int s, int it) {
             const int g = g_lo + 2 * (warp + it * NW);
             const uint32_t bytes = (g + 1 < g_hi ? 2 : 1) * REC;
             mbar_arrive_expect_tx(&mybar[s], bytes);
-            bulk_g2s(myring + s * STAGE, rec_base + (size_t)g * REC, bytes, &mybar[s]);
+            bulk_g2s_hint(myring + s * STAGE, rec_base + (size_t)g * REC, bytes, &mybar[s], rec_policy);
         };
         // q first, as (c, c + 1) pairs (one 32-bit bf16 or 64-bit fp32 load
         // each when the unit's q rows are aligned for it): every warp's first

@@ -132,6 +132,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     // the first stages of W before the wait for the previous kernel, so their
     // loads overlap its tail.  x, the residual and the outputs come after it.
     const int pre = A.early_w ? min(n, GSTAGES) : 0;
+    // W is read once per launch: its lines are marked evict-first, so the
+    // stream does not push x, the partials and this kernel's code out of L2
+    const uint64_t w_policy = l2_evict_first();
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tmX);
         tc::prefetch_tmap(&tmW);
@@ -139,8 +142,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             uint8_t *sw = sm + Gg::OFF_W + i * Gg::WB;
             const int k = (kb0 + i) * GK;
             mbar_arrive_expect_tx(&B->full[i], Gg::XB + Gg::WB);
-            tc::tma_load_3d(sw, &tmW, n0, k, 0, &B->full[i]);
-            tc::tma_load_3d(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[i]);
+            tc::tma_load_3d_hint(sw, &tmW, n0, k, 0, &B->full[i], w_policy);
+            tc::tma_load_3d_hint(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[i], w_policy);
         }
     }
     pdl_wait();
@@ -156,8 +159,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     if (*reinterpret_cast<volatile int32_t *>(&B->abort_flag)) break;
                     uint8_t *sw = sm + Gg::OFF_W + s * Gg::WB;
                     mbar_arrive_expect_tx(&B->full[s], Gg::XB + Gg::WB);
-                    tc::tma_load_3d(sw, &tmW, n0, k, 0, &B->full[s]);
-                    tc::tma_load_3d(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[s]);
+                    tc::tma_load_3d_hint(sw, &tmW, n0, k, 0, &B->full[s], w_policy);
+                    tc::tma_load_3d_hint(sw + GK * 128, &tmW, n0 + 64, k, 0, &B->full[s], w_policy);
                 }
                 tc::tma_load_3d(sm + s * Gg::XB, &tmX, k, m0, 0, &B->full[s]);
             }

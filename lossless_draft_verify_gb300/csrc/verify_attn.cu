@@ -78,6 +78,7 @@ struct TcParams {
     int32_t *status;
     int Hkv, Hq, Dq, grp, n_mtiles, n_cta_m, n_split, tiles_per_split;
     int tail_rows;               // rows of the second row tile done by the tail warp (0: none)
+    int kv_once;                 // every K/V tile is read by one CTA: load it evict-first
     float scale_log2;
 };
 
@@ -242,6 +243,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             tc::prefetch_tmap(&tmQ);
             tc::prefetch_tmap(&tmK);
             tc::prefetch_tmap(&tmV);
+            const uint64_t kv_policy = l2_evict_first();
             mbar_arrive_expect_tx(&B->q_full, MT * TC_M * TC_D * 2);
             for (int t = 0; t < MT; ++t) {
                 const int qrow = b * P.Dq + q_first + t * rows_q;
@@ -256,13 +258,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 if (j >= STAGES && !wait_or_abort(&B->k_empty[s], par, B, P.status, 11)) break;
                 uint8_t *sk = sm + Gm::SM_K + s * TC_N * TC_D * 2;
                 mbar_arrive_expect_tx(&B->k_full[s], TC_N * TC_D * 2);
-                tc::tma_load_3d(sk, &tmK, 0, key0, unit, &B->k_full[s]);
-                tc::tma_load_3d(sk + TC_N * 128, &tmK, 64, key0, unit, &B->k_full[s]);
+                if (P.kv_once) {
+                    tc::tma_load_3d_hint(sk, &tmK, 0, key0, unit, &B->k_full[s], kv_policy);
+                    tc::tma_load_3d_hint(sk + TC_N * 128, &tmK, 64, key0, unit, &B->k_full[s], kv_policy);
+                } else {
+                    tc::tma_load_3d(sk, &tmK, 0, key0, unit, &B->k_full[s]);
+                    tc::tma_load_3d(sk + TC_N * 128, &tmK, 64, key0, unit, &B->k_full[s]);
+                }
                 if (j >= STAGES && !wait_or_abort(&B->v_empty[s], par, B, P.status, 12)) break;
                 uint8_t *sv = sm + Gm::SM_V + s * TC_N * TC_D * 2;
                 mbar_arrive_expect_tx(&B->v_full[s], TC_N * TC_D * 2);
-                tc::tma_load_3d(sv, &tmV, 0, key0, unit, &B->v_full[s]);
-                tc::tma_load_3d(sv + TC_N * 128, &tmV, 64, key0, unit, &B->v_full[s]);
+                if (P.kv_once) {
+                    tc::tma_load_3d_hint(sv, &tmV, 0, key0, unit, &B->v_full[s], kv_policy);
+                    tc::tma_load_3d_hint(sv + TC_N * 128, &tmV, 64, key0, unit, &B->v_full[s], kv_policy);
+                } else {
+                    tc::tma_load_3d(sv, &tmV, 0, key0, unit, &B->v_full[s]);
+                    tc::tma_load_3d(sv + TC_N * 128, &tmV, 64, key0, unit, &B->v_full[s]);
+                }
                 if (*reinterpret_cast<volatile int32_t *>(&B->abort_flag)) break;
             }
         }
@@ -963,6 +975,9 @@ cudaError_t verify_attn(const void *q, const void *k, const void *v, vc_dtype dt
         P.grp = grp;
         P.n_mtiles = pl.n_mtiles;
         P.n_cta_m = pl.n_cta_m;
+        // with two row-tile CTAs per unit each K/V tile is read twice, close in
+        // time: the second read may find it in L2
+        P.kv_once = pl.n_cta_m == 1 ? 1 : 0;
         P.n_split = pl.n_split;
         P.tiles_per_split = pl.tiles_per_split;
         P.scale_log2 = sl2;
