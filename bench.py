@@ -70,9 +70,9 @@ def dist_env():
 # kernel reports traffic null until it is captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("27d917349fc87023672562faddf09a0fe0d9847f37c603dae611698bc466d9d5",
-               "b510bbe2c0a3fd00dc0834096e12cd05dbcccf7f60c5931ba04e9be74c8ea859"),
-    "bytes": 411.150848e6 + 4.481536e6,
+    "sha256": ("f37d1922291a3c0792d89637365d01d97e3f8541a5a5913222b6393363da07ca",
+               "0ef2dd4e95c52fb9f0c6061fe73f4251def32e1390a8a92b67daed799a6b2f12"),
+    "bytes": 409.686272e6 + 3.519488e6,
     "algorithmic_bytes": 409731072,
 }
 
