@@ -113,7 +113,16 @@ struct RopeDst {
     void *k2, *v2;
     size_t bstride2;
     int stride2;
+    // Draft steps (one row per sequence): the new K and V rows go straight
+    // into the compressed cache's ring of unquantized tokens at slot
+    // pos % res_cap, and the last CTA of a sequence advances its length, as
+    // the ring append would (no rotation, no re-quantization).  kr null: off.
+    void *kr, *vr;     // [B][Hkv][res_cap][hd]
+    int res_cap;
+    int32_t *len, *ngroups, *qstatus;   // the cache's seq_len, n_groups, status
+    unsigned int *arrive;               // [B] CTA arrivals, zero between launches
 };
+constexpr int kQGroup = 32;   // tokens per quantized group of the compressed cache
 
 // One CTA per (row, block of kRopeHeads heads of q|k|v), one thread per
 // rotated pair (j, j + hd/2).  The inverse frequencies are fp64 (tabulated
@@ -131,8 +140,25 @@ rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd
     pdl_trigger();
     const int m = blockIdx.x;
     const int b = m / rows_per_seq, i = m % rows_per_seq;
-    const int pos = pos_base[b] + i;
+    // the position is read once per CTA: in ring mode the sequence's last CTA
+    // to arrive advances the length that pos_base points to
+    __shared__ int s_pos;
+    if (threadIdx.x == 0) s_pos = pos_base[b] + i;
+    __syncthreads();
+    const int pos = s_pos;
     const int half = hd / 2;
+    bool ring_ok = false;
+    if (dst.kr) {
+        const int unq = pos - dst.ngroups[b] * kQGroup;   // unquantized tokens before this one
+        ring_ok = unq >= 0 && unq < dst.res_cap;
+        if (threadIdx.x == 0) {
+            if (blockIdx.y == 0 && !ring_ok) atomicOr(dst.qstatus, unq < 0 ? 2 : 1);
+            if (atomicAdd(&dst.arrive[b], 1u) == gridDim.y - 1) {
+                if (ring_ok) dst.len[b] = pos + 1;
+                dst.arrive[b] = 0u;
+            }
+        }
+    }
     const int row1 = dst.pos1 ? pos : i;
     if (row1 < 0 || row1 >= dst.stride1) {
         // a position outside the cache: record it, write nothing
@@ -148,6 +174,14 @@ rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd
         // v: copied into the cache (and the block copy)
         const int h = hh - Hq - Hkv;
         const T v0 = src[j], v1 = src[j + half];
+        if (dst.kr) {
+            if (ring_ok) {
+                T *r = (T *)dst.vr + (((size_t)b * Hkv + h) * dst.res_cap + pos % dst.res_cap) * hd;
+                r[j] = v0;
+                r[j + half] = v1;
+            }
+            return;
+        }
         T *d1 = (T *)dst.v1 + b * dst.bstride1 + ((size_t)h * dst.stride1 + row1) * hd;
         d1[j] = v0;
         d1[j + half] = v1;
@@ -170,6 +204,12 @@ rope_kernel(const T *__restrict__ qkv, int rows_per_seq, int Hq, int Hkv, int hd
         T *qo = q_out + (size_t)m * Hq * hd + (size_t)hh * hd;
         qo[j] = y1;
         qo[j + half] = y2;
+    } else if (dst.kr) {
+        if (ring_ok) {
+            T *r = (T *)dst.kr + (((size_t)b * Hkv + (hh - Hq)) * dst.res_cap + pos % dst.res_cap) * hd;
+            r[j] = y1;
+            r[j + half] = y2;
+        }
     } else {
         const int h = hh - Hq;
         T *k1 = (T *)dst.k1 + b * dst.bstride1 + ((size_t)h * dst.stride1 + row1) * hd;
@@ -239,7 +279,7 @@ __global__ void writeback_kernel(const T *__restrict__ kb, const T *__restrict__
 
 // ------------------------------------------------------------------ layout --
 struct Layout {
-    size_t x, h, qkv, q, att, gu, act, kvn, hl, part, dws, vws, aws, nacc, tmax, tidx, lsc, total;
+    size_t x, h, qkv, q, att, gu, act, kvn, hl, part, dws, vws, aws, nacc, tmax, tidx, lsc, rarr, total;
     bool fused_head;      // LM head with the argmax epilogue (else logits staged in lsc)
 };
 
@@ -289,6 +329,7 @@ Layout layout_of(const vc_decoder *d, int B, int max_rows, int max_ctx, size_t d
     L.tmax = take(L.fused_head ? M * nt * 4 : 0);
     L.tidx = take(L.fused_head ? M * nt * 4 : 0);
     L.lsc = take(L.fused_head ? 0 : M * (size_t)c.vocab * es);
+    L.rarr = take((size_t)B * 4);         // RoPE's per-sequence arrivals in draft steps
     L.total = o;
     return L;
 }
@@ -441,7 +482,7 @@ cudaError_t forward_impl(const Ctx &C, const int32_t *first_tok, const int32_t *
                         C.counters(), C.status(), C.st, C.plan);
         }));
         if (!C.d->layer_ev.empty()) VC_TRY(cudaStreamWaitEvent(C.st, C.d->layer_ev[l], 0));
-        RopeDst dst;
+        RopeDst dst{};
         dst.k1 = (T *)kc + l * layer_cache;
         dst.v1 = (T *)vcache + l * layer_cache;
         dst.bstride1 = (size_t)c.n_kv_heads * L_stride * hd;
@@ -496,6 +537,7 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
     // calls) share the workspace with regions that forward passes overwrite:
     // clear them first
     VC_TRY(cudaMemsetAsync(C.at(C.L.dws), 0, kStatusBytes + a256((size_t)B * c.n_kv_heads * 4), C.st));
+    VC_TRY(cudaMemsetAsync(C.at(C.L.rarr), 0, (size_t)B * 4, C.st));
     embed_kernel<T><<<M, kRowThreads, 0, C.st>>>(tok, nullptr, 0, 1, (const T *)C.d->embed, c.vocab, c.d_model,
                                                  (T *)x, C.status());
     VC_TRY(cudaGetLastError());
@@ -505,7 +547,7 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
             return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
                         C.counters(), C.status(), C.st, C.plan);
         }));
-        RopeDst dst;
+        RopeDst dst{};
         dst.k1 = kn;
         dst.v1 = vn;
         dst.bstride1 = (size_t)kvd;
@@ -514,10 +556,24 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         dst.k2 = dst.v2 = nullptr;
         dst.bstride2 = 0;
         dst.stride2 = 1;
+        // the new row straight into the ring (one launch less per layer),
+        // unless the cache rotates its keys on the way in
+        const vc_qcache &qc = caches[l];
+        const bool ring = !qc.cfg.rotate && qc.d == hd && qc.Hkv == c.n_kv_heads && qc.B >= B &&
+                          (qc.res_dtype == VC_BF16) == (sizeof(T) == 2);
+        if (ring) {
+            dst.kr = qc.k_res;
+            dst.vr = qc.v_res;
+            dst.res_cap = qc.res_cap;
+            dst.len = qc.seq_len;
+            dst.ngroups = qc.n_groups;
+            dst.qstatus = qc.status;
+            dst.arrive = C.at<unsigned int>(C.L.rarr);
+        }
         VC_TRY(launch_pdl(rope_kernel<T>, dim3(M, rope_blocks(c)), dim3(kRopeHeads * 64), 0, C.st,
                           C.at<const T>(C.L.qkv), 1, c.n_heads, c.n_kv_heads, hd, (const int32_t *)caches[l].seq_len,
                           C.d->rope, C.at<T>(C.L.q), dst, C.status()));
-        VC_TRY(qcache_append(&caches[l], kn, vn, nullptr, nullptr, nullptr, 1, 0, C.st));
+        if (!ring) VC_TRY(qcache_append(&caches[l], kn, vn, nullptr, nullptr, nullptr, 1, 0, C.st));
         vc_cache_view view{};
         view.kind = VC_CACHE_KIVI;
         view.kivi = &caches[l];
