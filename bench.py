@@ -1014,7 +1014,7 @@ def run_model(args, dev, rank, world, barrier, pg):
             "kernels_round_b16_32k": round_k,
             "accepted_per_round_mean": float(n_acc.float().mean()), "tokens_per_round": tokens / args.steps,
             "prefill_s": round(t_pf, 2), "status": st,
-            "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc, packed) * args.steps,
+            "clocks": clk, "gpu_launches": model_launches_per_round(cfg, vc, packed, args.rotate) * args.steps,
             "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": run_bytes(cfg, swap_rows, packed),
                     "d2h_bytes_per_step": d2h + model_writeback_bytes(cfg, n_acc, packed),
                     "how": "host wall clock over the same K rounds as value (which uses device events around "
@@ -1146,12 +1146,14 @@ def round_kernels(dev, hbm, tf_burst, steps: int = 5, warmup: int = 3) -> dict:
     return out
 
 
-def model_launches_per_round(cfg, vc, packed: bool = False) -> int:
+def model_launches_per_round(cfg, vc, packed: bool = False, rotate: bool = False) -> int:
     """Kernels the library launches in one round of the model workload,
     counted from the decoder's sequencing.  A GEMM with more than one K split
     adds a reduction launch when its grid has more than 64 output tiles (fewer
     tiles, or the LM head's argmax epilogue, sum the splits inside the GEMM).
-    A packed host cache adds the expansion of K and V per layer."""
+    A packed host cache adds the expansion of K and V per layer.  In draft
+    steps RoPE writes the new rows into the compressed cache's ring itself,
+    unless the cache rotates its keys (then a ring append follows)."""
     qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
     shapes = [(qd + 2 * kvd, cfg.d_model), (cfg.d_model, qd), (2 * cfg.d_ff, cfg.d_model), (cfg.d_model, cfg.d_ff)]
 
@@ -1167,8 +1169,8 @@ def model_launches_per_round(cfg, vc, packed: bool = False) -> int:
         return 2 + 1 + sum(g(M, N, K, decode) for N, K in shapes) + (0 if fused else 1) + attn_kernels
 
     rows_v = M_B * (M_HORIZON + 1)
-    # embed, layers (+ append), rmsnorm, LM head (argmax), acceptance, scatter, status fold
-    draft = 1 + cfg.n_layers * (layer(M_B, True, 1) + 1) + 1 + g(M_B, cfg.vocab, cfg.d_model, True, True) + 3
+    # embed, layers (+ append with rotated keys), rmsnorm, LM head (argmax), acceptance, scatter, status fold
+    draft = 1 + cfg.n_layers * (layer(M_B, True, 1) + int(rotate)) + 1 + g(M_B, cfg.vocab, cfg.d_model, True, True) + 3
     # embed, layers (verify attention + its combine), rmsnorm, LM head (argmax), acceptance, status fold
     verify = 1 + cfg.n_layers * layer(rows_v, False, 2) + 1 + g(rows_v, cfg.vocab, cfg.d_model, False, True) + 2
     # + the commit (one append per layer) and the host write-back
