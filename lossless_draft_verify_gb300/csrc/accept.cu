@@ -49,7 +49,7 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline int splits_for(int V) { return V >= 65536 ? 4 : (V >= 16384 ? 2 : 1); }
+inline int splits_for(int V) { return V >= 65536 ? 4 : (V >= 16384 ? 2 : 1); }   // at most 4
 
 __host__ __device__ inline WsLayout ws_layout(void *ws, int B)
 {
@@ -152,26 +152,35 @@ accept_kernel(const T *__restrict__ logits, const int32_t *__restrict__ drafts, 
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    // Last CTA of sequence b: fold the partials of its D+1 rows.
+    // Last CTA of sequence b: fold the partials of its D+1 rows (a row's S
+    // partials requested together, folded in split order), then the accepted
+    // length is the first row whose argmax differs from its draft: every row
+    // compares its own draft, and the lowest mismatching row wins.
     __shared__ int amax[1024 + 1];
+    __shared__ int first_miss;
+    if (threadIdx.x == 0) first_miss = D;
+    __syncthreads();
+    constexpr int kMaxS = 4;                      // splits_for() never exceeds it
     for (int i = threadIdx.x; i <= D; i += kThreads) {
         const ArgMax *pp = W.part + (size_t)(b * (D + 1) + i) * S;
-        ArgMax a;
-        a.v = __ldcg(&pp[0].v);
-        a.i = __ldcg(&pp[0].i);
-        for (int t = 1; t < S; ++t) {
-            ArgMax c;
-            c.v = __ldcg(&pp[t].v);
-            c.i = __ldcg(&pp[t].i);
-            a = better(a, c);
-        }
+        ArgMax c[kMaxS];
+#pragma unroll
+        for (int t = 0; t < kMaxS; ++t)
+            if (t < S) {
+                c[t].v = __ldcg(&pp[t].v);
+                c[t].i = __ldcg(&pp[t].i);
+            }
+        const int dr = i < D ? drafts[(size_t)b * D + i] : -1;
+        ArgMax a = c[0];
+#pragma unroll
+        for (int t = 1; t < kMaxS; ++t)
+            if (t < S) a = better(a, c[t]);
         amax[i] = a.i;
+        if (i < D && a.i != dr) atomicMin(&first_miss, i);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        int n = D;
-        for (int i = 0; i < D; ++i)
-            if (amax[i] != drafts[(size_t)b * D + i]) { n = i; break; }
+        const int n = first_miss;
         n_acc[b] = n;
         next_tok[b] = amax[n];
         W.counters[b] = 0u;                 // every CTA of b has arrived: ready for the next call
@@ -205,8 +214,9 @@ cudaError_t launch(const void *logits, const int32_t *drafts, int B, int D, int 
 
 // Acceptance from the LM head's tile maxima ([B][D+1][n_tiles] value and
 // column of each 128-column tile's first maximum): a warp per row folds the
-// tiles with the same order (larger value, then lower column), thread 0
-// applies the greedy rule.
+// tiles with the same order (larger value, then lower column) and compares
+// the row's argmax with its draft; the lowest mismatching row ends the
+// accepted prefix (the greedy rule).
 __global__ void __launch_bounds__(kThreads)
 accept_tiles_kernel(const float *__restrict__ tmax, const int32_t *__restrict__ tidx, int n_tiles,
                     const int32_t *__restrict__ drafts, int D, int32_t *__restrict__ n_acc,
@@ -217,22 +227,24 @@ accept_tiles_kernel(const float *__restrict__ tmax, const int32_t *__restrict__ 
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int amax[1024 + 1];
+    __shared__ int first_miss;
+    if (threadIdx.x == 0) first_miss = D;
+    __syncthreads();
     for (int i = warp; i <= D; i += kThreads / 32) {
         const size_t row = (size_t)b * (D + 1) + i;
+        const int dr = (lane == 0 && i < D) ? drafts[(size_t)b * D + i] : -1;
         ArgMax best{-INFINITY, 0x7fffffff};
         for (int t = lane; t < n_tiles; t += 32)
             best = better(best, ArgMax{tmax[row * n_tiles + t], tidx[row * n_tiles + t]});
         best = warp_argmax(best);
-        if (lane == 0) amax[i] = best.i;
+        if (lane == 0) {
+            amax[i] = best.i;
+            if (i < D && best.i != dr) atomicMin(&first_miss, i);   // the lowest mismatching row wins
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        int n = D;
-        for (int i = 0; i < D; ++i)
-            if (amax[i] != drafts[(size_t)b * D + i]) {
-                n = i;
-                break;
-            }
+        const int n = first_miss;
         n_acc[b] = n;
         next_tok[b] = amax[n];
     }
