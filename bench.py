@@ -1164,13 +1164,17 @@ def model_launches_per_round(cfg, vc, packed: bool = False, rotate: bool = False
 
     def layer(M, decode, attn_kernels):
         # rmsnorm, qkv, rope, attention, o, rmsnorm, gate_up, silu, down; the
-        # SwiGLU runs in the gate|up GEMM's epilogue when that product is unsplit
+        # SwiGLU runs in the gate|up GEMM's epilogue when that product is unsplit,
+        # and in draft steps (M <= 16) the q|k|v and gate|up GEMMs normalise
+        # their input rows themselves (no RMSNorm launches)
         fused = vc.vc_gemm_splits(torch.bfloat16, 2 * cfg.d_ff, cfg.d_model, decode) == 1
-        return 2 + 1 + sum(g(M, N, K, decode) for N, K in shapes) + (0 if fused else 1) + attn_kernels
+        norms = 0 if (decode and M <= 16) else 2
+        return norms + 1 + sum(g(M, N, K, decode) for N, K in shapes) + (0 if fused else 1) + attn_kernels
 
     rows_v = M_B * (M_HORIZON + 1)
-    # embed, layers (+ append with rotated keys), rmsnorm, LM head (argmax), acceptance, scatter, status fold
-    draft = 1 + cfg.n_layers * (layer(M_B, True, 1) + int(rotate)) + 1 + g(M_B, cfg.vocab, cfg.d_model, True, True) + 3
+    # embed, layers (+ append with rotated keys), LM head (argmax, normalising its rows), acceptance,
+    # scatter, status fold
+    draft = 1 + cfg.n_layers * (layer(M_B, True, 1) + int(rotate)) + g(M_B, cfg.vocab, cfg.d_model, True, True) + 3
     # embed, layers (verify attention + its combine), rmsnorm, LM head (argmax), acceptance, status fold
     verify = 1 + cfg.n_layers * layer(rows_v, False, 2) + 1 + g(rows_v, cfg.vocab, cfg.d_model, False, True) + 2
     # + the commit (one append per layer) and the host write-back

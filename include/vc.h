@@ -718,6 +718,21 @@ vc_status vc_gemm_argmax(const void *x, const void *w, vc_dtype dt, int M, int N
 vc_status vc_gemm_swiglu(const void *x, const void *w_gate_up, void *act, vc_dtype dt, int M, int F, int K,
                          int decode_plan, cudaStream_t stream);
 
+/*
+ * vc_gemm_rms -- the draft-step product of RMS-normalised rows, as the
+ * decoder's draft steps compute it: out = rmsnorm(x) W with rmsnorm(x)[m] =
+ * x[m] / sqrt(mean_k x[m][k]^2 + eps) (no gain), x [M][K], W [K][N], out
+ * [M][N]; or with swiglu != 0 the SwiGLU of that product (W [K][N] in the
+ * interleaved gate|up layout of vc_decoder_weights, out = act [M][N/2]).  The
+ * GEMM reads x itself and scales each output row by 1 / sqrt(mean x^2 + eps)
+ * in its epilogue (fp32), so the result is within fp32 rounding of the
+ * two-pass product, not bit-identical to it.  bf16, 1 <= M <= 16, K % 64 == 0,
+ * N % 128 == 0 (swiglu: the unsplit products of vc_gemm_swiglu);
+ * VC_ERR_UNSUPPORTED otherwise.  ws as for vc_gemm (the decode plan).
+ */
+vc_status vc_gemm_rms(const void *x, const void *w, void *out, vc_dtype dt, int M, int N, int K, float eps, int swiglu,
+                      void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* vc_gemm with the split plan chosen explicitly: decode_plan != 0 runs the plan
  * of vc_decoder_draft_step (for M <= 16 it loads only 16 rows of x per K slice
  * and keeps six slices of W in flight); 0 is vc_gemm.  The workspace size from

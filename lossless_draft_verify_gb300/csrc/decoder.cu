@@ -397,7 +397,10 @@ cudaError_t rmsnorm(const Ctx &C, const void *x, int rows, int in_step, int in_o
 }
 
 // The MLP and attention-output half of a layer, shared by both passes:
-// x += att Wo; x += silu(x' Wg) (x' Wu) Wd with x' = rmsnorm(x).
+// x += att Wo; x += silu(x' Wg) (x' Wu) Wd with x' = rmsnorm(x).  In draft
+// steps the gate|up GEMM takes x itself and scales its rows by 1 / rms (no
+// separate normalisation launch); forward passes keep the separate RMSNorm, so
+// a block's rows take the arithmetic of one-token forwards.
 template <typename T>
 cudaError_t layer_tail(const Ctx &C, int l, int M)
 {
@@ -408,14 +411,21 @@ cudaError_t layer_tail(const Ctx &C, int l, int M)
         return gemm(C.at(C.L.att), C.d->wo[l], x, x, c.dt, M, c.d_model, qd, qd, part, C.counters(), C.status(),
                     C.st, C.plan);
     }));
-    VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
-    if (gemm_swiglu_ok(c.dt, c.d_ff, c.d_model, C.plan)) {
+    if (gemm_swiglu_ok(c.dt, c.d_ff, c.d_model, C.plan) &&
+        gemm_rms_ok(c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, C.plan)) {
+        VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
+            return gemm_swiglu(x, C.d->wgu[l], C.at(C.L.act), c.dt, M, c.d_ff, c.d_model, c.d_model, C.status(),
+                               C.st, C.plan, c.norm_eps);
+        }));
+    } else if (gemm_swiglu_ok(c.dt, c.d_ff, c.d_model, C.plan)) {
+        VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         // gate|up product and SwiGLU in one launch (the tensor-core epilogue)
         VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
             return gemm_swiglu(h, C.d->wgu[l], C.at(C.L.act), c.dt, M, c.d_ff, c.d_model, c.d_model, C.status(),
                                C.st, C.plan);
         }));
     } else {
+        VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         VC_TRY(traced(C, VC_TRACE_GEMM_GATE_UP, [&] {
             return gemm(h, C.d->wgu[l], nullptr, C.at(C.L.gu), c.dt, M, 2 * c.d_ff, c.d_model, c.d_model, part,
                         C.counters(), C.status(), C.st, C.plan);
@@ -432,9 +442,10 @@ cudaError_t layer_tail(const Ctx &C, int l, int M)
 
 // The LM head of greedy decoding without a logits output: argmax epilogue and
 // acceptance over the tile maxima, or (no tensor-core head) staged logits and
-// the logits scan.  Rows [B][D+1]; drafts [B][D] (null for D = 0).
+// the logits scan.  Rows [B][D+1]; drafts [B][D] (null for D = 0).  rms_eps
+// >= 0: h is the raw residual stream, normalised inside the head's GEMM.
 cudaError_t greedy_head(const Ctx &C, const void *h, int B, int D, const int32_t *drafts, int32_t *n_acc,
-                        int32_t *next_tok)
+                        int32_t *next_tok, float rms_eps = -1.f)
 {
     const vc_decoder_cfg &c = C.d->c;
     const int M = B * (D + 1);
@@ -442,7 +453,8 @@ cudaError_t greedy_head(const Ctx &C, const void *h, int B, int D, const int32_t
         const int nt = c.vocab / kGemmTileN;
         VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
             return gemm(h, C.d->head, nullptr, nullptr, c.dt, M, c.vocab, c.d_model, c.d_model, C.at(C.L.part),
-                        C.counters(), C.status(), C.st, C.plan, C.at<float>(C.L.tmax), C.at<int32_t>(C.L.tidx));
+                        C.counters(), C.status(), C.st, C.plan, C.at<float>(C.L.tmax), C.at<int32_t>(C.L.tidx),
+                        rms_eps);
         }));
         return accept_tiles(C.at<float>(C.L.tmax), C.at<int32_t>(C.L.tidx), nt, drafts, B, D, n_acc, next_tok, C.st);
     }
@@ -541,11 +553,15 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
     embed_kernel<T><<<M, kRowThreads, 0, C.st>>>(tok, nullptr, 0, 1, (const T *)C.d->embed, c.vocab, c.d_model,
                                                  (T *)x, C.status());
     VC_TRY(cudaGetLastError());
+    // the q|k|v and LM-head products take x itself and normalise its rows in
+    // their epilogue (no RMSNorm launches in a draft step) when the shape allows
+    const bool rms_qkv = gemm_rms_ok(c.dt, M, nqkv, c.d_model, c.d_model, C.plan);
+    const bool rms_head = !logits && C.L.fused_head && gemm_rms_ok(c.dt, M, c.vocab, c.d_model, c.d_model, C.plan);
     for (int l = 0; l < c.n_layers; ++l) {
-        VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
+        if (!rms_qkv) VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
         VC_TRY(traced(C, VC_TRACE_GEMM_QKV, [&] {
-            return gemm(h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model, part,
-                        C.counters(), C.status(), C.st, C.plan);
+            return gemm(rms_qkv ? x : h, C.d->wqkv[l], nullptr, C.at(C.L.qkv), c.dt, M, nqkv, c.d_model, c.d_model,
+                        part, C.counters(), C.status(), C.st, C.plan, nullptr, nullptr, rms_qkv ? c.norm_eps : -1.f);
         }));
         RopeDst dst{};
         dst.k1 = kn;
@@ -582,7 +598,7 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         }));
         VC_TRY(layer_tail<T>(C, l, M));
     }
-    VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
+    if (!rms_head) VC_TRY(rmsnorm<T>(C, x, M, 1, 0, h));
     if (logits) {
         VC_TRY(traced(C, VC_TRACE_GEMM_HEAD, [&] {
             return gemm(h, C.d->head, nullptr, logits, c.dt, M, c.vocab, c.d_model, c.d_model, part, C.counters(),
@@ -590,6 +606,8 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         }));
         VC_TRY(accept(logits, c.dt, nullptr, B, 0, c.vocab, C.at<int32_t>(C.L.nacc), next_tok, C.at(C.L.aws),
                       C.st, true));
+    } else if (rms_head) {
+        VC_TRY(greedy_head(C, x, B, 0, nullptr, C.at<int32_t>(C.L.nacc), next_tok, c.norm_eps));
     } else {
         VC_TRY(greedy_head(C, h, B, 0, nullptr, C.at<int32_t>(C.L.nacc), next_tok));
     }
@@ -797,6 +815,22 @@ vc_status vc_gemm(const void *x, const void *w, const void *resid, void *out, vc
                   void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     return vc_gemm_ex(x, w, resid, out, dt, M, N, K, 0, ws, ws_bytes, stream);
+}
+
+vc_status vc_gemm_rms(const void *x, const void *w, void *out, vc_dtype dt, int M, int N, int K, float eps, int swiglu,
+                      void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!x || !w || !out || M <= 0 || N <= 0 || K <= 0 || !(eps >= 0.f)) return VC_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out)) return VC_ERR_INVALID;
+    if (!gemm_rms_ok(dt, M, N, K, K, kGemmDecode)) return VC_ERR_UNSUPPORTED;
+    if (swiglu) {
+        if (N % 2 || !gemm_swiglu_ok(dt, N / 2, K, kGemmDecode)) return VC_ERR_UNSUPPORTED;
+        return to_status(gemm_swiglu(x, w, out, dt, M, N / 2, K, K, nullptr, stream, kGemmDecode, eps));
+    }
+    const size_t need = gemm_ws_bytes(dt, M, N, K, kGemmDecode);
+    if (need && (!ws || ws_bytes < need + kGemmCounterBytes || !aligned16(ws))) return VC_ERR_INVALID;
+    return to_status(gemm(x, w, nullptr, out, dt, M, N, K, K, need ? (uint8_t *)ws + kGemmCounterBytes : nullptr,
+                          need ? (unsigned int *)ws : nullptr, nullptr, stream, kGemmDecode, nullptr, nullptr, eps));
 }
 
 vc_status vc_gemm_swiglu(const void *x, const void *w_gate_up, void *act, vc_dtype dt, int M, int F, int K,

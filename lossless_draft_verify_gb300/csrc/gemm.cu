@@ -51,8 +51,11 @@ struct GemmGeom {
     static_assert(XR == 128 || OFF_W - XB + GM * GK * 2 <= OFF_BAR, "MMA read window must stay in shared memory");
 };
 
+constexpr int kRmsMaxRows = 16;   // rows whose norm the epilogue warps compute
+
 struct GemmBars {
     uint64_t full[G_MAX_STAGES], empty[G_MAX_STAGES], acc_full;
+    float rms[kRmsMaxRows];          // 1 / rms of x's rows (row-scale epilogue)
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t is_last;
@@ -69,6 +72,13 @@ struct GemmArgs {
     int M, N, K, S, kb_per_split;
     int early_w;                 // W may be read before the previous kernel completes
     int swiglu;                  // SwiGLU epilogue (S = 1): out is act [M][N / 2]
+    // RMS-normalised input (draft steps, M <= 16, no residual): x is the raw
+    // residual stream; every output row m is scaled by 1 / sqrt(mean_k x[m][k]^2
+    // + rms_eps), which the epilogue warps compute from x while W streams in,
+    // so rmsnorm(x) W needs no separate normalisation pass.  Null: off.
+    const __nv_bfloat16 *rms_x;
+    int rms_ld;
+    float rms_eps;
 };
 
 // bf16 rounding of an output element, as the logits store would make it
@@ -192,6 +202,33 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int r = wq * 32 + lane;
         const int m = m0 + r;
         const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16);
+        float rsc = 1.f;
+        if (A.rms_x) {
+            // 8 epilogue threads per row (consecutive lanes of one warp), 16-byte
+            // loads, then a three-step shuffle sum; the four epilogue warps meet
+            // at a named barrier before reading the scales
+            const int et = threadIdx.x - 64, row = et >> 3, part = et & 7;
+            float ss = 0.f;
+            if (row < A.M) {
+                const __nv_bfloat16 *xr = A.rms_x + (size_t)row * A.rms_ld;
+                for (int k = part * 8; k < A.K; k += 64) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xr + k);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = bf16_lo(w4[e]), b = bf16_hi(w4[e]);
+                        ss = fmaf(a, a, ss);
+                        ss = fmaf(b, b, ss);
+                    }
+                }
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+            if (part == 0 && row < A.M) B->rms[row] = 1.0f / sqrtf(ss / (float)A.K + A.rms_eps);
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            rsc = m < A.M ? B->rms[r] : 1.f;
+        }
         const bool ok = g_wait(&B->acc_full, 0, B, A.status, 43);
         if (ok && A.swiglu) {
             // SwiGLU epilogue: columns [0, 64) of the tile are gate columns and
@@ -209,10 +246,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     uint32_t packed[16];
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
-                        const float g0 = bf16_round(__uint_as_float(ug[c]));
-                        const float g1 = bf16_round(__uint_as_float(ug[c + 1]));
-                        const float u0 = bf16_round(__uint_as_float(uu[c]));
-                        const float u1 = bf16_round(__uint_as_float(uu[c + 1]));
+                        const float g0 = bf16_round(__uint_as_float(ug[c]) * rsc);
+                        const float g1 = bf16_round(__uint_as_float(ug[c + 1]) * rsc);
+                        const float u0 = bf16_round(__uint_as_float(uu[c]) * rsc);
+                        const float u1 = bf16_round(__uint_as_float(uu[c + 1]) * rsc);
                         __nv_bfloat162 h2 = __floats2bfloat162_rn((g0 / (1.0f + expf(-g0))) * u0,
                                                                   (g1 / (1.0f + expf(-g1))) * u1);
                         packed[c / 2] = *reinterpret_cast<uint32_t *>(&h2);
@@ -232,6 +269,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 uint32_t u[32];
                 tc::ld32(taddr + h * 32, u);
                 tc::ld_wait();
+                if (A.rms_x) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) u[c] = __float_as_uint(__uint_as_float(u[c]) * rsc);
+                }
                 if (m < A.M) {
                     const int c0 = n0 + h * 32;
                     if (A.S == 1 && A.amax_val) {
@@ -495,11 +536,19 @@ bool gemm_argmax_ok(vc_dtype dt, int M, int N, int K, int plan, bool have_counte
     return gemm_splits(N, K, plan) == 1 || (have_counters && tiles <= kGemmMaxTiles);
 }
 
+bool gemm_rms_ok(vc_dtype dt, int M, int N, int K, int ldx, int plan)
+{
+    return dt == VC_BF16 && (plan & ~kGemmEarlyWeights) == kGemmDecode && M > 0 && M <= kRmsMaxRows &&
+           ldx % 8 == 0 && gemm_uses_tensor_cores(dt, N, K);
+}
+
 cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
                  int ldx, void *ws, unsigned int *counters, int32_t *status, cudaStream_t st, int plan,
-                 float *amax_val, int32_t *amax_idx)
+                 float *amax_val, int32_t *amax_idx, float rms_eps)
 {
     const bool early_w = (plan & kGemmEarlyWeights) != 0;
+    const bool rms = rms_eps >= 0.f;
+    if (rms && (resid || !gemm_rms_ok(dt, M, N, K, ldx, plan))) return cudaErrorNotSupported;
     plan &= ~kGemmEarlyWeights;
     if (M <= 0) return cudaSuccess;
     if (amax_val && !gemm_argmax_ok(dt, M, N, K, plan, counters != nullptr)) return cudaErrorNotSupported;
@@ -509,7 +558,7 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         if (!tma_map_bf16_3d(&mx, x, K, M, 1, (uint64_t)ldx * 2, (uint64_t)ldx * 2 * M, GK, small ? 16 : GM, 1) ||
             !tma_map_bf16_3d(&mw, w, N, K, 1, (uint64_t)N * 2, (uint64_t)N * 2 * K, 64, GK, 1))
             return cudaErrorInvalidValue;
-        GemmArgs A;
+        GemmArgs A = {};
         A.S = gemm_splits(N, K, plan);
         const int nkb = K / GK;
         A.kb_per_split = (nkb + A.S - 1) / A.S;
@@ -532,6 +581,9 @@ cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_
         A.K = K;
         A.early_w = early_w ? 1 : 0;
         A.swiglu = 0;
+        A.rms_x = rms ? (const __nv_bfloat16 *)x : nullptr;
+        A.rms_ld = ldx;
+        A.rms_eps = rms ? rms_eps : 0.f;
         dim3 grid((M + GM - 1) / GM, N / GN, A.S);
         cudaError_t e;
         if (small) {
@@ -570,9 +622,11 @@ bool gemm_swiglu_ok(vc_dtype dt, int F, int K, int plan)
 }
 
 cudaError_t gemm_swiglu(const void *x, const void *w, void *act, vc_dtype dt, int M, int F, int K, int ldx,
-                        int32_t *status, cudaStream_t st, int plan)
+                        int32_t *status, cudaStream_t st, int plan, float rms_eps)
 {
     if (!gemm_swiglu_ok(dt, F, K, plan)) return cudaErrorNotSupported;
+    const bool rms = rms_eps >= 0.f;
+    if (rms && !gemm_rms_ok(dt, M, 2 * F, K, ldx, plan)) return cudaErrorNotSupported;
     const bool early_w = (plan & kGemmEarlyWeights) != 0;
     plan &= ~kGemmEarlyWeights;
     if (M <= 0) return cudaSuccess;
@@ -582,7 +636,7 @@ cudaError_t gemm_swiglu(const void *x, const void *w, void *act, vc_dtype dt, in
     if (!tma_map_bf16_3d(&mx, x, K, M, 1, (uint64_t)ldx * 2, (uint64_t)ldx * 2 * M, GK, small ? 16 : GM, 1) ||
         !tma_map_bf16_3d(&mw, w, N, K, 1, (uint64_t)N * 2, (uint64_t)N * 2 * K, 64, GK, 1))
         return cudaErrorInvalidValue;
-    GemmArgs A;
+    GemmArgs A = {};
     A.S = 1;
     A.kb_per_split = K / GK;
     A.part = nullptr;
@@ -597,6 +651,9 @@ cudaError_t gemm_swiglu(const void *x, const void *w, void *act, vc_dtype dt, in
     A.K = K;
     A.early_w = early_w ? 1 : 0;
     A.swiglu = 1;
+    A.rms_x = rms ? (const __nv_bfloat16 *)x : nullptr;
+    A.rms_ld = ldx;
+    A.rms_eps = rms ? rms_eps : 0.f;
     dim3 grid((M + GM - 1) / GM, N / GN, 1);
     if (small) {
         using Gg = GemmGeom<16, 6>;

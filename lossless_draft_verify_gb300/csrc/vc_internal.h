@@ -78,9 +78,14 @@ constexpr size_t kGemmCounterBytes = (size_t)kGemmMaxTiles * 4;
 bool gemm_uses_tensor_cores(vc_dtype dt, int N, int K);
 int gemm_splits(int N, int K, int plan);
 size_t gemm_ws_bytes(vc_dtype dt, int M, int N, int K, int plan = kGemmRowInvariant);
+// rms_eps >= 0: x is the raw residual stream and every output row is scaled by
+// 1 / sqrt(mean(x_row^2) + rms_eps), i.e. the product of rmsnorm(x) (draft-step
+// products only: gemm_rms_ok; no residual)
 cudaError_t gemm(const void *x, const void *w, const void *resid, void *out, vc_dtype dt, int M, int N, int K,
                  int ldx, void *ws, unsigned int *counters, int32_t *status, cudaStream_t st,
-                 int plan = kGemmRowInvariant, float *amax_val = nullptr, int32_t *amax_idx = nullptr);
+                 int plan = kGemmRowInvariant, float *amax_val = nullptr, int32_t *amax_idx = nullptr,
+                 float rms_eps = -1.f);
+bool gemm_rms_ok(vc_dtype dt, int M, int N, int K, int ldx, int plan);
 // whether the argmax epilogue is available for this shape and plan (tensor-core
 // path, and one K split or per-tile counters)
 bool gemm_argmax_ok(vc_dtype dt, int M, int N, int K, int plan, bool have_counters);
@@ -90,7 +95,7 @@ bool gemm_argmax_ok(vc_dtype dt, int M, int N, int K, int plan, bool have_counte
 // tensor-core GEMM, for bf16 products the plan leaves unsplit
 bool gemm_swiglu_ok(vc_dtype dt, int F, int K, int plan);
 cudaError_t gemm_swiglu(const void *x, const void *w, void *act, vc_dtype dt, int M, int F, int K, int ldx,
-                        int32_t *status, cudaStream_t st, int plan);
+                        int32_t *status, cudaStream_t st, int plan, float rms_eps = -1.f);
 constexpr int kGemmTileN = 128;     // columns per argmax tile
 
 // host_util.cu

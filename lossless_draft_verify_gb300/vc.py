@@ -161,6 +161,8 @@ def load() -> ctypes.CDLL:
     L.vc_gemm_argmax.restype = c_int
     L.vc_gemm_argmax.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, P, P, P, c_size_t, P]
     L.vc_gemm_swiglu.restype = c_int
+    L.vc_gemm_rms.restype = c_int
+    L.vc_gemm_rms.argtypes = [P, P, P, c_int, c_int, c_int, c_int, ctypes.c_float, c_int, P, c_size_t, P]
     L.vc_swap_in_rows.restype = c_int
     L.vc_swap_in_rows.argtypes = [P, P, c_size_t, c_size_t, c_size_t, c_size_t, P, P]
     L.vc_gemm_swiglu.argtypes = [P, P, P, c_int, c_int, c_int, c_int, c_int, P]
@@ -192,7 +194,7 @@ EXPORTED = ["vc_status_str", "vc_version", "vc_check", "vc_workspace_init", "vc_
             "vc_swap_in_paced", "vc_gemm_argmax", "vc_accept_tiles", "vc_decoder_verify",
             "vc_kv_packed_row_bytes", "vc_kv_pack", "vc_kv_unpack", "vc_kv_writeback_packed",
             "vc_verify_attn_h2o_workspace_bytes", "vc_verify_attn_h2o", "vc_decoder_set_layer_events",
-            "vc_gemm_swiglu", "vc_swap_in_rows"]
+            "vc_gemm_swiglu", "vc_swap_in_rows", "vc_gemm_rms"]
 
 TRACE_KINDS = ["gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_head", "draft_attn", "verify_attn"]
 
@@ -502,6 +504,19 @@ def interleave_gate_up(wg: torch.Tensor, wu: torch.Tensor) -> torch.Tensor:
     K, F = wg.shape
     assert wu.shape == (K, F) and F % 64 == 0
     return torch.stack([wg.reshape(K, F // 64, 64), wu.reshape(K, F // 64, 64)], dim=2).reshape(K, 2 * F)
+
+
+def vc_gemm_rms(x, w, out, eps: float, swiglu: bool = False, ws: Workspace | None = None, stream=None):
+    """out = rmsnorm(x) W (swiglu: the SwiGLU of it, W interleaved gate|up,
+    out [M][N/2]) with the normalisation in the GEMM epilogue, as the
+    decoder's draft steps compute it (bf16, M <= 16)."""
+    M, K = x.shape
+    K2, N = w.shape
+    assert K == K2 and out.shape == ((M, N // 2) if swiglu else (M, N))
+    assert x.is_contiguous() and w.is_contiguous() and out.is_contiguous()
+    _check(load().vc_gemm_rms(x.data_ptr(), w.data_ptr(), out.data_ptr(), _dt(x), M, N, K, float(eps),
+                              int(bool(swiglu)), ws.ptr if ws is not None else None,
+                              ws.nbytes if ws is not None else 0, _stream(stream)), "vc_gemm_rms")
 
 
 def vc_gemm_swiglu(x, w_gate_up, act, stream=None, decode_plan: bool = False):

@@ -41,6 +41,50 @@ def test_gemm_bf16_matches_definition(M, N, K, plan):
         assert (np.abs(got - want) <= tol).all(), np.abs(got - want).max()
 
 
+@pytest.mark.parametrize("M,N,K", [(8, 6144, 4096), (8, 32000, 4096), (16, 4096, 14336), (3, 1024, 512)])
+def test_gemm_of_normalised_rows_matches_definition(M, N, K):
+    """vc_gemm_rms (the draft steps' q|k|v and head products): rmsnorm(x) W
+    with the row scale 1 / sqrt(mean x^2 + eps) applied in the epilogue, within
+    the fp32-accumulation bound of the fp64 definition; x un-normalised
+    (rows of different scales)."""
+    vc = lib()
+    eps = 1e-5
+    x = inputs.normal_bf16((M, K), 51 + M, device="cuda")
+    x = (x.float() * torch.linspace(0.5, 8.0, M, device="cuda")[:, None]).to(torch.bfloat16)
+    w = inputs.normal_bf16((K, N), 52 + N, device="cuda", std=0.02)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = vc.Workspace(vc.vc_gemm_workspace_bytes(x.dtype, M, N, K))
+    vc.vc_gemm_rms(x, w, out, eps, ws=ws)
+    torch.cuda.synchronize()
+    xd = f32(x).astype(np.float64)
+    h = xd / np.sqrt((xd * xd).mean(axis=1, keepdims=True) + eps)
+    want = h @ f32(w).astype(np.float64)
+    got = f32(out).astype(np.float64)
+    tol = 2.0 ** -8 * np.abs(want) + 1e-5 * np.sqrt(K) * np.abs(h).max() * np.abs(f32(w)).max() * 8
+    assert np.isfinite(got).all() and (np.abs(got - want) <= tol).all(), np.abs(got - want).max()
+
+
+def test_swiglu_of_normalised_rows_matches_definition():
+    """vc_gemm_rms with swiglu: act = silu(g) u of the normalised rows' gate and
+    up products, within a few bf16 ulps of the fp64 definition."""
+    vc = lib()
+    M, F, K, eps = 8, 14336, 1024, 1e-5        # the draft steps' unsplit gate|up width
+    x = (inputs.normal_bf16((M, K), 61, device="cuda").float() * 3.0).to(torch.bfloat16)
+    w = inputs.normal_bf16((K, 2 * F), 62, device="cuda", std=0.05)
+    act = torch.full((M, F), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc.vc_gemm_rms(x, w, act, eps, swiglu=True)
+    torch.cuda.synchronize()
+    xd = f32(x).astype(np.float64)
+    h = xd / np.sqrt((xd * xd).mean(axis=1, keepdims=True) + eps)
+    gu = (h @ f32(w).astype(np.float64)).reshape(M, F // 64, 2, 64)
+    g, u = gu[:, :, 0, :].reshape(M, F), gu[:, :, 1, :].reshape(M, F)
+    want = g / (1.0 + np.exp(-g)) * u
+    got = f32(act).astype(np.float64)
+    scale = np.maximum(np.abs(want), np.abs(g * u) * 0.0 + 1e-3)
+    assert np.isfinite(got).all()
+    assert (np.abs(got - want) <= 2.0 ** -6 * scale + 2e-3).all(), np.abs(got - want).max()
+
+
 def test_gemm_bf16_in_place_residual():
     vc = lib()
     M, N, K = 40, 256, 512
