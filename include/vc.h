@@ -279,7 +279,15 @@ typedef struct vc_cache_view {
     int32_t B, Hkv, d;           /* VC_CACHE_DENSE shape */
     int32_t L_stride;            /* VC_CACHE_DENSE row stride per (b, h) */
     int32_t max_len;             /* VC_CACHE_DENSE: upper bound of seq_len (grid sizing) */
+    int32_t flags;               /* VC_VIEW_* bits, 0 by default */
 } vc_cache_view;
+
+/* VC_CACHE_KIVI: the caller guarantees that the kernel launched just before on
+ * the stream writes neither the cache's records nor its n_groups (it may write
+ * the ring and seq_len, as a draft step's RoPE does), so the draft kernel may
+ * start copying records before that kernel has finished (programmatic
+ * dependent launch).  Without the flag every read waits for it. */
+#define VC_VIEW_RECORDS_STABLE 1
 
 size_t vc_draft_attn_workspace_bytes(const vc_cache_view *view, int Hq);
 

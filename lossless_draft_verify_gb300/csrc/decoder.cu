@@ -593,6 +593,9 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
         vc_cache_view view{};
         view.kind = VC_CACHE_KIVI;
         view.kivi = &caches[l];
+        // in a draft step the kernel before draft attention (RoPE, or the ring
+        // append) writes only the ring and the length: the records are stable
+        view.flags = VC_VIEW_RECORDS_STABLE;
         VC_TRY(traced(C, VC_TRACE_DRAFT_ATTN, [&] {
             return draft_attn(C.at(C.L.q), c.dt, &view, c.n_heads, scale, C.at(C.L.att), C.at(C.L.dws), C.st);
         }));

@@ -192,6 +192,7 @@ struct KiviParams {
     float *raw;                                        // optional [units][raw_stride][4] log2-domain scores (H2O)
     float *ml;                                         // optional [units][8]: each head's final max and sum
     int raw_stride;
+    int early_records;   // records and n_groups stable: the first record copies precede the grid-dependency wait
 };
 
 template <typename TQ, int D>
@@ -572,8 +573,10 @@ template <int BITS, int D, typename TQ, typename TR, bool ROT>
 __global__ void __launch_bounds__(kThreads, 4)
 draft_kivi_kernel(KiviParams P)
 {
-    pdl_wait();
-    pdl_trigger();
+    if (!P.early_records) {
+        pdl_wait();
+        pdl_trigger();
+    }
     using Gm = KiviGeom<BITS, D>;
     constexpr int KS = Gm::KS, NG = Gm::NG, REC = Gm::REC, NST = Gm::NST;
     constexpr int STAGE = 2 * REC;
@@ -627,18 +630,33 @@ draft_kivi_kernel(KiviParams P)
         const bool qvalid = hq < grp;
         const bool q_pairs = (reinterpret_cast<uintptr_t>(qg) & (2 * sizeof(TQ) - 1)) == 0;
         float2 qq[KS][2];
-        if constexpr (!ROT) {
+        auto load_qq = [&] {
+            if constexpr (!ROT) {
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
+                for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr)
-                    qq[ks][rr] = qvalid ? load_q2<TQ, D>(qg, hq * D + 16 * ks + 2 * tig + 8 * rr, q_pairs)
-                                        : make_float2(0.f, 0.f);
-        }
-        if (lane == 0) {
-            for (int s = 0; s < NST; ++s) mbar_init(&mybar[s], 1);
-            fence_mbar_init();
-            for (int s = 0; s < NST && s < n_mine; ++s) issue(s, s);
+                    for (int rr = 0; rr < 2; ++rr)
+                        qq[ks][rr] = qvalid ? load_q2<TQ, D>(qg, hq * D + 16 * ks + 2 * tig + 8 * rr, q_pairs)
+                                            : make_float2(0.f, 0.f);
+            }
+        };
+        auto first_copies = [&] {
+            if (lane == 0) {
+                for (int s = 0; s < NST; ++s) mbar_init(&mybar[s], 1);
+                fence_mbar_init();
+                for (int s = 0; s < NST && s < n_mine; ++s) issue(s, s);
+            }
+        };
+        if (P.early_records) {
+            // stable records: their first copies overlap the previous kernel's
+            // end; q (written by it) after the wait
+            first_copies();
+            pdl_wait();
+            pdl_trigger();
+            load_qq();
+        } else {
+            load_qq();
+            first_copies();
         }
         if constexpr (ROT) {
             rotate_queries<TQ, D>(qg, grp, rq);
@@ -853,6 +871,10 @@ draft_kivi_kernel(KiviParams P)
                                 P.ml ? P.ml + (size_t)unit * 8 : nullptr);
     } else {
         // ------------------------------------- residual ring (fp32 SIMT) --
+        if (P.early_records) {
+            pdl_wait();
+            pdl_trigger();
+        }
         // Split r of the ring takes positions p0 + r * res_per_split onwards;
         // its rows are staged in shared memory (the idle stream ring) by bulk
         // copies, a chunk at a time, so the per-token math never waits on a
@@ -1489,7 +1511,7 @@ inline int kivi_token_cap(const vc_qcache *c) { return c->max_groups * G + c->re
 
 template <int BITS, int D, typename TQ, typename TR, bool ROT>
 cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, void *out, void *ws,
-                        cudaStream_t st, float *raw = nullptr, float *ml = nullptr)
+                        cudaStream_t st, float *raw = nullptr, float *ml = nullptr, bool early = false)
 {
     using Gm = KiviGeom<BITS, D>;
     const KiviPlan pl = kivi_plan(c);
@@ -1516,6 +1538,7 @@ cudaError_t launch_kivi(const void *q, const vc_qcache *c, int Hq, float scale, 
     P.n_split_r = pl.n_split_r;
     P.res_per_split = pl.res_per_split;
     P.qscale = scale * kLog2e;
+    P.early_records = early ? 1 : 0;
     const size_t rot_bytes = ROT ? 16 * D : 0;
     size_t smem = 128 + 6 * D + rot_bytes + (size_t)NW * Gm::NST * 2 * Gm::REC;
     const size_t merge = 128 + 6 * D + rot_bytes + (size_t)merge_floats(D) * 4;
@@ -1573,22 +1596,23 @@ cudaError_t launch_dense(const void *q, const vc_cache_view *v, int Hq, float sc
 
 template <int BITS, int D, typename TQ>
 cudaError_t kivi_by_res(const void *q, const vc_qcache *c, int Hq, float s, void *o, void *ws,
-                        cudaStream_t st, float *raw = nullptr, float *ml = nullptr)
+                        cudaStream_t st, float *raw = nullptr, float *ml = nullptr, bool early = false)
 {
     if (c->cfg.rotate)
         return c->res_dtype == VC_BF16
-                   ? launch_kivi<BITS, D, TQ, __nv_bfloat16, true>(q, c, Hq, s, o, ws, st, raw, ml)
-                   : launch_kivi<BITS, D, TQ, float, true>(q, c, Hq, s, o, ws, st, raw, ml);
-    return c->res_dtype == VC_BF16 ? launch_kivi<BITS, D, TQ, __nv_bfloat16, false>(q, c, Hq, s, o, ws, st, raw, ml)
-                                   : launch_kivi<BITS, D, TQ, float, false>(q, c, Hq, s, o, ws, st, raw, ml);
+                   ? launch_kivi<BITS, D, TQ, __nv_bfloat16, true>(q, c, Hq, s, o, ws, st, raw, ml, early)
+                   : launch_kivi<BITS, D, TQ, float, true>(q, c, Hq, s, o, ws, st, raw, ml, early);
+    return c->res_dtype == VC_BF16
+               ? launch_kivi<BITS, D, TQ, __nv_bfloat16, false>(q, c, Hq, s, o, ws, st, raw, ml, early)
+               : launch_kivi<BITS, D, TQ, float, false>(q, c, Hq, s, o, ws, st, raw, ml, early);
 }
 
 template <int D, typename TQ>
 cudaError_t kivi_by_bits(const void *q, const vc_qcache *c, int Hq, float s, void *o, void *ws,
-                         cudaStream_t st, float *raw = nullptr, float *ml = nullptr)
+                         cudaStream_t st, float *raw = nullptr, float *ml = nullptr, bool early = false)
 {
-    return c->cfg.bits == 2 ? kivi_by_res<2, D, TQ>(q, c, Hq, s, o, ws, st, raw, ml)
-                            : kivi_by_res<4, D, TQ>(q, c, Hq, s, o, ws, st, raw, ml);
+    return c->cfg.bits == 2 ? kivi_by_res<2, D, TQ>(q, c, Hq, s, o, ws, st, raw, ml, early)
+                            : kivi_by_res<4, D, TQ>(q, c, Hq, s, o, ws, st, raw, ml, early);
 }
 
 }  // namespace
@@ -1623,11 +1647,12 @@ cudaError_t draft_attn(const void *q, vc_dtype q_dt, const vc_cache_view *view, 
 {
     if (view->kind == VC_CACHE_KIVI) {
         const vc_qcache *c = view->kivi;
+        const bool early = (view->flags & VC_VIEW_RECORDS_STABLE) != 0;
         if (c->d == 128)
-            return q_dt == VC_BF16 ? kivi_by_bits<128, __nv_bfloat16>(q, c, Hq, sm_scale, out, ws, st)
-                                   : kivi_by_bits<128, float>(q, c, Hq, sm_scale, out, ws, st);
-        return q_dt == VC_BF16 ? kivi_by_bits<64, __nv_bfloat16>(q, c, Hq, sm_scale, out, ws, st)
-                               : kivi_by_bits<64, float>(q, c, Hq, sm_scale, out, ws, st);
+            return q_dt == VC_BF16 ? kivi_by_bits<128, __nv_bfloat16>(q, c, Hq, sm_scale, out, ws, st, nullptr, nullptr, early)
+                                   : kivi_by_bits<128, float>(q, c, Hq, sm_scale, out, ws, st, nullptr, nullptr, early);
+        return q_dt == VC_BF16 ? kivi_by_bits<64, __nv_bfloat16>(q, c, Hq, sm_scale, out, ws, st, nullptr, nullptr, early)
+                               : kivi_by_bits<64, float>(q, c, Hq, sm_scale, out, ws, st, nullptr, nullptr, early);
     }
     if (view->d == 128)
         return view->dt == VC_BF16 ? launch_dense<__nv_bfloat16, 128>(q, view, Hq, sm_scale, out, ws, st)

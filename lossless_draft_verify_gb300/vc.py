@@ -49,7 +49,7 @@ class DropCfg(ctypes.Structure):
 class CacheView(ctypes.Structure):
     _fields_ = [("kind", c_int), ("kivi", ctypes.POINTER(QCacheC)), ("k", c_void_p), ("v", c_void_p),
                 ("dt", c_int), ("seq_len", c_void_p), ("B", c_int32), ("Hkv", c_int32), ("d", c_int32),
-                ("L_stride", c_int32), ("max_len", c_int32)]
+                ("L_stride", c_int32), ("max_len", c_int32), ("flags", c_int32)]
 
 
 class DecoderCfg(ctypes.Structure):
