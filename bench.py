@@ -70,9 +70,9 @@ def dist_env():
 # kernel reports traffic null until it is captured again.
 DRAFT_TRAFFIC = {
     "sources": ("lossless_draft_verify_gb300/csrc/draft_attn.cu", "lossless_draft_verify_gb300/csrc/vc_common.cuh"),
-    "sha256": ("f37d1922291a3c0792d89637365d01d97e3f8541a5a5913222b6393363da07ca",
+    "sha256": ("8c0c9ce64474c47871902141eb7d70c8a550ff7a5f5d442e2e8e938e2597b714",
                "0ef2dd4e95c52fb9f0c6061fe73f4251def32e1390a8a92b67daed799a6b2f12"),
-    "bytes": 409.686272e6 + 3.519488e6,
+    "bytes": 409.689088e6 + 3.538176e6,
     "algorithmic_bytes": 409731072,
 }
 
