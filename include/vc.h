@@ -279,7 +279,7 @@ typedef struct vc_cache_view {
     int32_t B, Hkv, d;           /* VC_CACHE_DENSE shape */
     int32_t L_stride;            /* VC_CACHE_DENSE row stride per (b, h) */
     int32_t max_len;             /* VC_CACHE_DENSE: upper bound of seq_len (grid sizing) */
-    int32_t flags;               /* VC_VIEW_* bits, 0 by default */
+    int32_t flags;               /* VC_VIEW_* bits; zero-initialise the view (0: none) */
 } vc_cache_view;
 
 /* VC_CACHE_KIVI: the caller guarantees that the kernel launched just before on
