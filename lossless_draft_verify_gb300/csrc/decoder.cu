@@ -54,10 +54,17 @@ size_t esize(vc_dtype dt) { return dt == VC_BF16 ? 2 : 4; }
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads)
 embed_kernel(const int32_t *__restrict__ first_tok, const int32_t *__restrict__ toks, int tok_stride,
-             int rows_per_seq, const T *__restrict__ E, int vocab, int D, T *__restrict__ x, int32_t *status)
+             int rows_per_seq, const T *__restrict__ E, int vocab, int D, T *__restrict__ x, int32_t *status,
+             uint32_t *z0 = nullptr, int z0_words = 0, uint32_t *z1 = nullptr, int z1_words = 0)
 {
     pdl_wait();
     pdl_trigger();
+    // a draft step's scratch words that later kernels of the step expect at
+    // zero (draft attention's status and arrival counters, RoPE's arrivals)
+    if (blockIdx.x == 0) {
+        for (int j = threadIdx.x; j < z0_words; j += kRowThreads) z0[j] = 0u;
+        for (int j = threadIdx.x; j < z1_words; j += kRowThreads) z1[j] = 0u;
+    }
     const int m = blockIdx.x;
     const int b = m / rows_per_seq, i = m % rows_per_seq;
     int t;
@@ -547,12 +554,12 @@ cudaError_t draft_impl(const Ctx &C, const int32_t *tok, int B, vc_qcache *cache
     const float scale = 1.0f / sqrtf((float)hd);
     // the draft kernel's status block and arrival counters (zero between its
     // calls) share the workspace with regions that forward passes overwrite:
-    // clear them first
-    VC_TRY(cudaMemsetAsync(C.at(C.L.dws), 0, kStatusBytes + a256((size_t)B * c.n_kv_heads * 4), C.st));
-    VC_TRY(cudaMemsetAsync(C.at(C.L.rarr), 0, (size_t)B * 4, C.st));
-    embed_kernel<T><<<M, kRowThreads, 0, C.st>>>(tok, nullptr, 0, 1, (const T *)C.d->embed, c.vocab, c.d_model,
-                                                 (T *)x, C.status());
-    VC_TRY(cudaGetLastError());
+    // the embedding launch clears them, and RoPE's arrivals, first (a kernel
+    // rather than memset nodes, so the chain of programmatic dependent
+    // launches runs on from one draft step into the next)
+    VC_TRY(launch_pdl(embed_kernel<T>, dim3(M), dim3(kRowThreads), 0, C.st, tok, (const int32_t *)nullptr, 0, 1,
+                      (const T *)C.d->embed, c.vocab, c.d_model, (T *)x, C.status(), C.at<uint32_t>(C.L.dws),
+                      (int)((kStatusBytes + a256((size_t)B * c.n_kv_heads * 4)) / 4), C.at<uint32_t>(C.L.rarr), B));
     // the q|k|v and LM-head products take x itself and normalise its rows in
     // their epilogue (no RMSNorm launches in a draft step) when the shape allows
     const bool rms_qkv = gemm_rms_ok(c.dt, M, nqkv, c.d_model, c.d_model, C.plan);
