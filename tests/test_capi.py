@@ -144,6 +144,30 @@ def test_greedy_head_and_rotation_validation_on_the_host(libvc):
     assert L.vc_quantize_kv(fake, fake, vc.VC_BF16, 1, 1, 32, 32, 128, ctypes.byref(q), None) == vc.VC_ERR_INVALID
 
 
+def test_normalised_row_gemm_validation_on_the_host(libvc):
+    """vc_gemm_rms (the draft steps' products of RMS-normalised rows) rejects
+    bad arguments and shapes outside its path before any CUDA call."""
+    from lossless_draft_verify_gb300 import vc
+    L = vc.load()
+    fake = 1 << 20                      # aligned, never dereferenced on these paths
+    ok_args = (fake, fake, fake, vc.VC_BF16, 8, 4096, 4096)
+    assert L.vc_gemm_rms(None, fake, fake, vc.VC_BF16, 8, 4096, 4096, 1e-5, 0, None, 0, None) == vc.VC_ERR_INVALID
+    assert L.vc_gemm_rms(*ok_args, -1.0, 0, None, 0, None) == vc.VC_ERR_INVALID          # eps < 0
+    assert L.vc_gemm_rms(*ok_args, float("nan"), 0, None, 0, None) == vc.VC_ERR_INVALID
+    assert L.vc_gemm_rms(fake + 2, fake, fake, vc.VC_BF16, 8, 4096, 4096, 1e-5, 0, None, 0,
+                         None) == vc.VC_ERR_INVALID                                    # x not 16-byte aligned
+    assert L.vc_gemm_rms(fake, fake, fake, vc.VC_BF16, 17, 4096, 4096, 1e-5, 0, None, 0,
+                         None) == vc.VC_ERR_UNSUPPORTED                                # more than 16 rows
+    assert L.vc_gemm_rms(fake, fake, fake, vc.VC_F32, 8, 4096, 4096, 1e-5, 0, None, 0,
+                         None) == vc.VC_ERR_UNSUPPORTED
+    assert L.vc_gemm_rms(fake, fake, fake, vc.VC_BF16, 8, 4000, 4096, 1e-5, 0, None, 0,
+                         None) == vc.VC_ERR_UNSUPPORTED                                # N not a multiple of 128
+    assert L.vc_gemm_rms(fake, fake, fake, vc.VC_BF16, 8, 2048, 1024, 1e-5, 1, None, 0,
+                         None) == vc.VC_ERR_UNSUPPORTED                                # SwiGLU of a split product
+    # a split product needs its workspace
+    assert L.vc_gemm_rms(*ok_args, 1e-5, 0, None, 0, None) == vc.VC_ERR_INVALID
+
+
 def test_kv_pack_validation_on_the_host(libvc):
     """Packing and unpacking reject bad arguments before any CUDA call; zero
     rows are a no-op."""
