@@ -126,6 +126,21 @@ def test_quantize_grid_aligned_group_is_exact():
     assert np.array_equal(codes, k)
 
 
+def test_quantize_exact_ties_round_to_even():
+    # grid z = 0, s = 1 (both ends present) and values exactly halfway between
+    # codes: the quotient is exact in fp32, and the rule rounds half to even
+    # (a rule that rounds halves up would give 1, 2, 3 here)
+    x = np.array([0.0, 3.0, 0.5, 1.5, 2.5] + [1.0] * 27, np.float32)
+    codes, s, z = _check_group(x, 2)
+    assert (s, z) == (1.0, 0.0)
+    assert codes[:5].tolist() == [0, 3, 0, 2, 2]
+    # 4-bit: grid 0..15 with s = 1; halves 6.5 and 7.5 go to 6 and 8
+    x = np.array([0.0, 15.0, 6.5, 7.5] + [3.0] * 28, np.float32)
+    codes, s, z = _check_group(x, 4)
+    assert (s, z) == (1.0, 0.0)
+    assert codes[:4].tolist() == [0, 15, 6, 8]
+
+
 def test_quantize_constant_groups():
     codes, s, z = _check_group(np.full(32, 0.75, np.float32), 2)   # fp16-exact
     assert s == 0.0 and z == 0.75 and not codes.any()
